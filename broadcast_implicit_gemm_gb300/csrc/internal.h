@@ -1,0 +1,117 @@
+// internal.h -- types shared by the library's translation units (host side).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/bigemm.h"
+
+namespace bigemm {
+
+inline size_t dtype_size(int dt) { return dt == BIGEMM_F32 ? 4 : 2; }
+
+inline int out_extent(int in, int k, int s, int p)
+{
+    const int span = in + 2 * p - k;
+    return span < 0 ? 0 : span / s + 1;
+}
+
+// Everything a conv kernel needs to know about the problem.
+struct ConvShape {
+    int N, CI, H, W, CO, KH, KW, stride, pad, groups;
+    int Ho, Wo;
+    int in_dt, out_dt, epi;
+};
+
+// -------------------------------------------------------------- UMMA kernel
+// Operand-A (pixel) modes of the implicit GEMM.
+enum AMode {
+    A_NHWC = 0,     // packed channels-last copy of data, K-major, 4-D box per tap
+    A_DIRECT = 1,   // 1x1 / stride 1 / pad 0: data read in place as [CI][H*W], MN-major
+};
+
+struct UmmaTiling {
+    int amode;        // AMode
+    int bn;           // output channels per tile (N of the MMA), multiple of 32
+    int stages;       // smem ring depth
+    int box_w, box_h; // output pixels per TMA box (A_NHWC); A_DIRECT: box_w = row pixels
+    int bpt;          // boxes per 128-pixel tile
+    int split;        // K slices
+};
+
+struct UmmaParams {
+    int N, CI, H, W, CO, KH, KW, stride, pad, Ho, Wo;
+    int box_w, box_h, bpt;          // pixel boxes
+    int boxes_x, boxes_y;           // boxes per image row / column (A_NHWC)
+    long long boxes_per_img;
+    long long total_boxes;
+    int pix_tiles, co_tiles;
+    int k_blocks, kb_per_split, split;
+    int ci_blocks, bk;              // channels per K block (128 bytes)
+    int cip;                        // packed weight channels per tap (A_NHWC)
+    long long units;
+    int epi;
+    float eps;
+    const float *bias;
+    void *out;
+    int out_dt;
+    float *ws;                      // split-K partial sums or null
+    long long out_elems;
+    int *err;
+    unsigned long long timeout_ns;
+};
+
+// Returns a CUDA error code of the launch.
+cudaError_t launch_umma_conv(const UmmaTiling &t, int in_dt, const UmmaParams &p,
+                             const CUtensorMap &map_a, const CUtensorMap &map_b, int grid,
+                             cudaStream_t stream);
+size_t umma_smem_bytes(const UmmaTiling &t);
+bool umma_tiling_compiled(const UmmaTiling &t, int in_dt);
+
+// -------------------------------------------------------------- other kernels
+cudaError_t launch_pack_nhwc(const void *x, void *xh, int N, int C, int HW, int Ch, int dt,
+                             cudaStream_t stream);
+cudaError_t launch_pack_weights(const void *w, void *wp, int CO, int CI, int KHKW, int cip,
+                                int dt, cudaStream_t stream);
+cudaError_t launch_splitk_reduce(const float *ws, int split, long long elems, int CO, int HoWo,
+                                 int epi, const float *bias, float eps, void *out, int out_dt,
+                                 cudaStream_t stream);
+cudaError_t launch_simt_conv(const ConvShape &s, const void *x, const void *w,
+                             const float *bias, float eps, void *out, int variant,
+                             cudaStream_t stream);
+cudaError_t launch_dw_conv(const ConvShape &s, const void *x, const void *w, const float *bias,
+                           float eps, void *out, int rows_per_block, cudaStream_t stream);
+cudaError_t launch_bcast(int N, int C, int HW, int op, const float *var, float eps, void *out,
+                         int out_dt, int flat, cudaStream_t stream);
+cudaError_t launch_wait_timeout_probe(int *err, unsigned long long timeout_ns,
+                                      cudaStream_t stream);
+
+// -------------------------------------------------------------- runtime state
+struct DeviceState {
+    int device = -1;
+    int sm_count = 0;
+    int max_smem_optin = 0;
+    int *err = nullptr;          // device word: sticky error flag
+};
+DeviceState *device_state();     // current device; nullptr on failure
+unsigned long long wait_timeout_ns();
+
+// Profiling hooks: record events around a launch when enabled.
+struct ProfScope {
+    ProfScope(const char *name, cudaStream_t s);
+    ~ProfScope();
+    const char *name_;
+    cudaStream_t s_;
+    int slot_ = -1;
+};
+
+// TMA descriptor encoding through the driver entry point.
+bool encode_tiled(CUtensorMap *map, CUtensorMapDataType dt, int rank, const void *base,
+                  const uint64_t *dims, const uint64_t *strides_bytes, const uint32_t *box,
+                  const uint32_t *estrides, CUtensorMapSwizzle swz);
+
+}  // namespace bigemm

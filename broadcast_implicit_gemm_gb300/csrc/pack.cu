@@ -1,0 +1,160 @@
+// pack.cu -- operand layouts for the implicit GEMM, and the split-K reduction.
+//
+//  pack_nhwc     data [N][C][H*W] -> [N][H*W][Ch] (channels innermost, zero
+//                padded to Ch), so that every (ry, rx) tap of a pixel box is one
+//                TMA box whose innermost coordinate is a channel offset (always
+//                16-byte aligned) and whose spatial coordinates may be negative
+//                (zero fill = the conv's inlined padding).
+//  pack_weights  kernel [CO][CI][KH*KW] -> [CO][KH*KW][cip]: the reduction
+//                order (ry, rx, ci) of the packed data, channels zero padded to
+//                whole 128-byte K blocks.
+//  splitk_reduce out = op(sum_s ws[s] + bias[f]) with the K slices added in
+//                index order (deterministic), then rounded to the output type.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "internal.h"
+
+namespace bigemm {
+
+namespace {
+
+template <typename T>
+__global__ void pack_nhwc_kernel(const T *__restrict__ x, T *__restrict__ xh, int C, int HW,
+                                 int Ch)
+{
+    __shared__ T tile[32][33];
+    const int n = blockIdx.z;
+    const int p0 = blockIdx.x * 32, c0 = blockIdx.y * 32;
+    const T *xs = x + (size_t)n * C * HW;
+    T *xd = xh + (size_t)n * HW * Ch;
+    for (int i = threadIdx.y; i < 32; i += 8) {
+        const int c = c0 + i, p = p0 + threadIdx.x;
+        T v;
+        if (c < C && p < HW)
+            v = xs[(size_t)c * HW + p];
+        else
+            v = T(0);
+        tile[i][threadIdx.x] = v;
+    }
+    __syncthreads();
+    for (int i = threadIdx.y; i < 32; i += 8) {
+        const int p = p0 + i, c = c0 + threadIdx.x;
+        if (p < HW && c < Ch) xd[(size_t)p * Ch + c] = tile[threadIdx.x][i];
+    }
+}
+
+template <typename T>
+__global__ void pack_weights_kernel(const T *__restrict__ w, T *__restrict__ wp, int CO, int CI,
+                                    int KHKW, int cip)
+{
+    const long long total = (long long)CO * KHKW * cip;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const int c = (int)(i % cip);
+        const long long r = i / cip;
+        const int t = (int)(r % KHKW);
+        const int f = (int)(r / KHKW);
+        wp[i] = c < CI ? w[((size_t)f * CI + c) * KHKW + t] : T(0);
+    }
+}
+
+__device__ __forceinline__ float epi_apply(int epi, float acc, float b, float eps)
+{
+    switch (epi) {
+    case BIGEMM_EPI_NONE: return acc;
+    case BIGEMM_EPI_BIAS: return acc + b;
+    case BIGEMM_EPI_BIAS_EXP: return expf(acc + b);
+    default: return rsqrtf(acc + b + eps);
+    }
+}
+
+template <typename TO>
+__device__ __forceinline__ TO to_out(float v);
+template <>
+__device__ __forceinline__ float to_out<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ __half to_out<__half>(float v) { return __float2half_rn(v); }
+template <>
+__device__ __forceinline__ __nv_bfloat16 to_out<__nv_bfloat16>(float v)
+{
+    return __float2bfloat16_rn(v);
+}
+
+template <typename TO>
+__global__ void splitk_reduce_kernel(const float *__restrict__ ws, int split, long long elems,
+                                     int CO, int HoWo, int epi, const float *__restrict__ bias,
+                                     float eps, TO *__restrict__ out)
+{
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < elems;
+         i += (long long)gridDim.x * blockDim.x) {
+        float s = ws[i];
+        for (int k = 1; k < split; ++k) s += ws[(long long)k * elems + i];
+        const int f = (int)((i / HoWo) % CO);
+        out[i] = to_out<TO>(epi_apply(epi, s, epi ? bias[f] : 0.f, eps));
+    }
+}
+
+int grid_for(long long work, int per_block)
+{
+    long long g = (work + per_block - 1) / per_block;
+    DeviceState *ds = device_state();
+    const long long cap = (long long)(ds ? ds->sm_count : 148) * 16;
+    if (g > cap) g = cap;
+    return (int)(g < 1 ? 1 : g);
+}
+
+}  // namespace
+
+cudaError_t launch_pack_nhwc(const void *x, void *xh, int N, int C, int HW, int Ch, int dt,
+                             cudaStream_t stream)
+{
+    ProfScope prof("pack_nhwc", stream);
+    dim3 grid((HW + 31) / 32, (Ch + 31) / 32, N), block(32, 8);
+    if (dtype_size(dt) == 4)
+        pack_nhwc_kernel<uint32_t><<<grid, block, 0, stream>>>(
+            static_cast<const uint32_t *>(x), static_cast<uint32_t *>(xh), C, HW, Ch);
+    else
+        pack_nhwc_kernel<uint16_t><<<grid, block, 0, stream>>>(
+            static_cast<const uint16_t *>(x), static_cast<uint16_t *>(xh), C, HW, Ch);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pack_weights(const void *w, void *wp, int CO, int CI, int KHKW, int cip,
+                                int dt, cudaStream_t stream)
+{
+    ProfScope prof("pack_weights", stream);
+    const long long total = (long long)CO * KHKW * cip;
+    const int grid = grid_for(total, 256);
+    if (dtype_size(dt) == 4)
+        pack_weights_kernel<uint32_t><<<grid, 256, 0, stream>>>(
+            static_cast<const uint32_t *>(w), static_cast<uint32_t *>(wp), CO, CI, KHKW, cip);
+    else
+        pack_weights_kernel<uint16_t><<<grid, 256, 0, stream>>>(
+            static_cast<const uint16_t *>(w), static_cast<uint16_t *>(wp), CO, CI, KHKW, cip);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_splitk_reduce(const float *ws, int split, long long elems, int CO, int HoWo,
+                                 int epi, const float *bias, float eps, void *out, int out_dt,
+                                 cudaStream_t stream)
+{
+    ProfScope prof("splitk_reduce", stream);
+    const int grid = grid_for(elems, 256);
+    switch (out_dt) {
+    case BIGEMM_F32:
+        splitk_reduce_kernel<float><<<grid, 256, 0, stream>>>(ws, split, elems, CO, HoWo, epi,
+                                                             bias, eps, static_cast<float *>(out));
+        break;
+    case BIGEMM_F16:
+        splitk_reduce_kernel<__half><<<grid, 256, 0, stream>>>(
+            ws, split, elems, CO, HoWo, epi, bias, eps, static_cast<__half *>(out));
+        break;
+    default:
+        splitk_reduce_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(
+            ws, split, elems, CO, HoWo, epi, bias, eps, static_cast<__nv_bfloat16 *>(out));
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace bigemm

@@ -1,0 +1,874 @@
+// plan.cu -- conv plans: validation, candidate kernels, timed search, cache,
+// and the conv entry points of the C ABI.
+//
+// The search follows the tuning flow of "Tuning High Performance Convolution
+// on NVIDIA GPUs" (TVM v0.5 autotvm tutorial), Step 2: a small space of
+// tilings (the analogue of its split knobs on f/y/x/rc and unroll options) is
+// enumerated; invalid points are rejected on the host before any launch
+// (its "invalid gpu kernel" records); each valid point is timed as three
+// repeats of back-to-back runs, each repeat lasting at least a minimum time
+// (its repeat / min_repeat_ms measure option); and the best record is kept per
+// workload, like its log of best configurations.
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <fstream>
+#include <map>
+#include <mutex>
+#include <sstream>
+#include <string>
+#include <vector>
+
+#include "internal.h"
+
+namespace bigemm {
+
+size_t dw_smem_bytes(const ConvShape &s, int rows);
+
+namespace {
+
+enum SimtVariant { SV_NAIVE = 0, SV_TILED = 1, SV_DW = 2 };
+
+struct Cand {
+    int kind = BIGEMM_KIND_SIMT;
+    int simt_variant = SV_NAIVE;
+    int dw_rows = 8;
+    UmmaTiling t{};
+};
+
+std::string cand_str(const Cand &c)
+{
+    char b[160];
+    if (c.kind == BIGEMM_KIND_UMMA)
+        snprintf(b, sizeof b, "umma:%s:bn%d:box%dx%dx%d:split%d",
+                 c.t.amode == A_DIRECT ? "direct" : "nhwc", c.t.bn, c.t.box_w, c.t.box_h, c.t.bpt,
+                 c.t.split);
+    else if (c.simt_variant == SV_DW)
+        snprintf(b, sizeof b, "simt:depthwise:rows%d", c.dw_rows);
+    else
+        snprintf(b, sizeof b, "simt:%s", c.simt_variant == SV_TILED ? "tiled" : "naive");
+    return b;
+}
+
+bool parse_cand(const std::string &s, Cand &c)
+{
+    int a, b, d, e, f, g;
+    char mode[16];
+    if (sscanf(s.c_str(), "umma:%15[a-z]:bn%d:box%dx%dx%d:split%d", mode, &a, &b, &d, &e, &f) == 6) {
+        c = Cand{};
+        c.kind = BIGEMM_KIND_UMMA;
+        c.t.amode = strcmp(mode, "direct") == 0 ? A_DIRECT : A_NHWC;
+        c.t.bn = a, c.t.box_w = b, c.t.box_h = d, c.t.bpt = e, c.t.split = f;
+        return true;
+    }
+    if (sscanf(s.c_str(), "simt:depthwise:rows%d", &g) == 1) {
+        c = Cand{};
+        c.simt_variant = SV_DW, c.dw_rows = g;
+        return true;
+    }
+    if (s == "simt:tiled") return c = Cand{}, c.simt_variant = SV_TILED, true;
+    if (s == "simt:naive") return c = Cand{}, c.simt_variant = SV_NAIVE, true;
+    return false;
+}
+
+CUtensorMapDataType tma_dt(int dt)
+{
+    return dt == BIGEMM_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+           : dt == BIGEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                               : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
+
+bool is_depthwise(const ConvShape &s) { return s.groups > 1 && s.groups == s.CI && s.CO == s.CI; }
+
+// Host-side validity of a UMMA tiling for a shape; reason on failure.
+bool umma_valid(const ConvShape &s, const UmmaTiling &t, int sm_count, std::string *why)
+{
+    auto bad = [&](const char *m) {
+        if (why) *why = m;
+        return false;
+    };
+    const size_t e = dtype_size(s.in_dt);
+    if (s.groups != 1) return bad("grouped conv");
+    if (t.bn != 64 && t.bn != 128 && t.bn != 256) return bad("tile_n not 64/128/256");
+    if (t.split < 1) return bad("split < 1");
+    if (t.bpt < 1) return bad("boxes per tile < 1");
+    if (t.amode == A_DIRECT) {
+        if (s.KH != 1 || s.KW != 1 || s.stride != 1 || s.pad != 0) return bad("direct mode needs 1x1/s1/p0");
+        if (((long long)s.H * s.W * e) % 16) return bad("H*W row not 16-byte multiple");
+        if ((s.CI * e) % 16) return bad("CI row not 16-byte multiple");
+        if (t.box_w != (int)(128 / e) || t.box_h != 1 || t.bpt * t.box_w != 128)
+            return bad("direct box must be one 128-byte row of pixels");
+    } else {
+        if (s.stride > 8) return bad("stride > 8");
+        if (t.box_w < 1 || t.box_h < 1) return bad("empty box");
+        if ((t.box_w * t.box_h) % 8) return bad("box pixels not a multiple of 8");
+        if (t.box_w * t.box_h * t.bpt > 128) return bad("boxes exceed 128 rows");
+        if (t.box_w * s.stride > 256 || t.box_h * s.stride > 256) return bad("box > 256");
+    }
+    if (umma_smem_bytes(t) == 0) return bad("no compiled kernel");
+    DeviceState *ds = device_state();
+    if (ds && (int)umma_smem_bytes(t) > ds->max_smem_optin) return bad("smem exceeds opt-in limit");
+    (void)sm_count;
+    return true;
+}
+
+struct Box {
+    int w, h, bpt;
+    double eff;
+};
+
+// Pixel boxes for the NHWC mode, best coverage first.
+std::vector<Box> box_options(const ConvShape &s)
+{
+    std::vector<Box> v;
+    for (int w = 1; w <= 128; w *= 2)
+        for (int h = 1; w * h <= 128; h *= 2) {
+            if ((w * h) % 8) continue;
+            const int bpt = 128 / (w * h);
+            if (w * s.stride > 256 || h * s.stride > 256) continue;
+            const double cover = (double)ceil_div(s.Ho, h) * h * ceil_div(s.Wo, w) * w;
+            const double eff = (double)s.Ho * s.Wo / cover;
+            v.push_back({w, h, bpt, eff});
+        }
+    // also boxes that match the image width exactly (w*h multiple of 8, < 128 rows)
+    for (int h = 1; h <= 128; ++h) {
+        const int w = s.Wo;
+        if (w > 128 || w * h > 128 || (w * h) % 8) continue;
+        if (w * s.stride > 256 || h * s.stride > 256) continue;
+        const int bpt = 128 / (w * h);
+        const double cover = (double)ceil_div(s.Ho, h) * h * w;
+        const double eff = (double)s.Ho * s.Wo / cover * (double)(bpt * w * h) / 128.0;
+        v.push_back({w, h, bpt, eff});
+    }
+    std::stable_sort(v.begin(), v.end(), [](const Box &a, const Box &b) {
+        if (std::fabs(a.eff - b.eff) > 1e-9) return a.eff > b.eff;
+        return a.bpt < b.bpt;
+    });
+    return v;
+}
+
+struct UmmaGeom {
+    UmmaParams p;
+    int grid;
+    int ch, cip;
+};
+
+UmmaGeom umma_geometry(const ConvShape &s, const UmmaTiling &t, int sm_count)
+{
+    UmmaGeom g{};
+    UmmaParams &p = g.p;
+    const int e = (int)dtype_size(s.in_dt);
+    p.N = s.N, p.CI = s.CI, p.H = s.H, p.W = s.W, p.CO = s.CO, p.KH = s.KH, p.KW = s.KW;
+    p.stride = s.stride, p.pad = s.pad, p.Ho = s.Ho, p.Wo = s.Wo;
+    p.bk = 128 / e;
+    p.ci_blocks = (int)ceil_div(s.CI, p.bk);
+    p.box_w = t.box_w, p.box_h = t.box_h, p.bpt = t.bpt;
+    if (t.amode == A_NHWC) {
+        p.boxes_x = (int)ceil_div(s.Wo, t.box_w);
+        p.boxes_y = (int)ceil_div(s.Ho, t.box_h);
+        p.boxes_per_img = (long long)p.boxes_x * p.boxes_y;
+        p.k_blocks = s.KH * s.KW * p.ci_blocks;
+        g.cip = p.ci_blocks * p.bk;
+        g.ch = (int)ceil_div(s.CI, 16 / e) * (16 / e);
+    } else {
+        p.boxes_x = 1, p.boxes_y = 1;
+        p.boxes_per_img = ceil_div((long long)s.H * s.W, t.box_w);
+        p.k_blocks = p.ci_blocks;
+        g.cip = s.CI;
+        g.ch = s.CI;
+    }
+    p.cip = g.cip;
+    p.total_boxes = (long long)s.N * p.boxes_per_img;
+    p.pix_tiles = (int)ceil_div(p.total_boxes, t.bpt);
+    p.co_tiles = (int)ceil_div(s.CO, t.bn);
+    p.kb_per_split = (int)ceil_div(p.k_blocks, t.split);
+    p.split = (int)ceil_div(p.k_blocks, p.kb_per_split);
+    p.units = (long long)p.pix_tiles * p.co_tiles * p.split;
+    p.epi = s.epi;
+    p.out_dt = s.out_dt;
+    p.out_elems = (long long)s.N * s.CO * s.Ho * s.Wo;
+    g.grid = (int)std::min<long long>(p.units, sm_count);
+    return g;
+}
+
+}  // namespace
+
+}  // namespace bigemm
+
+using namespace bigemm;
+
+struct bigemm_plan_s {
+    ConvShape s{};
+    int device = 0;
+    int sm_count = 0;
+    Cand c;
+    UmmaGeom g{};
+    void *xh = nullptr;
+    size_t xh_bytes = 0;
+    void *wp = nullptr;
+    size_t wp_bytes = 0;
+    float *ws = nullptr;
+    size_t ws_bytes = 0;
+    CUtensorMap map_a{}, map_b{};
+    const void *map_a_src = nullptr, *map_b_src = nullptr;   // DIRECT: pointers encoded
+    bool maps_ready = false;
+    std::string search_log;
+    std::string chosen_by = "heuristic";
+};
+
+namespace bigemm {
+namespace {
+
+bigemm_status validate(const ConvShape &s)
+{
+    if (s.N < 1 || s.H < 1 || s.W < 1 || s.CO < 1 || s.CI < 1 || s.KH < 1 || s.KW < 1)
+        return BIGEMM_ERR_INVALID_ARG;
+    if (s.stride < 1 || s.pad < 0 || s.groups < 1) return BIGEMM_ERR_INVALID_ARG;
+    if (s.CI % s.groups || s.CO % s.groups) return BIGEMM_ERR_INVALID_ARG;
+    if (s.in_dt < BIGEMM_F32 || s.in_dt > BIGEMM_BF16) return BIGEMM_ERR_INVALID_ARG;
+    if (s.out_dt < BIGEMM_F32 || s.out_dt > BIGEMM_BF16) return BIGEMM_ERR_INVALID_ARG;
+    if (s.epi < BIGEMM_EPI_NONE || s.epi > BIGEMM_EPI_BIAS_RSQRT) return BIGEMM_ERR_INVALID_ARG;
+    if (s.Ho < 1 || s.Wo < 1) return BIGEMM_ERR_INVALID_ARG;
+    if ((long long)s.H * s.W > (1ll << 30) || (long long)s.Ho * s.Wo > (1ll << 30))
+        return BIGEMM_ERR_UNSUPPORTED;
+    if (s.N > 65535 || s.CO > 65535) return BIGEMM_ERR_UNSUPPORTED;
+    return BIGEMM_OK;
+}
+
+bool simt_valid(const ConvShape &s, const Cand &c, std::string *why)
+{
+    if (c.simt_variant == SV_TILED && s.groups != 1) {
+        if (why) *why = "tiled SIMT needs groups = 1";
+        return false;
+    }
+    if (c.simt_variant == SV_DW) {
+        if (!is_depthwise(s)) return why && (*why = "not depthwise", true), false;
+        if (s.KH * s.KW > 49) return why && (*why = "depthwise kernel > 7x7", true), false;
+        DeviceState *ds = device_state();
+        const size_t smem = dw_smem_bytes(s, c.dw_rows);
+        if (c.dw_rows < 1 || (ds && smem > (size_t)ds->max_smem_optin))
+            return why && (*why = "depthwise band exceeds shared memory", true), false;
+    }
+    return true;
+}
+
+bool cand_valid(const ConvShape &s, const Cand &c, int sms, std::string *why)
+{
+    if (c.kind == BIGEMM_KIND_UMMA) return umma_valid(s, c.t, sms, why);
+    return simt_valid(s, c, why);
+}
+
+int heuristic_split(const ConvShape &s, UmmaTiling t, int sms)
+{
+    t.split = 1;
+    const UmmaGeom g = umma_geometry(s, t, sms);
+    const long long tiles = (long long)g.p.pix_tiles * g.p.co_tiles;
+    if (tiles * 2 >= sms || g.p.k_blocks < 4) return 1;
+    long long want = (sms + tiles - 1) / tiles;
+    want = std::min<long long>(want, g.p.k_blocks / 2);
+    return (int)std::max<long long>(1, want);
+}
+
+UmmaTiling default_tiling(const ConvShape &s, int amode, int bn, int sms)
+{
+    UmmaTiling t{};
+    t.amode = amode;
+    t.bn = bn;
+    t.stages = 0;
+    if (amode == A_DIRECT) {
+        t.box_w = (int)(128 / dtype_size(s.in_dt));
+        t.box_h = 1;
+        t.bpt = 128 / t.box_w;
+    } else {
+        const Box b = box_options(s).front();
+        t.box_w = b.w, t.box_h = b.h, t.bpt = b.bpt;
+    }
+    t.split = 1;
+    t.split = heuristic_split(s, t, sms);
+    return t;
+}
+
+int default_bn(const ConvShape &s)
+{
+    if (s.CO <= 64) return 64;
+    if (s.CO <= 128) return 128;
+    return (s.CO % 256 == 0) ? 256 : 128;
+}
+
+bool direct_ok(const ConvShape &s)
+{
+    UmmaTiling t{};
+    t.amode = A_DIRECT;
+    t.bn = 64;
+    t.box_w = (int)(128 / dtype_size(s.in_dt));
+    t.box_h = 1;
+    t.bpt = 128 / t.box_w;
+    t.split = 1;
+    return umma_valid(s, t, 1, nullptr);
+}
+
+Cand heuristic(const ConvShape &s, int sms)
+{
+    Cand c;
+    if (is_depthwise(s) && s.KH * s.KW <= 49) {
+        c.simt_variant = SV_DW;
+        c.dw_rows = std::max(1, std::min(s.Ho, 2048 / std::max(1, s.Wo)));
+        while (c.dw_rows > 1 && !simt_valid(s, c, nullptr)) c.dw_rows /= 2;
+        return c;
+    }
+    if (s.groups != 1) return c;   // naive
+    const long long kdim = (long long)s.CI * s.KH * s.KW;
+    if (kdim >= 32) {
+        Cand u;
+        u.kind = BIGEMM_KIND_UMMA;
+        u.t = default_tiling(s, direct_ok(s) ? A_DIRECT : A_NHWC, default_bn(s), sms);
+        if (umma_valid(s, u.t, sms, nullptr)) return u;
+    }
+    c.simt_variant = SV_TILED;
+    return c;
+}
+
+std::vector<Cand> candidates(const ConvShape &s, int sms)
+{
+    std::vector<Cand> v;
+    if (is_depthwise(s)) {
+        for (int rows : {1, 2, 4, 8, 16, 32}) {
+            Cand c;
+            c.simt_variant = SV_DW;
+            c.dw_rows = rows;
+            if (rows <= s.Ho && simt_valid(s, c, nullptr)) v.push_back(c);
+        }
+        if (v.empty()) v.push_back(Cand{});
+        return v;
+    }
+    if (s.groups != 1) {
+        v.push_back(Cand{});
+        return v;
+    }
+    std::vector<int> modes;
+    if (direct_ok(s)) modes.push_back(A_DIRECT);
+    modes.push_back(A_NHWC);
+    std::vector<Box> boxes = box_options(s);
+    for (int amode : modes) {
+        std::vector<std::pair<int, int>> bx;   // (w,h) with bpt
+        std::vector<int> bpts;
+        if (amode == A_DIRECT) {
+            const int w = (int)(128 / dtype_size(s.in_dt));
+            bx.push_back({w, 1});
+            bpts.push_back(128 / w);
+        } else {
+            for (size_t i = 0; i < boxes.size() && bx.size() < 2; ++i) {
+                if (i > 0 && boxes[i].eff < boxes[0].eff - 0.05) break;
+                bx.push_back({boxes[i].w, boxes[i].h});
+                bpts.push_back(boxes[i].bpt);
+            }
+        }
+        for (size_t bi = 0; bi < bx.size(); ++bi)
+            for (int bn : {64, 128, 256}) {
+                if (bn > 64 && bn / 2 >= s.CO) continue;   // a smaller tile covers CO
+                UmmaTiling t{};
+                t.amode = amode, t.bn = bn, t.box_w = bx[bi].first, t.box_h = bx[bi].second;
+                t.bpt = bpts[bi];
+                t.split = 1;
+                const UmmaGeom g = umma_geometry(s, t, sms);
+                const long long tiles = (long long)g.p.pix_tiles * g.p.co_tiles;
+                for (int split : {1, 2, 4, 8, 16, 32}) {
+                    if (split > 1 && (tiles * split > 4LL * sms || g.p.k_blocks / split < 2)) continue;
+                    t.split = split;
+                    Cand c;
+                    c.kind = BIGEMM_KIND_UMMA;
+                    c.t = t;
+                    if (umma_valid(s, t, sms, nullptr)) v.push_back(c);
+                }
+            }
+    }
+    Cand tiled;
+    tiled.simt_variant = SV_TILED;
+    v.push_back(tiled);
+    return v;
+}
+
+// ------------------------------------------------------------ scratch + run
+void free_scratch(bigemm_plan_s *p)
+{
+    if (p->xh) cudaFree(p->xh);
+    if (p->wp) cudaFree(p->wp);
+    if (p->ws) cudaFree(p->ws);
+    p->xh = p->wp = nullptr;
+    p->ws = nullptr;
+    p->xh_bytes = p->wp_bytes = p->ws_bytes = 0;
+    p->maps_ready = false;
+}
+
+bigemm_status setup_plan(bigemm_plan_s *p)
+{
+    const ConvShape &s = p->s;
+    if (p->c.kind != BIGEMM_KIND_UMMA) return BIGEMM_OK;
+    const UmmaTiling &t = p->c.t;
+    p->g = umma_geometry(s, t, p->sm_count);
+    const size_t e = dtype_size(s.in_dt);
+    if (t.amode == A_NHWC) {
+        p->xh_bytes = (size_t)s.N * s.H * s.W * p->g.ch * e;
+        p->wp_bytes = (size_t)s.CO * s.KH * s.KW * p->g.cip * e;
+        if (cudaMalloc(&p->xh, p->xh_bytes) != cudaSuccess) return BIGEMM_ERR_CUDA;
+        if (cudaMalloc(&p->wp, p->wp_bytes) != cudaSuccess) return BIGEMM_ERR_CUDA;
+        const uint64_t dims[4] = {(uint64_t)p->g.ch, (uint64_t)s.W, (uint64_t)s.H, (uint64_t)s.N};
+        const uint64_t str[3] = {p->g.ch * e, (uint64_t)s.W * p->g.ch * e,
+                                 (uint64_t)s.H * s.W * p->g.ch * e};
+        const uint32_t box[4] = {(uint32_t)p->g.p.bk, (uint32_t)(t.box_w * s.stride),
+                                 (uint32_t)(t.box_h * s.stride), 1u};
+        const uint32_t es[4] = {1u, (uint32_t)s.stride, (uint32_t)s.stride, 1u};
+        if (!encode_tiled(&p->map_a, tma_dt(s.in_dt), 4, p->xh, dims, str, box, es,
+                          CU_TENSOR_MAP_SWIZZLE_128B))
+            return BIGEMM_ERR_UNSUPPORTED;
+        const uint64_t kt = (uint64_t)s.KH * s.KW * p->g.cip;
+        const uint64_t bd[2] = {kt, (uint64_t)s.CO};
+        const uint64_t bs[1] = {kt * e};
+        const uint32_t bb[2] = {(uint32_t)p->g.p.bk, (uint32_t)t.bn};
+        const uint32_t bes[2] = {1u, 1u};
+        if (!encode_tiled(&p->map_b, tma_dt(s.in_dt), 2, p->wp, bd, bs, bb, bes,
+                          CU_TENSOR_MAP_SWIZZLE_128B))
+            return BIGEMM_ERR_UNSUPPORTED;
+        p->maps_ready = true;
+    }
+    if (p->g.p.split > 1) {
+        p->ws_bytes = (size_t)p->g.p.split * p->g.p.out_elems * sizeof(float);
+        if (cudaMalloc(&p->ws, p->ws_bytes) != cudaSuccess) return BIGEMM_ERR_CUDA;
+    }
+    return BIGEMM_OK;
+}
+
+bigemm_status encode_direct_maps(bigemm_plan_s *p, const void *data, const void *kernel)
+{
+    if (p->maps_ready && p->map_a_src == data && p->map_b_src == kernel) return BIGEMM_OK;
+    const ConvShape &s = p->s;
+    const UmmaTiling &t = p->c.t;
+    const size_t e = dtype_size(s.in_dt);
+    const uint64_t hw = (uint64_t)s.H * s.W;
+    const uint64_t dims[3] = {hw, (uint64_t)s.CI, (uint64_t)s.N};
+    const uint64_t str[2] = {hw * e, hw * s.CI * e};
+    const uint32_t box[3] = {(uint32_t)t.box_w, (uint32_t)p->g.p.bk, 1u};
+    const uint32_t es[3] = {1u, 1u, 1u};
+    if (!encode_tiled(&p->map_a, tma_dt(s.in_dt), 3, data, dims, str, box, es,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
+        return BIGEMM_ERR_INVALID_ARG;
+    const uint64_t bd[2] = {(uint64_t)s.CI, (uint64_t)s.CO};
+    const uint64_t bs[1] = {(uint64_t)s.CI * e};
+    const uint32_t bb[2] = {(uint32_t)p->g.p.bk, (uint32_t)t.bn};
+    const uint32_t bes[2] = {1u, 1u};
+    if (!encode_tiled(&p->map_b, tma_dt(s.in_dt), 2, kernel, bd, bs, bb, bes,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
+        return BIGEMM_ERR_INVALID_ARG;
+    p->map_a_src = data;
+    p->map_b_src = kernel;
+    p->maps_ready = true;
+    return BIGEMM_OK;
+}
+
+int launches_per_run(const bigemm_plan_s *p)
+{
+    if (p->c.kind != BIGEMM_KIND_UMMA) return 1;
+    int n = 1;
+    if (p->c.t.amode == A_NHWC) n += 2;
+    if (p->g.p.split > 1) n += 1;
+    return n;
+}
+
+bigemm_status run_plan(bigemm_plan_s *p, const void *data, const void *kernel, const float *bias,
+                       float eps, void *out, cudaStream_t st)
+{
+    const ConvShape &s = p->s;
+    if (!data || !kernel || !out) return BIGEMM_ERR_INVALID_ARG;
+    if (!aligned16(data) || !aligned16(kernel) || !aligned16(out)) return BIGEMM_ERR_INVALID_ARG;
+    if (s.epi != BIGEMM_EPI_NONE && !bias) return BIGEMM_ERR_INVALID_ARG;
+    DeviceState *ds = device_state();
+    if (!ds) return BIGEMM_ERR_CUDA;
+    cudaError_t e = cudaSuccess;
+    if (p->c.kind != BIGEMM_KIND_UMMA) {
+        if (p->c.simt_variant == SV_DW)
+            e = launch_dw_conv(s, data, kernel, bias, eps, out, p->c.dw_rows, st);
+        else
+            e = launch_simt_conv(s, data, kernel, bias, eps, out, p->c.simt_variant, st);
+        return e == cudaSuccess ? BIGEMM_OK : BIGEMM_ERR_CUDA;
+    }
+    UmmaParams up = p->g.p;
+    up.eps = eps;
+    up.bias = bias;
+    up.out = out;
+    up.ws = p->ws;
+    up.err = ds->err;
+    up.timeout_ns = wait_timeout_ns();
+    if (p->c.t.amode == A_NHWC) {
+        e = launch_pack_nhwc(data, p->xh, s.N, s.CI, s.H * s.W, p->g.ch, s.in_dt, st);
+        if (e != cudaSuccess) return BIGEMM_ERR_CUDA;
+        e = launch_pack_weights(kernel, p->wp, s.CO, s.CI, s.KH * s.KW, p->g.cip, s.in_dt, st);
+        if (e != cudaSuccess) return BIGEMM_ERR_CUDA;
+    } else {
+        bigemm_status r = encode_direct_maps(p, data, kernel);
+        if (r != BIGEMM_OK) return r;
+    }
+    e = launch_umma_conv(p->c.t, s.in_dt, up, p->map_a, p->map_b, p->g.grid, st);
+    if (e != cudaSuccess) return BIGEMM_ERR_CUDA;
+    if (up.split > 1) {
+        e = launch_splitk_reduce(p->ws, up.split, up.out_elems, s.CO, s.Ho * s.Wo, s.epi, bias, eps,
+                                 out, s.out_dt, st);
+        if (e != cudaSuccess) return BIGEMM_ERR_CUDA;
+    }
+    return BIGEMM_OK;
+}
+
+bigemm_status make_plan(const ConvShape &s, const Cand &c, int sms, bigemm_plan_s **out)
+{
+    bigemm_plan_s *p = new bigemm_plan_s;
+    p->s = s;
+    cudaGetDevice(&p->device);
+    p->sm_count = sms;
+    p->c = c;
+    bigemm_status r = setup_plan(p);
+    if (r != BIGEMM_OK) {
+        free_scratch(p);
+        delete p;
+        return r;
+    }
+    *out = p;
+    return BIGEMM_OK;
+}
+
+// ------------------------------------------------------------- plan cache
+std::mutex g_cache_mu;
+std::map<std::string, std::pair<std::string, double>> g_cache;   // key -> (cand, ms)
+bool g_cache_loaded = false;
+
+std::string cache_key(const ConvShape &s)
+{
+    char name[256] = "gpu";
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) == cudaSuccess) snprintf(name, sizeof name, "%s", prop.name);
+    char b[512];
+    snprintf(b, sizeof b, "%s|N%d|H%d|W%d|CO%d|CI%d|K%dx%d|s%d|p%d|g%d|in%d|out%d|epi%d", name, s.N,
+             s.H, s.W, s.CO, s.CI, s.KH, s.KW, s.stride, s.pad, s.groups, s.in_dt, s.out_dt, s.epi);
+    return b;
+}
+
+void load_cache_file()
+{
+    if (g_cache_loaded) return;
+    g_cache_loaded = true;
+    const char *path = getenv("BIGEMM_PLAN_CACHE");
+    if (!path || !*path) return;
+    std::ifstream f(path);
+    std::string line;
+    while (std::getline(f, line)) {
+        // {"key": "...", "cand": "...", "ms": x}
+        auto get = [&](const char *k) -> std::string {
+            std::string pat = std::string("\"") + k + "\": \"";
+            size_t a = line.find(pat);
+            if (a == std::string::npos) return "";
+            a += pat.size();
+            size_t b = line.find('"', a);
+            return b == std::string::npos ? "" : line.substr(a, b - a);
+        };
+        std::string key = get("key"), cand = get("cand");
+        double ms = 0;
+        size_t m = line.find("\"ms\": ");
+        if (m != std::string::npos) ms = atof(line.c_str() + m + 6);
+        Cand c;
+        if (!key.empty() && parse_cand(cand, c)) g_cache[key] = {cand, ms};
+    }
+}
+
+void append_cache_file(const std::string &key, const std::string &cand, double ms)
+{
+    const char *path = getenv("BIGEMM_PLAN_CACHE");
+    if (!path || !*path) return;
+    std::ofstream f(path, std::ios::app);
+    f << "{\"key\": \"" << key << "\", \"cand\": \"" << cand << "\", \"ms\": " << ms << "}\n";
+}
+
+// ------------------------------------------------------------ timed search
+struct SearchBuffers {
+    void *x = nullptr, *w = nullptr, *o = nullptr;
+    float *b = nullptr;
+    ~SearchBuffers()
+    {
+        if (x) cudaFree(x);
+        if (w) cudaFree(w);
+        if (o) cudaFree(o);
+        if (b) cudaFree(b);
+    }
+};
+
+double min_repeat_ms()
+{
+    const char *v = getenv("BIGEMM_MIN_REPEAT_MS");
+    double ms = v ? atof(v) : 2.0;
+    return ms > 0 ? ms : 2.0;
+}
+
+// Time one candidate: three repeats, each of `number` back-to-back runs lasting
+// at least min_repeat_ms; cost = median of the repeat means.  status as in the
+// tutorial's measure records: 0 ok, 1 invalid (host check), 4 run error,
+// 6 device wait timed out.
+int time_candidate(const ConvShape &s, const Cand &c, int sms, SearchBuffers &sb,
+                   cudaStream_t st, double *ms_out, std::string *why)
+{
+    if (!cand_valid(s, c, sms, why)) return 1;
+    bigemm_plan_s *p = nullptr;
+    if (make_plan(s, c, sms, &p) != BIGEMM_OK) {
+        if (why) *why = "scratch allocation or descriptor encoding failed";
+        return 4;
+    }
+    int status = 0;
+    cudaEvent_t a = nullptr, b = nullptr;
+    cudaEventCreate(&a);
+    cudaEventCreate(&b);
+    auto once = [&]() { return run_plan(p, sb.x, sb.w, sb.b, 1e-5f, sb.o, st); };
+    do {
+        if (once() != BIGEMM_OK || cudaStreamSynchronize(st) != cudaSuccess) {
+            status = 4;
+            break;
+        }
+        cudaEventRecord(a, st);
+        if (once() != BIGEMM_OK) { status = 4; break; }
+        cudaEventRecord(b, st);
+        if (cudaEventSynchronize(b) != cudaSuccess) { status = 4; break; }
+        float one = 0;
+        cudaEventElapsedTime(&one, a, b);
+        const double target = min_repeat_ms();
+        int number = (int)std::min(10000.0, std::max(1.0, std::ceil(target / std::max(one, 1e-4f))));
+        double rep[3];
+        for (int r = 0; r < 3 && status == 0; ++r) {
+            cudaEventRecord(a, st);
+            for (int i = 0; i < number; ++i)
+                if (once() != BIGEMM_OK) { status = 4; break; }
+            cudaEventRecord(b, st);
+            if (cudaEventSynchronize(b) != cudaSuccess) { status = 4; break; }
+            float tot = 0;
+            cudaEventElapsedTime(&tot, a, b);
+            rep[r] = tot / number;
+        }
+        if (status) break;
+        std::sort(rep, rep + 3);
+        *ms_out = rep[1];
+    } while (0);
+    cudaEventDestroy(a);
+    cudaEventDestroy(b);
+    if (status == 0 && bigemm_last_device_error() == BIGEMM_ERR_TIMEOUT) {
+        status = 6;
+        bigemm_clear_device_error();
+    }
+    if (status == 4 && why) *why = cudaGetErrorString(cudaGetLastError());
+    free_scratch(p);
+    delete p;
+    return status;
+}
+
+bigemm_status search(const ConvShape &s, int sms, cudaStream_t st, Cand *best, std::string *log,
+                     const std::vector<Cand> &cands)
+{
+    SearchBuffers sb;
+    const size_t e = dtype_size(s.in_dt);
+    const size_t xb = (size_t)s.N * s.CI * s.H * s.W * e;
+    const size_t wb = (size_t)s.CO * (s.CI / s.groups) * s.KH * s.KW * e;
+    const size_t ob = (size_t)s.N * s.CO * s.Ho * s.Wo * dtype_size(s.out_dt);
+    if (cudaMalloc(&sb.x, xb) != cudaSuccess || cudaMalloc(&sb.w, wb) != cudaSuccess ||
+        cudaMalloc(&sb.o, ob) != cudaSuccess || cudaMalloc(&sb.b, s.CO * sizeof(float)) != cudaSuccess)
+        return BIGEMM_ERR_CUDA;
+    cudaMemsetAsync(sb.x, 0, xb, st);
+    cudaMemsetAsync(sb.w, 0, wb, st);
+    cudaMemsetAsync(sb.b, 0, s.CO * sizeof(float), st);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return BIGEMM_ERR_CUDA;
+    double best_ms = 1e30;
+    int best_i = -1;
+    std::ostringstream os;
+    os << "[";
+    for (size_t i = 0; i < cands.size(); ++i) {
+        double ms = 0;
+        std::string why;
+        const int status = time_candidate(s, cands[i], sms, sb, st, &ms, &why);
+        if (getenv("BIGEMM_LOG"))
+            fprintf(stderr, "[bigemm] %-44s status=%d ms=%.5f %s\n", cand_str(cands[i]).c_str(),
+                    status, status ? 0.0 : ms, why.c_str());
+        os << (i ? ", " : "") << "{\"cand\": \"" << cand_str(cands[i]) << "\", \"status\": " << status;
+        if (status == 0) os << ", \"ms\": " << ms;
+        os << "}";
+        if (status == 0 && ms < best_ms) best_ms = ms, best_i = (int)i;   // ties: lowest index
+        if (status == 4 && cudaDeviceSynchronize() != cudaSuccess) break;  // context lost
+    }
+    os << "]";
+    *log = os.str();
+    if (best_i < 0) return BIGEMM_ERR_NO_CANDIDATE;
+    *best = cands[best_i];
+    return BIGEMM_OK;
+}
+
+bigemm_status plan_impl(int N, int H, int W, int CO, int CI, int KH, int KW, int stride,
+                        int padding, int groups, bigemm_dtype in_dt, bigemm_dtype out_dt,
+                        bigemm_epilogue epi, int do_search, const bigemm_plan_options *opts,
+                        void *stream, bigemm_plan *out_plan)
+{
+    if (!out_plan) return BIGEMM_ERR_INVALID_ARG;
+    *out_plan = nullptr;
+    ConvShape s{N, CI, H, W, CO, KH, KW, stride, padding, groups, 0, 0, (int)in_dt, (int)out_dt, (int)epi};
+    if (stride >= 1 && padding >= 0 && KH >= 1 && KW >= 1) {
+        s.Ho = out_extent(H, KH, stride, padding);
+        s.Wo = out_extent(W, KW, stride, padding);
+    }
+    bigemm_status r = validate(s);
+    if (r != BIGEMM_OK) return r;
+    DeviceState *ds = device_state();
+    if (!ds) return BIGEMM_ERR_CUDA;
+    const int sms = ds->sm_count;
+    cudaStream_t st = (cudaStream_t)stream;
+
+    const bool forced = opts && (opts->kind || opts->tile_n || opts->split_k || opts->box_w ||
+                                 opts->box_h || opts->stages);
+    Cand c;
+    std::string log, chosen = "heuristic";
+    if (forced) {
+        if (opts->kind == BIGEMM_KIND_SIMT || (opts->kind == 0 && !opts->tile_n && !opts->split_k &&
+                                               !opts->box_w && !opts->box_h && !opts->stages)) {
+            c = heuristic(s, sms);
+            if (c.kind == BIGEMM_KIND_UMMA) {
+                c = Cand{};
+                c.simt_variant = is_depthwise(s) ? SV_DW : (groups == 1 ? SV_TILED : SV_NAIVE);
+                if (c.simt_variant == SV_DW) {
+                    c.dw_rows = std::max(1, std::min(s.Ho, 2048 / std::max(1, s.Wo)));
+                    while (c.dw_rows > 1 && !simt_valid(s, c, nullptr)) c.dw_rows /= 2;
+                }
+            }
+        } else {
+            c.kind = BIGEMM_KIND_UMMA;
+            const int amode = (opts->box_w && opts->box_h) ? A_NHWC
+                              : direct_ok(s)                ? A_DIRECT
+                                                            : A_NHWC;
+            c.t = default_tiling(s, amode, opts->tile_n ? opts->tile_n : default_bn(s), sms);
+            if (opts->box_w && opts->box_h) {
+                c.t.box_w = opts->box_w, c.t.box_h = opts->box_h;
+                c.t.bpt = std::max(1, 128 / (opts->box_w * opts->box_h));
+                c.t.split = heuristic_split(s, c.t, sms);
+            }
+            if (opts->split_k) c.t.split = opts->split_k;
+            if (opts->stages) c.t.stages = opts->stages;
+        }
+        std::string why;
+        if (!cand_valid(s, c, sms, &why)) return BIGEMM_ERR_UNSUPPORTED;
+        chosen = "forced";
+    } else if (do_search) {
+        const std::string key = cache_key(s);
+        bool hit = false;
+        {
+            std::lock_guard<std::mutex> lk(g_cache_mu);
+            load_cache_file();
+            auto it = g_cache.find(key);
+            if (it != g_cache.end() && parse_cand(it->second.first, c) && cand_valid(s, c, sms, nullptr)) {
+                hit = true;
+                chosen = "cache";
+            }
+        }
+        if (!hit) {
+            r = search(s, sms, st, &c, &log, candidates(s, sms));
+            if (r != BIGEMM_OK) return r;
+            chosen = "search";
+            double ms = 0;
+            size_t at = log.find("\"cand\": \"" + cand_str(c) + "\"");
+            if (at != std::string::npos) {
+                size_t m = log.find("\"ms\": ", at);
+                if (m != std::string::npos) ms = atof(log.c_str() + m + 6);
+            }
+            std::lock_guard<std::mutex> lk(g_cache_mu);
+            g_cache[key] = {cand_str(c), ms};
+            append_cache_file(key, cand_str(c), ms);
+        }
+    } else {
+        c = heuristic(s, sms);
+    }
+    bigemm_plan_s *p = nullptr;
+    r = make_plan(s, c, sms, &p);
+    if (r != BIGEMM_OK) return r;
+    p->search_log = log;
+    p->chosen_by = chosen;
+    *out_plan = p;
+    return BIGEMM_OK;
+}
+
+}  // namespace
+}  // namespace bigemm
+
+extern "C" {
+
+bigemm_status conv2d_nchw_plan(int N, int H, int W, int CO, int CI, int KH, int KW, int stride,
+                               int padding, int groups, bigemm_dtype in_dtype,
+                               bigemm_dtype out_dtype, bigemm_epilogue epi, int search,
+                               void *stream, bigemm_plan *out_plan)
+{
+    return plan_impl(N, H, W, CO, CI, KH, KW, stride, padding, groups, in_dtype, out_dtype, epi,
+                     search, nullptr, stream, out_plan);
+}
+
+bigemm_status conv2d_nchw_plan_ex(int N, int H, int W, int CO, int CI, int KH, int KW,
+                                  int stride, int padding, int groups, bigemm_dtype in_dtype,
+                                  bigemm_dtype out_dtype, bigemm_epilogue epi, int search,
+                                  const bigemm_plan_options *opts, void *stream,
+                                  bigemm_plan *out_plan)
+{
+    return plan_impl(N, H, W, CO, CI, KH, KW, stride, padding, groups, in_dtype, out_dtype, epi,
+                     search, opts, stream, out_plan);
+}
+
+bigemm_status conv2d_nchw_run(bigemm_plan plan, const void *data, const void *kernel,
+                              const float *bias, float eps, void *out, void *stream)
+{
+    if (!plan) return BIGEMM_ERR_INVALID_ARG;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return BIGEMM_ERR_CUDA;
+    if (dev != plan->device) return BIGEMM_ERR_INVALID_ARG;
+    return run_plan(plan, data, kernel, bias, eps, out, (cudaStream_t)stream);
+}
+
+bigemm_status conv2d_nchw_plan_destroy(bigemm_plan plan)
+{
+    if (!plan) return BIGEMM_ERR_INVALID_ARG;
+    cudaDeviceSynchronize();
+    free_scratch(plan);
+    delete plan;
+    return BIGEMM_OK;
+}
+
+bigemm_status conv2d_nchw_plan_describe(bigemm_plan plan, char *buf, size_t len)
+{
+    if (!plan || !buf || len == 0) return BIGEMM_ERR_INVALID_ARG;
+    std::ostringstream os;
+    const Cand &c = plan->c;
+    os << "{\"cand\": \"" << cand_str(c) << "\", \"kind\": \""
+       << (c.kind == BIGEMM_KIND_UMMA ? "umma" : "simt") << "\"";
+    if (c.kind == BIGEMM_KIND_UMMA) {
+        const UmmaParams &p = plan->g.p;
+        os << ", \"amode\": \"" << (c.t.amode == A_DIRECT ? "direct" : "nhwc") << "\", \"bn\": " << c.t.bn
+           << ", \"box\": [" << c.t.box_w << ", " << c.t.box_h << ", " << c.t.bpt << "]"
+           << ", \"split\": " << p.split << ", \"k_blocks\": " << p.k_blocks
+           << ", \"pix_tiles\": " << p.pix_tiles << ", \"co_tiles\": " << p.co_tiles
+           << ", \"units\": " << p.units << ", \"grid\": " << plan->g.grid
+           << ", \"smem\": " << umma_smem_bytes(c.t);
+    }
+    os << ", \"launches\": " << launches_per_run(plan)
+       << ", \"scratch_bytes\": " << (plan->xh_bytes + plan->wp_bytes + plan->ws_bytes)
+       << ", \"chosen_by\": \"" << plan->chosen_by << "\"";
+    if (!plan->search_log.empty()) os << ", \"search\": " << plan->search_log;
+    os << "}";
+    const std::string s = os.str();
+    const size_t n = std::min(len - 1, s.size());
+    memcpy(buf, s.data(), n);
+    buf[n] = 0;
+    return BIGEMM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,265 @@
+// simt_conv.cu -- direct NCHW convolution on the FP32 pipes (no tensor cores).
+//
+// Three kernels, all computing the tutorial's conv2d_nchw definition with fp32
+// accumulation ("Tuning High Performance Convolution on NVIDIA GPUs", Step 1):
+//  * conv_tiled  (groups = 1): a 64-channel x 64-pixel output tile per block,
+//    256 threads with a 4x4 register block each; each K chunk of 16 reduction
+//    terms (ci, ry, rx) stages the kernel slice and the gathered, zero-padded
+//    input window in shared memory -- the tutorial's shared-memory cache stages
+//    and register accumulator, with padding folded into the gather.
+//  * conv_depthwise (groups = C = CO): one block per (image, channel, band of
+//    output rows); the band's input rows are staged once in shared memory with
+//    explicit zero borders, the channel's KHxKW taps sit in registers, and each
+//    thread slides along x producing neighbouring outputs.
+//  * conv_naive (any groups): one thread per output; the fallback for grouped
+//    shapes neither kernel above covers.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "internal.h"
+
+namespace bigemm {
+
+namespace {
+
+__device__ __forceinline__ float ld_in(const void *p, size_t i, int dt)
+{
+    if (dt == BIGEMM_F32) return __ldg(static_cast<const float *>(p) + i);
+    if (dt == BIGEMM_F16) return __half2float(__ldg(static_cast<const __half *>(p) + i));
+    return __bfloat162float(__ldg(static_cast<const __nv_bfloat16 *>(p) + i));
+}
+
+__device__ __forceinline__ void st_out(void *p, size_t i, float v, int dt)
+{
+    if (dt == BIGEMM_F32)
+        static_cast<float *>(p)[i] = v;
+    else if (dt == BIGEMM_F16)
+        static_cast<__half *>(p)[i] = __float2half_rn(v);
+    else
+        static_cast<__nv_bfloat16 *>(p)[i] = __float2bfloat16_rn(v);
+}
+
+__device__ __forceinline__ float epi_apply(int epi, float acc, const float *bias, int f, float eps)
+{
+    switch (epi) {
+    case BIGEMM_EPI_NONE: return acc;
+    case BIGEMM_EPI_BIAS: return acc + bias[f];
+    case BIGEMM_EPI_BIAS_EXP: return expf(acc + bias[f]);
+    default: return rsqrtf(acc + bias[f] + eps);
+    }
+}
+
+struct SimtArgs {
+    int N, CI, H, W, CO, KH, KW, stride, pad, groups, Ho, Wo;
+    int in_dt, out_dt, epi;
+    float eps;
+};
+
+constexpr int TM = 64, TN = 64, TK = 16;
+
+// grid: (pixel tiles of one image, co tiles, N)
+__global__ void __launch_bounds__(256) conv_tiled_kernel(SimtArgs a, const void *__restrict__ x,
+                                                         const void *__restrict__ w,
+                                                         const float *__restrict__ bias,
+                                                         void *__restrict__ out)
+{
+    __shared__ __align__(16) float ws[TK][TM];
+    __shared__ __align__(16) float xs[TK][TN];
+    const int n = blockIdx.z;
+    const int co0 = blockIdx.y * TM;
+    const int p0 = blockIdx.x * TN;
+    const int HoWo = a.Ho * a.Wo;
+    const int KK = a.KH * a.KW;
+    const int K = a.CI * KK;
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    const size_t xoff = (size_t)n * a.CI * a.H * a.W;
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+
+    for (int k0 = 0; k0 < K; k0 += TK) {
+        // kernel slice: ws[kk][m] = w[co0+m][k0+kk]
+        for (int e = threadIdx.x; e < TK * TM; e += 256) {
+            const int m = e / TK, kk = e - m * TK;
+            const int co = co0 + m, k = k0 + kk;
+            ws[kk][m] = (co < a.CO && k < K) ? ld_in(w, (size_t)co * K + k, a.in_dt) : 0.f;
+        }
+        // gathered input: xs[kk][j] = pad(data)[n, ci, y*s+ry-p, x*s+rx-p]
+        for (int e = threadIdx.x; e < TK * TN; e += 256) {
+            const int kk = e / TN, j = e - kk * TN;
+            const int k = k0 + kk, pix = p0 + j;
+            float v = 0.f;
+            if (k < K && pix < HoWo) {
+                const int ci = k / KK, t = k - ci * KK;
+                const int ry = t / a.KW, rx = t - ry * a.KW;
+                const int y = pix / a.Wo, xo = pix - y * a.Wo;
+                const int iy = y * a.stride + ry - a.pad, ix = xo * a.stride + rx - a.pad;
+                if (iy >= 0 && iy < a.H && ix >= 0 && ix < a.W)
+                    v = ld_in(x, xoff + ((size_t)ci * a.H + iy) * a.W + ix, a.in_dt);
+            }
+            xs[kk][j] = v;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int kk = 0; kk < TK; ++kk) {
+            const float4 wv = *reinterpret_cast<const float4 *>(&ws[kk][ty * 4]);
+            const float4 xv = *reinterpret_cast<const float4 *>(&xs[kk][tx * 4]);
+            const float wr[4] = {wv.x, wv.y, wv.z, wv.w};
+            const float xr[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(wr[i], xr[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int co = co0 + ty * 4 + i;
+        if (co >= a.CO) continue;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int pix = p0 + tx * 4 + j;
+            if (pix < HoWo)
+                st_out(out, ((size_t)n * a.CO + co) * HoWo + pix,
+                       epi_apply(a.epi, acc[i][j], bias, co, a.eps), a.out_dt);
+        }
+    }
+}
+
+__global__ void conv_naive_kernel(SimtArgs a, const void *__restrict__ x,
+                                  const void *__restrict__ w, const float *__restrict__ bias,
+                                  void *__restrict__ out)
+{
+    const long long total = (long long)a.N * a.CO * a.Ho * a.Wo;
+    const int cig = a.CI / a.groups, cog = a.CO / a.groups;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        long long t = i;
+        const int xo = (int)(t % a.Wo); t /= a.Wo;
+        const int y = (int)(t % a.Ho); t /= a.Ho;
+        const int f = (int)(t % a.CO);
+        const int n = (int)(t / a.CO);
+        const int g = f / cog;
+        float acc = 0.f;
+        for (int rc = 0; rc < cig; ++rc) {
+            const int ci = g * cig + rc;
+            for (int ry = 0; ry < a.KH; ++ry) {
+                const int iy = y * a.stride + ry - a.pad;
+                if (iy < 0 || iy >= a.H) continue;
+                for (int rx = 0; rx < a.KW; ++rx) {
+                    const int ix = xo * a.stride + rx - a.pad;
+                    if (ix < 0 || ix >= a.W) continue;
+                    acc = fmaf(ld_in(x, (((size_t)n * a.CI + ci) * a.H + iy) * a.W + ix, a.in_dt),
+                               ld_in(w, (((size_t)f * cig + rc) * a.KH + ry) * a.KW + rx, a.in_dt),
+                               acc);
+                }
+            }
+        }
+        st_out(out, (size_t)i, epi_apply(a.epi, acc, bias, f, a.eps), a.out_dt);
+    }
+}
+
+constexpr int kDwMaxTaps = 49;   // up to 7x7 kernels keep their taps in registers
+
+// grid: (row bands, C, N); dynamic smem: (rows_in) x (W + 2*pad) floats.
+__global__ void __launch_bounds__(256) conv_depthwise_kernel(SimtArgs a, int rows_per_block,
+                                                             const void *__restrict__ x,
+                                                             const void *__restrict__ w,
+                                                             const float *__restrict__ bias,
+                                                             void *__restrict__ out)
+{
+    extern __shared__ float srow[];
+    const int c = blockIdx.y, n = blockIdx.z;
+    const int y0 = blockIdx.x * rows_per_block;
+    const int y1 = min(a.Ho, y0 + rows_per_block);
+    const int iy0 = y0 * a.stride - a.pad;
+    const int rows_in = (y1 - 1 - y0) * a.stride + a.KH;
+    const int wp = a.W + 2 * a.pad;
+    const size_t plane = ((size_t)n * a.CI + c) * a.H * a.W;
+    // stage rows [iy0, iy0 + rows_in) with zero borders
+    for (int e = threadIdx.x; e < rows_in * wp; e += blockDim.x) {
+        const int r = e / wp, cc = e - r * wp;
+        const int iy = iy0 + r, ix = cc - a.pad;
+        float v = 0.f;
+        if (iy >= 0 && iy < a.H && ix >= 0 && ix < a.W) v = ld_in(x, plane + (size_t)iy * a.W + ix, a.in_dt);
+        srow[e] = v;
+    }
+    float tap[kDwMaxTaps];
+    const int KK = a.KH * a.KW;
+#pragma unroll
+    for (int t = 0; t < kDwMaxTaps; ++t) tap[t] = t < KK ? ld_in(w, (size_t)c * KK + t, a.in_dt) : 0.f;
+    __syncthreads();
+    const int HoWo = a.Ho * a.Wo;
+    const size_t obase = ((size_t)n * a.CO + c) * HoWo;
+    const int cnt = (y1 - y0) * a.Wo;
+    for (int e = threadIdx.x; e < cnt; e += blockDim.x) {
+        const int yy = e / a.Wo, xo = e - yy * a.Wo;
+        const float *base = srow + (yy * a.stride) * wp + xo * a.stride;
+        float acc = 0.f;
+        int t = 0;
+        for (int ry = 0; ry < a.KH; ++ry)
+            for (int rx = 0; rx < a.KW; ++rx, ++t) acc = fmaf(base[ry * wp + rx], tap[t], acc);
+        st_out(out, obase + (size_t)(y0 + yy) * a.Wo + xo, epi_apply(a.epi, acc, bias, c, a.eps),
+               a.out_dt);
+    }
+}
+
+SimtArgs make_args(const ConvShape &s, float eps)
+{
+    SimtArgs a;
+    a.N = s.N; a.CI = s.CI; a.H = s.H; a.W = s.W; a.CO = s.CO; a.KH = s.KH; a.KW = s.KW;
+    a.stride = s.stride; a.pad = s.pad; a.groups = s.groups; a.Ho = s.Ho; a.Wo = s.Wo;
+    a.in_dt = s.in_dt; a.out_dt = s.out_dt; a.epi = s.epi; a.eps = eps;
+    return a;
+}
+
+}  // namespace
+
+// variant 0: naive (any groups); variant 1: tiled (groups = 1)
+cudaError_t launch_simt_conv(const ConvShape &s, const void *x, const void *w,
+                             const float *bias, float eps, void *out, int variant,
+                             cudaStream_t stream)
+{
+    const SimtArgs a = make_args(s, eps);
+    if (variant == 1 && s.groups == 1) {
+        ProfScope prof("simt_conv_tiled", stream);
+        dim3 grid((s.Ho * s.Wo + TN - 1) / TN, (s.CO + TM - 1) / TM, s.N);
+        conv_tiled_kernel<<<grid, 256, 0, stream>>>(a, x, w, bias, out);
+        return cudaGetLastError();
+    }
+    ProfScope prof("simt_conv_naive", stream);
+    const long long total = (long long)s.N * s.CO * s.Ho * s.Wo;
+    long long g = (total + 255) / 256;
+    DeviceState *ds = device_state();
+    const long long cap = (long long)(ds ? ds->sm_count : 148) * 32;
+    if (g > cap) g = cap;
+    conv_naive_kernel<<<(int)g, 256, 0, stream>>>(a, x, w, bias, out);
+    return cudaGetLastError();
+}
+
+size_t dw_smem_bytes(const ConvShape &s, int rows)
+{
+    return (size_t)((rows - 1) * s.stride + s.KH) * (s.W + 2 * s.pad) * sizeof(float);
+}
+
+cudaError_t launch_dw_conv(const ConvShape &s, const void *x, const void *w, const float *bias,
+                           float eps, void *out, int rows_per_block, cudaStream_t stream)
+{
+    ProfScope prof("simt_conv_depthwise", stream);
+    if (s.KH * s.KW > kDwMaxTaps) return cudaErrorInvalidValue;
+    const SimtArgs a = make_args(s, eps);
+    const size_t smem = dw_smem_bytes(s, rows_per_block);
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(conv_depthwise_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    dim3 grid((s.Ho + rows_per_block - 1) / rows_per_block, s.CO, s.N);
+    conv_depthwise_kernel<<<grid, 256, smem, stream>>>(a, rows_per_block, x, w, bias, out);
+    return cudaGetLastError();
+}
+
+}  // namespace bigemm

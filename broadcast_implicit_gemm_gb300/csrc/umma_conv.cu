@@ -1,0 +1,401 @@
+// umma_conv.cu -- implicit-GEMM NCHW convolution on the sm_103a tensor cores.
+//
+// The convolution of "Tuning High Performance Convolution on NVIDIA GPUs"
+// (TVM v0.5 autotvm tutorial, Step 1: conv2d_nchw with inlined padding) is
+// computed as one GEMM per launch:
+//     D[pixel, f] = sum_k A[pixel, k] * B[f, k]
+// with pixel = (n, y, x) on the MMA's M axis (128 TMEM lanes), the output
+// channel f on its N axis (tile of BN), and k = (ry, rx, ci) on the reduction
+// axis.  The padded tensor is never built: TMA reads each tap's box at the
+// shifted (possibly negative) coordinates and fills out-of-range elements
+// with zeros, which is the tutorial's inlined padding done by the copy engine.
+//
+// Structure (one persistent CTA per SM, 6 warps):
+//   warp 0    TMA producer: for each K block loads the A box(es) and the B tile
+//             into a STAGES-deep shared-memory ring (mbarrier full/empty).
+//   warp 1    allocates TMEM, and one lane issues tcgen05.mma (4 per K block,
+//             128-byte swizzled operands) into one of two TMEM accumulators.
+//   warps 2-5 epilogue: tcgen05.ld the accumulator (lane = pixel), apply the
+//             fused per-channel epilogue op(acc + bias[f]) and store NCHW; for
+//             a fixed channel the 32 lanes of a warp write 32 neighbouring
+//             pixels, so stores coalesce without a shared-memory transpose.
+// The two accumulators let the epilogue of one tile overlap the MMAs of the
+// next.  Split-K writes fp32 partial sums to a workspace instead; a separate
+// kernel adds them in a fixed order and applies the epilogue.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace bigemm {
+
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kTileM = 128;
+constexpr int kRowBytes = 128;                  // one K block: a 128-byte swizzle row
+constexpr int kABytes = kTileM * kRowBytes;     // 16 KB of A per stage
+
+template <int BN>
+struct Cfg {
+    static constexpr int stages = BN <= 64 ? 8 : (BN <= 128 ? 6 : 4);
+    static constexpr int b_bytes = BN * kRowBytes;
+    static constexpr int ring = stages * (kABytes + b_bytes);
+    static constexpr int bars = (2 * stages + 5) * 8;
+    static constexpr int smem = ring + bars + 16 + 1024;   // + alignment slack
+    static constexpr uint32_t tmem_cols = (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
+                                         : (2 * BN <= 256) ? 256 : 512;
+};
+
+__device__ __forceinline__ float epi_apply(int epi, float acc, float b, float eps)
+{
+    switch (epi) {
+    case BIGEMM_EPI_NONE: return acc;
+    case BIGEMM_EPI_BIAS: return acc + b;
+    case BIGEMM_EPI_BIAS_EXP: return expf(acc + b);
+    default: return rsqrtf(acc + b + eps);
+    }
+}
+
+__device__ __forceinline__ void store_out(void *out, long long i, float v, int dt)
+{
+    if (dt == BIGEMM_F32)
+        static_cast<float *>(out)[i] = v;
+    else if (dt == BIGEMM_F16)
+        static_cast<__half *>(out)[i] = __float2half_rn(v);
+    else
+        static_cast<__nv_bfloat16 *>(out)[i] = __float2bfloat16_rn(v);
+}
+
+struct Unit {
+    int ct, pt, sp, kb0, kb1;
+};
+
+__device__ __forceinline__ Unit decode(const UmmaParams &p, long long u)
+{
+    Unit w;
+    w.ct = (int)(u % p.co_tiles);
+    const long long r = u / p.co_tiles;
+    w.pt = (int)(r % p.pix_tiles);
+    w.sp = (int)(r / p.pix_tiles);
+    w.kb0 = w.sp * p.kb_per_split;
+    w.kb1 = min(p.k_blocks, w.kb0 + p.kb_per_split);
+    return w;
+}
+
+template <int BN, int AMODE, int FMT>
+__global__ void __launch_bounds__(kThreads, 1)
+    umma_conv_kernel(const __grid_constant__ CUtensorMap map_a,
+                     const __grid_constant__ CUtensorMap map_b, const UmmaParams p)
+{
+    using C = Cfg<BN>;
+    constexpr int S = C::stages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint8_t *sa = smem;
+    uint8_t *sb = smem + S * kABytes;
+    uint64_t *full = reinterpret_cast<uint64_t *>(sb + S * C::b_bytes);
+    uint64_t *empty = full + S;
+    uint64_t *tfull = empty + S;
+    uint64_t *tempty = tfull + 2;
+    uint64_t *drain = tempty + 2;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int box_px = p.box_w * p.box_h;           // rows of A filled by one box
+    const uint32_t box_bytes = (uint32_t)box_px * kRowBytes;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&tfull[i], 1);
+            mbar_init(&tempty[i], 4);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&map_a);
+        tma_prefetch_desc(&map_b);
+    }
+    if (warp == 1) {
+        __syncwarp();
+        tmem_alloc(tmem_holder, C::tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t last_parity[S];
+            bool issued[S];
+            for (int i = 0; i < S; ++i) issued[i] = false, last_parity[i] = 0;
+            bool ok = true;
+            for (long long u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+                const Unit w = decode(p, u);
+                const long long box0 = (long long)w.pt * p.bpt;
+                const int nbox = (int)min((long long)p.bpt, p.total_boxes - box0);
+                const uint32_t tx = (uint32_t)nbox * box_bytes + (uint32_t)C::b_bytes;
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[stage], tx);
+                    issued[stage] = true;
+                    last_parity[stage] = phase;
+                    uint8_t *a_dst = sa + stage * kABytes;
+                    uint8_t *b_dst = sb + stage * C::b_bytes;
+                    if (AMODE == A_NHWC) {
+                        const int tap = kb / p.ci_blocks, cb = kb - tap * p.ci_blocks;
+                        const int ry = tap / p.KW, rx = tap - ry * p.KW;
+                        for (int i = 0; i < nbox; ++i) {
+                            const long long b = box0 + i;
+                            const int n = (int)(b / p.boxes_per_img);
+                            const int rem = (int)(b - (long long)n * p.boxes_per_img);
+                            const int byi = rem / p.boxes_x, bxi = rem - byi * p.boxes_x;
+                            const int x = bxi * p.box_w * p.stride - p.pad + rx;
+                            const int y = byi * p.box_h * p.stride - p.pad + ry;
+                            tma_load_4d(a_dst + i * box_bytes, &map_a, &full[stage], cb * p.bk,
+                                        x, y, n);
+                        }
+                        tma_load_2d(b_dst, &map_b, &full[stage], tap * p.cip + cb * p.bk,
+                                    w.ct * BN);
+                    } else {
+                        for (int i = 0; i < nbox; ++i) {
+                            const long long b = box0 + i;
+                            const int n = (int)(b / p.boxes_per_img);
+                            const int p0 = (int)(b - (long long)n * p.boxes_per_img) * p.box_w;
+                            tma_load_3d(a_dst + i * box_bytes, &map_a, &full[stage], p0,
+                                        kb * p.bk, n);
+                        }
+                        tma_load_2d(b_dst, &map_b, &full[stage], kb * p.bk, w.ct * BN);
+                    }
+                    if (++stage == S) stage = 0, phase ^= 1u;
+                }
+            }
+            if (!ok) {
+                // Let every copy already issued land before the block exits.
+                int local_abort = 0;
+                for (int i = 0; i < S; ++i)
+                    if (issued[i])
+                        mbar_wait(&full[i], last_parity[i], p.timeout_ns, &local_abort, p.err);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc =
+                make_idesc(FMT == 2 ? 2u : (uint32_t)FMT, AMODE == A_DIRECT ? 1u : 0u, 0u,
+                           kTileM, BN);
+            // Byte step of the A start address per MMA (K = 32 bytes of each row):
+            // K-major rows advance inside the swizzle row; MN-major advances by
+            // whole 8-row groups (16 rows for 16-bit types, 8 rows for tf32).
+            constexpr uint32_t a_kstep = AMODE == A_NHWC ? 32u : (FMT == 2 ? 1024u : 2048u);
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true, any = false;
+            for (long long u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+                const Unit w = decode(p, u);
+                if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, p.timeout_ns, abort_flag, p.err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                    if (!mbar_wait(&full[stage], phase, p.timeout_ns, abort_flag, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(sa + stage * kABytes);
+                    const uint32_t b_addr = smem_u32(sb + stage * C::b_bytes);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint64_t ad =
+                            AMODE == A_NHWC
+                                ? smem_desc(a_addr + k * a_kstep, 16u, 1024u, 2u)
+                                : smem_desc(a_addr + k * a_kstep, box_bytes, 1024u, 2u);
+                        const uint64_t bd = smem_desc(b_addr + k * 32u, 16u, 1024u, 2u);
+                        const uint32_t accum = (kb > w.kb0 || k > 0) ? 1u : 0u;
+                        if (FMT == 2)
+                            umma_tf32(d_tmem, ad, bd, idesc, accum);
+                        else
+                            umma_f16(d_tmem, ad, bd, idesc, accum);
+                    }
+                    any = true;
+                    umma_commit(&empty[stage]);
+                    if (++stage == S) stage = 0, phase ^= 1u;
+                }
+                if (!ok) break;
+                umma_commit(&tfull[acc]);
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+            if (!ok && any) {
+                // Wait for every MMA issued so far before TMEM is released.
+                int local_abort = 0;
+                umma_commit(drain);
+                mbar_wait(drain, 0, p.timeout_ns, &local_abort, p.err);
+            }
+        }
+    } else {
+        // --------------------------------------------------------- epilogue
+        const int q = warp & 3;                     // TMEM lane quadrant of this warp
+        const int row = q * 32 + lane;              // tile row = pixel
+        const int bi = row / box_px, bj = row - bi * box_px;
+        const long long howo = (long long)p.Ho * p.Wo;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (long long u = blockIdx.x; u < p.units; u += gridDim.x) {
+            const Unit w = decode(p, u);
+            if (!mbar_wait(&tfull[acc], acc_phase, p.timeout_ns, abort_flag, p.err)) break;
+            tc_fence_after();
+            const long long b = (long long)w.pt * p.bpt + bi;
+            bool valid = bi < p.bpt && b < p.total_boxes;
+            long long base = 0;
+            if (valid) {
+                const int n = (int)(b / p.boxes_per_img);
+                const long long rem = b - (long long)n * p.boxes_per_img;
+                long long pix;
+                if (AMODE == A_NHWC) {
+                    const int byi = (int)(rem / p.boxes_x), bxi = (int)(rem - (long long)byi * p.boxes_x);
+                    const int y = byi * p.box_h + bj / p.box_w;
+                    const int x = bxi * p.box_w + bj % p.box_w;
+                    valid = y < p.Ho && x < p.Wo;
+                    pix = (long long)y * p.Wo + x;
+                } else {
+                    pix = rem * p.box_w + bj;
+                    valid = pix < howo;
+                }
+                base = (long long)n * p.CO * howo + pix;
+            }
+            const int co0 = w.ct * BN;
+            float *ws = p.ws ? p.ws + (long long)w.sp * p.out_elems : nullptr;
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + c0),
+                                   r);
+                tmem_wait_ld();
+                if (valid) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int co = co0 + c0 + j;
+                        if (co < p.CO) {
+                            const long long o = base + (long long)co * howo;
+                            const float v = __uint_as_float(r[j]);
+                            if (ws)
+                                ws[o] = v;
+                            else
+                                store_out(p.out, o,
+                                          epi_apply(p.epi, v, p.epi ? __ldg(p.bias + co) : 0.f,
+                                                    p.eps),
+                                          p.out_dt);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[acc]);
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        tmem_dealloc(tmem_base, C::tmem_cols);
+    }
+}
+
+template <int BN, int AMODE, int FMT>
+cudaError_t launch_one(const UmmaParams &p, const CUtensorMap &ma, const CUtensorMap &mb,
+                       int grid, cudaStream_t stream)
+{
+    auto kern = umma_conv_kernel<BN, AMODE, FMT>;
+    static unsigned long long attr_set = 0;   // bit per device: smem opt-in done
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 64 || !(attr_set >> dev & 1ull)) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             Cfg<BN>::smem);
+        if (e != cudaSuccess) return e;
+        if (dev < 64) attr_set |= 1ull << dev;
+    }
+    kern<<<grid, kThreads, Cfg<BN>::smem, stream>>>(ma, mb, p);
+    return cudaGetLastError();
+}
+
+template <int AMODE, int FMT>
+cudaError_t dispatch_bn(int bn, const UmmaParams &p, const CUtensorMap &ma,
+                        const CUtensorMap &mb, int grid, cudaStream_t s)
+{
+    switch (bn) {
+    case 64: return launch_one<64, AMODE, FMT>(p, ma, mb, grid, s);
+    case 128: return launch_one<128, AMODE, FMT>(p, ma, mb, grid, s);
+    case 256: return launch_one<256, AMODE, FMT>(p, ma, mb, grid, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+template <int AMODE>
+cudaError_t dispatch_fmt(int fmt, int bn, const UmmaParams &p, const CUtensorMap &ma,
+                         const CUtensorMap &mb, int grid, cudaStream_t s)
+{
+    switch (fmt) {
+    case 0: return dispatch_bn<AMODE, 0>(bn, p, ma, mb, grid, s);
+    case 1: return dispatch_bn<AMODE, 1>(bn, p, ma, mb, grid, s);
+    case 2: return dispatch_bn<AMODE, 2>(bn, p, ma, mb, grid, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+int fmt_of(int in_dt) { return in_dt == BIGEMM_F16 ? 0 : in_dt == BIGEMM_BF16 ? 1 : 2; }
+
+}  // namespace
+
+size_t umma_smem_bytes(const UmmaTiling &t)
+{
+    switch (t.bn) {
+    case 64: return Cfg<64>::smem;
+    case 128: return Cfg<128>::smem;
+    case 256: return Cfg<256>::smem;
+    default: return 0;
+    }
+}
+
+bool umma_tiling_compiled(const UmmaTiling &t, int in_dt)
+{
+    (void)in_dt;
+    return (t.bn == 64 || t.bn == 128 || t.bn == 256) && (t.amode == A_NHWC || t.amode == A_DIRECT);
+}
+
+cudaError_t launch_umma_conv(const UmmaTiling &t, int in_dt, const UmmaParams &p,
+                             const CUtensorMap &map_a, const CUtensorMap &map_b, int grid,
+                             cudaStream_t stream)
+{
+    ProfScope prof(t.amode == A_NHWC ? "umma_conv_nhwc" : "umma_conv_direct", stream);
+    const int fmt = fmt_of(in_dt);
+    if (t.amode == A_NHWC) return dispatch_fmt<A_NHWC>(fmt, t.bn, p, map_a, map_b, grid, stream);
+    return dispatch_fmt<A_DIRECT>(fmt, t.bn, p, map_a, map_b, grid, stream);
+}
+
+}  // namespace bigemm

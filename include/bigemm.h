@@ -1,0 +1,209 @@
+/*
+ * bigemm.h -- C ABI of the broadcast / implicit-GEMM convolution library for
+ * one NVIDIA GB300 GPU (sm_103a).
+ *
+ * Operations (the sources that define them):
+ *
+ *  conv2d   NCHW 2-D convolution, as computed by topi.nn.conv2d_nchw in
+ *           "Tuning High Performance Convolution on NVIDIA GPUs" (TVM v0.5
+ *           autotvm tutorial), Step 1 (compute declaration, inlined padding):
+ *             out[n,f,y,x] = sum_{rc<CI/groups, ry<KH, rx<KW}
+ *                              pad(data)[n, g*CI/groups + rc, y*s+ry, x*s+rx]
+ *                              * kernel[f, rc, ry, rx]
+ *           with g = f / (CO/groups), pad() = `padding` zeros on every side,
+ *           dilation 1, Ho = floor((H + 2*padding - KH)/stride) + 1 (Wo alike).
+ *           The tutorial's template signature (N, H, W, CO, CI, KH, KW, stride,
+ *           padding) gives the argument order of conv2d_nchw_plan.
+ *  epilogue The per-channel broadcast of "[CINN] Add the TileBroadcastTactic
+ *           for NCHW broadcast" (PaddlePaddle PR 70092), Introduction and
+ *           Example, applied to the conv sum before the store:
+ *             out[n,f,y,x] = op(acc[n,f,y,x] + bias[f]).
+ *  bcast    The same PR's broadcast on its own:
+ *             out[n,c,h,w] = op(var[c]),  [1,C,1,1] => [N,C,H,W],
+ *           with the channel value computed once per channel block.
+ *  plan     A timed choice among a few kernel tilings per shape, the analogue
+ *           of the tutorial's Step 2 (tuning with a measure option of repeated
+ *           timed runs, keeping the best record for the workload).
+ *
+ * Conventions for every entry point:
+ *  * Tensors are contiguous and in the caller's DEVICE memory (pointers from
+ *    cudaMalloc / torch): data [N,CI,H,W] (NCHW), kernel [CO,CI/groups,KH,KW]
+ *    (OIHW), bias/var [C] fp32, out [N,CO,Ho,Wo] (NCHW).  The caller owns
+ *    them; the library never frees or retains them past the call.
+ *  * `stream` is a cudaStream_t (NULL = the legacy default stream).  Runs are
+ *    asynchronous on it; only conv2d_nchw_plan with search=1 synchronises.
+ *  * Every function returns a bigemm_status; none aborts or exits.  Shapes,
+ *    dtypes and alignment are checked before any launch.  A launch failure
+ *    returns BIGEMM_ERR_CUDA.  Kernels bound every wait; a wait that runs out
+ *    sets a sticky device flag read by bigemm_last_device_error().
+ *  * Plans own their scratch memory (packed operands, split-K partial sums),
+ *    allocated by conv2d_nchw_plan and freed by conv2d_nchw_plan_destroy.
+ *    Two runs of one plan must not overlap on the GPU (they share scratch).
+ */
+#ifndef BIGEMM_H
+#define BIGEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { BIGEMM_F32 = 0, BIGEMM_F16 = 1, BIGEMM_BF16 = 2 } bigemm_dtype;
+
+/* Fused epilogue: out = acc (NONE), acc + bias[f] (BIAS),
+ * exp(acc + bias[f]) (BIAS_EXP), 1/sqrt(acc + bias[f] + eps) (BIAS_RSQRT). */
+typedef enum {
+    BIGEMM_EPI_NONE = 0,
+    BIGEMM_EPI_BIAS = 1,
+    BIGEMM_EPI_BIAS_EXP = 2,
+    BIGEMM_EPI_BIAS_RSQRT = 3
+} bigemm_epilogue;
+
+typedef enum {
+    BIGEMM_OK = 0,
+    BIGEMM_ERR_INVALID_ARG = 1,   /* bad shape, null pointer, misaligned buffer   */
+    BIGEMM_ERR_UNSUPPORTED = 2,   /* valid conv this library does not implement  */
+    BIGEMM_ERR_CUDA = 3,          /* a CUDA runtime / driver call failed         */
+    BIGEMM_ERR_TIMEOUT = 4,       /* a bounded device wait ran out               */
+    BIGEMM_ERR_NO_CANDIDATE = 5   /* plan search found no runnable kernel        */
+} bigemm_status;
+
+/* Broadcast ops: out = var[c] (COPY), exp(var[c]) (EXP),
+ * 1/sqrt(fp32(var[c] + eps)) (RSQRT), 1/var[c] (RECIP). */
+typedef enum {
+    BIGEMM_BC_COPY = 0,
+    BIGEMM_BC_EXP = 1,
+    BIGEMM_BC_RSQRT = 2,
+    BIGEMM_BC_RECIP = 3
+} bigemm_bcast_op;
+
+/* Kernel families a plan can hold. */
+typedef enum {
+    BIGEMM_KIND_AUTO = 0,
+    BIGEMM_KIND_UMMA = 1,         /* tcgen05 implicit GEMM (TF32 / FP16 / BF16)  */
+    BIGEMM_KIND_SIMT = 2,         /* direct FP32-FMA conv (any shape, depthwise) */
+} bigemm_kind;
+
+typedef struct bigemm_plan_s *bigemm_plan;   /* opaque, library-owned */
+
+/* Optional overrides for conv2d_nchw_plan_ex; zero fields mean "choose". */
+typedef struct {
+    int kind;       /* bigemm_kind                                              */
+    int tile_n;     /* UMMA: output channels per tile, 16..256 step 16           */
+    int split_k;    /* UMMA: number of K slices (>= 1)                          */
+    int stages;     /* UMMA: shared-memory pipeline depth (2..8)                */
+    int box_w;      /* UMMA: output pixels per tile along W (with box_h)        */
+    int box_h;      /* UMMA: output rows per tile (box_w*box_h*boxes = 128)      */
+} bigemm_plan_options;
+
+/*
+ * conv2d_nchw_plan -- validate a conv shape and pick the kernel that runs it.
+ *   N,H,W      batch and input spatial size (N >= 1, H, W >= 1)
+ *   CO, CI     output / input channels; groups = 1, or groups = CI = CO
+ *              (depthwise)
+ *   KH, KW     kernel size; stride >= 1, padding >= 0 (dilation is 1)
+ *   in_dtype   type of data and kernel: F32 (TF32 tensor cores or FP32 FMA),
+ *              F16 or BF16 (fp32 accumulation)
+ *   out_dtype  type of out (F32, F16 or BF16)
+ *   epi        fused epilogue (bias is then required at run time)
+ *   search     0: heuristic choice, no launch; 1: time every valid candidate
+ *              with CUDA events on `stream` (synchronises) and keep the best
+ *   out_plan   receives the plan; free it with conv2d_nchw_plan_destroy.
+ * Errors: INVALID_ARG (Ho or Wo <= 0, bad groups, null out_plan),
+ * UNSUPPORTED (e.g. depthwise with a channel multiplier), CUDA,
+ * NO_CANDIDATE.  Plans are cached per (shape, dtypes, epilogue, device);
+ * each call still returns a fresh handle.
+ */
+bigemm_status conv2d_nchw_plan(int N, int H, int W, int CO, int CI, int KH, int KW,
+                               int stride, int padding, int groups,
+                               bigemm_dtype in_dtype, bigemm_dtype out_dtype,
+                               bigemm_epilogue epi, int search,
+                               void *stream, bigemm_plan *out_plan);
+
+/* As conv2d_nchw_plan, with optional overrides (opts may be NULL).  A forced
+ * choice that cannot run this shape returns UNSUPPORTED.  Forced plans are
+ * not cached. */
+bigemm_status conv2d_nchw_plan_ex(int N, int H, int W, int CO, int CI, int KH, int KW,
+                                  int stride, int padding, int groups,
+                                  bigemm_dtype in_dtype, bigemm_dtype out_dtype,
+                                  bigemm_epilogue epi, int search,
+                                  const bigemm_plan_options *opts,
+                                  void *stream, bigemm_plan *out_plan);
+
+/*
+ * conv2d_nchw_run -- run a plan on `stream`.
+ *   data   [N,CI,H,W] device, in_dtype, 16-byte aligned
+ *   kernel [CO,CI/groups,KH,KW] device, in_dtype, 16-byte aligned
+ *   bias   [CO] fp32 device, or NULL when the plan's epilogue is NONE
+ *   eps    added inside rsqrt for BIAS_RSQRT, ignored otherwise
+ *   out    [N,CO,Ho,Wo] device, out_dtype, 16-byte aligned; fully written
+ * Errors: INVALID_ARG (null or misaligned pointer, missing bias), CUDA.
+ */
+bigemm_status conv2d_nchw_run(bigemm_plan plan, const void *data, const void *kernel,
+                              const float *bias, float eps, void *out, void *stream);
+
+/* Free the plan and its scratch (synchronises with the device first). */
+bigemm_status conv2d_nchw_plan_destroy(bigemm_plan plan);
+
+/* Write a one-line JSON description of the plan (kernel, tiles, split-K,
+ * launches per run, scratch bytes, search records) into buf (NUL-terminated,
+ * truncated to len).  Returns INVALID_ARG for a NULL plan or buffer. */
+bigemm_status conv2d_nchw_plan_describe(bigemm_plan plan, char *buf, size_t len);
+
+/*
+ * bcast_nchw_run -- out[n,c,h,w] = op(var[c]) for all n < N, h < H, w < W.
+ *   var  [C] fp32 device; out [N,C,H,W] device of out_dtype (F32/F16/BF16).
+ *   op   bigemm_bcast_op; eps is used by RSQRT only.
+ * Errors: INVALID_ARG (N, C, H or W < 1, null pointer, bad op/dtype), CUDA.
+ */
+bigemm_status bcast_nchw_run(int N, int C, int H, int W, int op, const float *var, float eps,
+                             void *out, bigemm_dtype out_dtype, void *stream);
+
+/* The same broadcast written the way a generic fused-loop schedule does it:
+ * one flat loop over all N*C*H*W outputs, each recomputing op(var[c]) from
+ * its own index.  Kept to measure the per-channel mapping against it. */
+bigemm_status bcast_nchw_run_flat(int N, int C, int H, int W, int op, const float *var,
+                                  float eps, void *out, bigemm_dtype out_dtype, void *stream);
+
+/* Human-readable text of a status code (static storage). */
+const char *bigemm_status_string(bigemm_status s);
+
+/* Sticky device-side flag: BIGEMM_ERR_TIMEOUT once any kernel's bounded wait
+ * ran out on the current device, else BIGEMM_OK.  Synchronises the device. */
+bigemm_status bigemm_last_device_error(void);
+
+/* Clear the sticky device flag (synchronises the device). */
+bigemm_status bigemm_clear_device_error(void);
+
+/* Upper bound, in nanoseconds, of every device-side wait of later launches
+ * (default 2e9).  Values below 1000 are raised to 1000. */
+bigemm_status bigemm_set_wait_timeout_ns(uint64_t ns);
+
+/* Launch one block that waits on a barrier nothing will complete, bounded by
+ * timeout_ns; the host then sees BIGEMM_ERR_TIMEOUT from
+ * bigemm_last_device_error().  Exercises the timeout path without a fault. */
+bigemm_status bigemm_debug_wait_timeout(uint64_t timeout_ns, void *stream);
+
+/* Per-kernel timing with CUDA events recorded around each launch on its
+ * stream.  enable(1) starts recording (and clears old records). */
+typedef struct {
+    char name[48];
+    int launches;
+    double total_ms;
+} bigemm_kernel_time;
+
+bigemm_status bigemm_profile_enable(int on);
+/* Synchronises, then fills up to max entries; *count receives the number of
+ * distinct kernels.  Records stay until the next enable(1). */
+bigemm_status bigemm_profile_read(bigemm_kernel_time *out, int max, int *count);
+
+/* Library version string. */
+const char *bigemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BIGEMM_H */

@@ -1,0 +1,273 @@
+"""GPU parity of the convolution kernels against the CPU oracle, through the C ABI.
+
+Every case draws seeded inputs, runs the library (heuristic plan, a forced
+kernel, or the timed search), and compares every output element with the
+oracle's fp64 result within the bound of tests/tolerance.py.  Outputs start
+NaN-filled inside a guard band, so an unwritten element or a write outside
+the tensor fails the case.  Full-size cases (the benchmark's batch sizes)
+compare sampled output positions.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import broadcast_implicit_gemm_gb300 as bg
+import oracle
+from broadcast_implicit_gemm_gb300 import synth
+from tests.tolerance import TAU, assert_within, conv_bound, epi_bound
+
+pytestmark = pytest.mark.gpu
+
+DT = {"f32": bg.F32, "f16": bg.F16, "bf16": bg.BF16}
+NTH = max(1, os.cpu_count() or 1)
+GUARD = 4096
+SENTINEL = 12345.0
+
+
+def _alloc_out(shape, dtype):
+    n = int(np.prod(shape))
+    buf = torch.full((n + 2 * GUARD,), SENTINEL, dtype=dtype, device="cuda")
+    out = buf[GUARD:GUARD + n].view(shape)
+    out.fill_(float("nan"))
+    return buf, out
+
+
+def _guard_intact(buf):
+    g = torch.cat([buf[:GUARD], buf[-GUARD:]]).float().cpu()
+    return bool(torch.all(g == SENTINEL))
+
+
+def run(spec, options=None, search=0, seed=0, eps=1e-5):
+    x, w, b = synth.conv_inputs(spec, seed)
+    epi = bg.EPI_NAMES[spec.epi]
+    plan = bg.conv2d_nchw_plan_ex(spec.N, spec.H, spec.W, spec.CO, spec.CI, spec.K, spec.K,
+                                  spec.stride, spec.pad, spec.groups, DT[spec.in_dtype],
+                                  DT[spec.out_dtype], epi, search, options)
+    Ho = bg.out_size(spec.H, spec.K, spec.stride, spec.pad)
+    Wo = bg.out_size(spec.W, spec.K, spec.stride, spec.pad)
+    buf, out = _alloc_out((spec.N, spec.CO, Ho, Wo), synth.TORCH_DTYPES[spec.out_dtype])
+    bg.conv2d_nchw_run(plan, x.cuda(), w.cuda(), b.cuda() if b is not None else None, eps, out)
+    torch.cuda.synchronize()
+    assert bg.bigemm_last_device_error() == 0, "a device wait timed out"
+    assert _guard_intact(buf), "write outside the output tensor"
+    info = plan.describe()
+    plan.close()
+    return info, x, w, b, out
+
+
+def tau_for(spec, info):
+    if spec.in_dtype in ("f16", "bf16"):
+        return TAU["half"]
+    return TAU["tf32"] if info["kind"] == "umma" else TAU["fp32"]
+
+
+def check(spec, options=None, search=0, seed=0):
+    info, x, w, b, out = run(spec, options, search, seed)
+    got = out.cpu().double().numpy()
+    tau = tau_for(spec, info)
+    if spec.epi == "none":
+        ref, sabs = oracle.conv2d_nchw(x, w, stride=spec.stride, pad=spec.pad, groups=spec.groups,
+                                       nthreads=NTH)
+        bound = conv_bound(ref, sabs, tau, spec.out_dtype)
+    else:
+        epi = {"bias": oracle.EPI_BIAS, "bias_exp": oracle.EPI_BIAS_EXP,
+               "bias_rsqrt": oracle.EPI_BIAS_RSQRT}[spec.epi]
+        ref, sabs = oracle.conv2d_nchw(x, w, stride=spec.stride, pad=spec.pad, groups=spec.groups,
+                                       bias=b, epi=epi, nthreads=NTH)
+        pre, _ = oracle.conv2d_nchw(x, w, stride=spec.stride, pad=spec.pad, groups=spec.groups,
+                                    nthreads=NTH)
+        arg = pre + b.double().numpy().reshape(1, -1, 1, 1)
+        bound = epi_bound(arg, sabs, tau, spec.epi, spec.out_dtype, ref)
+    assert_within(got, ref, bound, f"{spec.name} [{info['cand']}]")
+    return info
+
+
+# ------------------------------------------------- workload shapes, heuristic plan
+SMALL = ([s for s in synth.RESNET_LAST] + synth.SWEEP_FP32
+         + [s.with_batch(2) for s in synth.RESNET50_FP16]
+         + [s.with_batch(2) for s in synth.FUSED_CONV]
+         + [s.with_batch(2) for s in synth.DEPTHWISE_FP16])
+
+
+@pytest.mark.parametrize("spec", SMALL, ids=lambda s: s.name)
+def test_workload_shapes_heuristic(spec):
+    info = check(spec)
+    if spec.groups == 1:
+        assert info["kind"] == "umma"
+
+
+# ------------------------------------------------- every kernel, forced
+FORCED_SHAPES = [synth.SWEEP_FP32[0], synth.SWEEP_FP32[3], synth.SWEEP_FP32[4],
+                 synth.RESNET50_FP16[1].with_batch(1), synth.RESNET50_FP16[4].with_batch(1)]
+
+
+@pytest.mark.parametrize("spec", FORCED_SHAPES, ids=lambda s: s.name)
+def test_simt_tiled_matches(spec):
+    info = check(spec, {"kind": bg.KIND_SIMT})
+    assert info["cand"] == "simt:tiled"
+
+
+@pytest.mark.parametrize("bn", [64, 128, 256])
+@pytest.mark.parametrize("spec", [synth.SWEEP_FP32[1], synth.RESNET50_FP16[1].with_batch(1),
+                                  synth.RESNET50_FP16[3].with_batch(2)], ids=lambda s: s.name)
+def test_umma_tile_n(spec, bn):
+    info = check(spec, {"kind": bg.KIND_UMMA, "tile_n": bn})
+    assert info["kind"] == "umma" and info["bn"] == bn
+
+
+@pytest.mark.parametrize("split", [1, 2, 3, 8, 32])
+def test_umma_split_k(split):
+    spec = synth.RESNET_LAST[0]
+    info = check(spec, {"kind": bg.KIND_UMMA, "tile_n": 128, "split_k": split})
+    kb = info["k_blocks"]
+    assert info["split"] == -(-kb // -(-kb // split))   # slices of ceil(kb/split) blocks
+
+
+@pytest.mark.parametrize("box", [(8, 16), (16, 8), (32, 4), (64, 2), (8, 8), (8, 4), (56, 1)])
+def test_umma_pixel_boxes(box):
+    spec = synth.RESNET50_FP16[1].with_batch(1)
+    info = check(spec, {"kind": bg.KIND_UMMA, "box_w": box[0], "box_h": box[1]})
+    assert info["box"][:2] == list(box) and info["amode"] == "nhwc"
+
+
+def test_umma_direct_and_nhwc_agree_on_1x1():
+    spec = synth.RESNET50_FP16[2].with_batch(2)
+    a = check(spec, {"kind": bg.KIND_UMMA, "tile_n": 128})
+    b = check(spec, {"kind": bg.KIND_UMMA, "tile_n": 128, "box_w": 8, "box_h": 16})
+    assert a["amode"] == "direct" and b["amode"] == "nhwc"
+
+
+# ------------------------------------------------- edge cases
+def S(name, N, CI, CO, H, W, K, s, p, g=1, i="f16", o="f16", epi="none", dd="uniform", kd="he"):
+    return synth.ConvSpec(name, N, CI, CO, H, W, K, s, p, g, i, o, dd, kd, epi)
+
+
+EDGE = [
+    S("ragged_13x11_ci24_co40", 2, 24, 40, 13, 11, 3, 1, 1),
+    S("ragged_fp32_ci20_co200", 1, 20, 200, 9, 10, 3, 1, 1, i="f32", o="f32"),
+    S("first_layer_ci3_k7_s2", 2, 3, 64, 31, 29, 7, 2, 3),
+    S("k5_pad2_bf16", 1, 32, 96, 17, 17, 5, 1, 2, i="bf16", o="bf16"),
+    S("k1_pad1_border", 1, 16, 32, 6, 6, 1, 1, 1),
+    S("stride3_k3", 1, 16, 48, 20, 20, 3, 3, 0),
+    S("out_1x1", 2, 64, 64, 3, 3, 3, 1, 0),
+    S("tall_kernel_5x1", 1, 16, 32, 12, 9, 5, 1, 0),
+    S("bias_exp_f32out", 2, 64, 128, 10, 10, 3, 1, 1, o="f32", epi="bias_exp"),
+    S("bias_rsqrt", 1, 32, 64, 8, 8, 3, 1, 1, o="f32", epi="bias_rsqrt", dd="absnormal"),
+    S("bias_only_bf16", 1, 32, 64, 8, 8, 3, 1, 1, i="bf16", o="f32", epi="bias"),
+    S("f32_in_f16_out", 1, 32, 64, 8, 8, 3, 1, 1, i="f32", o="f16"),
+    S("grouped_g2", 1, 16, 32, 9, 9, 3, 1, 1, g=2),
+    S("depthwise_k3_ragged", 3, 24, 24, 15, 13, 3, 2, 1, g=24, kd="dw"),
+    S("depthwise_k7", 1, 8, 8, 20, 20, 7, 1, 3, g=8, kd="dw"),
+    S("many_images_small", 37, 32, 32, 5, 5, 3, 1, 1),
+]
+
+
+@pytest.mark.parametrize("spec", EDGE, ids=lambda s: s.name)
+def test_edge_cases(spec):
+    check(spec)
+
+
+@pytest.mark.parametrize("spec", [e for e in EDGE if e.groups == 1][:8], ids=lambda s: s.name)
+def test_edge_cases_simt(spec):
+    check(spec, {"kind": bg.KIND_SIMT})
+
+
+# ------------------------------------------------- full size, sampled outputs
+FULL = synth.RESNET50_FP16 + synth.FUSED_CONV + synth.DEPTHWISE_FP16
+
+
+@pytest.mark.parametrize("spec", FULL, ids=lambda s: s.name)
+def test_full_size_sampled(spec):
+    info, x, w, b, out = run(spec)
+    total = out.numel()
+    idx = synth.random_flat_indices(total, 3000, seed=5)
+    # plus every border pixel of two planes
+    Ho, Wo = out.shape[2], out.shape[3]
+    planes = [0, total // (Ho * Wo) - 1]
+    border = [pl * Ho * Wo + y * Wo + xx for pl in planes for y in range(Ho) for xx in range(Wo)
+              if y in (0, Ho - 1) or xx in (0, Wo - 1)]
+    idx = torch.unique(torch.cat([idx, torch.tensor(border, dtype=torch.int64)])).numpy()
+    got = out.reshape(-1)[torch.from_numpy(idx).cuda()].cpu().double().numpy()
+    tau = tau_for(spec, info)
+    if spec.epi == "none":
+        ref, sabs = oracle.conv2d_nchw_points(x, w, idx, stride=spec.stride, pad=spec.pad,
+                                              groups=spec.groups)
+        bound = conv_bound(ref, sabs, tau, spec.out_dtype)
+    else:
+        ref, sabs = oracle.conv2d_nchw_points(x, w, idx, stride=spec.stride, pad=spec.pad,
+                                              groups=spec.groups, bias=b, epi=oracle.EPI_BIAS_EXP)
+        pre, _ = oracle.conv2d_nchw_points(x, w, idx, stride=spec.stride, pad=spec.pad,
+                                           groups=spec.groups)
+        f = (idx // (Ho * Wo)) % spec.CO
+        arg = pre + b.double().numpy()[f]
+        bound = epi_bound(arg, sabs, tau, spec.epi, spec.out_dtype, ref)
+    assert_within(got, ref, bound, f"{spec.name} [{info['cand']}]")
+    assert not torch.isnan(out).any()
+
+
+# ------------------------------------------------- plan search and cache
+def test_search_picks_a_timed_candidate_and_caches_it():
+    spec = S("search_small", 2, 64, 64, 14, 14, 3, 1, 1)
+    info = check(spec, search=1)
+    assert info["chosen_by"] in ("search", "cache")
+    if info["chosen_by"] == "search":
+        recs = info["search"]
+        assert len(recs) >= 3
+        ok = [r for r in recs if r["status"] == 0]
+        assert ok and info["cand"] == min(ok, key=lambda r: r["ms"])["cand"]
+    again = bg.conv2d_nchw_plan(spec.N, spec.H, spec.W, spec.CO, spec.CI, 3, 3, 1, 1, 1,
+                                bg.F16, bg.F16, bg.EPI_NONE, 1)
+    d = again.describe()
+    assert d["chosen_by"] == "cache" and d["cand"] == info["cand"]
+    again.close()
+
+
+def test_forced_invalid_tiling_is_rejected_before_launch():
+    with pytest.raises(bg.BigemmError) as e:
+        bg.conv2d_nchw_plan_ex(1, 8, 8, 64, 64, 3, 3, 1, 1, 1, bg.F16, bg.F16, bg.EPI_NONE, 0,
+                               {"kind": bg.KIND_UMMA, "tile_n": 96})
+    assert e.value.status == 2
+
+
+def test_misaligned_pointer_rejected():
+    plan = bg.conv2d_nchw_plan(1, 8, 8, 64, 64, 3, 3, 1, 1, 1, bg.F16, bg.F16, bg.EPI_NONE, 0)
+    x = torch.zeros(1 * 64 * 8 * 8 + 1, dtype=torch.float16, device="cuda")
+    w = torch.zeros(64 * 64 * 9, dtype=torch.float16, device="cuda")
+    o = torch.zeros(64 * 64, dtype=torch.float16, device="cuda")
+    with pytest.raises(bg.BigemmError) as e:
+        bg.conv2d_nchw_run(plan, x.data_ptr() + 2, w, None, 0.0, o)
+    assert e.value.status == 1
+    plan.close()
+
+
+def test_missing_bias_rejected():
+    plan = bg.conv2d_nchw_plan(1, 8, 8, 64, 64, 3, 3, 1, 1, 1, bg.F16, bg.F32, bg.EPI_BIAS_EXP, 0)
+    x = torch.zeros((1, 64, 8, 8), dtype=torch.float16, device="cuda")
+    w = torch.zeros((64, 64, 3, 3), dtype=torch.float16, device="cuda")
+    o = torch.zeros((1, 64, 8, 8), dtype=torch.float32, device="cuda")
+    with pytest.raises(bg.BigemmError) as e:
+        bg.conv2d_nchw_run(plan, x, w, None, 0.0, o)
+    assert e.value.status == 1
+    plan.close()
+
+
+def test_bounded_wait_reports_timeout_without_fault():
+    bg.bigemm_clear_device_error()
+    bg.bigemm_debug_wait_timeout(2_000_000)      # 2 ms on a barrier nothing completes
+    assert bg.bigemm_last_device_error() == 4
+    bg.bigemm_clear_device_error()
+    assert bg.bigemm_last_device_error() == 0
+    # the context is still usable
+    check(S("after_timeout", 1, 16, 32, 8, 8, 3, 1, 1))
+
+
+def test_profile_records_kernel_launches():
+    spec = synth.RESNET50_FP16[1].with_batch(1)
+    bg.bigemm_profile_enable(True)
+    run(spec)
+    rec = bg.bigemm_profile_read()
+    bg.bigemm_profile_enable(False)
+    assert any(k.startswith("umma_conv") for k in rec)
+    assert all(v[0] >= 1 and v[1] > 0 for v in rec.values())
