@@ -1,0 +1,560 @@
+#!/usr/bin/env python3
+"""Benchmark: NCHW conv2d TFLOP/s (and the broadcast's GB/s) on one GB300.
+
+Default workload: the fp32 batch-1 layer sweep, five layers
+(CI,CO,H,W,K,stride,pad) = (64,64,56,56,3,1,1), (128,128,28,28,3,1,1),
+(256,256,14,14,3,1,1), (256,512,14,14,3,2,1), (1024,256,14,14,1,1,0).  One
+step runs every layer once through the C ABI; the metric is the step's total
+FLOP over its device time.  Other workloads: --workload resnet_last |
+resnet50_fp16 | fused | depthwise_fp16 | bcast.
+
+Timing: W untimed warm-up steps; K timed steps, each bracketed by CUDA events
+on the launch stream (plus one event after every layer), with an L2 flush (a
+512 MB write) between steps outside the events.  Per-kernel device time comes
+from the library's own event records over the same steps.  `e2e` repeats the
+step with host buffers: pinned host->device copies of the inputs and a
+device->host copy of the outputs inside the timed region.  `cpu_baseline` times
+the CPU oracle on this host on a bounded sample of the same workload.  With
+--impl reference the CPU oracle is the measured arm.
+
+Multi-GPU: the layers and images are independent, so N ranks run N replicas of
+the step with no exchange (weak scaling); value = all ranks' work / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "conv2d TFLOP/s per shape and % of roofline at 1 GB300; broadcast HBM GB/s"
+L2_FLUSH_BYTES = 512 << 20
+
+
+# ---------------------------------------------------------------- workloads
+def workload_specs(name):
+    from broadcast_implicit_gemm_gb300 import synth
+    return {
+        "sweep_fp32": synth.SWEEP_FP32,
+        "resnet_last": synth.RESNET_LAST,
+        "resnet50_fp16": synth.RESNET50_FP16,
+        "fused": synth.FUSED_CONV,
+        "depthwise_fp16": synth.DEPTHWISE_FP16,
+    }[name]
+
+
+def out_hw(s):
+    return ((s.H + 2 * s.pad - s.K) // s.stride + 1, (s.W + 2 * s.pad - s.K) // s.stride + 1)
+
+
+def conv_flops(s):
+    Ho, Wo = out_hw(s)
+    return 2.0 * s.N * s.CO * Ho * Wo * (s.CI // s.groups) * s.K * s.K
+
+
+def _touched(n, k, stride, pad, nout):
+    return len({o * stride + r - pad for o in range(nout) for r in range(k)
+                if 0 <= o * stride + r - pad < n})
+
+
+def conv_bytes(s):
+    """Algorithmic bytes: the input pixels some tap reads, the kernel, the output, once each."""
+    Ho, Wo = out_hw(s)
+    e_in = 4 if s.in_dtype == "f32" else 2
+    e_out = 4 if s.out_dtype == "f32" else 2
+    pix = _touched(s.H, s.K, s.stride, s.pad, Ho) * _touched(s.W, s.K, s.stride, s.pad, Wo)
+    b = s.N * s.CI * pix * e_in + s.CO * (s.CI // s.groups) * s.K * s.K * e_in
+    b += s.N * s.CO * Ho * Wo * e_out
+    if s.epi != "none":
+        b += 4 * s.CO
+    return float(b)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm": float(p["hbm_gbs"]), "bf16": float(p["bf16_tflops"]),
+                "sm_max_mhz": float(p.get("sm_max_mhz", 2070.0)), "source": "measured"}
+    except Exception:
+        return {"hbm": 6800.0, "bf16": 1900.0, "sm_max_mhz": 2070.0, "source": "fallback"}
+
+
+def pipe_peak(peaks, in_dtype, kind):
+    """TFLOP/s of the pipe a kernel uses.  fp16 = bf16 (measured); tf32 = measured bf16 x
+    the nominal dense ratio 1.1/2.25; FP32 FMA = 152 SMs x 128 lanes x 2 x max clock."""
+    if kind == "simt":
+        return 152 * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12, "fp32 fma (derived)"
+    if in_dtype == "f32":
+        return peaks["bf16"] * 1.1 / 2.25, f"tf32 (bf16 {peaks['source']} x 1.1/2.25)"
+    return peaks["bf16"], f"bf16/fp16 ({peaks['source']})"
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = str(gpu_index)
+        try:
+            import torch
+            self.gpu = "GPU-" + str(torch.cuda.get_device_properties(gpu_index).uuid)
+        except Exception:
+            pass
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- GPU arm
+class ConvStep:
+    """Plans (timed search, cached) and device buffers for every layer of a workload."""
+
+    def __init__(self, specs, device, search=1, seed=0):
+        import torch
+
+        import broadcast_implicit_gemm_gb300 as bg
+        from broadcast_implicit_gemm_gb300 import synth
+        self.bg, self.torch = bg, torch
+        self.specs = specs
+        self.items = []
+        self.marks = None
+        for i, s in enumerate(specs):
+            x, w, b = synth.conv_inputs(s, seed + i)
+            Ho, Wo = out_hw(s)
+            plan = bg.conv2d_nchw_plan(s.N, s.H, s.W, s.CO, s.CI, s.K, s.K, s.stride, s.pad,
+                                       s.groups, bg.DTYPE_CODES[s.in_dtype],
+                                       bg.DTYPE_CODES[s.out_dtype], bg.EPI_NAMES[s.epi], search)
+            out = torch.empty((s.N, s.CO, Ho, Wo), dtype=synth.TORCH_DTYPES[s.out_dtype],
+                              device=device)
+            self.items.append({
+                "spec": s, "plan": plan, "info": plan.describe(),
+                "x_h": x.pin_memory(), "w_h": w.pin_memory(),
+                "b_h": b.pin_memory() if b is not None else None,
+                "x": x.to(device), "w": w.to(device), "b": b.to(device) if b is not None else None,
+                "out": out, "out_h": torch.empty(out.shape, dtype=out.dtype).pin_memory(),
+            })
+
+    def run(self, stream):
+        for i, it in enumerate(self.items):
+            self.bg.conv2d_nchw_run(it["plan"], it["x"], it["w"], it["b"], 1e-5, it["out"], stream)
+            if self.marks is not None:
+                ev = self.torch.cuda.Event(enable_timing=True)
+                ev.record(stream)
+                self.marks.append((i, ev))
+
+    def run_e2e(self, stream):
+        for it in self.items:
+            it["x"].copy_(it["x_h"], non_blocking=True)
+            it["w"].copy_(it["w_h"], non_blocking=True)
+            if it["b"] is not None:
+                it["b"].copy_(it["b_h"], non_blocking=True)
+            self.bg.conv2d_nchw_run(it["plan"], it["x"], it["w"], it["b"], 1e-5, it["out"], stream)
+            it["out_h"].copy_(it["out"], non_blocking=True)
+
+    def h2d_bytes(self):
+        return sum(it["x_h"].numel() * it["x_h"].element_size()
+                   + it["w_h"].numel() * it["w_h"].element_size()
+                   + (it["b_h"].numel() * 4 if it["b_h"] is not None else 0) for it in self.items)
+
+    def d2h_bytes(self):
+        return sum(it["out"].numel() * it["out"].element_size() for it in self.items)
+
+    def work(self):
+        return sum(conv_flops(it["spec"]) for it in self.items)
+
+
+class BcastStep:
+    def __init__(self, device, seed=0):
+        import torch
+
+        import broadcast_implicit_gemm_gb300 as bg
+        from broadcast_implicit_gemm_gb300 import synth
+        self.bg, self.torch = bg, torch
+        self.shape = synth.BCAST_SHAPE
+        N, C, H, W = self.shape
+        self.var_h = synth.bcast_var(C, seed).pin_memory()
+        self.var = self.var_h.to(device)
+        self.out = torch.empty(self.shape, dtype=torch.float32, device=device)
+        self.out_h = torch.empty(self.shape, dtype=torch.float32).pin_memory()
+        self.items = []
+        self.marks = None
+
+    def run(self, stream):
+        N, C, H, W = self.shape
+        self.bg.bcast_nchw_run(N, C, H, W, self.bg.BC_EXP, self.var, 1e-5, self.out, self.bg.F32,
+                               stream)
+
+    def run_e2e(self, stream):
+        self.var.copy_(self.var_h, non_blocking=True)
+        self.run(stream)
+        self.out_h.copy_(self.out, non_blocking=True)
+
+    def work(self):
+        return float(self.out.numel() * 4 + self.var.numel() * 4)
+
+    def h2d_bytes(self):
+        return self.var.numel() * 4
+
+    def d2h_bytes(self):
+        return self.out.numel() * 4
+
+
+def timed_steps(step_fn, steps, torch, stream, flush):
+    """Per-step CUDA event pairs (ms), with an L2 flush before each step."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for a, b in evs:
+            flush.fill_(1)
+            a.record(stream)
+            step_fn(stream)
+            b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs], evs
+
+
+def traffic_for(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if its source still matches."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(f"{kernel}@{workload}")
+    except Exception:
+        return None
+    if not rec:
+        return None
+    src = os.path.join(ROOT, "broadcast_implicit_gemm_gb300", "csrc", rec["source"])
+    try:
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    return rec["bytes_per_launch"] if h == rec["source_sha"] else None
+
+
+def kernel_work(name, it):
+    """Algorithmic (flop, bytes) of one layer's launch of kernel `name`, or None."""
+    s, info = it["spec"], it["info"]
+    e_in = 4 if s.in_dtype == "f32" else 2
+    Ho, Wo = out_hw(s)
+    if name.startswith("umma_conv"):
+        return (conv_flops(s), conv_bytes(s)) if name == "umma_conv_" + info.get("amode", "") else None
+    if name.startswith("simt_conv"):
+        return (conv_flops(s), conv_bytes(s)) if info["kind"] == "simt" else None
+    if name == "pack_nhwc" and info.get("amode") == "nhwc":
+        return (0.0, 2.0 * s.N * s.CI * s.H * s.W * e_in)
+    if name == "pack_weights" and info.get("amode") == "nhwc":
+        return (0.0, 2.0 * s.CO * s.CI * s.K * s.K * e_in)
+    if name == "splitk_reduce" and info.get("split", 1) > 1:
+        out = s.N * s.CO * Ho * Wo
+        return (0.0, out * 4.0 * info["split"] + out * (4 if s.out_dtype == "f32" else 2))
+    return None
+
+
+def kernel_roofline(name, prof, step, peaks, args):
+    """Roofline of kernel `name`: its algorithmic work per launch over its mean launch time."""
+    n, tms = prof[name]
+    works = [(kernel_work(name, it), it) for it in step.items]
+    works = [(w, it) for w, it in works if w is not None]
+    flop = sum(w[0] for w, _ in works) * args.steps / n
+    byts = sum(w[1] for w, _ in works) * args.steps / n
+    per_launch_s = tms / n / 1e3
+    kind = "simt" if name.startswith("simt") else "umma"
+    in_dt = works[0][1]["spec"].in_dtype if works else "f32"
+    tpk, src = pipe_peak(peaks, in_dt, kind)
+    t_flop = flop / (tpk * 1e12)
+    t_byte = byts / (peaks["hbm"] * 1e9)
+    if flop > 0 and t_flop >= t_byte:
+        ach = flop / per_launch_s / 1e12
+        r = {"bound": "tensor" if kind == "umma" else "alu", "achieved": ach, "peak": tpk,
+             "unit": "TFLOP/s", "frac": ach / tpk, "peak_source": src}
+    else:
+        ach = byts / per_launch_s / 1e9
+        r = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm"], "unit": "GB/s",
+             "frac": ach / peaks["hbm"], "peak_source": peaks["source"] + " copy bandwidth"}
+    r.update({"kernel": name, "launches": n, "avg_launch_us": per_launch_s * 1e6,
+              "flop_per_launch": flop, "bytes_per_launch": byts,
+              "roofline_frac": max(t_flop, t_byte) / per_launch_s,
+              "traffic": traffic_for(name, args.workload)})
+    return r
+
+
+def cpu_baseline(workload, specs, budget_s=12.0):
+    """The oracle as it stands, on this host's cores, on a bounded sample of the workload."""
+    import oracle
+    from broadcast_implicit_gemm_gb300 import synth
+    lib = oracle.load()
+    cores = oracle.num_threads(lib)
+    if workload == "bcast":
+        N, C, H, W = synth.BCAST_SHAPE
+        n_s = 8
+        var = synth.bcast_var(C, 0).numpy()
+        t0 = time.perf_counter()
+        reps = 0
+        while True:
+            oracle.bcast_nchw(n_s, C, H, W, oracle.BC_EXP, var, lib=lib)
+            reps += 1
+            if time.perf_counter() - t0 > budget_s or reps >= 50:
+                break
+        dt = (time.perf_counter() - t0) / reps
+        return {"value": n_s * C * H * W * 4 / dt / 1e9, "unit": "GB/s", "cores": 1,
+                "kind": "oracle",
+                "sample": f"[{n_s},{C},{H},{W}] of [{N},{C},{H},{W}] (fp32 bytes), {reps} reps"}
+    sample = [(s if s.N <= 2 else s.with_batch(1), i) for i, s in enumerate(specs)]
+    inputs = [(s, synth.conv_inputs(s, i)) for s, i in sample]
+    flops = sum(conv_flops(s) for s, _ in inputs)
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        for s, (x, w, b) in inputs:
+            oracle.conv2d_nchw(x, w, stride=s.stride, pad=s.pad, groups=s.groups, bias=b,
+                               epi=oracle.EPI_BIAS_EXP if s.epi == "bias_exp" else oracle.EPI_NONE,
+                               nthreads=cores, lib=lib)
+        reps += 1
+        if time.perf_counter() - t0 > budget_s or reps >= 200:
+            break
+    dt = (time.perf_counter() - t0) / reps
+    names = ", ".join(s.name for s, _ in sample)
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{len(sample)} layers ({names}); {reps} passes of {dt * 1e3:.1f} ms"}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as td
+        if args.impl == "reference":
+            td.init_process_group("gloo")
+        else:
+            import torch
+            torch.cuda.set_device(local)
+            td.init_process_group("nccl")
+        dist = td
+    return world, rank, local, dist
+
+
+def run_reference(args, world, rank):
+    """The CPU oracle as the measured arm (rank 0 only)."""
+    if rank != 0:
+        return 0
+    specs = None if args.workload == "bcast" else workload_specs(args.workload)
+    if specs is not None and args.layer:
+        specs = [x for x in specs if x.name == args.layer]
+    for _ in range(args.warmup):
+        cpu_baseline(args.workload, specs, budget_s=0.0)
+    budget = max(0.2, min(2.0, 120.0 / max(1, args.steps)))
+    per = [cpu_baseline(args.workload, specs, budget_s=budget) for _ in range(args.steps)]
+    v = statistics.median(p["value"] for p in per)
+    unit = per[0]["unit"]
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": unit, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload},
+        "cpu_baseline": {"value": v, "unit": unit, "cores": per[0]["cores"], "kind": "oracle",
+                         "sample": per[0]["sample"]},
+        "e2e": {"value": v, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default="sweep_fp32",
+                    choices=["sweep_fp32", "resnet_last", "resnet50_fp16", "fused",
+                             "depthwise_fp16", "bcast"])
+    ap.add_argument("--layer", default=None, help="run only the named layer of the workload")
+    ap.add_argument("--no-search", action="store_true", help="heuristic plans, no timed search")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world, rank, local, dist = dist_setup(args)
+    if args.impl == "reference":
+        rc = run_reference(args, world, rank)
+        if dist:
+            dist.destroy_process_group()
+        return rc
+
+    import torch
+
+    import broadcast_implicit_gemm_gb300 as bg
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    stream = torch.cuda.Stream(device)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+
+    if args.workload == "bcast":
+        step = BcastStep(device)
+        unit, scale = "GB/s", 1e9
+    else:
+        specs = workload_specs(args.workload)
+        if args.layer:
+            specs = [x for x in specs if x.name == args.layer]
+            if not specs:
+                raise SystemExit(f"no layer {args.layer} in {args.workload}")
+        step = ConvStep(specs, device, search=0 if args.no_search else 1)
+        unit, scale = "TFLOP/s", 1e12
+
+    for _ in range(args.warmup):
+        with torch.cuda.stream(stream):
+            step.run(stream)
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    bg.bigemm_profile_enable(True)
+    step.marks = []
+    times, evs = timed_steps(step.run, args.steps, torch, stream, flush)
+    marks, step.marks = step.marks, None
+    prof = bg.bigemm_profile_read()
+    bg.bigemm_profile_enable(False)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    if bg.bigemm_last_device_error() != 0:
+        raise SystemExit("a device wait timed out during the timed region")
+
+    total_ms = sum(times)
+    if dist:
+        t = torch.tensor([total_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = step.work() * world / (ms_per_step / 1e3) / scale
+
+    # end to end through the public call, host buffers in and out
+    for _ in range(2):
+        with torch.cuda.stream(stream):
+            step.run_e2e(stream)
+    torch.cuda.synchronize()
+    e2e_steps = max(3, min(args.steps, 20))
+    e2e_times, _ = timed_steps(step.run_e2e, e2e_steps, torch, stream, flush)
+    e2e_ms = sum(e2e_times) / e2e_steps
+    e2e_value = step.work() * world / (e2e_ms / 1e3) / scale
+
+    peaks = load_peaks()
+    line = {
+        "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "data": "synthetic",
+        "gpu_launches": sum(v[0] for v in prof.values()), "clocks": clk,
+        "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": step.h2d_bytes(),
+                "d2h_bytes_per_step": step.d2h_bytes(), "ms_per_step": e2e_ms},
+    }
+    if args.workload == "bcast":
+        line["dtype"] = "f32"
+        line["config"] = {"workload": "bcast_exp_[128,256,32,32]_fp32", "op": "exp",
+                          "l2": "output (134 MB) larger than L2; 512 MB flush between steps"}
+        n, tms = prof.get("bcast_nchw", (args.steps, total_ms))
+        ach = step.work() / (tms / n / 1e3) / 1e9
+        line["roofline"] = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm"], "unit": "GB/s",
+                            "frac": ach / peaks["hbm"], "kernel": "bcast_nchw", "launches": n,
+                            "avg_launch_us": tms / n * 1e3,
+                            "peak_source": peaks["source"] + " copy bandwidth",
+                            "traffic": traffic_for("bcast_nchw", args.workload)}
+    else:
+        kinds = sorted({it["info"]["kind"] for it in step.items})
+        in_dt = step.items[0]["spec"].in_dtype
+        line["dtype"] = "tf32" if in_dt == "f32" and kinds == ["umma"] else in_dt
+        line["config"] = {"workload": args.workload,
+                          "layers": [it["spec"].name for it in step.items],
+                          "batch": step.items[0]["spec"].N,
+                          "plans": [it["info"]["cand"] for it in step.items],
+                          "l2": "flushed between steps (512 MB write)"}
+        # per-layer device time from the marks recorded after each layer
+        layer_ms = [0.0] * len(step.items)
+        starts = [a for a, _ in evs]
+        per_step = len(step.items)
+        for s_i in range(args.steps):
+            prev = starts[s_i]
+            for j in range(per_step):
+                _, ev = marks[s_i * per_step + j]
+                layer_ms[j] += prev.elapsed_time(ev)
+                prev = ev
+        per_layer = []
+        for it, ms in zip(step.items, layer_ms):
+            s = it["spec"]
+            tpk, src = pipe_peak(peaks, s.in_dtype, it["info"]["kind"])
+            t_flop = conv_flops(s) / (tpk * 1e12)
+            t_byte = conv_bytes(s) / (peaks["hbm"] * 1e9)
+            t = ms / args.steps / 1e3
+            per_layer.append({"layer": s.name, "plan": it["info"]["cand"],
+                              "us": t * 1e6, "tflops": conv_flops(s) / t / 1e12,
+                              "roofline_us": max(t_flop, t_byte) * 1e6,
+                              "roofline_frac": max(t_flop, t_byte) / t,
+                              "bound": "tensor" if t_flop >= t_byte else "hbm"})
+        line["per_layer"] = per_layer
+        if prof:
+            dominant = max(prof.items(), key=lambda kv: kv[1][1])[0]
+            line["roofline"] = kernel_roofline(dominant, prof, step, peaks, args)
+        line["kernels"] = {k: {"launches": v[0], "ms": v[1]} for k, v in prof.items()}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.workload,
+                                            None if args.workload == "bcast" else step.specs)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

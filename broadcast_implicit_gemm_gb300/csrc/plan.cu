@@ -100,6 +100,9 @@ bool umma_valid(const ConvShape &s, const UmmaTiling &t, int sm_count, std::stri
     if (t.bpt < 1) return bad("boxes per tile < 1");
     if (t.amode == A_DIRECT) {
         if (s.KH != 1 || s.KW != 1 || s.stride != 1 || s.pad != 0) return bad("direct mode needs 1x1/s1/p0");
+        // The direct mode reads data as an MN-major operand; tf32 MMAs take
+        // K-major operands only (measured: an MN-major tf32 A reads as zeros).
+        if (s.in_dt == BIGEMM_F32) return bad("direct mode needs 16-bit operands");
         if (((long long)s.H * s.W * e) % 16) return bad("H*W row not 16-byte multiple");
         if ((s.CI * e) % 16) return bad("CI row not 16-byte multiple");
         if (t.box_w != (int)(128 / e) || t.box_h != 1 || t.bpt * t.box_w != 128)

@@ -47,7 +47,7 @@ def test_bcast_small(shape, op, dt):
     var = synth.bcast_var(C, seed=C)
     if op == "rsqrt":
         var[0] = 0.0
-        var[-1] = -np.float32(1e-5)   # the float sum is exactly zero: +inf
+        var[-1] = -float(np.float32(1e-5))   # the float sum is exactly zero: +inf
     out = torch.full((N, C, H, W), 7.0, dtype=TD[dt], device="cuda")
     bg.bcast_nchw_run(N, C, H, W, OPS[op], var.cuda(), 1e-5, out, bg.DTYPE_CODES[dt])
     torch.cuda.synchronize()

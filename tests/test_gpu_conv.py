@@ -23,7 +23,7 @@ pytestmark = pytest.mark.gpu
 DT = {"f32": bg.F32, "f16": bg.F16, "bf16": bg.BF16}
 NTH = max(1, os.cpu_count() or 1)
 GUARD = 4096
-SENTINEL = 12345.0
+SENTINEL = -7.25   # exact in fp32, fp16 and bf16
 
 
 def _alloc_out(shape, dtype):
