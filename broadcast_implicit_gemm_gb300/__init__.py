@@ -19,7 +19,8 @@ __all__ = [
     "BC_COPY", "BC_EXP", "BC_RSQRT", "BC_RECIP", "KIND_AUTO", "KIND_UMMA", "KIND_SIMT",
     "BigemmError", "Plan", "PlanOptions", "library_path", "load_library",
     "conv2d_nchw_plan", "conv2d_nchw_plan_ex", "conv2d_nchw_run", "conv2d_nchw_plan_destroy",
-    "conv2d_nchw_plan_describe", "bcast_nchw_run", "bcast_nchw_run_flat",
+    "conv2d_nchw_plan_describe", "conv2d_nchw_run_noalloc", "bcast_nchw_run",
+    "bcast_nchw_run_flat",
     "bigemm_status_string", "bigemm_last_device_error", "bigemm_clear_device_error",
     "bigemm_set_wait_timeout_ns", "bigemm_debug_wait_timeout", "bigemm_profile_enable",
     "bigemm_profile_read", "bigemm_version", "conv2d", "bcast", "out_size",
@@ -82,6 +83,7 @@ def _declare(lib):
     lib.conv2d_nchw_run.argtypes = [p, p, p, p, f, p, p]
     lib.conv2d_nchw_plan_destroy.argtypes = [p]
     lib.conv2d_nchw_plan_describe.argtypes = [p, ctypes.c_char_p, sz]
+    lib.conv2d_nchw_run_noalloc.argtypes = [i] * 9 + [i, i, i, p, p, p, f, p, p, p]
     lib.bcast_nchw_run.argtypes = [i, i, i, i, i, p, f, p, i, p]
     lib.bcast_nchw_run_flat.argtypes = [i, i, i, i, i, p, f, p, i, p]
     lib.bigemm_status_string.argtypes = [i]
@@ -95,6 +97,7 @@ def _declare(lib):
     lib.bigemm_version.argtypes = []
     lib.bigemm_version.restype = ctypes.c_char_p
     for name in ("conv2d_nchw_plan", "conv2d_nchw_plan_ex", "conv2d_nchw_run",
+                 "conv2d_nchw_run_noalloc",
                  "conv2d_nchw_plan_destroy", "conv2d_nchw_plan_describe", "bcast_nchw_run",
                  "bcast_nchw_run_flat", "bigemm_last_device_error", "bigemm_clear_device_error",
                  "bigemm_set_wait_timeout_ns", "bigemm_debug_wait_timeout",
@@ -201,6 +204,17 @@ def conv2d_nchw_plan_describe(plan: Plan) -> str:
     _check(load_library().conv2d_nchw_plan_describe(plan.handle, buf, len(buf)),
            "conv2d_nchw_plan_describe")
     return buf.value.decode()
+
+
+def conv2d_nchw_run_noalloc(N, H, W, CO, CI, KH, KW, stride, padding, in_dtype, out_dtype, epi,
+                            data, kernel, bias, eps, out, timeout_flag=None, stream=None):
+    """The allocation-free convolution (no plan; scratch in the library's fixed
+    device array).  For callers that cannot allocate device memory."""
+    _check(load_library().conv2d_nchw_run_noalloc(N, H, W, CO, CI, KH, KW, stride, padding,
+                                                  in_dtype, out_dtype, epi, _ptr(data),
+                                                  _ptr(kernel), _ptr(bias), float(eps), _ptr(out),
+                                                  _ptr(timeout_flag), _stream(stream)),
+           "conv2d_nchw_run_noalloc")
 
 
 def bcast_nchw_run(N, C, H, W, op, var, eps, out, out_dtype, stream=None):

@@ -167,6 +167,48 @@ bigemm_status bcast_nchw_run(int N, int C, int H, int W, int op, const float *va
 bigemm_status bcast_nchw_run_flat(int N, int C, int H, int W, int op, const float *var,
                                   float eps, void *out, bigemm_dtype out_dtype, void *stream);
 
+/*
+ * conv2d_nchw_run_noalloc -- the same convolution for callers that cannot
+ * allocate device memory: code that runs where cudaMalloc is forbidden or
+ * would break a memory budget someone else fixed, and so can neither create a
+ * plan (plans own cudaMalloc'd scratch) nor lend the library a workspace.
+ * The sources have no counterpart of this call; it exists for those callers.
+ *
+ * It runs the channels-last tensor-core kernel (the packed-operand path with
+ * split-K when the tiles alone leave SMs idle) with every scratch byte in one
+ * fixed array in the library's own device memory: 16 MiB (16777216 bytes),
+ * held on every GPU that loads the library until the process exits.  The
+ * scratch a shape needs is
+ *   256 + r(N*H*W*Ch*e) + r(CO*KH*KW*cip*e) + S*N*CO*Ho*Wo*4 bytes,
+ * where r() rounds up to 256, e is the input element size, Ch = CI rounded up
+ * to 16/e, cip = CI rounded up to 128/e, and S is the number of K slices
+ * (S = 1 unless the pixel tiles times the channel tiles cover less than half
+ * the SMs).  Shapes that need more return BIGEMM_ERR_UNSUPPORTED before any
+ * launch.
+ *
+ * Arguments and layouts are those of conv2d_nchw_plan + conv2d_nchw_run with
+ * groups = 1 (data [N,CI,H,W], kernel [CO,CI,KH,KW], bias [CO] fp32, out
+ * [N,CO,Ho,Wo], device pointers owned by the caller, 16-byte aligned;
+ * stride <= 8).  timeout_flag is an optional device int the kernels set to 4
+ * (BIGEMM_ERR_TIMEOUT) if a bounded device wait runs out; when NULL a word of
+ * the scratch array takes its place and is cleared at every call.
+ *
+ * The call allocates nothing: no cudaMalloc, cudaFree or allocating library
+ * routine.  The first call on a device looks up the device address of the
+ * scratch array (cudaGetSymbolAddress, with that device current), so make
+ * that first call before any stream capture.  Every call on a device shares
+ * the one array and leaves its contents behind; calls whose kernels overlap on
+ * the GPU (different streams, or several host threads) race on it and must be
+ * ordered by the caller.  Errors: INVALID_ARG (bad shape, dtype, epilogue,
+ * null or misaligned pointer, missing bias), UNSUPPORTED (scratch above the
+ * limit, stride > 8), CUDA.
+ */
+bigemm_status conv2d_nchw_run_noalloc(int N, int H, int W, int CO, int CI, int KH, int KW,
+                                      int stride, int padding, bigemm_dtype in_dtype,
+                                      bigemm_dtype out_dtype, bigemm_epilogue epi,
+                                      const void *data, const void *kernel, const float *bias,
+                                      float eps, void *out, int *timeout_flag, void *stream);
+
 /* Human-readable text of a status code (static storage). */
 const char *bigemm_status_string(bigemm_status s);
 
