@@ -540,7 +540,8 @@ def main():
                               "us": t * 1e6, "tflops": conv_flops(s) / t / 1e12,
                               "roofline_us": max(t_flop, t_byte) * 1e6,
                               "roofline_frac": max(t_flop, t_byte) / t,
-                              "bound": "tensor" if t_flop >= t_byte else "hbm"})
+                              "bound": ("tensor" if it["info"]["kind"] == "umma" else "alu")
+                              if t_flop >= t_byte else "hbm"})
         line["per_layer"] = per_layer
         if prof:
             dominant = max(prof.items(), key=lambda kv: kv[1][1])[0]

@@ -47,13 +47,13 @@ struct UmmaParams {
     int N, CI, H, W, CO, KH, KW, stride, pad, Ho, Wo;
     int box_w, box_h, bpt;          // pixel boxes
     int boxes_x, boxes_y;           // boxes per image row / column (A_NHWC)
-    long long boxes_per_img;
-    long long total_boxes;
+    int boxes_per_img;
+    int total_boxes;
     int pix_tiles, co_tiles;
     int k_blocks, kb_per_split, split;
     int ci_blocks, bk;              // channels per K block (128 bytes)
     int cip;                        // packed weight channels per tap (A_NHWC)
-    long long units;
+    int units;
     int epi;
     float eps;
     const float *bias;
@@ -63,12 +63,15 @@ struct UmmaParams {
     long long out_elems;
     int *err;
     unsigned long long timeout_ns;
+    int store_tma;                  // 1: stage tiles in smem, write with TMA stores (map_c)
 };
 
 // Returns a CUDA error code of the launch.
+// map_c describes the output (or the split-K workspace) for TMA stores; it is
+// read only when p.store_tma is set.
 cudaError_t launch_umma_conv(const UmmaTiling &t, int in_dt, const UmmaParams &p,
-                             const CUtensorMap &map_a, const CUtensorMap &map_b, int grid,
-                             cudaStream_t stream);
+                             const CUtensorMap &map_a, const CUtensorMap &map_b,
+                             const CUtensorMap &map_c, int grid, cudaStream_t stream);
 size_t umma_smem_bytes(const UmmaTiling &t);
 bool umma_tiling_compiled(const UmmaTiling &t, int in_dt);
 

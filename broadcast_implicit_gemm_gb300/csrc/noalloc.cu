@@ -149,10 +149,12 @@ extern "C" bigemm_status conv2d_nchw_run_noalloc(int N, int H, int W, int CO, in
     p.box_w = t.box_w, p.box_h = t.box_h, p.bpt = t.bpt;
     p.boxes_x = (int)cdiv(Wo, t.box_w);
     p.boxes_y = (int)cdiv(Ho, t.box_h);
-    p.boxes_per_img = (long long)p.boxes_x * p.boxes_y;
+    const long long bpi = (long long)p.boxes_x * p.boxes_y;
+    if ((long long)N * bpi >= (1ll << 30)) return BIGEMM_ERR_UNSUPPORTED;
+    p.boxes_per_img = (int)bpi;
     p.k_blocks = KH * KW * p.ci_blocks;
     p.cip = p.ci_blocks * p.bk;
-    p.total_boxes = (long long)N * p.boxes_per_img;
+    p.total_boxes = N * p.boxes_per_img;
     p.pix_tiles = (int)cdiv(p.total_boxes, t.bpt);
     p.co_tiles = (int)cdiv(CO, t.bn);
     const long long tiles = (long long)p.pix_tiles * p.co_tiles;
@@ -162,7 +164,8 @@ extern "C" bigemm_status conv2d_nchw_run_noalloc(int N, int H, int W, int CO, in
     p.kb_per_split = (int)cdiv(p.k_blocks, split);
     p.split = (int)cdiv(p.k_blocks, p.kb_per_split);
     t.split = p.split;
-    p.units = tiles * p.split;
+    if (tiles * p.split >= (1ll << 31)) return BIGEMM_ERR_UNSUPPORTED;
+    p.units = (int)(tiles * p.split);
     p.epi = epi, p.eps = eps, p.bias = bias, p.out_dt = out_dtype;
     p.out_elems = (long long)N * CO * Ho * Wo;
     p.timeout_ns = wait_timeout_ns();
@@ -219,7 +222,8 @@ extern "C" bigemm_status conv2d_nchw_run_noalloc(int N, int H, int W, int CO, in
                                                         KH * KW, p.cip);
     if (cudaGetLastError() != cudaSuccess) return BIGEMM_ERR_CUDA;
     const int grid = (int)std::min<long long>(p.units, sms);
-    if (launch_umma_conv(t, in_dtype, p, map_a, map_b, grid, s) != cudaSuccess)
+    // p.store_tma = 0: the epilogue stores straight from registers (map_c unread)
+    if (launch_umma_conv(t, in_dtype, p, map_a, map_b, map_a, grid, s) != cudaSuccess)
         return BIGEMM_ERR_CUDA;
     if (p.split > 1) {
         const int rgrid = (int)std::min<long long>(cdiv(p.out_elems, 256), (long long)sms * 16);

@@ -44,6 +44,49 @@ __global__ void pack_nhwc_kernel(const T *__restrict__ x, T *__restrict__ xh, in
     }
 }
 
+// 16-byte vectors on both sides: a tile of TILE channels x TILE pixels is read
+// as rows of pixels and written as rows of channels.  The odd row pitch keeps
+// the column reads of the transpose free of bank conflicts.
+template <typename T>
+__global__ void __launch_bounds__(256) pack_nhwc_vec_kernel(const T *__restrict__ x,
+                                                            T *__restrict__ xh, int C, int HW,
+                                                            int Ch)
+{
+    constexpr int VEC = 16 / sizeof(T);
+    constexpr int TILE = 8 * VEC;
+    __shared__ T tile[TILE][TILE + 1];
+    const int n = blockIdx.z;
+    const int p0 = blockIdx.x * TILE, c0 = blockIdx.y * TILE;
+    const T *xs = x + (size_t)n * C * HW;
+    T *xd = xh + (size_t)n * HW * Ch;
+    for (int v = threadIdx.x; v < TILE * 8; v += blockDim.x) {
+        const int cr = v >> 3, pv = v & 7;
+        const int c = c0 + cr, pix = p0 + pv * VEC;
+        union {
+            uint4 u;
+            T e[VEC];
+        } val;
+        val.u = make_uint4(0, 0, 0, 0);
+        if (c < C && pix < HW) val.u = *reinterpret_cast<const uint4 *>(xs + (size_t)c * HW + pix);
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) tile[cr][pv * VEC + i] = val.e[i];
+    }
+    __syncthreads();
+    for (int v = threadIdx.x; v < TILE * 8; v += blockDim.x) {
+        const int pr = v >> 3, cv = v & 7;
+        const int pix = p0 + pr, c = c0 + cv * VEC;
+        if (pix < HW && c < Ch) {
+            union {
+                uint4 u;
+                T e[VEC];
+            } val;
+#pragma unroll
+            for (int i = 0; i < VEC; ++i) val.e[i] = tile[cv * VEC + i][pr];
+            *reinterpret_cast<uint4 *>(xd + (size_t)pix * Ch + c) = val.u;
+        }
+    }
+}
+
 template <typename T>
 __global__ void pack_weights_kernel(const T *__restrict__ w, T *__restrict__ wp, int CO, int CI,
                                     int KHKW, int cip)
@@ -110,6 +153,19 @@ cudaError_t launch_pack_nhwc(const void *x, void *xh, int N, int C, int HW, int 
                              cudaStream_t stream)
 {
     ProfScope prof("pack_nhwc", stream);
+    const int vec = (int)(16 / dtype_size(dt));
+    const bool aligned = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(xh)) & 15) == 0;
+    if (aligned && HW % vec == 0 && Ch % vec == 0) {
+        const int tile = 8 * vec;
+        dim3 g((HW + tile - 1) / tile, (Ch + tile - 1) / tile, N);
+        if (dtype_size(dt) == 4)
+            pack_nhwc_vec_kernel<uint32_t><<<g, 256, 0, stream>>>(
+                static_cast<const uint32_t *>(x), static_cast<uint32_t *>(xh), C, HW, Ch);
+        else
+            pack_nhwc_vec_kernel<uint16_t><<<g, 256, 0, stream>>>(
+                static_cast<const uint16_t *>(x), static_cast<uint16_t *>(xh), C, HW, Ch);
+        return cudaGetLastError();
+    }
     dim3 grid((HW + 31) / 32, (Ch + 31) / 32, N), block(32, 8);
     if (dtype_size(dt) == 4)
         pack_nhwc_kernel<uint32_t><<<grid, block, 0, stream>>>(

@@ -10,6 +10,8 @@
 // (its repeat / min_repeat_ms measure option); and the best record is kept per
 // workload, like its log of best configurations.
 #include <algorithm>
+#include <climits>
+#include <cstdint>
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
@@ -86,41 +88,6 @@ long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 
 bool is_depthwise(const ConvShape &s) { return s.groups > 1 && s.groups == s.CI && s.CO == s.CI; }
 
-// Host-side validity of a UMMA tiling for a shape; reason on failure.
-bool umma_valid(const ConvShape &s, const UmmaTiling &t, int sm_count, std::string *why)
-{
-    auto bad = [&](const char *m) {
-        if (why) *why = m;
-        return false;
-    };
-    const size_t e = dtype_size(s.in_dt);
-    if (s.groups != 1) return bad("grouped conv");
-    if (t.bn != 64 && t.bn != 128 && t.bn != 256) return bad("tile_n not 64/128/256");
-    if (t.split < 1) return bad("split < 1");
-    if (t.bpt < 1) return bad("boxes per tile < 1");
-    if (t.amode == A_DIRECT) {
-        if (s.KH != 1 || s.KW != 1 || s.stride != 1 || s.pad != 0) return bad("direct mode needs 1x1/s1/p0");
-        // The direct mode reads data as an MN-major operand; tf32 MMAs take
-        // K-major operands only (measured: an MN-major tf32 A reads as zeros).
-        if (s.in_dt == BIGEMM_F32) return bad("direct mode needs 16-bit operands");
-        if (((long long)s.H * s.W * e) % 16) return bad("H*W row not 16-byte multiple");
-        if ((s.CI * e) % 16) return bad("CI row not 16-byte multiple");
-        if (t.box_w != (int)(128 / e) || t.box_h != 1 || t.bpt * t.box_w != 128)
-            return bad("direct box must be one 128-byte row of pixels");
-    } else {
-        if (s.stride > 8) return bad("stride > 8");
-        if (t.box_w < 1 || t.box_h < 1) return bad("empty box");
-        if ((t.box_w * t.box_h) % 8) return bad("box pixels not a multiple of 8");
-        if (t.box_w * t.box_h * t.bpt > 128) return bad("boxes exceed 128 rows");
-        if (t.box_w * s.stride > 256 || t.box_h * s.stride > 256) return bad("box > 256");
-    }
-    if (umma_smem_bytes(t) == 0) return bad("no compiled kernel");
-    DeviceState *ds = device_state();
-    if (ds && (int)umma_smem_bytes(t) > ds->max_smem_optin) return bad("smem exceeds opt-in limit");
-    (void)sm_count;
-    return true;
-}
-
 struct Box {
     int w, h, bpt;
     double eff;
@@ -160,6 +127,7 @@ struct UmmaGeom {
     UmmaParams p;
     int grid;
     int ch, cip;
+    bool fits;      // box and unit counts fit the kernel's 32-bit indexing
 };
 
 UmmaGeom umma_geometry(const ConvShape &s, const UmmaTiling &t, int sm_count)
@@ -172,32 +140,75 @@ UmmaGeom umma_geometry(const ConvShape &s, const UmmaTiling &t, int sm_count)
     p.bk = 128 / e;
     p.ci_blocks = (int)ceil_div(s.CI, p.bk);
     p.box_w = t.box_w, p.box_h = t.box_h, p.bpt = t.bpt;
+    long long bpi;
     if (t.amode == A_NHWC) {
         p.boxes_x = (int)ceil_div(s.Wo, t.box_w);
         p.boxes_y = (int)ceil_div(s.Ho, t.box_h);
-        p.boxes_per_img = (long long)p.boxes_x * p.boxes_y;
+        bpi = (long long)p.boxes_x * p.boxes_y;
         p.k_blocks = s.KH * s.KW * p.ci_blocks;
         g.cip = p.ci_blocks * p.bk;
         g.ch = (int)ceil_div(s.CI, 16 / e) * (16 / e);
     } else {
         p.boxes_x = 1, p.boxes_y = 1;
-        p.boxes_per_img = ceil_div((long long)s.H * s.W, t.box_w);
+        bpi = ceil_div((long long)s.H * s.W, t.box_w);
         p.k_blocks = p.ci_blocks;
         g.cip = s.CI;
         g.ch = s.CI;
     }
     p.cip = g.cip;
-    p.total_boxes = (long long)s.N * p.boxes_per_img;
-    p.pix_tiles = (int)ceil_div(p.total_boxes, t.bpt);
+    const long long total = (long long)s.N * bpi;
+    const long long ptiles = ceil_div(total, t.bpt);
     p.co_tiles = (int)ceil_div(s.CO, t.bn);
     p.kb_per_split = (int)ceil_div(p.k_blocks, t.split);
     p.split = (int)ceil_div(p.k_blocks, p.kb_per_split);
-    p.units = (long long)p.pix_tiles * p.co_tiles * p.split;
+    const long long units = ptiles * p.co_tiles * p.split;
+    g.fits = total < (1ll << 31) && units < (1ll << 31);
+    p.boxes_per_img = (int)std::min<long long>(bpi, INT32_MAX);
+    p.total_boxes = (int)std::min<long long>(total, INT32_MAX);
+    p.pix_tiles = (int)std::min<long long>(ptiles, INT32_MAX);
+    p.units = (int)std::min<long long>(units, INT32_MAX);
     p.epi = s.epi;
     p.out_dt = s.out_dt;
     p.out_elems = (long long)s.N * s.CO * s.Ho * s.Wo;
     g.grid = (int)std::min<long long>(p.units, sm_count);
     return g;
+}
+
+// Host-side validity of a UMMA tiling for a shape; reason on failure.
+bool umma_valid(const ConvShape &s, const UmmaTiling &t, int sm_count, std::string *why)
+{
+    auto bad = [&](const char *m) {
+        if (why) *why = m;
+        return false;
+    };
+    const size_t e = dtype_size(s.in_dt);
+    if (s.groups != 1) return bad("grouped conv");
+    if (t.bn != 64 && t.bn != 128 && t.bn != 256) return bad("tile_n not 64/128/256");
+    if (t.split < 1) return bad("split < 1");
+    if (t.bpt < 1) return bad("boxes per tile < 1");
+    if (t.amode == A_DIRECT) {
+        if (s.KH != 1 || s.KW != 1 || s.stride != 1 || s.pad != 0) return bad("direct mode needs 1x1/s1/p0");
+        // The direct mode reads data as an MN-major operand; tf32 MMAs take
+        // K-major operands only (measured: an MN-major tf32 A reads as zeros).
+        if (s.in_dt == BIGEMM_F32) return bad("direct mode needs 16-bit operands");
+        if (((long long)s.H * s.W * e) % 16) return bad("H*W row not 16-byte multiple");
+        if ((s.CI * e) % 16) return bad("CI row not 16-byte multiple");
+        if (t.box_w != (int)(128 / e) || t.box_h != 1 || t.bpt * t.box_w != 128)
+            return bad("direct box must be one 128-byte row of pixels");
+    } else {
+        if (s.stride > 8) return bad("stride > 8");
+        if (t.box_w < 1 || t.box_h < 1) return bad("empty box");
+        if ((t.box_w * t.box_h) % 8) return bad("box pixels not a multiple of 8");
+        if (t.box_w * t.box_h * t.bpt > 128) return bad("boxes exceed 128 rows");
+        if (t.box_w * s.stride > 256 || t.box_h * s.stride > 256) return bad("box > 256");
+    }
+    if (t.bpt > 16) return bad("more than 16 boxes per tile");
+    if (umma_smem_bytes(t) == 0) return bad("no compiled kernel");
+    if (!umma_geometry(s, t, 1).fits) return bad("more than 2^31 boxes or work units");
+    DeviceState *ds = device_state();
+    if (ds && (int)umma_smem_bytes(t) > ds->max_smem_optin) return bad("smem exceeds opt-in limit");
+    (void)sm_count;
+    return true;
 }
 
 }  // namespace
@@ -218,8 +229,10 @@ struct bigemm_plan_s {
     size_t wp_bytes = 0;
     float *ws = nullptr;
     size_t ws_bytes = 0;
-    CUtensorMap map_a{}, map_b{};
+    CUtensorMap map_a{}, map_b{}, map_c{};
     const void *map_a_src = nullptr, *map_b_src = nullptr;   // DIRECT: pointers encoded
+    const void *map_c_src = nullptr;                         // output pointer encoded in map_c
+    bool store_tma = false;
     bool maps_ready = false;
     std::string search_log;
     std::string chosen_by = "heuristic";
@@ -398,6 +411,44 @@ std::vector<Cand> candidates(const ConvShape &s, int sms)
 }
 
 // ------------------------------------------------------------ scratch + run
+// Output tiles can be written by TMA stores when the output's (or the split-K
+// workspace's) innermost extent and every box start are 16-byte aligned.
+bool store_tma_ok(const ConvShape &s, const UmmaTiling &t, int split)
+{
+    const long long ec = split > 1 ? 4 : (long long)dtype_size(s.out_dt);
+    if ((t.box_w * ec) % 16) return false;
+    // each epilogue warp stores its 32 pixels as one box: 32 of a row, or whole rows
+    const bool wide = t.box_w % 32 == 0;
+    if (!wide && !(32 % t.box_w == 0 && (t.box_w * t.box_h) % 32 == 0)) return false;
+    if (t.amode == A_DIRECT) return ((long long)s.Ho * s.Wo * ec) % 16 == 0;
+    return ((long long)s.Wo * ec) % 16 == 0;
+}
+
+bool encode_store_map(bigemm_plan_s *p, void *dst, bool is_ws)
+{
+    const ConvShape &s = p->s;
+    const UmmaTiling &t = p->c.t;
+    const int split = p->g.p.split;
+    const uint64_t ec = is_ws ? 4 : dtype_size(s.out_dt);
+    const CUtensorMapDataType dt = is_ws ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : tma_dt(s.out_dt);
+    const uint64_t nn = (uint64_t)s.N * (is_ws ? split : 1);
+    if (t.amode == A_DIRECT) {
+        const uint64_t hw = (uint64_t)s.Ho * s.Wo;
+        const uint64_t dims[3] = {hw, (uint64_t)s.CO, nn};
+        const uint64_t str[2] = {hw * ec, hw * s.CO * ec};
+        const uint32_t box[3] = {32u, 32u, 1u};
+        const uint32_t es[3] = {1u, 1u, 1u};
+        return encode_tiled(&p->map_c, dt, 3, dst, dims, str, box, es, CU_TENSOR_MAP_SWIZZLE_NONE);
+    }
+    const uint64_t dims[4] = {(uint64_t)s.Wo, (uint64_t)s.Ho, (uint64_t)s.CO, nn};
+    const uint64_t str[3] = {(uint64_t)s.Wo * ec, (uint64_t)s.Ho * s.Wo * ec,
+                             (uint64_t)s.CO * s.Ho * s.Wo * ec};
+    const uint32_t sw = t.box_w >= 32 ? 32u : (uint32_t)t.box_w;
+    const uint32_t box[4] = {sw, 32u / sw, 32u, 1u};
+    const uint32_t es[4] = {1u, 1u, 1u, 1u};
+    return encode_tiled(&p->map_c, dt, 4, dst, dims, str, box, es, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
 void free_scratch(bigemm_plan_s *p)
 {
     if (p->xh) cudaFree(p->xh);
@@ -443,6 +494,11 @@ bigemm_status setup_plan(bigemm_plan_s *p)
     if (p->g.p.split > 1) {
         p->ws_bytes = (size_t)p->g.p.split * p->g.p.out_elems * sizeof(float);
         if (cudaMalloc(&p->ws, p->ws_bytes) != cudaSuccess) return BIGEMM_ERR_CUDA;
+    }
+    p->store_tma = store_tma_ok(s, t, p->g.p.split) && !getenv("BIGEMM_NO_TMA_STORE");
+    if (p->store_tma && p->g.p.split > 1) {
+        if (!encode_store_map(p, p->ws, true)) p->store_tma = false;
+        p->map_c_src = p->ws;
     }
     return BIGEMM_OK;
 }
@@ -516,7 +572,17 @@ bigemm_status run_plan(bigemm_plan_s *p, const void *data, const void *kernel, c
         bigemm_status r = encode_direct_maps(p, data, kernel);
         if (r != BIGEMM_OK) return r;
     }
-    e = launch_umma_conv(p->c.t, s.in_dt, up, p->map_a, p->map_b, p->g.grid, st);
+    up.store_tma = 0;
+    if (p->store_tma) {
+        if (up.split == 1 && p->map_c_src != out) {
+            if (encode_store_map(p, out, false))
+                p->map_c_src = out;
+            else
+                p->map_c_src = nullptr;
+        }
+        up.store_tma = p->map_c_src != nullptr ? 1 : 0;
+    }
+    e = launch_umma_conv(p->c.t, s.in_dt, up, p->map_a, p->map_b, p->map_c, p->g.grid, st);
     if (e != cudaSuccess) return BIGEMM_ERR_CUDA;
     if (up.split > 1) {
         e = launch_splitk_reduce(p->ws, up.split, up.out_elems, s.CO, s.Ho * s.Wo, s.epi, bias, eps,
@@ -860,7 +926,8 @@ bigemm_status conv2d_nchw_plan_describe(bigemm_plan plan, char *buf, size_t len)
            << ", \"split\": " << p.split << ", \"k_blocks\": " << p.k_blocks
            << ", \"pix_tiles\": " << p.pix_tiles << ", \"co_tiles\": " << p.co_tiles
            << ", \"units\": " << p.units << ", \"grid\": " << plan->g.grid
-           << ", \"smem\": " << umma_smem_bytes(c.t);
+           << ", \"smem\": " << umma_smem_bytes(c.t)
+           << ", \"store\": \"" << (plan->store_tma ? "tma" : "direct") << "\"";
     }
     os << ", \"launches\": " << launches_per_run(plan)
        << ", \"scratch_bytes\": " << (plan->xh_bytes + plan->wp_bytes + plan->ws_bytes)

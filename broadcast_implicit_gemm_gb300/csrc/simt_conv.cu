@@ -162,9 +162,21 @@ __global__ void conv_naive_kernel(SimtArgs a, const void *__restrict__ x,
     }
 }
 
-constexpr int kDwMaxTaps = 49;   // up to 7x7 kernels keep their taps in registers
+constexpr int kDwMaxTaps = 49;   // up to 7x7 kernels
+constexpr int kDwPX = 4;         // neighbouring outputs per thread along x
 
-// grid: (row bands, C, N); dynamic smem: (rows_in) x (W + 2*pad) floats.
+// Row pitch of the staged band: room for every window of the last x group.
+__host__ __device__ inline int dw_pitch(int W, int pad, int Wo, int KW, int S)
+{
+    const int gx = (Wo + kDwPX - 1) / kDwPX;
+    const int need = (gx * kDwPX - 1) * S + KW;
+    const int wp = W + 2 * pad;
+    return need > wp ? need : wp;
+}
+
+// grid: (row bands, C, N); dynamic smem: rows_in x pitch floats.  K and S are
+// compile-time (0 = read from the arguments).
+template <int K, int S>
 __global__ void __launch_bounds__(256) conv_depthwise_kernel(SimtArgs a, int rows_per_block,
                                                              const void *__restrict__ x,
                                                              const void *__restrict__ w,
@@ -172,38 +184,72 @@ __global__ void __launch_bounds__(256) conv_depthwise_kernel(SimtArgs a, int row
                                                              void *__restrict__ out)
 {
     extern __shared__ float srow[];
+    __shared__ float tap_s[kDwMaxTaps];
+    const int KH = K ? K : a.KH, KW = K ? K : a.KW, st = S ? S : a.stride;
     const int c = blockIdx.y, n = blockIdx.z;
     const int y0 = blockIdx.x * rows_per_block;
     const int y1 = min(a.Ho, y0 + rows_per_block);
-    const int iy0 = y0 * a.stride - a.pad;
-    const int rows_in = (y1 - 1 - y0) * a.stride + a.KH;
-    const int wp = a.W + 2 * a.pad;
+    const int iy0 = y0 * st - a.pad;
+    const int rows_in = (y1 - 1 - y0) * st + KH;
+    const int pitch = dw_pitch(a.W, a.pad, a.Wo, KW, st);
     const size_t plane = ((size_t)n * a.CI + c) * a.H * a.W;
-    // stage rows [iy0, iy0 + rows_in) with zero borders
-    for (int e = threadIdx.x; e < rows_in * wp; e += blockDim.x) {
-        const int r = e / wp, cc = e - r * wp;
+    // stage rows [iy0, iy0 + rows_in) with zero borders (and zero tail columns)
+    for (int e = threadIdx.x; e < rows_in * pitch; e += blockDim.x) {
+        const int r = e / pitch, cc = e - r * pitch;
         const int iy = iy0 + r, ix = cc - a.pad;
         float v = 0.f;
-        if (iy >= 0 && iy < a.H && ix >= 0 && ix < a.W) v = ld_in(x, plane + (size_t)iy * a.W + ix, a.in_dt);
+        if (iy >= 0 && iy < a.H && ix >= 0 && ix < a.W)
+            v = ld_in(x, plane + (size_t)iy * a.W + ix, a.in_dt);
         srow[e] = v;
     }
-    float tap[kDwMaxTaps];
-    const int KK = a.KH * a.KW;
-#pragma unroll
-    for (int t = 0; t < kDwMaxTaps; ++t) tap[t] = t < KK ? ld_in(w, (size_t)c * KK + t, a.in_dt) : 0.f;
+    if (threadIdx.x < KH * KW) tap_s[threadIdx.x] = ld_in(w, (size_t)c * KH * KW + threadIdx.x, a.in_dt);
     __syncthreads();
-    const int HoWo = a.Ho * a.Wo;
-    const size_t obase = ((size_t)n * a.CO + c) * HoWo;
-    const int cnt = (y1 - y0) * a.Wo;
+    const size_t obase = ((size_t)n * a.CO + c) * a.Ho * a.Wo;
+    const int gx = (a.Wo + kDwPX - 1) / kDwPX;
+    const int cnt = (y1 - y0) * gx;
+    const float bv = a.epi != BIGEMM_EPI_NONE ? bias[c] : 0.f;
     for (int e = threadIdx.x; e < cnt; e += blockDim.x) {
-        const int yy = e / a.Wo, xo = e - yy * a.Wo;
-        const float *base = srow + (yy * a.stride) * wp + xo * a.stride;
-        float acc = 0.f;
-        int t = 0;
-        for (int ry = 0; ry < a.KH; ++ry)
-            for (int rx = 0; rx < a.KW; ++rx, ++t) acc = fmaf(base[ry * wp + rx], tap[t], acc);
-        st_out(out, obase + (size_t)(y0 + yy) * a.Wo + xo, epi_apply(a.epi, acc, bias, c, a.eps),
-               a.out_dt);
+        const int yy = e / gx, xg = e - yy * gx;
+        const int xo0 = xg * kDwPX;
+        float acc[kDwPX];
+#pragma unroll
+        for (int i = 0; i < kDwPX; ++i) acc[i] = 0.f;
+        if (K) {
+            constexpr int WIN = (kDwPX - 1) * (S ? S : 1) + (K ? K : 1);
+#pragma unroll
+            for (int ry = 0; ry < (K ? K : 1); ++ry) {
+                const float *rp = srow + (yy * st + ry) * pitch + xo0 * st;
+                float win[WIN];
+#pragma unroll
+                for (int i = 0; i < WIN; ++i) win[i] = rp[i];
+#pragma unroll
+                for (int i = 0; i < kDwPX; ++i)
+#pragma unroll
+                    for (int rx = 0; rx < (K ? K : 1); ++rx)
+                        acc[i] = fmaf(win[i * (S ? S : 1) + rx], tap_s[ry * (K ? K : 1) + rx], acc[i]);
+            }
+        } else {
+            for (int ry = 0; ry < KH; ++ry) {
+                const float *rp = srow + (yy * st + ry) * pitch + xo0 * st;
+                for (int rx = 0; rx < KW; ++rx) {
+                    const float t = tap_s[ry * KW + rx];
+#pragma unroll
+                    for (int i = 0; i < kDwPX; ++i) acc[i] = fmaf(rp[i * st + rx], t, acc[i]);
+                }
+            }
+        }
+        const size_t orow = obase + (size_t)(y0 + yy) * a.Wo;
+#pragma unroll
+        for (int i = 0; i < kDwPX; ++i) {
+            const int xo = xo0 + i;
+            if (xo < a.Wo) {
+                float v = acc[i];
+                if (a.epi == BIGEMM_EPI_BIAS) v += bv;
+                else if (a.epi == BIGEMM_EPI_BIAS_EXP) v = expf(v + bv);
+                else if (a.epi == BIGEMM_EPI_BIAS_RSQRT) v = rsqrtf(v + bv + a.eps);
+                st_out(out, orow + xo, v, a.out_dt);
+            }
+        }
     }
 }
 
@@ -242,7 +288,8 @@ cudaError_t launch_simt_conv(const ConvShape &s, const void *x, const void *w,
 
 size_t dw_smem_bytes(const ConvShape &s, int rows)
 {
-    return (size_t)((rows - 1) * s.stride + s.KH) * (s.W + 2 * s.pad) * sizeof(float);
+    return (size_t)((rows - 1) * s.stride + s.KH) * dw_pitch(s.W, s.pad, s.Wo, s.KW, s.stride) *
+           sizeof(float);
 }
 
 cudaError_t launch_dw_conv(const ConvShape &s, const void *x, const void *w, const float *bias,
@@ -252,14 +299,23 @@ cudaError_t launch_dw_conv(const ConvShape &s, const void *x, const void *w, con
     if (s.KH * s.KW > kDwMaxTaps) return cudaErrorInvalidValue;
     const SimtArgs a = make_args(s, eps);
     const size_t smem = dw_smem_bytes(s, rows_per_block);
-    if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(conv_depthwise_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-    }
     dim3 grid((s.Ho + rows_per_block - 1) / rows_per_block, s.CO, s.N);
-    conv_depthwise_kernel<<<grid, 256, smem, stream>>>(a, rows_per_block, x, w, bias, out);
-    return cudaGetLastError();
+    auto go = [&](auto kern) {
+        if (smem > 48 * 1024) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)smem);
+            if (e != cudaSuccess) return e;
+        }
+        kern<<<grid, 256, smem, stream>>>(a, rows_per_block, x, w, bias, out);
+        return cudaGetLastError();
+    };
+    const bool sq = s.KH == s.KW;
+    if (sq && s.KH == 3 && s.stride == 1) return go(conv_depthwise_kernel<3, 1>);
+    if (sq && s.KH == 3 && s.stride == 2) return go(conv_depthwise_kernel<3, 2>);
+    if (sq && s.KH == 5 && s.stride == 1) return go(conv_depthwise_kernel<5, 1>);
+    if (sq && s.KH == 5 && s.stride == 2) return go(conv_depthwise_kernel<5, 2>);
+    if (sq && s.KH == 7 && s.stride == 1) return go(conv_depthwise_kernel<7, 1>);
+    return go(conv_depthwise_kernel<0, 0>);
 }
 
 }  // namespace bigemm

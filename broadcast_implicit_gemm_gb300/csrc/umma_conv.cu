@@ -42,52 +42,37 @@ struct Cfg {
     static constexpr int stages = BN <= 64 ? 8 : (BN <= 128 ? 6 : 4);
     static constexpr int b_bytes = BN * kRowBytes;
     static constexpr int ring = stages * (kABytes + b_bytes);
+    static constexpr int stage_buf = 16384;                  // one staged 32-channel output chunk
+    static constexpr int staging = 2 * stage_buf;
     static constexpr int bars = (2 * stages + 5) * 8;
-    static constexpr int smem = ring + bars + 16 + 1024;   // + alignment slack
+    static constexpr int smem = ring + staging + bars + 16 + 16 + 1024;   // + alignment slack
     static constexpr uint32_t tmem_cols = (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
                                          : (2 * BN <= 256) ? 256 : 512;
 };
-
-__device__ __forceinline__ float epi_apply(int epi, float acc, float b, float eps)
-{
-    switch (epi) {
-    case BIGEMM_EPI_NONE: return acc;
-    case BIGEMM_EPI_BIAS: return acc + b;
-    case BIGEMM_EPI_BIAS_EXP: return expf(acc + b);
-    default: return rsqrtf(acc + b + eps);
-    }
-}
-
-__device__ __forceinline__ void store_out(void *out, long long i, float v, int dt)
-{
-    if (dt == BIGEMM_F32)
-        static_cast<float *>(out)[i] = v;
-    else if (dt == BIGEMM_F16)
-        static_cast<__half *>(out)[i] = __float2half_rn(v);
-    else
-        static_cast<__nv_bfloat16 *>(out)[i] = __float2bfloat16_rn(v);
-}
 
 struct Unit {
     int ct, pt, sp, kb0, kb1;
 };
 
-__device__ __forceinline__ Unit decode(const UmmaParams &p, long long u)
+__device__ __forceinline__ Unit decode(const UmmaParams &p, int u)
 {
     Unit w;
-    w.ct = (int)(u % p.co_tiles);
-    const long long r = u / p.co_tiles;
-    w.pt = (int)(r % p.pix_tiles);
-    w.sp = (int)(r / p.pix_tiles);
+    const int r = u / p.co_tiles;
+    w.ct = u - r * p.co_tiles;
+    w.sp = r / p.pix_tiles;
+    w.pt = r - w.sp * p.pix_tiles;
     w.kb0 = w.sp * p.kb_per_split;
     w.kb1 = min(p.k_blocks, w.kb0 + p.kb_per_split);
     return w;
 }
 
+constexpr int kMaxBoxes = 16;   // boxes per tile: 128 rows / at least 8 pixels per box
+
 template <int BN, int AMODE, int FMT>
 __global__ void __launch_bounds__(kThreads, 1)
     umma_conv_kernel(const __grid_constant__ CUtensorMap map_a,
-                     const __grid_constant__ CUtensorMap map_b, const UmmaParams p)
+                     const __grid_constant__ CUtensorMap map_b,
+                     const __grid_constant__ CUtensorMap map_c, const UmmaParams p)
 {
     using C = Cfg<BN>;
     constexpr int S = C::stages;
@@ -95,7 +80,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *sa = smem;
     uint8_t *sb = smem + S * kABytes;
-    uint64_t *full = reinterpret_cast<uint64_t *>(sb + S * C::b_bytes);
+    uint8_t *stage_out = sb + S * C::b_bytes;               // 4 warps x 2 x 4 KB output staging
+    uint64_t *full = reinterpret_cast<uint64_t *>(stage_out + C::staging);
     uint64_t *empty = full + S;
     uint64_t *tfull = empty + S;
     uint64_t *tempty = tfull + 2;
@@ -121,6 +107,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_mbar_init();
         tma_prefetch_desc(&map_a);
         tma_prefetch_desc(&map_b);
+        if (p.store_tma) tma_prefetch_desc(&map_c);
     }
     if (warp == 1) {
         __syncwarp();
@@ -141,11 +128,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool issued[S];
             for (int i = 0; i < S; ++i) issued[i] = false, last_parity[i] = 0;
             bool ok = true;
-            for (long long u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+            for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
                 const Unit w = decode(p, u);
-                const long long box0 = (long long)w.pt * p.bpt;
-                const int nbox = (int)min((long long)p.bpt, p.total_boxes - box0);
+                const int box0 = w.pt * p.bpt;
+                const int nbox = min(p.bpt, p.total_boxes - box0);
                 const uint32_t tx = (uint32_t)nbox * box_bytes + (uint32_t)C::b_bytes;
+                // per-box origin of this tile, computed once
+                int bx[kMaxBoxes], by[kMaxBoxes], bn[kMaxBoxes];
+#pragma unroll
+                for (int i = 0; i < kMaxBoxes; ++i) {
+                    bx[i] = by[i] = bn[i] = 0;
+                    if (i < nbox) {
+                        const int bb = box0 + i;
+                        const int n = bb / p.boxes_per_img;
+                        const int rem = bb - n * p.boxes_per_img;
+                        bn[i] = n;
+                        if (AMODE == A_NHWC) {
+                            const int byi = rem / p.boxes_x, bxi = rem - byi * p.boxes_x;
+                            bx[i] = bxi * p.box_w * p.stride - p.pad;
+                            by[i] = byi * p.box_h * p.stride - p.pad;
+                        } else {
+                            bx[i] = rem * p.box_w;
+                        }
+                    }
+                }
+                // walk K as (ry, rx, channel block) with counters
+                int tap = w.kb0 / p.ci_blocks;
+                int cb = w.kb0 - tap * p.ci_blocks;
+                int ry = tap / p.KW, rx = tap - ry * p.KW;
+                const int ncol = w.ct * BN;
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag, p.err)) {
                         ok = false;
@@ -157,31 +168,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint8_t *a_dst = sa + stage * kABytes;
                     uint8_t *b_dst = sb + stage * C::b_bytes;
                     if (AMODE == A_NHWC) {
-                        const int tap = kb / p.ci_blocks, cb = kb - tap * p.ci_blocks;
-                        const int ry = tap / p.KW, rx = tap - ry * p.KW;
-                        for (int i = 0; i < nbox; ++i) {
-                            const long long b = box0 + i;
-                            const int n = (int)(b / p.boxes_per_img);
-                            const int rem = (int)(b - (long long)n * p.boxes_per_img);
-                            const int byi = rem / p.boxes_x, bxi = rem - byi * p.boxes_x;
-                            const int x = bxi * p.box_w * p.stride - p.pad + rx;
-                            const int y = byi * p.box_h * p.stride - p.pad + ry;
-                            tma_load_4d(a_dst + i * box_bytes, &map_a, &full[stage], cb * p.bk,
-                                        x, y, n);
-                        }
-                        tma_load_2d(b_dst, &map_b, &full[stage], tap * p.cip + cb * p.bk,
-                                    w.ct * BN);
+#pragma unroll
+                        for (int i = 0; i < kMaxBoxes; ++i)
+                            if (i < nbox)
+                                tma_load_4d(a_dst + i * box_bytes, &map_a, &full[stage], cb * p.bk,
+                                            bx[i] + rx, by[i] + ry, bn[i]);
+                        tma_load_2d(b_dst, &map_b, &full[stage],
+                                    (ry * p.KW + rx) * p.cip + cb * p.bk, ncol);
                     } else {
-                        for (int i = 0; i < nbox; ++i) {
-                            const long long b = box0 + i;
-                            const int n = (int)(b / p.boxes_per_img);
-                            const int p0 = (int)(b - (long long)n * p.boxes_per_img) * p.box_w;
-                            tma_load_3d(a_dst + i * box_bytes, &map_a, &full[stage], p0,
-                                        kb * p.bk, n);
-                        }
-                        tma_load_2d(b_dst, &map_b, &full[stage], kb * p.bk, w.ct * BN);
+#pragma unroll
+                        for (int i = 0; i < kMaxBoxes; ++i)
+                            if (i < nbox)
+                                tma_load_3d(a_dst + i * box_bytes, &map_a, &full[stage], bx[i],
+                                            kb * p.bk, bn[i]);
+                        tma_load_2d(b_dst, &map_b, &full[stage], kb * p.bk, ncol);
                     }
                     if (++stage == S) stage = 0, phase ^= 1u;
+                    if (++cb == p.ci_blocks) {
+                        cb = 0;
+                        if (++rx == p.KW) rx = 0, ++ry;
+                    }
                 }
             }
             if (!ok) {
@@ -207,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true, any = false;
-            for (long long u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+            for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
                 const Unit w = decode(p, u);
                 if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, p.timeout_ns, abort_flag, p.err)) {
                     ok = false;
@@ -254,67 +260,149 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // --------------------------------------------------------- epilogue
+        // Each warp owns TMEM lanes 32q..32q+31 (32 pixels of the tile) and
+        // works alone: lane 0 waits for the accumulator and shares the outcome,
+        // so the warp stays converged.  With TMA stores the warp stages its
+        // 32 pixels x 32 channels in its own shared buffers and lane 0 writes
+        // them as one box.
         const int q = warp & 3;                     // TMEM lane quadrant of this warp
         const int row = q * 32 + lane;              // tile row = pixel
         const int bi = row / box_px, bj = row - bi * box_px;
+        const int wbi = (q * 32) / box_px;          // the warp's box
+        const int wj0 = (q * 32) - wbi * box_px;    // its first pixel in the box
         const long long howo = (long long)p.Ho * p.Wo;
-        int acc = 0;
+        const int ec = p.ws ? 4 : (p.out_dt == BIGEMM_F32 ? 4 : 2);
+        uint8_t *wstage = stage_out + q * 8192;     // 2 x 4 KB per warp
+        int acc = 0, chunk = 0;
         uint32_t acc_phase = 0;
-        for (long long u = blockIdx.x; u < p.units; u += gridDim.x) {
+        for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
             const Unit w = decode(p, u);
-            if (!mbar_wait(&tfull[acc], acc_phase, p.timeout_ns, abort_flag, p.err)) break;
+            int okw = 0;
+            if (lane == 0) okw = mbar_wait(&tfull[acc], acc_phase, p.timeout_ns, abort_flag, p.err);
+            if (!__shfl_sync(0xffffffffu, okw, 0)) break;
             tc_fence_after();
-            const long long b = (long long)w.pt * p.bpt + bi;
+            const int b = w.pt * p.bpt + bi;
             bool valid = bi < p.bpt && b < p.total_boxes;
             long long base = 0;
             if (valid) {
-                const int n = (int)(b / p.boxes_per_img);
-                const long long rem = b - (long long)n * p.boxes_per_img;
+                const int n = b / p.boxes_per_img;
+                const int rem = b - n * p.boxes_per_img;
                 long long pix;
                 if (AMODE == A_NHWC) {
-                    const int byi = (int)(rem / p.boxes_x), bxi = (int)(rem - (long long)byi * p.boxes_x);
+                    const int byi = rem / p.boxes_x, bxi = rem - byi * p.boxes_x;
                     const int y = byi * p.box_h + bj / p.box_w;
                     const int x = bxi * p.box_w + bj % p.box_w;
                     valid = y < p.Ho && x < p.Wo;
                     pix = (long long)y * p.Wo + x;
                 } else {
-                    pix = rem * p.box_w + bj;
+                    pix = (long long)rem * p.box_w + bj;
                     valid = pix < howo;
                 }
-                base = (long long)n * p.CO * howo + pix;
+                base = ((long long)w.sp * p.N + n) * p.CO * howo + pix;
+            }
+            // the warp's store box (TMA mode): origin and image index
+            const int wb = w.pt * p.bpt + wbi;
+            const bool wbox = p.store_tma && wbi < p.bpt && wb < p.total_boxes;
+            int sx = 0, sy = 0, sn = 0;
+            if (wbox) {
+                const int n = wb / p.boxes_per_img;
+                const int rem = wb - n * p.boxes_per_img;
+                sn = w.sp * p.N + n;
+                if (AMODE == A_NHWC) {
+                    const int byi = rem / p.boxes_x, bxi = rem - byi * p.boxes_x;
+                    sx = bxi * p.box_w + wj0 % p.box_w;
+                    sy = byi * p.box_h + wj0 / p.box_w;
+                } else {
+                    sx = rem * p.box_w + wj0;
+                }
             }
             const int co0 = w.ct * BN;
-            float *ws = p.ws ? p.ws + (long long)w.sp * p.out_elems : nullptr;
 #pragma unroll 1
-            for (int c0 = 0; c0 < BN; c0 += 32) {
+            for (int c0 = 0; c0 < BN; c0 += 32, ++chunk) {
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + c0),
                                    r);
                 tmem_wait_ld();
-                if (valid) {
+                if (c0 + 32 >= BN) {                // accumulator drained: hand it back
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&tempty[acc]);
+                }
+                const int cb = co0 + c0;
+                float v[32];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int co = co0 + c0 + j;
-                        if (co < p.CO) {
-                            const long long o = base + (long long)co * howo;
-                            const float v = __uint_as_float(r[j]);
-                            if (ws)
-                                ws[o] = v;
-                            else
-                                store_out(p.out, o,
-                                          epi_apply(p.epi, v, p.epi ? __ldg(p.bias + co) : 0.f,
-                                                    p.eps),
-                                          p.out_dt);
-                        }
+                for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                if (!p.ws && p.epi != BIGEMM_EPI_NONE) {
+                    float bv[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) bv[j] = cb + j < p.CO ? __ldg(p.bias + cb + j) : 0.f;
+                    if (p.epi == BIGEMM_EPI_BIAS) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] += bv[j];
+                    } else if (p.epi == BIGEMM_EPI_BIAS_EXP) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] = expf(v[j] + bv[j]);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] = rsqrtf(v[j] + bv[j] + p.eps);
+                    }
+                }
+                if (wbox) {
+                    uint8_t *buf = wstage + (chunk & 1) * 4096;
+                    if (lane == 0) bulk_wait_read<1>();   // the store that used buf has read it
+                    __syncwarp();
+                    uint8_t *dst = buf + lane * ec;
+                    if (ec == 4) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) *reinterpret_cast<float *>(dst + j * 128) = v[j];
+                    } else if (p.out_dt == BIGEMM_F16) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            *reinterpret_cast<__half *>(dst + j * 64) = __float2half_rn(v[j]);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            *reinterpret_cast<__nv_bfloat16 *>(dst + j * 64) = __float2bfloat16_rn(v[j]);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (AMODE == A_NHWC)
+                            tma_store_4d(&map_c, buf, sx, sy, cb, sn);
+                        else
+                            tma_store_3d(&map_c, buf, sx, cb, sn);
+                        bulk_commit();
+                    }
+                } else if (!p.store_tma && valid) {
+                    const long long o0 = base + (long long)cb * howo;
+                    const int jn = min(32, p.CO - cb);
+                    if (p.ws) {
+                        float *o = p.ws + o0;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (j < jn) o[j * howo] = v[j];
+                    } else if (p.out_dt == BIGEMM_F32) {
+                        float *o = static_cast<float *>(p.out) + o0;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (j < jn) o[j * howo] = v[j];
+                    } else if (p.out_dt == BIGEMM_F16) {
+                        __half *o = static_cast<__half *>(p.out) + o0;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (j < jn) o[j * howo] = __float2half_rn(v[j]);
+                    } else {
+                        __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.out) + o0;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (j < jn) o[j * howo] = __float2bfloat16_rn(v[j]);
                     }
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[acc]);
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
         }
+        if (lane == 0) bulk_wait<0>();              // stores complete before the block exits
     }
 
     tc_fence_before();
@@ -328,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int BN, int AMODE, int FMT>
 cudaError_t launch_one(const UmmaParams &p, const CUtensorMap &ma, const CUtensorMap &mb,
-                       int grid, cudaStream_t stream)
+                       const CUtensorMap &mc, int grid, cudaStream_t stream)
 {
     auto kern = umma_conv_kernel<BN, AMODE, FMT>;
     static unsigned long long attr_set = 0;   // bit per device: smem opt-in done
@@ -340,30 +428,30 @@ cudaError_t launch_one(const UmmaParams &p, const CUtensorMap &ma, const CUtenso
         if (e != cudaSuccess) return e;
         if (dev < 64) attr_set |= 1ull << dev;
     }
-    kern<<<grid, kThreads, Cfg<BN>::smem, stream>>>(ma, mb, p);
+    kern<<<grid, kThreads, Cfg<BN>::smem, stream>>>(ma, mb, mc, p);
     return cudaGetLastError();
 }
 
 template <int AMODE, int FMT>
 cudaError_t dispatch_bn(int bn, const UmmaParams &p, const CUtensorMap &ma,
-                        const CUtensorMap &mb, int grid, cudaStream_t s)
+                        const CUtensorMap &mb, const CUtensorMap &mc, int grid, cudaStream_t s)
 {
     switch (bn) {
-    case 64: return launch_one<64, AMODE, FMT>(p, ma, mb, grid, s);
-    case 128: return launch_one<128, AMODE, FMT>(p, ma, mb, grid, s);
-    case 256: return launch_one<256, AMODE, FMT>(p, ma, mb, grid, s);
+    case 64: return launch_one<64, AMODE, FMT>(p, ma, mb, mc, grid, s);
+    case 128: return launch_one<128, AMODE, FMT>(p, ma, mb, mc, grid, s);
+    case 256: return launch_one<256, AMODE, FMT>(p, ma, mb, mc, grid, s);
     default: return cudaErrorInvalidValue;
     }
 }
 
 template <int AMODE>
 cudaError_t dispatch_fmt(int fmt, int bn, const UmmaParams &p, const CUtensorMap &ma,
-                         const CUtensorMap &mb, int grid, cudaStream_t s)
+                         const CUtensorMap &mb, const CUtensorMap &mc, int grid, cudaStream_t s)
 {
     switch (fmt) {
-    case 0: return dispatch_bn<AMODE, 0>(bn, p, ma, mb, grid, s);
-    case 1: return dispatch_bn<AMODE, 1>(bn, p, ma, mb, grid, s);
-    case 2: return dispatch_bn<AMODE, 2>(bn, p, ma, mb, grid, s);
+    case 0: return dispatch_bn<AMODE, 0>(bn, p, ma, mb, mc, grid, s);
+    case 1: return dispatch_bn<AMODE, 1>(bn, p, ma, mb, mc, grid, s);
+    case 2: return dispatch_bn<AMODE, 2>(bn, p, ma, mb, mc, grid, s);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -389,13 +477,14 @@ bool umma_tiling_compiled(const UmmaTiling &t, int in_dt)
 }
 
 cudaError_t launch_umma_conv(const UmmaTiling &t, int in_dt, const UmmaParams &p,
-                             const CUtensorMap &map_a, const CUtensorMap &map_b, int grid,
-                             cudaStream_t stream)
+                             const CUtensorMap &map_a, const CUtensorMap &map_b,
+                             const CUtensorMap &map_c, int grid, cudaStream_t stream)
 {
     ProfScope prof(t.amode == A_NHWC ? "umma_conv_nhwc" : "umma_conv_direct", stream);
     const int fmt = fmt_of(in_dt);
-    if (t.amode == A_NHWC) return dispatch_fmt<A_NHWC>(fmt, t.bn, p, map_a, map_b, grid, stream);
-    return dispatch_fmt<A_DIRECT>(fmt, t.bn, p, map_a, map_b, grid, stream);
+    if (t.amode == A_NHWC)
+        return dispatch_fmt<A_NHWC>(fmt, t.bn, p, map_a, map_b, map_c, grid, stream);
+    return dispatch_fmt<A_DIRECT>(fmt, t.bn, p, map_a, map_b, map_c, grid, stream);
 }
 
 }  // namespace bigemm
