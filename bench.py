@@ -231,6 +231,11 @@ class BcastStep:
         self.bg.bcast_nchw_run(N, C, H, W, self.bg.BC_EXP, self.var, 1e-5, self.out, self.bg.F32,
                                stream)
 
+    def run_op(self, stream, op, flat):
+        N, C, H, W = self.shape
+        fn = self.bg.bcast_nchw_run_flat if flat else self.bg.bcast_nchw_run
+        fn(N, C, H, W, op, self.var, 1e-5, self.out, self.bg.F32, stream)
+
     def run_e2e(self, stream):
         self.var.copy_(self.var_h, non_blocking=True)
         self.run(stream)
@@ -287,6 +292,8 @@ def kernel_work(name, it):
         return (conv_flops(s), conv_bytes(s)) if name == "umma_conv_" + info.get("amode", "") else None
     if name.startswith("simt_conv"):
         return (conv_flops(s), conv_bytes(s)) if info["kind"] == "simt" else None
+    if name == "pack_operands" and info.get("amode") == "nhwc":
+        return (0.0, 2.0 * (s.N * s.CI * s.H * s.W + s.CO * s.CI * s.K * s.K) * e_in)
     if name == "pack_nhwc" and info.get("amode") == "nhwc":
         return (0.0, 2.0 * s.N * s.CI * s.H * s.W * e_in)
     if name == "pack_weights" and info.get("amode") == "nhwc":
@@ -505,6 +512,21 @@ def main():
                           "l2": "output (134 MB) larger than L2; 512 MB flush between steps"}
         n, tms = prof.get("bcast_nchw", (args.steps, total_ms))
         ach = step.work() / (tms / n / 1e3) / 1e9
+        # A/B: the per-channel mapping against the flat fused-index schedule, per op
+        ab = {}
+        for opname, op in (("exp", bg.BC_EXP), ("rsqrt", bg.BC_RSQRT), ("recip", bg.BC_RECIP),
+                           ("copy", bg.BC_COPY)):
+            res = {}
+            for flat in (False, True):
+                fn = (lambda st, o=op, f=flat: step.run_op(st, o, f))
+                for _ in range(3):
+                    with torch.cuda.stream(stream):
+                        fn(stream)
+                tt, _ = timed_steps(fn, max(5, min(args.steps, 20)), torch, stream, flush)
+                res["flat" if flat else "per_channel"] = step.work() / (sum(tt) / len(tt) / 1e3) / 1e9
+            ab[opname] = {"per_channel_gbs": res["per_channel"], "flat_gbs": res["flat"],
+                          "speedup": res["per_channel"] / res["flat"]}
+        line["bcast_ab"] = ab
         line["roofline"] = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm"], "unit": "GB/s",
                             "frac": ach / peaks["hbm"], "kernel": "bcast_nchw", "launches": n,
                             "avg_launch_us": tms / n * 1e3,

@@ -78,6 +78,11 @@ bool umma_tiling_compiled(const UmmaTiling &t, int in_dt);
 // -------------------------------------------------------------- other kernels
 cudaError_t launch_pack_nhwc(const void *x, void *xh, int N, int C, int HW, int Ch, int dt,
                              cudaStream_t stream);
+// Both packs in one launch when the data transpose can use 16-byte vectors
+// (else the two kernels above, back to back).
+cudaError_t launch_pack_operands(const void *x, void *xh, int N, int C, int HW, int Ch,
+                                 const void *w, void *wp, int CO, int CI, int KHKW, int cip,
+                                 int dt, cudaStream_t stream);
 cudaError_t launch_pack_weights(const void *w, void *wp, int CO, int CI, int KHKW, int cip,
                                 int dt, cudaStream_t stream);
 cudaError_t launch_splitk_reduce(const float *ws, int split, long long elems, int CO, int HoWo,

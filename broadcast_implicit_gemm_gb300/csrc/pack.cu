@@ -10,6 +10,9 @@
 //                whole 128-byte K blocks.
 //  splitk_reduce out = op(sum_s ws[s] + bias[f]) with the K slices added in
 //                index order (deterministic), then rounded to the output type.
+#include <algorithm>
+#include <climits>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -84,6 +87,68 @@ __global__ void __launch_bounds__(256) pack_nhwc_vec_kernel(const T *__restrict_
             for (int i = 0; i < VEC; ++i) val.e[i] = tile[cv * VEC + i][pr];
             *reinterpret_cast<uint4 *>(xd + (size_t)pix * Ch + c) = val.u;
         }
+    }
+}
+
+// Both operands in one launch: blocks [0, data_blocks) transpose data tiles
+// (as pack_nhwc_vec_kernel, tile index flattened as (pixel tile, channel tile,
+// image)); the remaining blocks re-lay out the kernel.
+template <typename T>
+__global__ void __launch_bounds__(256) pack_operands_kernel(const T *__restrict__ x,
+                                                            T *__restrict__ xh, int C, int HW,
+                                                            int Ch, int ptiles, int ctiles,
+                                                            int data_blocks,
+                                                            const T *__restrict__ w,
+                                                            T *__restrict__ wp, int CO, int CI,
+                                                            int KHKW, int cip)
+{
+    constexpr int VEC = 16 / sizeof(T);
+    constexpr int TILE = 8 * VEC;
+    __shared__ T tile[TILE][TILE + 1];
+    if ((int)blockIdx.x < data_blocks) {
+        const int t = blockIdx.x;
+        const int pt = t % ptiles, r = t / ptiles;
+        const int ct = r % ctiles, n = r / ctiles;
+        const int p0 = pt * TILE, c0 = ct * TILE;
+        const T *xs = x + (size_t)n * C * HW;
+        T *xd = xh + (size_t)n * HW * Ch;
+        for (int v = threadIdx.x; v < TILE * 8; v += blockDim.x) {
+            const int cr = v >> 3, pv = v & 7;
+            const int c = c0 + cr, pix = p0 + pv * VEC;
+            union {
+                uint4 u;
+                T e[VEC];
+            } val;
+            val.u = make_uint4(0, 0, 0, 0);
+            if (c < C && pix < HW) val.u = *reinterpret_cast<const uint4 *>(xs + (size_t)c * HW + pix);
+#pragma unroll
+            for (int i = 0; i < VEC; ++i) tile[cr][pv * VEC + i] = val.e[i];
+        }
+        __syncthreads();
+        for (int v = threadIdx.x; v < TILE * 8; v += blockDim.x) {
+            const int pr = v >> 3, cv = v & 7;
+            const int pix = p0 + pr, c = c0 + cv * VEC;
+            if (pix < HW && c < Ch) {
+                union {
+                    uint4 u;
+                    T e[VEC];
+                } val;
+#pragma unroll
+                for (int i = 0; i < VEC; ++i) val.e[i] = tile[cv * VEC + i][pr];
+                *reinterpret_cast<uint4 *>(xd + (size_t)pix * Ch + c) = val.u;
+            }
+        }
+        return;
+    }
+    const long long total = (long long)CO * KHKW * cip;
+    const long long nthreads = (long long)(gridDim.x - data_blocks) * blockDim.x;
+    for (long long i = (long long)(blockIdx.x - data_blocks) * blockDim.x + threadIdx.x; i < total;
+         i += nthreads) {
+        const int c = (int)(i % cip);
+        const long long r = i / cip;
+        const int t = (int)(r % KHKW);
+        const int f = (int)(r / KHKW);
+        wp[i] = c < CI ? w[((size_t)f * CI + c) * KHKW + t] : T(0);
     }
 }
 
@@ -173,6 +238,37 @@ cudaError_t launch_pack_nhwc(const void *x, void *xh, int N, int C, int HW, int 
     else
         pack_nhwc_kernel<uint16_t><<<grid, block, 0, stream>>>(
             static_cast<const uint16_t *>(x), static_cast<uint16_t *>(xh), C, HW, Ch);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pack_operands(const void *x, void *xh, int N, int C, int HW, int Ch,
+                                 const void *w, void *wp, int CO, int CI, int KHKW, int cip,
+                                 int dt, cudaStream_t stream)
+{
+    const int vec = (int)(16 / dtype_size(dt));
+    const bool aligned = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(xh)) & 15) == 0;
+    const int tile = 8 * vec;
+    const long long ptiles = (HW + tile - 1) / tile, ctiles = (Ch + tile - 1) / tile;
+    const long long data_blocks = ptiles * ctiles * N;
+    const long long wtotal = (long long)CO * KHKW * cip;
+    const long long wblocks = std::min<long long>((wtotal + 255) / 256, 1024);
+    if (!aligned || HW % vec || Ch % vec || data_blocks + wblocks > INT32_MAX) {
+        cudaError_t e = launch_pack_nhwc(x, xh, N, C, HW, Ch, dt, stream);
+        if (e != cudaSuccess) return e;
+        return launch_pack_weights(w, wp, CO, CI, KHKW, cip, dt, stream);
+    }
+    ProfScope prof("pack_operands", stream);
+    const int grid = (int)(data_blocks + wblocks);
+    if (dtype_size(dt) == 4)
+        pack_operands_kernel<uint32_t><<<grid, 256, 0, stream>>>(
+            static_cast<const uint32_t *>(x), static_cast<uint32_t *>(xh), C, HW, Ch, (int)ptiles,
+            (int)ctiles, (int)data_blocks, static_cast<const uint32_t *>(w),
+            static_cast<uint32_t *>(wp), CO, CI, KHKW, cip);
+    else
+        pack_operands_kernel<uint16_t><<<grid, 256, 0, stream>>>(
+            static_cast<const uint16_t *>(x), static_cast<uint16_t *>(xh), C, HW, Ch, (int)ptiles,
+            (int)ctiles, (int)data_blocks, static_cast<const uint16_t *>(w),
+            static_cast<uint16_t *>(wp), CO, CI, KHKW, cip);
     return cudaGetLastError();
 }
 

@@ -534,7 +534,7 @@ int launches_per_run(const bigemm_plan_s *p)
 {
     if (p->c.kind != BIGEMM_KIND_UMMA) return 1;
     int n = 1;
-    if (p->c.t.amode == A_NHWC) n += 2;
+    if (p->c.t.amode == A_NHWC) n += 1;
     if (p->g.p.split > 1) n += 1;
     return n;
 }
@@ -564,9 +564,8 @@ bigemm_status run_plan(bigemm_plan_s *p, const void *data, const void *kernel, c
     up.err = ds->err;
     up.timeout_ns = wait_timeout_ns();
     if (p->c.t.amode == A_NHWC) {
-        e = launch_pack_nhwc(data, p->xh, s.N, s.CI, s.H * s.W, p->g.ch, s.in_dt, st);
-        if (e != cudaSuccess) return BIGEMM_ERR_CUDA;
-        e = launch_pack_weights(kernel, p->wp, s.CO, s.CI, s.KH * s.KW, p->g.cip, s.in_dt, st);
+        e = launch_pack_operands(data, p->xh, s.N, s.CI, s.H * s.W, p->g.ch, kernel, p->wp, s.CO,
+                                 s.CI, s.KH * s.KW, p->g.cip, s.in_dt, st);
         if (e != cudaSuccess) return BIGEMM_ERR_CUDA;
     } else {
         bigemm_status r = encode_direct_maps(p, data, kernel);

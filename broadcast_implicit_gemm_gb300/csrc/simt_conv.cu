@@ -13,6 +13,8 @@
 //    thread slides along x producing neighbouring outputs.
 //  * conv_naive (any groups): one thread per output; the fallback for grouped
 //    shapes neither kernel above covers.
+#include <algorithm>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -163,9 +165,10 @@ __global__ void conv_naive_kernel(SimtArgs a, const void *__restrict__ x,
 }
 
 constexpr int kDwMaxTaps = 49;   // up to 7x7 kernels
-constexpr int kDwPX = 4;         // neighbouring outputs per thread along x
+constexpr int kDwPX = 8;         // neighbouring outputs per thread along x
 
-// Row pitch of the staged band: room for every window of the last x group.
+// Row pitch of a staged plane band: the left padding, the row, and room for
+// every window of the last x group (zeros beyond the row).
 __host__ __device__ inline int dw_pitch(int W, int pad, int Wo, int KW, int S)
 {
     const int gx = (Wo + kDwPX - 1) / kDwPX;
@@ -174,82 +177,148 @@ __host__ __device__ inline int dw_pitch(int W, int pad, int Wo, int KW, int S)
     return need > wp ? need : wp;
 }
 
-// grid: (row bands, C, N); dynamic smem: rows_in x pitch floats.  K and S are
-// compile-time (0 = read from the arguments).
+__device__ __forceinline__ void dw_store8(void *out, size_t o, const float (&v)[kDwPX], int n, int dt,
+                                          bool vec)
+{
+    if (vec && dt != BIGEMM_F32) {
+        union {
+            uint4 u;
+            __half h[8];
+            __nv_bfloat16 b[8];
+        } pk;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (dt == BIGEMM_F16)
+                pk.h[i] = __float2half_rn(v[i]);
+            else
+                pk.b[i] = __float2bfloat16_rn(v[i]);
+        }
+        *reinterpret_cast<uint4 *>(static_cast<char *>(out) + o * 2) = pk.u;
+        return;
+    }
+#pragma unroll
+    for (int i = 0; i < kDwPX; ++i)
+        if (i < n) st_out(out, o + i, v[i], dt);
+}
+
+// grid: (plane groups, row bands).  A block owns `ppb` consecutive (image,
+// channel) planes and output rows [y0, y0 + rows).  K and S are compile-time
+// (0: read from the arguments).
 template <int K, int S>
-__global__ void __launch_bounds__(256) conv_depthwise_kernel(SimtArgs a, int rows_per_block,
+__global__ void __launch_bounds__(256) conv_depthwise_kernel(SimtArgs a, int rows, int ppb,
                                                              const void *__restrict__ x,
                                                              const void *__restrict__ w,
                                                              const float *__restrict__ bias,
                                                              void *__restrict__ out)
 {
-    extern __shared__ float srow[];
-    __shared__ float tap_s[kDwMaxTaps];
+    extern __shared__ float sm[];
     const int KH = K ? K : a.KH, KW = K ? K : a.KW, st = S ? S : a.stride;
-    const int c = blockIdx.y, n = blockIdx.z;
-    const int y0 = blockIdx.x * rows_per_block;
-    const int y1 = min(a.Ho, y0 + rows_per_block);
+    const int nplanes = a.N * a.CI;
+    const int pl0 = blockIdx.x * ppb;
+    const int np = min(ppb, nplanes - pl0);
+    const int y0 = blockIdx.y * rows;
+    const int y1 = min(a.Ho, y0 + rows);
     const int iy0 = y0 * st - a.pad;
     const int rows_in = (y1 - 1 - y0) * st + KH;
     const int pitch = dw_pitch(a.W, a.pad, a.Wo, KW, st);
-    const size_t plane = ((size_t)n * a.CI + c) * a.H * a.W;
-    // stage rows [iy0, iy0 + rows_in) with zero borders (and zero tail columns)
-    for (int e = threadIdx.x; e < rows_in * pitch; e += blockDim.x) {
-        const int r = e / pitch, cc = e - r * pitch;
-        const int iy = iy0 + r, ix = cc - a.pad;
-        float v = 0.f;
-        if (iy >= 0 && iy < a.H && ix >= 0 && ix < a.W)
-            v = ld_in(x, plane + (size_t)iy * a.W + ix, a.in_dt);
-        srow[e] = v;
+    const int band = rows_in * pitch;
+    float *taps = sm + ppb * band;
+    // stage: zero everything, then the in-image part of each row
+    for (int e = threadIdx.x; e < np * band; e += blockDim.x) sm[e] = 0.f;
+    for (int e = threadIdx.x; e < np * KH * KW; e += blockDim.x) {
+        const int j = e / (KH * KW), t = e - j * KH * KW;
+        const int c = (pl0 + j) % a.CI;
+        taps[e] = ld_in(w, (size_t)c * KH * KW + t, a.in_dt);
     }
-    if (threadIdx.x < KH * KW) tap_s[threadIdx.x] = ld_in(w, (size_t)c * KH * KW + threadIdx.x, a.in_dt);
     __syncthreads();
-    const size_t obase = ((size_t)n * a.CO + c) * a.Ho * a.Wo;
+    const bool vec_in = a.in_dt != BIGEMM_F32 && (a.W & 7) == 0 &&
+                        ((reinterpret_cast<uintptr_t>(x) & 15) == 0);
+    if (vec_in) {
+        const int vpr = a.W >> 3;                   // 16-byte vectors per row
+        const int total = np * rows_in * vpr;
+        for (int e = threadIdx.x; e < total; e += blockDim.x) {
+            const int j = e / (rows_in * vpr);
+            const int rem = e - j * rows_in * vpr;
+            const int r = rem / vpr, v = rem - r * vpr;
+            const int iy = iy0 + r;
+            if (iy < 0 || iy >= a.H) continue;
+            const size_t src = ((size_t)(pl0 + j) * a.H + iy) * a.W + (size_t)v * 8;
+            union {
+                uint4 u;
+                __half h[8];
+                __nv_bfloat16 b[8];
+            } pk;
+            pk.u = __ldg(reinterpret_cast<const uint4 *>(static_cast<const char *>(x) + src * 2));
+            float *dst = sm + j * band + r * pitch + a.pad + v * 8;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                dst[i] = a.in_dt == BIGEMM_F16 ? __half2float(pk.h[i]) : __bfloat162float(pk.b[i]);
+        }
+    } else {
+        const int total = np * rows_in * a.W;
+        for (int e = threadIdx.x; e < total; e += blockDim.x) {
+            const int j = e / (rows_in * a.W);
+            const int rem = e - j * rows_in * a.W;
+            const int r = rem / a.W, ix = rem - r * a.W;
+            const int iy = iy0 + r;
+            if (iy < 0 || iy >= a.H) continue;
+            sm[j * band + r * pitch + a.pad + ix] =
+                ld_in(x, ((size_t)(pl0 + j) * a.H + iy) * a.W + ix, a.in_dt);
+        }
+    }
+    __syncthreads();
     const int gx = (a.Wo + kDwPX - 1) / kDwPX;
-    const int cnt = (y1 - y0) * gx;
-    const float bv = a.epi != BIGEMM_EPI_NONE ? bias[c] : 0.f;
-    for (int e = threadIdx.x; e < cnt; e += blockDim.x) {
-        const int yy = e / gx, xg = e - yy * gx;
+    const int per_plane = (y1 - y0) * gx;
+    const bool vec_out = a.out_dt != BIGEMM_F32 && (a.Wo & 7) == 0 &&
+                         ((reinterpret_cast<uintptr_t>(out) & 15) == 0);
+    for (int e = threadIdx.x; e < np * per_plane; e += blockDim.x) {
+        const int j = e / per_plane;
+        const int rem = e - j * per_plane;
+        const int yy = rem / gx, xg = rem - yy * gx;
         const int xo0 = xg * kDwPX;
+        const float *tp = taps + j * KH * KW;
+        const float *bandp = sm + j * band;
         float acc[kDwPX];
 #pragma unroll
         for (int i = 0; i < kDwPX; ++i) acc[i] = 0.f;
         if (K) {
-            constexpr int WIN = (kDwPX - 1) * (S ? S : 1) + (K ? K : 1);
+            constexpr int KK = K ? K : 1, SS = S ? S : 1;
+            constexpr int WIN = (kDwPX - 1) * SS + KK;
 #pragma unroll
-            for (int ry = 0; ry < (K ? K : 1); ++ry) {
-                const float *rp = srow + (yy * st + ry) * pitch + xo0 * st;
+            for (int ry = 0; ry < KK; ++ry) {
+                const float *rp = bandp + (yy * SS + ry) * pitch + xo0 * SS;
                 float win[WIN];
 #pragma unroll
                 for (int i = 0; i < WIN; ++i) win[i] = rp[i];
 #pragma unroll
-                for (int i = 0; i < kDwPX; ++i)
+                for (int rx = 0; rx < KK; ++rx) {
+                    const float t = tp[ry * KK + rx];
 #pragma unroll
-                    for (int rx = 0; rx < (K ? K : 1); ++rx)
-                        acc[i] = fmaf(win[i * (S ? S : 1) + rx], tap_s[ry * (K ? K : 1) + rx], acc[i]);
+                    for (int i = 0; i < kDwPX; ++i) acc[i] = fmaf(win[i * SS + rx], t, acc[i]);
+                }
             }
         } else {
             for (int ry = 0; ry < KH; ++ry) {
-                const float *rp = srow + (yy * st + ry) * pitch + xo0 * st;
+                const float *rp = bandp + (yy * st + ry) * pitch + xo0 * st;
                 for (int rx = 0; rx < KW; ++rx) {
-                    const float t = tap_s[ry * KW + rx];
+                    const float t = tp[ry * KW + rx];
 #pragma unroll
                     for (int i = 0; i < kDwPX; ++i) acc[i] = fmaf(rp[i * st + rx], t, acc[i]);
                 }
             }
         }
-        const size_t orow = obase + (size_t)(y0 + yy) * a.Wo;
+        const int c = (pl0 + j) % a.CI;
+        if (a.epi != BIGEMM_EPI_NONE) {
+            const float bv = bias[c];
 #pragma unroll
-        for (int i = 0; i < kDwPX; ++i) {
-            const int xo = xo0 + i;
-            if (xo < a.Wo) {
-                float v = acc[i];
-                if (a.epi == BIGEMM_EPI_BIAS) v += bv;
-                else if (a.epi == BIGEMM_EPI_BIAS_EXP) v = expf(v + bv);
-                else if (a.epi == BIGEMM_EPI_BIAS_RSQRT) v = rsqrtf(v + bv + a.eps);
-                st_out(out, orow + xo, v, a.out_dt);
+            for (int i = 0; i < kDwPX; ++i) {
+                if (a.epi == BIGEMM_EPI_BIAS) acc[i] += bv;
+                else if (a.epi == BIGEMM_EPI_BIAS_EXP) acc[i] = expf(acc[i] + bv);
+                else acc[i] = rsqrtf(acc[i] + bv + a.eps);
             }
         }
+        const size_t o = ((size_t)(pl0 + j) * a.Ho + (y0 + yy)) * a.Wo + xo0;
+        dw_store8(out, o, acc, min(kDwPX, a.Wo - xo0), a.out_dt, vec_out);
     }
 }
 
@@ -286,10 +355,22 @@ cudaError_t launch_simt_conv(const ConvShape &s, const void *x, const void *w,
     return cudaGetLastError();
 }
 
+// Planes per block: enough (image, channel) planes that each block has work
+// for about 256 threads when a plane is small.
+int dw_planes_per_block(const ConvShape &s, int rows)
+{
+    const int gx = (s.Wo + kDwPX - 1) / kDwPX;
+    const int items = std::min(rows, s.Ho) * gx;
+    if (items >= 128) return 1;
+    return std::max(1, std::min(16, 256 / std::max(1, items)));
+}
+
 size_t dw_smem_bytes(const ConvShape &s, int rows)
 {
-    return (size_t)((rows - 1) * s.stride + s.KH) * dw_pitch(s.W, s.pad, s.Wo, s.KW, s.stride) *
-           sizeof(float);
+    const int r = std::min(rows, s.Ho);
+    const int ppb = dw_planes_per_block(s, rows);
+    const size_t band = (size_t)((r - 1) * s.stride + s.KH) * dw_pitch(s.W, s.pad, s.Wo, s.KW, s.stride);
+    return (ppb * band + (size_t)ppb * s.KH * s.KW) * sizeof(float);
 }
 
 cudaError_t launch_dw_conv(const ConvShape &s, const void *x, const void *w, const float *bias,
@@ -298,15 +379,18 @@ cudaError_t launch_dw_conv(const ConvShape &s, const void *x, const void *w, con
     ProfScope prof("simt_conv_depthwise", stream);
     if (s.KH * s.KW > kDwMaxTaps) return cudaErrorInvalidValue;
     const SimtArgs a = make_args(s, eps);
-    const size_t smem = dw_smem_bytes(s, rows_per_block);
-    dim3 grid((s.Ho + rows_per_block - 1) / rows_per_block, s.CO, s.N);
+    const int rows = std::min(rows_per_block, s.Ho);
+    const int ppb = dw_planes_per_block(s, rows);
+    const size_t smem = dw_smem_bytes(s, rows);
+    const long long planes = (long long)s.N * s.CI;
+    dim3 grid((unsigned)((planes + ppb - 1) / ppb), (unsigned)((s.Ho + rows - 1) / rows));
     auto go = [&](auto kern) {
         if (smem > 48 * 1024) {
             cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  (int)smem);
             if (e != cudaSuccess) return e;
         }
-        kern<<<grid, 256, smem, stream>>>(a, rows_per_block, x, w, bias, out);
+        kern<<<grid, 256, smem, stream>>>(a, rows, ppb, x, w, bias, out);
         return cudaGetLastError();
     };
     const bool sq = s.KH == s.KW;

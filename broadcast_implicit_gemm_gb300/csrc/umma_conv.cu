@@ -66,7 +66,7 @@ __device__ __forceinline__ Unit decode(const UmmaParams &p, int u)
     return w;
 }
 
-constexpr int kMaxBoxes = 16;   // boxes per tile: 128 rows / at least 8 pixels per box
+constexpr int kMaxBoxes = 16;   // boxes per tile: 128 rows / at least 8 pixels per box (< 32 lanes)
 
 template <int BN, int AMODE, int FMT>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -121,67 +121,61 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
-        if (lane == 0) {
+        // The warp walks the loop together: lane 0 waits for a free slot and
+        // arms its barrier, then lanes 0..nbox-1 each issue one A box and lane
+        // nbox the B tile, so the copies of a K block leave in one instruction.
+        {
             int stage = 0;
             uint32_t phase = 0;
+            bool ok = true;
             uint32_t last_parity[S];
             bool issued[S];
             for (int i = 0; i < S; ++i) issued[i] = false, last_parity[i] = 0;
-            bool ok = true;
             for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
                 const Unit w = decode(p, u);
                 const int box0 = w.pt * p.bpt;
                 const int nbox = min(p.bpt, p.total_boxes - box0);
                 const uint32_t tx = (uint32_t)nbox * box_bytes + (uint32_t)C::b_bytes;
-                // per-box origin of this tile, computed once
-                int bx[kMaxBoxes], by[kMaxBoxes], bn[kMaxBoxes];
-#pragma unroll
-                for (int i = 0; i < kMaxBoxes; ++i) {
-                    bx[i] = by[i] = bn[i] = 0;
-                    if (i < nbox) {
-                        const int bb = box0 + i;
-                        const int n = bb / p.boxes_per_img;
-                        const int rem = bb - n * p.boxes_per_img;
-                        bn[i] = n;
-                        if (AMODE == A_NHWC) {
-                            const int byi = rem / p.boxes_x, bxi = rem - byi * p.boxes_x;
-                            bx[i] = bxi * p.box_w * p.stride - p.pad;
-                            by[i] = byi * p.box_h * p.stride - p.pad;
-                        } else {
-                            bx[i] = rem * p.box_w;
-                        }
+                int mbx = 0, mby = 0, mbn = 0;
+                if (lane < nbox) {
+                    const int bb = box0 + lane;
+                    const int n = bb / p.boxes_per_img;
+                    const int rem = bb - n * p.boxes_per_img;
+                    mbn = n;
+                    if (AMODE == A_NHWC) {
+                        const int byi = rem / p.boxes_x, bxi = rem - byi * p.boxes_x;
+                        mbx = bxi * p.box_w * p.stride - p.pad;
+                        mby = byi * p.box_h * p.stride - p.pad;
+                    } else {
+                        mbx = rem * p.box_w;
                     }
                 }
-                // walk K as (ry, rx, channel block) with counters
                 int tap = w.kb0 / p.ci_blocks;
                 int cb = w.kb0 - tap * p.ci_blocks;
                 int ry = tap / p.KW, rx = tap - ry * p.KW;
                 const int ncol = w.ct * BN;
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag, p.err)) {
-                        ok = false;
-                        break;
+                    int okw = 1;
+                    if (lane == 0) {
+                        okw = mbar_wait(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag, p.err);
+                        if (okw) mbar_arrive_expect_tx(&full[stage], tx);
                     }
-                    mbar_arrive_expect_tx(&full[stage], tx);
+                    if (!__shfl_sync(0xffffffffu, okw, 0)) { ok = false; break; }
                     issued[stage] = true;
                     last_parity[stage] = phase;
                     uint8_t *a_dst = sa + stage * kABytes;
                     uint8_t *b_dst = sb + stage * C::b_bytes;
-                    if (AMODE == A_NHWC) {
-#pragma unroll
-                        for (int i = 0; i < kMaxBoxes; ++i)
-                            if (i < nbox)
-                                tma_load_4d(a_dst + i * box_bytes, &map_a, &full[stage], cb * p.bk,
-                                            bx[i] + rx, by[i] + ry, bn[i]);
-                        tma_load_2d(b_dst, &map_b, &full[stage],
-                                    (ry * p.KW + rx) * p.cip + cb * p.bk, ncol);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < kMaxBoxes; ++i)
-                            if (i < nbox)
-                                tma_load_3d(a_dst + i * box_bytes, &map_a, &full[stage], bx[i],
-                                            kb * p.bk, bn[i]);
-                        tma_load_2d(b_dst, &map_b, &full[stage], kb * p.bk, ncol);
+                    if (lane < nbox) {
+                        if (AMODE == A_NHWC)
+                            tma_load_4d(a_dst + lane * box_bytes, &map_a, &full[stage], cb * p.bk,
+                                        mbx + rx, mby + ry, mbn);
+                        else
+                            tma_load_3d(a_dst + lane * box_bytes, &map_a, &full[stage], mbx, kb * p.bk, mbn);
+                    } else if (lane == nbox) {
+                        if (AMODE == A_NHWC)
+                            tma_load_2d(b_dst, &map_b, &full[stage], (ry * p.KW + rx) * p.cip + cb * p.bk, ncol);
+                        else
+                            tma_load_2d(b_dst, &map_b, &full[stage], kb * p.bk, ncol);
                     }
                     if (++stage == S) stage = 0, phase ^= 1u;
                     if (++cb == p.ci_blocks) {
@@ -190,13 +184,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            if (!ok) {
-                // Let every copy already issued land before the block exits.
+            if (!ok && lane == 0) {
                 int local_abort = 0;
                 for (int i = 0; i < S; ++i)
-                    if (issued[i])
-                        mbar_wait(&full[i], last_parity[i], p.timeout_ns, &local_abort, p.err);
+                    if (issued[i]) mbar_wait(&full[i], last_parity[i], p.timeout_ns, &local_abort, p.err);
             }
+            __syncwarp();
         }
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
@@ -283,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const int b = w.pt * p.bpt + bi;
             bool valid = bi < p.bpt && b < p.total_boxes;
-            long long base = 0;
+            long long base = 0, base_out = 0;
             if (valid) {
                 const int n = b / p.boxes_per_img;
                 const int rem = b - n * p.boxes_per_img;
@@ -298,7 +291,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     pix = (long long)rem * p.box_w + bj;
                     valid = pix < howo;
                 }
-                base = ((long long)w.sp * p.N + n) * p.CO * howo + pix;
+                base_out = (long long)n * p.CO * howo + pix;
+                base = (long long)w.sp * p.out_elems + base_out;
             }
             // the warp's store box (TMA mode): origin and image index
             const int wb = w.pt * p.bpt + wbi;
