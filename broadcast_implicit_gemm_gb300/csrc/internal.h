@@ -32,6 +32,7 @@ struct ConvShape {
 enum AMode {
     A_NHWC = 0,     // packed channels-last copy of data, K-major, 4-D box per tap
     A_DIRECT = 1,   // 1x1 / stride 1 / pad 0: data read in place as [CI][H*W], MN-major
+    A_HALO = 2,     // stride 1, K x K: one halo box per channel block serves every tap
 };
 
 struct UmmaTiling {

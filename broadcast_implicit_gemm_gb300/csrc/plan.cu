@@ -45,7 +45,8 @@ std::string cand_str(const Cand &c)
     char b[160];
     if (c.kind == BIGEMM_KIND_UMMA)
         snprintf(b, sizeof b, "umma:%s:bn%d:box%dx%dx%d:split%d",
-                 c.t.amode == A_DIRECT ? "direct" : "nhwc", c.t.bn, c.t.box_w, c.t.box_h, c.t.bpt,
+                 c.t.amode == A_DIRECT ? "direct" : c.t.amode == A_HALO ? "halo" : "nhwc", c.t.bn,
+                 c.t.box_w, c.t.box_h, c.t.bpt,
                  c.t.split);
     else if (c.simt_variant == SV_DW)
         snprintf(b, sizeof b, "simt:depthwise:rows%d", c.dw_rows);
@@ -61,7 +62,9 @@ bool parse_cand(const std::string &s, Cand &c)
     if (sscanf(s.c_str(), "umma:%15[a-z]:bn%d:box%dx%dx%d:split%d", mode, &a, &b, &d, &e, &f) == 6) {
         c = Cand{};
         c.kind = BIGEMM_KIND_UMMA;
-        c.t.amode = strcmp(mode, "direct") == 0 ? A_DIRECT : A_NHWC;
+        c.t.amode = strcmp(mode, "direct") == 0 ? A_DIRECT
+                    : strcmp(mode, "halo") == 0   ? A_HALO
+                                                  : A_NHWC;
         c.t.bn = a, c.t.box_w = b, c.t.box_h = d, c.t.bpt = e, c.t.split = f;
         return true;
     }
@@ -141,11 +144,12 @@ UmmaGeom umma_geometry(const ConvShape &s, const UmmaTiling &t, int sm_count)
     p.ci_blocks = (int)ceil_div(s.CI, p.bk);
     p.box_w = t.box_w, p.box_h = t.box_h, p.bpt = t.bpt;
     long long bpi;
-    if (t.amode == A_NHWC) {
+    if (t.amode == A_NHWC || t.amode == A_HALO) {
         p.boxes_x = (int)ceil_div(s.Wo, t.box_w);
         p.boxes_y = (int)ceil_div(s.Ho, t.box_h);
         bpi = (long long)p.boxes_x * p.boxes_y;
-        p.k_blocks = s.KH * s.KW * p.ci_blocks;
+        // halo: one K block is a channel block with every tap inside it
+        p.k_blocks = (t.amode == A_HALO ? 1 : s.KH * s.KW) * p.ci_blocks;
         g.cip = p.ci_blocks * p.bk;
         g.ch = (int)ceil_div(s.CI, 16 / e) * (16 / e);
     } else {
@@ -195,6 +199,11 @@ bool umma_valid(const ConvShape &s, const UmmaTiling &t, int sm_count, std::stri
         if ((s.CI * e) % 16) return bad("CI row not 16-byte multiple");
         if (t.box_w != (int)(128 / e) || t.box_h != 1 || t.bpt * t.box_w != 128)
             return bad("direct box must be one 128-byte row of pixels");
+    } else if (t.amode == A_HALO) {
+        if (s.stride != 1) return bad("halo mode needs stride 1");
+        if (s.KH * s.KW < 2) return bad("halo mode is for kernels larger than 1x1");
+        if (s.KH > 7 || s.KW > 8) return bad("halo mode holds up to 7 rows x 8 columns of taps");
+        if (t.box_w != 8 || t.box_h != 16 || t.bpt != 1) return bad("halo tile is 8 x 16 pixels");
     } else {
         if (s.stride > 8) return bad("stride > 8");
         if (t.box_w < 1 || t.box_h < 1) return bad("empty box");
@@ -301,6 +310,8 @@ UmmaTiling default_tiling(const ConvShape &s, int amode, int bn, int sms)
         t.box_w = (int)(128 / dtype_size(s.in_dt));
         t.box_h = 1;
         t.bpt = 128 / t.box_w;
+    } else if (amode == A_HALO) {
+        t.box_w = 8, t.box_h = 16, t.bpt = 1;
     } else {
         const Box b = box_options(s).front();
         t.box_w = b.w, t.box_h = b.h, t.bpt = b.bpt;
@@ -315,6 +326,20 @@ int default_bn(const ConvShape &s)
     if (s.CO <= 64) return 64;
     if (s.CO <= 128) return 128;
     return (s.CO % 256 == 0) ? 256 : 128;
+}
+
+// Halo tiles cover 8 x 16 output pixels; worth it when they are mostly inside
+// the image.
+bool halo_ok(const ConvShape &s)
+{
+    UmmaTiling t{};
+    t.amode = A_HALO;
+    t.bn = 64;
+    t.box_w = 8, t.box_h = 16, t.bpt = 1;
+    t.split = 1;
+    if (!umma_valid(s, t, 1, nullptr)) return false;
+    const double cover = (double)ceil_div(s.Ho, 16) * 16 * ceil_div(s.Wo, 8) * 8;
+    return (double)s.Ho * s.Wo / cover >= 0.7;
 }
 
 bool direct_ok(const ConvShape &s)
@@ -343,7 +368,8 @@ Cand heuristic(const ConvShape &s, int sms)
     if (kdim >= 32) {
         Cand u;
         u.kind = BIGEMM_KIND_UMMA;
-        u.t = default_tiling(s, direct_ok(s) ? A_DIRECT : A_NHWC, default_bn(s), sms);
+        u.t = default_tiling(s, direct_ok(s) ? A_DIRECT : halo_ok(s) ? A_HALO : A_NHWC,
+                             default_bn(s), sms);
         if (umma_valid(s, u.t, sms, nullptr)) return u;
     }
     c.simt_variant = SV_TILED;
@@ -369,6 +395,7 @@ std::vector<Cand> candidates(const ConvShape &s, int sms)
     }
     std::vector<int> modes;
     if (direct_ok(s)) modes.push_back(A_DIRECT);
+    if (halo_ok(s)) modes.push_back(A_HALO);
     modes.push_back(A_NHWC);
     std::vector<Box> boxes = box_options(s);
     for (int amode : modes) {
@@ -378,6 +405,9 @@ std::vector<Cand> candidates(const ConvShape &s, int sms)
             const int w = (int)(128 / dtype_size(s.in_dt));
             bx.push_back({w, 1});
             bpts.push_back(128 / w);
+        } else if (amode == A_HALO) {
+            bx.push_back({8, 16});
+            bpts.push_back(1);
         } else {
             for (size_t i = 0; i < boxes.size() && bx.size() < 2; ++i) {
                 if (i > 0 && boxes[i].eff < boxes[0].eff - 0.05) break;
@@ -467,7 +497,34 @@ bigemm_status setup_plan(bigemm_plan_s *p)
     const UmmaTiling &t = p->c.t;
     p->g = umma_geometry(s, t, p->sm_count);
     const size_t e = dtype_size(s.in_dt);
-    if (t.amode == A_NHWC) {
+    if (t.amode == A_HALO) {
+        // channels-last data read as one halo box per channel block: 16 pixels
+        // wide (the 2 KB smem row pitch), 16 + KH - 1 rows high
+        p->xh_bytes = (size_t)s.N * s.H * s.W * p->g.ch * e;
+        p->wp_bytes = (size_t)s.CO * s.KH * s.KW * p->g.cip * e;
+        if (cudaMalloc(&p->xh, p->xh_bytes) != cudaSuccess) return BIGEMM_ERR_CUDA;
+        if (cudaMalloc(&p->wp, p->wp_bytes) != cudaSuccess) return BIGEMM_ERR_CUDA;
+        const uint64_t dims[4] = {(uint64_t)p->g.ch, (uint64_t)s.W, (uint64_t)s.H, (uint64_t)s.N};
+        const uint64_t str[3] = {p->g.ch * e, (uint64_t)s.W * p->g.ch * e,
+                                 (uint64_t)s.H * s.W * p->g.ch * e};
+        const uint32_t box[4] = {(uint32_t)p->g.p.bk, 16u, (uint32_t)(16 + s.KH - 1), 1u};
+        const uint32_t es[4] = {1u, 1u, 1u, 1u};
+        if (!encode_tiled(&p->map_a, tma_dt(s.in_dt), 4, p->xh, dims, str, box, es,
+                          CU_TENSOR_MAP_SWIZZLE_128B))
+            return BIGEMM_ERR_UNSUPPORTED;
+        // packed weights [CO][tap][cip] viewed as (channel, output channel, tap):
+        // one box brings TB taps, each a [BN][128 B] K-major tile
+        const int tb = 32768 / (t.bn * 128);
+        const uint64_t kk = (uint64_t)s.KH * s.KW;
+        const uint64_t bd[3] = {(uint64_t)p->g.cip, (uint64_t)s.CO, kk};
+        const uint64_t bs[2] = {kk * p->g.cip * e, (uint64_t)p->g.cip * e};
+        const uint32_t bb[3] = {(uint32_t)p->g.p.bk, (uint32_t)t.bn, (uint32_t)tb};
+        const uint32_t bes[3] = {1u, 1u, 1u};
+        if (!encode_tiled(&p->map_b, tma_dt(s.in_dt), 3, p->wp, bd, bs, bb, bes,
+                          CU_TENSOR_MAP_SWIZZLE_128B))
+            return BIGEMM_ERR_UNSUPPORTED;
+        p->maps_ready = true;
+    } else if (t.amode == A_NHWC) {
         p->xh_bytes = (size_t)s.N * s.H * s.W * p->g.ch * e;
         p->wp_bytes = (size_t)s.CO * s.KH * s.KW * p->g.cip * e;
         if (cudaMalloc(&p->xh, p->xh_bytes) != cudaSuccess) return BIGEMM_ERR_CUDA;
@@ -534,7 +591,7 @@ int launches_per_run(const bigemm_plan_s *p)
 {
     if (p->c.kind != BIGEMM_KIND_UMMA) return 1;
     int n = 1;
-    if (p->c.t.amode == A_NHWC) n += 1;
+    if (p->c.t.amode != A_DIRECT) n += 1;
     if (p->g.p.split > 1) n += 1;
     return n;
 }
@@ -563,7 +620,7 @@ bigemm_status run_plan(bigemm_plan_s *p, const void *data, const void *kernel, c
     up.ws = p->ws;
     up.err = ds->err;
     up.timeout_ns = wait_timeout_ns();
-    if (p->c.t.amode == A_NHWC) {
+    if (p->c.t.amode != A_DIRECT) {
         e = launch_pack_operands(data, p->xh, s.N, s.CI, s.H * s.W, p->g.ch, kernel, p->wp, s.CO,
                                  s.CI, s.KH * s.KW, p->g.cip, s.in_dt, st);
         if (e != cudaSuccess) return BIGEMM_ERR_CUDA;
@@ -798,12 +855,13 @@ bigemm_status plan_impl(int N, int H, int W, int CO, int CI, int KH, int KW, int
     cudaStream_t st = (cudaStream_t)stream;
 
     const bool forced = opts && (opts->kind || opts->tile_n || opts->split_k || opts->box_w ||
-                                 opts->box_h || opts->stages);
+                                 opts->box_h || opts->stages || opts->mode);
     Cand c;
     std::string log, chosen = "heuristic";
     if (forced) {
         if (opts->kind == BIGEMM_KIND_SIMT || (opts->kind == 0 && !opts->tile_n && !opts->split_k &&
-                                               !opts->box_w && !opts->box_h && !opts->stages)) {
+                                               !opts->box_w && !opts->box_h && !opts->stages &&
+                                               !opts->mode)) {
             c = heuristic(s, sms);
             if (c.kind == BIGEMM_KIND_UMMA) {
                 c = Cand{};
@@ -815,8 +873,12 @@ bigemm_status plan_impl(int N, int H, int W, int CO, int CI, int KH, int KW, int
             }
         } else {
             c.kind = BIGEMM_KIND_UMMA;
-            const int amode = (opts->box_w && opts->box_h) ? A_NHWC
+            const int amode = opts->mode == 1 ? A_NHWC
+                              : opts->mode == 2 ? A_DIRECT
+                              : opts->mode == 3 ? A_HALO
+                              : (opts->box_w && opts->box_h) ? A_NHWC
                               : direct_ok(s)                ? A_DIRECT
+                              : halo_ok(s)                  ? A_HALO
                                                             : A_NHWC;
             c.t = default_tiling(s, amode, opts->tile_n ? opts->tile_n : default_bn(s), sms);
             if (opts->box_w && opts->box_h) {
@@ -920,7 +982,9 @@ bigemm_status conv2d_nchw_plan_describe(bigemm_plan plan, char *buf, size_t len)
        << (c.kind == BIGEMM_KIND_UMMA ? "umma" : "simt") << "\"";
     if (c.kind == BIGEMM_KIND_UMMA) {
         const UmmaParams &p = plan->g.p;
-        os << ", \"amode\": \"" << (c.t.amode == A_DIRECT ? "direct" : "nhwc") << "\", \"bn\": " << c.t.bn
+        os << ", \"amode\": \""
+           << (c.t.amode == A_DIRECT ? "direct" : c.t.amode == A_HALO ? "halo" : "nhwc")
+           << "\", \"bn\": " << c.t.bn
            << ", \"box\": [" << c.t.box_w << ", " << c.t.box_h << ", " << c.t.bpt << "]"
            << ", \"split\": " << p.split << ", \"k_blocks\": " << p.k_blocks
            << ", \"pix_tiles\": " << p.pix_tiles << ", \"co_tiles\": " << p.co_tiles

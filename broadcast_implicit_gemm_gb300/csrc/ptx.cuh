@@ -270,15 +270,58 @@ __device__ __forceinline__ void tmem_wait_ld()
 // stride byte offsets (all >> 4), the fixed version bit at 46, base offset 0,
 // and the swizzle mode in bits 61..63 (0 none, 2 = 128-byte swizzle).
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo,
-                                              uint32_t swz)
+                                              uint32_t swz, uint32_t base_offset = 0)
 {
     uint64_t d = 0;
     d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
     d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
     d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
     d |= (uint64_t)1 << 46;
+    // matrix base offset (bits 49..51); the kernels keep it 0: starts that are
+    // not on a 1024-byte boundary still read the swizzle phase from their
+    // address bits
+    d |= (uint64_t)(base_offset & 7u) << 49;
     d |= (uint64_t)(swz & 7u) << 61;
     return d;
+}
+
+// The two 32-bit halves of a shared-memory descriptor, so that issue loops
+// can step the start address with one 32-bit add (start >> 4 sits in the low
+// 14 bits; shared memory offsets stay below 2^18, so the field never carries).
+__device__ __forceinline__ uint32_t desc_lo(uint32_t saddr, uint32_t lbo)
+{
+    return ((saddr >> 4) & 0x3FFFu) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+
+__device__ __forceinline__ uint32_t desc_hi(uint32_t sbo, uint32_t swz)
+{
+    return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | ((swz & 7u) << 29);
+}
+
+// tcgen05.mma with the descriptors given as (lo, hi) halves.
+template <bool TF32>
+__device__ __forceinline__ void umma_lohi(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
+                                          uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
+                                          uint32_t accum)
+{
+    if (TF32)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t.reg .b64 ad, bd;\n\t"
+            "mov.b64 ad, {%1, %2};\n\t"
+            "mov.b64 bd, {%3, %4};\n\t"
+            "setp.ne.b32 p, %6, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::tf32 [%0], ad, bd, %5, p;\n\t}" ::"r"(d_tmem),
+            "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accum)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t.reg .b64 ad, bd;\n\t"
+            "mov.b64 ad, {%1, %2};\n\t"
+            "mov.b64 bd, {%3, %4};\n\t"
+            "setp.ne.b32 p, %6, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %5, p;\n\t}" ::"r"(d_tmem),
+            "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accum)
+            : "memory");
 }
 
 // Instruction descriptor for kind::f16 / kind::tf32 with an fp32 accumulator:

@@ -68,6 +68,162 @@ __device__ __forceinline__ Unit decode(const UmmaParams &p, int u)
 
 constexpr int kMaxBoxes = 16;   // boxes per tile: 128 rows / at least 8 pixels per box (< 32 lanes)
 
+// Epilogue of one warp (warps 2..5 of the block).  BOXED: the tile's pixels
+// are 2-D boxes (box_w x box_h) of one image; otherwise runs of box_w
+// consecutive flattened pixels (the direct mode).
+template <int BN, bool BOXED>
+__device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtensorMap *map_c,
+                                              uint32_t tmem_base, uint64_t *tfull,
+                                              uint64_t *tempty, uint8_t *stage_out,
+                                              volatile int *abort_flag, int warp, int lane,
+                                              int box_px)
+{
+    // Each warp owns TMEM lanes 32q..32q+31 (32 pixels of the tile) and
+    // works alone: lane 0 waits for the accumulator and shares the outcome,
+    // so the warp stays converged.  With TMA stores the warp stages its
+    // 32 pixels x 32 channels in its own shared buffers and lane 0 writes
+    // them as one box.
+    const int q = warp & 3;                     // TMEM lane quadrant of this warp
+    const int row = q * 32 + lane;              // tile row = pixel
+    const int bi = row / box_px, bj = row - bi * box_px;
+    const int wbi = (q * 32) / box_px;          // the warp's box
+    const int wj0 = (q * 32) - wbi * box_px;    // its first pixel in the box
+    const long long howo = (long long)p.Ho * p.Wo;
+    const int ec = p.ws ? 4 : (p.out_dt == BIGEMM_F32 ? 4 : 2);
+    uint8_t *wstage = stage_out + q * 8192;     // 2 x 4 KB per warp
+    int acc = 0, chunk = 0;
+    uint32_t acc_phase = 0;
+    for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+        const Unit w = decode(p, u);
+        int okw = 0;
+        if (lane == 0) okw = mbar_wait(&tfull[acc], acc_phase, p.timeout_ns, abort_flag, p.err);
+        if (!__shfl_sync(0xffffffffu, okw, 0)) break;
+        tc_fence_after();
+        const int b = w.pt * p.bpt + bi;
+        bool valid = bi < p.bpt && b < p.total_boxes;
+        long long base = 0, base_out = 0;
+        if (valid) {
+            const int n = b / p.boxes_per_img;
+            const int rem = b - n * p.boxes_per_img;
+            long long pix;
+            if (BOXED) {
+                const int byi = rem / p.boxes_x, bxi = rem - byi * p.boxes_x;
+                const int y = byi * p.box_h + bj / p.box_w;
+                const int x = bxi * p.box_w + bj % p.box_w;
+                valid = y < p.Ho && x < p.Wo;
+                pix = (long long)y * p.Wo + x;
+            } else {
+                pix = (long long)rem * p.box_w + bj;
+                valid = pix < howo;
+            }
+            base_out = (long long)n * p.CO * howo + pix;
+            base = (long long)w.sp * p.out_elems + base_out;
+        }
+        // the warp's store box (TMA mode): origin and image index
+        const int wb = w.pt * p.bpt + wbi;
+        const bool wbox = p.store_tma && wbi < p.bpt && wb < p.total_boxes;
+        int sx = 0, sy = 0, sn = 0;
+        if (wbox) {
+            const int n = wb / p.boxes_per_img;
+            const int rem = wb - n * p.boxes_per_img;
+            sn = w.sp * p.N + n;
+            if (BOXED) {
+                const int byi = rem / p.boxes_x, bxi = rem - byi * p.boxes_x;
+                sx = bxi * p.box_w + wj0 % p.box_w;
+                sy = byi * p.box_h + wj0 / p.box_w;
+            } else {
+                sx = rem * p.box_w + wj0;
+            }
+        }
+        const int co0 = w.ct * BN;
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32, ++chunk) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + c0),
+                               r);
+            tmem_wait_ld();
+            if (c0 + 32 >= BN) {                // accumulator drained: hand it back
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[acc]);
+            }
+            const int cb = co0 + c0;
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+            if (!p.ws && p.epi != BIGEMM_EPI_NONE) {
+                float bv[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) bv[j] = cb + j < p.CO ? __ldg(p.bias + cb + j) : 0.f;
+                if (p.epi == BIGEMM_EPI_BIAS) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] += bv[j];
+                } else if (p.epi == BIGEMM_EPI_BIAS_EXP) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = expf(v[j] + bv[j]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = rsqrtf(v[j] + bv[j] + p.eps);
+                }
+            }
+            if (wbox) {
+                uint8_t *buf = wstage + (chunk & 1) * 4096;
+                if (lane == 0) bulk_wait_read<1>();   // the store that used buf has read it
+                __syncwarp();
+                uint8_t *dst = buf + lane * ec;
+                if (ec == 4) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) *reinterpret_cast<float *>(dst + j * 128) = v[j];
+                } else if (p.out_dt == BIGEMM_F16) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        *reinterpret_cast<__half *>(dst + j * 64) = __float2half_rn(v[j]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        *reinterpret_cast<__nv_bfloat16 *>(dst + j * 64) = __float2bfloat16_rn(v[j]);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    if (BOXED)
+                        tma_store_4d(map_c, buf, sx, sy, cb, sn);
+                    else
+                        tma_store_3d(map_c, buf, sx, cb, sn);
+                    bulk_commit();
+                }
+            } else if (!p.store_tma && valid) {
+                const long long o0 = base + (long long)cb * howo;
+                const int jn = min(32, p.CO - cb);
+                if (p.ws) {
+                    float *o = p.ws + o0;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (j < jn) o[j * howo] = v[j];
+                } else if (p.out_dt == BIGEMM_F32) {
+                    float *o = static_cast<float *>(p.out) + o0;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (j < jn) o[j * howo] = v[j];
+                } else if (p.out_dt == BIGEMM_F16) {
+                    __half *o = static_cast<__half *>(p.out) + o0;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (j < jn) o[j * howo] = __float2half_rn(v[j]);
+                } else {
+                    __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.out) + o0;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (j < jn) o[j * howo] = __float2bfloat16_rn(v[j]);
+                }
+            }
+        }
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+    }
+    if (lane == 0) bulk_wait<0>();              // stores complete before the block exits
+}
+
 template <int BN, int AMODE, int FMT>
 __global__ void __launch_bounds__(kThreads, 1)
     umma_conv_kernel(const __grid_constant__ CUtensorMap map_a,
@@ -201,6 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // K-major rows advance inside the swizzle row; MN-major advances by
             // whole 8-row groups (16 rows for 16-bit types, 8 rows for tf32).
             constexpr uint32_t a_kstep = AMODE == A_NHWC ? 32u : (FMT == 2 ? 1024u : 2048u);
+            const uint32_t a_hi = desc_hi(1024u, 2u), b_hi = desc_hi(1024u, 2u);
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -220,21 +377,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_addr = smem_u32(sa + stage * kABytes);
-                    const uint32_t b_addr = smem_u32(sb + stage * C::b_bytes);
+                    const uint32_t a_lo = desc_lo(smem_u32(sa + stage * kABytes),
+                                                  AMODE == A_NHWC ? 16u : box_bytes);
+                    const uint32_t b_lo = desc_lo(smem_u32(sb + stage * C::b_bytes), 16u);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const uint64_t ad =
-                            AMODE == A_NHWC
-                                ? smem_desc(a_addr + k * a_kstep, 16u, 1024u, 2u)
-                                : smem_desc(a_addr + k * a_kstep, box_bytes, 1024u, 2u);
-                        const uint64_t bd = smem_desc(b_addr + k * 32u, 16u, 1024u, 2u);
-                        const uint32_t accum = (kb > w.kb0 || k > 0) ? 1u : 0u;
-                        if (FMT == 2)
-                            umma_tf32(d_tmem, ad, bd, idesc, accum);
-                        else
-                            umma_f16(d_tmem, ad, bd, idesc, accum);
-                    }
+                    for (int k = 0; k < 4; ++k)
+                        umma_lohi<FMT == 2>(d_tmem, a_lo + k * (a_kstep >> 4), a_hi, b_lo + k * 2u,
+                                            b_hi, idesc, (kb > w.kb0 || k > 0) ? 1u : 0u);
                     any = true;
                     umma_commit(&empty[stage]);
                     if (++stage == S) stage = 0, phase ^= 1u;
@@ -253,150 +402,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // --------------------------------------------------------- epilogue
-        // Each warp owns TMEM lanes 32q..32q+31 (32 pixels of the tile) and
-        // works alone: lane 0 waits for the accumulator and shares the outcome,
-        // so the warp stays converged.  With TMA stores the warp stages its
-        // 32 pixels x 32 channels in its own shared buffers and lane 0 writes
-        // them as one box.
-        const int q = warp & 3;                     // TMEM lane quadrant of this warp
-        const int row = q * 32 + lane;              // tile row = pixel
-        const int bi = row / box_px, bj = row - bi * box_px;
-        const int wbi = (q * 32) / box_px;          // the warp's box
-        const int wj0 = (q * 32) - wbi * box_px;    // its first pixel in the box
-        const long long howo = (long long)p.Ho * p.Wo;
-        const int ec = p.ws ? 4 : (p.out_dt == BIGEMM_F32 ? 4 : 2);
-        uint8_t *wstage = stage_out + q * 8192;     // 2 x 4 KB per warp
-        int acc = 0, chunk = 0;
-        uint32_t acc_phase = 0;
-        for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
-            const Unit w = decode(p, u);
-            int okw = 0;
-            if (lane == 0) okw = mbar_wait(&tfull[acc], acc_phase, p.timeout_ns, abort_flag, p.err);
-            if (!__shfl_sync(0xffffffffu, okw, 0)) break;
-            tc_fence_after();
-            const int b = w.pt * p.bpt + bi;
-            bool valid = bi < p.bpt && b < p.total_boxes;
-            long long base = 0, base_out = 0;
-            if (valid) {
-                const int n = b / p.boxes_per_img;
-                const int rem = b - n * p.boxes_per_img;
-                long long pix;
-                if (AMODE == A_NHWC) {
-                    const int byi = rem / p.boxes_x, bxi = rem - byi * p.boxes_x;
-                    const int y = byi * p.box_h + bj / p.box_w;
-                    const int x = bxi * p.box_w + bj % p.box_w;
-                    valid = y < p.Ho && x < p.Wo;
-                    pix = (long long)y * p.Wo + x;
-                } else {
-                    pix = (long long)rem * p.box_w + bj;
-                    valid = pix < howo;
-                }
-                base_out = (long long)n * p.CO * howo + pix;
-                base = (long long)w.sp * p.out_elems + base_out;
-            }
-            // the warp's store box (TMA mode): origin and image index
-            const int wb = w.pt * p.bpt + wbi;
-            const bool wbox = p.store_tma && wbi < p.bpt && wb < p.total_boxes;
-            int sx = 0, sy = 0, sn = 0;
-            if (wbox) {
-                const int n = wb / p.boxes_per_img;
-                const int rem = wb - n * p.boxes_per_img;
-                sn = w.sp * p.N + n;
-                if (AMODE == A_NHWC) {
-                    const int byi = rem / p.boxes_x, bxi = rem - byi * p.boxes_x;
-                    sx = bxi * p.box_w + wj0 % p.box_w;
-                    sy = byi * p.box_h + wj0 / p.box_w;
-                } else {
-                    sx = rem * p.box_w + wj0;
-                }
-            }
-            const int co0 = w.ct * BN;
-#pragma unroll 1
-            for (int c0 = 0; c0 < BN; c0 += 32, ++chunk) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + c0),
-                                   r);
-                tmem_wait_ld();
-                if (c0 + 32 >= BN) {                // accumulator drained: hand it back
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&tempty[acc]);
-                }
-                const int cb = co0 + c0;
-                float v[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-                if (!p.ws && p.epi != BIGEMM_EPI_NONE) {
-                    float bv[32];
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) bv[j] = cb + j < p.CO ? __ldg(p.bias + cb + j) : 0.f;
-                    if (p.epi == BIGEMM_EPI_BIAS) {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] += bv[j];
-                    } else if (p.epi == BIGEMM_EPI_BIAS_EXP) {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] = expf(v[j] + bv[j]);
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] = rsqrtf(v[j] + bv[j] + p.eps);
-                    }
-                }
-                if (wbox) {
-                    uint8_t *buf = wstage + (chunk & 1) * 4096;
-                    if (lane == 0) bulk_wait_read<1>();   // the store that used buf has read it
-                    __syncwarp();
-                    uint8_t *dst = buf + lane * ec;
-                    if (ec == 4) {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) *reinterpret_cast<float *>(dst + j * 128) = v[j];
-                    } else if (p.out_dt == BIGEMM_F16) {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            *reinterpret_cast<__half *>(dst + j * 64) = __float2half_rn(v[j]);
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            *reinterpret_cast<__nv_bfloat16 *>(dst + j * 64) = __float2bfloat16_rn(v[j]);
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        if (AMODE == A_NHWC)
-                            tma_store_4d(&map_c, buf, sx, sy, cb, sn);
-                        else
-                            tma_store_3d(&map_c, buf, sx, cb, sn);
-                        bulk_commit();
-                    }
-                } else if (!p.store_tma && valid) {
-                    const long long o0 = base + (long long)cb * howo;
-                    const int jn = min(32, p.CO - cb);
-                    if (p.ws) {
-                        float *o = p.ws + o0;
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if (j < jn) o[j * howo] = v[j];
-                    } else if (p.out_dt == BIGEMM_F32) {
-                        float *o = static_cast<float *>(p.out) + o0;
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if (j < jn) o[j * howo] = v[j];
-                    } else if (p.out_dt == BIGEMM_F16) {
-                        __half *o = static_cast<__half *>(p.out) + o0;
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if (j < jn) o[j * howo] = __float2half_rn(v[j]);
-                    } else {
-                        __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.out) + o0;
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if (j < jn) o[j * howo] = __float2bfloat16_rn(v[j]);
-                    }
-                }
-            }
-            acc ^= 1;
-            if (acc == 0) acc_phase ^= 1u;
-        }
-        if (lane == 0) bulk_wait<0>();              // stores complete before the block exits
+        epilogue_warp<BN, AMODE != A_DIRECT>(p, &map_c, tmem_base, tfull, tempty, stage_out,
+                                             abort_flag, warp, lane, box_px);
     }
 
     tc_fence_before();
@@ -405,6 +412,237 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) {
         __syncwarp();
         tmem_dealloc(tmem_base, C::tmem_cols);
+    }
+}
+
+
+// ------------------------------------------------------------------ halo mode
+// Stride-1 K x K convolutions: the tile is 16 output rows x 8 output columns of
+// one image.  For each 128-byte channel block one TMA box brings the tile's
+// input halo, (16 + KH - 1) rows x 16 pixels, into shared memory with a row
+// pitch of 16 pixels (2 KB, a whole number of 1 KB swizzle periods).  The A
+// operand of tap (ry, rx) is then this halo read from row ry, column rx: a
+// descriptor start (ry*16 + rx) rows in and the 8-row groups (output rows) 2 KB
+// apart.  The 128-byte swizzle is a function of the shared-memory address bits
+// (measured: the descriptor's base offset must stay 0 for such starts), and
+// both TMA and the MMA see the same address for each halo pixel.  The
+// B operand (packed weights) arrives TB taps per copy from a (channel, output
+// channel, tap) view, so a 3x3 tile needs 1 A copy and 9/TB B copies per
+// channel block instead of 9 of each.
+constexpr int kHaloPitch = 16;
+constexpr int kHaloRowBytes = kHaloPitch * kRowBytes;        // 2 KB
+constexpr int kHaloMaxKH = 7;
+constexpr int kHaloBytes = (16 + kHaloMaxKH - 1) * kHaloRowBytes;   // 44 KB
+
+template <int BN>
+struct HaloCfg {
+    static constexpr int a_stages = 2;
+    static constexpr int b_bytes = 32768;
+    static constexpr int tb = b_bytes / (BN * kRowBytes);    // taps per B copy: 4, 2, 1
+    static constexpr int b_stages = 3;
+    static constexpr int staging = 32768;
+    static constexpr int bars = (2 * a_stages + 2 * b_stages + 5) * 8;
+    static constexpr int smem = a_stages * kHaloBytes + b_stages * b_bytes + staging + bars + 16 + 1024;
+    static constexpr uint32_t tmem_cols = Cfg<BN>::tmem_cols;
+};
+
+template <int BN, int FMT>
+__global__ void __launch_bounds__(kThreads, 1)
+    umma_conv_halo_kernel(const __grid_constant__ CUtensorMap map_a,
+                          const __grid_constant__ CUtensorMap map_b,
+                          const __grid_constant__ CUtensorMap map_c, const UmmaParams p)
+{
+    using C = HaloCfg<BN>;
+    constexpr int SA = C::a_stages, SB = C::b_stages, TB = C::tb;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint8_t *sa = smem;
+    uint8_t *sb = sa + SA * kHaloBytes;
+    uint8_t *stage_out = sb + SB * C::b_bytes;
+    uint64_t *a_full = reinterpret_cast<uint64_t *>(stage_out + C::staging);
+    uint64_t *a_empty = a_full + SA;
+    uint64_t *b_full = a_empty + SA;
+    uint64_t *b_empty = b_full + SB;
+    uint64_t *tfull = b_empty + SB;
+    uint64_t *tempty = tfull + 2;
+    uint64_t *drain = tempty + 2;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int KK = p.KH * p.KW;
+    const uint32_t halo_bytes = (uint32_t)(16 + p.KH - 1) * kHaloRowBytes;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < SA; ++i) mbar_init(&a_full[i], 1), mbar_init(&a_empty[i], 1);
+        for (int i = 0; i < SB; ++i) mbar_init(&b_full[i], 1), mbar_init(&b_empty[i], 1);
+        for (int i = 0; i < 2; ++i) mbar_init(&tfull[i], 1), mbar_init(&tempty[i], 4);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&map_a);
+        tma_prefetch_desc(&map_b);
+        if (p.store_tma) tma_prefetch_desc(&map_c);
+    }
+    if (warp == 1) {
+        __syncwarp();
+        tmem_alloc(tmem_holder, C::tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int as = 0, bs = 0;
+            uint32_t aph = 0, bph = 0;
+            uint32_t a_par[SA], b_par[SB];
+            bool a_iss[SA], b_iss[SB];
+            for (int i = 0; i < SA; ++i) a_iss[i] = false, a_par[i] = 0;
+            for (int i = 0; i < SB; ++i) b_iss[i] = false, b_par[i] = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+                const Unit w = decode(p, u);
+                const int n = w.pt / p.boxes_per_img;
+                const int rem = w.pt - n * p.boxes_per_img;
+                const int byi = rem / p.boxes_x, bxi = rem - byi * p.boxes_x;
+                const int x0 = bxi * 8 - p.pad, y0 = byi * 16 - p.pad;
+                const int ncol = w.ct * BN;
+                for (int cb = w.kb0; ok && cb < w.kb1; ++cb) {
+                    if (!mbar_wait(&a_empty[as], aph ^ 1u, p.timeout_ns, abort_flag, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&a_full[as], halo_bytes);
+                    a_iss[as] = true, a_par[as] = aph;
+                    tma_load_4d(sa + as * kHaloBytes, &map_a, &a_full[as], cb * p.bk, x0, y0, n);
+                    if (++as == SA) as = 0, aph ^= 1u;
+                    for (int t0 = 0; t0 < KK; t0 += TB) {
+                        if (!mbar_wait(&b_empty[bs], bph ^ 1u, p.timeout_ns, abort_flag, p.err)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&b_full[bs], (uint32_t)C::b_bytes);
+                        b_iss[bs] = true, b_par[bs] = bph;
+                        tma_load_3d(sb + bs * C::b_bytes, &map_b, &b_full[bs], cb * p.bk, ncol, t0);
+                        if (++bs == SB) bs = 0, bph ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // Let every copy already issued land before the block exits.
+                int local_abort = 0;
+                for (int i = 0; i < SA; ++i)
+                    if (a_iss[i]) mbar_wait(&a_full[i], a_par[i], p.timeout_ns, &local_abort, p.err);
+                for (int i = 0; i < SB; ++i)
+                    if (b_iss[i]) mbar_wait(&b_full[i], b_par[i], p.timeout_ns, &local_abort, p.err);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = make_idesc(FMT == 2 ? 2u : (uint32_t)FMT, 0u, 0u, kTileM, BN);
+            const uint32_t a_hi = desc_hi((uint32_t)kHaloRowBytes, 2u), b_hi = desc_hi(1024u, 2u);
+            int as = 0, bs = 0, acc = 0;
+            uint32_t aph = 0, bph = 0, acc_phase = 0;
+            bool ok = true, any = false;
+            for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+                const Unit w = decode(p, u);
+                if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, p.timeout_ns, abort_flag, p.err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                uint32_t accum = 0;
+                for (int cb = w.kb0; ok && cb < w.kb1; ++cb) {
+                    if (!mbar_wait(&a_full[as], aph, p.timeout_ns, abort_flag, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t a_lo0 = desc_lo(smem_u32(sa + as * kHaloBytes), 16u);
+                    int ry = 0, rx = 0;
+                    for (int t0 = 0; t0 < KK; t0 += TB) {
+                        if (!mbar_wait(&b_full[bs], bph, p.timeout_ns, abort_flag, p.err)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        uint32_t b_lo = desc_lo(smem_u32(sb + bs * C::b_bytes), 16u);
+                        const int nt = min(TB, KK - t0);
+                        for (int tt = 0; tt < nt; ++tt) {
+                            const uint32_t a_lo =
+                                a_lo0 + (uint32_t)(ry * kHaloPitch + rx) * (kRowBytes >> 4);
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                umma_lohi<FMT == 2>(d_tmem, a_lo + k * 2u, a_hi, b_lo + k * 2u, b_hi,
+                                                    idesc, accum);
+                                accum = 1u;
+                            }
+                            b_lo += (uint32_t)(BN * kRowBytes) >> 4;
+                            if (++rx == p.KW) rx = 0, ++ry;
+                        }
+                        any = true;
+                        umma_commit(&b_empty[bs]);
+                        if (++bs == SB) bs = 0, bph ^= 1u;
+                    }
+                    umma_commit(&a_empty[as]);
+                    if (++as == SA) as = 0, aph ^= 1u;
+                }
+                if (!ok) break;
+                umma_commit(&tfull[acc]);
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+            if (!ok && any) {
+                int local_abort = 0;
+                umma_commit(drain);
+                mbar_wait(drain, 0, p.timeout_ns, &local_abort, p.err);
+            }
+        }
+    } else {
+        epilogue_warp<BN, true>(p, &map_c, tmem_base, tfull, tempty, stage_out, abort_flag, warp,
+                                lane, 128);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        tmem_dealloc(tmem_base, C::tmem_cols);
+    }
+}
+
+template <int BN, int FMT>
+cudaError_t launch_halo(const UmmaParams &p, const CUtensorMap &ma, const CUtensorMap &mb,
+                        const CUtensorMap &mc, int grid, cudaStream_t stream)
+{
+    auto kern = umma_conv_halo_kernel<BN, FMT>;
+    static unsigned long long attr_set = 0;   // bit per device: smem opt-in done
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 64 || !(attr_set >> dev & 1ull)) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             HaloCfg<BN>::smem);
+        if (e != cudaSuccess) return e;
+        if (dev < 64) attr_set |= 1ull << dev;
+    }
+    kern<<<grid, kThreads, HaloCfg<BN>::smem, stream>>>(ma, mb, mc, p);
+    return cudaGetLastError();
+}
+
+template <int FMT>
+cudaError_t dispatch_halo_bn(int bn, const UmmaParams &p, const CUtensorMap &ma,
+                             const CUtensorMap &mb, const CUtensorMap &mc, int grid, cudaStream_t s)
+{
+    switch (bn) {
+    case 64: return launch_halo<64, FMT>(p, ma, mb, mc, grid, s);
+    case 128: return launch_halo<128, FMT>(p, ma, mb, mc, grid, s);
+    case 256: return launch_halo<256, FMT>(p, ma, mb, mc, grid, s);
+    default: return cudaErrorInvalidValue;
     }
 }
 
@@ -456,6 +694,14 @@ int fmt_of(int in_dt) { return in_dt == BIGEMM_F16 ? 0 : in_dt == BIGEMM_BF16 ? 
 
 size_t umma_smem_bytes(const UmmaTiling &t)
 {
+    if (t.amode == A_HALO) {
+        switch (t.bn) {
+        case 64: return HaloCfg<64>::smem;
+        case 128: return HaloCfg<128>::smem;
+        case 256: return HaloCfg<256>::smem;
+        default: return 0;
+        }
+    }
     switch (t.bn) {
     case 64: return Cfg<64>::smem;
     case 128: return Cfg<128>::smem;
@@ -467,15 +713,26 @@ size_t umma_smem_bytes(const UmmaTiling &t)
 bool umma_tiling_compiled(const UmmaTiling &t, int in_dt)
 {
     (void)in_dt;
-    return (t.bn == 64 || t.bn == 128 || t.bn == 256) && (t.amode == A_NHWC || t.amode == A_DIRECT);
+    return (t.bn == 64 || t.bn == 128 || t.bn == 256) &&
+           (t.amode == A_NHWC || t.amode == A_DIRECT || t.amode == A_HALO);
 }
 
 cudaError_t launch_umma_conv(const UmmaTiling &t, int in_dt, const UmmaParams &p,
                              const CUtensorMap &map_a, const CUtensorMap &map_b,
                              const CUtensorMap &map_c, int grid, cudaStream_t stream)
 {
-    ProfScope prof(t.amode == A_NHWC ? "umma_conv_nhwc" : "umma_conv_direct", stream);
+    ProfScope prof(t.amode == A_NHWC ? "umma_conv_nhwc"
+                   : t.amode == A_HALO ? "umma_conv_halo"
+                                       : "umma_conv_direct",
+                   stream);
     const int fmt = fmt_of(in_dt);
+    if (t.amode == A_HALO) {
+        switch (fmt) {
+        case 0: return dispatch_halo_bn<0>(t.bn, p, map_a, map_b, map_c, grid, stream);
+        case 1: return dispatch_halo_bn<1>(t.bn, p, map_a, map_b, map_c, grid, stream);
+        default: return dispatch_halo_bn<2>(t.bn, p, map_a, map_b, map_c, grid, stream);
+        }
+    }
     if (t.amode == A_NHWC)
         return dispatch_fmt<A_NHWC>(fmt, t.bn, p, map_a, map_b, map_c, grid, stream);
     return dispatch_fmt<A_DIRECT>(fmt, t.bn, p, map_a, map_b, map_c, grid, stream);

@@ -96,6 +96,9 @@ typedef struct {
     int stages;     /* UMMA: shared-memory pipeline depth (2..8)                */
     int box_w;      /* UMMA: output pixels per tile along W (with box_h)        */
     int box_h;      /* UMMA: output rows per tile (box_w*box_h*boxes = 128)      */
+    int mode;       /* UMMA operand-A mode: 1 channels-last boxes per tap,
+                       2 NCHW read in place (1x1, stride 1, 16-bit),
+                       3 one halo box per channel block (stride 1)              */
 } bigemm_plan_options;
 
 /*

@@ -139,6 +139,43 @@ def test_umma_direct_and_nhwc_agree_on_1x1():
     assert a["amode"] == "direct" and b["amode"] == "nhwc"
 
 
+# ------------------------------------------------- halo mode (stride 1, K x K)
+def _H(name, N, CI, CO, H, W, K, p, i="f16", o="f16", epi="none"):
+    return synth.ConvSpec(name, N, CI, CO, H, W, K, 1, p, 1, i, o, "uniform", "he", epi)
+
+
+HALO = [
+    synth.RESNET50_FP16[1].with_batch(1),
+    synth.SWEEP_FP32[0], synth.SWEEP_FP32[1], synth.SWEEP_FP32[2],
+    _H("halo_ragged_13x11_ci24_co40", 2, 24, 40, 13, 11, 3, 1),
+    _H("halo_k5_bf16", 1, 32, 96, 17, 19, 5, 2, i="bf16", o="bf16"),
+    _H("halo_k7_pad3", 1, 16, 64, 20, 18, 7, 3),
+    _H("halo_k3_pad0", 2, 64, 128, 18, 18, 3, 0),
+    _H("halo_exp_f32out", 2, 64, 256, 32, 32, 3, 1, o="f32", epi="bias_exp"),
+    _H("halo_rect_1x3", 1, 64, 64, 9, 30, 3, 1),
+]
+
+
+@pytest.mark.parametrize("spec", HALO, ids=lambda s: s.name)
+def test_umma_halo_mode(spec):
+    info = check(spec, {"kind": bg.KIND_UMMA, "mode": bg.MODE_HALO})
+    assert info["amode"] == "halo"
+
+
+@pytest.mark.parametrize("bn", [64, 128, 256])
+def test_umma_halo_tile_n(bn):
+    spec = _H("halo_bn", 1, 64, 300, 20, 24, 3, 1)
+    info = check(spec, {"kind": bg.KIND_UMMA, "mode": bg.MODE_HALO, "tile_n": bn})
+    assert info["bn"] == bn and info["amode"] == "halo"
+
+
+@pytest.mark.parametrize("split", [2, 4, 16])
+def test_umma_halo_split_k(split):
+    spec = synth.RESNET_LAST[0]
+    info = check(spec, {"kind": bg.KIND_UMMA, "mode": bg.MODE_HALO, "tile_n": 128, "split_k": split})
+    assert info["amode"] == "halo" and info["split"] > 1
+
+
 # ------------------------------------------------- edge cases
 def S(name, N, CI, CO, H, W, K, s, p, g=1, i="f16", o="f16", epi="none", dd="uniform", kd="he"):
     return synth.ConvSpec(name, N, CI, CO, H, W, K, s, p, g, i, o, dd, kd, epi)
