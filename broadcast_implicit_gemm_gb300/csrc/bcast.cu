@@ -13,6 +13,7 @@
 #include <cuda_fp16.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace bigemm {
 
@@ -61,6 +62,7 @@ __global__ void __launch_bounds__(256) bcast_kernel(int N, int C, long long HW, 
                                                     const float *__restrict__ var, float eps,
                                                     T *__restrict__ out)
 {
+    griddep_wait();
     const int c = blockIdx.x;
     const T tv = cvt<T>(bc_op(op, __ldg(var + c), eps));   // once per thread
     if (VEC) {
@@ -84,6 +86,7 @@ __global__ void __launch_bounds__(256) bcast_flat_kernel(long long total, int C,
                                                          int op, const float *__restrict__ var,
                                                          float eps, T *__restrict__ out)
 {
+    griddep_wait();
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
          i += (long long)gridDim.x * blockDim.x) {
         const int c = (int)((i / HW) % C);
@@ -103,8 +106,8 @@ cudaError_t launch_typed(int N, int C, long long HW, int op, const float *var, f
         const long long total = (long long)N * C * HW;
         long long g = (total + 255) / 256;
         if (g > (long long)sms * 32) g = (long long)sms * 32;
-        bcast_flat_kernel<T><<<(int)g, 256, 0, stream>>>(total, C, HW, op, var, eps, o);
-        return cudaGetLastError();
+        return launch_pdl(bcast_flat_kernel<T>, dim3((unsigned)g), dim3(256), 0, stream, total, C, HW,
+                          op, var, eps, o);
     }
     ProfScope prof("bcast_nchw", stream);
     // enough blocks for ~16 resident 256-thread blocks per SM, each covering
@@ -116,11 +119,8 @@ cudaError_t launch_typed(int N, int C, long long HW, int op, const float *var, f
     dim3 grid(C, (unsigned)gy);
     const bool vec = ((HW * (long long)sizeof(T)) % 16 == 0) &&
                      ((reinterpret_cast<uintptr_t>(out) & 15) == 0);
-    if (vec)
-        bcast_kernel<T, true><<<grid, 256, 0, stream>>>(N, C, HW, op, var, eps, o);
-    else
-        bcast_kernel<T, false><<<grid, 256, 0, stream>>>(N, C, HW, op, var, eps, o);
-    return cudaGetLastError();
+    if (vec) return launch_pdl(bcast_kernel<T, true>, grid, dim3(256), 0, stream, N, C, HW, op, var, eps, o);
+    return launch_pdl(bcast_kernel<T, false>, grid, dim3(256), 0, stream, N, C, HW, op, var, eps, o);
 }
 
 }  // namespace

@@ -3,6 +3,7 @@
 #include <cstddef>
 #include <cstdint>
 #include <string>
+#include <utility>
 #include <vector>
 
 #include <cuda.h>
@@ -98,6 +99,26 @@ cudaError_t launch_bcast(int N, int C, int HW, int op, const float *var, float e
                          int out_dt, int flat, cudaStream_t stream);
 cudaError_t launch_wait_timeout_probe(int *err, unsigned long long timeout_ns,
                                       cudaStream_t stream);
+
+// Launch with programmatic stream serialization: the kernel may start while
+// the previous kernel on the stream finishes; it calls griddepcontrol.wait
+// before touching memory the previous kernel uses.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // -------------------------------------------------------------- runtime state
 struct DeviceState {

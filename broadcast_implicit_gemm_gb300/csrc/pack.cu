@@ -17,6 +17,7 @@
 #include <cuda_fp16.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace bigemm {
 
@@ -26,6 +27,7 @@ template <typename T>
 __global__ void pack_nhwc_kernel(const T *__restrict__ x, T *__restrict__ xh, int C, int HW,
                                  int Ch)
 {
+    griddep_wait();
     __shared__ T tile[32][33];
     const int n = blockIdx.z;
     const int p0 = blockIdx.x * 32, c0 = blockIdx.y * 32;
@@ -55,6 +57,7 @@ __global__ void __launch_bounds__(256) pack_nhwc_vec_kernel(const T *__restrict_
                                                             T *__restrict__ xh, int C, int HW,
                                                             int Ch)
 {
+    griddep_wait();
     constexpr int VEC = 16 / sizeof(T);
     constexpr int TILE = 8 * VEC;
     __shared__ T tile[TILE][TILE + 1];
@@ -102,6 +105,7 @@ __global__ void __launch_bounds__(256) pack_operands_kernel(const T *__restrict_
                                                             T *__restrict__ wp, int CO, int CI,
                                                             int KHKW, int cip)
 {
+    griddep_wait();
     constexpr int VEC = 16 / sizeof(T);
     constexpr int TILE = 8 * VEC;
     __shared__ T tile[TILE][TILE + 1];
@@ -156,6 +160,7 @@ template <typename T>
 __global__ void pack_weights_kernel(const T *__restrict__ w, T *__restrict__ wp, int CO, int CI,
                                     int KHKW, int cip)
 {
+    griddep_wait();
     const long long total = (long long)CO * KHKW * cip;
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
          i += (long long)gridDim.x * blockDim.x) {
@@ -194,6 +199,7 @@ __global__ void splitk_reduce_kernel(const float *__restrict__ ws, int split, lo
                                      int CO, int HoWo, int epi, const float *__restrict__ bias,
                                      float eps, TO *__restrict__ out)
 {
+    griddep_wait();
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < elems;
          i += (long long)gridDim.x * blockDim.x) {
         float s = ws[i];
@@ -224,21 +230,17 @@ cudaError_t launch_pack_nhwc(const void *x, void *xh, int N, int C, int HW, int 
         const int tile = 8 * vec;
         dim3 g((HW + tile - 1) / tile, (Ch + tile - 1) / tile, N);
         if (dtype_size(dt) == 4)
-            pack_nhwc_vec_kernel<uint32_t><<<g, 256, 0, stream>>>(
-                static_cast<const uint32_t *>(x), static_cast<uint32_t *>(xh), C, HW, Ch);
-        else
-            pack_nhwc_vec_kernel<uint16_t><<<g, 256, 0, stream>>>(
-                static_cast<const uint16_t *>(x), static_cast<uint16_t *>(xh), C, HW, Ch);
-        return cudaGetLastError();
+            return launch_pdl(pack_nhwc_vec_kernel<uint32_t>, g, dim3(256), 0, stream,
+                              static_cast<const uint32_t *>(x), static_cast<uint32_t *>(xh), C, HW, Ch);
+        return launch_pdl(pack_nhwc_vec_kernel<uint16_t>, g, dim3(256), 0, stream,
+                          static_cast<const uint16_t *>(x), static_cast<uint16_t *>(xh), C, HW, Ch);
     }
     dim3 grid((HW + 31) / 32, (Ch + 31) / 32, N), block(32, 8);
     if (dtype_size(dt) == 4)
-        pack_nhwc_kernel<uint32_t><<<grid, block, 0, stream>>>(
-            static_cast<const uint32_t *>(x), static_cast<uint32_t *>(xh), C, HW, Ch);
-    else
-        pack_nhwc_kernel<uint16_t><<<grid, block, 0, stream>>>(
-            static_cast<const uint16_t *>(x), static_cast<uint16_t *>(xh), C, HW, Ch);
-    return cudaGetLastError();
+        return launch_pdl(pack_nhwc_kernel<uint32_t>, grid, block, 0, stream,
+                          static_cast<const uint32_t *>(x), static_cast<uint32_t *>(xh), C, HW, Ch);
+    return launch_pdl(pack_nhwc_kernel<uint16_t>, grid, block, 0, stream,
+                      static_cast<const uint16_t *>(x), static_cast<uint16_t *>(xh), C, HW, Ch);
 }
 
 cudaError_t launch_pack_operands(const void *x, void *xh, int N, int C, int HW, int Ch,
@@ -260,16 +262,14 @@ cudaError_t launch_pack_operands(const void *x, void *xh, int N, int C, int HW, 
     ProfScope prof("pack_operands", stream);
     const int grid = (int)(data_blocks + wblocks);
     if (dtype_size(dt) == 4)
-        pack_operands_kernel<uint32_t><<<grid, 256, 0, stream>>>(
-            static_cast<const uint32_t *>(x), static_cast<uint32_t *>(xh), C, HW, Ch, (int)ptiles,
-            (int)ctiles, (int)data_blocks, static_cast<const uint32_t *>(w),
-            static_cast<uint32_t *>(wp), CO, CI, KHKW, cip);
-    else
-        pack_operands_kernel<uint16_t><<<grid, 256, 0, stream>>>(
-            static_cast<const uint16_t *>(x), static_cast<uint16_t *>(xh), C, HW, Ch, (int)ptiles,
-            (int)ctiles, (int)data_blocks, static_cast<const uint16_t *>(w),
-            static_cast<uint16_t *>(wp), CO, CI, KHKW, cip);
-    return cudaGetLastError();
+        return launch_pdl(pack_operands_kernel<uint32_t>, dim3(grid), dim3(256), 0, stream,
+                          static_cast<const uint32_t *>(x), static_cast<uint32_t *>(xh), C, HW, Ch,
+                          (int)ptiles, (int)ctiles, (int)data_blocks, static_cast<const uint32_t *>(w),
+                          static_cast<uint32_t *>(wp), CO, CI, KHKW, cip);
+    return launch_pdl(pack_operands_kernel<uint16_t>, dim3(grid), dim3(256), 0, stream,
+                      static_cast<const uint16_t *>(x), static_cast<uint16_t *>(xh), C, HW, Ch,
+                      (int)ptiles, (int)ctiles, (int)data_blocks, static_cast<const uint16_t *>(w),
+                      static_cast<uint16_t *>(wp), CO, CI, KHKW, cip);
 }
 
 cudaError_t launch_pack_weights(const void *w, void *wp, int CO, int CI, int KHKW, int cip,
@@ -279,12 +279,10 @@ cudaError_t launch_pack_weights(const void *w, void *wp, int CO, int CI, int KHK
     const long long total = (long long)CO * KHKW * cip;
     const int grid = grid_for(total, 256);
     if (dtype_size(dt) == 4)
-        pack_weights_kernel<uint32_t><<<grid, 256, 0, stream>>>(
-            static_cast<const uint32_t *>(w), static_cast<uint32_t *>(wp), CO, CI, KHKW, cip);
-    else
-        pack_weights_kernel<uint16_t><<<grid, 256, 0, stream>>>(
-            static_cast<const uint16_t *>(w), static_cast<uint16_t *>(wp), CO, CI, KHKW, cip);
-    return cudaGetLastError();
+        return launch_pdl(pack_weights_kernel<uint32_t>, dim3(grid), dim3(256), 0, stream,
+                          static_cast<const uint32_t *>(w), static_cast<uint32_t *>(wp), CO, CI, KHKW, cip);
+    return launch_pdl(pack_weights_kernel<uint16_t>, dim3(grid), dim3(256), 0, stream,
+                      static_cast<const uint16_t *>(w), static_cast<uint16_t *>(wp), CO, CI, KHKW, cip);
 }
 
 cudaError_t launch_splitk_reduce(const float *ws, int split, long long elems, int CO, int HoWo,
@@ -295,18 +293,15 @@ cudaError_t launch_splitk_reduce(const float *ws, int split, long long elems, in
     const int grid = grid_for(elems, 256);
     switch (out_dt) {
     case BIGEMM_F32:
-        splitk_reduce_kernel<float><<<grid, 256, 0, stream>>>(ws, split, elems, CO, HoWo, epi,
-                                                             bias, eps, static_cast<float *>(out));
-        break;
+        return launch_pdl(splitk_reduce_kernel<float>, dim3(grid), dim3(256), 0, stream, ws, split,
+                          elems, CO, HoWo, epi, bias, eps, static_cast<float *>(out));
     case BIGEMM_F16:
-        splitk_reduce_kernel<__half><<<grid, 256, 0, stream>>>(
-            ws, split, elems, CO, HoWo, epi, bias, eps, static_cast<__half *>(out));
-        break;
+        return launch_pdl(splitk_reduce_kernel<__half>, dim3(grid), dim3(256), 0, stream, ws, split,
+                          elems, CO, HoWo, epi, bias, eps, static_cast<__half *>(out));
     default:
-        splitk_reduce_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(
-            ws, split, elems, CO, HoWo, epi, bias, eps, static_cast<__nv_bfloat16 *>(out));
+        return launch_pdl(splitk_reduce_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, stream, ws,
+                          split, elems, CO, HoWo, epi, bias, eps, static_cast<__nv_bfloat16 *>(out));
     }
-    return cudaGetLastError();
 }
 
 }  // namespace bigemm

@@ -21,6 +21,14 @@ __device__ __forceinline__ uint64_t globaltimer_ns()
     return t;
 }
 
+// Programmatic dependent launch: wait until the grids this one depends on
+// have completed (their writes visible); let dependent grids start launching.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
 {

@@ -19,6 +19,7 @@
 #include <cuda_fp16.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace bigemm {
 
@@ -65,6 +66,7 @@ __global__ void __launch_bounds__(256) conv_tiled_kernel(SimtArgs a, const void 
                                                          const float *__restrict__ bias,
                                                          void *__restrict__ out)
 {
+    griddep_wait();
     __shared__ __align__(16) float ws[TK][TM];
     __shared__ __align__(16) float xs[TK][TN];
     const int n = blockIdx.z;
@@ -135,6 +137,7 @@ __global__ void conv_naive_kernel(SimtArgs a, const void *__restrict__ x,
                                   const void *__restrict__ w, const float *__restrict__ bias,
                                   void *__restrict__ out)
 {
+    griddep_wait();
     const long long total = (long long)a.N * a.CO * a.Ho * a.Wo;
     const int cig = a.CI / a.groups, cog = a.CO / a.groups;
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
@@ -211,6 +214,7 @@ __global__ void __launch_bounds__(256) conv_depthwise_kernel(SimtArgs a, int row
                                                              const float *__restrict__ bias,
                                                              void *__restrict__ out)
 {
+    griddep_wait();
     extern __shared__ float sm[];
     const int KH = K ? K : a.KH, KW = K ? K : a.KW, st = S ? S : a.stride;
     const int nplanes = a.N * a.CI;
@@ -342,8 +346,7 @@ cudaError_t launch_simt_conv(const ConvShape &s, const void *x, const void *w,
     if (variant == 1 && s.groups == 1) {
         ProfScope prof("simt_conv_tiled", stream);
         dim3 grid((s.Ho * s.Wo + TN - 1) / TN, (s.CO + TM - 1) / TM, s.N);
-        conv_tiled_kernel<<<grid, 256, 0, stream>>>(a, x, w, bias, out);
-        return cudaGetLastError();
+        return launch_pdl(conv_tiled_kernel, grid, dim3(256), 0, stream, a, x, w, bias, out);
     }
     ProfScope prof("simt_conv_naive", stream);
     const long long total = (long long)s.N * s.CO * s.Ho * s.Wo;
@@ -351,8 +354,7 @@ cudaError_t launch_simt_conv(const ConvShape &s, const void *x, const void *w,
     DeviceState *ds = device_state();
     const long long cap = (long long)(ds ? ds->sm_count : 148) * 32;
     if (g > cap) g = cap;
-    conv_naive_kernel<<<(int)g, 256, 0, stream>>>(a, x, w, bias, out);
-    return cudaGetLastError();
+    return launch_pdl(conv_naive_kernel, dim3((unsigned)g), dim3(256), 0, stream, a, x, w, bias, out);
 }
 
 // Planes per block: enough (image, channel) planes that each block has work
@@ -390,8 +392,7 @@ cudaError_t launch_dw_conv(const ConvShape &s, const void *x, const void *w, con
                                                  (int)smem);
             if (e != cudaSuccess) return e;
         }
-        kern<<<grid, 256, smem, stream>>>(a, rows, ppb, x, w, bias, out);
-        return cudaGetLastError();
+        return launch_pdl(kern, grid, dim3(256), smem, stream, a, rows, ppb, x, w, bias, out);
     };
     const bool sq = s.KH == s.KW;
     if (sq && s.KH == 3 && s.stride == 1) return go(conv_depthwise_kernel<3, 1>);

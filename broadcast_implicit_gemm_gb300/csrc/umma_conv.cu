@@ -274,6 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
+    griddep_wait();   // the set-up above overlapped the previous kernel; its data is ready now
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
@@ -406,6 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              abort_flag, warp, lane, box_px);
     }
 
+    griddep_launch_dependents();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -492,6 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
+    griddep_wait();   // the set-up above overlapped the previous kernel; its data is ready now
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
@@ -607,6 +610,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 lane, 128);
     }
 
+    griddep_launch_dependents();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -630,8 +634,8 @@ cudaError_t launch_halo(const UmmaParams &p, const CUtensorMap &ma, const CUtens
         if (e != cudaSuccess) return e;
         if (dev < 64) attr_set |= 1ull << dev;
     }
-    kern<<<grid, kThreads, HaloCfg<BN>::smem, stream>>>(ma, mb, mc, p);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(kThreads), (size_t)HaloCfg<BN>::smem, stream, ma, mb, mc,
+                      p);
 }
 
 template <int FMT>
@@ -660,8 +664,7 @@ cudaError_t launch_one(const UmmaParams &p, const CUtensorMap &ma, const CUtenso
         if (e != cudaSuccess) return e;
         if (dev < 64) attr_set |= 1ull << dev;
     }
-    kern<<<grid, kThreads, Cfg<BN>::smem, stream>>>(ma, mb, mc, p);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(kThreads), (size_t)Cfg<BN>::smem, stream, ma, mb, mc, p);
 }
 
 template <int AMODE, int FMT>
