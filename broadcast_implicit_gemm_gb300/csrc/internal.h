@@ -10,6 +10,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/bigemm.h"
+#include "fastdiv.h"
 
 namespace bigemm {
 
@@ -36,8 +37,18 @@ enum AMode {
     A_HALO = 2,     // stride 1, K x K: one halo box per channel block serves every tap
 };
 
+// How the pack lays the data out for the A_NHWC / A_HALO kernels.
+enum PackLayout {
+    PACK_PLAIN = 0,   // [N][H][W][Ch]
+    PACK_SUB = 1,     // 1x1, pad 0, stride s: [N][Ho][Wo][Ch] of the pixels the conv reads;
+                      // the kernel then runs a stride-1 1x1 conv over it
+    PACK_STACK = 2,   // stride 1: [N][H+pad][W][Ch], images stacked with pad zero rows
+                      // between them, so a halo tile may span several images
+};
+
 struct UmmaTiling {
     int amode;        // AMode
+    int pack;         // PackLayout
     int bn;           // output channels per tile (N of the MMA), multiple of 32
     int stages;       // smem ring depth
     int box_w, box_h; // output pixels per TMA box (A_NHWC); A_DIRECT: box_w = row pixels
@@ -66,6 +77,10 @@ struct UmmaParams {
     int *err;
     unsigned long long timeout_ns;
     int store_tma;                  // 1: stage tiles in smem, write with TMA stores (map_c)
+    int hp;                         // A_HALO over stacked images: rows per image (H + pad)
+                                    // in the packed data and in tile row space; 0 otherwise
+    // divisors of the index arithmetic; launch_umma_conv fills them from the fields above
+    FastDiv fd_co, fd_pix, fd_bpi, fd_bx, fd_hp, fd_cib, fd_kw;
 };
 
 // Returns a CUDA error code of the launch.
@@ -80,13 +95,13 @@ bool umma_tiling_compiled(const UmmaTiling &t, int in_dt);
 // -------------------------------------------------------------- other kernels
 cudaError_t launch_pack_nhwc(const void *x, void *xh, int N, int C, int HW, int Ch, int dt,
                              cudaStream_t stream);
-// Both packs in one launch when the data transpose can use 16-byte vectors
-// (else the two kernels above, back to back).
-cudaError_t launch_pack_operands(const void *x, void *xh, int N, int C, int HW, int Ch,
-                                 const void *w, void *wp, int CO, int CI, int KHKW, int cip,
-                                 int dt, cudaStream_t stream);
-cudaError_t launch_pack_weights(const void *w, void *wp, int CO, int CI, int KHKW, int cip,
-                                int dt, cudaStream_t stream);
+// Both packs in one launch.  The data goes to a per-image [Hop][Wop][Ch] grid
+// whose pixel (yo, xo) is input pixel (s*yo, s*xo), zero outside the image:
+// (H, W, 1) is the plain copy, Hop > H adds zero rows below each image, s > 1
+// subsamples.  xh must be 16-byte aligned.
+cudaError_t launch_pack_operands(const void *x, void *xh, int N, int C, int H, int W, int Hop,
+                                 int Wop, int s, int Ch, const void *w, void *wp, int CO, int CI,
+                                 int KHKW, int cip, int dt, cudaStream_t stream);
 cudaError_t launch_splitk_reduce(const float *ws, int split, long long elems, int CO, int HoWo,
                                  int epi, const float *bias, float eps, void *out, int out_dt,
                                  cudaStream_t stream);

@@ -5,9 +5,16 @@
 //                TMA box whose innermost coordinate is a channel offset (always
 //                16-byte aligned) and whose spatial coordinates may be negative
 //                (zero fill = the conv's inlined padding).
-//  pack_weights  kernel [CO][CI][KH*KW] -> [CO][KH*KW][cip]: the reduction
+//  pack_operands the same transpose into a per-image grid [Hop][Wop] whose
+//                pixel (yo, xo) takes input pixel (s*yo, s*xo), zero where that
+//                lies outside the image -- plus the kernel re-layout, in one
+//                launch.  Hop = H, Wop = W, s = 1 is the plain copy; Hop > H
+//                appends zero rows below each image (images stacked with a
+//                padding gap, read by one tensor map over all rows); s > 1
+//                keeps only the pixels a strided 1x1 conv reads.
+//  weights       kernel [CO][CI][KH*KW] -> [CO][KH*KW][cip]: the reduction
 //                order (ry, rx, ci) of the packed data, channels zero padded to
-//                whole 128-byte K blocks.
+//                whole 128-byte K blocks (part of pack_operands).
 //  splitk_reduce out = op(sum_s ws[s] + bias[f]) with the K slices added in
 //                index order (deterministic), then rounded to the output type.
 #include <algorithm>
@@ -93,14 +100,64 @@ __global__ void __launch_bounds__(256) pack_nhwc_vec_kernel(const T *__restrict_
     }
 }
 
-// Both operands in one launch: blocks [0, data_blocks) transpose data tiles
-// (as pack_nhwc_vec_kernel, tile index flattened as (pixel tile, channel tile,
-// image)); the remaining blocks re-lay out the kernel.
+// Shared memory of a pack_operands block: a data tile, or the weight buffer
+// (16 KB, so that a run of input channels x taps of one output channel fits).
+constexpr int kPackSmemBytes = 16384;
+
+// The kernel re-layout [CO][CI][KHKW] -> [CO][KHKW][cip] by blocks
+// first, first + nblocks, ...: each work item is one output channel f and a
+// run of cc input channels, whose cc * KHKW source elements are contiguous.
+// They are read coalesced into the shared buffer `buf` (cap elements) and
+// written back as KHKW runs of cc channels, zero past CI.
+template <typename T>
+__device__ __forceinline__ void pack_weight_part(const T *__restrict__ w, T *__restrict__ wp,
+                                                 int CO, int CI, int KHKW, int cip, int first,
+                                                 int nblocks, T *buf, int cap)
+{
+    int cc = cap / KHKW;
+    if (cc >= 32) cc &= ~31;
+    if (cc < 1) {   // a kernel too large for the buffer: element by element
+        const long long total = (long long)CO * KHKW * cip;
+        const long long nthreads = (long long)nblocks * blockDim.x;
+        for (long long i = (long long)first * blockDim.x + threadIdx.x; i < total; i += nthreads) {
+            const int c = (int)(i % cip);
+            const long long r = i / cip;
+            const int t = (int)(r % KHKW);
+            const int f = (int)(r / KHKW);
+            wp[i] = c < CI ? w[((size_t)f * CI + c) * KHKW + t] : T(0);
+        }
+        return;
+    }
+    const int runs = (cip + cc - 1) / cc;
+    const long long items = (long long)CO * runs;
+    for (long long it = first; it < items; it += nblocks) {
+        const int f = (int)(it / runs);
+        const int c0 = (int)(it - (long long)f * runs) * cc;
+        const int nc = min(cc, CI - c0);   // source channels in this run (may be <= 0)
+        const T *src = w + ((size_t)f * CI + c0) * KHKW;
+        const int nsrc = nc > 0 ? nc * KHKW : 0;
+        for (int i = threadIdx.x; i < nsrc; i += blockDim.x) buf[i] = __ldg(src + i);
+        __syncthreads();
+        const int wc = min(cc, cip - c0);  // destination channels in this run
+        for (int i = threadIdx.x; i < KHKW * wc; i += blockDim.x) {
+            const int t = i / wc, c = i - t * wc;
+            wp[((size_t)f * KHKW + t) * cip + c0 + c] = c < nc ? buf[c * KHKW + t] : T(0);
+        }
+        __syncthreads();
+    }
+}
+
+// Both operands in one launch: blocks [0, wblocks) re-lay out the kernel
+// (first, so that this work overlaps the data tiles), the remaining blocks
+// transpose data tiles (as pack_nhwc_vec_kernel, tile index flattened as
+// (pixel tile, channel tile, image)).  Output pixel p of an image copies input
+// pixel p when p < HWi and is zero up to HWo (the zero rows below a stacked
+// image).  wblocks = 0: no kernel re-layout.
 template <typename T>
 __global__ void __launch_bounds__(256) pack_operands_kernel(const T *__restrict__ x,
-                                                            T *__restrict__ xh, int C, int HW,
-                                                            int Ch, int ptiles, int ctiles,
-                                                            int data_blocks,
+                                                            T *__restrict__ xh, int C, int HWi,
+                                                            int HWo, int Ch, int ptiles,
+                                                            int ctiles, int wblocks,
                                                             const T *__restrict__ w,
                                                             T *__restrict__ wp, int CO, int CI,
                                                             int KHKW, int cip)
@@ -108,14 +165,21 @@ __global__ void __launch_bounds__(256) pack_operands_kernel(const T *__restrict_
     griddep_wait();
     constexpr int VEC = 16 / sizeof(T);
     constexpr int TILE = 8 * VEC;
-    __shared__ T tile[TILE][TILE + 1];
-    if ((int)blockIdx.x < data_blocks) {
-        const int t = blockIdx.x;
+    static_assert(TILE * (TILE + 1) * sizeof(T) <= kPackSmemBytes, "tile fits the buffer");
+    __shared__ __align__(16) T sbuf[kPackSmemBytes / sizeof(T)];
+    T(*tile)[TILE + 1] = reinterpret_cast<T(*)[TILE + 1]>(sbuf);
+    if ((int)blockIdx.x < wblocks) {
+        pack_weight_part(w, wp, CO, CI, KHKW, cip, (int)blockIdx.x, wblocks, sbuf,
+                         (int)(kPackSmemBytes / sizeof(T)));
+        return;
+    }
+    {
+        const int t = (int)blockIdx.x - wblocks;
         const int pt = t % ptiles, r = t / ptiles;
         const int ct = r % ctiles, n = r / ctiles;
         const int p0 = pt * TILE, c0 = ct * TILE;
-        const T *xs = x + (size_t)n * C * HW;
-        T *xd = xh + (size_t)n * HW * Ch;
+        const T *xs = x + (size_t)n * C * HWi;
+        T *xd = xh + (size_t)n * HWo * Ch;
         for (int v = threadIdx.x; v < TILE * 8; v += blockDim.x) {
             const int cr = v >> 3, pv = v & 7;
             const int c = c0 + cr, pix = p0 + pv * VEC;
@@ -124,7 +188,7 @@ __global__ void __launch_bounds__(256) pack_operands_kernel(const T *__restrict_
                 T e[VEC];
             } val;
             val.u = make_uint4(0, 0, 0, 0);
-            if (c < C && pix < HW) val.u = *reinterpret_cast<const uint4 *>(xs + (size_t)c * HW + pix);
+            if (c < C && pix < HWi) val.u = *reinterpret_cast<const uint4 *>(xs + (size_t)c * HWi + pix);
 #pragma unroll
             for (int i = 0; i < VEC; ++i) tile[cr][pv * VEC + i] = val.e[i];
         }
@@ -132,7 +196,7 @@ __global__ void __launch_bounds__(256) pack_operands_kernel(const T *__restrict_
         for (int v = threadIdx.x; v < TILE * 8; v += blockDim.x) {
             const int pr = v >> 3, cv = v & 7;
             const int pix = p0 + pr, c = c0 + cv * VEC;
-            if (pix < HW && c < Ch) {
+            if (pix < HWo && c < Ch) {
                 union {
                     uint4 u;
                     T e[VEC];
@@ -142,33 +206,74 @@ __global__ void __launch_bounds__(256) pack_operands_kernel(const T *__restrict_
                 *reinterpret_cast<uint4 *>(xd + (size_t)pix * Ch + c) = val.u;
             }
         }
-        return;
-    }
-    const long long total = (long long)CO * KHKW * cip;
-    const long long nthreads = (long long)(gridDim.x - data_blocks) * blockDim.x;
-    for (long long i = (long long)(blockIdx.x - data_blocks) * blockDim.x + threadIdx.x; i < total;
-         i += nthreads) {
-        const int c = (int)(i % cip);
-        const long long r = i / cip;
-        const int t = (int)(r % KHKW);
-        const int f = (int)(r / KHKW);
-        wp[i] = c < CI ? w[((size_t)f * CI + c) * KHKW + t] : T(0);
     }
 }
 
+// The general form: output pixel (yo, xo) of the [Hop][Wop] grid takes input
+// pixel (s*yo, s*xo), zero outside the image.  Element reads (any alignment,
+// any stride), 16-byte channel-row writes.
 template <typename T>
-__global__ void pack_weights_kernel(const T *__restrict__ w, T *__restrict__ wp, int CO, int CI,
-                                    int KHKW, int cip)
+__global__ void __launch_bounds__(256) pack_remap_kernel(const T *__restrict__ x,
+                                                         T *__restrict__ xh, int C, int H, int W,
+                                                         int Hop, int Wop, int s, int Ch,
+                                                         int ptiles, int ctiles, int wblocks,
+                                                         const T *__restrict__ w,
+                                                         T *__restrict__ wp, int CO, int CI,
+                                                         int KHKW, int cip)
 {
     griddep_wait();
-    const long long total = (long long)CO * KHKW * cip;
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-         i += (long long)gridDim.x * blockDim.x) {
-        const int c = (int)(i % cip);
-        const long long r = i / cip;
-        const int t = (int)(r % KHKW);
-        const int f = (int)(r / KHKW);
-        wp[i] = c < CI ? w[((size_t)f * CI + c) * KHKW + t] : T(0);
+    constexpr int VEC = 16 / sizeof(T);
+    constexpr int TILE = 8 * VEC;
+    static_assert(256 % TILE == 0, "a thread keeps one pixel column");
+    static_assert(TILE * (TILE + 1) * sizeof(T) <= kPackSmemBytes, "tile fits the buffer");
+    __shared__ __align__(16) T sbuf[kPackSmemBytes / sizeof(T)];
+    T(*tile)[TILE + 1] = reinterpret_cast<T(*)[TILE + 1]>(sbuf);
+    if ((int)blockIdx.x < wblocks) {
+        pack_weight_part(w, wp, CO, CI, KHKW, cip, (int)blockIdx.x, wblocks, sbuf,
+                         (int)(kPackSmemBytes / sizeof(T)));
+        return;
+    }
+    {
+        const int t = (int)blockIdx.x - wblocks;
+        const int pt = t % ptiles, r = t / ptiles;
+        const int ct = r % ctiles, n = r / ctiles;
+        const int p0 = pt * TILE, c0 = ct * TILE;
+        const long long hwi = (long long)H * W, hwo = (long long)Hop * Wop;
+        const T *xs = x + (size_t)n * C * hwi;
+        T *xd = xh + (size_t)n * hwo * Ch;
+        const int pc = threadIdx.x % TILE;
+        const long long pix = (long long)p0 + pc;
+        long long src = -1;
+        if (pix < hwo) {
+            const long long yo = pix / Wop, xo = pix - yo * Wop;
+            const long long yi = yo * s, xi = xo * s;
+            if (yi < H && xi < W) src = yi * W + xi;
+        }
+        // all of the thread's loads first, so that they are in flight together
+        constexpr int kRows = 256 / TILE, kPer = TILE / kRows;
+        T val[kPer];
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int c = c0 + threadIdx.x / TILE + k * kRows;
+            val[k] = (c < C && src >= 0) ? __ldg(xs + (size_t)c * hwi + src) : T(0);
+        }
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) tile[threadIdx.x / TILE + k * kRows][pc] = val[k];
+        __syncthreads();
+        for (int v = threadIdx.x; v < TILE * 8; v += blockDim.x) {
+            const int pr = v >> 3, cv = v & 7;
+            const long long op = (long long)p0 + pr;
+            const int c = c0 + cv * VEC;
+            if (op < hwo && c < Ch) {
+                union {
+                    uint4 u;
+                    T e[VEC];
+                } val;
+#pragma unroll
+                for (int i = 0; i < VEC; ++i) val.e[i] = tile[cv * VEC + i][pr];
+                *reinterpret_cast<uint4 *>(xd + (size_t)op * Ch + c) = val.u;
+            }
+        }
     }
 }
 
@@ -243,46 +348,54 @@ cudaError_t launch_pack_nhwc(const void *x, void *xh, int N, int C, int HW, int 
                       static_cast<const uint16_t *>(x), static_cast<uint16_t *>(xh), C, HW, Ch);
 }
 
-cudaError_t launch_pack_operands(const void *x, void *xh, int N, int C, int HW, int Ch,
-                                 const void *w, void *wp, int CO, int CI, int KHKW, int cip,
-                                 int dt, cudaStream_t stream)
+cudaError_t launch_pack_operands(const void *x, void *xh, int N, int C, int H, int W, int Hop,
+                                 int Wop, int s, int Ch, const void *w, void *wp, int CO, int CI,
+                                 int KHKW, int cip, int dt, cudaStream_t stream)
 {
     const int vec = (int)(16 / dtype_size(dt));
-    const bool aligned = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(xh)) & 15) == 0;
+    if (Ch % vec || (reinterpret_cast<uintptr_t>(xh) & 15)) return cudaErrorInvalidValue;
+    const bool aligned = (reinterpret_cast<uintptr_t>(x) & 15) == 0;
+    const long long hwi = (long long)H * W, hwo = (long long)Hop * Wop;
     const int tile = 8 * vec;
-    const long long ptiles = (HW + tile - 1) / tile, ctiles = (Ch + tile - 1) / tile;
+    const long long ptiles = (hwo + tile - 1) / tile, ctiles = (Ch + tile - 1) / tile;
     const long long data_blocks = ptiles * ctiles * N;
-    const long long wtotal = (long long)CO * KHKW * cip;
-    const long long wblocks = std::min<long long>((wtotal + 255) / 256, 1024);
-    if (!aligned || HW % vec || Ch % vec || data_blocks + wblocks > INT32_MAX) {
-        cudaError_t e = launch_pack_nhwc(x, xh, N, C, HW, Ch, dt, stream);
-        if (e != cudaSuccess) return e;
-        return launch_pack_weights(w, wp, CO, CI, KHKW, cip, dt, stream);
-    }
+    // weight blocks: one per (output channel, channel run) item of pack_weight_part;
+    // none when w is null (the conv reads the caller's kernel as it is)
+    const long long cap = kPackSmemBytes / (long long)dtype_size(dt);
+    long long cc = cap / KHKW;
+    if (cc >= 32) cc &= ~31ll;
+    const long long witems = cc >= 1 ? (long long)CO * ((cip + cc - 1) / cc)
+                                     : ((long long)CO * KHKW * cip + 255) / 256;
+    const long long wblocks = w ? std::max<long long>(1, std::min<long long>(witems, 2048)) : 0;
+    if (data_blocks + wblocks > INT32_MAX || hwo > INT32_MAX) return cudaErrorInvalidValue;
     ProfScope prof("pack_operands", stream);
     const int grid = (int)(data_blocks + wblocks);
+    // pixel p of the output is pixel p of the input (or zero below it)
+    const bool linear = s == 1 && Wop == W && Hop >= H;
+    if (linear && aligned && hwi % vec == 0 && hwo % vec == 0) {
+        if (dtype_size(dt) == 4)
+            return launch_pdl(pack_operands_kernel<uint32_t>, dim3(grid), dim3(256), 0, stream,
+                              static_cast<const uint32_t *>(x), static_cast<uint32_t *>(xh), C,
+                              (int)hwi, (int)hwo, Ch, (int)ptiles, (int)ctiles, (int)wblocks,
+                              static_cast<const uint32_t *>(w), static_cast<uint32_t *>(wp), CO, CI,
+                              KHKW, cip);
+        return launch_pdl(pack_operands_kernel<uint16_t>, dim3(grid), dim3(256), 0, stream,
+                          static_cast<const uint16_t *>(x), static_cast<uint16_t *>(xh), C,
+                          (int)hwi, (int)hwo, Ch, (int)ptiles, (int)ctiles, (int)wblocks,
+                          static_cast<const uint16_t *>(w), static_cast<uint16_t *>(wp), CO, CI,
+                          KHKW, cip);
+    }
     if (dtype_size(dt) == 4)
-        return launch_pdl(pack_operands_kernel<uint32_t>, dim3(grid), dim3(256), 0, stream,
-                          static_cast<const uint32_t *>(x), static_cast<uint32_t *>(xh), C, HW, Ch,
-                          (int)ptiles, (int)ctiles, (int)data_blocks, static_cast<const uint32_t *>(w),
-                          static_cast<uint32_t *>(wp), CO, CI, KHKW, cip);
-    return launch_pdl(pack_operands_kernel<uint16_t>, dim3(grid), dim3(256), 0, stream,
-                      static_cast<const uint16_t *>(x), static_cast<uint16_t *>(xh), C, HW, Ch,
-                      (int)ptiles, (int)ctiles, (int)data_blocks, static_cast<const uint16_t *>(w),
-                      static_cast<uint16_t *>(wp), CO, CI, KHKW, cip);
-}
-
-cudaError_t launch_pack_weights(const void *w, void *wp, int CO, int CI, int KHKW, int cip,
-                                int dt, cudaStream_t stream)
-{
-    ProfScope prof("pack_weights", stream);
-    const long long total = (long long)CO * KHKW * cip;
-    const int grid = grid_for(total, 256);
-    if (dtype_size(dt) == 4)
-        return launch_pdl(pack_weights_kernel<uint32_t>, dim3(grid), dim3(256), 0, stream,
-                          static_cast<const uint32_t *>(w), static_cast<uint32_t *>(wp), CO, CI, KHKW, cip);
-    return launch_pdl(pack_weights_kernel<uint16_t>, dim3(grid), dim3(256), 0, stream,
-                      static_cast<const uint16_t *>(w), static_cast<uint16_t *>(wp), CO, CI, KHKW, cip);
+        return launch_pdl(pack_remap_kernel<uint32_t>, dim3(grid), dim3(256), 0, stream,
+                          static_cast<const uint32_t *>(x), static_cast<uint32_t *>(xh), C, H, W,
+                          Hop, Wop, s, Ch, (int)ptiles, (int)ctiles, (int)wblocks,
+                          static_cast<const uint32_t *>(w), static_cast<uint32_t *>(wp), CO, CI,
+                          KHKW, cip);
+    return launch_pdl(pack_remap_kernel<uint16_t>, dim3(grid), dim3(256), 0, stream,
+                      static_cast<const uint16_t *>(x), static_cast<uint16_t *>(xh), C, H, W, Hop,
+                      Wop, s, Ch, (int)ptiles, (int)ctiles, (int)wblocks,
+                      static_cast<const uint16_t *>(w), static_cast<uint16_t *>(wp), CO, CI, KHKW,
+                      cip);
 }
 
 cudaError_t launch_splitk_reduce(const float *ws, int split, long long elems, int CO, int HoWo,

@@ -44,10 +44,10 @@ std::string cand_str(const Cand &c)
 {
     char b[160];
     if (c.kind == BIGEMM_KIND_UMMA)
-        snprintf(b, sizeof b, "umma:%s:bn%d:box%dx%dx%d:split%d",
+        snprintf(b, sizeof b, "umma:%s:bn%d:box%dx%dx%d:split%d%s",
                  c.t.amode == A_DIRECT ? "direct" : c.t.amode == A_HALO ? "halo" : "nhwc", c.t.bn,
-                 c.t.box_w, c.t.box_h, c.t.bpt,
-                 c.t.split);
+                 c.t.box_w, c.t.box_h, c.t.bpt, c.t.split,
+                 c.t.pack == PACK_SUB ? ":sub" : c.t.pack == PACK_STACK ? ":stack" : "");
     else if (c.simt_variant == SV_DW)
         snprintf(b, sizeof b, "simt:depthwise:rows%d", c.dw_rows);
     else
@@ -58,13 +58,17 @@ std::string cand_str(const Cand &c)
 bool parse_cand(const std::string &s, Cand &c)
 {
     int a, b, d, e, f, g;
-    char mode[16];
-    if (sscanf(s.c_str(), "umma:%15[a-z]:bn%d:box%dx%dx%d:split%d", mode, &a, &b, &d, &e, &f) == 6) {
+    char mode[16], layout[16] = "";
+    const int got = sscanf(s.c_str(), "umma:%15[a-z]:bn%d:box%dx%dx%d:split%d:%15[a-z]", mode, &a,
+                           &b, &d, &e, &f, layout);
+    if (got == 6 || got == 7) {
         c = Cand{};
         c.kind = BIGEMM_KIND_UMMA;
         c.t.amode = strcmp(mode, "direct") == 0 ? A_DIRECT
                     : strcmp(mode, "halo") == 0   ? A_HALO
                                                   : A_NHWC;
+        c.t.pack = strcmp(layout, "sub") == 0 ? PACK_SUB : strcmp(layout, "stack") == 0 ? PACK_STACK
+                                                                                       : PACK_PLAIN;
         c.t.bn = a, c.t.box_w = b, c.t.box_h = d, c.t.bpt = e, c.t.split = f;
         return true;
     }
@@ -90,6 +94,32 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 
 bool is_depthwise(const ConvShape &s) { return s.groups > 1 && s.groups == s.CI && s.CO == s.CI; }
+
+// The conv the UMMA kernel computes: with the subsampling pack, a strided 1x1
+// conv becomes a stride-1 1x1 conv over the [Ho][Wo] grid of pixels it reads.
+ConvShape kernel_shape(const ConvShape &s, const UmmaTiling &t)
+{
+    if (t.pack != PACK_SUB) return s;
+    ConvShape k = s;
+    k.H = s.Ho, k.W = s.Wo, k.stride = 1;
+    return k;
+}
+
+bool sub_ok(const ConvShape &s)
+{
+    return s.groups == 1 && s.KH == 1 && s.KW == 1 && s.pad == 0 && s.stride > 1;
+}
+
+// Rows per image in the stacked layout: at least pad zero rows below each
+// image, which serve as the bottom padding of that image and the top padding
+// of the next.  When the output rows can take TMA stores, the pitch is rounded
+// up to 4 rows so that an epilogue warp's 4 x 8 pixels lie in one image.
+int stack_pitch(const ConvShape &s, const UmmaTiling &t)
+{
+    const int ec = t.split > 1 ? 4 : (int)dtype_size(s.out_dt);
+    const int rows = s.H + s.pad;
+    return (s.Wo * ec) % 16 == 0 ? (rows + 3) / 4 * 4 : rows;
+}
 
 struct Box {
     int w, h, bpt;
@@ -133,10 +163,11 @@ struct UmmaGeom {
     bool fits;      // box and unit counts fit the kernel's 32-bit indexing
 };
 
-UmmaGeom umma_geometry(const ConvShape &s, const UmmaTiling &t, int sm_count)
+UmmaGeom umma_geometry(const ConvShape &s0, const UmmaTiling &t, int sm_count)
 {
     UmmaGeom g{};
     UmmaParams &p = g.p;
+    const ConvShape s = kernel_shape(s0, t);
     const int e = (int)dtype_size(s.in_dt);
     p.N = s.N, p.CI = s.CI, p.H = s.H, p.W = s.W, p.CO = s.CO, p.KH = s.KH, p.KW = s.KW;
     p.stride = s.stride, p.pad = s.pad, p.Ho = s.Ho, p.Wo = s.Wo;
@@ -147,6 +178,11 @@ UmmaGeom umma_geometry(const ConvShape &s, const UmmaTiling &t, int sm_count)
     if (t.amode == A_NHWC || t.amode == A_HALO) {
         p.boxes_x = (int)ceil_div(s.Wo, t.box_w);
         p.boxes_y = (int)ceil_div(s.Ho, t.box_h);
+        if (t.pack == PACK_STACK) {
+            // one tall image of N * hp rows
+            p.hp = stack_pitch(s, t);
+            p.boxes_y = (int)std::min<long long>(ceil_div((long long)s.N * p.hp, t.box_h), INT32_MAX);
+        }
         bpi = (long long)p.boxes_x * p.boxes_y;
         // halo: one K block is a channel block with every tap inside it
         p.k_blocks = (t.amode == A_HALO ? 1 : s.KH * s.KW) * p.ci_blocks;
@@ -160,7 +196,7 @@ UmmaGeom umma_geometry(const ConvShape &s, const UmmaTiling &t, int sm_count)
         g.ch = s.CI;
     }
     p.cip = g.cip;
-    const long long total = (long long)s.N * bpi;
+    const long long total = (t.pack == PACK_STACK ? 1 : (long long)s.N) * bpi;
     const long long ptiles = ceil_div(total, t.bpt);
     p.co_tiles = (int)ceil_div(s.CO, t.bn);
     p.kb_per_split = (int)ceil_div(p.k_blocks, t.split);
@@ -179,12 +215,23 @@ UmmaGeom umma_geometry(const ConvShape &s, const UmmaTiling &t, int sm_count)
 }
 
 // Host-side validity of a UMMA tiling for a shape; reason on failure.
-bool umma_valid(const ConvShape &s, const UmmaTiling &t, int sm_count, std::string *why)
+bool umma_valid(const ConvShape &s0, const UmmaTiling &t, int sm_count, std::string *why)
 {
     auto bad = [&](const char *m) {
         if (why) *why = m;
         return false;
     };
+    if (t.pack == PACK_SUB) {
+        if (t.amode != A_NHWC) return bad("the subsampling pack feeds the nhwc mode");
+        if (!sub_ok(s0)) return bad("the subsampling pack needs a strided 1x1 conv without padding");
+    } else if (t.pack == PACK_STACK) {
+        if (t.amode != A_HALO) return bad("stacked images feed the halo mode");
+        if (s0.Ho > s0.H + s0.pad) return bad("stacking needs pad <= KH - 1");
+        if ((long long)s0.N * stack_pitch(s0, t) + 16 >= (1ll << 31)) return bad("stacked rows exceed 2^31");
+    } else if (t.pack != PACK_PLAIN) {
+        return bad("unknown pack layout");
+    }
+    const ConvShape s = kernel_shape(s0, t);
     const size_t e = dtype_size(s.in_dt);
     if (s.groups != 1) return bad("grouped conv");
     if (t.bn != 64 && t.bn != 128 && t.bn != 256) return bad("tile_n not 64/128/256");
@@ -213,7 +260,7 @@ bool umma_valid(const ConvShape &s, const UmmaTiling &t, int sm_count, std::stri
     }
     if (t.bpt > 16) return bad("more than 16 boxes per tile");
     if (umma_smem_bytes(t) == 0) return bad("no compiled kernel");
-    if (!umma_geometry(s, t, 1).fits) return bad("more than 2^31 boxes or work units");
+    if (!umma_geometry(s0, t, 1).fits) return bad("more than 2^31 boxes or work units");
     DeviceState *ds = device_state();
     if (ds && (int)umma_smem_bytes(t) > ds->max_smem_optin) return bad("smem exceeds opt-in limit");
     (void)sm_count;
@@ -243,6 +290,7 @@ struct bigemm_plan_s {
     const void *map_c_src = nullptr;                         // output pointer encoded in map_c
     bool store_tma = false;
     bool maps_ready = false;
+    bool raw_b = false;        // 1x1 nhwc mode: map_b reads the caller's kernel [CO][CI] as is
     std::string search_log;
     std::string chosen_by = "heuristic";
 };
@@ -300,10 +348,11 @@ int heuristic_split(const ConvShape &s, UmmaTiling t, int sms)
     return (int)std::max<long long>(1, want);
 }
 
-UmmaTiling default_tiling(const ConvShape &s, int amode, int bn, int sms)
+UmmaTiling default_tiling(const ConvShape &s, int amode, int bn, int sms, int pack = PACK_PLAIN)
 {
     UmmaTiling t{};
     t.amode = amode;
+    t.pack = pack;
     t.bn = bn;
     t.stages = 0;
     if (amode == A_DIRECT) {
@@ -313,7 +362,7 @@ UmmaTiling default_tiling(const ConvShape &s, int amode, int bn, int sms)
     } else if (amode == A_HALO) {
         t.box_w = 8, t.box_h = 16, t.bpt = 1;
     } else {
-        const Box b = box_options(s).front();
+        const Box b = box_options(kernel_shape(s, t)).front();
         t.box_w = b.w, t.box_h = b.h, t.bpt = b.bpt;
     }
     t.split = 1;
@@ -328,18 +377,33 @@ int default_bn(const ConvShape &s)
     return (s.CO % 256 == 0) ? 256 : 128;
 }
 
-// Halo tiles cover 8 x 16 output pixels; worth it when they are mostly inside
-// the image.
-bool halo_ok(const ConvShape &s)
+// Fraction of the halo tiles' 16 x 8 output pixels that lie inside the
+// output, per image or with the images stacked; 0 when the layout does not
+// apply.
+double halo_cover(const ConvShape &s, int pack)
 {
     UmmaTiling t{};
     t.amode = A_HALO;
+    t.pack = pack;
     t.bn = 64;
     t.box_w = 8, t.box_h = 16, t.bpt = 1;
     t.split = 1;
-    if (!umma_valid(s, t, 1, nullptr)) return false;
-    const double cover = (double)ceil_div(s.Ho, 16) * 16 * ceil_div(s.Wo, 8) * 8;
-    return (double)s.Ho * s.Wo / cover >= 0.7;
+    if (!umma_valid(s, t, 1, nullptr)) return 0.0;
+    const double rows = pack == PACK_STACK ? (double)ceil_div((long long)s.N * stack_pitch(s, t), 16) * 16
+                                           : (double)s.N * ceil_div(s.Ho, 16) * 16;
+    return (double)s.N * s.Ho * s.Wo / (rows * ceil_div(s.Wo, 8) * 8);
+}
+
+// Halo tiles are worth it when they are mostly inside the output.
+bool halo_ok(const ConvShape &s)
+{
+    return std::max(halo_cover(s, PACK_PLAIN), halo_cover(s, PACK_STACK)) >= 0.7;
+}
+
+// The better halo layout for a shape: stacking when it covers clearly more.
+int halo_pack(const ConvShape &s)
+{
+    return halo_cover(s, PACK_STACK) > halo_cover(s, PACK_PLAIN) + 0.02 ? PACK_STACK : PACK_PLAIN;
 }
 
 bool direct_ok(const ConvShape &s)
@@ -368,8 +432,14 @@ Cand heuristic(const ConvShape &s, int sms)
     if (kdim >= 32) {
         Cand u;
         u.kind = BIGEMM_KIND_UMMA;
-        u.t = default_tiling(s, direct_ok(s) ? A_DIRECT : halo_ok(s) ? A_HALO : A_NHWC,
-                             default_bn(s), sms);
+        if (direct_ok(s))
+            u.t = default_tiling(s, A_DIRECT, default_bn(s), sms);
+        else if (sub_ok(s))
+            u.t = default_tiling(s, A_NHWC, default_bn(s), sms, PACK_SUB);
+        else if (halo_ok(s))
+            u.t = default_tiling(s, A_HALO, default_bn(s), sms, halo_pack(s));
+        else
+            u.t = default_tiling(s, A_NHWC, default_bn(s), sms);
         if (umma_valid(s, u.t, sms, nullptr)) return u;
     }
     c.simt_variant = SV_TILED;
@@ -393,12 +463,18 @@ std::vector<Cand> candidates(const ConvShape &s, int sms)
         v.push_back(Cand{});
         return v;
     }
-    std::vector<int> modes;
-    if (direct_ok(s)) modes.push_back(A_DIRECT);
-    if (halo_ok(s)) modes.push_back(A_HALO);
-    modes.push_back(A_NHWC);
-    std::vector<Box> boxes = box_options(s);
-    for (int amode : modes) {
+    std::vector<std::pair<int, int>> modes;   // (A mode, pack layout)
+    if (direct_ok(s)) modes.push_back({A_DIRECT, PACK_PLAIN});
+    const double hc_plain = halo_cover(s, PACK_PLAIN), hc_stack = halo_cover(s, PACK_STACK);
+    if (hc_plain >= 0.7) modes.push_back({A_HALO, PACK_PLAIN});
+    if (hc_stack >= 0.7 && hc_stack > hc_plain + 0.02) modes.push_back({A_HALO, PACK_STACK});
+    if (sub_ok(s)) modes.push_back({A_NHWC, PACK_SUB});
+    modes.push_back({A_NHWC, PACK_PLAIN});
+    for (const auto &mp : modes) {
+        const int amode = mp.first, pack = mp.second;
+        UmmaTiling probe{};
+        probe.pack = pack;
+        const std::vector<Box> boxes = box_options(kernel_shape(s, probe));
         std::vector<std::pair<int, int>> bx;   // (w,h) with bpt
         std::vector<int> bpts;
         if (amode == A_DIRECT) {
@@ -414,12 +490,26 @@ std::vector<Cand> candidates(const ConvShape &s, int sms)
                 bx.push_back({boxes[i].w, boxes[i].h});
                 bpts.push_back(boxes[i].bpt);
             }
+            // Output rows that TMA cannot store are written by the lanes
+            // directly; boxes spanning whole output rows keep a warp's 32
+            // pixels contiguous in each channel plane.
+            const ConvShape ks = kernel_shape(s, probe);
+            if ((ks.Wo * (long long)dtype_size(s.out_dt)) % 16 != 0) {
+                for (const Box &b : boxes)
+                    if (b.w == ks.Wo &&
+                        std::find(bx.begin(), bx.end(), std::make_pair(b.w, b.h)) == bx.end()) {
+                        bx.push_back({b.w, b.h});
+                        bpts.push_back(b.bpt);
+                        break;
+                    }
+            }
         }
         for (size_t bi = 0; bi < bx.size(); ++bi)
             for (int bn : {64, 128, 256}) {
                 if (bn > 64 && bn / 2 >= s.CO) continue;   // a smaller tile covers CO
                 UmmaTiling t{};
-                t.amode = amode, t.bn = bn, t.box_w = bx[bi].first, t.box_h = bx[bi].second;
+                t.amode = amode, t.pack = pack, t.bn = bn, t.box_w = bx[bi].first,
+                t.box_h = bx[bi].second;
                 t.bpt = bpts[bi];
                 t.split = 1;
                 const UmmaGeom g = umma_geometry(s, t, sms);
@@ -451,6 +541,8 @@ bool store_tma_ok(const ConvShape &s, const UmmaTiling &t, int split)
     const bool wide = t.box_w % 32 == 0;
     if (!wide && !(32 % t.box_w == 0 && (t.box_w * t.box_h) % 32 == 0)) return false;
     if (t.amode == A_DIRECT) return ((long long)s.Ho * s.Wo * ec) % 16 == 0;
+    // stacked images: a warp's rows (32 / box_w of them) must not straddle two images
+    if (t.pack == PACK_STACK && (wide || stack_pitch(s, t) % (32 / t.box_w))) return false;
     return ((long long)s.Wo * ec) % 16 == 0;
 }
 
@@ -499,14 +591,18 @@ bigemm_status setup_plan(bigemm_plan_s *p)
     const size_t e = dtype_size(s.in_dt);
     if (t.amode == A_HALO) {
         // channels-last data read as one halo box per channel block: 16 pixels
-        // wide (the 2 KB smem row pitch), 16 + KH - 1 rows high
-        p->xh_bytes = (size_t)s.N * s.H * s.W * p->g.ch * e;
+        // wide (the 2 KB smem row pitch), 16 + KH - 1 rows high.  Stacked: one
+        // image of N * (H + pad) rows.
+        const bool stack = t.pack == PACK_STACK;
+        const uint64_t rows = stack ? (uint64_t)s.N * p->g.p.hp : (uint64_t)s.H;
+        const uint64_t imgs = stack ? 1u : (uint64_t)s.N;
+        p->xh_bytes = (size_t)(imgs * rows) * s.W * p->g.ch * e;
         p->wp_bytes = (size_t)s.CO * s.KH * s.KW * p->g.cip * e;
         if (cudaMalloc(&p->xh, p->xh_bytes) != cudaSuccess) return BIGEMM_ERR_CUDA;
         if (cudaMalloc(&p->wp, p->wp_bytes) != cudaSuccess) return BIGEMM_ERR_CUDA;
-        const uint64_t dims[4] = {(uint64_t)p->g.ch, (uint64_t)s.W, (uint64_t)s.H, (uint64_t)s.N};
+        const uint64_t dims[4] = {(uint64_t)p->g.ch, (uint64_t)s.W, rows, imgs};
         const uint64_t str[3] = {p->g.ch * e, (uint64_t)s.W * p->g.ch * e,
-                                 (uint64_t)s.H * s.W * p->g.ch * e};
+                                 rows * s.W * p->g.ch * e};
         const uint32_t box[4] = {(uint32_t)p->g.p.bk, 16u, (uint32_t)(16 + s.KH - 1), 1u};
         const uint32_t es[4] = {1u, 1u, 1u, 1u};
         if (!encode_tiled(&p->map_a, tma_dt(s.in_dt), 4, p->xh, dims, str, box, es,
@@ -525,27 +621,33 @@ bigemm_status setup_plan(bigemm_plan_s *p)
             return BIGEMM_ERR_UNSUPPORTED;
         p->maps_ready = true;
     } else if (t.amode == A_NHWC) {
-        p->xh_bytes = (size_t)s.N * s.H * s.W * p->g.ch * e;
-        p->wp_bytes = (size_t)s.CO * s.KH * s.KW * p->g.cip * e;
+        // the subsampling pack hands the kernel a stride-1 1x1 conv over [Ho][Wo]
+        const ConvShape k = kernel_shape(s, t);
+        // a 1x1 kernel [CO][CI] is already the K-major B operand
+        p->raw_b = k.KH * k.KW == 1 && (k.CI * e) % 16 == 0;
+        p->xh_bytes = (size_t)k.N * k.H * k.W * p->g.ch * e;
+        p->wp_bytes = p->raw_b ? 0 : (size_t)k.CO * k.KH * k.KW * p->g.cip * e;
         if (cudaMalloc(&p->xh, p->xh_bytes) != cudaSuccess) return BIGEMM_ERR_CUDA;
-        if (cudaMalloc(&p->wp, p->wp_bytes) != cudaSuccess) return BIGEMM_ERR_CUDA;
-        const uint64_t dims[4] = {(uint64_t)p->g.ch, (uint64_t)s.W, (uint64_t)s.H, (uint64_t)s.N};
-        const uint64_t str[3] = {p->g.ch * e, (uint64_t)s.W * p->g.ch * e,
-                                 (uint64_t)s.H * s.W * p->g.ch * e};
-        const uint32_t box[4] = {(uint32_t)p->g.p.bk, (uint32_t)(t.box_w * s.stride),
-                                 (uint32_t)(t.box_h * s.stride), 1u};
-        const uint32_t es[4] = {1u, (uint32_t)s.stride, (uint32_t)s.stride, 1u};
+        if (!p->raw_b && cudaMalloc(&p->wp, p->wp_bytes) != cudaSuccess) return BIGEMM_ERR_CUDA;
+        const uint64_t dims[4] = {(uint64_t)p->g.ch, (uint64_t)k.W, (uint64_t)k.H, (uint64_t)k.N};
+        const uint64_t str[3] = {p->g.ch * e, (uint64_t)k.W * p->g.ch * e,
+                                 (uint64_t)k.H * k.W * p->g.ch * e};
+        const uint32_t box[4] = {(uint32_t)p->g.p.bk, (uint32_t)(t.box_w * k.stride),
+                                 (uint32_t)(t.box_h * k.stride), 1u};
+        const uint32_t es[4] = {1u, (uint32_t)k.stride, (uint32_t)k.stride, 1u};
         if (!encode_tiled(&p->map_a, tma_dt(s.in_dt), 4, p->xh, dims, str, box, es,
                           CU_TENSOR_MAP_SWIZZLE_128B))
             return BIGEMM_ERR_UNSUPPORTED;
-        const uint64_t kt = (uint64_t)s.KH * s.KW * p->g.cip;
-        const uint64_t bd[2] = {kt, (uint64_t)s.CO};
-        const uint64_t bs[1] = {kt * e};
-        const uint32_t bb[2] = {(uint32_t)p->g.p.bk, (uint32_t)t.bn};
-        const uint32_t bes[2] = {1u, 1u};
-        if (!encode_tiled(&p->map_b, tma_dt(s.in_dt), 2, p->wp, bd, bs, bb, bes,
-                          CU_TENSOR_MAP_SWIZZLE_128B))
-            return BIGEMM_ERR_UNSUPPORTED;
+        if (!p->raw_b) {
+            const uint64_t kt = (uint64_t)k.KH * k.KW * p->g.cip;
+            const uint64_t bd[2] = {kt, (uint64_t)k.CO};
+            const uint64_t bs[1] = {kt * e};
+            const uint32_t bb[2] = {(uint32_t)p->g.p.bk, (uint32_t)t.bn};
+            const uint32_t bes[2] = {1u, 1u};
+            if (!encode_tiled(&p->map_b, tma_dt(s.in_dt), 2, p->wp, bd, bs, bb, bes,
+                              CU_TENSOR_MAP_SWIZZLE_128B))
+                return BIGEMM_ERR_UNSUPPORTED;
+        }
         p->maps_ready = true;
     }
     if (p->g.p.split > 1) {
@@ -587,6 +689,24 @@ bigemm_status encode_direct_maps(bigemm_plan_s *p, const void *data, const void 
     return BIGEMM_OK;
 }
 
+// The raw-kernel B map of a 1x1 nhwc plan, re-encoded when the kernel pointer
+// changes: [CO][CI] with channel blocks past CI zero-filled by the copy.
+bigemm_status encode_raw_b(bigemm_plan_s *p, const void *kernel)
+{
+    if (p->map_b_src == kernel) return BIGEMM_OK;
+    const ConvShape &s = p->s;
+    const size_t e = dtype_size(s.in_dt);
+    const uint64_t bd[2] = {(uint64_t)s.CI, (uint64_t)s.CO};
+    const uint64_t bs[1] = {(uint64_t)s.CI * e};
+    const uint32_t bb[2] = {(uint32_t)p->g.p.bk, (uint32_t)p->c.t.bn};
+    const uint32_t bes[2] = {1u, 1u};
+    if (!encode_tiled(&p->map_b, tma_dt(s.in_dt), 2, kernel, bd, bs, bb, bes,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
+        return BIGEMM_ERR_INVALID_ARG;
+    p->map_b_src = kernel;
+    return BIGEMM_OK;
+}
+
 int launches_per_run(const bigemm_plan_s *p)
 {
     if (p->c.kind != BIGEMM_KIND_UMMA) return 1;
@@ -621,8 +741,16 @@ bigemm_status run_plan(bigemm_plan_s *p, const void *data, const void *kernel, c
     up.err = ds->err;
     up.timeout_ns = wait_timeout_ns();
     if (p->c.t.amode != A_DIRECT) {
-        e = launch_pack_operands(data, p->xh, s.N, s.CI, s.H * s.W, p->g.ch, kernel, p->wp, s.CO,
-                                 s.CI, s.KH * s.KW, p->g.cip, s.in_dt, st);
+        const int pk = p->c.t.pack;
+        const int hop = pk == PACK_SUB ? s.Ho : pk == PACK_STACK ? up.hp : s.H;
+        const int wop = pk == PACK_SUB ? s.Wo : s.W;
+        if (p->raw_b) {
+            bigemm_status r = encode_raw_b(p, kernel);
+            if (r != BIGEMM_OK) return r;
+        }
+        e = launch_pack_operands(data, p->xh, s.N, s.CI, s.H, s.W, hop, wop,
+                                 pk == PACK_SUB ? s.stride : 1, p->g.ch, p->raw_b ? nullptr : kernel,
+                                 p->wp, s.CO, s.CI, s.KH * s.KW, p->g.cip, s.in_dt, st);
         if (e != cudaSuccess) return BIGEMM_ERR_CUDA;
     } else {
         bigemm_status r = encode_direct_maps(p, data, kernel);
@@ -873,14 +1001,22 @@ bigemm_status plan_impl(int N, int H, int W, int CO, int CI, int KH, int KW, int
             }
         } else {
             c.kind = BIGEMM_KIND_UMMA;
-            const int amode = opts->mode == 1 ? A_NHWC
-                              : opts->mode == 2 ? A_DIRECT
-                              : opts->mode == 3 ? A_HALO
-                              : (opts->box_w && opts->box_h) ? A_NHWC
-                              : direct_ok(s)                ? A_DIRECT
-                              : halo_ok(s)                  ? A_HALO
-                                                            : A_NHWC;
-            c.t = default_tiling(s, amode, opts->tile_n ? opts->tile_n : default_bn(s), sms);
+            if (opts->mode < 0 || opts->mode > 5) return BIGEMM_ERR_INVALID_ARG;
+            const int amode = (opts->mode == 1 || opts->mode == 4) ? A_NHWC
+                              : opts->mode == 2                    ? A_DIRECT
+                              : (opts->mode == 3 || opts->mode == 5) ? A_HALO
+                              : (opts->box_w && opts->box_h)         ? A_NHWC
+                              : direct_ok(s)                         ? A_DIRECT
+                              : sub_ok(s)                            ? A_NHWC
+                              : halo_ok(s)                           ? A_HALO
+                                                                     : A_NHWC;
+            const int pack = opts->mode == 4   ? PACK_SUB
+                             : opts->mode == 5 ? PACK_STACK
+                             : opts->mode != 0 ? PACK_PLAIN
+                             : amode == A_NHWC && sub_ok(s) && !(opts->box_w && opts->box_h) ? PACK_SUB
+                             : amode == A_HALO ? halo_pack(s)
+                                               : PACK_PLAIN;
+            c.t = default_tiling(s, amode, opts->tile_n ? opts->tile_n : default_bn(s), sms, pack);
             if (opts->box_w && opts->box_h) {
                 c.t.box_w = opts->box_w, c.t.box_h = opts->box_h;
                 c.t.bpt = std::max(1, 128 / (opts->box_w * opts->box_h));
@@ -984,6 +1120,8 @@ bigemm_status conv2d_nchw_plan_describe(bigemm_plan plan, char *buf, size_t len)
         const UmmaParams &p = plan->g.p;
         os << ", \"amode\": \""
            << (c.t.amode == A_DIRECT ? "direct" : c.t.amode == A_HALO ? "halo" : "nhwc")
+           << "\", \"pack\": \""
+           << (c.t.pack == PACK_SUB ? "sub" : c.t.pack == PACK_STACK ? "stack" : "plain")
            << "\", \"bn\": " << c.t.bn
            << ", \"box\": [" << c.t.box_w << ", " << c.t.box_h << ", " << c.t.bpt << "]"
            << ", \"split\": " << p.split << ", \"k_blocks\": " << p.k_blocks

@@ -10,15 +10,18 @@
 // shifted (possibly negative) coordinates and fills out-of-range elements
 // with zeros, which is the tutorial's inlined padding done by the copy engine.
 //
-// Structure (one persistent CTA per SM, 6 warps):
+// Structure (one persistent CTA per SM, 10 warps):
 //   warp 0    TMA producer: for each K block loads the A box(es) and the B tile
 //             into a STAGES-deep shared-memory ring (mbarrier full/empty).
 //   warp 1    allocates TMEM, and one lane issues tcgen05.mma (4 per K block,
 //             128-byte swizzled operands) into one of two TMEM accumulators.
-//   warps 2-5 epilogue: tcgen05.ld the accumulator (lane = pixel), apply the
-//             fused per-channel epilogue op(acc + bias[f]) and store NCHW; for
-//             a fixed channel the 32 lanes of a warp write 32 neighbouring
-//             pixels, so stores coalesce without a shared-memory transpose.
+//   warps 2-9 epilogue, two warps per TMEM lane quadrant (a warp may only
+//             read the 32 lanes of quadrant warp % 4), each taking every other
+//             32-channel chunk: tcgen05.ld the accumulator (lane = pixel),
+//             apply the fused per-channel epilogue op(acc + bias[f]) and store
+//             NCHW, through a TMA tensor store of a staged 32 x 32 box or, where
+//             TMA cannot address the output rows, directly: for a fixed
+//             channel the 32 lanes of a warp write 32 neighbouring pixels.
 // The two accumulators let the epilogue of one tile overlap the MMAs of the
 // next.  Split-K writes fp32 partial sums to a workspace instead; a separate
 // kernel adds them in a fixed order and applies the epilogue.
@@ -32,7 +35,8 @@ namespace bigemm {
 
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;                  // producer, MMA, 8 epilogue warps
+constexpr int kEpiWarps = 8;
 constexpr int kTileM = 128;
 constexpr int kRowBytes = 128;                  // one K block: a 128-byte swizzle row
 constexpr int kABytes = kTileM * kRowBytes;     // 16 KB of A per stage
@@ -42,8 +46,7 @@ struct Cfg {
     static constexpr int stages = BN <= 64 ? 8 : (BN <= 128 ? 6 : 4);
     static constexpr int b_bytes = BN * kRowBytes;
     static constexpr int ring = stages * (kABytes + b_bytes);
-    static constexpr int stage_buf = 16384;                  // one staged 32-channel output chunk
-    static constexpr int staging = 2 * stage_buf;
+    static constexpr int staging = kEpiWarps * 4096;          // 4 KB output staging per epilogue warp
     static constexpr int bars = (2 * stages + 5) * 8;
     static constexpr int smem = ring + staging + bars + 16 + 16 + 1024;   // + alignment slack
     static constexpr uint32_t tmem_cols = (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
@@ -57,10 +60,11 @@ struct Unit {
 __device__ __forceinline__ Unit decode(const UmmaParams &p, int u)
 {
     Unit w;
-    const int r = u / p.co_tiles;
-    w.ct = u - r * p.co_tiles;
-    w.sp = r / p.pix_tiles;
-    w.pt = r - w.sp * p.pix_tiles;
+    uint32_t rem;
+    const int r = (int)fd_divmod((uint32_t)u, p.fd_co, &rem);
+    w.ct = (int)rem;
+    w.sp = (int)fd_divmod((uint32_t)r, p.fd_pix, &rem);
+    w.pt = (int)rem;
     w.kb0 = w.sp * p.kb_per_split;
     w.kb1 = min(p.k_blocks, w.kb0 + p.kb_per_split);
     return w;
@@ -68,9 +72,38 @@ __device__ __forceinline__ Unit decode(const UmmaParams &p, int u)
 
 constexpr int kMaxBoxes = 16;   // boxes per tile: 128 rows / at least 8 pixels per box (< 32 lanes)
 
-// Epilogue of one warp (warps 2..5 of the block).  BOXED: the tile's pixels
-// are 2-D boxes (box_w x box_h) of one image; otherwise runs of box_w
-// consecutive flattened pixels (the direct mode).
+// Two floats rounded to nearest-even 16-bit values (fp16 or bf16), a in the
+// low half: one packed conversion instruction for the pair.
+__device__ __forceinline__ uint32_t pack2_16(float a, float b, bool f16)
+{
+    if (f16) {
+        const __half2 h = __floats2half2_rn(a, b);
+        return *reinterpret_cast<const uint32_t *>(&h);
+    }
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// tcgen05.wait::ld that also names the loaded registers, so that no use of
+// them can be scheduled above the wait.
+__device__ __forceinline__ void tmem_wait_ld_regs(uint32_t (&r)[32])
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
+                   "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                   "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                   "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
+}
+
+// Epilogue of one warp (warps 2..9 of the block: two warps per TMEM lane
+// quadrant, each taking every other 32-channel chunk of the accumulator).
+// BOXED: the tile's pixels are 2-D boxes (box_w x box_h) of one image (or of
+// the stacked images); otherwise runs of box_w consecutive flattened pixels
+// (the direct mode).
 template <int BN, bool BOXED>
 __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtensorMap *map_c,
                                               uint32_t tmem_base, uint64_t *tfull,
@@ -78,79 +111,102 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
                                               volatile int *abort_flag, int warp, int lane,
                                               int box_px)
 {
-    // Each warp owns TMEM lanes 32q..32q+31 (32 pixels of the tile) and
-    // works alone: lane 0 waits for the accumulator and shares the outcome,
-    // so the warp stays converged.  With TMA stores the warp stages its
-    // 32 pixels x 32 channels in its own shared buffers and lane 0 writes
-    // them as one box.
+    // The warp owns TMEM lanes 32q..32q+31 (32 pixels of the tile) and the
+    // chunks h, h+2, ... of the BN accumulator columns.  Lane 0 waits for the
+    // accumulator and shares the outcome, so the warp stays converged.  The
+    // load of the warp's next chunk is issued before the current one is
+    // processed.  With TMA stores the warp stages its 32 pixels x 32 channels
+    // in its own 4 KB of shared memory and lane 0 writes them as one box.
+    constexpr int kChunks = BN / 32;            // 2, 4 or 8
+    constexpr int kMine = kChunks / 2;          // chunks per warp
     const int q = warp & 3;                     // TMEM lane quadrant of this warp
+    const int h = (warp - 2) >> 2;              // which half of the chunks
     const int row = q * 32 + lane;              // tile row = pixel
     const int bi = row / box_px, bj = row - bi * box_px;
     const int wbi = (q * 32) / box_px;          // the warp's box
     const int wj0 = (q * 32) - wbi * box_px;    // its first pixel in the box
+    const int bj_y = bj / p.box_w, bj_x = bj - bj_y * p.box_w;
+    const int wj0_y = wj0 / p.box_w, wj0_x = wj0 - wj0_y * p.box_w;
     const long long howo = (long long)p.Ho * p.Wo;
     const int ec = p.ws ? 4 : (p.out_dt == BIGEMM_F32 ? 4 : 2);
-    uint8_t *wstage = stage_out + q * 8192;     // 2 x 4 KB per warp
-    int acc = 0, chunk = 0;
+    uint8_t *wstage = stage_out + (warp - 2) * 4096;
+    const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16);
+    int acc = 0;
     uint32_t acc_phase = 0;
     for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
         const Unit w = decode(p, u);
-        int okw = 0;
-        if (lane == 0) okw = mbar_wait(&tfull[acc], acc_phase, p.timeout_ns, abort_flag, p.err);
-        if (!__shfl_sync(0xffffffffu, okw, 0)) break;
-        tc_fence_after();
+        // where this lane's pixel and this warp's store box go: computed
+        // before the accumulator is ready
         const int b = w.pt * p.bpt + bi;
         bool valid = bi < p.bpt && b < p.total_boxes;
-        long long base = 0, base_out = 0;
+        long long base = 0;
         if (valid) {
-            const int n = b / p.boxes_per_img;
-            const int rem = b - n * p.boxes_per_img;
+            uint32_t urem;
+            int n = (int)fd_divmod((uint32_t)b, p.fd_bpi, &urem);
+            const int rem = (int)urem;
             long long pix;
             if (BOXED) {
-                const int byi = rem / p.boxes_x, bxi = rem - byi * p.boxes_x;
-                const int y = byi * p.box_h + bj / p.box_w;
-                const int x = bxi * p.box_w + bj % p.box_w;
-                valid = y < p.Ho && x < p.Wo;
+                const int byi = (int)fd_divmod((uint32_t)rem, p.fd_bx, &urem), bxi = (int)urem;
+                int y = byi * p.box_h + bj_y;
+                const int x = bxi * p.box_w + bj_x;
+                if (p.hp) {                     // stacked images: row -> (image, row)
+                    n = (int)fd_divmod((uint32_t)y, p.fd_hp, &urem);
+                    y = (int)urem;
+                }
+                valid = n < p.N && y < p.Ho && x < p.Wo;
                 pix = (long long)y * p.Wo + x;
             } else {
                 pix = (long long)rem * p.box_w + bj;
                 valid = pix < howo;
             }
-            base_out = (long long)n * p.CO * howo + pix;
-            base = (long long)w.sp * p.out_elems + base_out;
+            base = (long long)w.sp * p.out_elems + (long long)n * p.CO * howo + pix;
         }
         // the warp's store box (TMA mode): origin and image index
         const int wb = w.pt * p.bpt + wbi;
         const bool wbox = p.store_tma && wbi < p.bpt && wb < p.total_boxes;
         int sx = 0, sy = 0, sn = 0;
         if (wbox) {
-            const int n = wb / p.boxes_per_img;
-            const int rem = wb - n * p.boxes_per_img;
-            sn = w.sp * p.N + n;
+            uint32_t urem;
+            int n = (int)fd_divmod((uint32_t)wb, p.fd_bpi, &urem);
+            const int rem = (int)urem;
             if (BOXED) {
-                const int byi = rem / p.boxes_x, bxi = rem - byi * p.boxes_x;
-                sx = bxi * p.box_w + wj0 % p.box_w;
-                sy = byi * p.box_h + wj0 / p.box_w;
+                const int byi = (int)fd_divmod((uint32_t)rem, p.fd_bx, &urem), bxi = (int)urem;
+                sx = bxi * p.box_w + wj0_x;
+                sy = byi * p.box_h + wj0_y;
+                if (p.hp) {                     // the warp's rows lie in one image (hp % rows == 0)
+                    n = (int)fd_divmod((uint32_t)sy, p.fd_hp, &urem);
+                    sy = (int)urem;
+                }
             } else {
                 sx = rem * p.box_w + wj0;
             }
+            sn = w.sp * p.N + n;
         }
+        const bool wstore = wbox && sn < (w.sp + 1) * p.N;
+        int okw = 0;
+        if (lane == 0) okw = mbar_wait(&tfull[acc], acc_phase, p.timeout_ns, abort_flag, p.err);
+        if (!__shfl_sync(0xffffffffu, okw, 0)) break;
+        tc_fence_after();
+        const uint32_t acc_col = lane_base + (uint32_t)(acc * BN);
+        uint32_t ra[32], rb[32];
+        tmem_ld_32x32b_x32(acc_col + (uint32_t)(h * 32), ra);
         const int co0 = w.ct * BN;
-#pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 32, ++chunk) {
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + c0),
-                               r);
-            tmem_wait_ld();
-            if (c0 + 32 >= BN) {                // accumulator drained: hand it back
+#pragma unroll
+        for (int i = 0; i < kMine; ++i) {
+            uint32_t(&cur)[32] = (i & 1) ? rb : ra;
+            uint32_t(&nxt)[32] = (i & 1) ? ra : rb;
+            tmem_wait_ld_regs(cur);
+            if (i + 1 < kMine) {
+                tmem_ld_32x32b_x32(acc_col + (uint32_t)((h + 2 * (i + 1)) * 32), nxt);
+            } else {                            // accumulator drained by this warp: hand it back
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&tempty[acc]);
             }
-            const int cb = co0 + c0;
+            const int cb = co0 + (h + 2 * i) * 32;
             float v[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+            for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(cur[j]);
             if (!p.ws && p.epi != BIGEMM_EPI_NONE) {
                 float bv[32];
 #pragma unroll
@@ -166,30 +222,29 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
                     for (int j = 0; j < 32; ++j) v[j] = rsqrtf(v[j] + bv[j] + p.eps);
                 }
             }
-            if (wbox) {
-                uint8_t *buf = wstage + (chunk & 1) * 4096;
-                if (lane == 0) bulk_wait_read<1>();   // the store that used buf has read it
+            if (wstore) {
+                if (lane == 0) bulk_wait_read<0>();   // the previous store has read the buffer
                 __syncwarp();
-                uint8_t *dst = buf + lane * ec;
+                uint8_t *dst = wstage + lane * ec;
                 if (ec == 4) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) *reinterpret_cast<float *>(dst + j * 128) = v[j];
-                } else if (p.out_dt == BIGEMM_F16) {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        *reinterpret_cast<__half *>(dst + j * 64) = __float2half_rn(v[j]);
                 } else {
+                    // two channels per conversion (cvt.rn.{f16,bf16}x2.f32), one per 16-bit store
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        *reinterpret_cast<__nv_bfloat16 *>(dst + j * 64) = __float2bfloat16_rn(v[j]);
+                    for (int j = 0; j < 32; j += 2) {
+                        const uint32_t pk = pack2_16(v[j], v[j + 1], p.out_dt == BIGEMM_F16);
+                        *reinterpret_cast<uint16_t *>(dst + j * 64) = (uint16_t)(pk & 0xFFFFu);
+                        *reinterpret_cast<uint16_t *>(dst + (j + 1) * 64) = (uint16_t)(pk >> 16);
+                    }
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
                     if (BOXED)
-                        tma_store_4d(map_c, buf, sx, sy, cb, sn);
+                        tma_store_4d(map_c, wstage, sx, sy, cb, sn);
                     else
-                        tma_store_3d(map_c, buf, sx, cb, sn);
+                        tma_store_3d(map_c, wstage, sx, cb, sn);
                     bulk_commit();
                 }
             } else if (!p.store_tma && valid) {
@@ -205,16 +260,15 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
                         if (j < jn) o[j * howo] = v[j];
-                } else if (p.out_dt == BIGEMM_F16) {
-                    __half *o = static_cast<__half *>(p.out) + o0;
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        if (j < jn) o[j * howo] = __float2half_rn(v[j]);
                 } else {
-                    __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.out) + o0;
+                    uint16_t *o = static_cast<uint16_t *>(p.out) + o0;
+                    const bool f16 = p.out_dt == BIGEMM_F16;
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        if (j < jn) o[j * howo] = __float2bfloat16_rn(v[j]);
+                    for (int j = 0; j < 32; j += 2) {
+                        const uint32_t pk = pack2_16(v[j], v[j + 1], f16);
+                        if (j < jn) o[j * howo] = (uint16_t)(pk & 0xFFFFu);
+                        if (j + 1 < jn) o[(j + 1) * howo] = (uint16_t)(pk >> 16);
+                    }
                 }
             }
         }
@@ -236,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *sa = smem;
     uint8_t *sb = smem + S * kABytes;
-    uint8_t *stage_out = sb + S * C::b_bytes;               // 4 warps x 2 x 4 KB output staging
+    uint8_t *stage_out = sb + S * C::b_bytes;               // 8 warps x 4 KB output staging
     uint64_t *full = reinterpret_cast<uint64_t *>(stage_out + C::staging);
     uint64_t *empty = full + S;
     uint64_t *tfull = empty + S;
@@ -256,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull[i], 1);
-            mbar_init(&tempty[i], 4);
+            mbar_init(&tempty[i], kEpiWarps);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -296,20 +350,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int mbx = 0, mby = 0, mbn = 0;
                 if (lane < nbox) {
                     const int bb = box0 + lane;
-                    const int n = bb / p.boxes_per_img;
-                    const int rem = bb - n * p.boxes_per_img;
+                    uint32_t urem;
+                    const int n = (int)fd_divmod((uint32_t)bb, p.fd_bpi, &urem);
+                    const int rem = (int)urem;
                     mbn = n;
                     if (AMODE == A_NHWC) {
-                        const int byi = rem / p.boxes_x, bxi = rem - byi * p.boxes_x;
+                        const int byi = (int)fd_divmod((uint32_t)rem, p.fd_bx, &urem), bxi = (int)urem;
                         mbx = bxi * p.box_w * p.stride - p.pad;
                         mby = byi * p.box_h * p.stride - p.pad;
                     } else {
                         mbx = rem * p.box_w;
                     }
                 }
-                int tap = w.kb0 / p.ci_blocks;
-                int cb = w.kb0 - tap * p.ci_blocks;
-                int ry = tap / p.KW, rx = tap - ry * p.KW;
+                uint32_t urem;
+                const int tap = (int)fd_divmod((uint32_t)w.kb0, p.fd_cib, &urem);
+                int cb = (int)urem;
+                int ry = (int)fd_divmod((uint32_t)tap, p.fd_kw, &urem), rx = (int)urem;
                 const int ncol = w.ct * BN;
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     int okw = 1;
@@ -442,7 +498,7 @@ struct HaloCfg {
     static constexpr int b_bytes = 32768;
     static constexpr int tb = b_bytes / (BN * kRowBytes);    // taps per B copy: 4, 2, 1
     static constexpr int b_stages = 3;
-    static constexpr int staging = 32768;
+    static constexpr int staging = kEpiWarps * 4096;
     static constexpr int bars = (2 * a_stages + 2 * b_stages + 5) * 8;
     static constexpr int smem = a_stages * kHaloBytes + b_stages * b_bytes + staging + bars + 16 + 1024;
     static constexpr uint32_t tmem_cols = Cfg<BN>::tmem_cols;
@@ -477,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < SA; ++i) mbar_init(&a_full[i], 1), mbar_init(&a_empty[i], 1);
         for (int i = 0; i < SB; ++i) mbar_init(&b_full[i], 1), mbar_init(&b_empty[i], 1);
-        for (int i = 0; i < 2; ++i) mbar_init(&tfull[i], 1), mbar_init(&tempty[i], 4);
+        for (int i = 0; i < 2; ++i) mbar_init(&tfull[i], 1), mbar_init(&tempty[i], kEpiWarps);
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -508,9 +564,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
                 const Unit w = decode(p, u);
-                const int n = w.pt / p.boxes_per_img;
-                const int rem = w.pt - n * p.boxes_per_img;
-                const int byi = rem / p.boxes_x, bxi = rem - byi * p.boxes_x;
+                uint32_t urem;
+                const int n = (int)fd_divmod((uint32_t)w.pt, p.fd_bpi, &urem);
+                const int byi = (int)fd_divmod(urem, p.fd_bx, &urem), bxi = (int)urem;
                 const int x0 = bxi * 8 - p.pad, y0 = byi * 16 - p.pad;
                 const int ncol = w.ct * BN;
                 for (int cb = w.kb0; ok && cb < w.kb1; ++cb) {
@@ -720,10 +776,18 @@ bool umma_tiling_compiled(const UmmaTiling &t, int in_dt)
            (t.amode == A_NHWC || t.amode == A_DIRECT || t.amode == A_HALO);
 }
 
-cudaError_t launch_umma_conv(const UmmaTiling &t, int in_dt, const UmmaParams &p,
+cudaError_t launch_umma_conv(const UmmaTiling &t, int in_dt, const UmmaParams &p0,
                              const CUtensorMap &map_a, const CUtensorMap &map_b,
                              const CUtensorMap &map_c, int grid, cudaStream_t stream)
 {
+    UmmaParams p = p0;
+    p.fd_co = make_fastdiv((uint32_t)p.co_tiles);
+    p.fd_pix = make_fastdiv((uint32_t)p.pix_tiles);
+    p.fd_bpi = make_fastdiv((uint32_t)p.boxes_per_img);
+    p.fd_bx = make_fastdiv((uint32_t)p.boxes_x);
+    p.fd_hp = make_fastdiv((uint32_t)p.hp);
+    p.fd_cib = make_fastdiv((uint32_t)p.ci_blocks);
+    p.fd_kw = make_fastdiv((uint32_t)p.KW);
     ProfScope prof(t.amode == A_NHWC ? "umma_conv_nhwc"
                    : t.amode == A_HALO ? "umma_conv_halo"
                                        : "umma_conv_direct",

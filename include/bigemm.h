@@ -98,7 +98,12 @@ typedef struct {
     int box_h;      /* UMMA: output rows per tile (box_w*box_h*boxes = 128)      */
     int mode;       /* UMMA operand-A mode: 1 channels-last boxes per tap,
                        2 NCHW read in place (1x1, stride 1, 16-bit),
-                       3 one halo box per channel block (stride 1)              */
+                       3 one halo box per channel block (stride 1),
+                       4 mode 1 over a subsampled copy (1x1, pad 0, stride > 1:
+                         only the pixels the conv reads are packed),
+                       5 mode 3 with the images stacked, pad zero rows apart,
+                         so that one 16-row tile spans several small images.
+                       Other values: INVALID_ARG.                               */
 } bigemm_plan_options;
 
 /*

@@ -181,6 +181,80 @@ def S(name, N, CI, CO, H, W, K, s, p, g=1, i="f16", o="f16", epi="none", dd="uni
     return synth.ConvSpec(name, N, CI, CO, H, W, K, s, p, g, i, o, dd, kd, epi)
 
 
+# ------------------------------------------------- halo tiles over stacked images
+# The pack writes the images one under another with `pad` zero rows between
+# them; a 16-row tile then spans several images and the gap rows are the
+# padding of both neighbours.  Output rows that fall on a gap are computed
+# and dropped.
+STACK = [
+    synth.RESNET50_FP16[3].with_batch(3),                        # 512 -> 512 on 7 x 7
+    _H("stack_7x7_ragged_ci40_co72", 5, 40, 72, 7, 7, 3, 1),
+    _H("stack_11x12_f32out_tma_store", 3, 64, 96, 11, 12, 3, 1, o="f32"),   # 12 rows per image
+    _H("stack_k5_pad2_6x6_bf16", 4, 32, 64, 6, 6, 5, 2, i="bf16", o="bf16"),
+    _H("stack_k3_pad0_9x9", 3, 64, 64, 9, 9, 3, 0),
+    _H("stack_tf32_5x5", 3, 48, 64, 5, 5, 3, 1, i="f32", o="f32"),
+    _H("stack_exp_7x7", 4, 64, 128, 7, 7, 3, 1, o="f32", epi="bias_exp"),
+    _H("stack_one_image", 1, 64, 64, 7, 7, 3, 1),
+]
+
+
+@pytest.mark.parametrize("spec", STACK, ids=lambda s: s.name)
+def test_umma_halo_stacked_images(spec):
+    info = check(spec, {"kind": bg.KIND_UMMA, "mode": bg.MODE_STACK})
+    assert info["amode"] == "halo" and info["pack"] == "stack"
+
+
+@pytest.mark.parametrize("split", [2, 5])
+def test_umma_halo_stacked_split_k(split):
+    spec = _H("stack_split", 3, 256, 128, 7, 7, 3, 1, o="f32")
+    info = check(spec, {"kind": bg.KIND_UMMA, "mode": bg.MODE_STACK, "split_k": split})
+    assert info["pack"] == "stack" and info["split"] > 1
+
+
+def test_stacking_rejects_padding_wider_than_the_kernel():
+    # pad 3 with a 3x3 kernel: 11 output rows per image, but only 10 stacked rows
+    with pytest.raises(bg.BigemmError) as e:
+        bg.conv2d_nchw_plan_ex(2, 7, 7, 64, 64, 3, 3, 1, 3, 1, bg.F16, bg.F16, bg.EPI_NONE, 0,
+                               {"kind": bg.KIND_UMMA, "mode": bg.MODE_STACK})
+    assert e.value.status == 2
+
+
+def test_heuristic_stacks_small_images():
+    spec = synth.RESNET50_FP16[3].with_batch(2)
+    info = check(spec)
+    assert info["amode"] == "halo" and info["pack"] == "stack"
+
+
+# ------------------------------------------------- subsampling pack (strided 1x1)
+SUB = [
+    synth.RESNET50_FP16[4].with_batch(2),                        # 256 -> 512, 28 x 28, stride 2
+    S("sub_s2_13x13_ragged", 3, 40, 72, 13, 13, 1, 2, 0),
+    S("sub_s3_tf32", 2, 64, 64, 16, 17, 1, 3, 0, i="f32", o="f32"),
+    S("sub_s2_bf16_bias", 2, 128, 96, 14, 14, 1, 2, 0, i="bf16", o="f32", epi="bias"),
+    S("sub_s4_one_column", 1, 32, 64, 9, 1, 1, 4, 0),
+]
+
+
+@pytest.mark.parametrize("spec", SUB, ids=lambda s: s.name)
+def test_umma_subsampled_1x1(spec):
+    info = check(spec, {"kind": bg.KIND_UMMA, "mode": bg.MODE_SUB})
+    assert info["amode"] == "nhwc" and info["pack"] == "sub"
+
+
+def test_subsampled_and_strided_boxes_agree():
+    spec = synth.RESNET50_FP16[4].with_batch(1)
+    a = check(spec, {"kind": bg.KIND_UMMA, "mode": bg.MODE_SUB, "tile_n": 128})
+    b = check(spec, {"kind": bg.KIND_UMMA, "mode": bg.MODE_NHWC, "tile_n": 128})
+    assert a["pack"] == "sub" and b["pack"] == "plain"
+
+
+def test_subsampling_needs_a_strided_1x1():
+    with pytest.raises(bg.BigemmError) as e:
+        bg.conv2d_nchw_plan_ex(1, 8, 8, 64, 64, 3, 3, 2, 1, 1, bg.F16, bg.F16, bg.EPI_NONE, 0,
+                               {"kind": bg.KIND_UMMA, "mode": bg.MODE_SUB})
+    assert e.value.status == 2
+
+
 EDGE = [
     S("ragged_13x11_ci24_co40", 2, 24, 40, 13, 11, 3, 1, 1),
     S("ragged_fp32_ci20_co200", 1, 20, 200, 9, 10, 3, 1, 1, i="f32", o="f32"),
