@@ -110,6 +110,11 @@ cudaError_t launch_simt_conv(const ConvShape &s, const void *x, const void *w,
                              cudaStream_t stream);
 cudaError_t launch_dw_conv(const ConvShape &s, const void *x, const void *w, const float *bias,
                            float eps, void *out, int rows_per_block, cudaStream_t stream);
+// Streaming depthwise kernel (square 3/5/7 with pad K/2, stride 1 or 2).
+bool dw_stream_ok(const ConvShape &s);
+// rows: output rows per thread (2, 4 or 8).
+cudaError_t launch_dw_stream(const ConvShape &s, const void *x, const void *w, const float *bias,
+                             float eps, void *out, int rows, cudaStream_t stream);
 cudaError_t launch_bcast(int N, int C, int HW, int op, const float *var, float eps, void *out,
                          int out_dt, int flat, cudaStream_t stream);
 cudaError_t launch_wait_timeout_probe(int *err, unsigned long long timeout_ns,

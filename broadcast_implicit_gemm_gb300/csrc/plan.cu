@@ -31,7 +31,7 @@ size_t dw_smem_bytes(const ConvShape &s, int rows);
 
 namespace {
 
-enum SimtVariant { SV_NAIVE = 0, SV_TILED = 1, SV_DW = 2 };
+enum SimtVariant { SV_NAIVE = 0, SV_TILED = 1, SV_DW = 2, SV_DWS = 3 };
 
 struct Cand {
     int kind = BIGEMM_KIND_SIMT;
@@ -50,6 +50,9 @@ std::string cand_str(const Cand &c)
                  c.t.pack == PACK_SUB ? ":sub" : c.t.pack == PACK_STACK ? ":stack" : "");
     else if (c.simt_variant == SV_DW)
         snprintf(b, sizeof b, "simt:depthwise:rows%d", c.dw_rows);
+    else if (c.simt_variant == SV_DWS)
+        snprintf(b, sizeof b, "simt:depthwise:stream%d", c.dw_rows);
+
     else
         snprintf(b, sizeof b, "simt:%s", c.simt_variant == SV_TILED ? "tiled" : "naive");
     return b;
@@ -75,6 +78,11 @@ bool parse_cand(const std::string &s, Cand &c)
     if (sscanf(s.c_str(), "simt:depthwise:rows%d", &g) == 1) {
         c = Cand{};
         c.simt_variant = SV_DW, c.dw_rows = g;
+        return true;
+    }
+    if (sscanf(s.c_str(), "simt:depthwise:stream%d", &g) == 1 && (g == 2 || g == 4 || g == 8)) {
+        c = Cand{};
+        c.simt_variant = SV_DWS, c.dw_rows = g;
         return true;
     }
     if (s == "simt:tiled") return c = Cand{}, c.simt_variant = SV_TILED, true;
@@ -320,6 +328,10 @@ bool simt_valid(const ConvShape &s, const Cand &c, std::string *why)
         if (why) *why = "tiled SIMT needs groups = 1";
         return false;
     }
+    if (c.simt_variant == SV_DWS && !dw_stream_ok(s))
+        return why && (*why = "streaming depthwise needs a square 3/5/7 kernel, pad K/2, stride 1-2",
+                       true),
+               false;
     if (c.simt_variant == SV_DW) {
         if (!is_depthwise(s)) return why && (*why = "not depthwise", true), false;
         if (s.KH * s.KW > 49) return why && (*why = "depthwise kernel > 7x7", true), false;
@@ -421,6 +433,11 @@ bool direct_ok(const ConvShape &s)
 Cand heuristic(const ConvShape &s, int sms)
 {
     Cand c;
+    if (dw_stream_ok(s)) {
+        c.simt_variant = SV_DWS;
+        c.dw_rows = 2;
+        return c;
+    }
     if (is_depthwise(s) && s.KH * s.KW <= 49) {
         c.simt_variant = SV_DW;
         c.dw_rows = std::max(1, std::min(s.Ho, 2048 / std::max(1, s.Wo)));
@@ -450,6 +467,14 @@ std::vector<Cand> candidates(const ConvShape &s, int sms)
 {
     std::vector<Cand> v;
     if (is_depthwise(s)) {
+        if (dw_stream_ok(s))
+            for (int rows : {2, 4, 8}) {
+                if (rows == 8 && !(s.stride == 1 && s.KH <= 5)) continue;
+                Cand c;
+                c.simt_variant = SV_DWS;
+                c.dw_rows = rows;
+                v.push_back(c);
+            }
         for (int rows : {1, 2, 4, 8, 16, 32}) {
             Cand c;
             c.simt_variant = SV_DW;
@@ -727,7 +752,9 @@ bigemm_status run_plan(bigemm_plan_s *p, const void *data, const void *kernel, c
     if (!ds) return BIGEMM_ERR_CUDA;
     cudaError_t e = cudaSuccess;
     if (p->c.kind != BIGEMM_KIND_UMMA) {
-        if (p->c.simt_variant == SV_DW)
+        if (p->c.simt_variant == SV_DWS)
+            e = launch_dw_stream(s, data, kernel, bias, eps, out, p->c.dw_rows, st);
+        else if (p->c.simt_variant == SV_DW)
             e = launch_dw_conv(s, data, kernel, bias, eps, out, p->c.dw_rows, st);
         else
             e = launch_simt_conv(s, data, kernel, bias, eps, out, p->c.simt_variant, st);
@@ -991,7 +1018,27 @@ bigemm_status plan_impl(int N, int H, int W, int CO, int CI, int KH, int KW, int
                                                !opts->box_w && !opts->box_h && !opts->stages &&
                                                !opts->mode)) {
             c = heuristic(s, sms);
-            if (c.kind == BIGEMM_KIND_UMMA) {
+            if (opts->kind == BIGEMM_KIND_SIMT && opts->mode != 0) {
+                // an explicit SIMT kernel: 1 tiled (groups = 1) or naive, 2 depthwise staged
+                // band (box_h rows per block), 3 depthwise streaming (box_h rows per thread)
+                if (opts->mode < 1 || opts->mode > 3) return BIGEMM_ERR_INVALID_ARG;
+                c = Cand{};
+                if (opts->mode == 1) {
+                    c.simt_variant = groups == 1 ? SV_TILED : SV_NAIVE;
+                } else if (opts->mode == 2) {
+                    c.simt_variant = SV_DW;
+                    c.dw_rows = opts->box_h > 0 ? opts->box_h : 8;
+                } else {
+                    c.simt_variant = SV_DWS;
+                    c.dw_rows = opts->box_h > 0 ? opts->box_h : 2;
+                    if (c.dw_rows != 2 && c.dw_rows != 4 && c.dw_rows != 8) return BIGEMM_ERR_INVALID_ARG;
+                }
+            } else if (opts->kind == BIGEMM_KIND_SIMT && is_depthwise(s) && opts->box_h > 0) {
+                // the staged-band depthwise kernel with box_h output rows per block
+                c = Cand{};
+                c.simt_variant = SV_DW;
+                c.dw_rows = opts->box_h;
+            } else if (c.kind == BIGEMM_KIND_UMMA) {
                 c = Cand{};
                 c.simt_variant = is_depthwise(s) ? SV_DW : (groups == 1 ? SV_TILED : SV_NAIVE);
                 if (c.simt_variant == SV_DW) {

@@ -95,7 +95,9 @@ typedef struct {
     int split_k;    /* UMMA: number of K slices (>= 1)                          */
     int stages;     /* UMMA: shared-memory pipeline depth (2..8)                */
     int box_w;      /* UMMA: output pixels per tile along W (with box_h)        */
-    int box_h;      /* UMMA: output rows per tile (box_w*box_h*boxes = 128)      */
+    int box_h;      /* UMMA: output rows per tile (box_w*box_h*boxes = 128);
+                       SIMT depthwise: output rows per block of the staged-band
+                       kernel (selects it over the streaming kernel)            */
     int mode;       /* UMMA operand-A mode: 1 channels-last boxes per tap,
                        2 NCHW read in place (1x1, stride 1, 16-bit),
                        3 one halo box per channel block (stride 1),
@@ -103,6 +105,10 @@ typedef struct {
                          only the pixels the conv reads are packed),
                        5 mode 3 with the images stacked, pad zero rows apart,
                          so that one 16-row tile spans several small images.
+                       With kind = SIMT it names the kernel instead: 1 tiled
+                       (groups = 1) or naive, 2 depthwise staged band (box_h
+                       rows per block), 3 depthwise streaming (box_h = 2, 4
+                       or 8 rows per thread).
                        Other values: INVALID_ARG.                               */
 } bigemm_plan_options;
 

@@ -285,6 +285,42 @@ def test_edge_cases_simt(spec):
     check(spec, {"kind": bg.KIND_SIMT})
 
 
+# ------------------------------------------------- depthwise kernels
+DW = [
+    S("dws_k3s1_f16_w16", 2, 24, 24, 21, 16, 3, 1, 1, g=24, kd="dw"),
+    S("dws_k3s1_f16_ragged_w", 2, 16, 16, 19, 13, 3, 1, 1, g=16, kd="dw"),
+    S("dws_k3s2_bf16", 3, 40, 40, 23, 24, 3, 2, 1, g=40, i="bf16", o="bf16", kd="dw"),
+    S("dws_k5s1_f16_14", 2, 48, 48, 14, 14, 5, 1, 2, g=48, kd="dw"),
+    S("dws_k5s2_f32", 2, 8, 8, 17, 20, 5, 2, 2, g=8, i="f32", o="f32", kd="dw"),
+    S("dws_k7s1_f16", 1, 8, 8, 30, 32, 7, 1, 3, g=8, kd="dw"),
+    S("dws_k7s2_f32out", 1, 8, 8, 29, 29, 7, 2, 3, g=8, o="f32", kd="dw"),
+    S("dws_k3s1_f32_bias_exp", 2, 16, 16, 12, 12, 3, 1, 1, g=16, i="f32", o="f32", epi="bias_exp", kd="dw"),
+    S("dws_k3s1_rsqrt", 1, 16, 16, 16, 16, 3, 1, 1, g=16, o="f32", epi="bias_rsqrt", dd="absnormal", kd="dw"),
+    S("dws_one_row", 2, 8, 8, 1, 40, 3, 1, 1, g=8, kd="dw"),
+    S("dws_k3s1_f32_w10_words", 2, 8, 8, 9, 10, 3, 1, 1, g=8, i="f32", o="f32", kd="dw"),
+    S("dws_k3s2_f16_w18_words", 2, 8, 8, 11, 18, 3, 2, 1, g=8, kd="dw"),
+]
+
+
+@pytest.mark.parametrize("spec", DW, ids=lambda s: s.name)
+def test_depthwise_heuristic(spec):
+    info = check(spec)
+    assert info["cand"].startswith("simt:depthwise:stream")
+
+
+@pytest.mark.parametrize("rows", [2, 4, 8])
+@pytest.mark.parametrize("spec", [DW[0], DW[2], DW[4], DW[10]], ids=lambda s: s.name)
+def test_depthwise_streaming_rows(spec, rows):
+    info = check(spec, {"kind": bg.KIND_SIMT, "mode": 3, "box_h": rows})
+    assert info["cand"].startswith("simt:depthwise:stream")
+
+
+@pytest.mark.parametrize("spec", DW[:5], ids=lambda s: s.name)
+def test_depthwise_staged_band(spec):
+    info = check(spec, {"kind": bg.KIND_SIMT, "mode": 2, "box_h": 4})
+    assert info["cand"] == "simt:depthwise:rows4"
+
+
 # ------------------------------------------------- full size, sampled outputs
 FULL = synth.RESNET50_FP16 + synth.FUSED_CONV + synth.DEPTHWISE_FP16
 
