@@ -49,6 +49,7 @@ enum PackLayout {
 struct UmmaTiling {
     int amode;        // AMode
     int pack;         // PackLayout
+    int bres;         // A_HALO: weights resident in shared memory (one output-channel tile)
     int bn;           // output channels per tile (N of the MMA), multiple of 32
     int stages;       // smem ring depth
     int box_w, box_h; // output pixels per TMA box (A_NHWC); A_DIRECT: box_w = row pixels
@@ -79,6 +80,8 @@ struct UmmaParams {
     int store_tma;                  // 1: stage tiles in smem, write with TMA stores (map_c)
     int hp;                         // A_HALO over stacked images: rows per image (H + pad)
                                     // in the packed data and in tile row space; 0 otherwise
+    int res_sa;                     // A_HALO with resident weights: halo stages (0: streamed B)
+    int res_b_bytes;                // ... and the bytes of all taps of all channel blocks
     // divisors of the index arithmetic; launch_umma_conv fills them from the fields above
     FastDiv fd_co, fd_pix, fd_bpi, fd_bx, fd_hp, fd_cib, fd_kw;
 };
@@ -90,6 +93,8 @@ cudaError_t launch_umma_conv(const UmmaTiling &t, int in_dt, const UmmaParams &p
                              const CUtensorMap &map_a, const CUtensorMap &map_b,
                              const CUtensorMap &map_c, int grid, cudaStream_t stream);
 size_t umma_smem_bytes(const UmmaTiling &t);
+// Halo stages that fit beside resident weights of b_bytes (0: none fit).
+int halo_res_stages(int bn, int kh, size_t b_bytes, int smem_limit);
 bool umma_tiling_compiled(const UmmaTiling &t, int in_dt);
 
 // -------------------------------------------------------------- other kernels

@@ -44,10 +44,11 @@ std::string cand_str(const Cand &c)
 {
     char b[160];
     if (c.kind == BIGEMM_KIND_UMMA)
-        snprintf(b, sizeof b, "umma:%s:bn%d:box%dx%dx%d:split%d%s",
+        snprintf(b, sizeof b, "umma:%s:bn%d:box%dx%dx%d:split%d%s%s",
                  c.t.amode == A_DIRECT ? "direct" : c.t.amode == A_HALO ? "halo" : "nhwc", c.t.bn,
                  c.t.box_w, c.t.box_h, c.t.bpt, c.t.split,
-                 c.t.pack == PACK_SUB ? ":sub" : c.t.pack == PACK_STACK ? ":stack" : "");
+                 c.t.pack == PACK_SUB ? ":sub" : c.t.pack == PACK_STACK ? ":stack" : "",
+                 c.t.bres ? ":bres" : "");
     else if (c.simt_variant == SV_DW)
         snprintf(b, sizeof b, "simt:depthwise:rows%d", c.dw_rows);
     else if (c.simt_variant == SV_DWS)
@@ -61,10 +62,10 @@ std::string cand_str(const Cand &c)
 bool parse_cand(const std::string &s, Cand &c)
 {
     int a, b, d, e, f, g;
-    char mode[16], layout[16] = "";
-    const int got = sscanf(s.c_str(), "umma:%15[a-z]:bn%d:box%dx%dx%d:split%d:%15[a-z]", mode, &a,
-                           &b, &d, &e, &f, layout);
-    if (got == 6 || got == 7) {
+    char mode[16], layout[16] = "", layout2[16] = "";
+    const int got = sscanf(s.c_str(), "umma:%15[a-z]:bn%d:box%dx%dx%d:split%d:%15[a-z]:%15[a-z]",
+                           mode, &a, &b, &d, &e, &f, layout, layout2);
+    if (got >= 6 && got <= 8) {
         c = Cand{};
         c.kind = BIGEMM_KIND_UMMA;
         c.t.amode = strcmp(mode, "direct") == 0 ? A_DIRECT
@@ -72,6 +73,7 @@ bool parse_cand(const std::string &s, Cand &c)
                                                   : A_NHWC;
         c.t.pack = strcmp(layout, "sub") == 0 ? PACK_SUB : strcmp(layout, "stack") == 0 ? PACK_STACK
                                                                                        : PACK_PLAIN;
+        c.t.bres = strcmp(layout, "bres") == 0 || strcmp(layout2, "bres") == 0;
         c.t.bn = a, c.t.box_w = b, c.t.box_h = d, c.t.bpt = e, c.t.split = f;
         return true;
     }
@@ -218,6 +220,14 @@ UmmaGeom umma_geometry(const ConvShape &s0, const UmmaTiling &t, int sm_count)
     p.epi = s.epi;
     p.out_dt = s.out_dt;
     p.out_elems = (long long)s.N * s.CO * s.Ho * s.Wo;
+    if (t.amode == A_HALO && t.bres) {
+        // every tap of every channel block of the (single) output-channel tile
+        const long long bytes = (long long)p.ci_blocks * s.KH * s.KW * t.bn * 128;
+        DeviceState *ds = device_state();
+        const int limit = ds ? ds->max_smem_optin : 232448;
+        p.res_b_bytes = (int)std::min<long long>(bytes, INT32_MAX);
+        p.res_sa = bytes < (1 << 20) ? halo_res_stages(t.bn, s.KH, (size_t)bytes, limit) : 0;
+    }
     g.grid = (int)std::min<long long>(p.units, sm_count);
     return g;
 }
@@ -255,6 +265,10 @@ bool umma_valid(const ConvShape &s0, const UmmaTiling &t, int sm_count, std::str
         if (t.box_w != (int)(128 / e) || t.box_h != 1 || t.bpt * t.box_w != 128)
             return bad("direct box must be one 128-byte row of pixels");
     } else if (t.amode == A_HALO) {
+        if (t.bres) {
+            if (s.CO > t.bn) return bad("resident weights need one output-channel tile");
+            if (umma_geometry(s0, t, 1).p.res_sa < 2) return bad("weights too large to stay resident");
+        }
         if (s.stride != 1) return bad("halo mode needs stride 1");
         if (s.KH * s.KW < 2) return bad("halo mode is for kernels larger than 1x1");
         if (s.KH > 7 || s.KW > 8) return bad("halo mode holds up to 7 rows x 8 columns of taps");
@@ -266,6 +280,7 @@ bool umma_valid(const ConvShape &s0, const UmmaTiling &t, int sm_count, std::str
         if (t.box_w * t.box_h * t.bpt > 128) return bad("boxes exceed 128 rows");
         if (t.box_w * s.stride > 256 || t.box_h * s.stride > 256) return bad("box > 256");
     }
+    if (t.bres && t.amode != A_HALO) return bad("resident weights are a halo-mode form");
     if (t.bpt > 16) return bad("more than 16 boxes per tile");
     if (umma_smem_bytes(t) == 0) return bad("no compiled kernel");
     if (!umma_geometry(s0, t, 1).fits) return bad("more than 2^31 boxes or work units");
@@ -406,6 +421,15 @@ double halo_cover(const ConvShape &s, int pack)
     return (double)s.N * s.Ho * s.Wo / (rows * ceil_div(s.Wo, 8) * 8);
 }
 
+// Keep the weights resident when one output-channel tile covers CO and they fit.
+void prefer_resident(const ConvShape &s, UmmaTiling &t)
+{
+    if (t.amode != A_HALO || s.CO > t.bn) return;
+    UmmaTiling r = t;
+    r.bres = 1;
+    if (umma_valid(s, r, 1, nullptr)) t.bres = 1;
+}
+
 // Halo tiles are worth it when they are mostly inside the output.
 bool halo_ok(const ConvShape &s)
 {
@@ -453,9 +477,10 @@ Cand heuristic(const ConvShape &s, int sms)
             u.t = default_tiling(s, A_DIRECT, default_bn(s), sms);
         else if (sub_ok(s))
             u.t = default_tiling(s, A_NHWC, default_bn(s), sms, PACK_SUB);
-        else if (halo_ok(s))
+        else if (halo_ok(s)) {
             u.t = default_tiling(s, A_HALO, default_bn(s), sms, halo_pack(s));
-        else
+            prefer_resident(s, u.t);
+        } else
             u.t = default_tiling(s, A_NHWC, default_bn(s), sms);
         if (umma_valid(s, u.t, sms, nullptr)) return u;
     }
@@ -546,6 +571,10 @@ std::vector<Cand> candidates(const ConvShape &s, int sms)
                     c.kind = BIGEMM_KIND_UMMA;
                     c.t = t;
                     if (umma_valid(s, t, sms, nullptr)) v.push_back(c);
+                    if (amode == A_HALO && s.CO <= bn) {   // the resident-weights form too
+                        c.t.bres = 1;
+                        if (umma_valid(s, c.t, sms, nullptr)) v.push_back(c);
+                    }
                 }
             }
     }
@@ -635,7 +664,7 @@ bigemm_status setup_plan(bigemm_plan_s *p)
             return BIGEMM_ERR_UNSUPPORTED;
         // packed weights [CO][tap][cip] viewed as (channel, output channel, tap):
         // one box brings TB taps, each a [BN][128 B] K-major tile
-        const int tb = 32768 / (t.bn * 128);
+        const int tb = t.bres ? 1 : 32768 / (t.bn * 128);
         const uint64_t kk = (uint64_t)s.KH * s.KW;
         const uint64_t bd[3] = {(uint64_t)p->g.cip, (uint64_t)s.CO, kk};
         const uint64_t bs[2] = {kk * p->g.cip * e, (uint64_t)p->g.cip * e};
@@ -1010,13 +1039,13 @@ bigemm_status plan_impl(int N, int H, int W, int CO, int CI, int KH, int KW, int
     cudaStream_t st = (cudaStream_t)stream;
 
     const bool forced = opts && (opts->kind || opts->tile_n || opts->split_k || opts->box_w ||
-                                 opts->box_h || opts->stages || opts->mode);
+                                 opts->box_h || opts->stages || opts->mode || opts->resident_b);
     Cand c;
     std::string log, chosen = "heuristic";
     if (forced) {
         if (opts->kind == BIGEMM_KIND_SIMT || (opts->kind == 0 && !opts->tile_n && !opts->split_k &&
                                                !opts->box_w && !opts->box_h && !opts->stages &&
-                                               !opts->mode)) {
+                                               !opts->mode && !opts->resident_b)) {
             c = heuristic(s, sms);
             if (opts->kind == BIGEMM_KIND_SIMT && opts->mode != 0) {
                 // an explicit SIMT kernel: 1 tiled (groups = 1) or naive, 2 depthwise staged
@@ -1071,6 +1100,11 @@ bigemm_status plan_impl(int N, int H, int W, int CO, int CI, int KH, int KW, int
             }
             if (opts->split_k) c.t.split = opts->split_k;
             if (opts->stages) c.t.stages = opts->stages;
+            if (opts->resident_b < -1 || opts->resident_b > 1) return BIGEMM_ERR_INVALID_ARG;
+            if (opts->resident_b == 1)
+                c.t.bres = 1;
+            else if (opts->resident_b == 0)
+                prefer_resident(s, c.t);
         }
         std::string why;
         if (!cand_valid(s, c, sms, &why)) return BIGEMM_ERR_UNSUPPORTED;
@@ -1169,12 +1203,13 @@ bigemm_status conv2d_nchw_plan_describe(bigemm_plan plan, char *buf, size_t len)
            << (c.t.amode == A_DIRECT ? "direct" : c.t.amode == A_HALO ? "halo" : "nhwc")
            << "\", \"pack\": \""
            << (c.t.pack == PACK_SUB ? "sub" : c.t.pack == PACK_STACK ? "stack" : "plain")
-           << "\", \"bn\": " << c.t.bn
+           << "\", \"resident_b\": " << (c.t.bres ? "true" : "false")
+           << ", \"bn\": " << c.t.bn
            << ", \"box\": [" << c.t.box_w << ", " << c.t.box_h << ", " << c.t.bpt << "]"
            << ", \"split\": " << p.split << ", \"k_blocks\": " << p.k_blocks
            << ", \"pix_tiles\": " << p.pix_tiles << ", \"co_tiles\": " << p.co_tiles
            << ", \"units\": " << p.units << ", \"grid\": " << plan->g.grid
-           << ", \"smem\": " << umma_smem_bytes(c.t)
+           << ", \"smem\": " << umma_smem_bytes(c.t) << ", \"halo_stages\": " << p.res_sa
            << ", \"store\": \"" << (plan->store_tma ? "tma" : "direct") << "\"";
     }
     os << ", \"launches\": " << launches_per_run(plan)

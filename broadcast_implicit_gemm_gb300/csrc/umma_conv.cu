@@ -504,22 +504,48 @@ struct HaloCfg {
     static constexpr uint32_t tmem_cols = Cfg<BN>::tmem_cols;
 };
 
-template <int BN, int FMT>
+// Resident-weights form (RES): when one output-channel tile covers CO and all
+// of its taps fit in shared memory, the producer loads B once (one tap per
+// copy, every channel block) and only the halos stream; up to kResMaxA halo
+// stages then fit beside it.  The host sizes the layout (p.res_sa stages of
+// (16 + KH - 1) rows, p.res_b_bytes of weights) within the shared-memory limit.
+constexpr int kResMaxA = 4;
+
+template <int BN, bool RES>
+struct HaloBars {
+    static constexpr int a = RES ? kResMaxA : HaloCfg<BN>::a_stages;
+    static constexpr int b = RES ? 1 : HaloCfg<BN>::b_stages;
+    static constexpr int bytes = (2 * a + 2 * b + 5) * 8;
+};
+
+template <int BN>
+size_t halo_res_smem(int sa, int kh, size_t b_bytes)
+{
+    return (size_t)sa * (16 + kh - 1) * kHaloRowBytes + b_bytes + HaloCfg<BN>::staging +
+           HaloBars<BN, true>::bytes + 16 + 1024;
+}
+
+template <int BN, int FMT, bool RES>
 __global__ void __launch_bounds__(kThreads, 1)
     umma_conv_halo_kernel(const __grid_constant__ CUtensorMap map_a,
                           const __grid_constant__ CUtensorMap map_b,
                           const __grid_constant__ CUtensorMap map_c, const UmmaParams p)
 {
     using C = HaloCfg<BN>;
-    constexpr int SA = C::a_stages, SB = C::b_stages, TB = C::tb;
+    using BARS = HaloBars<BN, RES>;
+    constexpr int SAMAX = BARS::a, SB = BARS::b;
+    constexpr int TB = RES ? 1 : C::tb;
+    const int SA = RES ? p.res_sa : C::a_stages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t halo_bytes = (uint32_t)(16 + p.KH - 1) * kHaloRowBytes;
+    const uint32_t a_stride = RES ? halo_bytes : (uint32_t)kHaloBytes;
     uint8_t *sa = smem;
-    uint8_t *sb = sa + SA * kHaloBytes;
-    uint8_t *stage_out = sb + SB * C::b_bytes;
+    uint8_t *sb = sa + SA * a_stride;
+    uint8_t *stage_out = sb + (RES ? (uint32_t)p.res_b_bytes : (uint32_t)(SB * C::b_bytes));
     uint64_t *a_full = reinterpret_cast<uint64_t *>(stage_out + C::staging);
-    uint64_t *a_empty = a_full + SA;
-    uint64_t *b_full = a_empty + SA;
+    uint64_t *a_empty = a_full + SAMAX;
+    uint64_t *b_full = a_empty + SAMAX;
     uint64_t *b_empty = b_full + SB;
     uint64_t *tfull = b_empty + SB;
     uint64_t *tempty = tfull + 2;
@@ -528,7 +554,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int KK = p.KH * p.KW;
-    const uint32_t halo_bytes = (uint32_t)(16 + p.KH - 1) * kHaloRowBytes;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < SA; ++i) mbar_init(&a_full[i], 1), mbar_init(&a_empty[i], 1);
@@ -557,11 +582,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             int as = 0, bs = 0;
             uint32_t aph = 0, bph = 0;
-            uint32_t a_par[SA], b_par[SB];
-            bool a_iss[SA], b_iss[SB];
-            for (int i = 0; i < SA; ++i) a_iss[i] = false, a_par[i] = 0;
+            uint32_t a_par[SAMAX], b_par[SB];
+            bool a_iss[SAMAX], b_iss[SB];
+            for (int i = 0; i < SAMAX; ++i) a_iss[i] = false, a_par[i] = 0;
             for (int i = 0; i < SB; ++i) b_iss[i] = false, b_par[i] = 0;
             bool ok = true;
+            if (RES) {
+                // every tap of every channel block, once, on b_full[0]
+                mbar_arrive_expect_tx(&b_full[0], (uint32_t)p.res_b_bytes);
+                b_iss[0] = true;
+                for (int cb = 0; cb < p.ci_blocks; ++cb)
+                    for (int t = 0; t < KK; ++t)
+                        tma_load_3d(sb + (size_t)(cb * KK + t) * (BN * kRowBytes), &map_b, &b_full[0],
+                                    cb * p.bk, 0, t);
+            }
             for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
                 const Unit w = decode(p, u);
                 uint32_t urem;
@@ -576,8 +610,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     mbar_arrive_expect_tx(&a_full[as], halo_bytes);
                     a_iss[as] = true, a_par[as] = aph;
-                    tma_load_4d(sa + as * kHaloBytes, &map_a, &a_full[as], cb * p.bk, x0, y0, n);
+                    tma_load_4d(sa + as * a_stride, &map_a, &a_full[as], cb * p.bk, x0, y0, n);
                     if (++as == SA) as = 0, aph ^= 1u;
+                    if (RES) continue;
                     for (int t0 = 0; t0 < KK; t0 += TB) {
                         if (!mbar_wait(&b_empty[bs], bph ^ 1u, p.timeout_ns, abort_flag, p.err)) {
                             ok = false;
@@ -597,6 +632,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (a_iss[i]) mbar_wait(&a_full[i], a_par[i], p.timeout_ns, &local_abort, p.err);
                 for (int i = 0; i < SB; ++i)
                     if (b_iss[i]) mbar_wait(&b_full[i], b_par[i], p.timeout_ns, &local_abort, p.err);
+            } else if (RES) {
+                // the weights may still be in flight if this block had no unit to run
+                int local_abort = 0;
+                mbar_wait(&b_full[0], 0, p.timeout_ns, &local_abort, p.err);
             }
         }
     } else if (warp == 1) {
@@ -607,6 +646,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             int as = 0, bs = 0, acc = 0;
             uint32_t aph = 0, bph = 0, acc_phase = 0;
             bool ok = true, any = false;
+            if (RES && blockIdx.x < p.units)
+                ok = mbar_wait(&b_full[0], 0, p.timeout_ns, abort_flag, p.err);
+            const uint32_t b_res0 = desc_lo(smem_u32(sb), 16u);
             for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
                 const Unit w = decode(p, u);
                 if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, p.timeout_ns, abort_flag, p.err)) {
@@ -621,17 +663,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    const uint32_t a_lo0 = desc_lo(smem_u32(sa + as * kHaloBytes), 16u);
+                    const uint32_t a_lo0 = desc_lo(smem_u32(sa + as * a_stride), 16u);
                     int ry = 0, rx = 0;
-                    for (int t0 = 0; t0 < KK; t0 += TB) {
-                        if (!mbar_wait(&b_full[bs], bph, p.timeout_ns, abort_flag, p.err)) {
-                            ok = false;
-                            break;
-                        }
+                    if (RES) {
                         tc_fence_after();
-                        uint32_t b_lo = desc_lo(smem_u32(sb + bs * C::b_bytes), 16u);
-                        const int nt = min(TB, KK - t0);
-                        for (int tt = 0; tt < nt; ++tt) {
+                        uint32_t b_lo = b_res0 + (uint32_t)(cb * KK) * ((uint32_t)(BN * kRowBytes) >> 4);
+                        for (int t = 0; t < KK; ++t) {
                             const uint32_t a_lo =
                                 a_lo0 + (uint32_t)(ry * kHaloPitch + rx) * (kRowBytes >> 4);
 #pragma unroll
@@ -644,8 +681,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (++rx == p.KW) rx = 0, ++ry;
                         }
                         any = true;
-                        umma_commit(&b_empty[bs]);
-                        if (++bs == SB) bs = 0, bph ^= 1u;
+                    } else {
+                        for (int t0 = 0; t0 < KK; t0 += TB) {
+                            if (!mbar_wait(&b_full[bs], bph, p.timeout_ns, abort_flag, p.err)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            uint32_t b_lo = desc_lo(smem_u32(sb + bs * C::b_bytes), 16u);
+                            const int nt = min(TB, KK - t0);
+                            for (int tt = 0; tt < nt; ++tt) {
+                                const uint32_t a_lo =
+                                    a_lo0 + (uint32_t)(ry * kHaloPitch + rx) * (kRowBytes >> 4);
+#pragma unroll
+                                for (int k = 0; k < 4; ++k) {
+                                    umma_lohi<FMT == 2>(d_tmem, a_lo + k * 2u, a_hi, b_lo + k * 2u,
+                                                        b_hi, idesc, accum);
+                                    accum = 1u;
+                                }
+                                b_lo += (uint32_t)(BN * kRowBytes) >> 4;
+                                if (++rx == p.KW) rx = 0, ++ry;
+                            }
+                            any = true;
+                            umma_commit(&b_empty[bs]);
+                            if (++bs == SB) bs = 0, bph ^= 1u;
+                        }
                     }
                     umma_commit(&a_empty[as]);
                     if (++as == SA) as = 0, aph ^= 1u;
@@ -680,10 +740,23 @@ template <int BN, int FMT>
 cudaError_t launch_halo(const UmmaParams &p, const CUtensorMap &ma, const CUtensorMap &mb,
                         const CUtensorMap &mc, int grid, cudaStream_t stream)
 {
-    auto kern = umma_conv_halo_kernel<BN, FMT>;
-    static unsigned long long attr_set = 0;   // bit per device: smem opt-in done
     int dev = 0;
     cudaGetDevice(&dev);
+    if (p.res_sa > 0) {
+        auto kern = umma_conv_halo_kernel<BN, FMT, true>;
+        const size_t smem = halo_res_smem<BN>(p.res_sa, p.KH, (size_t)p.res_b_bytes);
+        static unsigned long long attr_set = 0;
+        if (dev >= 64 || !(attr_set >> dev & 1ull)) {
+            DeviceState *ds = device_state();
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 ds ? ds->max_smem_optin : (int)smem);
+            if (e != cudaSuccess) return e;
+            if (dev < 64) attr_set |= 1ull << dev;
+        }
+        return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, stream, ma, mb, mc, p);
+    }
+    auto kern = umma_conv_halo_kernel<BN, FMT, false>;
+    static unsigned long long attr_set = 0;   // bit per device: smem opt-in done
     if (dev >= 64 || !(attr_set >> dev & 1ull)) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              HaloCfg<BN>::smem);
@@ -750,6 +823,21 @@ cudaError_t dispatch_fmt(int fmt, int bn, const UmmaParams &p, const CUtensorMap
 int fmt_of(int in_dt) { return in_dt == BIGEMM_F16 ? 0 : in_dt == BIGEMM_BF16 ? 1 : 2; }
 
 }  // namespace
+
+int halo_res_stages(int bn, int kh, size_t b_bytes, int smem_limit)
+{
+    for (int sa = kResMaxA; sa >= 2; --sa) {
+        size_t need = 0;
+        switch (bn) {
+        case 64: need = halo_res_smem<64>(sa, kh, b_bytes); break;
+        case 128: need = halo_res_smem<128>(sa, kh, b_bytes); break;
+        case 256: need = halo_res_smem<256>(sa, kh, b_bytes); break;
+        default: return 0;
+        }
+        if (need <= (size_t)smem_limit) return sa;
+    }
+    return 0;
+}
 
 size_t umma_smem_bytes(const UmmaTiling &t)
 {

@@ -110,6 +110,9 @@ typedef struct {
                        rows per block), 3 depthwise streaming (box_h = 2, 4
                        or 8 rows per thread).
                        Other values: INVALID_ARG.                               */
+    int resident_b; /* UMMA halo modes: 1 keeps the packed weights resident in
+                       shared memory (one output-channel tile must cover CO and
+                       every tap must fit), -1 streams them, 0 chooses          */
 } bigemm_plan_options;
 
 /*

@@ -181,6 +181,46 @@ def S(name, N, CI, CO, H, W, K, s, p, g=1, i="f16", o="f16", epi="none", dd="uni
     return synth.ConvSpec(name, N, CI, CO, H, W, K, s, p, g, i, o, dd, kd, epi)
 
 
+# ------------------------------------------------- halo with resident weights
+# Resident weights need one 64-channel output tile and one 128-byte channel
+# block (9 taps x 8 KB beside three halo stages).
+RES = [
+    synth.RESNET50_FP16[1].with_batch(1),                        # 64 -> 64, 56 x 56
+    _H("res_ragged_ci40_co56", 2, 40, 56, 19, 21, 3, 1),
+    _H("res_bf16_co48", 1, 64, 48, 17, 18, 3, 1, i="bf16", o="bf16"),
+    _H("res_tf32_ci32", 1, 32, 64, 20, 20, 3, 1, i="f32", o="f32"),
+    _H("res_exp_f32out", 2, 64, 64, 16, 24, 3, 1, o="f32", epi="bias_exp"),
+]
+
+
+@pytest.mark.parametrize("spec", RES, ids=lambda s: s.name)
+def test_umma_halo_resident_weights(spec):
+    info = check(spec, {"kind": bg.KIND_UMMA, "mode": bg.MODE_HALO, "resident_b": 1})
+    assert info["amode"] == "halo" and info["resident_b"] and info["halo_stages"] >= 2
+
+
+def test_umma_halo_resident_weights_stacked():
+    spec = _H("res_stack", 5, 64, 64, 7, 7, 3, 1, o="f32")
+    info = check(spec, {"kind": bg.KIND_UMMA, "mode": bg.MODE_STACK, "resident_b": 1})
+    assert info["resident_b"] and info["pack"] == "stack"
+
+
+def test_umma_halo_streamed_weights_forced():
+    spec = synth.RESNET50_FP16[1].with_batch(1)
+    info = check(spec, {"kind": bg.KIND_UMMA, "mode": bg.MODE_HALO, "resident_b": -1})
+    assert not info["resident_b"]
+
+
+@pytest.mark.parametrize("shape", [(256, 64, 128), (64, 256, 64)], ids=["two_co_tiles", "too_large"])
+def test_resident_weights_rejected_when_they_cannot_stay(shape):
+    co, ci, bn = shape
+    with pytest.raises(bg.BigemmError) as e:
+        bg.conv2d_nchw_plan_ex(1, 16, 16, co, ci, 3, 3, 1, 1, 1, bg.F16, bg.F16, bg.EPI_NONE, 0,
+                               {"kind": bg.KIND_UMMA, "mode": bg.MODE_HALO, "tile_n": bn,
+                                "resident_b": 1})
+    assert e.value.status == 2
+
+
 # ------------------------------------------------- halo tiles over stacked images
 # The pack writes the images one under another with `pad` zero rows between
 # them; a 16-row tile then spans several images and the gap rows are the
