@@ -80,8 +80,10 @@ struct UmmaParams {
     int store_tma;                  // 1: stage tiles in smem, write with TMA stores (map_c)
     int hp;                         // A_HALO over stacked images: rows per image (H + pad)
                                     // in the packed data and in tile row space; 0 otherwise
-    int res_sa;                     // A_HALO with resident weights: halo stages (0: streamed B)
-    int res_b_bytes;                // ... and the bytes of all taps of all channel blocks
+    int res_b_bytes;                // A_HALO with resident weights: bytes of every tap (0: streamed)
+    // A_HALO shared-memory layout (halo_layout): halo stages, byte offsets of the
+    // weights, the output staging and the barriers, and the total
+    int halo_sa, halo_b_off, halo_stage_off, halo_bar_off, halo_smem;
     // divisors of the index arithmetic; launch_umma_conv fills them from the fields above
     FastDiv fd_co, fd_pix, fd_bpi, fd_bx, fd_hp, fd_cib, fd_kw;
 };
@@ -93,8 +95,14 @@ cudaError_t launch_umma_conv(const UmmaTiling &t, int in_dt, const UmmaParams &p
                              const CUtensorMap &map_a, const CUtensorMap &map_b,
                              const CUtensorMap &map_c, int grid, cudaStream_t stream);
 size_t umma_smem_bytes(const UmmaTiling &t);
-// Halo stages that fit beside resident weights of b_bytes (0: none fit).
-int halo_res_stages(int bn, int kh, size_t b_bytes, int smem_limit);
+// The halo kernel's shared-memory layout for a tiling (res: resident
+// weights), written into p; false when it does not fit in smem_limit bytes.
+bool halo_layout(int bn, bool res, int kh, int kk, int ci_blocks, int smem_limit, UmmaParams &p);
+// The halo-mode kernels (halo_conv.cu); fmt 0 f16, 1 bf16, 2 tf32.
+size_t halo_smem_bytes(int bn);
+cudaError_t launch_halo_conv(int bn, int fmt, const UmmaParams &p, const CUtensorMap &map_a,
+                             const CUtensorMap &map_b, const CUtensorMap &map_c, int grid,
+                             cudaStream_t stream);
 bool umma_tiling_compiled(const UmmaTiling &t, int in_dt);
 
 // -------------------------------------------------------------- other kernels

@@ -220,13 +220,11 @@ UmmaGeom umma_geometry(const ConvShape &s0, const UmmaTiling &t, int sm_count)
     p.epi = s.epi;
     p.out_dt = s.out_dt;
     p.out_elems = (long long)s.N * s.CO * s.Ho * s.Wo;
-    if (t.amode == A_HALO && t.bres) {
-        // every tap of every channel block of the (single) output-channel tile
-        const long long bytes = (long long)p.ci_blocks * s.KH * s.KW * t.bn * 128;
+    if (t.amode == A_HALO) {
+        // shared-memory layout: streamed or resident weights
         DeviceState *ds = device_state();
         const int limit = ds ? ds->max_smem_optin : 232448;
-        p.res_b_bytes = (int)std::min<long long>(bytes, INT32_MAX);
-        p.res_sa = bytes < (1 << 20) ? halo_res_stages(t.bn, s.KH, (size_t)bytes, limit) : 0;
+        g.fits = g.fits && halo_layout(t.bn, t.bres != 0, s.KH, s.KH * s.KW, p.ci_blocks, limit, p);
     }
     g.grid = (int)std::min<long long>(p.units, sm_count);
     return g;
@@ -265,10 +263,8 @@ bool umma_valid(const ConvShape &s0, const UmmaTiling &t, int sm_count, std::str
         if (t.box_w != (int)(128 / e) || t.box_h != 1 || t.bpt * t.box_w != 128)
             return bad("direct box must be one 128-byte row of pixels");
     } else if (t.amode == A_HALO) {
-        if (t.bres) {
-            if (s.CO > t.bn) return bad("resident weights need one output-channel tile");
-            if (umma_geometry(s0, t, 1).p.res_sa < 2) return bad("weights too large to stay resident");
-        }
+        if (t.bres && s.CO > t.bn) return bad("resident weights need one output-channel tile");
+        if (!umma_geometry(s0, t, 1).fits) return bad("halo buffers exceed shared memory");
         if (s.stride != 1) return bad("halo mode needs stride 1");
         if (s.KH * s.KW < 2) return bad("halo mode is for kernels larger than 1x1");
         if (s.KH > 7 || s.KW > 8) return bad("halo mode holds up to 7 rows x 8 columns of taps");
@@ -436,10 +432,12 @@ bool halo_ok(const ConvShape &s)
     return std::max(halo_cover(s, PACK_PLAIN), halo_cover(s, PACK_STACK)) >= 0.7;
 }
 
-// The better halo layout for a shape: stacking when it covers clearly more.
+// The halo layout for a shape: stacked images when they cover clearly more of
+// the tiles, else the plain packed copy.
 int halo_pack(const ConvShape &s)
 {
-    return halo_cover(s, PACK_STACK) > halo_cover(s, PACK_PLAIN) + 0.02 ? PACK_STACK : PACK_PLAIN;
+    const double cp = halo_cover(s, PACK_PLAIN), cs = halo_cover(s, PACK_STACK);
+    return cs > cp + 0.02 ? PACK_STACK : PACK_PLAIN;
 }
 
 bool direct_ok(const ConvShape &s)
@@ -1209,7 +1207,8 @@ bigemm_status conv2d_nchw_plan_describe(bigemm_plan plan, char *buf, size_t len)
            << ", \"split\": " << p.split << ", \"k_blocks\": " << p.k_blocks
            << ", \"pix_tiles\": " << p.pix_tiles << ", \"co_tiles\": " << p.co_tiles
            << ", \"units\": " << p.units << ", \"grid\": " << plan->g.grid
-           << ", \"smem\": " << umma_smem_bytes(c.t) << ", \"halo_stages\": " << p.res_sa
+           << ", \"smem\": " << (c.t.amode == A_HALO ? (size_t)p.halo_smem : umma_smem_bytes(c.t))
+           << ", \"halo_stages\": " << p.halo_sa
            << ", \"store\": \"" << (plan->store_tma ? "tma" : "direct") << "\"";
     }
     os << ", \"launches\": " << launches_per_run(plan)

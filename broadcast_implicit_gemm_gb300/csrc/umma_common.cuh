@@ -1,0 +1,263 @@
+// umma_common.cuh -- pieces shared by the implicit-GEMM conv kernels
+// (umma_conv.cu: per-tap and direct operand modes; halo_conv.cu: halo mode):
+// tile constants, the work-unit decode, and the epilogue warps that drain the
+// TMEM accumulators into NCHW outputs.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace bigemm {
+namespace {
+
+constexpr int kThreads = 320;                  // producer, MMA, 8 epilogue warps
+constexpr int kEpiWarps = 8;
+constexpr int kTileM = 128;
+constexpr int kRowBytes = 128;                  // one K block: a 128-byte swizzle row
+constexpr int kABytes = kTileM * kRowBytes;     // 16 KB of A per stage
+
+template <int BN>
+struct Cfg {
+    static constexpr int stages = BN <= 64 ? 8 : (BN <= 128 ? 6 : 4);
+    static constexpr int b_bytes = BN * kRowBytes;
+    static constexpr int ring = stages * (kABytes + b_bytes);
+    static constexpr int staging = kEpiWarps * 4096;          // 4 KB output staging per epilogue warp
+    static constexpr int bars = (2 * stages + 5) * 8;
+    static constexpr int smem = ring + staging + bars + 16 + 16 + 1024;   // + alignment slack
+    static constexpr uint32_t tmem_cols = (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
+                                         : (2 * BN <= 256) ? 256 : 512;
+};
+
+struct Unit {
+    int ct, pt, sp, kb0, kb1;
+};
+
+__device__ __forceinline__ Unit decode(const UmmaParams &p, int u)
+{
+    Unit w;
+    uint32_t rem;
+    const int r = (int)fd_divmod((uint32_t)u, p.fd_co, &rem);
+    w.ct = (int)rem;
+    w.sp = (int)fd_divmod((uint32_t)r, p.fd_pix, &rem);
+    w.pt = (int)rem;
+    w.kb0 = w.sp * p.kb_per_split;
+    w.kb1 = min(p.k_blocks, w.kb0 + p.kb_per_split);
+    return w;
+}
+
+constexpr int kMaxBoxes = 16;   // boxes per tile: 128 rows / at least 8 pixels per box (< 32 lanes)
+
+// Two floats rounded to nearest-even 16-bit values (fp16 or bf16), a in the
+// low half: one packed conversion instruction for the pair.
+__device__ __forceinline__ uint32_t pack2_16(float a, float b, bool f16)
+{
+    if (f16) {
+        const __half2 h = __floats2half2_rn(a, b);
+        return *reinterpret_cast<const uint32_t *>(&h);
+    }
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// tcgen05.wait::ld that also names the loaded registers, so that no use of
+// them can be scheduled above the wait.
+__device__ __forceinline__ void tmem_wait_ld_regs(uint32_t (&r)[32])
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
+                   "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                   "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                   "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
+}
+
+// Epilogue of one warp (warps 2 .. 2 + NEPI - 1 of the block).  NEPI = 8: two
+// warps per TMEM lane quadrant, each taking every other 32-channel chunk of
+// the accumulator; NEPI = 4: one warp per quadrant takes every chunk.
+// BOXED: the tile's pixels are 2-D boxes (box_w x box_h) of one image (or of
+// the stacked images); otherwise runs of box_w consecutive flattened pixels
+// (the direct mode).
+template <int BN, bool BOXED, int NEPI = kEpiWarps>
+__device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtensorMap *map_c,
+                                              uint32_t tmem_base, uint64_t *tfull,
+                                              uint64_t *tempty, uint8_t *stage_out,
+                                              volatile int *abort_flag, int warp, int lane,
+                                              int box_px)
+{
+    // The warp owns TMEM lanes 32q..32q+31 (32 pixels of the tile) and the
+    // chunks h, h+2, ... of the BN accumulator columns.  Lane 0 waits for the
+    // accumulator and shares the outcome, so the warp stays converged.  The
+    // load of the warp's next chunk is issued before the current one is
+    // processed.  With TMA stores the warp stages its 32 pixels x 32 channels
+    // in its own 4 KB of shared memory and lane 0 writes them as one box.
+    static_assert(NEPI == 4 || NEPI == 8, "one or two warps per TMEM lane quadrant");
+    constexpr int kSplit = NEPI / 4;            // warps sharing a quadrant
+    constexpr int kChunks = BN / 32;            // 2, 4 or 8
+    constexpr int kMine = kChunks / kSplit;     // chunks per warp
+    const int q = warp & 3;                     // TMEM lane quadrant of this warp
+    const int h = (warp - 2) >> 2;              // which share of the chunks (0 when NEPI = 4)
+    const int row = q * 32 + lane;              // tile row = pixel
+    const int bi = row / box_px, bj = row - bi * box_px;
+    const int wbi = (q * 32) / box_px;          // the warp's box
+    const int wj0 = (q * 32) - wbi * box_px;    // its first pixel in the box
+    const int bj_y = bj / p.box_w, bj_x = bj - bj_y * p.box_w;
+    const int wj0_y = wj0 / p.box_w, wj0_x = wj0 - wj0_y * p.box_w;
+    const long long howo = (long long)p.Ho * p.Wo;
+    const int ec = p.ws ? 4 : (p.out_dt == BIGEMM_F32 ? 4 : 2);
+    uint8_t *wstage = stage_out + (warp - 2) * 4096;
+    const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+        const Unit w = decode(p, u);
+        // where this lane's pixel and this warp's store box go: computed
+        // before the accumulator is ready
+        const int b = w.pt * p.bpt + bi;
+        bool valid = bi < p.bpt && b < p.total_boxes;
+        long long base = 0;
+        if (valid) {
+            uint32_t urem;
+            int n = (int)fd_divmod((uint32_t)b, p.fd_bpi, &urem);
+            const int rem = (int)urem;
+            long long pix;
+            if (BOXED) {
+                const int byi = (int)fd_divmod((uint32_t)rem, p.fd_bx, &urem), bxi = (int)urem;
+                int y = byi * p.box_h + bj_y;
+                const int x = bxi * p.box_w + bj_x;
+                if (p.hp) {                     // stacked images: row -> (image, row)
+                    n = (int)fd_divmod((uint32_t)y, p.fd_hp, &urem);
+                    y = (int)urem;
+                }
+                valid = n < p.N && y < p.Ho && x < p.Wo;
+                pix = (long long)y * p.Wo + x;
+            } else {
+                pix = (long long)rem * p.box_w + bj;
+                valid = pix < howo;
+            }
+            base = (long long)w.sp * p.out_elems + (long long)n * p.CO * howo + pix;
+        }
+        // the warp's store box (TMA mode): origin and image index
+        const int wb = w.pt * p.bpt + wbi;
+        const bool wbox = p.store_tma && wbi < p.bpt && wb < p.total_boxes;
+        int sx = 0, sy = 0, sn = 0;
+        if (wbox) {
+            uint32_t urem;
+            int n = (int)fd_divmod((uint32_t)wb, p.fd_bpi, &urem);
+            const int rem = (int)urem;
+            if (BOXED) {
+                const int byi = (int)fd_divmod((uint32_t)rem, p.fd_bx, &urem), bxi = (int)urem;
+                sx = bxi * p.box_w + wj0_x;
+                sy = byi * p.box_h + wj0_y;
+                if (p.hp) {                     // the warp's rows lie in one image (hp % rows == 0)
+                    n = (int)fd_divmod((uint32_t)sy, p.fd_hp, &urem);
+                    sy = (int)urem;
+                }
+            } else {
+                sx = rem * p.box_w + wj0;
+            }
+            sn = w.sp * p.N + n;
+        }
+        const bool wstore = wbox && sn < (w.sp + 1) * p.N;
+        int okw = 0;
+        if (lane == 0) okw = mbar_wait(&tfull[acc], acc_phase, p.timeout_ns, abort_flag, p.err);
+        if (!__shfl_sync(0xffffffffu, okw, 0)) break;
+        tc_fence_after();
+        const uint32_t acc_col = lane_base + (uint32_t)(acc * BN);
+        uint32_t ra[32], rb[32];
+        tmem_ld_32x32b_x32(acc_col + (uint32_t)(h * 32), ra);
+        const int co0 = w.ct * BN;
+#pragma unroll
+        for (int i = 0; i < kMine; ++i) {
+            uint32_t(&cur)[32] = (i & 1) ? rb : ra;
+            uint32_t(&nxt)[32] = (i & 1) ? ra : rb;
+            tmem_wait_ld_regs(cur);
+            if (i + 1 < kMine) {
+                tmem_ld_32x32b_x32(acc_col + (uint32_t)((h + kSplit * (i + 1)) * 32), nxt);
+            } else {                            // accumulator drained by this warp: hand it back
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[acc]);
+            }
+            const int cb = co0 + (h + kSplit * i) * 32;
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(cur[j]);
+            if (!p.ws && p.epi != BIGEMM_EPI_NONE) {
+                float bv[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) bv[j] = cb + j < p.CO ? __ldg(p.bias + cb + j) : 0.f;
+                if (p.epi == BIGEMM_EPI_BIAS) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] += bv[j];
+                } else if (p.epi == BIGEMM_EPI_BIAS_EXP) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = expf(v[j] + bv[j]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = rsqrtf(v[j] + bv[j] + p.eps);
+                }
+            }
+            if (wstore) {
+                if (lane == 0) bulk_wait_read<0>();   // the previous store has read the buffer
+                __syncwarp();
+                uint8_t *dst = wstage + lane * ec;
+                if (ec == 4) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) *reinterpret_cast<float *>(dst + j * 128) = v[j];
+                } else {
+                    // two channels per conversion (cvt.rn.{f16,bf16}x2.f32), one per 16-bit store
+#pragma unroll
+                    for (int j = 0; j < 32; j += 2) {
+                        const uint32_t pk = pack2_16(v[j], v[j + 1], p.out_dt == BIGEMM_F16);
+                        *reinterpret_cast<uint16_t *>(dst + j * 64) = (uint16_t)(pk & 0xFFFFu);
+                        *reinterpret_cast<uint16_t *>(dst + (j + 1) * 64) = (uint16_t)(pk >> 16);
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    if (BOXED)
+                        tma_store_4d(map_c, wstage, sx, sy, cb, sn);
+                    else
+                        tma_store_3d(map_c, wstage, sx, cb, sn);
+                    bulk_commit();
+                }
+            } else if (!p.store_tma && valid) {
+                const long long o0 = base + (long long)cb * howo;
+                const int jn = min(32, p.CO - cb);
+                if (p.ws) {
+                    float *o = p.ws + o0;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (j < jn) o[j * howo] = v[j];
+                } else if (p.out_dt == BIGEMM_F32) {
+                    float *o = static_cast<float *>(p.out) + o0;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (j < jn) o[j * howo] = v[j];
+                } else {
+                    uint16_t *o = static_cast<uint16_t *>(p.out) + o0;
+                    const bool f16 = p.out_dt == BIGEMM_F16;
+#pragma unroll
+                    for (int j = 0; j < 32; j += 2) {
+                        const uint32_t pk = pack2_16(v[j], v[j + 1], f16);
+                        if (j < jn) o[j * howo] = (uint16_t)(pk & 0xFFFFu);
+                        if (j + 1 < jn) o[(j + 1) * howo] = (uint16_t)(pk >> 16);
+                    }
+                }
+            }
+        }
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+    }
+    if (lane == 0) bulk_wait<0>();              // stores complete before the block exits
+}
+
+
+}  // namespace
+}  // namespace bigemm
