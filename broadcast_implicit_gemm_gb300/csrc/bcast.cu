@@ -62,7 +62,7 @@ __global__ void __launch_bounds__(256) bcast_kernel(int N, int C, long long HW, 
                                                     const float *__restrict__ var, float eps,
                                                     T *__restrict__ out)
 {
-    griddep_wait();
+    griddep_enter();
     const int c = blockIdx.x;
     const T tv = cvt<T>(bc_op(op, __ldg(var + c), eps));   // once per thread
     if (VEC) {
@@ -86,7 +86,7 @@ __global__ void __launch_bounds__(256) bcast_flat_kernel(long long total, int C,
                                                          int op, const float *__restrict__ var,
                                                          float eps, T *__restrict__ out)
 {
-    griddep_wait();
+    griddep_enter();
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
          i += (long long)gridDim.x * blockDim.x) {
         const int c = (int)((i / HW) % C);

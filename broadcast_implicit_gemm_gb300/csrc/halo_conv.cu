@@ -40,6 +40,10 @@ struct HaloCfg {
 // of its taps fit in shared memory, the producer loads B once (one tap per
 // copy, every channel block) and only the input halos stream.
 constexpr int kHaloMaxA = 4;   // halo stages at most
+constexpr int kHaloMaxB = 6;   // streamed weight stages at most
+// Epilogue warps of the halo kernels: two per TMEM lane quadrant (measured:
+// with one, the 256-channel exp epilogue of the fused layer limits the kernel).
+constexpr int kHaloEpi = kEpiWarps;
 
 template <int BN, int FMT, bool RES>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -48,7 +52,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                           const __grid_constant__ CUtensorMap map_c, const UmmaParams p)
 {
     using C = HaloCfg<BN>;
-    constexpr int SAMAX = kHaloMaxA, SB = RES ? 1 : C::b_stages;
+    constexpr int SAMAX = kHaloMaxA, SBMAX = RES ? 1 : kHaloMaxB;
+    const int SB = RES ? 1 : p.halo_sb;
     constexpr int TB = RES ? 1 : C::tb;
     // shared-memory layout computed on the host (halo_layout): halo stages,
     // weights, output staging, barriers
@@ -63,8 +68,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *a_full = reinterpret_cast<uint64_t *>(smem + p.halo_bar_off);
     uint64_t *a_empty = a_full + SAMAX;
     uint64_t *b_full = a_empty + SAMAX;
-    uint64_t *b_empty = b_full + SB;
-    uint64_t *tfull = b_empty + SB;
+    uint64_t *b_empty = b_full + SBMAX;
+    uint64_t *tfull = b_empty + SBMAX;
     uint64_t *tempty = tfull + 2;
     uint64_t *drain = tempty + 2;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain + 1);
@@ -75,7 +80,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < SA; ++i) mbar_init(&a_full[i], 1), mbar_init(&a_empty[i], 1);
         for (int i = 0; i < SB; ++i) mbar_init(&b_full[i], 1), mbar_init(&b_empty[i], 1);
-        for (int i = 0; i < 2; ++i) mbar_init(&tfull[i], 1), mbar_init(&tempty[i], kEpiWarps);
+        for (int i = 0; i < 2; ++i) mbar_init(&tfull[i], 1), mbar_init(&tempty[i], kHaloEpi);
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -92,17 +97,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
-    griddep_wait();   // the set-up above overlapped the previous kernel; its data is ready now
+    griddep_enter();   // the set-up above overlapped the previous kernel; its data is ready now
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
             int as = 0, bs = 0;
             uint32_t aph = 0, bph = 0;
-            uint32_t a_par[SAMAX], b_par[SB];
-            bool a_iss[SAMAX], b_iss[SB];
+            uint32_t a_par[SAMAX], b_par[SBMAX];
+            bool a_iss[SAMAX], b_iss[SBMAX];
             for (int i = 0; i < SAMAX; ++i) a_iss[i] = false, a_par[i] = 0;
-            for (int i = 0; i < SB; ++i) b_iss[i] = false, b_par[i] = 0;
+            for (int i = 0; i < SBMAX; ++i) b_iss[i] = false, b_par[i] = 0;
             bool ok = true;
             if (RES) {
                 // every tap of every channel block, once, on b_full[0]
@@ -237,12 +242,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_wait(drain, 0, p.timeout_ns, &local_abort, p.err);
             }
         }
-    } else {
-        epilogue_warp<BN, true>(p, &map_c, tmem_base, tfull, tempty, stage_out, abort_flag, warp,
-                                lane, 128);
+    } else if (warp < 2 + kHaloEpi) {
+        epilogue_warp<BN, true, kHaloEpi>(p, &map_c, tmem_base, tfull, tempty, stage_out,
+                                          abort_flag, warp, lane, 128);
     }
 
-    griddep_launch_dependents();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -288,28 +292,37 @@ cudaError_t dispatch_halo_bn(int bn, const UmmaParams &p, const CUtensorMap &ma,
 bool halo_layout(int bn, bool res, int kh, int kk, int ci_blocks, int smem_limit, UmmaParams &p)
 {
     const uint32_t a_stride = (uint32_t)(16 + kh - 1) * kHaloRowBytes;
-    const long long b_ll = res ? (long long)ci_blocks * kk * bn * kRowBytes
-                               : (long long)HaloCfg<64>::b_stages * HaloCfg<64>::b_bytes;
-    if (b_ll >= (1ll << 20)) return false;
-    const uint32_t b_bytes = (uint32_t)b_ll;
-    const uint32_t staging = (uint32_t)kEpiWarps * 4096u;
-    const uint32_t bars = (2 * kHaloMaxA + 2 * HaloCfg<64>::b_stages + 5) * 8 + 16;
-    for (int sa = kHaloMaxA; sa >= 2; --sa) {
-        const uint32_t b_off = (uint32_t)sa * a_stride;
-        const uint32_t stage_off = b_off + b_bytes;
-        const uint32_t bar_off = stage_off + staging;
-        const uint32_t total = bar_off + bars + 1024;
-        if (total <= (uint32_t)smem_limit) {
-            p.halo_sa = sa;
-            p.halo_b_off = (int)b_off;
-            p.halo_stage_off = (int)stage_off;
-            p.halo_bar_off = (int)bar_off;
-            p.halo_smem = (int)total;
-            p.res_b_bytes = res ? (int)b_bytes : 0;
-            return true;
-        }
+    const long long res_ll = (long long)ci_blocks * kk * bn * kRowBytes;
+    if (res && res_ll >= (1ll << 20)) return false;
+    const uint32_t stage_b = (uint32_t)HaloCfg<64>::b_bytes;    // one streamed weight stage
+    const uint32_t staging = (uint32_t)kHaloEpi * 4096u;
+    const uint32_t bars = (2 * kHaloMaxA + 2 * kHaloMaxB + 5) * 8 + 16;
+    const uint32_t fixed = staging + bars + 1024;
+    // resident weights: as many halo stages as fit; streamed: two halo stages
+    // and as deep a weight ring as fits (then a third halo stage if room is left)
+    int best_sa = 0, best_sb = 0;
+    uint32_t b_bytes = 0;
+    if (res) {
+        for (int sa = kHaloMaxA; sa >= 2 && !best_sa; --sa)
+            if ((uint32_t)sa * a_stride + (uint32_t)res_ll + fixed <= (uint32_t)smem_limit)
+                best_sa = sa, best_sb = 1, b_bytes = (uint32_t)res_ll;
+    } else {
+        for (int sb = kHaloMaxB; sb >= 2 && !best_sa; --sb)
+            if (2u * a_stride + (uint32_t)sb * stage_b + fixed <= (uint32_t)smem_limit)
+                best_sa = 2, best_sb = sb, b_bytes = (uint32_t)sb * stage_b;
+        while (best_sa > 0 && best_sa < kHaloMaxA &&
+               (uint32_t)(best_sa + 1) * a_stride + b_bytes + fixed <= (uint32_t)smem_limit)
+            ++best_sa;
     }
-    return false;
+    if (!best_sa) return false;
+    p.halo_sa = best_sa;
+    p.halo_sb = best_sb;
+    p.halo_b_off = (int)((uint32_t)best_sa * a_stride);
+    p.halo_stage_off = p.halo_b_off + (int)b_bytes;
+    p.halo_bar_off = p.halo_stage_off + (int)staging;
+    p.halo_smem = p.halo_bar_off + (int)bars + 1024;
+    p.res_b_bytes = res ? (int)b_bytes : 0;
+    return true;
 }
 
 size_t halo_smem_bytes(int bn)

@@ -81,9 +81,10 @@ struct UmmaParams {
     int hp;                         // A_HALO over stacked images: rows per image (H + pad)
                                     // in the packed data and in tile row space; 0 otherwise
     int res_b_bytes;                // A_HALO with resident weights: bytes of every tap (0: streamed)
-    // A_HALO shared-memory layout (halo_layout): halo stages, byte offsets of the
-    // weights, the output staging and the barriers, and the total
-    int halo_sa, halo_b_off, halo_stage_off, halo_bar_off, halo_smem;
+    // A_HALO shared-memory layout (halo_layout): halo stages, streamed weight
+    // stages, byte offsets of the weights, the output staging and the
+    // barriers, and the total
+    int halo_sa, halo_sb, halo_b_off, halo_stage_off, halo_bar_off, halo_smem;
     // divisors of the index arithmetic; launch_umma_conv fills them from the fields above
     FastDiv fd_co, fd_pix, fd_bpi, fd_bx, fd_hp, fd_cib, fd_kw;
 };

@@ -34,7 +34,7 @@ template <typename T>
 __global__ void pack_nhwc_kernel(const T *__restrict__ x, T *__restrict__ xh, int C, int HW,
                                  int Ch)
 {
-    griddep_wait();
+    griddep_enter();
     __shared__ T tile[32][33];
     const int n = blockIdx.z;
     const int p0 = blockIdx.x * 32, c0 = blockIdx.y * 32;
@@ -64,7 +64,7 @@ __global__ void __launch_bounds__(256) pack_nhwc_vec_kernel(const T *__restrict_
                                                             T *__restrict__ xh, int C, int HW,
                                                             int Ch)
 {
-    griddep_wait();
+    griddep_enter();
     constexpr int VEC = 16 / sizeof(T);
     constexpr int TILE = 8 * VEC;
     __shared__ T tile[TILE][TILE + 1];
@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(256) pack_operands_kernel(const T *__restrict_
                                                             T *__restrict__ wp, int CO, int CI,
                                                             int KHKW, int cip)
 {
-    griddep_wait();
+    griddep_enter();
     constexpr int VEC = 16 / sizeof(T);
     constexpr int TILE = 8 * VEC;
     static_assert(TILE * (TILE + 1) * sizeof(T) <= kPackSmemBytes, "tile fits the buffer");
@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(256) pack_remap_kernel(const T *__restrict__ x
                                                          T *__restrict__ wp, int CO, int CI,
                                                          int KHKW, int cip)
 {
-    griddep_wait();
+    griddep_enter();
     constexpr int VEC = 16 / sizeof(T);
     constexpr int TILE = 8 * VEC;
     static_assert(256 % TILE == 0, "a thread keeps one pixel column");
@@ -304,7 +304,7 @@ __global__ void splitk_reduce_kernel(const float *__restrict__ ws, int split, lo
                                      int CO, int HoWo, int epi, const float *__restrict__ bias,
                                      float eps, TO *__restrict__ out)
 {
-    griddep_wait();
+    griddep_enter();
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < elems;
          i += (long long)gridDim.x * blockDim.x) {
         float s = ws[i];

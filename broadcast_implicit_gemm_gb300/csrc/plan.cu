@@ -1208,7 +1208,7 @@ bigemm_status conv2d_nchw_plan_describe(bigemm_plan plan, char *buf, size_t len)
            << ", \"pix_tiles\": " << p.pix_tiles << ", \"co_tiles\": " << p.co_tiles
            << ", \"units\": " << p.units << ", \"grid\": " << plan->g.grid
            << ", \"smem\": " << (c.t.amode == A_HALO ? (size_t)p.halo_smem : umma_smem_bytes(c.t))
-           << ", \"halo_stages\": " << p.halo_sa
+           << ", \"halo_stages\": " << p.halo_sa << ", \"weight_stages\": " << p.halo_sb
            << ", \"store\": \"" << (plan->store_tma ? "tma" : "direct") << "\"";
     }
     os << ", \"launches\": " << launches_per_run(plan)

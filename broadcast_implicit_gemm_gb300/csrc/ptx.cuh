@@ -29,6 +29,16 @@ __device__ __forceinline__ void griddep_launch_dependents()
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Kernel entry of the library's launches: wait for the previous grid, then let
+// the next one launch at once, so its launch and set-up overlap this grid.
+// Safe because every kernel of the library waits before it reads anything the
+// grid before it writes (griddepcontrol.wait waits for that grid to finish).
+__device__ __forceinline__ void griddep_enter()
+{
+    griddep_wait();
+    griddep_launch_dependents();
+}
+
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
 {

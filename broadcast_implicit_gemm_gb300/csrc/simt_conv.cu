@@ -72,7 +72,7 @@ __global__ void __launch_bounds__(256) conv_tiled_kernel(SimtArgs a, const void 
                                                          const float *__restrict__ bias,
                                                          void *__restrict__ out)
 {
-    griddep_wait();
+    griddep_enter();
     __shared__ __align__(16) float ws[TK][TM];
     __shared__ __align__(16) float xs[TK][TN];
     const int n = blockIdx.z;
@@ -143,7 +143,7 @@ __global__ void conv_naive_kernel(SimtArgs a, const void *__restrict__ x,
                                   const void *__restrict__ w, const float *__restrict__ bias,
                                   void *__restrict__ out)
 {
-    griddep_wait();
+    griddep_enter();
     const long long total = (long long)a.N * a.CO * a.Ho * a.Wo;
     const int cig = a.CI / a.groups, cog = a.CO / a.groups;
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(256) conv_depthwise_kernel(SimtArgs a, int row
                                                              const float *__restrict__ bias,
                                                              void *__restrict__ out)
 {
-    griddep_wait();
+    griddep_enter();
     extern __shared__ float sm[];
     const int KH = K ? K : a.KH, KW = K ? K : a.KW, st = S ? S : a.stride;
     const int nplanes = a.N * a.CI;
@@ -441,7 +441,7 @@ __global__ void __launch_bounds__(128) dw_stream_kernel(SimtArgs a, int gx, int 
                                                         void *__restrict__ out, int vec_in,
                                                         int vec_out)
 {
-    griddep_wait();
+    griddep_enter();
     constexpr int XO = kDwsXO;
     constexpr int P = K / 2;
     constexpr int VE = DwIn<DT>::VE;

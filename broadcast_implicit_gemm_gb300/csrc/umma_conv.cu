@@ -81,7 +81,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
-    griddep_wait();   // the set-up above overlapped the previous kernel; its data is ready now
+    griddep_enter();   // the set-up above overlapped the previous kernel; its data is ready now
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
@@ -216,7 +216,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              abort_flag, warp, lane, box_px);
     }
 
-    griddep_launch_dependents();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
