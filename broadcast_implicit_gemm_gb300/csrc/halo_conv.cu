@@ -42,10 +42,24 @@ struct HaloCfg {
 constexpr int kHaloMaxA = 4;   // halo stages at most
 constexpr int kHaloMaxB = 6;   // streamed weight stages at most
 // Epilogue warps of the halo kernels: two per TMEM lane quadrant (measured:
-// with one, the 256-channel exp epilogue of the fused layer limits the kernel).
+// with one, the 256-channel exp epilogue of the fused layer limits the kernel),
+// each staging 2 KB of output at a time, so that the room goes to the weight
+// ring (measured: the MMA thread waited on weight tiles for a third of its loop
+// with three 32 KB stages).
 constexpr int kHaloEpi = kEpiWarps;
+constexpr int kHaloStage = 2048;
 
-template <int BN, int FMT, bool RES>
+// MT = 2: a unit is two 16-row tiles stacked vertically (32 output rows x 8
+// columns) that share every weight tile, so the weights cost half as many
+// bytes per MMA; the two 128-pixel accumulators sit BN columns apart.
+template <int BN, int MT>
+struct HaloTmem {
+    static constexpr uint32_t cols = (2 * MT * BN <= 64) ? 64 : (2 * MT * BN <= 128) ? 128
+                                     : (2 * MT * BN <= 256) ? 256 : 512;
+    static_assert(2 * MT * BN <= 512, "two accumulators of MT tiles must fit TMEM");
+};
+
+template <int BN, int FMT, bool RES, int MT>
 __global__ void __launch_bounds__(kThreads, 1)
     umma_conv_halo_kernel(const __grid_constant__ CUtensorMap map_a,
                           const __grid_constant__ CUtensorMap map_b,
@@ -54,13 +68,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     using C = HaloCfg<BN>;
     constexpr int SAMAX = kHaloMaxA, SBMAX = RES ? 1 : kHaloMaxB;
     const int SB = RES ? 1 : p.halo_sb;
-    constexpr int TB = RES ? 1 : C::tb;
+    // taps per weight copy: 32 KB copies, or one tap with resident weights or two M tiles
+    constexpr int TB = (RES || MT == 2) ? 1 : C::tb;
+    constexpr int BB = TB * BN * kRowBytes;   // bytes of one streamed weight stage
     // shared-memory layout computed on the host (halo_layout): halo stages,
     // weights, output staging, barriers
     const int SA = p.halo_sa;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    const uint32_t halo_bytes = (uint32_t)(16 + p.KH - 1) * kHaloRowBytes;
+    const uint32_t halo_bytes = (uint32_t)(16 * MT + p.KH - 1) * kHaloRowBytes;
     const uint32_t a_stride = halo_bytes;
     uint8_t *sa = smem;
     uint8_t *sb = smem + p.halo_b_off;
@@ -90,7 +106,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (warp == 1) {
         __syncwarp();
-        tmem_alloc(tmem_holder, C::tmem_cols);
+        tmem_alloc(tmem_holder, HaloTmem<BN, MT>::cols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -123,7 +139,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t urem;
                 const int n = (int)fd_divmod((uint32_t)w.pt, p.fd_bpi, &urem);
                 const int byi = (int)fd_divmod(urem, p.fd_bx, &urem), bxi = (int)urem;
-                const int x0 = bxi * 8 - p.pad, y0 = byi * 16 - p.pad;
+                const int x0 = bxi * 8 - p.pad, y0 = byi * (16 * MT) - p.pad;
                 const int ncol = w.ct * BN;
                 for (int cb = w.kb0; ok && cb < w.kb1; ++cb) {
                     if (!mbar_wait(&a_empty[as], aph ^ 1u, p.timeout_ns, abort_flag, p.err)) {
@@ -139,9 +155,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ok = false;
                             break;
                         }
-                        mbar_arrive_expect_tx(&b_full[bs], (uint32_t)C::b_bytes);
+                        mbar_arrive_expect_tx(&b_full[bs], (uint32_t)BB);
                         b_iss[bs] = true, b_par[bs] = bph;
-                        tma_load_3d(sb + bs * C::b_bytes, &map_b, &b_full[bs], cb * p.bk, ncol, t0);
+                        tma_load_3d(sb + bs * BB, &map_b, &b_full[bs], cb * p.bk, ncol, t0);
                         if (++bs == SB) bs = 0, bph ^= 1u;
                     }
                 }
@@ -169,7 +185,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true, any = false;
             if (RES && blockIdx.x < p.units)
                 ok = mbar_wait(&b_full[0], 0, p.timeout_ns, abort_flag, p.err);
-            const uint32_t b_res0 = desc_lo(smem_u32(sb), 16u);
+            const uint32_t b_res0 = desc_lo(smem_u32(sb), 16u);   // resident weights
+            const uint32_t b_ring0 = b_res0;                        // or the first ring slot
             for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
                 const Unit w = decode(p, u);
                 if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, p.timeout_ns, abort_flag, p.err)) {
@@ -177,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * MT * BN);
                 uint32_t accum = 0;
                 for (int cb = w.kb0; ok && cb < w.kb1; ++cb) {
                     if (!mbar_wait(&a_full[as], aph, p.timeout_ns, abort_flag, p.err)) {
@@ -185,41 +202,83 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     const uint32_t a_lo0 = desc_lo(smem_u32(sa + as * a_stride), 16u);
-                    int ry = 0, rx = 0;
-                    if (RES) {
+                    const uint32_t acc_cb = accum;   // accumulate into the tile from the first MMA on?
+                    accum = 1u;
+                    if (p.KH == 3 && p.KW == 3) {
+                        // 3x3: every tap's A start and B slot are constants, the loop unrolls
+                        constexpr uint32_t kTapOff[9] = {0, 8, 16, 128, 136, 144, 256, 264, 272};
+                        constexpr uint32_t kBStep = (uint32_t)(BN * kRowBytes) >> 4;
+                        constexpr uint32_t kMStep = (16u * kHaloRowBytes) >> 4;   // 16 rows down
+                        if (RES) {
+                            tc_fence_after();
+                            const uint32_t b_lo = b_res0 + (uint32_t)(cb * 9) * kBStep;
+#pragma unroll
+                            for (int t = 0; t < 9; ++t)
+#pragma unroll
+                                for (int m = 0; m < MT; ++m)
+                                    umma4_kmajor<FMT == 2>(d_tmem + m * BN, a_lo0 + kTapOff[t] + m * kMStep,
+                                                           a_hi, b_lo + (uint32_t)t * kBStep, b_hi,
+                                                           idesc, t == 0 ? acc_cb : 1u);
+                            any = true;
+                        } else {
+                            constexpr int NST = (9 + TB - 1) / TB;   // weight stages per channel block
+#pragma unroll
+                            for (int g = 0; g < NST; ++g) {
+                                if (!mbar_wait(&b_full[bs], bph, p.timeout_ns, abort_flag, p.err)) {
+                                    ok = false;
+                                    break;
+                                }
+                                tc_fence_after();
+                                const uint32_t b_lo = b_ring0 + (uint32_t)bs * ((uint32_t)BB >> 4);
+#pragma unroll
+                                for (int tt = 0; tt < TB; ++tt) {
+                                    const int t = g * TB + tt;
+                                    if (t < 9)
+#pragma unroll
+                                        for (int m = 0; m < MT; ++m)
+                                            umma4_kmajor<FMT == 2>(
+                                                d_tmem + m * BN, a_lo0 + kTapOff[t] + m * kMStep, a_hi,
+                                                b_lo + (uint32_t)tt * kBStep, b_hi, idesc,
+                                                t == 0 ? acc_cb : 1u);
+                                }
+                                any = true;
+                                umma_commit(&b_empty[bs]);
+                                if (++bs == SB) bs = 0, bph ^= 1u;
+                            }
+                        }
+                    } else if (RES) {
+                        int ry = 0, rx = 0;
                         tc_fence_after();
                         uint32_t b_lo = b_res0 + (uint32_t)(cb * KK) * ((uint32_t)(BN * kRowBytes) >> 4);
                         for (int t = 0; t < KK; ++t) {
                             const uint32_t a_lo =
                                 a_lo0 + (uint32_t)(ry * kHaloPitch + rx) * (kRowBytes >> 4);
-#pragma unroll
-                            for (int k = 0; k < 4; ++k) {
-                                umma_lohi<FMT == 2>(d_tmem, a_lo + k * 2u, a_hi, b_lo + k * 2u, b_hi,
-                                                    idesc, accum);
-                                accum = 1u;
-                            }
+                            for (int m = 0; m < MT; ++m)
+                                umma4_kmajor<FMT == 2>(d_tmem + m * BN,
+                                                       a_lo + m * ((16u * kHaloRowBytes) >> 4), a_hi,
+                                                       b_lo, b_hi, idesc, t == 0 ? acc_cb : 1u);
                             b_lo += (uint32_t)(BN * kRowBytes) >> 4;
                             if (++rx == p.KW) rx = 0, ++ry;
                         }
                         any = true;
                     } else {
+                        int ry = 0, rx = 0, t = 0;
                         for (int t0 = 0; t0 < KK; t0 += TB) {
                             if (!mbar_wait(&b_full[bs], bph, p.timeout_ns, abort_flag, p.err)) {
                                 ok = false;
                                 break;
                             }
                             tc_fence_after();
-                            uint32_t b_lo = desc_lo(smem_u32(sb + bs * C::b_bytes), 16u);
+                            uint32_t b_lo = b_ring0 + (uint32_t)bs * ((uint32_t)BB >> 4);
                             const int nt = min(TB, KK - t0);
-                            for (int tt = 0; tt < nt; ++tt) {
+                            for (int tt = 0; tt < nt; ++tt, ++t) {
                                 const uint32_t a_lo =
                                     a_lo0 + (uint32_t)(ry * kHaloPitch + rx) * (kRowBytes >> 4);
-#pragma unroll
-                                for (int k = 0; k < 4; ++k) {
-                                    umma_lohi<FMT == 2>(d_tmem, a_lo + k * 2u, a_hi, b_lo + k * 2u,
-                                                        b_hi, idesc, accum);
-                                    accum = 1u;
-                                }
+                                for (int m = 0; m < MT; ++m)
+                                    umma4_kmajor<FMT == 2>(d_tmem + m * BN,
+                                                           a_lo + m * ((16u * kHaloRowBytes) >> 4),
+                                                           a_hi, b_lo, b_hi, idesc,
+                                                           t == 0 ? acc_cb : 1u);
                                 b_lo += (uint32_t)(BN * kRowBytes) >> 4;
                                 if (++rx == p.KW) rx = 0, ++ry;
                             }
@@ -228,6 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (++bs == SB) bs = 0, bph ^= 1u;
                         }
                     }
+                    if (!ok) break;
                     umma_commit(&a_empty[as]);
                     if (++as == SA) as = 0, aph ^= 1u;
                 }
@@ -243,8 +303,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else if (warp < 2 + kHaloEpi) {
-        epilogue_warp<BN, true, kHaloEpi>(p, &map_c, tmem_base, tfull, tempty, stage_out,
-                                          abort_flag, warp, lane, 128);
+        epilogue_warp<BN, true, kHaloEpi, MT, kHaloStage>(p, &map_c, tmem_base, tfull, tempty,
+                                                          stage_out, abort_flag, warp, lane, 128);
     }
 
     tc_fence_before();
@@ -252,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     if (warp == 1) {
         __syncwarp();
-        tmem_dealloc(tmem_base, C::tmem_cols);
+        tmem_dealloc(tmem_base, HaloTmem<BN, MT>::cols);
     }
 }
 
@@ -262,9 +322,13 @@ cudaError_t launch_halo(const UmmaParams &p, const CUtensorMap &ma, const CUtens
 {
     int dev = 0;
     cudaGetDevice(&dev);
-    const int which = p.res_b_bytes > 0 ? 1 : 0;
-    auto kern = which ? umma_conv_halo_kernel<BN, FMT, true> : umma_conv_halo_kernel<BN, FMT, false>;
-    static unsigned long long attr_set[2] = {0, 0};   // bit per device: smem opt-in done
+    // resident weights take one M tile; two M tiles need 2 x 2 x BN <= 512 TMEM columns
+    const int mt = (p.box_h == 32 && BN <= 128) ? 2 : 1;
+    const int which = p.res_b_bytes > 0 ? 0 : mt;
+    auto kern = which == 0   ? umma_conv_halo_kernel<BN, FMT, true, 1>
+                : which == 1 ? umma_conv_halo_kernel<BN, FMT, false, 1>
+                             : umma_conv_halo_kernel<BN, FMT, false, (BN <= 128 ? 2 : 1)>;
+    static unsigned long long attr_set[3] = {0, 0, 0};   // bit per device: smem opt-in done
     if (dev >= 64 || !(attr_set[which] >> dev & 1ull)) {
         DeviceState *ds = device_state();
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -289,13 +353,15 @@ cudaError_t dispatch_halo_bn(int bn, const UmmaParams &p, const CUtensorMap &ma,
 
 }  // namespace
 
-bool halo_layout(int bn, bool res, int kh, int kk, int ci_blocks, int smem_limit, UmmaParams &p)
+bool halo_layout(int bn, bool res, int rows, int kh, int kk, int ci_blocks, int smem_limit,
+                 UmmaParams &p)
 {
-    const uint32_t a_stride = (uint32_t)(16 + kh - 1) * kHaloRowBytes;
+    const uint32_t a_stride = (uint32_t)(rows + kh - 1) * kHaloRowBytes;
     const long long res_ll = (long long)ci_blocks * kk * bn * kRowBytes;
     if (res && res_ll >= (1ll << 20)) return false;
-    const uint32_t stage_b = (uint32_t)HaloCfg<64>::b_bytes;    // one streamed weight stage
-    const uint32_t staging = (uint32_t)kHaloEpi * 4096u;
+    // one streamed weight stage: 32 KB, or a single tap for two-tile units
+    const uint32_t stage_b = rows == 32 ? (uint32_t)bn * kRowBytes : (uint32_t)HaloCfg<64>::b_bytes;
+    const uint32_t staging = (uint32_t)kHaloEpi * kHaloStage;
     const uint32_t bars = (2 * kHaloMaxA + 2 * kHaloMaxB + 5) * 8 + 16;
     const uint32_t fixed = staging + bars + 1024;
     // resident weights: as many halo stages as fit; streamed: two halo stages

@@ -96,9 +96,11 @@ cudaError_t launch_umma_conv(const UmmaTiling &t, int in_dt, const UmmaParams &p
                              const CUtensorMap &map_a, const CUtensorMap &map_b,
                              const CUtensorMap &map_c, int grid, cudaStream_t stream);
 size_t umma_smem_bytes(const UmmaTiling &t);
-// The halo kernel's shared-memory layout for a tiling (res: resident
-// weights), written into p; false when it does not fit in smem_limit bytes.
-bool halo_layout(int bn, bool res, int kh, int kk, int ci_blocks, int smem_limit, UmmaParams &p);
+// The halo kernel's shared-memory layout for a tiling (res: resident weights;
+// rows: output rows per tile, 16 or 32), written into p; false when it does
+// not fit in smem_limit bytes.
+bool halo_layout(int bn, bool res, int rows, int kh, int kk, int ci_blocks, int smem_limit,
+                 UmmaParams &p);
 // The halo-mode kernels (halo_conv.cu); fmt 0 f16, 1 bf16, 2 tf32.
 size_t halo_smem_bytes(int bn);
 cudaError_t launch_halo_conv(int bn, int fmt, const UmmaParams &p, const CUtensorMap &map_a,

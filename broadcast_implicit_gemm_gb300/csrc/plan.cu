@@ -224,7 +224,8 @@ UmmaGeom umma_geometry(const ConvShape &s0, const UmmaTiling &t, int sm_count)
         // shared-memory layout: streamed or resident weights
         DeviceState *ds = device_state();
         const int limit = ds ? ds->max_smem_optin : 232448;
-        g.fits = g.fits && halo_layout(t.bn, t.bres != 0, s.KH, s.KH * s.KW, p.ci_blocks, limit, p);
+        g.fits = g.fits && halo_layout(t.bn, t.bres != 0, t.box_h, s.KH, s.KH * s.KW, p.ci_blocks,
+                                       limit, p);
     }
     g.grid = (int)std::min<long long>(p.units, sm_count);
     return g;
@@ -268,7 +269,10 @@ bool umma_valid(const ConvShape &s0, const UmmaTiling &t, int sm_count, std::str
         if (s.stride != 1) return bad("halo mode needs stride 1");
         if (s.KH * s.KW < 2) return bad("halo mode is for kernels larger than 1x1");
         if (s.KH > 7 || s.KW > 8) return bad("halo mode holds up to 7 rows x 8 columns of taps");
-        if (t.box_w != 8 || t.box_h != 16 || t.bpt != 1) return bad("halo tile is 8 x 16 pixels");
+        if (t.box_w != 8 || (t.box_h != 16 && t.box_h != 32) || t.bpt != 1)
+            return bad("halo tile is 8 x 16 pixels, or two of them stacked (8 x 32)");
+        if (t.box_h == 32 && (t.bn > 128 || t.bres))
+            return bad("two-tile halo units need BN <= 128 and streamed weights");
     } else {
         if (s.stride > 8) return bad("stride > 8");
         if (t.box_w < 1 || t.box_h < 1) return bad("empty box");
@@ -532,6 +536,8 @@ std::vector<Cand> candidates(const ConvShape &s, int sms)
         } else if (amode == A_HALO) {
             bx.push_back({8, 16});
             bpts.push_back(1);
+            bx.push_back({8, 32});   // two tiles sharing each weight tile
+            bpts.push_back(1);
         } else {
             for (size_t i = 0; i < boxes.size() && bx.size() < 2; ++i) {
                 if (i > 0 && boxes[i].eff < boxes[0].eff - 0.05) break;
@@ -618,7 +624,9 @@ bool encode_store_map(bigemm_plan_s *p, void *dst, bool is_ws)
     const uint64_t str[3] = {(uint64_t)s.Wo * ec, (uint64_t)s.Ho * s.Wo * ec,
                              (uint64_t)s.CO * s.Ho * s.Wo * ec};
     const uint32_t sw = t.box_w >= 32 ? 32u : (uint32_t)t.box_w;
-    const uint32_t box[4] = {sw, 32u / sw, 32u, 1u};
+    // the halo kernel stages 2 KB per warp: 4-byte outputs go 16 channels per box
+    const uint32_t co_box = (t.amode == A_HALO && ec == 4) ? 16u : 32u;
+    const uint32_t box[4] = {sw, 32u / sw, co_box, 1u};
     const uint32_t es[4] = {1u, 1u, 1u, 1u};
     return encode_tiled(&p->map_c, dt, 4, dst, dims, str, box, es, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
@@ -655,14 +663,14 @@ bigemm_status setup_plan(bigemm_plan_s *p)
         const uint64_t dims[4] = {(uint64_t)p->g.ch, (uint64_t)s.W, rows, imgs};
         const uint64_t str[3] = {p->g.ch * e, (uint64_t)s.W * p->g.ch * e,
                                  rows * s.W * p->g.ch * e};
-        const uint32_t box[4] = {(uint32_t)p->g.p.bk, 16u, (uint32_t)(16 + s.KH - 1), 1u};
+        const uint32_t box[4] = {(uint32_t)p->g.p.bk, 16u, (uint32_t)(t.box_h + s.KH - 1), 1u};
         const uint32_t es[4] = {1u, 1u, 1u, 1u};
         if (!encode_tiled(&p->map_a, tma_dt(s.in_dt), 4, p->xh, dims, str, box, es,
                           CU_TENSOR_MAP_SWIZZLE_128B))
             return BIGEMM_ERR_UNSUPPORTED;
         // packed weights [CO][tap][cip] viewed as (channel, output channel, tap):
         // one box brings TB taps, each a [BN][128 B] K-major tile
-        const int tb = t.bres ? 1 : 32768 / (t.bn * 128);
+        const int tb = (t.bres || t.box_h == 32) ? 1 : 32768 / (t.bn * 128);
         const uint64_t kk = (uint64_t)s.KH * s.KW;
         const uint64_t bd[3] = {(uint64_t)p->g.cip, (uint64_t)s.CO, kk};
         const uint64_t bs[2] = {kk * p->g.cip * e, (uint64_t)p->g.cip * e};

@@ -342,6 +342,54 @@ __device__ __forceinline__ void umma_lohi(uint32_t d_tmem, uint32_t a_lo, uint32
             : "memory");
 }
 
+// The four MMAs of one 128-byte K block of K-major, 128-byte swizzled operands
+// (the start address advances 32 bytes, 2 in descriptor units, per MMA) in one
+// asm block: the first accumulates when `accum_first` != 0, the rest always.
+// One issuing thread pays for every instruction between MMAs, so the block
+// keeps that to two adds and two register pairings per MMA.
+template <bool TF32>
+__device__ __forceinline__ void umma4_kmajor(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
+                                             uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
+                                             uint32_t accum_first)
+{
+    if (TF32)
+        asm volatile(
+            "{\n\t.reg .pred p, q;\n\t.reg .b64 ad, bd;\n\t.reg .b32 al, bl;\n\t"
+            "setp.ne.b32 p, %6, 0;\n\t"
+            "setp.eq.b32 q, %6, %6;\n\t"
+            "mov.b64 ad, {%1, %2};\n\tmov.b64 bd, {%3, %4};\n\t"
+            "tcgen05.mma.cta_group::1.kind::tf32 [%0], ad, bd, %5, p;\n\t"
+            "add.u32 al, %1, 2;\n\tadd.u32 bl, %3, 2;\n\t"
+            "mov.b64 ad, {al, %2};\n\tmov.b64 bd, {bl, %4};\n\t"
+            "tcgen05.mma.cta_group::1.kind::tf32 [%0], ad, bd, %5, q;\n\t"
+            "add.u32 al, %1, 4;\n\tadd.u32 bl, %3, 4;\n\t"
+            "mov.b64 ad, {al, %2};\n\tmov.b64 bd, {bl, %4};\n\t"
+            "tcgen05.mma.cta_group::1.kind::tf32 [%0], ad, bd, %5, q;\n\t"
+            "add.u32 al, %1, 6;\n\tadd.u32 bl, %3, 6;\n\t"
+            "mov.b64 ad, {al, %2};\n\tmov.b64 bd, {bl, %4};\n\t"
+            "tcgen05.mma.cta_group::1.kind::tf32 [%0], ad, bd, %5, q;\n\t}" ::"r"(d_tmem),
+            "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accum_first)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p, q;\n\t.reg .b64 ad, bd;\n\t.reg .b32 al, bl;\n\t"
+            "setp.ne.b32 p, %6, 0;\n\t"
+            "setp.eq.b32 q, %6, %6;\n\t"
+            "mov.b64 ad, {%1, %2};\n\tmov.b64 bd, {%3, %4};\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %5, p;\n\t"
+            "add.u32 al, %1, 2;\n\tadd.u32 bl, %3, 2;\n\t"
+            "mov.b64 ad, {al, %2};\n\tmov.b64 bd, {bl, %4};\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %5, q;\n\t"
+            "add.u32 al, %1, 4;\n\tadd.u32 bl, %3, 4;\n\t"
+            "mov.b64 ad, {al, %2};\n\tmov.b64 bd, {bl, %4};\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %5, q;\n\t"
+            "add.u32 al, %1, 6;\n\tadd.u32 bl, %3, 6;\n\t"
+            "mov.b64 ad, {al, %2};\n\tmov.b64 bd, {bl, %4};\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %5, q;\n\t}" ::"r"(d_tmem),
+            "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accum_first)
+            : "memory");
+}
+
 // Instruction descriptor for kind::f16 / kind::tf32 with an fp32 accumulator:
 // operand format (0 f16, 1 bf16, 2 tf32) for A and B, major-ness of A and B
 // (0 K-major, 1 MN-major), N >> 3 at bit 17, M >> 4 at bit 24.

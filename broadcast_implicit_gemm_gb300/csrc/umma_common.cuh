@@ -78,11 +78,16 @@ __device__ __forceinline__ void tmem_wait_ld_regs(uint32_t (&r)[32])
 
 // Epilogue of one warp (warps 2 .. 2 + NEPI - 1 of the block).  NEPI = 8: two
 // warps per TMEM lane quadrant, each taking every other 32-channel chunk of
-// the accumulator; NEPI = 4: one warp per quadrant takes every chunk.
+// the accumulator; NEPI = 4: one warp per quadrant takes every chunk.  MT = 2:
+// a unit is two 128-pixel M tiles stacked vertically (box_h = 32 rows of a
+// halo tile), with accumulators at TMEM columns acc * 2BN and acc * 2BN + BN.
 // BOXED: the tile's pixels are 2-D boxes (box_w x box_h) of one image (or of
 // the stacked images); otherwise runs of box_w consecutive flattened pixels
 // (the direct mode).
-template <int BN, bool BOXED, int NEPI = kEpiWarps>
+// STG: bytes of output staging per warp.  4096 holds a 32 x 32 chunk of fp32;
+// with 2048, fp32 chunks leave as two 16-channel boxes (the store map's box is
+// then 16 channels deep for 4-byte outputs).
+template <int BN, bool BOXED, int NEPI = kEpiWarps, int MT = 1, int STG = 4096>
 __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtensorMap *map_c,
                                               uint32_t tmem_base, uint64_t *tfull,
                                               uint64_t *tempty, uint8_t *stage_out,
@@ -109,12 +114,15 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
     const int wj0_y = wj0 / p.box_w, wj0_x = wj0 - wj0_y * p.box_w;
     const long long howo = (long long)p.Ho * p.Wo;
     const int ec = p.ws ? 4 : (p.out_dt == BIGEMM_F32 ? 4 : 2);
-    uint8_t *wstage = stage_out + (warp - 2) * 4096;
+    uint8_t *wstage = stage_out + (warp - 2) * STG;
     const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16);
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+    bool alive = true;
+    for (int u = blockIdx.x; alive && u < p.units; u += gridDim.x) {
         const Unit w = decode(p, u);
+#pragma unroll 1
+      for (int m = 0; m < MT; ++m) {
         // where this lane's pixel and this warp's store box go: computed
         // before the accumulator is ready
         const int b = w.pt * p.bpt + bi;
@@ -127,7 +135,7 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
             long long pix;
             if (BOXED) {
                 const int byi = (int)fd_divmod((uint32_t)rem, p.fd_bx, &urem), bxi = (int)urem;
-                int y = byi * p.box_h + bj_y;
+                int y = byi * p.box_h + m * 16 + bj_y;
                 const int x = bxi * p.box_w + bj_x;
                 if (p.hp) {                     // stacked images: row -> (image, row)
                     n = (int)fd_divmod((uint32_t)y, p.fd_hp, &urem);
@@ -152,7 +160,7 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
             if (BOXED) {
                 const int byi = (int)fd_divmod((uint32_t)rem, p.fd_bx, &urem), bxi = (int)urem;
                 sx = bxi * p.box_w + wj0_x;
-                sy = byi * p.box_h + wj0_y;
+                sy = byi * p.box_h + m * 16 + wj0_y;
                 if (p.hp) {                     // the warp's rows lie in one image (hp % rows == 0)
                     n = (int)fd_divmod((uint32_t)sy, p.fd_hp, &urem);
                     sy = (int)urem;
@@ -163,11 +171,16 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
             sn = w.sp * p.N + n;
         }
         const bool wstore = wbox && sn < (w.sp + 1) * p.N;
-        int okw = 0;
-        if (lane == 0) okw = mbar_wait(&tfull[acc], acc_phase, p.timeout_ns, abort_flag, p.err);
-        if (!__shfl_sync(0xffffffffu, okw, 0)) break;
-        tc_fence_after();
-        const uint32_t acc_col = lane_base + (uint32_t)(acc * BN);
+        if (m == 0) {
+            int okw = 0;
+            if (lane == 0) okw = mbar_wait(&tfull[acc], acc_phase, p.timeout_ns, abort_flag, p.err);
+            if (!__shfl_sync(0xffffffffu, okw, 0)) {
+                alive = false;
+                break;
+            }
+            tc_fence_after();
+        }
+        const uint32_t acc_col = lane_base + (uint32_t)(acc * MT * BN + m * BN);
         uint32_t ra[32], rb[32];
         tmem_ld_32x32b_x32(acc_col + (uint32_t)(h * 32), ra);
         const int co0 = w.ct * BN;
@@ -178,7 +191,7 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
             tmem_wait_ld_regs(cur);
             if (i + 1 < kMine) {
                 tmem_ld_32x32b_x32(acc_col + (uint32_t)((h + kSplit * (i + 1)) * 32), nxt);
-            } else {                            // accumulator drained by this warp: hand it back
+            } else if (m == MT - 1) {           // accumulator drained by this warp: hand it back
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&tempty[acc]);
@@ -202,7 +215,26 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
                     for (int j = 0; j < 32; ++j) v[j] = rsqrtf(v[j] + bv[j] + p.eps);
                 }
             }
-            if (wstore) {
+            if (wstore && STG < 4096 && ec == 4) {
+                // two 16-channel boxes through the one 2 KB buffer
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    if (lane == 0) bulk_wait_read<0>();   // the previous store has read the buffer
+                    __syncwarp();
+                    uint8_t *dst = wstage + lane * 4;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) *reinterpret_cast<float *>(dst + j * 128) = v[hh * 16 + j];
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (BOXED)
+                            tma_store_4d(map_c, wstage, sx, sy, cb + hh * 16, sn);
+                        else
+                            tma_store_3d(map_c, wstage, sx, cb + hh * 16, sn);
+                        bulk_commit();
+                    }
+                }
+            } else if (wstore) {
                 if (lane == 0) bulk_wait_read<0>();   // the previous store has read the buffer
                 __syncwarp();
                 uint8_t *dst = wstage + lane * ec;
@@ -252,6 +284,7 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
                 }
             }
         }
+      }
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
     }

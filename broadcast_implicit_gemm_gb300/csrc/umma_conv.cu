@@ -190,10 +190,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t a_lo = desc_lo(smem_u32(sa + stage * kABytes),
                                                   AMODE == A_NHWC ? 16u : box_bytes);
                     const uint32_t b_lo = desc_lo(smem_u32(sb + stage * C::b_bytes), 16u);
+                    if (AMODE == A_NHWC) {
+                        umma4_kmajor<FMT == 2>(d_tmem, a_lo, a_hi, b_lo, b_hi, idesc,
+                                               kb > w.kb0 ? 1u : 0u);
+                    } else {
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        umma_lohi<FMT == 2>(d_tmem, a_lo + k * (a_kstep >> 4), a_hi, b_lo + k * 2u,
-                                            b_hi, idesc, (kb > w.kb0 || k > 0) ? 1u : 0u);
+                        for (int k = 0; k < 4; ++k)
+                            umma_lohi<FMT == 2>(d_tmem, a_lo + k * (a_kstep >> 4), a_hi,
+                                                b_lo + k * 2u, b_hi, idesc,
+                                                (kb > w.kb0 || k > 0) ? 1u : 0u);
+                    }
                     any = true;
                     umma_commit(&empty[stage]);
                     if (++stage == S) stage = 0, phase ^= 1u;

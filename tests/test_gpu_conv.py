@@ -181,6 +181,41 @@ def S(name, N, CI, CO, H, W, K, s, p, g=1, i="f16", o="f16", epi="none", dd="uni
     return synth.ConvSpec(name, N, CI, CO, H, W, K, s, p, g, i, o, dd, kd, epi)
 
 
+# ------------------------------------------------- halo units of two stacked tiles
+# A unit of 32 output rows x 8 columns: two 128-pixel M tiles share every
+# weight tile (BN <= 128), accumulators BN TMEM columns apart.
+TWO = [
+    _H("two_fused_like_exp", 2, 256, 256, 32, 32, 3, 1, o="f32", epi="bias_exp"),
+    _H("two_ragged_ci40_co72", 2, 40, 72, 19, 21, 3, 1),
+    _H("two_rows_not_whole", 1, 64, 128, 45, 24, 3, 1),
+    _H("two_tf32", 1, 64, 128, 34, 16, 3, 1, i="f32", o="f32"),
+    _H("two_bf16_pad0", 1, 64, 96, 40, 24, 3, 0, i="bf16", o="bf16"),
+]
+
+
+@pytest.mark.parametrize("bn", [64, 128])
+@pytest.mark.parametrize("spec", TWO, ids=lambda s: s.name)
+def test_umma_halo_two_tiles(spec, bn):
+    info = check(spec, {"kind": bg.KIND_UMMA, "mode": bg.MODE_HALO, "box_w": 8, "box_h": 32,
+                        "tile_n": bn, "resident_b": -1})
+    assert info["amode"] == "halo" and info["box"][:2] == [8, 32] and info["bn"] == bn
+
+
+def test_umma_halo_two_tiles_stacked_and_split():
+    spec = synth.RESNET50_FP16[3].with_batch(3)                  # 512 -> 512 on 7 x 7
+    info = check(spec, {"kind": bg.KIND_UMMA, "mode": bg.MODE_STACK, "box_w": 8, "box_h": 32,
+                        "tile_n": 128, "split_k": 2})
+    assert info["pack"] == "stack" and info["box"][:2] == [8, 32] and info["split"] == 2
+
+
+def test_umma_halo_two_tiles_need_bn_128():
+    with pytest.raises(bg.BigemmError) as e:
+        bg.conv2d_nchw_plan_ex(1, 32, 32, 256, 64, 3, 3, 1, 1, 1, bg.F16, bg.F16, bg.EPI_NONE, 0,
+                               {"kind": bg.KIND_UMMA, "mode": bg.MODE_HALO, "box_w": 8,
+                                "box_h": 32, "tile_n": 256})
+    assert e.value.status == 2
+
+
 # ------------------------------------------------- halo with resident weights
 # Resident weights need one 64-channel output tile and one 128-byte channel
 # block (9 taps x 8 KB beside three halo stages).
