@@ -74,6 +74,9 @@ struct UmmaParams {
     void *out;
     int out_dt;
     float *ws;                      // split-K partial sums or null
+    int red_add;                    // split-K into a zeroed fp32 output: each K slice adds
+                                    // its partial tile to out (atomic adds; the first slice
+                                    // adds the bias of EPI_BIAS), no workspace
     long long out_elems;
     int *err;
     unsigned long long timeout_ns;
@@ -114,10 +117,13 @@ cudaError_t launch_pack_nhwc(const void *x, void *xh, int N, int C, int HW, int 
 // Both packs in one launch.  The data goes to a per-image [Hop][Wop][Ch] grid
 // whose pixel (yo, xo) is input pixel (s*yo, s*xo), zero outside the image:
 // (H, W, 1) is the plain copy, Hop > H adds zero rows below each image, s > 1
-// subsamples.  xh must be 16-byte aligned.
+// subsamples.  xh must be 16-byte aligned.  zero (16-byte aligned, or null):
+// zero_elems floats that the same launch sets to 0 (the output that split-K
+// slices then add into).
 cudaError_t launch_pack_operands(const void *x, void *xh, int N, int C, int H, int W, int Hop,
                                  int Wop, int s, int Ch, const void *w, void *wp, int CO, int CI,
-                                 int KHKW, int cip, int dt, cudaStream_t stream);
+                                 int KHKW, int cip, int dt, cudaStream_t stream,
+                                 float *zero = nullptr, long long zero_elems = 0);
 cudaError_t launch_splitk_reduce(const float *ws, int split, long long elems, int CO, int HoWo,
                                  int epi, const float *bias, float eps, void *out, int out_dt,
                                  cudaStream_t stream);

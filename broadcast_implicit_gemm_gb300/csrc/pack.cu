@@ -147,12 +147,24 @@ __device__ __forceinline__ void pack_weight_part(const T *__restrict__ w, T *__r
     }
 }
 
+// Blocks [0, zblocks) of a zero-fill part: n floats at z (16-byte aligned) set to 0.
+__device__ __forceinline__ void zero_part(float *__restrict__ z, long long n, int blk, int nblk)
+{
+    const long long nv = n >> 2;
+    uint4 *zv = reinterpret_cast<uint4 *>(z);
+    for (long long i = (long long)blk * blockDim.x + threadIdx.x; i < nv;
+         i += (long long)nblk * blockDim.x)
+        zv[i] = make_uint4(0, 0, 0, 0);
+    if (blk == 0 && threadIdx.x < (n & 3)) z[(nv << 2) + threadIdx.x] = 0.f;
+}
+
 // Both operands in one launch: blocks [0, wblocks) re-lay out the kernel
 // (first, so that this work overlaps the data tiles), the remaining blocks
 // transpose data tiles (as pack_nhwc_vec_kernel, tile index flattened as
 // (pixel tile, channel tile, image)).  Output pixel p of an image copies input
 // pixel p when p < HWi and is zero up to HWo (the zero rows below a stacked
-// image).  wblocks = 0: no kernel re-layout.
+// image).  wblocks = 0: no kernel re-layout.  The last zblocks blocks zero
+// zn floats at z.
 template <typename T>
 __global__ void __launch_bounds__(256) pack_operands_kernel(const T *__restrict__ x,
                                                             T *__restrict__ xh, int C, int HWi,
@@ -160,7 +172,8 @@ __global__ void __launch_bounds__(256) pack_operands_kernel(const T *__restrict_
                                                             int ctiles, int wblocks,
                                                             const T *__restrict__ w,
                                                             T *__restrict__ wp, int CO, int CI,
-                                                            int KHKW, int cip)
+                                                            int KHKW, int cip, float *z,
+                                                            long long zn, int zblocks)
 {
     griddep_enter();
     constexpr int VEC = 16 / sizeof(T);
@@ -171,6 +184,10 @@ __global__ void __launch_bounds__(256) pack_operands_kernel(const T *__restrict_
     if ((int)blockIdx.x < wblocks) {
         pack_weight_part(w, wp, CO, CI, KHKW, cip, (int)blockIdx.x, wblocks, sbuf,
                          (int)(kPackSmemBytes / sizeof(T)));
+        return;
+    }
+    if ((int)blockIdx.x >= (int)gridDim.x - zblocks) {
+        zero_part(z, zn, (int)blockIdx.x - ((int)gridDim.x - zblocks), zblocks);
         return;
     }
     {
@@ -219,7 +236,8 @@ __global__ void __launch_bounds__(256) pack_remap_kernel(const T *__restrict__ x
                                                          int ptiles, int ctiles, int wblocks,
                                                          const T *__restrict__ w,
                                                          T *__restrict__ wp, int CO, int CI,
-                                                         int KHKW, int cip)
+                                                         int KHKW, int cip, float *z,
+                                                         long long zn, int zblocks)
 {
     griddep_enter();
     constexpr int VEC = 16 / sizeof(T);
@@ -231,6 +249,10 @@ __global__ void __launch_bounds__(256) pack_remap_kernel(const T *__restrict__ x
     if ((int)blockIdx.x < wblocks) {
         pack_weight_part(w, wp, CO, CI, KHKW, cip, (int)blockIdx.x, wblocks, sbuf,
                          (int)(kPackSmemBytes / sizeof(T)));
+        return;
+    }
+    if ((int)blockIdx.x >= (int)gridDim.x - zblocks) {
+        zero_part(z, zn, (int)blockIdx.x - ((int)gridDim.x - zblocks), zblocks);
         return;
     }
     {
@@ -350,7 +372,8 @@ cudaError_t launch_pack_nhwc(const void *x, void *xh, int N, int C, int HW, int 
 
 cudaError_t launch_pack_operands(const void *x, void *xh, int N, int C, int H, int W, int Hop,
                                  int Wop, int s, int Ch, const void *w, void *wp, int CO, int CI,
-                                 int KHKW, int cip, int dt, cudaStream_t stream)
+                                 int KHKW, int cip, int dt, cudaStream_t stream, float *zero,
+                                 long long zero_elems)
 {
     const int vec = (int)(16 / dtype_size(dt));
     if (Ch % vec || (reinterpret_cast<uintptr_t>(xh) & 15)) return cudaErrorInvalidValue;
@@ -367,9 +390,12 @@ cudaError_t launch_pack_operands(const void *x, void *xh, int N, int C, int H, i
     const long long witems = cc >= 1 ? (long long)CO * ((cip + cc - 1) / cc)
                                      : ((long long)CO * KHKW * cip + 255) / 256;
     const long long wblocks = w ? std::max<long long>(1, std::min<long long>(witems, 2048)) : 0;
-    if (data_blocks + wblocks > INT32_MAX || hwo > INT32_MAX) return cudaErrorInvalidValue;
+    if (zero && (reinterpret_cast<uintptr_t>(zero) & 15)) return cudaErrorInvalidValue;
+    const long long zblocks =
+        zero && zero_elems > 0 ? std::min<long long>((zero_elems / 4 + 255) / 256 + 1, 1024) : 0;
+    if (data_blocks + wblocks + zblocks > INT32_MAX || hwo > INT32_MAX) return cudaErrorInvalidValue;
     ProfScope prof("pack_operands", stream);
-    const int grid = (int)(data_blocks + wblocks);
+    const int grid = (int)(data_blocks + wblocks + zblocks);
     // pixel p of the output is pixel p of the input (or zero below it)
     const bool linear = s == 1 && Wop == W && Hop >= H;
     if (linear && aligned && hwi % vec == 0 && hwo % vec == 0) {
@@ -378,24 +404,24 @@ cudaError_t launch_pack_operands(const void *x, void *xh, int N, int C, int H, i
                               static_cast<const uint32_t *>(x), static_cast<uint32_t *>(xh), C,
                               (int)hwi, (int)hwo, Ch, (int)ptiles, (int)ctiles, (int)wblocks,
                               static_cast<const uint32_t *>(w), static_cast<uint32_t *>(wp), CO, CI,
-                              KHKW, cip);
+                              KHKW, cip, zero, zero_elems, (int)zblocks);
         return launch_pdl(pack_operands_kernel<uint16_t>, dim3(grid), dim3(256), 0, stream,
                           static_cast<const uint16_t *>(x), static_cast<uint16_t *>(xh), C,
                           (int)hwi, (int)hwo, Ch, (int)ptiles, (int)ctiles, (int)wblocks,
                           static_cast<const uint16_t *>(w), static_cast<uint16_t *>(wp), CO, CI,
-                          KHKW, cip);
+                          KHKW, cip, zero, zero_elems, (int)zblocks);
     }
     if (dtype_size(dt) == 4)
         return launch_pdl(pack_remap_kernel<uint32_t>, dim3(grid), dim3(256), 0, stream,
                           static_cast<const uint32_t *>(x), static_cast<uint32_t *>(xh), C, H, W,
                           Hop, Wop, s, Ch, (int)ptiles, (int)ctiles, (int)wblocks,
                           static_cast<const uint32_t *>(w), static_cast<uint32_t *>(wp), CO, CI,
-                          KHKW, cip);
+                          KHKW, cip, zero, zero_elems, (int)zblocks);
     return launch_pdl(pack_remap_kernel<uint16_t>, dim3(grid), dim3(256), 0, stream,
                       static_cast<const uint16_t *>(x), static_cast<uint16_t *>(xh), C, H, W, Hop,
                       Wop, s, Ch, (int)ptiles, (int)ctiles, (int)wblocks,
                       static_cast<const uint16_t *>(w), static_cast<uint16_t *>(wp), CO, CI, KHKW,
-                      cip);
+                      cip, zero, zero_elems, (int)zblocks);
 }
 
 cudaError_t launch_splitk_reduce(const float *ws, int split, long long elems, int CO, int HoWo,

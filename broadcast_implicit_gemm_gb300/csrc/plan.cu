@@ -314,6 +314,7 @@ struct bigemm_plan_s {
     bool store_tma = false;
     bool maps_ready = false;
     bool raw_b = false;        // 1x1 nhwc mode: map_b reads the caller's kernel [CO][CI] as is
+    bool red_add = false;      // split K into the zeroed fp32 output by atomic adds (no workspace)
     std::string search_log;
     std::string chosen_by = "heuristic";
 };
@@ -710,12 +711,17 @@ bigemm_status setup_plan(bigemm_plan_s *p)
         }
         p->maps_ready = true;
     }
-    if (p->g.p.split > 1) {
+    // fp32 outputs whose epilogue is linear take the K slices' partial tiles as
+    // atomic adds (TMA reduce-add) into the output, zeroed first; the others go
+    // through a workspace and a reduction pass
+    p->red_add = p->g.p.split > 1 && s.out_dt == BIGEMM_F32 &&
+                 (s.epi == BIGEMM_EPI_NONE || s.epi == BIGEMM_EPI_BIAS);
+    if (p->g.p.split > 1 && !p->red_add) {
         p->ws_bytes = (size_t)p->g.p.split * p->g.p.out_elems * sizeof(float);
         if (cudaMalloc(&p->ws, p->ws_bytes) != cudaSuccess) return BIGEMM_ERR_CUDA;
     }
     p->store_tma = store_tma_ok(s, t, p->g.p.split) && !getenv("BIGEMM_NO_TMA_STORE");
-    if (p->store_tma && p->g.p.split > 1) {
+    if (p->store_tma && p->g.p.split > 1 && !p->red_add) {
         if (!encode_store_map(p, p->ws, true)) p->store_tma = false;
         p->map_c_src = p->ws;
     }
@@ -772,7 +778,7 @@ int launches_per_run(const bigemm_plan_s *p)
     if (p->c.kind != BIGEMM_KIND_UMMA) return 1;
     int n = 1;
     if (p->c.t.amode != A_DIRECT) n += 1;
-    if (p->g.p.split > 1) n += 1;
+    if (p->g.p.split > 1 && !p->red_add) n += 1;
     return n;
 }
 
@@ -799,7 +805,8 @@ bigemm_status run_plan(bigemm_plan_s *p, const void *data, const void *kernel, c
     up.eps = eps;
     up.bias = bias;
     up.out = out;
-    up.ws = p->ws;
+    up.ws = p->red_add ? nullptr : p->ws;
+    up.red_add = p->red_add ? 1 : 0;
     up.err = ds->err;
     up.timeout_ns = wait_timeout_ns();
     if (p->c.t.amode != A_DIRECT) {
@@ -812,15 +819,19 @@ bigemm_status run_plan(bigemm_plan_s *p, const void *data, const void *kernel, c
         }
         e = launch_pack_operands(data, p->xh, s.N, s.CI, s.H, s.W, hop, wop,
                                  pk == PACK_SUB ? s.stride : 1, p->g.ch, p->raw_b ? nullptr : kernel,
-                                 p->wp, s.CO, s.CI, s.KH * s.KW, p->g.cip, s.in_dt, st);
+                                 p->wp, s.CO, s.CI, s.KH * s.KW, p->g.cip, s.in_dt, st,
+                                 p->red_add ? static_cast<float *>(out) : nullptr, up.out_elems);
         if (e != cudaSuccess) return BIGEMM_ERR_CUDA;
     } else {
         bigemm_status r = encode_direct_maps(p, data, kernel);
         if (r != BIGEMM_OK) return r;
+        if (p->red_add &&
+            cudaMemsetAsync(out, 0, (size_t)up.out_elems * sizeof(float), st) != cudaSuccess)
+            return BIGEMM_ERR_CUDA;
     }
     up.store_tma = 0;
     if (p->store_tma) {
-        if (up.split == 1 && p->map_c_src != out) {
+        if ((up.split == 1 || p->red_add) && p->map_c_src != out) {
             if (encode_store_map(p, out, false))
                 p->map_c_src = out;
             else
@@ -830,7 +841,7 @@ bigemm_status run_plan(bigemm_plan_s *p, const void *data, const void *kernel, c
     }
     e = launch_umma_conv(p->c.t, s.in_dt, up, p->map_a, p->map_b, p->map_c, p->g.grid, st);
     if (e != cudaSuccess) return BIGEMM_ERR_CUDA;
-    if (up.split > 1) {
+    if (up.split > 1 && !p->red_add) {
         e = launch_splitk_reduce(p->ws, up.split, up.out_elems, s.CO, s.Ho * s.Wo, s.epi, bias, eps,
                                  out, s.out_dt, st);
         if (e != cudaSuccess) return BIGEMM_ERR_CUDA;
@@ -1213,6 +1224,7 @@ bigemm_status conv2d_nchw_plan_describe(bigemm_plan plan, char *buf, size_t len)
            << ", \"bn\": " << c.t.bn
            << ", \"box\": [" << c.t.box_w << ", " << c.t.box_h << ", " << c.t.bpt << "]"
            << ", \"split\": " << p.split << ", \"k_blocks\": " << p.k_blocks
+           << ", \"split_sum\": \"" << (p.split == 1 ? "none" : plan->red_add ? "add" : "reduce") << "\""
            << ", \"pix_tiles\": " << p.pix_tiles << ", \"co_tiles\": " << p.co_tiles
            << ", \"units\": " << p.units << ", \"grid\": " << plan->g.grid
            << ", \"smem\": " << (c.t.amode == A_HALO ? (size_t)p.halo_smem : umma_smem_bytes(c.t))

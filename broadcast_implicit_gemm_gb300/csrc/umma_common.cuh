@@ -113,7 +113,7 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
     const int bj_y = bj / p.box_w, bj_x = bj - bj_y * p.box_w;
     const int wj0_y = wj0 / p.box_w, wj0_x = wj0 - wj0_y * p.box_w;
     const long long howo = (long long)p.Ho * p.Wo;
-    const int ec = p.ws ? 4 : (p.out_dt == BIGEMM_F32 ? 4 : 2);
+    const int ec = (p.ws || p.out_dt == BIGEMM_F32) ? 4 : 2;
     uint8_t *wstage = stage_out + (warp - 2) * STG;
     const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16);
     int acc = 0;
@@ -147,7 +147,7 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
                 pix = (long long)rem * p.box_w + bj;
                 valid = pix < howo;
             }
-            base = (long long)w.sp * p.out_elems + (long long)n * p.CO * howo + pix;
+            base = (p.ws ? (long long)w.sp * p.out_elems : 0ll) + (long long)n * p.CO * howo + pix;
         }
         // the warp's store box (TMA mode): origin and image index
         const int wb = w.pt * p.bpt + wbi;
@@ -168,9 +168,10 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
             } else {
                 sx = rem * p.box_w + wj0;
             }
-            sn = w.sp * p.N + n;
+            sn = n;
         }
-        const bool wstore = wbox && sn < (w.sp + 1) * p.N;
+        const bool wstore = wbox && sn < p.N;
+        if (p.ws) sn += w.sp * p.N;             // K slice w.sp's plane of the workspace
         if (m == 0) {
             int okw = 0;
             if (lane == 0) okw = mbar_wait(&tfull[acc], acc_phase, p.timeout_ns, abort_flag, p.err);
@@ -200,7 +201,9 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
             float v[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(cur[j]);
-            if (!p.ws && p.epi != BIGEMM_EPI_NONE) {
+            // partial sums take no epilogue, except the bias that the first of the
+            // slices adding into the output brings
+            if (!p.ws && p.epi != BIGEMM_EPI_NONE && !(p.red_add && w.sp != 0)) {
                 float bv[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) bv[j] = cb + j < p.CO ? __ldg(p.bias + cb + j) : 0.f;
@@ -227,10 +230,16 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        if (BOXED)
+                        if (p.red_add) {
+                            if (BOXED)
+                                tma_reduce_add_4d(map_c, wstage, sx, sy, cb + hh * 16, sn);
+                            else
+                                tma_reduce_add_3d(map_c, wstage, sx, cb + hh * 16, sn);
+                        } else if (BOXED) {
                             tma_store_4d(map_c, wstage, sx, sy, cb + hh * 16, sn);
-                        else
+                        } else {
                             tma_store_3d(map_c, wstage, sx, cb + hh * 16, sn);
+                        }
                         bulk_commit();
                     }
                 }
@@ -253,10 +262,16 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    if (BOXED)
+                    if (p.red_add) {
+                        if (BOXED)
+                            tma_reduce_add_4d(map_c, wstage, sx, sy, cb, sn);
+                        else
+                            tma_reduce_add_3d(map_c, wstage, sx, cb, sn);
+                    } else if (BOXED) {
                         tma_store_4d(map_c, wstage, sx, sy, cb, sn);
-                    else
+                    } else {
                         tma_store_3d(map_c, wstage, sx, cb, sn);
+                    }
                     bulk_commit();
                 }
             } else if (!p.store_tma && valid) {
@@ -267,6 +282,11 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
                         if (j < jn) o[j * howo] = v[j];
+                } else if (p.red_add) {
+                    float *o = static_cast<float *>(p.out) + o0;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (j < jn) atomicAdd(o + j * howo, v[j]);
                 } else if (p.out_dt == BIGEMM_F32) {
                     float *o = static_cast<float *>(p.out) + o0;
 #pragma unroll

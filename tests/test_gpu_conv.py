@@ -181,6 +181,31 @@ def S(name, N, CI, CO, H, W, K, s, p, g=1, i="f16", o="f16", epi="none", dd="uni
     return synth.ConvSpec(name, N, CI, CO, H, W, K, s, p, g, i, o, dd, kd, epi)
 
 
+# ------------------------------------------------- how K slices are summed
+# fp32 outputs with no epilogue or a bias take the slices' partial tiles as
+# atomic adds into the zeroed output (TMA reduce-add boxes, or per-element adds
+# where TMA cannot store); other outputs go through the workspace and the
+# reduction pass.
+SPLIT_SUM = [
+    (S("ss_halo_f32_tma_add", 1, 256, 128, 12, 12, 3, 1, 1, i="f32", o="f32"), bg.MODE_HALO, "add"),
+    (S("ss_halo_f32_ragged_atomic", 1, 256, 96, 7, 7, 3, 1, 1, i="f32", o="f32"), bg.MODE_HALO, "add"),
+    (S("ss_nhwc_bias_f32", 2, 128, 96, 9, 12, 3, 1, 1, o="f32", epi="bias"), bg.MODE_NHWC, "add"),
+    (S("ss_nhwc_s2_f32", 1, 256, 64, 14, 14, 3, 2, 1, i="f32", o="f32"), bg.MODE_NHWC, "add"),
+    (S("ss_direct_bias_f32", 2, 256, 64, 16, 16, 1, 1, 0, o="f32", epi="bias"), bg.MODE_DIRECT, "add"),
+    (S("ss_exp_f32_reduce", 1, 128, 64, 9, 12, 3, 1, 1, o="f32", epi="bias_exp"), bg.MODE_HALO, "reduce"),
+    (S("ss_f16_out_reduce", 1, 128, 64, 9, 12, 3, 1, 1), bg.MODE_HALO, "reduce"),
+]
+
+
+@pytest.mark.parametrize("split", [2, 4])
+@pytest.mark.parametrize("case", SPLIT_SUM, ids=lambda c: c[0].name)
+def test_split_k_sums(case, split):
+    spec, mode, how = case
+    info = check(spec, {"kind": bg.KIND_UMMA, "mode": mode, "split_k": split})
+    assert info["split"] > 1 and info["split_sum"] == how
+
+
+
 # ------------------------------------------------- halo units of two stacked tiles
 # A unit of 32 output rows x 8 columns: two 128-pixel M tiles share every
 # weight tile (BN <= 128), accumulators BN TMEM columns apart.
