@@ -49,7 +49,8 @@ enum PackLayout {
 struct UmmaTiling {
     int amode;        // AMode
     int pack;         // PackLayout
-    int bres;         // A_HALO: weights resident in shared memory (one output-channel tile)
+    int bres;         // weights resident in shared memory (A_HALO: one output-channel
+                      // tile; A_NHWC / A_DIRECT: the block's tile, split 1)
     int bn;           // output channels per tile (N of the MMA), multiple of 32
     int stages;       // smem ring depth
     int box_w, box_h; // output pixels per TMA box (A_NHWC); A_DIRECT: box_w = row pixels
@@ -83,9 +84,10 @@ struct UmmaParams {
     int store_tma;                  // 1: stage tiles in smem, write with TMA stores (map_c)
     int hp;                         // A_HALO over stacked images: rows per image (H + pad)
                                     // in the packed data and in tile row space; 0 otherwise
-    int res_b_bytes;                // A_HALO with resident weights: bytes of every tap (0: streamed)
-    // A_HALO shared-memory layout (halo_layout): halo stages, streamed weight
-    // stages, byte offsets of the weights, the output staging and the
+    int res_b_bytes;                // resident weights: their bytes (0: streamed)
+    // Dynamic shared-memory layout of the halo kernels (halo_layout) and of the
+    // resident-weight nhwc / direct kernels (main_res_layout): A stages, streamed
+    // weight stages, byte offsets of the weights, the output staging and the
     // barriers, and the total
     int halo_sa, halo_sb, halo_b_off, halo_stage_off, halo_bar_off, halo_smem;
     // divisors of the index arithmetic; launch_umma_conv fills them from the fields above
@@ -110,6 +112,14 @@ cudaError_t launch_halo_conv(int bn, int fmt, const UmmaParams &p, const CUtenso
                              const CUtensorMap &map_b, const CUtensorMap &map_c, int grid,
                              cudaStream_t stream);
 bool umma_tiling_compiled(const UmmaTiling &t, int in_dt);
+// The nhwc / direct kernels with resident weights (umma_res.cu): the layout
+// (A stages, weights, output staging, barriers) of one output-channel tile's
+// k_blocks K blocks, written into p's layout fields; false when it does not fit.
+bool main_res_layout(int bn, int k_blocks, int smem_limit, UmmaParams &p);
+// Launch; the grid must be a multiple of p.co_tiles and p.split must be 1.
+cudaError_t launch_umma_res(int amode, int fmt, int bn, const UmmaParams &p,
+                            const CUtensorMap &map_a, const CUtensorMap &map_b,
+                            const CUtensorMap &map_c, int grid, cudaStream_t stream);
 
 // -------------------------------------------------------------- other kernels
 cudaError_t launch_pack_nhwc(const void *x, void *xh, int N, int C, int HW, int Ch, int dt,

@@ -220,14 +220,21 @@ UmmaGeom umma_geometry(const ConvShape &s0, const UmmaTiling &t, int sm_count)
     p.epi = s.epi;
     p.out_dt = s.out_dt;
     p.out_elems = (long long)s.N * s.CO * s.Ho * s.Wo;
+    DeviceState *ds = device_state();
+    const int limit = ds ? ds->max_smem_optin : 232448;
     if (t.amode == A_HALO) {
         // shared-memory layout: streamed or resident weights
-        DeviceState *ds = device_state();
-        const int limit = ds ? ds->max_smem_optin : 232448;
         g.fits = g.fits && halo_layout(t.bn, t.bres != 0, t.box_h, s.KH, s.KH * s.KW, p.ci_blocks,
                                        limit, p);
+    } else if (t.bres) {
+        // resident weights of one output-channel tile, every K block
+        g.fits = g.fits && main_res_layout(t.bn, p.k_blocks, limit, p);
     }
     g.grid = (int)std::min<long long>(p.units, sm_count);
+    if (t.bres && t.amode != A_HALO && p.co_tiles > 0) {
+        // each block keeps one output-channel tile: a grid of whole tile groups
+        g.grid = std::max(p.co_tiles, g.grid / p.co_tiles * p.co_tiles);
+    }
     return g;
 }
 
@@ -280,12 +287,14 @@ bool umma_valid(const ConvShape &s0, const UmmaTiling &t, int sm_count, std::str
         if (t.box_w * t.box_h * t.bpt > 128) return bad("boxes exceed 128 rows");
         if (t.box_w * s.stride > 256 || t.box_h * s.stride > 256) return bad("box > 256");
     }
-    if (t.bres && t.amode != A_HALO) return bad("resident weights are a halo-mode form");
+    if (t.bres && t.amode != A_HALO && t.split != 1) return bad("resident weights need split 1");
     if (t.bpt > 16) return bad("more than 16 boxes per tile");
     if (umma_smem_bytes(t) == 0) return bad("no compiled kernel");
     if (!umma_geometry(s0, t, 1).fits) return bad("more than 2^31 boxes or work units");
     DeviceState *ds = device_state();
-    if (ds && (int)umma_smem_bytes(t) > ds->max_smem_optin) return bad("smem exceeds opt-in limit");
+    if (ds && !t.bres && (int)umma_smem_bytes(t) > ds->max_smem_optin) return bad("smem exceeds opt-in limit");
+    if (t.bres && t.amode != A_HALO && !umma_geometry(s0, t, 1).fits)
+        return bad("resident weights exceed shared memory");
     (void)sm_count;
     return true;
 }
@@ -576,8 +585,8 @@ std::vector<Cand> candidates(const ConvShape &s, int sms)
                     c.kind = BIGEMM_KIND_UMMA;
                     c.t = t;
                     if (umma_valid(s, t, sms, nullptr)) v.push_back(c);
-                    if (amode == A_HALO && s.CO <= bn) {   // the resident-weights form too
-                        c.t.bres = 1;
+                    if ((amode == A_HALO && s.CO <= bn) || (amode != A_HALO && split == 1)) {
+                        c.t.bres = 1;   // the resident-weights form too
                         if (umma_valid(s, c.t, sms, nullptr)) v.push_back(c);
                     }
                 }
@@ -1118,10 +1127,13 @@ bigemm_status plan_impl(int N, int H, int W, int CO, int CI, int KH, int KW, int
             if (opts->split_k) c.t.split = opts->split_k;
             if (opts->stages) c.t.stages = opts->stages;
             if (opts->resident_b < -1 || opts->resident_b > 1) return BIGEMM_ERR_INVALID_ARG;
-            if (opts->resident_b == 1)
+            if (opts->resident_b == 1) {
                 c.t.bres = 1;
-            else if (opts->resident_b == 0)
+                // resident weights outside the halo modes run whole K ranges
+                if (c.t.amode != A_HALO && !opts->split_k) c.t.split = 1;
+            } else if (opts->resident_b == 0) {
                 prefer_resident(s, c.t);
+            }
         }
         std::string why;
         if (!cand_valid(s, c, sms, &why)) return BIGEMM_ERR_UNSUPPORTED;
@@ -1227,7 +1239,7 @@ bigemm_status conv2d_nchw_plan_describe(bigemm_plan plan, char *buf, size_t len)
            << ", \"split_sum\": \"" << (p.split == 1 ? "none" : plan->red_add ? "add" : "reduce") << "\""
            << ", \"pix_tiles\": " << p.pix_tiles << ", \"co_tiles\": " << p.co_tiles
            << ", \"units\": " << p.units << ", \"grid\": " << plan->g.grid
-           << ", \"smem\": " << (c.t.amode == A_HALO ? (size_t)p.halo_smem : umma_smem_bytes(c.t))
+           << ", \"smem\": " << ((c.t.amode == A_HALO || c.t.bres) ? (size_t)p.halo_smem : umma_smem_bytes(c.t))
            << ", \"halo_stages\": " << p.halo_sa << ", \"weight_stages\": " << p.halo_sb
            << ", \"store\": \"" << (plan->store_tma ? "tma" : "direct") << "\"";
     }

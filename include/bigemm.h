@@ -110,9 +110,11 @@ typedef struct {
                        rows per block), 3 depthwise streaming (box_h = 2, 4
                        or 8 rows per thread).
                        Other values: INVALID_ARG.                               */
-    int resident_b; /* UMMA halo modes: 1 keeps the packed weights resident in
-                       shared memory (one output-channel tile must cover CO and
-                       every tap must fit), -1 streams them, 0 chooses          */
+    int resident_b; /* UMMA: 1 keeps the weights resident in shared memory --
+                       halo modes: one output-channel tile must cover CO and
+                       every tap must fit; other modes: split_k 1, and every K
+                       block of one output-channel tile must fit (each block
+                       keeps one tile) -- -1 streams them, 0 chooses            */
 } bigemm_plan_options;
 
 /*

@@ -181,6 +181,42 @@ def S(name, N, CI, CO, H, W, K, s, p, g=1, i="f16", o="f16", epi="none", dd="uni
     return synth.ConvSpec(name, N, CI, CO, H, W, K, s, p, g, i, o, dd, kd, epi)
 
 
+# ------------------------------------------------- resident weights, nhwc / direct
+# Each block keeps one output-channel tile's weights in shared memory and
+# streams only pixels; the grid is a whole number of tile groups.
+RES_MAIN = [
+    (S("rm_direct_64_64", 2, 64, 64, 56, 56, 1, 1, 0), bg.MODE_DIRECT, 0),
+    (S("rm_direct_64_256_bf16", 1, 64, 256, 28, 28, 1, 1, 0, i="bf16", o="bf16"), bg.MODE_DIRECT, 0),
+    (S("rm_direct_bias_f32", 2, 128, 200, 16, 16, 1, 1, 0, o="f32", epi="bias"), bg.MODE_DIRECT, 64),
+    (S("rm_sub_256_512_s2", 2, 256, 512, 28, 28, 1, 2, 0), bg.MODE_SUB, 128),
+    (S("rm_nhwc_k3_ci32", 2, 32, 64, 19, 21, 3, 1, 1), bg.MODE_NHWC, 0),
+    (S("rm_nhwc_tf32_1x1", 1, 96, 72, 14, 14, 1, 1, 0, i="f32", o="f32"), bg.MODE_NHWC, 0),
+    (S("rm_nhwc_exp_ragged", 1, 40, 136, 13, 11, 3, 1, 1, o="f32", epi="bias_exp"), bg.MODE_NHWC, 64),
+]
+
+
+@pytest.mark.parametrize("case", RES_MAIN, ids=lambda c: c[0].name)
+def test_umma_resident_weights_main(case):
+    spec, mode, bn = case
+    opts = {"kind": bg.KIND_UMMA, "mode": mode, "resident_b": 1}
+    if bn:
+        opts["tile_n"] = bn
+    info = check(spec, opts)
+    assert info["resident_b"] and info["split"] == 1 and info["grid"] % info["co_tiles"] == 0
+
+
+@pytest.mark.parametrize("opts", [{"mode": bg.MODE_NHWC, "split_k": 2, "resident_b": 1},
+                                  {"mode": bg.MODE_DIRECT, "tile_n": 256, "resident_b": 1}])
+def test_resident_weights_main_rejected(opts):
+    base = {"kind": bg.KIND_UMMA}
+    base.update(opts)
+    with pytest.raises(bg.BigemmError) as e:
+        # 2048 input channels: 32 K blocks of 32 KB cannot stay resident
+        bg.conv2d_nchw_plan_ex(1, 16, 16, 256, 2048, 1, 1, 1, 0, 1, bg.F16, bg.F16, bg.EPI_NONE, 0,
+                               base)
+    assert e.value.status == 2
+
+
 # ------------------------------------------------- how K slices are summed
 # fp32 outputs with no epilogue or a bias take the slices' partial tiles as
 # atomic adds into the zeroed output (TMA reduce-add boxes, or per-element adds
