@@ -626,7 +626,8 @@ bool encode_store_map(bigemm_plan_s *p, void *dst, bool is_ws)
         const uint64_t hw = (uint64_t)s.Ho * s.Wo;
         const uint64_t dims[3] = {hw, (uint64_t)s.CO, nn};
         const uint64_t str[2] = {hw * ec, hw * s.CO * ec};
-        const uint32_t box[3] = {32u, 32u, 1u};
+        // 2 KB boxes: 32 channels of 16-bit output, 16 of fp32
+        const uint32_t box[3] = {32u, ec == 4 ? 16u : 32u, 1u};
         const uint32_t es[3] = {1u, 1u, 1u};
         return encode_tiled(&p->map_c, dt, 3, dst, dims, str, box, es, CU_TENSOR_MAP_SWIZZLE_NONE);
     }
@@ -634,8 +635,8 @@ bool encode_store_map(bigemm_plan_s *p, void *dst, bool is_ws)
     const uint64_t str[3] = {(uint64_t)s.Wo * ec, (uint64_t)s.Ho * s.Wo * ec,
                              (uint64_t)s.CO * s.Ho * s.Wo * ec};
     const uint32_t sw = t.box_w >= 32 ? 32u : (uint32_t)t.box_w;
-    // the halo kernel stages 2 KB per warp: 4-byte outputs go 16 channels per box
-    const uint32_t co_box = (t.amode == A_HALO && ec == 4) ? 16u : 32u;
+    // 2 KB boxes: 32 channels of 16-bit output, 16 of fp32
+    const uint32_t co_box = ec == 4 ? 16u : 32u;
     const uint32_t box[4] = {sw, 32u / sw, co_box, 1u};
     const uint32_t es[4] = {1u, 1u, 1u, 1u};
     return encode_tiled(&p->map_c, dt, 4, dst, dims, str, box, es, CU_TENSOR_MAP_SWIZZLE_NONE);

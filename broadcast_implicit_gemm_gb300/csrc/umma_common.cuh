@@ -84,9 +84,10 @@ __device__ __forceinline__ void tmem_wait_ld_regs(uint32_t (&r)[32])
 // BOXED: the tile's pixels are 2-D boxes (box_w x box_h) of one image (or of
 // the stacked images); otherwise runs of box_w consecutive flattened pixels
 // (the direct mode).
-// STG: bytes of output staging per warp.  4096 holds a 32 x 32 chunk of fp32;
-// with 2048, fp32 chunks leave as two 16-channel boxes (the store map's box is
-// then 16 channels deep for 4-byte outputs).
+// STG: bytes of output staging per warp, used as STG / 2 KB buffers in turn.
+// A store box is 2 KB: 32 channels x 32 pixels of 16-bit output, or 16
+// channels of fp32 (the store map's box is 16 channels deep for 4-byte
+// outputs), so a 32-channel chunk of fp32 leaves as two boxes.
 template <int BN, bool BOXED, int NEPI = kEpiWarps, int MT = 1, int STG = 4096>
 __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtensorMap *map_c,
                                               uint32_t tmem_base, uint64_t *tfull,
@@ -115,6 +116,9 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
     const long long howo = (long long)p.Ho * p.Wo;
     const int ec = (p.ws || p.out_dt == BIGEMM_F32) ? 4 : 2;
     uint8_t *wstage = stage_out + (warp - 2) * STG;
+    constexpr int kNB = STG / 2048;             // 2 KB store buffers of the warp
+    static_assert(kNB >= 1, "at least one 2 KB buffer per warp");
+    int piece = 0;
     const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16);
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -218,61 +222,47 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
                     for (int j = 0; j < 32; ++j) v[j] = rsqrtf(v[j] + bv[j] + p.eps);
                 }
             }
-            if (wstore && STG < 4096 && ec == 4) {
-                // two 16-channel boxes through the one 2 KB buffer
+            if (wstore) {
+                // 2 KB pieces (32 channels of 16-bit output, or 16 of fp32), each
+                // written to the next of the warp's NB staging buffers and sent as
+                // one TMA box; a buffer is rewritten once the store that last used
+                // it has read it, so NB - 1 stores stay in flight
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    if (lane == 0) bulk_wait_read<0>();   // the previous store has read the buffer
+                for (int hh = 0; hh < (ec == 4 ? 2 : 1); ++hh) {
+                    uint8_t *buf = wstage + (piece % kNB) * 2048;
+                    ++piece;
+                    if (lane == 0) bulk_wait_read<kNB - 1>();
                     __syncwarp();
-                    uint8_t *dst = wstage + lane * 4;
+                    if (ec == 4) {
+                        uint8_t *dst = buf + lane * 4;
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) *reinterpret_cast<float *>(dst + j * 128) = v[hh * 16 + j];
+                        for (int j = 0; j < 16; ++j) *reinterpret_cast<float *>(dst + j * 128) = v[hh * 16 + j];
+                    } else {
+                        // two channels per conversion (cvt.rn.{f16,bf16}x2.f32), one per 16-bit store
+                        uint8_t *dst = buf + lane * 2;
+#pragma unroll
+                        for (int j = 0; j < 32; j += 2) {
+                            const uint32_t pk = pack2_16(v[j], v[j + 1], p.out_dt == BIGEMM_F16);
+                            *reinterpret_cast<uint16_t *>(dst + j * 64) = (uint16_t)(pk & 0xFFFFu);
+                            *reinterpret_cast<uint16_t *>(dst + (j + 1) * 64) = (uint16_t)(pk >> 16);
+                        }
+                    }
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
+                        const int cc = cb + hh * 16;
                         if (p.red_add) {
                             if (BOXED)
-                                tma_reduce_add_4d(map_c, wstage, sx, sy, cb + hh * 16, sn);
+                                tma_reduce_add_4d(map_c, buf, sx, sy, cc, sn);
                             else
-                                tma_reduce_add_3d(map_c, wstage, sx, cb + hh * 16, sn);
+                                tma_reduce_add_3d(map_c, buf, sx, cc, sn);
                         } else if (BOXED) {
-                            tma_store_4d(map_c, wstage, sx, sy, cb + hh * 16, sn);
+                            tma_store_4d(map_c, buf, sx, sy, cc, sn);
                         } else {
-                            tma_store_3d(map_c, wstage, sx, cb + hh * 16, sn);
+                            tma_store_3d(map_c, buf, sx, cc, sn);
                         }
                         bulk_commit();
                     }
-                }
-            } else if (wstore) {
-                if (lane == 0) bulk_wait_read<0>();   // the previous store has read the buffer
-                __syncwarp();
-                uint8_t *dst = wstage + lane * ec;
-                if (ec == 4) {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) *reinterpret_cast<float *>(dst + j * 128) = v[j];
-                } else {
-                    // two channels per conversion (cvt.rn.{f16,bf16}x2.f32), one per 16-bit store
-#pragma unroll
-                    for (int j = 0; j < 32; j += 2) {
-                        const uint32_t pk = pack2_16(v[j], v[j + 1], p.out_dt == BIGEMM_F16);
-                        *reinterpret_cast<uint16_t *>(dst + j * 64) = (uint16_t)(pk & 0xFFFFu);
-                        *reinterpret_cast<uint16_t *>(dst + (j + 1) * 64) = (uint16_t)(pk >> 16);
-                    }
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    if (p.red_add) {
-                        if (BOXED)
-                            tma_reduce_add_4d(map_c, wstage, sx, sy, cb, sn);
-                        else
-                            tma_reduce_add_3d(map_c, wstage, sx, cb, sn);
-                    } else if (BOXED) {
-                        tma_store_4d(map_c, wstage, sx, sy, cb, sn);
-                    } else {
-                        tma_store_3d(map_c, wstage, sx, cb, sn);
-                    }
-                    bulk_commit();
                 }
             } else if (!p.store_tma && valid) {
                 const long long o0 = base + (long long)cb * howo;
