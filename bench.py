@@ -267,8 +267,17 @@ def timed_steps(step_fn, steps, torch, stream, flush):
     return [a.elapsed_time(b) for a, b in evs], evs
 
 
+def sources_sha(names):
+    """Digest of the kernel sources a traffic figure was measured on."""
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "broadcast_implicit_gemm_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def traffic_for(kernel, workload):
-    """DRAM bytes per launch from the committed ncu summary, if its source still matches."""
+    """DRAM bytes per launch from the committed ncu summary, if its sources still match."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -277,12 +286,11 @@ def traffic_for(kernel, workload):
         return None
     if not rec:
         return None
-    src = os.path.join(ROOT, "broadcast_implicit_gemm_gb300", "csrc", rec["source"])
     try:
-        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    except OSError:
+        h = sources_sha(rec["sources"])
+    except (OSError, KeyError):
         return None
-    return rec["bytes_per_launch"] if h == rec["source_sha"] else None
+    return rec["bytes_per_launch"] if h == rec["sources_sha"] else None
 
 
 def kernel_work(name, it):
@@ -428,6 +436,9 @@ def main():
                              "depthwise_fp16", "bcast"])
     ap.add_argument("--layer", default=None, help="run only the named layer of the workload")
     ap.add_argument("--no-search", action="store_true", help="heuristic plans, no timed search")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's batch size (smaller cases for profiling; "
+                         "the line's config records it)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -455,6 +466,8 @@ def main():
             specs = [x for x in specs if x.name == args.layer]
             if not specs:
                 raise SystemExit(f"no layer {args.layer} in {args.workload}")
+        if args.batch:
+            specs = [x.with_batch(args.batch) for x in specs]
         step = ConvStep(specs, device, search=0 if args.no_search else 1)
         unit, scale = "TFLOP/s", 1e12
 
