@@ -58,7 +58,7 @@ __device__ __forceinline__ uint4 splat16(T v)
 // VEC: the plane (H*W elements) is a whole number of 16-byte vectors and the
 // output base is 16-byte aligned.
 template <typename T, bool VEC>
-__global__ void __launch_bounds__(256) bcast_kernel(int N, int C, long long HW, int op,
+__global__ void __launch_bounds__(128) bcast_kernel(int N, int C, long long HW, int op,
                                                     const float *__restrict__ var, float eps,
                                                     T *__restrict__ out)
 {
@@ -110,17 +110,18 @@ cudaError_t launch_typed(int N, int C, long long HW, int op, const float *var, f
                           op, var, eps, o);
     }
     ProfScope prof("bcast_nchw", stream);
-    // enough blocks for ~16 resident 256-thread blocks per SM, each covering
-    // whole planes of one channel
-    long long gy = ((long long)sms * 16 + C - 1) / C;
+    // ~64 blocks of 128 threads per SM over the launch, each covering whole
+    // planes of one channel (measured on [128,256,32,32] fp32: 16 blocks of
+    // 256 threads per SM reached 0.81 of the copy bandwidth, 64 of 128 0.88)
+    long long gy = ((long long)sms * 64 + C - 1) / C;
     if (gy > N) gy = N;
     if (gy > 65535) gy = 65535;
     if (gy < 1) gy = 1;
     dim3 grid(C, (unsigned)gy);
     const bool vec = ((HW * (long long)sizeof(T)) % 16 == 0) &&
                      ((reinterpret_cast<uintptr_t>(out) & 15) == 0);
-    if (vec) return launch_pdl(bcast_kernel<T, true>, grid, dim3(256), 0, stream, N, C, HW, op, var, eps, o);
-    return launch_pdl(bcast_kernel<T, false>, grid, dim3(256), 0, stream, N, C, HW, op, var, eps, o);
+    if (vec) return launch_pdl(bcast_kernel<T, true>, grid, dim3(128), 0, stream, N, C, HW, op, var, eps, o);
+    return launch_pdl(bcast_kernel<T, false>, grid, dim3(128), 0, stream, N, C, HW, op, var, eps, o);
 }
 
 }  // namespace
