@@ -125,6 +125,18 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
     bool alive = true;
     for (int u = blockIdx.x; alive && u < p.units; u += gridDim.x) {
         const Unit w = decode(p, u);
+        // partial sums take no epilogue, except the bias that the first of the
+        // slices adding into the output brings.  Lane l fetches channel l of each
+        // of the warp's chunks now, before the accumulator is ready; the chunk
+        // loop hands the values round with shuffles (a per-chunk load of all 32
+        // biases cost a DRAM round trip per chunk after a cold start).
+        const bool use_bias = !p.ws && p.epi != BIGEMM_EPI_NONE && !(p.red_add && w.sp != 0);
+        float bl[kMine];
+#pragma unroll
+        for (int i = 0; i < kMine; ++i) {
+            const int c = w.ct * BN + (h + kSplit * i) * 32 + lane;
+            bl[i] = (use_bias && c < p.CO) ? __ldg(p.bias + c) : 0.f;
+        }
 #pragma unroll 1
       for (int m = 0; m < MT; ++m) {
         // where this lane's pixel and this warp's store box go: computed
@@ -205,12 +217,10 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
             float v[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(cur[j]);
-            // partial sums take no epilogue, except the bias that the first of the
-            // slices adding into the output brings
-            if (!p.ws && p.epi != BIGEMM_EPI_NONE && !(p.red_add && w.sp != 0)) {
+            if (use_bias) {
                 float bv[32];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) bv[j] = cb + j < p.CO ? __ldg(p.bias + cb + j) : 0.f;
+                for (int j = 0; j < 32; ++j) bv[j] = __shfl_sync(0xffffffffu, bl[i], j);
                 if (p.epi == BIGEMM_EPI_BIAS) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] += bv[j];
