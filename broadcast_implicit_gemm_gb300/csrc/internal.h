@@ -147,6 +147,11 @@ bool dw_stream_ok(const ConvShape &s);
 // rows: output rows per thread (2, 4 or 8).
 cudaError_t launch_dw_stream(const ConvShape &s, const void *x, const void *w, const float *bias,
                              float eps, void *out, int rows, cudaStream_t stream);
+// Whole-plane depthwise kernel for planes up to 32 x 32 (same kernels as the
+// streaming one): one or two planes per warp staged in shared memory.
+bool dw_plane_ok(const ConvShape &s);
+cudaError_t launch_dw_plane(const ConvShape &s, const void *x, const void *w, const float *bias,
+                            float eps, void *out, cudaStream_t stream);
 cudaError_t launch_bcast(int N, int C, int HW, int op, const float *var, float eps, void *out,
                          int out_dt, int flat, cudaStream_t stream);
 cudaError_t launch_wait_timeout_probe(int *err, unsigned long long timeout_ns,

@@ -31,7 +31,7 @@ size_t dw_smem_bytes(const ConvShape &s, int rows);
 
 namespace {
 
-enum SimtVariant { SV_NAIVE = 0, SV_TILED = 1, SV_DW = 2, SV_DWS = 3 };
+enum SimtVariant { SV_NAIVE = 0, SV_TILED = 1, SV_DW = 2, SV_DWS = 3, SV_DWP = 4 };
 
 struct Cand {
     int kind = BIGEMM_KIND_SIMT;
@@ -53,6 +53,8 @@ std::string cand_str(const Cand &c)
         snprintf(b, sizeof b, "simt:depthwise:rows%d", c.dw_rows);
     else if (c.simt_variant == SV_DWS)
         snprintf(b, sizeof b, "simt:depthwise:stream%d", c.dw_rows);
+    else if (c.simt_variant == SV_DWP)
+        snprintf(b, sizeof b, "simt:depthwise:plane");
 
     else
         snprintf(b, sizeof b, "simt:%s", c.simt_variant == SV_TILED ? "tiled" : "naive");
@@ -87,6 +89,7 @@ bool parse_cand(const std::string &s, Cand &c)
         c.simt_variant = SV_DWS, c.dw_rows = g;
         return true;
     }
+    if (s == "simt:depthwise:plane") return c = Cand{}, c.simt_variant = SV_DWP, true;
     if (s == "simt:tiled") return c = Cand{}, c.simt_variant = SV_TILED, true;
     if (s == "simt:naive") return c = Cand{}, c.simt_variant = SV_NAIVE, true;
     return false;
@@ -353,6 +356,9 @@ bool simt_valid(const ConvShape &s, const Cand &c, std::string *why)
         if (why) *why = "tiled SIMT needs groups = 1";
         return false;
     }
+    if (c.simt_variant == SV_DWP && !dw_plane_ok(s))
+        return why && (*why = "plane depthwise needs a streaming-kernel shape with H, W <= 32", true),
+               false;
     if (c.simt_variant == SV_DWS && !dw_stream_ok(s))
         return why && (*why = "streaming depthwise needs a square 3/5/7 kernel, pad K/2, stride 1-2",
                        true),
@@ -504,6 +510,11 @@ std::vector<Cand> candidates(const ConvShape &s, int sms)
 {
     std::vector<Cand> v;
     if (is_depthwise(s)) {
+        if (dw_plane_ok(s)) {
+            Cand c;
+            c.simt_variant = SV_DWP;
+            v.push_back(c);
+        }
         if (dw_stream_ok(s))
             for (int rows : {2, 4, 8}) {
                 if (rows == 8 && !(s.stride == 1 && s.KH <= 5)) continue;
@@ -803,7 +814,9 @@ bigemm_status run_plan(bigemm_plan_s *p, const void *data, const void *kernel, c
     if (!ds) return BIGEMM_ERR_CUDA;
     cudaError_t e = cudaSuccess;
     if (p->c.kind != BIGEMM_KIND_UMMA) {
-        if (p->c.simt_variant == SV_DWS)
+        if (p->c.simt_variant == SV_DWP)
+            e = launch_dw_plane(s, data, kernel, bias, eps, out, st);
+        else if (p->c.simt_variant == SV_DWS)
             e = launch_dw_stream(s, data, kernel, bias, eps, out, p->c.dw_rows, st);
         else if (p->c.simt_variant == SV_DW)
             e = launch_dw_conv(s, data, kernel, bias, eps, out, p->c.dw_rows, st);
@@ -1076,14 +1089,17 @@ bigemm_status plan_impl(int N, int H, int W, int CO, int CI, int KH, int KW, int
             c = heuristic(s, sms);
             if (opts->kind == BIGEMM_KIND_SIMT && opts->mode != 0) {
                 // an explicit SIMT kernel: 1 tiled (groups = 1) or naive, 2 depthwise staged
-                // band (box_h rows per block), 3 depthwise streaming (box_h rows per thread)
-                if (opts->mode < 1 || opts->mode > 3) return BIGEMM_ERR_INVALID_ARG;
+                // band (box_h rows per block), 3 depthwise streaming (box_h rows per thread),
+                // 4 depthwise whole planes (H, W <= 32)
+                if (opts->mode < 1 || opts->mode > 4) return BIGEMM_ERR_INVALID_ARG;
                 c = Cand{};
                 if (opts->mode == 1) {
                     c.simt_variant = groups == 1 ? SV_TILED : SV_NAIVE;
                 } else if (opts->mode == 2) {
                     c.simt_variant = SV_DW;
                     c.dw_rows = opts->box_h > 0 ? opts->box_h : 8;
+                } else if (opts->mode == 4) {
+                    c.simt_variant = SV_DWP;
                 } else {
                     c.simt_variant = SV_DWS;
                     c.dw_rows = opts->box_h > 0 ? opts->box_h : 2;

@@ -585,6 +585,136 @@ __global__ void __launch_bounds__(128) dw_stream_kernel(SimtArgs a, int gx, int 
     dw_store_rows<R>(a, acc, bias, out, c, plane, x0, y0, vec_out);
 }
 
+// Small planes (depthwise, H and W up to 32): each warp takes one or two whole
+// (image, channel) planes at a time (two when the output is at most 16 wide,
+// one per half-warp).  The planes are staged as fp32 in the warp's shared
+// memory with their zero border, and lane x computes output column x of its
+// plane down all rows, keeping K input rows of K values in registers: each
+// output row costs S*K shared loads and K*K FMAs.  The row loop is unrolled
+// by K so that the ring slot of input row r, r mod K, is a constant.
+constexpr int kDwpMax = 32;   // largest H and W of the plane kernel
+
+template <int DT, int K, int S>
+__global__ void __launch_bounds__(256) dw_plane_kernel(SimtArgs a, int lp, int tstride, FastDiv fd_w,
+                                                       const void *__restrict__ x,
+                                                       const void *__restrict__ w,
+                                                       const float *__restrict__ bias,
+                                                       void *__restrict__ out)
+{
+    griddep_enter();
+    constexpr int P = K / 2;
+    extern __shared__ __align__(16) float dwp_smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // a fixed row pitch (the widest plane plus its border), so that every
+    // shared-memory read of the window is a constant offset from the row base
+    constexpr int TW = kDwpMax + 2 * P;
+    const int TH = a.H + 2 * P;
+    const int ppw = 32 / lp;                           // planes per warp
+    float *tw = dwp_smem + (size_t)warp * ppw * tstride;
+    const int half = lane / lp, xl = lane - half * lp;
+    const long long planes = (long long)a.N * a.CI;
+    const int HW = a.H * a.W, HWo = a.Ho * a.Wo;
+    const long long nwarps = (long long)gridDim.x * (blockDim.x >> 5);
+    for (long long pp = ((long long)blockIdx.x * (blockDim.x >> 5) + warp) * ppw; pp < planes;
+         pp += nwarps * ppw) {
+        const int np = (int)min((long long)ppw, planes - pp);
+        __syncwarp();                                  // the previous planes' reads are done
+        // zero border (whole tiles), then the interiors
+        for (int i = lane * 4; i < ppw * tstride; i += 128)
+            *reinterpret_cast<float4 *>(tw + i) = make_float4(0.f, 0.f, 0.f, 0.f);
+        __syncwarp();
+        // the weights first, so that their loads overlap the plane's
+        const long long plane = pp + half;
+        const int c = (int)(plane % a.CI);
+        float wr[K][K];
+#pragma unroll
+        for (int ky = 0; ky < K; ++ky)
+#pragma unroll
+            for (int kx = 0; kx < K; ++kx) wr[ky][kx] = ld_in(w, (size_t)c * K * K + ky * K + kx, DT);
+        // the np planes are one contiguous run: 16-byte loads, four per lane in
+        // flight, where it is aligned
+        constexpr int VE = DwIn<DT>::VE;
+        const int nel = np * HW;
+        const char *src = static_cast<const char *>(x) + (size_t)(pp * HW) * (DT == BIGEMM_F32 ? 4 : 2);
+        if ((reinterpret_cast<uintptr_t>(src) & 15) == 0 && nel % VE == 0) {
+            const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
+            const int nv = nel / VE;
+            for (int v0 = 0; v0 < nv; v0 += 128) {
+                uint4 u[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int v = v0 + k * 32 + lane;
+                    u[k] = v < nv ? __ldg(s4 + v) : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int v = v0 + k * 32 + lane;
+                    if (v < nv) {
+                        float f[VE];
+                        DwIn<DT>::cvt(u[k], f);
+#pragma unroll
+                        for (int e = 0; e < VE; ++e) {
+                            const int g = v * VE + e;
+                            uint32_t q = 0, r = (uint32_t)g;
+                            if (g >= HW) q = 1, r -= (uint32_t)HW;
+                            uint32_t ix;
+                            const uint32_t iy = fd_divmod(r, fd_w, &ix);
+                            tw[q * tstride + (iy + P) * TW + ix + P] = f[e];
+                        }
+                    }
+                }
+            }
+        } else {
+            for (int i = lane; i < nel; i += 32) {
+                uint32_t q = 0, r = (uint32_t)i;
+                if (i >= HW) q = 1, r -= (uint32_t)HW;
+                uint32_t ix;
+                const uint32_t iy = fd_divmod(r, fd_w, &ix);
+                tw[q * tstride + (iy + P) * TW + ix + P] = ld_in(x, (size_t)(pp * HW) + i, DT);
+            }
+        }
+        __syncwarp();
+        if (half >= np || xl >= a.Wo) continue;
+        const float *t = tw + half * tstride + S * xl;
+        const size_t obase = (size_t)plane * HWo + xl;
+        float win[K][K];                               // ring: input row r in slot r % K
+#pragma unroll
+        for (int r = 0; r < K - S; ++r)
+#pragma unroll
+            for (int kx = 0; kx < K; ++kx) win[r % K][kx] = t[r * TW + kx];
+        for (int y0 = 0; y0 < a.Ho; y0 += K) {
+#pragma unroll
+            for (int u = 0; u < K; ++u) {
+                const int y = y0 + u;
+                if (y < a.Ho) {
+#pragma unroll
+                    for (int j = 0; j < S; ++j) {   // the S rows this output row adds
+                        const int r = S * y + K - S + j;
+                        const int sl = (S * u + K - S + j) % K;
+#pragma unroll
+                        for (int kx = 0; kx < K; ++kx) win[sl][kx] = t[r * TW + kx];
+                    }
+                    // one partial sum per kernel row: K independent FMA chains
+                    float pr[K];
+#pragma unroll
+                    for (int ky = 0; ky < K; ++ky) {
+                        pr[ky] = win[(S * u + ky) % K][0] * wr[ky][0];
+#pragma unroll
+                        for (int kx = 1; kx < K; ++kx)
+                            pr[ky] = fmaf(win[(S * u + ky) % K][kx], wr[ky][kx], pr[ky]);
+                    }
+                    float acc = pr[0];
+#pragma unroll
+                    for (int ky = 1; ky < K; ++ky) acc += pr[ky];
+                    st_out(out, obase + (size_t)y * a.Wo, epi_apply(a.epi, acc, bias, c, a.eps),
+                           a.out_dt);
+                }
+            }
+        }
+        (void)TH;
+    }
+}
+
 SimtArgs make_args(const ConvShape &s, float eps)
 {
     SimtArgs a;
@@ -669,6 +799,60 @@ bool dw_stream_ok(const ConvShape &s)
     if (s.KH != s.KW || s.pad != s.KH / 2) return false;
     if (!(s.KH == 3 || s.KH == 5 || s.KH == 7)) return false;
     return s.stride == 1 || s.stride == 2;
+}
+
+size_t dw_plane_smem(const ConvShape &s, int *lp, int *tstride);
+
+bool dw_plane_ok(const ConvShape &s)
+{
+    if (!(dw_stream_ok(s) && s.H <= kDwpMax && s.W <= kDwpMax && s.Wo <= 32)) return false;
+    int lp = 0, ts = 0;
+    return dw_plane_smem(s, &lp, &ts) <= 48 * 1024;   // static-size limit, no opt-in
+}
+
+size_t dw_plane_smem(const ConvShape &s, int *lp, int *tstride)
+{
+    const int P = s.KH / 2;
+    const int tsz = (s.H + 2 * P) * (kDwpMax + 2 * P);   // the kernel's fixed row pitch
+    // a plane's floats rounded up to 4; with two planes per warp, an odd
+    // multiple of 16 so that the two half-warps' planes sit on different banks
+    const int t1 = (tsz + 3) & ~3;
+    const int t2 = ((t1 + 15) / 16 | 1) * 16;
+    const bool two = s.Wo <= 16 && (size_t)8 * 2 * t2 * sizeof(float) <= 48 * 1024;
+    *lp = two ? 16 : 32;
+    *tstride = two ? t2 : t1;
+    return (size_t)8 * (two ? 2 : 1) * (*tstride) * sizeof(float);
+}
+
+cudaError_t launch_dw_plane(const ConvShape &s, const void *x, const void *w, const float *bias,
+                            float eps, void *out, cudaStream_t stream)
+{
+    if (!dw_plane_ok(s)) return cudaErrorInvalidValue;
+    ProfScope prof("simt_conv_depthwise", stream);
+    const SimtArgs a = make_args(s, eps);
+    int lp = 32, tstride = 0;
+    const size_t smem = dw_plane_smem(s, &lp, &tstride);
+    const long long planes = (long long)s.N * s.CI;
+    DeviceState *ds = device_state();
+    const int sms = ds ? ds->sm_count : 148;
+    const long long warps_needed = (planes + (32 / lp) - 1) / (32 / lp);
+    long long blocks = std::min<long long>((warps_needed + 7) / 8, (long long)sms * 8);
+    if (blocks < 1) blocks = 1;
+    const FastDiv fdw = make_fastdiv((uint32_t)s.W);
+    auto go = [&](auto kern) {
+        return launch_pdl(kern, dim3((unsigned)blocks), dim3(256), smem, stream, a, lp, tstride, fdw,
+                          x, w, bias, out);
+    };
+#define BIGEMM_DWP(DTV, KV, SV) \
+    if (s.KH == KV && s.stride == SV) return go(dw_plane_kernel<DTV, KV, SV>);
+#define BIGEMM_DWPS(DTV)                                                                 \
+    BIGEMM_DWP(DTV, 3, 1) BIGEMM_DWP(DTV, 3, 2) BIGEMM_DWP(DTV, 5, 1) BIGEMM_DWP(DTV, 5, 2) \
+    BIGEMM_DWP(DTV, 7, 1) BIGEMM_DWP(DTV, 7, 2) return cudaErrorInvalidValue;
+    if (s.in_dt == BIGEMM_F32) { BIGEMM_DWPS(BIGEMM_F32) }
+    if (s.in_dt == BIGEMM_F16) { BIGEMM_DWPS(BIGEMM_F16) }
+    BIGEMM_DWPS(BIGEMM_BF16)
+#undef BIGEMM_DWPS
+#undef BIGEMM_DWP
 }
 
 cudaError_t launch_dw_stream(const ConvShape &s, const void *x, const void *w, const float *bias,

@@ -108,7 +108,8 @@ typedef struct {
                        With kind = SIMT it names the kernel instead: 1 tiled
                        (groups = 1) or naive, 2 depthwise staged band (box_h
                        rows per block), 3 depthwise streaming (box_h = 2, 4
-                       or 8 rows per thread).
+                       or 8 rows per thread), 4 depthwise whole planes
+                       (H, W <= 32, one or two planes per warp).
                        Other values: INVALID_ARG.                               */
     int resident_b; /* UMMA: 1 keeps the weights resident in shared memory --
                        halo modes: one output-channel tile must cover CO and

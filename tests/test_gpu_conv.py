@@ -457,6 +457,28 @@ def test_depthwise_staged_band(spec):
     assert info["cand"] == "simt:depthwise:rows4"
 
 
+# Whole planes per warp (H, W <= 32): two planes per warp for outputs up to
+# 16 wide, one above; an odd plane count leaves the last warp one plane.
+DW_PLANE = [x for x in DW if x.H <= 32 and x.W <= 32] + [
+    S("dwp_odd_planes_k3", 1, 7, 7, 14, 14, 3, 1, 1, g=7, kd="dw"),
+    S("dwp_k5_576_like", 2, 24, 24, 14, 14, 5, 1, 2, g=24, kd="dw"),
+    S("dwp_k3s2_32wide", 1, 12, 12, 32, 32, 3, 2, 1, g=12, o="f32", epi="bias", kd="dw"),
+]
+
+
+@pytest.mark.parametrize("spec", DW_PLANE, ids=lambda s: s.name)
+def test_depthwise_whole_planes(spec):
+    info = check(spec, {"kind": bg.KIND_SIMT, "mode": 4})
+    assert info["cand"] == "simt:depthwise:plane"
+
+
+def test_depthwise_whole_planes_rejects_wide_rows():
+    with pytest.raises(bg.BigemmError) as e:
+        bg.conv2d_nchw_plan_ex(1, 8, 40, 8, 8, 3, 3, 1, 1, 8, bg.F16, bg.F16, bg.EPI_NONE, 0,
+                               {"kind": bg.KIND_SIMT, "mode": 4})
+    assert e.value.status == 2
+
+
 # ------------------------------------------------- full size, sampled outputs
 FULL = synth.RESNET50_FP16 + synth.FUSED_CONV + synth.DEPTHWISE_FP16
 
