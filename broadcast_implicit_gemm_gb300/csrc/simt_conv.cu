@@ -1,6 +1,6 @@
 // simt_conv.cu -- direct NCHW convolution on the FP32 pipes (no tensor cores).
 //
-// Three kernels, all computing the tutorial's conv2d_nchw definition with fp32
+// The kernels here all compute the tutorial's conv2d_nchw definition with fp32
 // accumulation ("Tuning High Performance Convolution on NVIDIA GPUs", Step 1):
 //  * conv_tiled  (groups = 1): a 64-channel x 64-pixel output tile per block,
 //    256 threads with a 4x4 register block each; each K chunk of 16 reduction
@@ -11,58 +11,16 @@
 //    output rows); the band's input rows are staged once in shared memory with
 //    explicit zero borders, the channel's KHxKW taps sit in registers, and each
 //    thread slides along x producing neighbouring outputs.
-//  * dw_stream (groups = C = CO, square 3x3 / 5x5 / 7x7 kernels with pad K/2,
-//    stride 1 or 2): one thread per 8 neighbouring outputs x R output rows of a
-//    plane, reading each input row of its window once with 16-byte loads
-//    straight from global memory (neighbours' overlapping vectors hit L1),
-//    converting it to fp32 once and adding it into every output row it feeds.
-//    No shared memory and no block barrier, so it streams at HBM rate.
 //  * conv_naive (any groups): one thread per output; the fallback for grouped
 //    shapes neither kernel above covers.
 #include <algorithm>
 
-#include <cuda_bf16.h>
-#include <cuda_fp16.h>
+#include "simt_common.cuh"
 
-#include "internal.h"
-#include "ptx.cuh"
-
+// (The streaming and whole-plane depthwise kernels are in dw_conv.cu.)
 namespace bigemm {
 
 namespace {
-
-__device__ __forceinline__ float ld_in(const void *p, size_t i, int dt)
-{
-    if (dt == BIGEMM_F32) return __ldg(static_cast<const float *>(p) + i);
-    if (dt == BIGEMM_F16) return __half2float(__ldg(static_cast<const __half *>(p) + i));
-    return __bfloat162float(__ldg(static_cast<const __nv_bfloat16 *>(p) + i));
-}
-
-__device__ __forceinline__ void st_out(void *p, size_t i, float v, int dt)
-{
-    if (dt == BIGEMM_F32)
-        static_cast<float *>(p)[i] = v;
-    else if (dt == BIGEMM_F16)
-        static_cast<__half *>(p)[i] = __float2half_rn(v);
-    else
-        static_cast<__nv_bfloat16 *>(p)[i] = __float2bfloat16_rn(v);
-}
-
-__device__ __forceinline__ float epi_apply(int epi, float acc, const float *bias, int f, float eps)
-{
-    switch (epi) {
-    case BIGEMM_EPI_NONE: return acc;
-    case BIGEMM_EPI_BIAS: return acc + bias[f];
-    case BIGEMM_EPI_BIAS_EXP: return expf(acc + bias[f]);
-    default: return rsqrtf(acc + bias[f] + eps);
-    }
-}
-
-struct SimtArgs {
-    int N, CI, H, W, CO, KH, KW, stride, pad, groups, Ho, Wo;
-    int in_dt, out_dt, epi;
-    float eps;
-};
 
 constexpr int TM = 64, TN = 64, TK = 16;
 
@@ -332,399 +290,8 @@ __global__ void __launch_bounds__(256) conv_depthwise_kernel(SimtArgs a, int row
     }
 }
 
-// ---------------------------------------------------------- streaming depthwise
-constexpr int kDwsXO = 8;   // neighbouring outputs per thread
-
-// Epilogue and stores of a thread's R x 8 outputs (rows y0.., columns x0..).
-template <int R>
-__device__ __forceinline__ void dw_store_rows(const SimtArgs &a, const float (&acc)[R][kDwsXO],
-                                              const float *__restrict__ bias,
-                                              void *__restrict__ out, int c, long long plane,
-                                              int x0, int y0, int vec_out)
-{
-    constexpr int XO = kDwsXO;
-    const float bv = a.epi != BIGEMM_EPI_NONE ? bias[c] : 0.f;
-    const int xn = min(XO, a.Wo - x0);
-#pragma unroll
-    for (int i = 0; i < R; ++i) {
-        const int y = y0 + i;
-        if (y >= a.Ho) break;
-        float o8[XO];
-#pragma unroll
-        for (int o = 0; o < XO; ++o) {
-            float vv = acc[i][o];
-            if (a.epi == BIGEMM_EPI_BIAS) vv += bv;
-            else if (a.epi == BIGEMM_EPI_BIAS_EXP) vv = expf(vv + bv);
-            else if (a.epi == BIGEMM_EPI_BIAS_RSQRT) vv = rsqrtf(vv + bv + a.eps);
-            o8[o] = vv;
-        }
-        const size_t o = ((size_t)plane * a.Ho + y) * a.Wo + x0;
-        if (vec_out && xn == XO) {
-            if (a.out_dt == BIGEMM_F32) {
-                float4 *q = reinterpret_cast<float4 *>(static_cast<float *>(out) + o);
-                q[0] = make_float4(o8[0], o8[1], o8[2], o8[3]);
-                q[1] = make_float4(o8[4], o8[5], o8[6], o8[7]);
-            } else {
-                uint32_t pk[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    if (a.out_dt == BIGEMM_F16) {
-                        const __half2 h = __floats2half2_rn(o8[2 * k], o8[2 * k + 1]);
-                        pk[k] = *reinterpret_cast<const uint32_t *>(&h);
-                    } else {
-                        const __nv_bfloat162 h = __floats2bfloat162_rn(o8[2 * k], o8[2 * k + 1]);
-                        pk[k] = *reinterpret_cast<const uint32_t *>(&h);
-                    }
-                }
-                *reinterpret_cast<uint4 *>(static_cast<char *>(out) + o * 2) =
-                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            }
-        } else {
-#pragma unroll
-            for (int k = 0; k < XO; ++k)
-                if (k < xn) st_out(out, o + k, o8[k], a.out_dt);
-        }
-    }
-}
-
-// DT: input type (BIGEMM_F32 / F16 / BF16); K: kernel size (pad K/2); S: stride;
-// R: output rows per thread.  A "row unit" is R output rows of one plane, split
-// into gx groups of 8 columns.  rpw > 0: each warp holds rpw whole row units
-// (lane = unit * gx + g, gx <= 32), so a group's neighbours are the lanes
-// beside it; rpw = 0: thread t -> (g, unit) = (t % gx, t / gx).
-template <int DT>
-struct DwIn;
-template <>
-struct DwIn<BIGEMM_F32> {
-    static constexpr int VE = 4;
-    __device__ static void cvt(const uint4 &u, float *f)
-    {
-        f[0] = __uint_as_float(u.x), f[1] = __uint_as_float(u.y);
-        f[2] = __uint_as_float(u.z), f[3] = __uint_as_float(u.w);
-    }
-};
-template <>
-struct DwIn<BIGEMM_F16> {
-    static constexpr int VE = 8;
-    __device__ static void cvt(const uint4 &u, float *f)
-    {
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 p = __half22float2(*reinterpret_cast<const __half2 *>(&w[i]));
-            f[2 * i] = p.x, f[2 * i + 1] = p.y;
-        }
-    }
-};
-template <>
-struct DwIn<BIGEMM_BF16> {
-    static constexpr int VE = 8;
-    __device__ static void cvt(const uint4 &u, float *f)
-    {
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 p = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[i]));
-            f[2 * i] = p.x, f[2 * i + 1] = p.y;
-        }
-    }
-};
-
-
-template <int DT, int K, int S, int R>
-__global__ void __launch_bounds__(128) dw_stream_kernel(SimtArgs a, int gx, int nrr, int rpw,
-                                                        FastDiv fd_gx, FastDiv fd_nrr,
-                                                        FastDiv fd_ci,
-                                                        const void *__restrict__ x,
-                                                        const void *__restrict__ w,
-                                                        const float *__restrict__ bias,
-                                                        void *__restrict__ out, int vec_in,
-                                                        int vec_out)
-{
-    griddep_enter();
-    constexpr int XO = kDwsXO;
-    constexpr int P = K / 2;
-    constexpr int VE = DwIn<DT>::VE;
-    constexpr int WIN = (XO - 1) * S + K;            // input columns of one row
-    constexpr int NR = (R - 1) * S + K;              // input rows of the window
-    constexpr int OWN = XO * S;                      // columns x0*S .. x0*S + OWN - 1
-    constexpr int NVO = OWN / VE;                    // their vectors (x0*S is a multiple of VE)
-    constexpr int RH = P + 1 - S > 0 ? P + 1 - S : 0;   // columns right of OWN in the window
-    static_assert(P + OWN + RH == WIN, "window = left halo + own columns + right halo");
-    static_assert(P <= OWN && RH <= OWN, "halos come from the neighbouring lanes");
-    // indices stay below 2^31 (checked at launch); divisions by the launch's
-    // fixed gx, nrr and CI are multiply-high sequences
-    const uint32_t t = blockIdx.x * blockDim.x + threadIdx.x;
-    const uint32_t units = (uint32_t)(a.N * a.CI) * (uint32_t)nrr;
-    int g;
-    uint32_t unit;
-    if (rpw > 0) {
-        const int lane = threadIdx.x & 31, ui = lane / gx;
-        g = lane - ui * gx;
-        unit = (t >> 5) * (uint32_t)rpw + (uint32_t)ui;
-        if (ui >= rpw) unit = units;                 // spare lanes of the warp
-    } else {
-        uint32_t gg;
-        unit = fd_divmod(t, fd_gx, &gg);
-        g = (int)gg;
-    }
-    const bool active = unit < units;
-    uint32_t rr32, c32;
-    const uint32_t plane = fd_divmod(active ? unit : units - 1, fd_nrr, &rr32);
-    fd_divmod(plane, fd_ci, &c32);
-    const int rr = (int)rr32, c = (int)c32;
-    const int x0 = g * XO, y0 = rr * R;
-    const int xs = x0 * S - P, iy0 = y0 * S - P;
-    const size_t esz = DT == BIGEMM_F32 ? 4 : 2;
-    const char *xp = static_cast<const char *>(x) + (size_t)plane * a.H * a.W * esz;
-
-    float wt[K * K];
-#pragma unroll
-    for (int i = 0; i < K * K; ++i) wt[i] = ld_in(w, (size_t)c * K * K + i, DT);
-    float acc[R][XO];
-#pragma unroll
-    for (int i = 0; i < R; ++i)
-#pragma unroll
-        for (int o = 0; o < XO; ++o) acc[i][o] = 0.f;
-
-    if (vec_in != 0) {
-        // Each lane loads only its own columns, every row of the window at
-        // once; the halos come from the lanes of the neighbouring x groups
-        // (with rpw > 0, groups g - 1 and g + 1 of a unit are lanes - 1 and
-        // + 1; at the row ends the halo lies in the zero padding).  The whole
-        // warp takes part in the shuffles.
-        uint4 raw[NR][NVO];
-#pragma unroll
-        for (int j = 0; j < NR; ++j) {
-            const int iy = iy0 + j;
-            const bool row_in = active && iy >= 0 && iy < a.H;
-            const char *row = xp + (size_t)(row_in ? iy : 0) * a.W * esz;
-#pragma unroll
-            for (int k = 0; k < NVO; ++k) {
-                const int vx = x0 * S + k * VE;
-                if (vec_in == 1) {          // 16-byte vectors (W % VE == 0)
-                    raw[j][k] = (row_in && vx < a.W)
-                                    ? __ldg(reinterpret_cast<const uint4 *>(row + (size_t)vx * esz))
-                                    : make_uint4(0u, 0u, 0u, 0u);
-                } else {                    // 4-byte words (W * esz % 4 == 0)
-                    constexpr int EW = (int)(4 / (DT == BIGEMM_F32 ? 4 : 2));   // elements per word
-                    uint32_t wd[4];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int ex = vx + q * EW;
-                        wd[q] = (row_in && ex + EW <= a.W)
-                                    ? __ldg(reinterpret_cast<const uint32_t *>(row + (size_t)ex * esz))
-                                    : 0u;
-                    }
-                    raw[j][k] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
-                }
-            }
-        }
-        const bool left_ok = g > 0, right_ok = g + 1 < gx;
-#pragma unroll
-        for (int j = 0; j < NR; ++j) {
-            float v[WIN];
-#pragma unroll
-            for (int k = 0; k < NVO; ++k) DwIn<DT>::cvt(raw[j][k], v + P + k * VE);
-#pragma unroll
-            for (int h = 0; h < P; ++h) {
-                const float lv = __shfl_up_sync(0xffffffffu, v[P + OWN - P + h], 1);
-                v[h] = left_ok ? lv : 0.f;
-            }
-#pragma unroll
-            for (int h = 0; h < RH; ++h) {
-                const float rv = __shfl_down_sync(0xffffffffu, v[P + h], 1);
-                v[P + OWN + h] = right_ok ? rv : 0.f;
-            }
-#pragma unroll
-            for (int i = 0; i < R; ++i) {
-                const int ry = j - i * S;
-                if (ry >= 0 && ry < K) {
-#pragma unroll
-                    for (int rx = 0; rx < K; ++rx) {
-                        const float tap = wt[ry * K + rx];
-#pragma unroll
-                        for (int o = 0; o < XO; ++o)
-                            acc[i][o] = fmaf(v[o * S + rx], tap, acc[i][o]);
-                    }
-                }
-            }
-        }
-    } else {
-        // element loads with bounds checks, one row at a time
-#pragma unroll
-        for (int j = 0; j < NR; ++j) {
-            const int iy = iy0 + j;
-            float v[WIN];
-#pragma unroll
-            for (int i = 0; i < WIN; ++i) v[i] = 0.f;
-            if (active && iy >= 0 && iy < a.H) {
-                const char *row = xp + (size_t)iy * a.W * esz;
-#pragma unroll
-                for (int i = 0; i < WIN; ++i) {
-                    const int ix = xs + i;
-                    if (ix >= 0 && ix < a.W) v[i] = ld_in(row, (size_t)ix, DT);
-                }
-            }
-#pragma unroll
-            for (int i = 0; i < R; ++i) {
-                const int ry = j - i * S;
-                if (ry >= 0 && ry < K) {
-#pragma unroll
-                    for (int rx = 0; rx < K; ++rx) {
-                        const float tap = wt[ry * K + rx];
-#pragma unroll
-                        for (int o = 0; o < XO; ++o)
-                            acc[i][o] = fmaf(v[o * S + rx], tap, acc[i][o]);
-                    }
-                }
-            }
-        }
-    }
-    if (!active) return;
-    dw_store_rows<R>(a, acc, bias, out, c, plane, x0, y0, vec_out);
-}
-
-// Small planes (depthwise, H and W up to 32): each warp takes one or two whole
-// (image, channel) planes at a time (two when the output is at most 16 wide,
-// one per half-warp).  The planes are staged as fp32 in the warp's shared
-// memory with their zero border, and lane x computes output column x of its
-// plane down all rows, keeping K input rows of K values in registers: each
-// output row costs S*K shared loads and K*K FMAs.  The row loop is unrolled
-// by K so that the ring slot of input row r, r mod K, is a constant.
-constexpr int kDwpMax = 32;   // largest H and W of the plane kernel
-
-template <int DT, int K, int S>
-__global__ void __launch_bounds__(256) dw_plane_kernel(SimtArgs a, int lp, int tstride, FastDiv fd_w,
-                                                       const void *__restrict__ x,
-                                                       const void *__restrict__ w,
-                                                       const float *__restrict__ bias,
-                                                       void *__restrict__ out)
-{
-    griddep_enter();
-    constexpr int P = K / 2;
-    extern __shared__ __align__(16) float dwp_smem[];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // a fixed row pitch (the widest plane plus its border), so that every
-    // shared-memory read of the window is a constant offset from the row base
-    constexpr int TW = kDwpMax + 2 * P;
-    const int TH = a.H + 2 * P;
-    const int ppw = 32 / lp;                           // planes per warp
-    float *tw = dwp_smem + (size_t)warp * ppw * tstride;
-    const int half = lane / lp, xl = lane - half * lp;
-    const long long planes = (long long)a.N * a.CI;
-    const int HW = a.H * a.W, HWo = a.Ho * a.Wo;
-    const long long nwarps = (long long)gridDim.x * (blockDim.x >> 5);
-    for (long long pp = ((long long)blockIdx.x * (blockDim.x >> 5) + warp) * ppw; pp < planes;
-         pp += nwarps * ppw) {
-        const int np = (int)min((long long)ppw, planes - pp);
-        __syncwarp();                                  // the previous planes' reads are done
-        // zero border (whole tiles), then the interiors
-        for (int i = lane * 4; i < ppw * tstride; i += 128)
-            *reinterpret_cast<float4 *>(tw + i) = make_float4(0.f, 0.f, 0.f, 0.f);
-        __syncwarp();
-        // the weights first, so that their loads overlap the plane's
-        const long long plane = pp + half;
-        const int c = (int)(plane % a.CI);
-        float wr[K][K];
-#pragma unroll
-        for (int ky = 0; ky < K; ++ky)
-#pragma unroll
-            for (int kx = 0; kx < K; ++kx) wr[ky][kx] = ld_in(w, (size_t)c * K * K + ky * K + kx, DT);
-        // the np planes are one contiguous run: 16-byte loads, four per lane in
-        // flight, where it is aligned
-        constexpr int VE = DwIn<DT>::VE;
-        const int nel = np * HW;
-        const char *src = static_cast<const char *>(x) + (size_t)(pp * HW) * (DT == BIGEMM_F32 ? 4 : 2);
-        if ((reinterpret_cast<uintptr_t>(src) & 15) == 0 && nel % VE == 0) {
-            const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
-            const int nv = nel / VE;
-            for (int v0 = 0; v0 < nv; v0 += 128) {
-                uint4 u[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int v = v0 + k * 32 + lane;
-                    u[k] = v < nv ? __ldg(s4 + v) : make_uint4(0, 0, 0, 0);
-                }
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int v = v0 + k * 32 + lane;
-                    if (v < nv) {
-                        float f[VE];
-                        DwIn<DT>::cvt(u[k], f);
-#pragma unroll
-                        for (int e = 0; e < VE; ++e) {
-                            const int g = v * VE + e;
-                            uint32_t q = 0, r = (uint32_t)g;
-                            if (g >= HW) q = 1, r -= (uint32_t)HW;
-                            uint32_t ix;
-                            const uint32_t iy = fd_divmod(r, fd_w, &ix);
-                            tw[q * tstride + (iy + P) * TW + ix + P] = f[e];
-                        }
-                    }
-                }
-            }
-        } else {
-            for (int i = lane; i < nel; i += 32) {
-                uint32_t q = 0, r = (uint32_t)i;
-                if (i >= HW) q = 1, r -= (uint32_t)HW;
-                uint32_t ix;
-                const uint32_t iy = fd_divmod(r, fd_w, &ix);
-                tw[q * tstride + (iy + P) * TW + ix + P] = ld_in(x, (size_t)(pp * HW) + i, DT);
-            }
-        }
-        __syncwarp();
-        if (half >= np || xl >= a.Wo) continue;
-        const float *t = tw + half * tstride + S * xl;
-        const size_t obase = (size_t)plane * HWo + xl;
-        float win[K][K];                               // ring: input row r in slot r % K
-#pragma unroll
-        for (int r = 0; r < K - S; ++r)
-#pragma unroll
-            for (int kx = 0; kx < K; ++kx) win[r % K][kx] = t[r * TW + kx];
-        for (int y0 = 0; y0 < a.Ho; y0 += K) {
-#pragma unroll
-            for (int u = 0; u < K; ++u) {
-                const int y = y0 + u;
-                if (y < a.Ho) {
-#pragma unroll
-                    for (int j = 0; j < S; ++j) {   // the S rows this output row adds
-                        const int r = S * y + K - S + j;
-                        const int sl = (S * u + K - S + j) % K;
-#pragma unroll
-                        for (int kx = 0; kx < K; ++kx) win[sl][kx] = t[r * TW + kx];
-                    }
-                    // one partial sum per kernel row: K independent FMA chains
-                    float pr[K];
-#pragma unroll
-                    for (int ky = 0; ky < K; ++ky) {
-                        pr[ky] = win[(S * u + ky) % K][0] * wr[ky][0];
-#pragma unroll
-                        for (int kx = 1; kx < K; ++kx)
-                            pr[ky] = fmaf(win[(S * u + ky) % K][kx], wr[ky][kx], pr[ky]);
-                    }
-                    float acc = pr[0];
-#pragma unroll
-                    for (int ky = 1; ky < K; ++ky) acc += pr[ky];
-                    st_out(out, obase + (size_t)y * a.Wo, epi_apply(a.epi, acc, bias, c, a.eps),
-                           a.out_dt);
-                }
-            }
-        }
-        (void)TH;
-    }
-}
-
-SimtArgs make_args(const ConvShape &s, float eps)
-{
-    SimtArgs a;
-    a.N = s.N; a.CI = s.CI; a.H = s.H; a.W = s.W; a.CO = s.CO; a.KH = s.KH; a.KW = s.KW;
-    a.stride = s.stride; a.pad = s.pad; a.groups = s.groups; a.Ho = s.Ho; a.Wo = s.Wo;
-    a.in_dt = s.in_dt; a.out_dt = s.out_dt; a.epi = s.epi; a.eps = eps;
-    return a;
-}
-
 }  // namespace
+
 
 // variant 0: naive (any groups); variant 1: tiled (groups = 1)
 cudaError_t launch_simt_conv(const ConvShape &s, const void *x, const void *w,
@@ -793,118 +360,4 @@ cudaError_t launch_dw_conv(const ConvShape &s, const void *x, const void *w, con
 }
 
 // Streaming depthwise: square K in {3, 5, 7} with pad K/2, stride 1 or 2.
-bool dw_stream_ok(const ConvShape &s)
-{
-    if (!(s.groups > 1 && s.groups == s.CI && s.CO == s.CI)) return false;
-    if (s.KH != s.KW || s.pad != s.KH / 2) return false;
-    if (!(s.KH == 3 || s.KH == 5 || s.KH == 7)) return false;
-    return s.stride == 1 || s.stride == 2;
-}
-
-size_t dw_plane_smem(const ConvShape &s, int *lp, int *tstride);
-
-bool dw_plane_ok(const ConvShape &s)
-{
-    if (!(dw_stream_ok(s) && s.H <= kDwpMax && s.W <= kDwpMax && s.Wo <= 32)) return false;
-    int lp = 0, ts = 0;
-    return dw_plane_smem(s, &lp, &ts) <= 48 * 1024;   // static-size limit, no opt-in
-}
-
-size_t dw_plane_smem(const ConvShape &s, int *lp, int *tstride)
-{
-    const int P = s.KH / 2;
-    const int tsz = (s.H + 2 * P) * (kDwpMax + 2 * P);   // the kernel's fixed row pitch
-    // a plane's floats rounded up to 4; with two planes per warp, an odd
-    // multiple of 16 so that the two half-warps' planes sit on different banks
-    const int t1 = (tsz + 3) & ~3;
-    const int t2 = ((t1 + 15) / 16 | 1) * 16;
-    const bool two = s.Wo <= 16 && (size_t)8 * 2 * t2 * sizeof(float) <= 48 * 1024;
-    *lp = two ? 16 : 32;
-    *tstride = two ? t2 : t1;
-    return (size_t)8 * (two ? 2 : 1) * (*tstride) * sizeof(float);
-}
-
-cudaError_t launch_dw_plane(const ConvShape &s, const void *x, const void *w, const float *bias,
-                            float eps, void *out, cudaStream_t stream)
-{
-    if (!dw_plane_ok(s)) return cudaErrorInvalidValue;
-    ProfScope prof("simt_conv_depthwise", stream);
-    const SimtArgs a = make_args(s, eps);
-    int lp = 32, tstride = 0;
-    const size_t smem = dw_plane_smem(s, &lp, &tstride);
-    const long long planes = (long long)s.N * s.CI;
-    DeviceState *ds = device_state();
-    const int sms = ds ? ds->sm_count : 148;
-    const long long warps_needed = (planes + (32 / lp) - 1) / (32 / lp);
-    long long blocks = std::min<long long>((warps_needed + 7) / 8, (long long)sms * 8);
-    if (blocks < 1) blocks = 1;
-    const FastDiv fdw = make_fastdiv((uint32_t)s.W);
-    auto go = [&](auto kern) {
-        return launch_pdl(kern, dim3((unsigned)blocks), dim3(256), smem, stream, a, lp, tstride, fdw,
-                          x, w, bias, out);
-    };
-#define BIGEMM_DWP(DTV, KV, SV) \
-    if (s.KH == KV && s.stride == SV) return go(dw_plane_kernel<DTV, KV, SV>);
-#define BIGEMM_DWPS(DTV)                                                                 \
-    BIGEMM_DWP(DTV, 3, 1) BIGEMM_DWP(DTV, 3, 2) BIGEMM_DWP(DTV, 5, 1) BIGEMM_DWP(DTV, 5, 2) \
-    BIGEMM_DWP(DTV, 7, 1) BIGEMM_DWP(DTV, 7, 2) return cudaErrorInvalidValue;
-    if (s.in_dt == BIGEMM_F32) { BIGEMM_DWPS(BIGEMM_F32) }
-    if (s.in_dt == BIGEMM_F16) { BIGEMM_DWPS(BIGEMM_F16) }
-    BIGEMM_DWPS(BIGEMM_BF16)
-#undef BIGEMM_DWPS
-#undef BIGEMM_DWP
-}
-
-cudaError_t launch_dw_stream(const ConvShape &s, const void *x, const void *w, const float *bias,
-                             float eps, void *out, int rows, cudaStream_t stream)
-{
-    if (!dw_stream_ok(s)) return cudaErrorInvalidValue;
-    // rows per thread: 2, 4 or 8 (8 only at stride 1 with K <= 5)
-    const int R = rows >= 8 && s.stride == 1 && s.KH <= 5 ? 8 : rows >= 4 ? 4 : 2;
-    ProfScope prof("simt_conv_depthwise", stream);
-    const SimtArgs a = make_args(s, eps);
-    const int gx = (s.Wo + kDwsXO - 1) / kDwsXO;
-    const int nrr = (s.Ho + R - 1) / R;
-    const long long units = (long long)s.N * s.CI * nrr;
-    // whole row units per warp when a row's groups fit in one warp
-    const int rpw = gx <= 32 ? 32 / gx : 0;
-    const long long threads = rpw > 0 ? (units + rpw - 1) / rpw * 32 : units * gx;
-    const long long blocks = (threads + 127) / 128;
-    if (threads + 128 >= (1ll << 31) || units >= (1ll << 31)) return cudaErrorInvalidValue;
-    const int ve = s.in_dt == BIGEMM_F32 ? 4 : 8;
-    // the vector paths take their halos from neighbouring lanes: 16-byte
-    // vectors when rows are 16-byte aligned, else 4-byte words when they are
-    // 4-byte aligned
-    const size_t esz = dtype_size(s.in_dt);
-    const uintptr_t xa = reinterpret_cast<uintptr_t>(x);
-    const int vec_in = rpw == 0                                    ? 0
-                       : (s.W % ve == 0 && (xa & 15) == 0)          ? 1
-                       : ((s.W * esz) % 4 == 0 && (xa & 3) == 0) ? 2
-                                                                   : 0;
-    const int vo = s.out_dt == BIGEMM_F32 ? 4 : 8;
-    const int vec_out = (s.Wo % vo == 0) && ((reinterpret_cast<uintptr_t>(out) & 15) == 0);
-    auto go = [&](auto kern) {
-        return launch_pdl(kern, dim3((unsigned)blocks), dim3(128), 0, stream, a, gx, nrr, rpw,
-                          make_fastdiv((uint32_t)gx), make_fastdiv((uint32_t)nrr),
-                          make_fastdiv((uint32_t)s.CI), x, w, bias, out, vec_in, vec_out);
-    };
-#define BIGEMM_DWK(DTV, KV, SV)                                                           \
-    if (s.KH == KV && s.stride == SV) {                                                   \
-        if (R == 8) return go(dw_stream_kernel<DTV, KV, SV, (SV == 1 && KV <= 5) ? 8 : 4>); \
-        if (R == 4) return go(dw_stream_kernel<DTV, KV, SV, 4>);                          \
-        return go(dw_stream_kernel<DTV, KV, SV, 2>);                                      \
-    }
-#define BIGEMM_DWS(DTV)                                                                   \
-    BIGEMM_DWK(DTV, 3, 1) BIGEMM_DWK(DTV, 3, 2) BIGEMM_DWK(DTV, 5, 1)                     \
-    BIGEMM_DWK(DTV, 5, 2) BIGEMM_DWK(DTV, 7, 1) BIGEMM_DWK(DTV, 7, 2)                     \
-    return cudaErrorInvalidValue;
-    if (s.in_dt == BIGEMM_F32) { BIGEMM_DWS(BIGEMM_F32) }
-    if (s.in_dt == BIGEMM_F16) { BIGEMM_DWS(BIGEMM_F16) }
-    BIGEMM_DWS(BIGEMM_BF16)
-#undef BIGEMM_DWS
-#undef BIGEMM_DWK
-}
-
-
-
 }  // namespace bigemm
