@@ -338,6 +338,108 @@ __global__ void __launch_bounds__(256) pack_plane_kernel(const T *__restrict__ x
     }
 }
 
+// Subsampling over small planes (Hop * Wop <= kPlaneMax, input rows a whole
+// number of 8-byte words): output pixel (yo, xo) of an image takes input pixel
+// (s*yo, s*xo), zero past the image.  A data tile is the whole output plane of
+// one image for 128 bytes of channels: the threads read the input rows s*yo
+// as 8-byte words (the rows the conv skips are never read), keep the pixels
+// at multiples of s in shared memory as [channel][output pixel], and write
+// 16-byte channel runs per output pixel as the plane kernel does.  Tile index
+// flattened as (channel tile, image).
+template <typename T>
+__global__ void __launch_bounds__(256) pack_subplane_kernel(const T *__restrict__ x,
+                                                            T *__restrict__ xh, int C, int H,
+                                                            int W, int Hop, int Wop, int s,
+                                                            int Ch, int ctiles, int wblocks,
+                                                            FastDiv fd_wpr, FastDiv fd_rows,
+                                                            FastDiv fd_wop,
+                                                            const T *__restrict__ w,
+                                                            T *__restrict__ wp, int CO, int CI,
+                                                            int KHKW, int cip, float *z,
+                                                            long long zn, int zblocks)
+{
+    griddep_enter();
+    constexpr int E = sizeof(T);
+    constexpr int VEC = 16 / E;
+    constexpr int TC = 128 / E;
+    constexpr int KC = TC / VEC;
+    constexpr int G = 8 / E;             // elements per 8-byte word
+    // item indices are split with multiply-high divisions by the launch's fixed
+    // row length, row count and output width (runtime divisions dominated)
+    static_assert(TC * kPlaneMax * E >= kPackSmemBytes, "the buffer also serves the weights");
+    __shared__ __align__(16) T sp[TC * kPlaneMax];
+    if ((int)blockIdx.x < wblocks) {
+        pack_weight_part(w, wp, CO, CI, KHKW, cip, (int)blockIdx.x, wblocks, sp,
+                         (int)(kPackSmemBytes / E));
+        return;
+    }
+    if ((int)blockIdx.x >= (int)gridDim.x - zblocks) {
+        zero_part(z, zn, (int)blockIdx.x - ((int)gridDim.x - zblocks), zblocks);
+        return;
+    }
+    const int t = (int)blockIdx.x - wblocks;
+    const int ct = t % ctiles, n = t / ctiles;
+    const int c0 = ct * TC;
+    const int nc = min(TC, C - c0);
+    const int hwo = Hop * Wop;
+    const int wpr = W / G;                               // words per input row
+    // rows actually read: s*yo < H
+    const int rows = min(Hop, (H + s - 1) / s);
+    const long long hw = (long long)H * W;
+    const int items = (nc > 0 ? nc : 0) * rows * wpr;    // (channel, output row, word)
+    // eight words per thread in flight, then their pixels to shared memory
+    constexpr int UN = 8;
+    for (int i0 = threadIdx.x; i0 < items; i0 += UN * (int)blockDim.x) {
+        uint2 u[UN];
+#pragma unroll
+        for (int k = 0; k < UN; ++k) {
+            const int i = i0 + k * (int)blockDim.x;
+            if (i < items) {
+                uint32_t wd, yo;
+                const uint32_t r = fd_divmod((uint32_t)i, fd_wpr, &wd);
+                const uint32_t c = fd_divmod(r, fd_rows, &yo);
+                u[k] = __ldg(reinterpret_cast<const uint2 *>(
+                                 x + ((size_t)n * C + c0 + c) * hw + (size_t)(s * yo) * W) + wd);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < UN; ++k) {
+            const int i = i0 + k * (int)blockDim.x;
+            if (i < items) {
+                uint32_t wd, yo;
+                const uint32_t r = fd_divmod((uint32_t)i, fd_wpr, &wd);
+                const uint32_t c = fd_divmod(r, fd_rows, &yo);
+                const T *e = reinterpret_cast<const T *>(&u[k]);
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const int xi = (int)wd * G + g;
+                    if (xi % s == 0 && xi / s < Wop) sp[(int)c * hwo + (int)yo * Wop + xi / s] = e[g];
+                }
+            }
+        }
+    }
+    __syncthreads();
+    T *xd = xh + (size_t)n * hwo * Ch;
+    for (int q = threadIdx.x; q < hwo * KC; q += blockDim.x) {
+        const int pix = q / KC, k = q - pix * KC;
+        const int c = c0 + k * VEC;
+        if (c >= Ch) continue;
+        uint32_t xo;
+        const int yo = (int)fd_divmod((uint32_t)pix, fd_wop, &xo);
+        const bool inside = yo < rows && (int)xo * s < W;
+        union {
+            uint4 u;
+            T e[VEC];
+        } o;
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) {
+            const int ch = k * VEC + j;
+            o.e[j] = (inside && ch < nc) ? sp[ch * hwo + pix] : T(0);
+        }
+        *reinterpret_cast<uint4 *>(xd + (size_t)pix * Ch + c) = o.u;
+    }
+}
+
 // The general form: output pixel (yo, xo) of the [Hop][Wop] grid takes input
 // pixel (s*yo, s*xo), zero outside the image.  Element reads (any alignment,
 // any stride), 16-byte channel-row writes.
@@ -493,12 +595,17 @@ cudaError_t launch_pack_operands(const void *x, void *xh, int N, int C, int H, i
     const long long hwi = (long long)H * W, hwo = (long long)Hop * Wop;
     // pixel p of the output is pixel p of the input (or zero below it)
     const bool linear = s == 1 && Wop == W && Hop >= H;
+    // the subsampled copy of small planes, rows read as 8-byte words
+    const bool subplane = !linear && s > 1 && hwo <= kPlaneMax &&
+                          ((long long)W * dtype_size(dt)) % 8 == 0 &&
+                          (reinterpret_cast<uintptr_t>(x) & 7) == 0;
     const int kind = (linear && hwi <= kPlaneMax) ? 0                                  // plane
                      : (linear && aligned && hwi % vec == 0 && hwo % vec == 0) ? 1    // rows
-                                                                                : 2;  // remap
+                     : subplane ? 3                                                    // subsampled planes
+                                : 2;                                                   // remap
     const int tile = 8 * vec;                          // remap tiles: tile x tile
     const long long tc = 128 / (long long)dtype_size(dt);   // plane / rows tiles: 128 B of channels
-    const long long ptiles = kind == 0 ? 1 : kind == 1 ? (hwo + 127) / 128 : (hwo + tile - 1) / tile;
+    const long long ptiles = (kind == 0 || kind == 3) ? 1 : kind == 1 ? (hwo + 127) / 128 : (hwo + tile - 1) / tile;
     const long long ctiles = kind == 2 ? (Ch + tile - 1) / tile : (Ch + tc - 1) / tc;
     const long long data_blocks = ptiles * ctiles * N;
     // weight blocks: one per (output channel, channel run) item of pack_weight_part;
@@ -525,6 +632,22 @@ cudaError_t launch_pack_operands(const void *x, void *xh, int N, int C, int H, i
         return launch_pdl(pack_plane_kernel<uint16_t>, dim3(grid), dim3(256), 0, stream,
                           static_cast<const uint16_t *>(x), static_cast<uint16_t *>(xh), C,
                           (int)hwi, (int)hwo, Ch, (int)ctiles, (int)wblocks,
+                          static_cast<const uint16_t *>(w), static_cast<uint16_t *>(wp), CO, CI,
+                          KHKW, cip, zero, zero_elems, (int)zblocks);
+    }
+    if (kind == 3) {
+        const FastDiv fd_wpr = make_fastdiv((uint32_t)(W * dtype_size(dt) / 8));
+        const FastDiv fd_rows = make_fastdiv((uint32_t)std::min<long long>(Hop, (H + s - 1) / s));
+        const FastDiv fd_wop = make_fastdiv((uint32_t)Wop);
+        if (dtype_size(dt) == 4)
+            return launch_pdl(pack_subplane_kernel<uint32_t>, dim3(grid), dim3(256), 0, stream,
+                              static_cast<const uint32_t *>(x), static_cast<uint32_t *>(xh), C, H, W,
+                              Hop, Wop, s, Ch, (int)ctiles, (int)wblocks, fd_wpr, fd_rows, fd_wop,
+                              static_cast<const uint32_t *>(w), static_cast<uint32_t *>(wp), CO, CI,
+                              KHKW, cip, zero, zero_elems, (int)zblocks);
+        return launch_pdl(pack_subplane_kernel<uint16_t>, dim3(grid), dim3(256), 0, stream,
+                          static_cast<const uint16_t *>(x), static_cast<uint16_t *>(xh), C, H, W,
+                          Hop, Wop, s, Ch, (int)ctiles, (int)wblocks, fd_wpr, fd_rows, fd_wop,
                           static_cast<const uint16_t *>(w), static_cast<uint16_t *>(wp), CO, CI,
                           KHKW, cip, zero, zero_elems, (int)zblocks);
     }

@@ -368,6 +368,11 @@ SUB = [
     S("sub_s3_tf32", 2, 64, 64, 16, 17, 1, 3, 0, i="f32", o="f32"),
     S("sub_s2_bf16_bias", 2, 128, 96, 14, 14, 1, 2, 0, i="bf16", o="f32", epi="bias"),
     S("sub_s4_one_column", 1, 32, 64, 9, 1, 1, 4, 0),
+    # rows of whole 8-byte words: the subsampling whole-plane pack
+    S("sub_s2_tf32_words", 2, 48, 64, 20, 12, 1, 2, 0, i="f32", o="f32"),
+    S("sub_s3_f16_words", 2, 64, 64, 24, 24, 1, 3, 0),
+    S("sub_s2_bf16_ragged_ci100", 1, 100, 64, 32, 32, 1, 2, 0, i="bf16", o="bf16"),
+    S("sub_s2_f16_wide_16x40", 2, 64, 96, 16, 40, 1, 2, 0),
 ]
 
 
