@@ -56,6 +56,8 @@ struct UmmaTiling {
     int box_w, box_h; // output pixels per TMA box (A_NHWC); A_DIRECT: box_w = row pixels
     int bpt;          // boxes per 128-pixel tile
     int split;        // K slices
+    int epi16;        // A_NHWC / A_DIRECT, bn = 128: 16 epilogue warps (four per TMEM
+                      // lane quadrant, 576 threads) instead of 8
 };
 
 struct UmmaParams {
@@ -117,7 +119,7 @@ bool umma_tiling_compiled(const UmmaTiling &t, int in_dt);
 // k_blocks K blocks, written into p's layout fields; false when it does not fit.
 bool main_res_layout(int bn, int k_blocks, int smem_limit, UmmaParams &p);
 // Launch; the grid must be a multiple of p.co_tiles and p.split must be 1.
-cudaError_t launch_umma_res(int amode, int fmt, int bn, const UmmaParams &p,
+cudaError_t launch_umma_res(int amode, int fmt, int bn, bool epi16, const UmmaParams &p,
                             const CUtensorMap &map_a, const CUtensorMap &map_b,
                             const CUtensorMap &map_c, int grid, cudaStream_t stream);
 

@@ -44,11 +44,11 @@ std::string cand_str(const Cand &c)
 {
     char b[160];
     if (c.kind == BIGEMM_KIND_UMMA)
-        snprintf(b, sizeof b, "umma:%s:bn%d:box%dx%dx%d:split%d%s%s",
+        snprintf(b, sizeof b, "umma:%s:bn%d:box%dx%dx%d:split%d%s%s%s",
                  c.t.amode == A_DIRECT ? "direct" : c.t.amode == A_HALO ? "halo" : "nhwc", c.t.bn,
                  c.t.box_w, c.t.box_h, c.t.bpt, c.t.split,
                  c.t.pack == PACK_SUB ? ":sub" : c.t.pack == PACK_STACK ? ":stack" : "",
-                 c.t.bres ? ":bres" : "");
+                 c.t.bres ? ":bres" : "", c.t.epi16 ? ":e16" : "");
     else if (c.simt_variant == SV_DW)
         snprintf(b, sizeof b, "simt:depthwise:rows%d", c.dw_rows);
     else if (c.simt_variant == SV_DWS)
@@ -64,10 +64,11 @@ std::string cand_str(const Cand &c)
 bool parse_cand(const std::string &s, Cand &c)
 {
     int a, b, d, e, f, g;
-    char mode[16], layout[16] = "", layout2[16] = "";
-    const int got = sscanf(s.c_str(), "umma:%15[a-z]:bn%d:box%dx%dx%d:split%d:%15[a-z]:%15[a-z]",
-                           mode, &a, &b, &d, &e, &f, layout, layout2);
-    if (got >= 6 && got <= 8) {
+    char mode[16], layout[16] = "", layout2[16] = "", layout3[16] = "";
+    const int got = sscanf(s.c_str(),
+                           "umma:%15[a-z]:bn%d:box%dx%dx%d:split%d:%15[a-z0-9]:%15[a-z0-9]:%15[a-z0-9]",
+                           mode, &a, &b, &d, &e, &f, layout, layout2, layout3);
+    if (got >= 6 && got <= 9) {
         c = Cand{};
         c.kind = BIGEMM_KIND_UMMA;
         c.t.amode = strcmp(mode, "direct") == 0 ? A_DIRECT
@@ -76,6 +77,8 @@ bool parse_cand(const std::string &s, Cand &c)
         c.t.pack = strcmp(layout, "sub") == 0 ? PACK_SUB : strcmp(layout, "stack") == 0 ? PACK_STACK
                                                                                        : PACK_PLAIN;
         c.t.bres = strcmp(layout, "bres") == 0 || strcmp(layout2, "bres") == 0;
+        c.t.epi16 = strcmp(layout, "e16") == 0 || strcmp(layout2, "e16") == 0 ||
+                    strcmp(layout3, "e16") == 0;
         c.t.bn = a, c.t.box_w = b, c.t.box_h = d, c.t.bpt = e, c.t.split = f;
         return true;
     }
@@ -291,6 +294,8 @@ bool umma_valid(const ConvShape &s0, const UmmaTiling &t, int sm_count, std::str
         if (t.box_w * s.stride > 256 || t.box_h * s.stride > 256) return bad("box > 256");
     }
     if (t.bres && t.amode != A_HALO && t.split != 1) return bad("resident weights need split 1");
+    if (t.epi16 && (t.amode == A_HALO || t.bn != 128))
+        return bad("16 epilogue warps need the nhwc or direct mode and BN = 128");
     if (t.bpt > 16) return bad("more than 16 boxes per tile");
     if (umma_smem_bytes(t) == 0) return bad("no compiled kernel");
     if (!umma_geometry(s0, t, 1).fits) return bad("more than 2^31 boxes or work units");
@@ -446,6 +451,17 @@ void prefer_resident(const ConvShape &s, UmmaTiling &t)
     if (umma_valid(s, r, 1, nullptr)) t.bres = 1;
 }
 
+// Sixteen epilogue warps for 128-channel tiles over whole K ranges: the
+// epilogue, not the MMA, paces such tiles (measured on the 1x1 64->256 layer
+// at 56x56, N = 256: 110 -> 90 us).
+void prefer_epi16(const ConvShape &s, UmmaTiling &t)
+{
+    if (t.amode == A_HALO || t.bn != 128 || t.split != 1) return;
+    UmmaTiling r = t;
+    r.epi16 = 1;
+    if (umma_valid(s, r, 1, nullptr)) t.epi16 = 1;
+}
+
 // Halo tiles are worth it when they are mostly inside the output.
 bool halo_ok(const ConvShape &s)
 {
@@ -500,6 +516,7 @@ Cand heuristic(const ConvShape &s, int sms)
             prefer_resident(s, u.t);
         } else
             u.t = default_tiling(s, A_NHWC, default_bn(s), sms);
+        prefer_epi16(s, u.t);
         if (umma_valid(s, u.t, sms, nullptr)) return u;
     }
     c.simt_variant = SV_TILED;
@@ -599,6 +616,15 @@ std::vector<Cand> candidates(const ConvShape &s, int sms)
                     if ((amode == A_HALO && s.CO <= bn) || (amode != A_HALO && split == 1)) {
                         c.t.bres = 1;   // the resident-weights form too
                         if (umma_valid(s, c.t, sms, nullptr)) v.push_back(c);
+                    }
+                    if (amode != A_HALO && bn == 128) {
+                        // both forms again with 16 epilogue warps
+                        for (int br : {0, 1}) {
+                            if (br && split != 1) continue;
+                            Cand e = c;
+                            e.t.bres = br, e.t.epi16 = 1;
+                            if (umma_valid(s, e.t, sms, nullptr)) v.push_back(e);
+                        }
                     }
                 }
             }
@@ -1079,7 +1105,8 @@ bigemm_status plan_impl(int N, int H, int W, int CO, int CI, int KH, int KW, int
     cudaStream_t st = (cudaStream_t)stream;
 
     const bool forced = opts && (opts->kind || opts->tile_n || opts->split_k || opts->box_w ||
-                                 opts->box_h || opts->stages || opts->mode || opts->resident_b);
+                                 opts->box_h || opts->stages || opts->mode || opts->resident_b ||
+                                 opts->epi_warps);
     Cand c;
     std::string log, chosen = "heuristic";
     if (forced) {
@@ -1087,6 +1114,10 @@ bigemm_status plan_impl(int N, int H, int W, int CO, int CI, int KH, int KW, int
                                                !opts->box_w && !opts->box_h && !opts->stages &&
                                                !opts->mode && !opts->resident_b)) {
             c = heuristic(s, sms);
+            if (opts->epi_warps != 0 && opts->epi_warps != 8 && opts->epi_warps != 16)
+                return BIGEMM_ERR_INVALID_ARG;
+            if (c.kind == BIGEMM_KIND_UMMA && opts->epi_warps)
+                c.t.epi16 = opts->epi_warps == 16 ? 1 : 0;
             if (opts->kind == BIGEMM_KIND_SIMT && opts->mode != 0) {
                 // an explicit SIMT kernel: 1 tiled (groups = 1) or naive, 2 depthwise staged
                 // band (box_h rows per block), 3 depthwise streaming (box_h rows per thread),
@@ -1151,6 +1182,12 @@ bigemm_status plan_impl(int N, int H, int W, int CO, int CI, int KH, int KW, int
             } else if (opts->resident_b == 0) {
                 prefer_resident(s, c.t);
             }
+            if (opts->epi_warps != 0 && opts->epi_warps != 8 && opts->epi_warps != 16)
+                return BIGEMM_ERR_INVALID_ARG;
+            if (opts->epi_warps == 16)
+                c.t.epi16 = 1;
+            else if (opts->epi_warps == 0)
+                prefer_epi16(s, c.t);
         }
         std::string why;
         if (!cand_valid(s, c, sms, &why)) return BIGEMM_ERR_UNSUPPORTED;
@@ -1250,6 +1287,7 @@ bigemm_status conv2d_nchw_plan_describe(bigemm_plan plan, char *buf, size_t len)
            << "\", \"pack\": \""
            << (c.t.pack == PACK_SUB ? "sub" : c.t.pack == PACK_STACK ? "stack" : "plain")
            << "\", \"resident_b\": " << (c.t.bres ? "true" : "false")
+           << ", \"epi_warps\": " << (c.t.epi16 ? 16 : 8)
            << ", \"bn\": " << c.t.bn
            << ", \"box\": [" << c.t.box_w << ", " << c.t.box_h << ", " << c.t.bpt << "]"
            << ", \"split\": " << p.split << ", \"k_blocks\": " << p.k_blocks

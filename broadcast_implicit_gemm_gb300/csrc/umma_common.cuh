@@ -78,7 +78,8 @@ __device__ __forceinline__ void tmem_wait_ld_regs(uint32_t (&r)[32])
 
 // Epilogue of one warp (warps 2 .. 2 + NEPI - 1 of the block).  NEPI = 8: two
 // warps per TMEM lane quadrant, each taking every other 32-channel chunk of
-// the accumulator; NEPI = 4: one warp per quadrant takes every chunk.  MT = 2:
+// the accumulator; NEPI = 16: four per quadrant, each taking every fourth;
+// NEPI = 4: one warp per quadrant takes every chunk.  MT = 2:
 // a unit is two 128-pixel M tiles stacked vertically (box_h = 32 rows of a
 // halo tile), with accumulators at TMEM columns acc * 2BN and acc * 2BN + BN.
 // BOXED: the tile's pixels are 2-D boxes (box_w x box_h) of one image (or of
@@ -96,12 +97,13 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
                                               int box_px)
 {
     // The warp owns TMEM lanes 32q..32q+31 (32 pixels of the tile) and the
-    // chunks h, h+2, ... of the BN accumulator columns.  Lane 0 waits for the
-    // accumulator and shares the outcome, so the warp stays converged.  The
-    // load of the warp's next chunk is issued before the current one is
+    // chunks h, h + NEPI/4, ... of the BN accumulator columns.  Lane 0 waits
+    // for the accumulator and shares the outcome, so the warp stays converged.
+    // The load of the warp's next chunk is issued before the current one is
     // processed.  With TMA stores the warp stages its 32 pixels x 32 channels
-    // in its own 4 KB of shared memory and lane 0 writes them as one box.
-    static_assert(NEPI == 4 || NEPI == 8, "one or two warps per TMEM lane quadrant");
+    // in its own STG bytes of shared memory and lane 0 writes them as one box.
+    static_assert(NEPI == 4 || NEPI == 8 || NEPI == 16, "one, two or four warps per TMEM lane quadrant");
+    static_assert(BN / 32 >= NEPI / 4, "every warp of a quadrant takes at least one chunk");
     constexpr int kSplit = NEPI / 4;            // warps sharing a quadrant
     constexpr int kChunks = BN / 32;            // 2, 4 or 8
     constexpr int kMine = kChunks / kSplit;     // chunks per warp
@@ -115,6 +117,11 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
     const int wj0_y = wj0 / p.box_w, wj0_x = wj0 - wj0_y * p.box_w;
     const long long howo = (long long)p.Ho * p.Wo;
     const int ec = (p.ws || p.out_dt == BIGEMM_F32) ? 4 : 2;
+    // 4-pixel register stores need plain stores into the output (no workspace,
+    // no atomic adds), planes of a whole number of 4-element groups and an
+    // output base on a 4-element boundary
+    const bool vec_static = !p.store_tma && !p.ws && !p.red_add && howo % 4 == 0 &&
+                            (reinterpret_cast<uintptr_t>(p.out) & (uintptr_t)(4 * ec - 1)) == 0;
     uint8_t *wstage = stage_out + (warp - 2) * STG;
     constexpr int kNB = STG / 2048;             // 2 KB store buffers of the warp
     static_assert(kNB >= 1, "at least one 2 KB buffer per warp");
@@ -188,6 +195,28 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
         }
         const bool wstore = wbox && sn < p.N;
         if (p.ws) sn += w.sp * p.N;             // K slice w.sp's plane of the workspace
+        // Stores from registers (no TMA box fits the output rows): where every
+        // group of four lanes holds four consecutive pixels of one plane, at a
+        // 4-element boundary, or no valid pixel at all, the warp regroups each
+        // 32 x 32 block through its staging buffer and a lane writes 4-pixel
+        // runs of one channel (8 or 16 bytes) instead of single elements.
+        bool vec4 = false, gok = false;
+        long long gbase = 0;
+        if (vec_static) {
+            const long long lead = __shfl_sync(0xffffffffu, base, lane & ~3);
+            const bool mine = valid && base == lead + (lane & 3) && (lead & 3) == 0;
+            const unsigned okm = __ballot_sync(0xffffffffu, mine);
+            const unsigned vm = __ballot_sync(0xffffffffu, valid);
+            bool uniform = true;
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+                const unsigned no = (okm >> (4 * g)) & 0xFu, nv = (vm >> (4 * g)) & 0xFu;
+                uniform = uniform && (no == 0xFu || nv == 0u);
+            }
+            vec4 = uniform;
+            gbase = __shfl_sync(0xffffffffu, base, (lane & 7) * 4);
+            gok = ((okm >> ((lane & 7) * 4)) & 0xFu) == 0xFu;
+        }
         if (m == 0) {
             int okw = 0;
             if (lane == 0) okw = mbar_wait(&tfull[acc], acc_phase, p.timeout_ns, abort_flag, p.err);
@@ -272,6 +301,52 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
                             tma_store_3d(map_c, buf, sx, cc, sn);
                         }
                         bulk_commit();
+                    }
+                }
+            } else if (vec4) {
+                // the block of 32 pixels x 32 channels goes through the first
+                // 2 KB of the warp's staging as [channel][pixel] (16 channels at a
+                // time for fp32); lane l then takes pixel group l % 8 of channels
+                // l / 8, l / 8 + 4, ... and writes each as one 4-pixel run
+                const int g = lane & 7, c0 = lane >> 3;
+                if (ec == 4) {
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        __syncwarp();
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            *reinterpret_cast<float *>(wstage + j * 128 + lane * 4) = v[hh * 16 + j];
+                        __syncwarp();
+                        if (gok) {
+                            float *o = static_cast<float *>(p.out) + gbase + (long long)(cb + hh * 16) * howo;
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                const int c = c0 + 4 * k;
+                                if (cb + hh * 16 + c < p.CO)
+                                    *reinterpret_cast<float4 *>(o + c * howo) =
+                                        *reinterpret_cast<const float4 *>(wstage + c * 128 + g * 16);
+                            }
+                        }
+                    }
+                } else {
+                    const bool f16 = p.out_dt == BIGEMM_F16;
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 32; j += 2) {
+                        const uint32_t pk = pack2_16(v[j], v[j + 1], f16);
+                        *reinterpret_cast<uint16_t *>(wstage + j * 64 + lane * 2) = (uint16_t)(pk & 0xFFFFu);
+                        *reinterpret_cast<uint16_t *>(wstage + (j + 1) * 64 + lane * 2) = (uint16_t)(pk >> 16);
+                    }
+                    __syncwarp();
+                    if (gok) {
+                        uint16_t *o = static_cast<uint16_t *>(p.out) + gbase + (long long)cb * howo;
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            const int c = c0 + 4 * k;
+                            if (cb + c < p.CO)
+                                *reinterpret_cast<uint2 *>(o + c * howo) =
+                                    *reinterpret_cast<const uint2 *>(wstage + c * 64 + g * 8);
+                        }
                     }
                 }
             } else if (!p.store_tma && valid) {

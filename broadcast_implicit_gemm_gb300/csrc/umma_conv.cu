@@ -74,10 +74,11 @@ cudaError_t launch_umma_conv(const UmmaTiling &t, int in_dt, const UmmaParams &p
                    stream);
     const int fmt = fmt_of(in_dt);
     if (t.amode == A_HALO) return launch_halo_conv(t.bn, fmt, p, map_a, map_b, map_c, grid, stream);
-    if (t.bres) return launch_umma_res(t.amode, fmt, t.bn, p, map_a, map_b, map_c, grid, stream);
+    const bool e16 = t.epi16 != 0;
+    if (t.bres) return launch_umma_res(t.amode, fmt, t.bn, e16, p, map_a, map_b, map_c, grid, stream);
     if (t.amode == A_NHWC)
-        return dispatch_fmt<A_NHWC, false>(fmt, t.bn, p, map_a, map_b, map_c, grid, stream);
-    return dispatch_fmt<A_DIRECT, false>(fmt, t.bn, p, map_a, map_b, map_c, grid, stream);
+        return dispatch_fmt<A_NHWC, false>(fmt, t.bn, e16, p, map_a, map_b, map_c, grid, stream);
+    return dispatch_fmt<A_DIRECT, false>(fmt, t.bn, e16, p, map_a, map_b, map_c, grid, stream);
 }
 
 }  // namespace bigemm

@@ -16,8 +16,16 @@ constexpr int kResMaxA = 10;   // A stages at most with resident weights
 // advance by the grid), so the producer loads every K block of that tile's
 // weights once, into shared memory laid out by main_res_layout, and the ring
 // carries only the A boxes.
-template <int BN, int AMODE, int FMT, bool RB>
-__global__ void __launch_bounds__(kThreads, 1)
+// NEPI: epilogue warps, 8 (two per TMEM lane quadrant) or 16 (four, for
+// BN = 128): each warp then drains one 32-channel chunk per tile, and the
+// quadrant's stores and address arithmetic run in more warps at once.  The 16
+// warps stage 2 KB each, so the shared-memory layout is the same.  (At
+// BN = 256 the 576-thread block's register budget would spill.)
+template <int NEPI>
+constexpr int main_threads() { return 64 + 32 * NEPI; }
+
+template <int BN, int AMODE, int FMT, bool RB, int NEPI>
+__global__ void __launch_bounds__(main_threads<NEPI>(), 1)
     umma_conv_kernel(const __grid_constant__ CUtensorMap map_a,
                      const __grid_constant__ CUtensorMap map_b,
                      const __grid_constant__ CUtensorMap map_c, const UmmaParams p)
@@ -29,7 +37,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *sa = smem;
     uint8_t *sb = RB ? smem + p.halo_b_off : smem + S * kABytes;
-    uint8_t *stage_out = RB ? smem + p.halo_stage_off : sb + S * C::b_bytes;   // 8 warps x 4 KB
+    uint8_t *stage_out = RB ? smem + p.halo_stage_off : sb + S * C::b_bytes;   // 32 KB of staging
     uint64_t *full = reinterpret_cast<uint64_t *>(RB ? smem + p.halo_bar_off : stage_out + C::staging);
     uint64_t *empty = full + SMAX;
     uint64_t *tfull = empty + SMAX;
@@ -52,7 +60,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull[i], 1);
-            mbar_init(&tempty[i], kEpiWarps);
+            mbar_init(&tempty[i], NEPI);
         }
         mbar_init(drain, 1);
         mbar_init(b_full, 1);
@@ -232,8 +240,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // --------------------------------------------------------- epilogue
-        epilogue_warp<BN, AMODE != A_DIRECT>(p, &map_c, tmem_base, tfull, tempty, stage_out,
-                                             abort_flag, warp, lane, box_px);
+        static_assert(NEPI == kEpiWarps || (NEPI == 16 && BN == 128), "16 epilogue warps need BN = 128");
+        epilogue_warp<BN, AMODE != A_DIRECT, NEPI, 1, kEpiWarps * 4096 / NEPI>(
+            p, &map_c, tmem_base, tfull, tempty, stage_out, abort_flag, warp, lane, box_px);
     }
 
     tc_fence_before();
@@ -246,11 +255,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 
-template <int BN, int AMODE, int FMT, bool RB>
+template <int BN, int AMODE, int FMT, bool RB, int NEPI>
 cudaError_t launch_one(const UmmaParams &p, const CUtensorMap &ma, const CUtensorMap &mb,
                        const CUtensorMap &mc, int grid, cudaStream_t stream)
 {
-    auto kern = umma_conv_kernel<BN, AMODE, FMT, RB>;
+    auto kern = umma_conv_kernel<BN, AMODE, FMT, RB, NEPI>;
     static unsigned long long attr_set = 0;   // bit per device: smem opt-in done
     int dev = 0;
     cudaGetDevice(&dev);
@@ -262,29 +271,35 @@ cudaError_t launch_one(const UmmaParams &p, const CUtensorMap &ma, const CUtenso
         if (e != cudaSuccess) return e;
         if (dev < 64) attr_set |= 1ull << dev;
     }
-    return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, stream, ma, mb, mc, p);
+    return launch_pdl(kern, dim3(grid), dim3(main_threads<NEPI>()), smem, stream, ma, mb, mc, p);
 }
 
 template <int AMODE, int FMT, bool RB>
-cudaError_t dispatch_bn(int bn, const UmmaParams &p, const CUtensorMap &ma,
+cudaError_t dispatch_bn(int bn, bool epi16, const UmmaParams &p, const CUtensorMap &ma,
                         const CUtensorMap &mb, const CUtensorMap &mc, int grid, cudaStream_t s)
 {
     switch (bn) {
-    case 64: return launch_one<64, AMODE, FMT, RB>(p, ma, mb, mc, grid, s);
-    case 128: return launch_one<128, AMODE, FMT, RB>(p, ma, mb, mc, grid, s);
-    case 256: return launch_one<256, AMODE, FMT, RB>(p, ma, mb, mc, grid, s);
+    case 64:
+        if (epi16) return cudaErrorInvalidValue;
+        return launch_one<64, AMODE, FMT, RB, kEpiWarps>(p, ma, mb, mc, grid, s);
+    case 128:
+        if (epi16) return launch_one<128, AMODE, FMT, RB, 16>(p, ma, mb, mc, grid, s);
+        return launch_one<128, AMODE, FMT, RB, kEpiWarps>(p, ma, mb, mc, grid, s);
+    case 256:
+        if (epi16) return cudaErrorInvalidValue;
+        return launch_one<256, AMODE, FMT, RB, kEpiWarps>(p, ma, mb, mc, grid, s);
     default: return cudaErrorInvalidValue;
     }
 }
 
 template <int AMODE, bool RB>
-cudaError_t dispatch_fmt(int fmt, int bn, const UmmaParams &p, const CUtensorMap &ma,
+cudaError_t dispatch_fmt(int fmt, int bn, bool epi16, const UmmaParams &p, const CUtensorMap &ma,
                          const CUtensorMap &mb, const CUtensorMap &mc, int grid, cudaStream_t s)
 {
     switch (fmt) {
-    case 0: return dispatch_bn<AMODE, 0, RB>(bn, p, ma, mb, mc, grid, s);
-    case 1: return dispatch_bn<AMODE, 1, RB>(bn, p, ma, mb, mc, grid, s);
-    case 2: return dispatch_bn<AMODE, 2, RB>(bn, p, ma, mb, mc, grid, s);
+    case 0: return dispatch_bn<AMODE, 0, RB>(bn, epi16, p, ma, mb, mc, grid, s);
+    case 1: return dispatch_bn<AMODE, 1, RB>(bn, epi16, p, ma, mb, mc, grid, s);
+    case 2: return dispatch_bn<AMODE, 2, RB>(bn, epi16, p, ma, mb, mc, grid, s);
     default: return cudaErrorInvalidValue;
     }
 }

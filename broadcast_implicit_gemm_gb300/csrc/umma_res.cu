@@ -28,13 +28,15 @@ bool main_res_layout(int bn, int k_blocks, int smem_limit, UmmaParams &p)
     return true;
 }
 
-cudaError_t launch_umma_res(int amode, int fmt, int bn, const UmmaParams &p,
+cudaError_t launch_umma_res(int amode, int fmt, int bn, bool epi16, const UmmaParams &p,
                             const CUtensorMap &map_a, const CUtensorMap &map_b,
                             const CUtensorMap &map_c, int grid, cudaStream_t stream)
 {
     if (p.split != 1 || grid % p.co_tiles != 0 || p.res_b_bytes <= 0) return cudaErrorInvalidValue;
-    if (amode == A_NHWC) return dispatch_fmt<A_NHWC, true>(fmt, bn, p, map_a, map_b, map_c, grid, stream);
-    if (amode == A_DIRECT) return dispatch_fmt<A_DIRECT, true>(fmt, bn, p, map_a, map_b, map_c, grid, stream);
+    if (amode == A_NHWC)
+        return dispatch_fmt<A_NHWC, true>(fmt, bn, epi16, p, map_a, map_b, map_c, grid, stream);
+    if (amode == A_DIRECT)
+        return dispatch_fmt<A_DIRECT, true>(fmt, bn, epi16, p, map_a, map_b, map_c, grid, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -116,6 +116,10 @@ typedef struct {
                        every tap must fit; other modes: split_k 1, and every K
                        block of one output-channel tile must fit (each block
                        keeps one tile) -- -1 streams them, 0 chooses            */
+    int epi_warps;  /* UMMA modes 1, 2 and 4 with tile_n = 128: 16 runs four
+                       epilogue warps per TMEM lane quadrant (576 threads per
+                       block) instead of two (8); 0 chooses; other values:
+                       INVALID_ARG                                              */
 } bigemm_plan_options;
 
 /*

@@ -552,6 +552,106 @@ def test_misaligned_pointer_rejected():
     plan.close()
 
 
+# ------------------------------------------------- 16 epilogue warps
+# 128-channel tiles drained by four warps per TMEM lane quadrant (one 32-channel
+# chunk each, 2 KB of staging each) instead of two.
+EPI16 = [
+    (S("e16_direct_64_256", 2, 64, 256, 28, 28, 1, 1, 0), bg.MODE_DIRECT, 0, 1),
+    (S("e16_direct_ragged_co200_bias_f32", 1, 128, 200, 16, 16, 1, 1, 0, o="f32", epi="bias"),
+     bg.MODE_DIRECT, 0, 1),
+    (S("e16_nhwc_k3_exp_f32", 1, 64, 136, 13, 11, 3, 1, 1, o="f32", epi="bias_exp"), bg.MODE_NHWC, 0, 1),
+    # non-negative data and kernel keep every rsqrt argument well above zero
+    (S("e16_nhwc_tf32_rsqrt", 1, 96, 128, 9, 12, 3, 1, 1, i="f32", o="f32", epi="bias_rsqrt",
+       dd="absnormal", kd="absnormal"), bg.MODE_NHWC, -1, 1),
+    (S("e16_sub_s2_bf16", 2, 256, 256, 28, 28, 1, 2, 0, i="bf16", o="bf16"), bg.MODE_SUB, 1, 1),
+    (S("e16_nhwc_split_add_f32", 1, 256, 128, 14, 14, 3, 1, 1, i="f32", o="f32"), bg.MODE_NHWC, -1, 4),
+    (S("e16_nhwc_split_reduce_f16", 1, 256, 128, 12, 12, 3, 1, 1), bg.MODE_NHWC, -1, 2),
+]
+
+
+@pytest.mark.parametrize("resident", [0, 1])
+@pytest.mark.parametrize("case", EPI16, ids=lambda c: c[0].name)
+def test_sixteen_epilogue_warps(case, resident):
+    spec, mode, res, split = case
+    if res == -1 and resident:
+        pytest.skip("split K, or weights too large to stay resident")
+    opts = {"kind": bg.KIND_UMMA, "mode": mode, "tile_n": 128, "split_k": split, "epi_warps": 16,
+            "resident_b": 1 if resident else -1}
+    info = check(spec, opts)
+    assert info["epi_warps"] == 16 and info["bn"] == 128 and info["resident_b"] == bool(resident)
+
+
+def test_eight_epilogue_warps_on_request():
+    spec = S("e8_direct_64_256", 1, 64, 256, 28, 28, 1, 1, 0)
+    info = check(spec, {"kind": bg.KIND_UMMA, "mode": bg.MODE_DIRECT, "tile_n": 128, "epi_warps": 8})
+    assert info["epi_warps"] == 8
+
+
+@pytest.mark.parametrize("opts,status", [
+    ({"kind": 1, "mode": bg.MODE_DIRECT, "tile_n": 64, "epi_warps": 16}, 2),
+    ({"kind": 1, "mode": bg.MODE_DIRECT, "tile_n": 256, "epi_warps": 16}, 2),
+    ({"kind": 1, "mode": bg.MODE_HALO, "tile_n": 128, "epi_warps": 16}, 2),
+    ({"kind": 1, "mode": bg.MODE_DIRECT, "tile_n": 128, "epi_warps": 12}, 1),
+])
+def test_sixteen_epilogue_warps_rejected(opts, status):
+    k = 3 if opts["mode"] == bg.MODE_HALO else 1
+    with pytest.raises(bg.BigemmError) as e:
+        bg.conv2d_nchw_plan_ex(1, 16, 16, 256, 64, k, k, 1, k // 2, 1, bg.F16, bg.F16, bg.EPI_NONE, 0,
+                               opts)
+    assert e.value.status == status
+
+
+# ------------------------------------------------- stores from registers
+# Outputs whose rows no TMA box can address (Wo x element size not a multiple
+# of 16 bytes) leave the epilogue from registers: as 4-pixel runs where each
+# group of four lanes holds four consecutive pixels of a plane at a 4-element
+# boundary (or none at all), as single elements otherwise.
+REG_STORE = [
+    (S("rs_sub_14_f16_bn128", 2, 256, 256, 28, 28, 1, 2, 0), bg.MODE_SUB, 128),
+    (S("rs_nhwc_14_f16_ragged_co", 2, 96, 136, 14, 14, 1, 1, 0), bg.MODE_NHWC, 64),
+    (S("rs_nhwc_14_bf16_bn256", 1, 64, 256, 14, 14, 1, 1, 0, i="bf16", o="bf16"), bg.MODE_NHWC, 256),
+    (S("rs_halo_28_bf16", 1, 64, 72, 28, 28, 3, 1, 1, i="bf16", o="bf16"), bg.MODE_HALO, 64),
+    (S("rs_nhwc_14_f32_bias", 1, 64, 80, 14, 14, 3, 1, 1, i="f32", o="f32", epi="bias"), bg.MODE_NHWC, 64),
+    (S("rs_halo_10x6_f32_exp", 2, 32, 48, 10, 6, 3, 1, 1, o="f32", epi="bias_exp"), bg.MODE_HALO, 64),
+    (S("rs_halo_7_f16_elements", 2, 64, 64, 7, 7, 3, 1, 1), bg.MODE_HALO, 64),
+    (S("rs_nhwc_9x5_f16_elements", 1, 32, 40, 9, 5, 3, 1, 1), bg.MODE_NHWC, 64),
+]
+
+
+@pytest.mark.parametrize("case", REG_STORE, ids=lambda c: c[0].name)
+def test_register_stores(case):
+    spec, mode, bn = case
+    info = check(spec, {"kind": bg.KIND_UMMA, "mode": mode, "tile_n": bn, "split_k": 1})
+    assert info["store"] == "direct" and info["split"] == 1
+
+
+@pytest.mark.parametrize("spec", [S("rs_forced_direct_56", 1, 64, 64, 56, 56, 1, 1, 0),
+                                  S("rs_forced_halo_16", 2, 64, 96, 16, 16, 3, 1, 1, o="f32")],
+                         ids=lambda s: s.name)
+def test_register_stores_forced(spec, monkeypatch):
+    # rows TMA could store, written from registers instead
+    monkeypatch.setenv("BIGEMM_NO_TMA_STORE", "1")
+    info = check(spec, {"kind": bg.KIND_UMMA, "split_k": 1})
+    assert info["store"] == "direct"
+
+
+def test_misaligned_output_rejected():
+    # outputs must start on a 16-byte boundary: one 2 bytes past it is refused
+    # before any launch, and nothing is written
+    plan = bg.conv2d_nchw_plan_ex(1, 14, 14, 72, 64, 1, 1, 1, 0, 1, bg.F16, bg.F16, bg.EPI_NONE, 0,
+                                  {"kind": bg.KIND_UMMA, "mode": bg.MODE_NHWC, "split_k": 1})
+    x = torch.zeros((1, 64, 14, 14), dtype=torch.float16, device="cuda")
+    w = torch.zeros((72, 64, 1, 1), dtype=torch.float16, device="cuda")
+    n = 72 * 14 * 14
+    buf = torch.full((n + 1,), SENTINEL, dtype=torch.float16, device="cuda")
+    with pytest.raises(bg.BigemmError) as e:
+        bg.conv2d_nchw_run(plan, x, w, None, 0.0, buf[1:].view(1, 72, 14, 14))
+    assert e.value.status == 1
+    torch.cuda.synchronize()
+    assert bool(torch.all(buf.float().cpu() == SENTINEL))
+    plan.close()
+
+
 def test_missing_bias_rejected():
     plan = bg.conv2d_nchw_plan(1, 8, 8, 64, 64, 3, 3, 1, 1, 1, bg.F16, bg.F32, bg.EPI_BIAS_EXP, 0)
     x = torch.zeros((1, 64, 8, 8), dtype=torch.float16, device="cuda")
