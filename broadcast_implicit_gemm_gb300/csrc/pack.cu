@@ -343,16 +343,19 @@ __global__ void __launch_bounds__(256) pack_plane_kernel(const T *__restrict__ x
 // (s*yo, s*xo), zero past the image.  A data tile is the whole output plane of
 // one image for 128 bytes of channels: the threads read the input rows s*yo
 // as 8-byte words (the rows the conv skips are never read), keep the pixels
-// at multiples of s in shared memory as [channel][output pixel], and write
-// 16-byte channel runs per output pixel as the plane kernel does.  Tile index
-// flattened as (channel tile, image).
+// at multiples of s in shared memory as [channel][output pixel] with an odd
+// row pitch (so that the gather below reads eight channel rows from eight
+// bank groups), and write 16-byte channel runs per output pixel as the plane
+// kernel does.  Each word finds its first output column with one
+// multiply-high division (a per-element remainder test had made the kernel
+// ALU-bound).  Tile index flattened as (channel tile, image).
 template <typename T>
 __global__ void __launch_bounds__(256) pack_subplane_kernel(const T *__restrict__ x,
                                                             T *__restrict__ xh, int C, int H,
                                                             int W, int Hop, int Wop, int s,
                                                             int Ch, int ctiles, int wblocks,
                                                             FastDiv fd_wpr, FastDiv fd_rows,
-                                                            FastDiv fd_wop,
+                                                            FastDiv fd_wop, FastDiv fd_s,
                                                             const T *__restrict__ w,
                                                             T *__restrict__ wp, int CO, int CI,
                                                             int KHKW, int cip, float *z,
@@ -382,38 +385,58 @@ __global__ void __launch_bounds__(256) pack_subplane_kernel(const T *__restrict_
     const int c0 = ct * TC;
     const int nc = min(TC, C - c0);
     const int hwo = Hop * Wop;
+    const int pitch = ((hwo | 1) <= kPlaneMax) ? (hwo | 1) : hwo;   // shared row pitch
     const int wpr = W / G;                               // words per input row
     // rows actually read: s*yo < H
     const int rows = min(Hop, (H + s - 1) / s);
     const long long hw = (long long)H * W;
     const int items = (nc > 0 ? nc : 0) * rows * wpr;    // (channel, output row, word)
-    // eight words per thread in flight, then their pixels to shared memory
+    // eight words per thread in flight, then their pixels to shared memory; the
+    // first pass keeps each word's shared-memory row offset and first column
     constexpr int UN = 8;
     for (int i0 = threadIdx.x; i0 < items; i0 += UN * (int)blockDim.x) {
         uint2 u[UN];
+        int off[UN], x0s[UN];
 #pragma unroll
         for (int k = 0; k < UN; ++k) {
             const int i = i0 + k * (int)blockDim.x;
+            off[k] = -1;
+            x0s[k] = 0;
             if (i < items) {
                 uint32_t wd, yo;
                 const uint32_t r = fd_divmod((uint32_t)i, fd_wpr, &wd);
                 const uint32_t c = fd_divmod(r, fd_rows, &yo);
                 u[k] = __ldg(reinterpret_cast<const uint2 *>(
                                  x + ((size_t)n * C + c0 + c) * hw + (size_t)(s * yo) * W) + wd);
+                off[k] = (int)c * pitch + (int)yo * Wop;
+                x0s[k] = (int)wd * G;
             }
         }
 #pragma unroll
         for (int k = 0; k < UN; ++k) {
-            const int i = i0 + k * (int)blockDim.x;
-            if (i < items) {
-                uint32_t wd, yo;
-                const uint32_t r = fd_divmod((uint32_t)i, fd_wpr, &wd);
-                const uint32_t c = fd_divmod(r, fd_rows, &yo);
-                const T *e = reinterpret_cast<const T *>(&u[k]);
+            if (off[k] < 0) continue;
+            const T *e = reinterpret_cast<const T *>(&u[k]);
+            T *dst = sp + off[k];
+            const int x0 = x0s[k];
+            if (s == 2) {
+                // a word starts at an even column: its even pixels are outputs x0/2, x0/2 + 1, ...
+                const int xo0 = x0 >> 1;
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const int xi = (int)wd * G + g;
-                    if (xi % s == 0 && xi / s < Wop) sp[(int)c * hwo + (int)yo * Wop + xi / s] = e[g];
+                for (int j = 0; j < G / 2; ++j)
+                    if (xo0 + j < Wop) dst[xo0 + j] = e[2 * j];
+            } else {
+                // output columns xo0, xo0 + 1, ... read pixels (xo0 + j) * s of this word
+                const int xo0 = (int)fd_div((uint32_t)(x0 + s - 1), fd_s);
+#pragma unroll
+                for (int j = 0; j < G; ++j) {
+                    const int d = (xo0 + j) * s - x0;
+                    if (d < G && xo0 + j < Wop) {
+                        T val = e[0];
+#pragma unroll
+                        for (int g = 1; g < G; ++g)
+                            if (d == g) val = e[g];
+                        dst[xo0 + j] = val;
+                    }
                 }
             }
         }
@@ -434,7 +457,7 @@ __global__ void __launch_bounds__(256) pack_subplane_kernel(const T *__restrict_
 #pragma unroll
         for (int j = 0; j < VEC; ++j) {
             const int ch = k * VEC + j;
-            o.e[j] = (inside && ch < nc) ? sp[ch * hwo + pix] : T(0);
+            o.e[j] = (inside && ch < nc) ? sp[ch * pitch + pix] : T(0);
         }
         *reinterpret_cast<uint4 *>(xd + (size_t)pix * Ch + c) = o.u;
     }
@@ -639,15 +662,16 @@ cudaError_t launch_pack_operands(const void *x, void *xh, int N, int C, int H, i
         const FastDiv fd_wpr = make_fastdiv((uint32_t)(W * dtype_size(dt) / 8));
         const FastDiv fd_rows = make_fastdiv((uint32_t)std::min<long long>(Hop, (H + s - 1) / s));
         const FastDiv fd_wop = make_fastdiv((uint32_t)Wop);
+        const FastDiv fd_s = make_fastdiv((uint32_t)s);
         if (dtype_size(dt) == 4)
             return launch_pdl(pack_subplane_kernel<uint32_t>, dim3(grid), dim3(256), 0, stream,
                               static_cast<const uint32_t *>(x), static_cast<uint32_t *>(xh), C, H, W,
-                              Hop, Wop, s, Ch, (int)ctiles, (int)wblocks, fd_wpr, fd_rows, fd_wop,
+                              Hop, Wop, s, Ch, (int)ctiles, (int)wblocks, fd_wpr, fd_rows, fd_wop, fd_s,
                               static_cast<const uint32_t *>(w), static_cast<uint32_t *>(wp), CO, CI,
                               KHKW, cip, zero, zero_elems, (int)zblocks);
         return launch_pdl(pack_subplane_kernel<uint16_t>, dim3(grid), dim3(256), 0, stream,
                           static_cast<const uint16_t *>(x), static_cast<uint16_t *>(xh), C, H, W,
-                          Hop, Wop, s, Ch, (int)ctiles, (int)wblocks, fd_wpr, fd_rows, fd_wop,
+                          Hop, Wop, s, Ch, (int)ctiles, (int)wblocks, fd_wpr, fd_rows, fd_wop, fd_s,
                           static_cast<const uint16_t *>(w), static_cast<uint16_t *>(wp), CO, CI,
                           KHKW, cip, zero, zero_elems, (int)zblocks);
     }
