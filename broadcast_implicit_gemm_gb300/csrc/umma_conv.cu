@@ -75,6 +75,20 @@ cudaError_t launch_umma_conv(const UmmaTiling &t, int in_dt, const UmmaParams &p
     const int fmt = fmt_of(in_dt);
     if (t.amode == A_HALO) return launch_halo_conv(t.bn, fmt, p, map_a, map_b, map_c, grid, stream);
     const bool e16 = t.epi16 != 0;
+    // a 16-bit output written in place with no epilogue op takes the kernel
+    // whose epilogue carries only that path
+    const bool plain = fmt != 2 && !p.ws && !p.red_add && p.epi == BIGEMM_EPI_NONE &&
+                       p.out_dt != BIGEMM_F32;
+    if (plain && t.amode != A_HALO) {
+        // the checks launch_umma_res makes for resident weights
+        if (t.bres && (p.split != 1 || grid % p.co_tiles != 0 || p.res_b_bytes <= 0))
+            return cudaErrorInvalidValue;
+        if (p.store_tma)
+            return launch_umma_plain_tma(t.amode, t.bres != 0, fmt, t.bn, e16, p, map_a, map_b,
+                                         map_c, grid, stream);
+        return launch_umma_plain_reg(t.amode, t.bres != 0, fmt, t.bn, e16, p, map_a, map_b, map_c,
+                                     grid, stream);
+    }
     if (t.bres) return launch_umma_res(t.amode, fmt, t.bn, e16, p, map_a, map_b, map_c, grid, stream);
     if (t.amode == A_NHWC)
         return dispatch_fmt<A_NHWC, false>(fmt, t.bn, e16, p, map_a, map_b, map_c, grid, stream);

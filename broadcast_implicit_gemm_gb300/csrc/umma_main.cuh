@@ -24,7 +24,8 @@ constexpr int kResMaxA = 10;   // A stages at most with resident weights
 template <int NEPI>
 constexpr int main_threads() { return 64 + 32 * NEPI; }
 
-template <int BN, int AMODE, int FMT, bool RB, int NEPI>
+// FORM: the epilogue's output form (epilogue_warp).
+template <int BN, int AMODE, int FMT, bool RB, int NEPI, int FORM>
 __global__ void __launch_bounds__(main_threads<NEPI>(), 1)
     umma_conv_kernel(const __grid_constant__ CUtensorMap map_a,
                      const __grid_constant__ CUtensorMap map_b,
@@ -241,7 +242,7 @@ __global__ void __launch_bounds__(main_threads<NEPI>(), 1)
     } else {
         // --------------------------------------------------------- epilogue
         static_assert(NEPI == kEpiWarps || (NEPI == 16 && BN == 128), "16 epilogue warps need BN = 128");
-        epilogue_warp<BN, AMODE != A_DIRECT, NEPI, 1, kEpiWarps * 4096 / NEPI>(
+        epilogue_warp<BN, AMODE != A_DIRECT, NEPI, 1, kEpiWarps * 4096 / NEPI, FORM>(
             p, &map_c, tmem_base, tfull, tempty, stage_out, abort_flag, warp, lane, box_px);
     }
 
@@ -255,11 +256,11 @@ __global__ void __launch_bounds__(main_threads<NEPI>(), 1)
 }
 
 
-template <int BN, int AMODE, int FMT, bool RB, int NEPI>
+template <int BN, int AMODE, int FMT, bool RB, int NEPI, int FORM>
 cudaError_t launch_one(const UmmaParams &p, const CUtensorMap &ma, const CUtensorMap &mb,
                        const CUtensorMap &mc, int grid, cudaStream_t stream)
 {
-    auto kern = umma_conv_kernel<BN, AMODE, FMT, RB, NEPI>;
+    auto kern = umma_conv_kernel<BN, AMODE, FMT, RB, NEPI, FORM>;
     static unsigned long long attr_set = 0;   // bit per device: smem opt-in done
     int dev = 0;
     cudaGetDevice(&dev);
@@ -274,32 +275,36 @@ cudaError_t launch_one(const UmmaParams &p, const CUtensorMap &ma, const CUtenso
     return launch_pdl(kern, dim3(grid), dim3(main_threads<NEPI>()), smem, stream, ma, mb, mc, p);
 }
 
-template <int AMODE, int FMT, bool RB>
+template <int AMODE, int FMT, bool RB, int FORM>
 cudaError_t dispatch_bn(int bn, bool epi16, const UmmaParams &p, const CUtensorMap &ma,
                         const CUtensorMap &mb, const CUtensorMap &mc, int grid, cudaStream_t s)
 {
     switch (bn) {
     case 64:
         if (epi16) return cudaErrorInvalidValue;
-        return launch_one<64, AMODE, FMT, RB, kEpiWarps>(p, ma, mb, mc, grid, s);
+        return launch_one<64, AMODE, FMT, RB, kEpiWarps, FORM>(p, ma, mb, mc, grid, s);
     case 128:
-        if (epi16) return launch_one<128, AMODE, FMT, RB, 16>(p, ma, mb, mc, grid, s);
-        return launch_one<128, AMODE, FMT, RB, kEpiWarps>(p, ma, mb, mc, grid, s);
+        if (epi16) return launch_one<128, AMODE, FMT, RB, 16, FORM>(p, ma, mb, mc, grid, s);
+        return launch_one<128, AMODE, FMT, RB, kEpiWarps, FORM>(p, ma, mb, mc, grid, s);
     case 256:
         if (epi16) return cudaErrorInvalidValue;
-        return launch_one<256, AMODE, FMT, RB, kEpiWarps>(p, ma, mb, mc, grid, s);
+        return launch_one<256, AMODE, FMT, RB, kEpiWarps, FORM>(p, ma, mb, mc, grid, s);
     default: return cudaErrorInvalidValue;
     }
 }
 
-template <int AMODE, bool RB>
+// FORM 0 for every operand format; the 16-bit plain forms (1, 2) only where
+// the launching translation unit asks for them (umma_plain.cu).
+template <int AMODE, bool RB, int FORM = 0>
 cudaError_t dispatch_fmt(int fmt, int bn, bool epi16, const UmmaParams &p, const CUtensorMap &ma,
                          const CUtensorMap &mb, const CUtensorMap &mc, int grid, cudaStream_t s)
 {
     switch (fmt) {
-    case 0: return dispatch_bn<AMODE, 0, RB>(bn, epi16, p, ma, mb, mc, grid, s);
-    case 1: return dispatch_bn<AMODE, 1, RB>(bn, epi16, p, ma, mb, mc, grid, s);
-    case 2: return dispatch_bn<AMODE, 2, RB>(bn, epi16, p, ma, mb, mc, grid, s);
+    case 0: return dispatch_bn<AMODE, 0, RB, FORM>(bn, epi16, p, ma, mb, mc, grid, s);
+    case 1: return dispatch_bn<AMODE, 1, RB, FORM>(bn, epi16, p, ma, mb, mc, grid, s);
+    case 2:
+        if (FORM != 0) return cudaErrorInvalidValue;
+        return dispatch_bn<AMODE, 2, RB, 0>(bn, epi16, p, ma, mb, mc, grid, s);
     default: return cudaErrorInvalidValue;
     }
 }
