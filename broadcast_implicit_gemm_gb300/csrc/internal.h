@@ -119,6 +119,18 @@ bool umma_tiling_compiled(const UmmaTiling &t, int in_dt);
 // k_blocks K blocks, written into p's layout fields; false when it does not fit.
 bool main_res_layout(int bn, int k_blocks, int smem_limit, UmmaParams &p);
 // Launch; the grid must be a multiple of p.co_tiles and p.split must be 1.
+// The halo kernel narrowed to an output form (16-bit operands): 16-bit output
+// with no epilogue op by TMA stores or from registers, fp32 output by TMA
+// stores (halo_forms_*.cu).
+cudaError_t launch_halo_plain_tma(int bn, int fmt, const UmmaParams &p, const CUtensorMap &map_a,
+                                  const CUtensorMap &map_b, const CUtensorMap &map_c, int grid,
+                                  cudaStream_t stream);
+cudaError_t launch_halo_plain_reg(int bn, int fmt, const UmmaParams &p, const CUtensorMap &map_a,
+                                  const CUtensorMap &map_b, const CUtensorMap &map_c, int grid,
+                                  cudaStream_t stream);
+cudaError_t launch_halo_f32_tma(int bn, int fmt, const UmmaParams &p, const CUtensorMap &map_a,
+                                const CUtensorMap &map_b, const CUtensorMap &map_c, int grid,
+                                cudaStream_t stream);
 // The per-tap and direct kernels narrowed to a 16-bit output with no epilogue
 // op, written in place by TMA stores (umma_plain_tma.cu) or from registers
 // (umma_plain_reg.cu); 16-bit operand formats only.

@@ -92,7 +92,8 @@ __device__ __forceinline__ void tmem_wait_ld_regs(uint32_t (&r)[32])
 // FORM narrows what the launch's tiles can need, so that the kernel carries
 // only that code: 0 any output (every case decided at run time); 1 a 16-bit
 // output written in place by TMA stores, with no epilogue op; 2 the same
-// written from registers.  (Measured on the 1x1 ResNet-50 layers: the general
+// written from registers; 3 an fp32 output written in place by TMA stores,
+// the epilogue op chosen at run time.  (Measured on the 1x1 ResNet-50 layers: the general
 // form's unused paths cost a third of the epilogue's time per tile.)
 template <int BN, bool BOXED, int NEPI = kEpiWarps, int MT = 1, int STG = 4096, int FORM = 0>
 __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtensorMap *map_c,
@@ -121,14 +122,16 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
     const int bj_y = bj / p.box_w, bj_x = bj - bj_y * p.box_w;
     const int wj0_y = wj0 / p.box_w, wj0_x = wj0 - wj0_y * p.box_w;
     const long long howo = (long long)p.Ho * p.Wo;
-    static_assert(FORM >= 0 && FORM <= 2, "output form");
-    constexpr bool kPlain = FORM != 0;          // 16-bit, in place, no epilogue op
-    const int ec = kPlain ? 2 : ((p.ws || p.out_dt == BIGEMM_F32) ? 4 : 2);
-    const bool tma_out = FORM == 1 ? true : FORM == 2 ? false : p.store_tma != 0;
+    static_assert(FORM >= 0 && FORM <= 3, "output form");
+    constexpr bool kPlain = FORM == 1 || FORM == 2;   // 16-bit, in place, no epilogue op
+    constexpr bool kInPlace = FORM != 0;              // no workspace, no atomic adds
+    const int ec = FORM == 3 ? 4 : kPlain ? 2 : ((p.ws || p.out_dt == BIGEMM_F32) ? 4 : 2);
+    const bool tma_out = (FORM == 1 || FORM == 3) ? true : FORM == 2 ? false : p.store_tma != 0;
     // 4-pixel register stores need plain stores into the output (no workspace,
     // no atomic adds), planes of a whole number of 4-element groups and an
     // output base on a 4-element boundary
-    const bool vec_static = FORM != 1 && !tma_out && (kPlain || (!p.ws && !p.red_add)) && howo % 4 == 0 &&
+    const bool vec_static = (FORM == 0 || FORM == 2) && !tma_out && (kInPlace || (!p.ws && !p.red_add)) &&
+                            howo % 4 == 0 &&
                             (reinterpret_cast<uintptr_t>(p.out) & (uintptr_t)(4 * ec - 1)) == 0;
     uint8_t *wstage = stage_out + (warp - 2) * STG;
     constexpr int kNB = STG / 2048;             // 2 KB store buffers of the warp
@@ -145,7 +148,8 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
         // of the warp's chunks now, before the accumulator is ready; the chunk
         // loop hands the values round with shuffles (a per-chunk load of all 32
         // biases cost a DRAM round trip per chunk after a cold start).
-        const bool use_bias = !kPlain && !p.ws && p.epi != BIGEMM_EPI_NONE && !(p.red_add && w.sp != 0);
+        const bool use_bias = !kPlain && (kInPlace || !p.ws) && p.epi != BIGEMM_EPI_NONE &&
+                              !(!kInPlace && p.red_add && w.sp != 0);
         float bl[kMine];
 #pragma unroll
         for (int i = 0; i < kMine; ++i) {
@@ -178,7 +182,7 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
                 pix = (long long)rem * p.box_w + bj;
                 valid = pix < howo;
             }
-            base = ((!kPlain && p.ws) ? (long long)w.sp * p.out_elems : 0ll) + (long long)n * p.CO * howo + pix;
+            base = ((!kInPlace && p.ws) ? (long long)w.sp * p.out_elems : 0ll) + (long long)n * p.CO * howo + pix;
         }
         // the warp's store box (TMA mode): origin and image index
         const int wb = w.pt * p.bpt + wbi;
@@ -202,7 +206,7 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
             sn = n;
         }
         const bool wstore = wbox && sn < p.N;
-        if (!kPlain && p.ws) sn += w.sp * p.N;  // K slice w.sp's plane of the workspace
+        if (!kInPlace && p.ws) sn += w.sp * p.N;   // K slice w.sp's plane of the workspace
         // Stores from registers (no TMA box fits the output rows): where every
         // group of four lanes holds four consecutive pixels of one plane, at a
         // 4-element boundary, or no valid pixel at all, the warp regroups each
@@ -298,7 +302,7 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
                     __syncwarp();
                     if (lane == 0) {
                         const int cc = cb + hh * 16;
-                        if (!kPlain && p.red_add) {
+                        if (!kInPlace && p.red_add) {
                             if (BOXED)
                                 tma_reduce_add_4d(map_c, buf, sx, sy, cc, sn);
                             else
@@ -357,15 +361,15 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
                         }
                     }
                 }
-            } else if (FORM != 1 && !tma_out && valid) {
+            } else if ((FORM == 0 || FORM == 2) && !tma_out && valid) {
                 const long long o0 = base + (long long)cb * howo;
                 const int jn = min(32, p.CO - cb);
-                if (!kPlain && p.ws) {
+                if (!kInPlace && p.ws) {
                     float *o = p.ws + o0;
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
                         if (j < jn) o[j * howo] = v[j];
-                } else if (!kPlain && p.red_add) {
+                } else if (!kInPlace && p.red_add) {
                     float *o = static_cast<float *>(p.out) + o0;
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
