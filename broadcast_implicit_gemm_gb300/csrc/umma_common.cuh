@@ -266,8 +266,10 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] += bv[j];
                 } else if (p.epi == BIGEMM_EPI_BIAS_EXP) {
+                    // the hardware exp2 with one multiply (a few ulp): far inside the
+                    // conv's own error bound, and half the instructions of expf
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = expf(v[j] + bv[j]);
+                    for (int j = 0; j < 32; ++j) v[j] = __expf(v[j] + bv[j]);
                 } else {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = rsqrtf(v[j] + bv[j] + p.eps);
