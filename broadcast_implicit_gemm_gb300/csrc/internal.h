@@ -142,6 +142,11 @@ cudaError_t launch_umma_plain_reg(int amode, bool rb, int fmt, int bn, bool epi1
                                   const UmmaParams &p, const CUtensorMap &map_a,
                                   const CUtensorMap &map_b, const CUtensorMap &map_c, int grid,
                                   cudaStream_t stream);
+// The per-tap and direct kernels narrowed to split-K slices added into an fp32
+// output (umma_add.cu), weights streamed.
+cudaError_t launch_umma_add(int amode, int fmt, int bn, bool epi16, const UmmaParams &p,
+                            const CUtensorMap &map_a, const CUtensorMap &map_b,
+                            const CUtensorMap &map_c, int grid, cudaStream_t stream);
 cudaError_t launch_umma_res(int amode, int fmt, int bn, bool epi16, const UmmaParams &p,
                             const CUtensorMap &map_a, const CUtensorMap &map_b,
                             const CUtensorMap &map_c, int grid, cudaStream_t stream);

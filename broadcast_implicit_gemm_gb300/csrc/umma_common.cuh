@@ -93,7 +93,8 @@ __device__ __forceinline__ void tmem_wait_ld_regs(uint32_t (&r)[32])
 // only that code: 0 any output (every case decided at run time); 1 a 16-bit
 // output written in place by TMA stores, with no epilogue op; 2 the same
 // written from registers; 3 an fp32 output written in place by TMA stores,
-// the epilogue op chosen at run time.  (Measured on the 1x1 ResNet-50 layers: the general
+// the epilogue op chosen at run time; 4 K slices added into an fp32 output
+// (TMA reduce-add boxes or atomic adds), no op but the first slice's bias.  (Measured on the 1x1 ResNet-50 layers: the general
 // form's unused paths cost a third of the epilogue's time per tile.)
 template <int BN, bool BOXED, int NEPI = kEpiWarps, int MT = 1, int STG = 4096, int FORM = 0>
 __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtensorMap *map_c,
@@ -122,15 +123,16 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
     const int bj_y = bj / p.box_w, bj_x = bj - bj_y * p.box_w;
     const int wj0_y = wj0 / p.box_w, wj0_x = wj0 - wj0_y * p.box_w;
     const long long howo = (long long)p.Ho * p.Wo;
-    static_assert(FORM >= 0 && FORM <= 3, "output form");
+    static_assert(FORM >= 0 && FORM <= 4, "output form");
     constexpr bool kPlain = FORM == 1 || FORM == 2;   // 16-bit, in place, no epilogue op
-    constexpr bool kInPlace = FORM != 0;              // no workspace, no atomic adds
-    const int ec = FORM == 3 ? 4 : kPlain ? 2 : ((p.ws || p.out_dt == BIGEMM_F32) ? 4 : 2);
+    constexpr bool kInPlace = FORM != 0;              // no workspace
+    const bool red = FORM == 4 || (FORM == 0 && p.red_add);   // adds into an fp32 output
+    const int ec = (FORM == 3 || FORM == 4) ? 4 : kPlain ? 2 : ((p.ws || p.out_dt == BIGEMM_F32) ? 4 : 2);
     const bool tma_out = (FORM == 1 || FORM == 3) ? true : FORM == 2 ? false : p.store_tma != 0;
     // 4-pixel register stores need plain stores into the output (no workspace,
     // no atomic adds), planes of a whole number of 4-element groups and an
     // output base on a 4-element boundary
-    const bool vec_static = (FORM == 0 || FORM == 2) && !tma_out && (kInPlace || (!p.ws && !p.red_add)) &&
+    const bool vec_static = (FORM == 0 || FORM == 2) && !tma_out && !red && (kInPlace || !p.ws) &&
                             howo % 4 == 0 &&
                             (reinterpret_cast<uintptr_t>(p.out) & (uintptr_t)(4 * ec - 1)) == 0;
     uint8_t *wstage = stage_out + (warp - 2) * STG;
@@ -149,7 +151,7 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
         // loop hands the values round with shuffles (a per-chunk load of all 32
         // biases cost a DRAM round trip per chunk after a cold start).
         const bool use_bias = !kPlain && (kInPlace || !p.ws) && p.epi != BIGEMM_EPI_NONE &&
-                              !(!kInPlace && p.red_add && w.sp != 0);
+                              !(red && w.sp != 0);
         float bl[kMine];
 #pragma unroll
         for (int i = 0; i < kMine; ++i) {
@@ -262,7 +264,7 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
                 float bv[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) bv[j] = __shfl_sync(0xffffffffu, bl[i], j);
-                if (p.epi == BIGEMM_EPI_BIAS) {
+                if (FORM == 4 || p.epi == BIGEMM_EPI_BIAS) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] += bv[j];
                 } else if (p.epi == BIGEMM_EPI_BIAS_EXP) {
@@ -304,7 +306,7 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
                     __syncwarp();
                     if (lane == 0) {
                         const int cc = cb + hh * 16;
-                        if (!kInPlace && p.red_add) {
+                        if (red) {
                             if (BOXED)
                                 tma_reduce_add_4d(map_c, buf, sx, sy, cc, sn);
                             else
@@ -363,7 +365,7 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
                         }
                     }
                 }
-            } else if ((FORM == 0 || FORM == 2) && !tma_out && valid) {
+            } else if ((FORM == 0 || FORM == 2 || FORM == 4) && !tma_out && valid) {
                 const long long o0 = base + (long long)cb * howo;
                 const int jn = min(32, p.CO - cb);
                 if (!kInPlace && p.ws) {
@@ -371,12 +373,12 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
                         if (j < jn) o[j * howo] = v[j];
-                } else if (!kInPlace && p.red_add) {
+                } else if (red) {
                     float *o = static_cast<float *>(p.out) + o0;
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
                         if (j < jn) atomicAdd(o + j * howo, v[j]);
-                } else if (!kPlain && p.out_dt == BIGEMM_F32) {
+                } else if (FORM == 0 && p.out_dt == BIGEMM_F32) {
                     float *o = static_cast<float *>(p.out) + o0;
 #pragma unroll
                     for (int j = 0; j < 32; ++j)

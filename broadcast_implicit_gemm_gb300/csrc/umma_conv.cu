@@ -79,6 +79,9 @@ cudaError_t launch_umma_conv(const UmmaTiling &t, int in_dt, const UmmaParams &p
     // whose epilogue carries only that path
     const bool plain = fmt != 2 && !p.ws && !p.red_add && p.epi == BIGEMM_EPI_NONE &&
                        p.out_dt != BIGEMM_F32;
+    // split-K slices adding into an fp32 output take the kernel narrowed to that
+    if (p.red_add && !p.ws && !t.bres && t.amode != A_HALO)
+        return launch_umma_add(t.amode, fmt, t.bn, e16, p, map_a, map_b, map_c, grid, stream);
     if (plain && t.amode != A_HALO) {
         // the checks launch_umma_res makes for resident weights
         if (t.bres && (p.split != 1 || grid % p.co_tiles != 0 || p.res_b_bytes <= 0))

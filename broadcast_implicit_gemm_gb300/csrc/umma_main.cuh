@@ -293,8 +293,9 @@ cudaError_t dispatch_bn(int bn, bool epi16, const UmmaParams &p, const CUtensorM
     }
 }
 
-// FORM 0 for every operand format; the 16-bit plain forms (1, 2) only where
-// the launching translation unit asks for them (umma_plain.cu).
+// FORM 0 for every operand format; the narrowed forms only where the
+// launching translation unit asks for them (umma_plain_*.cu: 16-bit outputs,
+// 16-bit operands; umma_add.cu: split-K adds into fp32, any operand format).
 template <int AMODE, bool RB, int FORM = 0>
 cudaError_t dispatch_fmt(int fmt, int bn, bool epi16, const UmmaParams &p, const CUtensorMap &ma,
                          const CUtensorMap &mb, const CUtensorMap &mc, int grid, cudaStream_t s)
@@ -303,8 +304,10 @@ cudaError_t dispatch_fmt(int fmt, int bn, bool epi16, const UmmaParams &p, const
     case 0: return dispatch_bn<AMODE, 0, RB, FORM>(bn, epi16, p, ma, mb, mc, grid, s);
     case 1: return dispatch_bn<AMODE, 1, RB, FORM>(bn, epi16, p, ma, mb, mc, grid, s);
     case 2:
-        if (FORM != 0) return cudaErrorInvalidValue;
-        return dispatch_bn<AMODE, 2, RB, 0>(bn, epi16, p, ma, mb, mc, grid, s);
+        if constexpr (FORM == 1 || FORM == 2)
+            return cudaErrorInvalidValue;   // 16-bit output forms take 16-bit operands
+        else
+            return dispatch_bn<AMODE, 2, RB, FORM>(bn, epi16, p, ma, mb, mc, grid, s);
     default: return cudaErrorInvalidValue;
     }
 }
