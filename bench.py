@@ -14,8 +14,9 @@ the events.  A second pass of K steps, also timed, adds the library's own
 per-kernel event records and an event after every layer; the roofline and the
 per-layer figures come from it (those events serialise the launches, so it is
 reported separately as profiled_ms_per_step).  `e2e` repeats the
-step with host buffers: pinned host->device copies of the inputs and a
-device->host copy of the outputs inside the timed region.  `cpu_baseline` times
+step with host buffers: pinned host->device copies of every layer's inputs and
+device->host copies of its output inside the timed region, on two copy streams
+that overlap the layers' convs (the layers are independent problems).  `cpu_baseline` times
 the CPU oracle on this host on a bounded sample of the same workload.  With
 --impl reference the CPU oracle is the measured arm.
 
@@ -192,13 +193,35 @@ class ConvStep:
                 self.marks.append((i, ev))
 
     def run_e2e(self, stream):
-        for it in self.items:
-            it["x"].copy_(it["x_h"], non_blocking=True)
-            it["w"].copy_(it["w_h"], non_blocking=True)
-            if it["b"] is not None:
-                it["b"].copy_(it["b_h"], non_blocking=True)
+        """The step from pinned host buffers: every layer's inputs go in on a
+        copy-in stream, its conv runs on `stream` once they have landed, and its
+        output comes back on a copy-out stream, so the copies of one layer
+        overlap the other layers' convs and the two directions overlap each other.
+        The step ends on `stream` when the last output is on the host."""
+        torch = self.torch
+        if getattr(self, "copy_streams", None) is None:
+            self.copy_streams = (torch.cuda.Stream(), torch.cuda.Stream())
+        h2d, d2h = self.copy_streams
+        h2d.wait_stream(stream)          # the previous step is done with the input buffers
+        landed = []
+        with torch.cuda.stream(h2d):
+            for it in self.items:
+                it["x"].copy_(it["x_h"], non_blocking=True)
+                it["w"].copy_(it["w_h"], non_blocking=True)
+                if it["b"] is not None:
+                    it["b"].copy_(it["b_h"], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(h2d)
+                landed.append(ev)
+        for it, ev in zip(self.items, landed):
+            stream.wait_event(ev)
             self.bg.conv2d_nchw_run(it["plan"], it["x"], it["w"], it["b"], 1e-5, it["out"], stream)
-            it["out_h"].copy_(it["out"], non_blocking=True)
+            done = torch.cuda.Event()
+            done.record(stream)
+            d2h.wait_event(done)
+            with torch.cuda.stream(d2h):
+                it["out_h"].copy_(it["out"], non_blocking=True)
+        stream.wait_stream(d2h)
 
     def h2d_bytes(self):
         return sum(it["x_h"].numel() * it["x_h"].element_size()
