@@ -129,10 +129,10 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
     const bool red = FORM == 4 || (FORM == 0 && p.red_add);   // adds into an fp32 output
     const int ec = (FORM == 3 || FORM == 4) ? 4 : kPlain ? 2 : ((p.ws || p.out_dt == BIGEMM_F32) ? 4 : 2);
     const bool tma_out = (FORM == 1 || FORM == 3) ? true : FORM == 2 ? false : p.store_tma != 0;
-    // 4-pixel register stores need plain stores into the output (no workspace,
-    // no atomic adds), planes of a whole number of 4-element groups and an
-    // output base on a 4-element boundary
-    const bool vec_static = (FORM == 0 || FORM == 2) && !tma_out && !red && (kInPlace || !p.ws) &&
+    // 4-pixel register stores need the output itself (stored into, or added into
+    // by K slices; not the workspace), planes of a whole number of 4-element
+    // groups and an output base on a 4-element boundary
+    const bool vec_static = (FORM == 0 || FORM == 2 || FORM == 4) && !tma_out && (kInPlace || !p.ws) &&
                             howo % 4 == 0 &&
                             (reinterpret_cast<uintptr_t>(p.out) & (uintptr_t)(4 * ec - 1)) == 0;
     uint8_t *wstage = stage_out + (warp - 2) * STG;
@@ -213,7 +213,8 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
         // group of four lanes holds four consecutive pixels of one plane, at a
         // 4-element boundary, or no valid pixel at all, the warp regroups each
         // 32 x 32 block through its staging buffer and a lane writes 4-pixel
-        // runs of one channel (8 or 16 bytes) instead of single elements.
+        // runs of one channel (8 or 16 bytes; K slices add them with one
+        // 16-byte vector atomic) instead of single elements.
         bool vec4 = false, gok = false;
         long long gbase = 0;
         if (vec_static) {
@@ -338,9 +339,13 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
 #pragma unroll
                             for (int k = 0; k < 4; ++k) {
                                 const int c = c0 + 4 * k;
-                                if (cb + hh * 16 + c < p.CO)
-                                    *reinterpret_cast<float4 *>(o + c * howo) =
-                                        *reinterpret_cast<const float4 *>(wstage + c * 128 + g * 16);
+                                if (cb + hh * 16 + c < p.CO) {
+                                    const float4 val = *reinterpret_cast<const float4 *>(wstage + c * 128 + g * 16);
+                                    if (red)   // a K slice: one 16-byte vector add per run
+                                        atomicAdd(reinterpret_cast<float4 *>(o + c * howo), val);
+                                    else
+                                        *reinterpret_cast<float4 *>(o + c * howo) = val;
+                                }
                             }
                         }
                     }

@@ -241,6 +241,22 @@ def test_split_k_sums(case, split):
     assert info["split"] > 1 and info["split_sum"] == how
 
 
+# 56-byte fp32 output rows under whole-row 14 x 8 boxes: each group of four lanes
+# adds a 4-pixel run with one 16-byte vector atomic
+@pytest.mark.parametrize("split", [2, 4])
+@pytest.mark.parametrize("spec", [
+    S("va_nhwc_14_tf32", 1, 256, 96, 14, 14, 3, 1, 1, i="f32", o="f32"),
+    S("va_nhwc_14_f16in_bias", 2, 128, 80, 14, 14, 1, 1, 0, o="f32", epi="bias"),
+    S("va_nhwc_28_tf32_ragged_co", 1, 128, 72, 28, 28, 3, 1, 1, i="f32", o="f32"),
+], ids=lambda s: s.name)
+def test_split_k_vector_atomics(spec, split):
+    bw = spec.W
+    bh = {14: 8, 28: 4}[bw]                    # 112-pixel tiles: whole, 4-aligned lane groups
+    info = check(spec, {"kind": bg.KIND_UMMA, "mode": bg.MODE_NHWC, "box_w": bw, "box_h": bh,
+                        "split_k": split})
+    assert info["split"] > 1 and info["split_sum"] == "add" and info["store"] == "direct"
+
+
 
 # ------------------------------------------------- halo units of two stacked tiles
 # A unit of 32 output rows x 8 columns: two 128-pixel M tiles share every
