@@ -276,6 +276,12 @@ class BcastStep:
         return self.out.numel() * 4
 
 
+def bg_long_rows(B1, esize=4):
+    """Whether the library runs [B0,P,B1] on its per-channel kernel (rows of at
+    least 1 KB) rather than its short-row kernel."""
+    return B1 * esize >= 1024
+
+
 def timed_steps(step_fn, steps, torch, stream, flush):
     """Per-step CUDA event pairs (ms), with an L2 flush before each step."""
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -475,6 +481,7 @@ def main():
     import torch
 
     import broadcast_implicit_gemm_gb300 as bg
+    from broadcast_implicit_gemm_gb300 import synth
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     stream = torch.cuda.Stream(device)
@@ -571,6 +578,23 @@ def main():
             ab[opname] = {"per_channel_gbs": res["per_channel"], "flat_gbs": res["flat"],
                           "speedup": res["per_channel"] / res["flat"]}
         line["bcast_ab"] = ab
+        # the general form [1,P,1] => [B0,P,B1] (bcast_run), exp to fp32, on
+        # short, single-element and long rows
+        gen = []
+        for B0, P, B1 in synth.BCAST_GENERAL:
+            gvar = synth.bcast_var(P, seed=1).to(device)
+            gout = torch.empty((B0, P, B1), dtype=torch.float32, device=device)
+            fn = (lambda st, a=(B0, P, B1), v=gvar, o=gout:
+                  bg.bcast_run(*a, bg.BC_EXP, v, 1e-5, o, bg.F32, st))
+            for _ in range(3):
+                with torch.cuda.stream(stream):
+                    fn(stream)
+            tt, _ = timed_steps(fn, max(5, min(args.steps, 20)), torch, stream, flush)
+            gbs = (gout.numel() * 4 + P * 4) / (sum(tt) / len(tt) / 1e3) / 1e9
+            gen.append({"shape": [B0, P, B1], "gbs": gbs, "frac": gbs / peaks["hbm"],
+                        "kernel": "bcast_nchw" if bg_long_rows(B1) else "bcast_rows"})
+            del gout
+        line["bcast_general"] = gen
         line["roofline"] = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm"], "unit": "GB/s",
                             "frac": ach / peaks["hbm"], "kernel": "bcast_nchw", "launches": n,
                             "avg_launch_us": tms / n * 1e3,

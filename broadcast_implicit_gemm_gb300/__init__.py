@@ -21,7 +21,7 @@ __all__ = [
     "BigemmError", "Plan", "PlanOptions", "library_path", "load_library",
     "conv2d_nchw_plan", "conv2d_nchw_plan_ex", "conv2d_nchw_run", "conv2d_nchw_plan_destroy",
     "conv2d_nchw_plan_describe", "conv2d_nchw_run_noalloc", "bcast_nchw_run",
-    "bcast_nchw_run_flat",
+    "bcast_nchw_run_flat", "bcast_run",
     "bigemm_status_string", "bigemm_last_device_error", "bigemm_clear_device_error",
     "bigemm_set_wait_timeout_ns", "bigemm_debug_wait_timeout", "bigemm_profile_enable",
     "bigemm_profile_read", "bigemm_version", "conv2d", "bcast", "out_size",
@@ -89,6 +89,7 @@ def _declare(lib):
     lib.conv2d_nchw_run_noalloc.argtypes = [i] * 9 + [i, i, i, p, p, p, f, p, p, p]
     lib.bcast_nchw_run.argtypes = [i, i, i, i, i, p, f, p, i, p]
     lib.bcast_nchw_run_flat.argtypes = [i, i, i, i, i, p, f, p, i, p]
+    lib.bcast_run.argtypes = [i, i, i, i, p, f, p, i, p]
     lib.bigemm_status_string.argtypes = [i]
     lib.bigemm_status_string.restype = ctypes.c_char_p
     lib.bigemm_last_device_error.argtypes = []
@@ -102,7 +103,8 @@ def _declare(lib):
     for name in ("conv2d_nchw_plan", "conv2d_nchw_plan_ex", "conv2d_nchw_run",
                  "conv2d_nchw_run_noalloc",
                  "conv2d_nchw_plan_destroy", "conv2d_nchw_plan_describe", "bcast_nchw_run",
-                 "bcast_nchw_run_flat", "bigemm_last_device_error", "bigemm_clear_device_error",
+                 "bcast_nchw_run_flat", "bcast_run", "bigemm_last_device_error",
+                 "bigemm_clear_device_error",
                  "bigemm_set_wait_timeout_ns", "bigemm_debug_wait_timeout",
                  "bigemm_profile_enable", "bigemm_profile_read"):
         getattr(lib, name).restype = i
@@ -228,6 +230,12 @@ def bcast_nchw_run(N, C, H, W, op, var, eps, out, out_dtype, stream=None):
 def bcast_nchw_run_flat(N, C, H, W, op, var, eps, out, out_dtype, stream=None):
     _check(load_library().bcast_nchw_run_flat(N, C, H, W, op, _ptr(var), float(eps), _ptr(out),
                                               out_dtype, _stream(stream)), "bcast_nchw_run_flat")
+
+
+def bcast_run(B0, P, B1, op, var, eps, out, out_dtype, stream=None):
+    """The general broadcast [1,P,1] => [B0,P,B1]: out[b0,p,b1] = op(var[p])."""
+    _check(load_library().bcast_run(B0, P, B1, op, _ptr(var), float(eps), _ptr(out), out_dtype,
+                                    _stream(stream)), "bcast_run")
 
 
 def bigemm_last_device_error() -> int:

@@ -182,6 +182,11 @@ cudaError_t launch_dw_stream(const ConvShape &s, const void *x, const void *w, c
 bool dw_plane_ok(const ConvShape &s);
 cudaError_t launch_dw_plane(const ConvShape &s, const void *x, const void *w, const float *bias,
                             float eps, void *out, cudaStream_t stream);
+// [1, P, 1] => [B0, P, B1]: the per-channel kernel for long rows, bcast_rows
+// for short ones (bcast.cu).
+bool bcast_long_rows(long long B1, int out_dt);
+cudaError_t launch_bcast_general(int B0, int P, int B1, int op, const float *var, float eps,
+                                 void *out, int out_dt, cudaStream_t stream);
 cudaError_t launch_bcast(int N, int C, int HW, int op, const float *var, float eps, void *out,
                          int out_dt, int flat, cudaStream_t stream);
 cudaError_t launch_wait_timeout_probe(int *err, unsigned long long timeout_ns,

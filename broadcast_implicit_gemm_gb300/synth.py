@@ -85,6 +85,10 @@ DEPTHWISE_FP16 = [
 ]
 
 BCAST_SHAPE = (128, 256, 32, 32)   # N, C, H, W
+# general [1,P,1] => [B0,P,B1] broadcasts, fp32 outputs larger than L2: short
+# rows (7x7 and 4x4 planes), single-element rows ([N, C] from [C]), and a tiny
+# preserved axis with long rows
+BCAST_GENERAL = [(1024, 1024, 49), (512, 4096, 16), (32768, 1024, 1), (64, 16, 65536)]
 BCAST_EPS = 1e-5
 
 ALL_CONVS = RESNET_LAST + SWEEP_FP32 + RESNET50_FP16 + FUSED_CONV + DEPTHWISE_FP16

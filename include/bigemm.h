@@ -185,6 +185,23 @@ bigemm_status conv2d_nchw_plan_describe(bigemm_plan plan, char *buf, size_t len)
 bigemm_status bcast_nchw_run(int N, int C, int H, int W, int op, const float *var, float eps,
                              void *out, bigemm_dtype out_dtype, void *stream);
 
+/*
+ * bcast_run -- the general form, out[b0,p,b1] = op(var[p]) for b0 < B0,
+ * p < P, b1 < B1: any broadcast [1,P,1] => [B0,P,B1] after fusing adjacent axes
+ * of the same kind, the last axis broadcast ("[CINN] Add the TileBroadcastTactic
+ * for NCHW broadcast", PaddlePaddle PR 70092, Introduction).  The NCHW case is
+ * B0 = N, P = C, B1 = H*W.  Long rows (B1 * element size >= 1 KB) run the
+ * per-channel kernel of bcast_nchw_run; shorter rows a kernel whose threads
+ * each own a fixed 16-byte piece of the P*B1 run and repeat it down B0.
+ *   var  [P] fp32 device; out [B0,P,B1] device of out_dtype (F32/F16/BF16),
+ *        aligned to its element size (16-byte alignment takes vector stores).
+ *   op   bigemm_bcast_op; eps is used by RSQRT only.
+ * Errors: INVALID_ARG (a size < 1, null pointer, bad op/dtype, misaligned
+ * output), UNSUPPORTED (P*B1 > 2^31 - 1), CUDA.
+ */
+bigemm_status bcast_run(int B0, int P, int B1, int op, const float *var, float eps, void *out,
+                        bigemm_dtype out_dtype, void *stream);
+
 /* The same broadcast written the way a generic fused-loop schedule does it:
  * one flat loop over all N*C*H*W outputs, each recomputing op(var[c]) from
  * its own index.  Kept to measure the per-channel mapping against it. */

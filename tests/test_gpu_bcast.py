@@ -79,3 +79,65 @@ def test_bcast_unaligned_output_pointer():
     torch.cuda.synchronize()
     assert buf[0].item() == 0.0
     check_planes(out, var, "exp", "f32")
+
+
+# ---------------------------------------------------------- [1,P,1] => [B0,P,B1]
+# The general form is the NCHW one with N = B0, C = P, H*W = B1, so the same
+# oracle values and plane check apply (viewed as [B0, P, 1, B1]).  Short rows
+# (B1 * element size < 1 KB) take the short-row kernel, long rows the
+# per-channel one; both vector and element stores.
+GENERAL = [
+    (3, 5, 1), (2, 7, 3), (4, 64, 4), (1, 1000, 2), (5, 9, 17), (2, 33, 64), (7, 3, 255),
+    (2, 6, 256), (3, 4, 1031), (128, 2, 8), (1, 1, 1),
+]
+
+
+@pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("op", ["copy", "exp", "rsqrt", "recip"])
+@pytest.mark.parametrize("shape", GENERAL, ids=lambda s: "x".join(map(str, s)))
+def test_bcast_general(shape, op, dt):
+    B0, P, B1 = shape
+    var = synth.bcast_var(P, seed=P + B1)
+    if op == "rsqrt" and P > 1:
+        var[0] = 0.0
+    guard = 64
+    buf = torch.full((B0 * P * B1 + 2 * guard,), 7.0, dtype=TD[dt], device="cuda")
+    out = buf[guard:guard + B0 * P * B1].view(B0, P, 1, B1)
+    bg.bcast_run(B0, P, B1, OPS[op], var.cuda(), 1e-5, out, bg.DTYPE_CODES[dt])
+    torch.cuda.synchronize()
+    assert bool(torch.all(buf[:guard] == 7.0)) and bool(torch.all(buf[-guard:] == 7.0))
+    check_planes(out, var, op, dt)
+
+
+@pytest.mark.parametrize("shape", [(16, 1024, 49), (8, 3, 100000), (64, 4096, 1)])
+def test_bcast_general_unaligned_and_large(shape):
+    # output 4 bytes past a 16-byte boundary: element stores in either kernel
+    B0, P, B1 = shape
+    var = synth.bcast_var(P, seed=3)
+    buf = torch.zeros(B0 * P * B1 + 1, dtype=torch.float32, device="cuda")
+    out = buf[1:].view(B0, P, 1, B1)
+    bg.bcast_run(B0, P, B1, bg.BC_EXP, var.cuda(), 1e-5, out, bg.F32)
+    torch.cuda.synchronize()
+    assert buf[0].item() == 0.0
+    check_planes(out, var, "exp", "f32")
+
+
+def test_bcast_general_matches_nchw():
+    N, C, H, W = 4, 12, 5, 7
+    var = synth.bcast_var(C, seed=4).cuda()
+    a = torch.empty((N, C, H, W), dtype=torch.float16, device="cuda")
+    b = torch.empty_like(a)
+    bg.bcast_nchw_run(N, C, H, W, bg.BC_RSQRT, var, 1e-5, a, bg.F16)
+    bg.bcast_run(N, C, H * W, bg.BC_RSQRT, var, 1e-5, b, bg.F16)
+    torch.cuda.synchronize()
+    assert torch.equal(torch.nan_to_num(a, 1.0), torch.nan_to_num(b, 1.0))
+
+
+@pytest.mark.parametrize("args,status", [((0, 4, 4), 1), ((2, 0, 4), 1), ((2, 4, 0), 1),
+                                         ((1, 65536, 65536), 2)])
+def test_bcast_general_rejects(args, status):
+    var = torch.zeros(4, dtype=torch.float32, device="cuda")
+    out = torch.zeros(16, dtype=torch.float32, device="cuda")
+    with pytest.raises(bg.BigemmError) as e:
+        bg.bcast_run(*args, bg.BC_EXP, var, 1e-5, out, bg.F32)
+    assert e.value.status == status
