@@ -27,6 +27,7 @@ MUTANTS = {
     "out_size_ceil": ("return span / stride + 1;", "return (span + stride - 1) / stride + 1;"),
     "absum_signed": ("sabs += fabs(a * w);", "sabs += a * w;"),
     "bias_channel_zero": ("return exp(acc + bias[f]);", "return exp(acc + bias[0]);"),
+    "recip_bias_dropped": ("return 1.0 / (acc + bias[f]);", "return 1.0 / acc;"),
     "eps_added_in_double": ("volatile float t = v + eps;", "volatile double t = (double)v + eps;"),
     "image_index_dropped": ("data[(((size_t)n * s->CI + ci)", "data[(((size_t)0 * s->CI + ci)"),
     "flops_missing_factor2": ("return 2.0 * N * CO", "return 1.0 * N * CO"),
@@ -81,6 +82,14 @@ def _battery(lib):
         failed.append("rsqrt_eps_fp32")
     if oracle.bcast_value(oracle.BC_EXP, 0.0, lib=lib) != 1.0:
         failed.append("exp0")
+    # div epilogue on all-ones data and kernel (interior sum 27, corner 12)
+    try:
+        out, _ = oracle.conv2d_nchw(np.ones((1, 3, 5, 6)), np.ones((2, 3, 3, 3)), stride=1, pad=1,
+                                    bias=np.array([-30.0, 0.5]), epi=oracle.EPI_BIAS_RECIP, lib=lib)
+        if out[0, 0, 2, 2] != 1.0 / -3.0 or out[0, 1, 0, 0] != 1.0 / 12.5:
+            failed.append("recip")
+    except ValueError:
+        failed.append("recip-rejected")
     return failed
 
 

@@ -59,6 +59,23 @@ def test_epilogue_bias_exp_per_channel(orc):
                    bias=bias, epi=oracle.EPI_BIAS_RSQRT, eps=0.25)
     np.testing.assert_allclose(out, 1.0 / np.sqrt(hand + bias.reshape(1, 2, 1, 1) + 0.25),
                                rtol=1e-15)
+    # div: the reciprocal of the biased sum, per channel
+    out, _ = _conv(orc, case["shape"], case["data"], case["kernel"],
+                   bias=bias, epi=oracle.EPI_BIAS_RECIP)
+    np.testing.assert_allclose(out, 1.0 / (hand + bias.reshape(1, 2, 1, 1)), rtol=1e-15)
+
+
+def test_epilogue_recip_closed_form(orc):
+    """All-ones data and kernel: an interior output sums CI*K*K ones, a corner of
+    a pad-1 3x3 conv only the 4 taps inside the image, so with bias b the
+    reciprocal is 1/(count + b) exactly, sign included."""
+    CI, CO, H, W = 3, 2, 5, 6
+    x = np.ones((1, CI, H, W))
+    w = np.ones((CO, CI, 3, 3))
+    bias = np.array([-30.0, 0.5])
+    out, _ = oracle.conv2d_nchw(x, w, stride=1, pad=1, bias=bias, epi=oracle.EPI_BIAS_RECIP, lib=orc)
+    assert out[0, 0, 2, 2] == 1.0 / (27 - 30.0) and out[0, 1, 2, 2] == 1.0 / 27.5
+    assert out[0, 0, 0, 0] == 1.0 / (12 - 30.0) and out[0, 1, 0, 0] == 1.0 / 12.5
 
 
 def _rand(shape, seed):
