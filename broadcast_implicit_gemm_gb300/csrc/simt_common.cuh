@@ -35,7 +35,8 @@ __device__ __forceinline__ float epi_apply(int epi, float acc, const float *bias
     case BIGEMM_EPI_NONE: return acc;
     case BIGEMM_EPI_BIAS: return acc + bias[f];
     case BIGEMM_EPI_BIAS_EXP: return expf(acc + bias[f]);
-    default: return rsqrtf(acc + bias[f] + eps);
+    case BIGEMM_EPI_BIAS_RSQRT: return rsqrtf(acc + bias[f] + eps);
+    default: return 1.0f / (acc + bias[f]);
     }
 }
 

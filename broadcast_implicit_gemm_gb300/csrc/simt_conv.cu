@@ -282,7 +282,8 @@ __global__ void __launch_bounds__(256) conv_depthwise_kernel(SimtArgs a, int row
             for (int i = 0; i < kDwPX; ++i) {
                 if (a.epi == BIGEMM_EPI_BIAS) acc[i] += bv;
                 else if (a.epi == BIGEMM_EPI_BIAS_EXP) acc[i] = expf(acc[i] + bv);
-                else acc[i] = rsqrtf(acc[i] + bv + a.eps);
+                else if (a.epi == BIGEMM_EPI_BIAS_RSQRT) acc[i] = rsqrtf(acc[i] + bv + a.eps);
+                else acc[i] = 1.0f / (acc[i] + bv);
             }
         }
         const size_t o = ((size_t)(pl0 + j) * a.Ho + (y0 + yy)) * a.Wo + xo0;

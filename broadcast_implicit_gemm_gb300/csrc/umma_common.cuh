@@ -273,9 +273,12 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
                     // conv's own error bound, and half the instructions of expf
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = __expf(v[j] + bv[j]);
-                } else {
+                } else if (p.epi == BIGEMM_EPI_BIAS_RSQRT) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = rsqrtf(v[j] + bv[j] + p.eps);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = 1.0f / (v[j] + bv[j]);
                 }
             }
             if (wstore) {

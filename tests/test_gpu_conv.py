@@ -73,7 +73,7 @@ def check(spec, options=None, search=0, seed=0):
         bound = conv_bound(ref, sabs, tau, spec.out_dtype)
     else:
         epi = {"bias": oracle.EPI_BIAS, "bias_exp": oracle.EPI_BIAS_EXP,
-               "bias_rsqrt": oracle.EPI_BIAS_RSQRT}[spec.epi]
+               "bias_rsqrt": oracle.EPI_BIAS_RSQRT, "bias_recip": oracle.EPI_BIAS_RECIP}[spec.epi]
         ref, sabs = oracle.conv2d_nchw(x, w, stride=spec.stride, pad=spec.pad, groups=spec.groups,
                                        bias=b, epi=epi, nthreads=NTH)
         pre, _ = oracle.conv2d_nchw(x, w, stride=spec.stride, pad=spec.pad, groups=spec.groups,
@@ -440,6 +440,34 @@ def test_edge_cases(spec):
 @pytest.mark.parametrize("spec", [e for e in EDGE if e.groups == 1][:8], ids=lambda s: s.name)
 def test_edge_cases_simt(spec):
     check(spec, {"kind": bg.KIND_SIMT})
+
+
+# ------------------------------------------------- the div epilogue, 1/(conv + bias)
+# Non-negative data and kernels keep every argument well away from zero.
+def _R(name, N, CI, CO, H, W, K, s, p, g=1, i="f16", o="f32"):
+    return S(name, N, CI, CO, H, W, K, s, p, g=g, i=i, o=o, epi="bias_recip", dd="absnormal",
+             kd="absnormal")
+
+
+RECIP = [
+    (_R("recip_halo_f32", 2, 64, 96, 12, 12, 3, 1, 1), {"kind": bg.KIND_UMMA, "mode": bg.MODE_HALO}),
+    (_R("recip_nhwc_f16", 1, 32, 64, 9, 11, 3, 1, 1, o="f16"), {"kind": bg.KIND_UMMA, "mode": bg.MODE_NHWC}),
+    (_R("recip_direct_bf16", 2, 64, 128, 16, 16, 1, 1, 0, i="bf16", o="bf16"),
+     {"kind": bg.KIND_UMMA, "mode": bg.MODE_DIRECT}),
+    (_R("recip_tf32_split_reduce", 1, 256, 64, 9, 12, 3, 1, 1, i="f32"),
+     {"kind": bg.KIND_UMMA, "mode": bg.MODE_NHWC, "split_k": 4}),
+    (_R("recip_simt_tiled", 1, 16, 40, 10, 9, 3, 1, 1, i="f32"), {"kind": bg.KIND_SIMT}),
+    (_R("recip_depthwise_stream", 2, 16, 16, 14, 16, 3, 1, 1, g=16), None),
+    (_R("recip_depthwise_plane_k5", 2, 24, 24, 14, 14, 5, 1, 2, g=24), {"kind": bg.KIND_SIMT, "mode": 4}),
+]
+
+
+@pytest.mark.parametrize("case", RECIP, ids=lambda c: c[0].name)
+def test_div_epilogue(case):
+    spec, opts = case
+    info = check(spec, opts)
+    if opts and opts.get("split_k"):
+        assert info["split_sum"] == "reduce"
 
 
 # ------------------------------------------------- depthwise kernels

@@ -41,6 +41,11 @@ def epi_bound(arg, sabs, tau, epi, out_dtype, ref, eps=1e-5):
         lo = arg + eps - d
         with np.errstate(divide="ignore", invalid="ignore"):
             prop = np.where(lo > 0, 1.0 / np.sqrt(lo) - 1.0 / np.sqrt(arg + eps), np.inf)
+    elif epi == "bias_recip":
+        # 1/x moves by at most 1/(|x| - d) - 1/|x| while x keeps its sign
+        lo = np.abs(arg) - d
+        with np.errstate(divide="ignore", invalid="ignore"):
+            prop = np.where(lo > 0, 1.0 / lo - 1.0 / np.abs(arg), np.inf)
     else:
         raise ValueError(epi)
     return prop + 4 * ulp(ref, out_dtype) + 1e-30
