@@ -280,6 +280,10 @@ __global__ void __launch_bounds__(256) pack_operands_kernel(const T *__restrict_
 // each thread writes 16-byte channel runs of output pixels gathered from the
 // plane rows.  Tile index flattened as (channel tile, image).
 constexpr int kPlaneMax = 256;
+// the whole-plane kernels' shared buffer (128 bytes of channels x kPlaneMax
+// pixels), which their weight blocks use whole: twice the channel run of the
+// other kernels, so a large kernel takes half the weight blocks
+constexpr int kPlaneBufBytes = 128 * kPlaneMax;
 
 template <typename T>
 __global__ void __launch_bounds__(256) pack_plane_kernel(const T *__restrict__ x,
@@ -295,11 +299,11 @@ __global__ void __launch_bounds__(256) pack_plane_kernel(const T *__restrict__ x
     constexpr int VEC = 16 / E;
     constexpr int TC = 128 / E;
     constexpr int KC = TC / VEC;         // 16-byte channel runs per pixel (8)
-    static_assert(TC * kPlaneMax * E >= kPackSmemBytes, "the buffer also serves the weights");
+    static_assert(TC * kPlaneMax * E == kPlaneBufBytes, "the weight blocks use the whole buffer");
     __shared__ __align__(16) T sp[TC * kPlaneMax];
     if ((int)blockIdx.x < wblocks) {
         pack_weight_part(w, wp, CO, CI, KHKW, cip, (int)blockIdx.x, wblocks, sp,
-                         (int)(kPackSmemBytes / E));
+                         (int)(kPlaneBufBytes / E));
         return;
     }
     if ((int)blockIdx.x >= (int)gridDim.x - zblocks) {
@@ -369,11 +373,11 @@ __global__ void __launch_bounds__(256) pack_subplane_kernel(const T *__restrict_
     constexpr int G = 8 / E;             // elements per 8-byte word
     // item indices are split with multiply-high divisions by the launch's fixed
     // row length, row count and output width (runtime divisions dominated)
-    static_assert(TC * kPlaneMax * E >= kPackSmemBytes, "the buffer also serves the weights");
+    static_assert(TC * kPlaneMax * E == kPlaneBufBytes, "the weight blocks use the whole buffer");
     __shared__ __align__(16) T sp[TC * kPlaneMax];
     if ((int)blockIdx.x < wblocks) {
         pack_weight_part(w, wp, CO, CI, KHKW, cip, (int)blockIdx.x, wblocks, sp,
-                         (int)(kPackSmemBytes / E));
+                         (int)(kPlaneBufBytes / E));
         return;
     }
     if ((int)blockIdx.x >= (int)gridDim.x - zblocks) {
@@ -634,7 +638,8 @@ cudaError_t launch_pack_operands(const void *x, void *xh, int N, int C, int H, i
     const long long data_blocks = ptiles * ctiles * N;
     // weight blocks: one per (output channel, channel run) item of pack_weight_part;
     // none when w is null (the conv reads the caller's kernel as it is)
-    const long long cap = kPackSmemBytes / (long long)dtype_size(dt);
+    const long long cap = ((kind == 0 || kind == 3) ? kPlaneBufBytes : kPackSmemBytes) /
+                          (long long)dtype_size(dt);
     long long cc = cap / KHKW;
     if (cc >= 32) cc &= ~31ll;
     const long long witems = cc >= 1 ? (long long)CO * ((cip + cc - 1) / cc)
