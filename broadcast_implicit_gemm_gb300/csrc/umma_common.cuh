@@ -94,8 +94,9 @@ __device__ __forceinline__ void tmem_wait_ld_regs(uint32_t (&r)[32])
 // output written in place by TMA stores, with no epilogue op; 2 the same
 // written from registers; 3 an fp32 output written in place by TMA stores,
 // the epilogue op chosen at run time; 4 K slices added into an fp32 output
-// (TMA reduce-add boxes or atomic adds), no op but the first slice's bias.  (Measured on the 1x1 ResNet-50 layers: the general
-// form's unused paths cost a third of the epilogue's time per tile.)
+// (TMA reduce-add boxes or atomic adds), no op but the first slice's bias.
+// (Measured on the 1x1 ResNet-50 layers: the general form's unused paths cost
+// a third of the epilogue's time per tile.)
 template <int BN, bool BOXED, int NEPI = kEpiWarps, int MT = 1, int STG = 4096, int FORM = 0>
 __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtensorMap *map_c,
                                               uint32_t tmem_base, uint64_t *tfull,
