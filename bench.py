@@ -168,21 +168,51 @@ class ConvStep:
         self.specs = specs
         self.items = []
         self.marks = None
-        for i, s in enumerate(specs):
-            x, w, b = synth.conv_inputs(s, seed + i)
+        # Every layer's inputs (data, kernel, bias) sit back to back, 256-byte
+        # aligned, in one pinned host buffer and one device buffer, so that the
+        # end-to-end step moves each layer's inputs with a single copy.
+        inputs = [synth.conv_inputs(s, seed + i) for i, s in enumerate(specs)]
+        def align(n):
+            return (n + 255) // 256 * 256
+        layout, off = [], 0
+        for x, w, b in inputs:
+            segs = []
+            for t in (x, w, b):
+                if t is None:
+                    segs.append(None)
+                    continue
+                nb = t.numel() * t.element_size()
+                segs.append((off, nb, t.dtype, tuple(t.shape)))
+                off = align(off + nb)
+            layout.append(segs)
+        self.stage_h = torch.empty(max(off, 256), dtype=torch.uint8).pin_memory()
+        self.stage_d = torch.empty(max(off, 256), dtype=torch.uint8, device=device)
+
+        def view(buf, seg):
+            o, nb, dt, shape = seg
+            return buf[o:o + nb].view(dt).view(shape)
+
+        for i, (s, (x, w, b), segs) in enumerate(zip(specs, inputs, layout)):
+            for t, seg in zip((x, w, b), segs):
+                if seg is not None:
+                    view(self.stage_h, seg).copy_(t)
             Ho, Wo = out_hw(s)
             plan = bg.conv2d_nchw_plan(s.N, s.H, s.W, s.CO, s.CI, s.K, s.K, s.stride, s.pad,
                                        s.groups, bg.DTYPE_CODES[s.in_dtype],
                                        bg.DTYPE_CODES[s.out_dtype], bg.EPI_NAMES[s.epi], search)
             out = torch.empty((s.N, s.CO, Ho, Wo), dtype=synth.TORCH_DTYPES[s.out_dtype],
                               device=device)
+            first = segs[0][0]
+            last = max(sg[0] + sg[1] for sg in segs if sg is not None)
             self.items.append({
                 "spec": s, "plan": plan, "info": plan.describe(),
-                "x_h": x.pin_memory(), "w_h": w.pin_memory(),
-                "b_h": b.pin_memory() if b is not None else None,
-                "x": x.to(device), "w": w.to(device), "b": b.to(device) if b is not None else None,
+                "x": view(self.stage_d, segs[0]), "w": view(self.stage_d, segs[1]),
+                "b": view(self.stage_d, segs[2]) if segs[2] is not None else None,
+                "in_d": self.stage_d[first:last], "in_h": self.stage_h[first:last],
                 "out": out, "out_h": torch.empty(out.shape, dtype=out.dtype).pin_memory(),
             })
+        self.stage_d.copy_(self.stage_h)
+        torch.cuda.synchronize()
 
     def run(self, stream):
         for i, it in enumerate(self.items):
@@ -206,10 +236,7 @@ class ConvStep:
         landed = []
         with torch.cuda.stream(h2d):
             for it in self.items:
-                it["x"].copy_(it["x_h"], non_blocking=True)
-                it["w"].copy_(it["w_h"], non_blocking=True)
-                if it["b"] is not None:
-                    it["b"].copy_(it["b_h"], non_blocking=True)
+                it["in_d"].copy_(it["in_h"], non_blocking=True)   # data, kernel, bias in one copy
                 ev = torch.cuda.Event()
                 ev.record(h2d)
                 landed.append(ev)
@@ -224,9 +251,7 @@ class ConvStep:
         stream.wait_stream(d2h)
 
     def h2d_bytes(self):
-        return sum(it["x_h"].numel() * it["x_h"].element_size()
-                   + it["w_h"].numel() * it["w_h"].element_size()
-                   + (it["b_h"].numel() * 4 if it["b_h"] is not None else 0) for it in self.items)
+        return sum(it["in_h"].numel() for it in self.items)   # the copied bytes, alignment gaps included
 
     def d2h_bytes(self):
         return sum(it["out"].numel() * it["out"].element_size() for it in self.items)
