@@ -1,0 +1,60 @@
+"""Seeded random shapes through every tensor-core operand mode, output form and
+epilogue: each case is checked element by element against the oracle, like the
+hand-picked cases of test_gpu_conv.py.  A forced choice that the library
+refuses for a shape (UNSUPPORTED) is skipped, not failed."""
+import numpy as np
+import pytest
+
+import broadcast_implicit_gemm_gb300 as bg
+from tests.test_gpu_conv import S, check
+
+pytestmark = pytest.mark.gpu
+
+MODES = {"auto": None, "nhwc": bg.MODE_NHWC, "halo": bg.MODE_HALO, "direct": bg.MODE_DIRECT,
+         "sub": bg.MODE_SUB, "stack": bg.MODE_STACK}
+
+
+def _cases(n=48, seed=2024):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        K = int(rng.choice([1, 1, 3, 3, 3, 5]))
+        stride = int(rng.choice([1, 1, 1, 2]))
+        pad = int(rng.integers(0, K // 2 + 1))
+        H, W = int(rng.integers(K, 31)), int(rng.integers(K, 31))
+        CI = int(rng.choice([8, 16, 24, 40, 64, 96, 128]))
+        CO = int(rng.choice([16, 40, 64, 72, 128, 136, 200, 256]))
+        N = int(rng.integers(1, 4))
+        i_dt = str(rng.choice(["f16", "bf16", "f32"]))
+        o_dt = str(rng.choice(["f16", "f32"])) if i_dt == "f16" else (i_dt if rng.random() < 0.5 else "f32")
+        epi = str(rng.choice(["none", "none", "bias", "bias_exp", "bias_recip"]))
+        dd, kd = ("absnormal", "absnormal") if epi == "bias_recip" else ("uniform", "he")
+        if epi == "bias_exp":
+            o_dt = "f32"          # exp of a large sum would overflow a 16-bit output
+        mode = str(rng.choice(list(MODES)))
+        opts = {"kind": bg.KIND_UMMA}
+        if MODES[mode] is not None:
+            opts["mode"] = MODES[mode]
+        r = rng.random()
+        if r < 0.3:
+            opts["tile_n"] = 128
+            opts["epi_warps"] = 16
+        elif r < 0.5:
+            opts["split_k"] = int(rng.choice([2, 3, 4]))
+        elif r < 0.65:
+            opts["resident_b"] = 1
+        spec = S(f"rand{i}_{mode}_k{K}s{stride}p{pad}_{H}x{W}_ci{CI}_co{CO}_{i_dt}{o_dt}_{epi}",
+                 N, CI, CO, H, W, K, stride, pad, i=i_dt, o=o_dt, epi=epi, dd=dd, kd=kd)
+        out.append((spec, opts))
+    return out
+
+
+@pytest.mark.parametrize("case", _cases(), ids=lambda c: c[0].name)
+def test_random_shape(case):
+    spec, opts = case
+    try:
+        check(spec, opts)
+    except bg.BigemmError as e:
+        if e.status == 2:        # UNSUPPORTED: the forced choice does not fit this shape
+            pytest.skip(f"unsupported: {opts}")
+        raise
