@@ -95,3 +95,30 @@ def test_product_path_does_not_reach_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"(import\s+oracle|from\s+oracle|liboracle|oracle\.c)", text), f
+
+
+def _c_struct_fields(name):
+    """Field names of a typedef'd C struct in the header, in order."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    m = re.search(r"typedef\s+struct\s*\{(.*?)\}\s*" + name + r"\s*;", text, flags=re.S)
+    assert m, name
+    return re.findall(r"\b([a-z_][a-z0-9_]*)\s*;", m.group(1))
+
+
+def test_plan_options_binding_matches_header():
+    # the ctypes mirror must list the header's int fields in the same order
+    sys.path.insert(0, ROOT)
+    import broadcast_implicit_gemm_gb300 as bg
+    assert [f for f, _ in bg.PlanOptions._fields_] == _c_struct_fields("bigemm_plan_options")
+    assert all(t is ctypes.c_int for _, t in bg.PlanOptions._fields_)
+
+
+def test_enum_values_match_header():
+    # the binding's epilogue, broadcast-op and mode constants equal the header's
+    sys.path.insert(0, ROOT)
+    import broadcast_implicit_gemm_gb300 as bg
+    text = open(HEADER).read()
+    vals = dict((k, int(v)) for k, v in re.findall(r"\b(BIGEMM_[A-Z0-9_]+)\s*=\s*(\d+)", text))
+    for name in ("EPI_NONE", "EPI_BIAS", "EPI_BIAS_EXP", "EPI_BIAS_RSQRT", "EPI_BIAS_RECIP",
+                 "BC_COPY", "BC_EXP", "BC_RSQRT", "BC_RECIP", "KIND_UMMA", "KIND_SIMT"):
+        assert getattr(bg, name) == vals["BIGEMM_" + name], name
