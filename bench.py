@@ -436,6 +436,23 @@ def cpu_baseline(workload, specs, budget_s=12.0):
             "sample": f"{len(sample)} layers ({names}); {reps} passes of {dt * 1e3:.1f} ms"}
 
 
+def reduce_max(value, dist, device):
+    """The largest of the ranks' values (each rank's timed total: the job takes
+    as long as its slowest replica); the value itself on one rank."""
+    if not dist:
+        return value
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(work_per_rank, world, ms_per_step, scale):
+    """Whole-job throughput: every rank runs the same step (weak scaling), so
+    the job does world x the per-rank work in the slowest rank's time."""
+    return work_per_rank * world / (ms_per_step / 1e3) / scale
+
+
 def dist_setup(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -554,13 +571,9 @@ def main():
     if bg.bigemm_last_device_error() != 0:
         raise SystemExit("a device wait timed out during the timed region")
 
-    total_ms = sum(times)
-    if dist:
-        t = torch.tensor([total_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = reduce_max(sum(times), dist, device)   # the slowest rank's time
     ms_per_step = total_ms / args.steps
-    value = step.work() * world / (ms_per_step / 1e3) / scale
+    value = job_rate(step.work(), world, ms_per_step, scale)
 
     # end to end through the public call, host buffers in and out
     for _ in range(2):
@@ -569,8 +582,8 @@ def main():
     torch.cuda.synchronize()
     e2e_steps = max(3, min(args.steps, 20))
     e2e_times, _ = timed_steps(step.run_e2e, e2e_steps, torch, stream, flush)
-    e2e_ms = sum(e2e_times) / e2e_steps
-    e2e_value = step.work() * world / (e2e_ms / 1e3) / scale
+    e2e_ms = reduce_max(sum(e2e_times), dist, device) / e2e_steps
+    e2e_value = job_rate(step.work(), world, e2e_ms, scale)
 
     peaks = load_peaks()
     line = {
