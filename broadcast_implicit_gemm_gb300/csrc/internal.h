@@ -217,9 +217,13 @@ struct DeviceState {
     int device = -1;
     int sm_count = 0;
     int max_smem_optin = 0;
-    int *err = nullptr;          // device word: sticky error flag
+    int *err = nullptr;          // device address of the sticky error word (a file-scope
+                                 // __device__ int, not an allocation)
 };
-DeviceState *device_state();     // current device; nullptr on failure
+// The current device's state; nullptr on failure.  Allocates nothing: the
+// first call on a device queries its attributes and looks up the address of
+// the error word (cudaGetSymbolAddress), so make it before any stream capture.
+DeviceState *device_state();
 unsigned long long wait_timeout_ns();
 
 // Profiling hooks: record events around a launch when enabled.

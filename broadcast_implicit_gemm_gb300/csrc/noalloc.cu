@@ -133,6 +133,10 @@ extern "C" bigemm_status conv2d_nchw_run_noalloc(int N, int H, int W, int CO, in
     int sms = 0;
     bigemm_status st = setup_device(dev, &scratch, &sms);
     if (st != BIGEMM_OK) return st;
+    // Without a caller's flag the kernels raise the library's sticky error word
+    // (itself a file-scope device variable, so this allocates nothing either).
+    DeviceState *ds = timeout_flag ? nullptr : device_state();
+    if (!timeout_flag && (!ds || !ds->err)) return BIGEMM_ERR_CUDA;
 
     // Tiling: 128 output pixels per tile as two 8x8 boxes, BN output channels,
     // K blocks of 128 bytes of channels per tap; split K when the tiles alone
@@ -159,29 +163,36 @@ extern "C" bigemm_status conv2d_nchw_run_noalloc(int N, int H, int W, int CO, in
     p.pix_tiles = (int)cdiv(p.total_boxes, t.bpt);
     p.co_tiles = (int)cdiv(CO, t.bn);
     const long long tiles = (long long)p.pix_tiles * p.co_tiles;
-    int split = 1;
-    if (tiles * 2 < sms && p.k_blocks >= 4)
-        split = (int)std::max(1ll, std::min(cdiv(sms, tiles), (long long)p.k_blocks / 2));
-    p.kb_per_split = (int)cdiv(p.k_blocks, split);
-    p.split = (int)cdiv(p.k_blocks, p.kb_per_split);
-    t.split = p.split;
-    if (tiles * p.split >= (1ll << 31)) return BIGEMM_ERR_UNSUPPORTED;
-    p.units = (int)(tiles * p.split);
-    p.epi = epi, p.eps = eps, p.bias = bias, p.out_dt = out_dtype;
     p.out_elems = (long long)N * CO * Ho * Wo;
-    p.timeout_ns = wait_timeout_ns();
 
-    // Scratch layout: [error word | channels-last data | packed kernel | partial sums].
+    // Scratch layout: [channels-last data | packed kernel | partial sums].
     const int ch = (int)cdiv(CI, 16 / e) * (16 / e);
-    const size_t off_x = 256;
+    const size_t off_x = 0;
     const size_t xh_bytes = (size_t)N * H * W * ch * e;
     const size_t off_w = off_x + round256(xh_bytes);
     const size_t wp_bytes = (size_t)CO * KH * KW * p.cip * e;
     const size_t off_ws = off_w + round256(wp_bytes);
-    const size_t ws_bytes = p.split > 1 ? (size_t)p.split * p.out_elems * sizeof(float) : 0;
-    if (off_ws + ws_bytes > kScratchBytes) return BIGEMM_ERR_UNSUPPORTED;
+    if (off_ws > kScratchBytes) return BIGEMM_ERR_UNSUPPORTED;
+    // K slices: enough to give most SMs a unit when the tiles alone would
+    // leave them idle, then fewer until the partial sums fit in what is left
+    // of the array (split 1 needs none).
+    const long long room = (long long)((kScratchBytes - off_ws) / sizeof(float));
+    int split = 1;
+    if (tiles * 2 < sms && p.k_blocks >= 4)
+        split = (int)std::max(1ll, std::min(cdiv(sms, tiles), (long long)p.k_blocks / 2));
+    for (;;) {
+        p.kb_per_split = (int)cdiv(p.k_blocks, split);
+        p.split = (int)cdiv(p.k_blocks, p.kb_per_split);
+        if (p.split == 1 || (long long)p.split * p.out_elems <= room) break;
+        split = p.split - 1;
+    }
+    t.split = p.split;
+    if (tiles * p.split >= (1ll << 31)) return BIGEMM_ERR_UNSUPPORTED;
+    p.units = (int)(tiles * p.split);
+    p.epi = epi, p.eps = eps, p.bias = bias, p.out_dt = out_dtype;
+    p.timeout_ns = wait_timeout_ns();
     unsigned char *base = static_cast<unsigned char *>(scratch);
-    int *err = timeout_flag ? timeout_flag : reinterpret_cast<int *>(base);
+    int *err = timeout_flag ? timeout_flag : ds->err;
     void *xh = base + off_x, *wp = base + off_w;
     float *ws = p.split > 1 ? reinterpret_cast<float *>(base + off_ws) : nullptr;
     p.err = err;
@@ -207,8 +218,6 @@ extern "C" bigemm_status conv2d_nchw_run_noalloc(int N, int H, int W, int CO, in
         return BIGEMM_ERR_UNSUPPORTED;
 
     cudaStream_t s = (cudaStream_t)stream;
-    if (!timeout_flag && cudaMemsetAsync(err, 0, sizeof(int), s) != cudaSuccess)
-        return BIGEMM_ERR_CUDA;
     if (launch_pack_nhwc(data, xh, N, CI, H * W, ch, in_dtype, s) != cudaSuccess)
         return BIGEMM_ERR_CUDA;
     const long long wtotal = (long long)CO * KH * KW * p.cip;

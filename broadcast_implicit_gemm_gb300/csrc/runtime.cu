@@ -16,6 +16,10 @@ namespace {
 
 std::mutex g_mu;
 DeviceState g_dev[64];
+// The sticky error word, one per device (every GPU that loads the library
+// holds its own copy, zero at load).  A file-scope device variable rather than
+// an allocation, so that the allocation-free entry point can raise it too.
+static __device__ int g_err_word;
 std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
 
 struct ProfRec {
@@ -88,12 +92,11 @@ DeviceState *device_state()
         return nullptr;
     if (cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
         return nullptr;
+    // the device address of g_err_word on this device (its name in host code
+    // is a host-side stand-in, not a device address)
     int *err = nullptr;
-    if (cudaMalloc(&err, sizeof(int)) != cudaSuccess) return nullptr;
-    if (cudaMemset(err, 0, sizeof(int)) != cudaSuccess) {
-        cudaFree(err);
+    if (cudaGetSymbolAddress(reinterpret_cast<void **>(&err), g_err_word) != cudaSuccess || !err)
         return nullptr;
-    }
     d.sm_count = sms;
     d.max_smem_optin = smem;
     d.err = err;

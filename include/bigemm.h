@@ -223,19 +223,22 @@ bigemm_status bcast_nchw_run_flat(int N, int C, int H, int W, int op, const floa
  * fixed array in the library's own device memory: 16 MiB (16777216 bytes),
  * held on every GPU that loads the library until the process exits.  The
  * scratch a shape needs is
- *   256 + r(N*H*W*Ch*e) + r(CO*KH*KW*cip*e) + S*N*CO*Ho*Wo*4 bytes,
+ *   r(N*H*W*Ch*e) + r(CO*KH*KW*cip*e) + S*N*CO*Ho*Wo*4 bytes,
  * where r() rounds up to 256, e is the input element size, Ch = CI rounded up
- * to 16/e, cip = CI rounded up to 128/e, and S is the number of K slices
- * (S = 1 unless the pixel tiles times the channel tiles cover less than half
- * the SMs).  Shapes that need more return BIGEMM_ERR_UNSUPPORTED before any
- * launch.
+ * to 16/e, cip = CI rounded up to 128/e, and S is the number of K slices.
+ * S = 1 unless the pixel tiles times the channel tiles cover less than half
+ * the SMs; then S is lowered, down to 1, until the partial sums fit.  Shapes
+ * whose data and kernel copies alone exceed 16 MiB return
+ * BIGEMM_ERR_UNSUPPORTED before any launch.
  *
  * Arguments and layouts are those of conv2d_nchw_plan + conv2d_nchw_run with
  * groups = 1 (data [N,CI,H,W], kernel [CO,CI,KH,KW], bias [CO] fp32, out
  * [N,CO,Ho,Wo], device pointers owned by the caller, 16-byte aligned;
  * stride <= 8).  timeout_flag is an optional device int the kernels set to 4
- * (BIGEMM_ERR_TIMEOUT) if a bounded device wait runs out; when NULL a word of
- * the scratch array takes its place and is cleared at every call.
+ * (BIGEMM_ERR_TIMEOUT) if a bounded device wait runs out (the caller clears
+ * it); when NULL the kernels raise the library's sticky device flag instead,
+ * which bigemm_last_device_error() reports and bigemm_clear_device_error()
+ * clears.  That flag is a file-scope device variable too, not an allocation.
  *
  * The call allocates nothing: no cudaMalloc, cudaFree or allocating library
  * routine.  The first call on a device looks up the device address of the
@@ -257,7 +260,10 @@ bigemm_status conv2d_nchw_run_noalloc(int N, int H, int W, int CO, int CI, int K
 const char *bigemm_status_string(bigemm_status s);
 
 /* Sticky device-side flag: BIGEMM_ERR_TIMEOUT once any kernel's bounded wait
- * ran out on the current device, else BIGEMM_OK.  Synchronises the device. */
+ * ran out on the current device (planned runs, broadcasts, and
+ * conv2d_nchw_run_noalloc calls given no timeout_flag), else BIGEMM_OK.
+ * Synchronises the device.  The flag is a file-scope device variable of the
+ * library (one per device, zero at load), so reading it allocates nothing. */
 bigemm_status bigemm_last_device_error(void);
 
 /* Clear the sticky device flag (synchronises the device). */

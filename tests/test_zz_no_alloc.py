@@ -1,13 +1,17 @@
-"""The allocation-free convolution entry point, checked against the planned one.
+"""The allocation-free convolution entry point, checked against the oracle and
+against the planned entry point.
 
-conv2d_nchw_run_noalloc is for callers that cannot allocate device memory
-(they cannot create a plan, which owns cudaMalloc'd scratch); it keeps its
-scratch in a fixed array inside the library.  These tests call it through the
-C ABI twice in a row -- different shapes and inputs, so stale scratch from the
-first call would show in the second -- and compare each output with
-conv2d_nchw_run on the same inputs.  Each of the two results is within
-tau * S of the exact convolution (S = sum |a*w|, from the CPU oracle), so they
-may differ by up to 2 * tau * S.  The file is collected last on purpose.
+conv2d_nchw_run_noalloc serves callers that cannot allocate device memory: code
+running where cudaMalloc is forbidden, or inside a memory budget that someone
+else fixed.  Such callers cannot create a plan, because a plan owns cudaMalloc'd
+scratch, so the call keeps its scratch in a fixed array inside the library.
+These tests call it through the C ABI twice in a row -- different shapes and
+inputs, so stale scratch from the first call would show in the second -- and
+compare each output element with the exact convolution from the CPU oracle
+within tau * S (S = sum |a*w|), and with conv2d_nchw_run on the same inputs
+within 2 * tau * S (each of the two is within tau * S of the exact result).
+The file is collected last on purpose: a run that stops at the first failure
+has then run every other test.
 """
 import numpy as np
 import pytest
@@ -21,6 +25,8 @@ from tests.tolerance import TAU, assert_within, conv_bound, epi_bound
 pytestmark = pytest.mark.gpu
 
 DT = {"f32": bg.F32, "f16": bg.F16, "bf16": bg.BF16}
+ORACLE_EPI = {"bias": oracle.EPI_BIAS, "bias_exp": oracle.EPI_BIAS_EXP,
+              "bias_rsqrt": oracle.EPI_BIAS_RSQRT, "bias_recip": oracle.EPI_BIAS_RECIP}
 
 CASES = [
     # fp32 (tf32 MMAs), N=1: few tiles, so the K dimension is split (partial sums in scratch)
@@ -30,52 +36,99 @@ CASES = [
                    "bias_exp"),
     # bf16, stride 2, ragged channels
     synth.ConvSpec("noalloc_bf16_s2", 3, 40, 72, 17, 17, 3, 2, 1, 1, "bf16", "bf16"),
+    # N=1, one tile and 36 K blocks: split K, then 1/(acc + bias) and fp16 rounding in the
+    # reduction pass (non-negative operands keep the argument away from zero)
+    synth.ConvSpec("noalloc_f16_split_recip", 1, 256, 128, 8, 8, 3, 1, 1, 1, "f16", "f16",
+                   "absnormal", "absnormal", "bias_recip"),
+    # split K with exp(acc + bias) rounded to bf16 in the reduction pass
+    synth.ConvSpec("noalloc_bf16_split_exp", 1, 192, 64, 7, 9, 3, 1, 1, 1, "bf16", "bf16",
+                   "uniform", "he", "bias_exp"),
+    # fp32 with an 11.8 MB kernel copy: the split the SM count asks for (60 slices of partial
+    # sums) does not fit beside it in the 16 MiB array, so the call takes fewer slices
+    synth.ConvSpec("noalloc_f32_split_lowered", 1, 640, 512, 7, 7, 3, 1, 1, 1, "f32", "f32",
+                   "uniform", "he"),
 ]
 
 
-def _outputs(spec, seed):
+def _inputs(spec, seed):
     x, w, b = synth.conv_inputs(spec, seed)
-    xd, wd = x.cuda(), w.cuda()
-    bd = b.cuda() if b is not None else None
-    Ho = bg.out_size(spec.H, spec.K, spec.stride, spec.pad)
-    Wo = bg.out_size(spec.W, spec.K, spec.stride, spec.pad)
-    odt = synth.TORCH_DTYPES[spec.out_dtype]
-    epi = bg.EPI_NAMES[spec.epi]
-    planned = torch.full((spec.N, spec.CO, Ho, Wo), float("nan"), dtype=odt, device="cuda")
+    return x, w, b, x.cuda(), w.cuda(), (b.cuda() if b is not None else None)
+
+
+def _out_shape(spec):
+    return (spec.N, spec.CO, bg.out_size(spec.H, spec.K, spec.stride, spec.pad),
+            bg.out_size(spec.W, spec.K, spec.stride, spec.pad))
+
+
+def _noalloc(spec, xd, wd, bd, flag):
+    out = torch.full(_out_shape(spec), float("nan"), dtype=synth.TORCH_DTYPES[spec.out_dtype],
+                     device="cuda")
+    bg.conv2d_nchw_run_noalloc(spec.N, spec.H, spec.W, spec.CO, spec.CI, spec.K, spec.K,
+                               spec.stride, spec.pad, DT[spec.in_dtype], DT[spec.out_dtype],
+                               bg.EPI_NAMES[spec.epi], xd, wd, bd, 1e-5, out, flag)
+    return out
+
+
+def _planned(spec, xd, wd, bd):
+    out = torch.full(_out_shape(spec), float("nan"), dtype=synth.TORCH_DTYPES[spec.out_dtype],
+                     device="cuda")
     plan = bg.conv2d_nchw_plan(spec.N, spec.H, spec.W, spec.CO, spec.CI, spec.K, spec.K,
                                spec.stride, spec.pad, 1, DT[spec.in_dtype], DT[spec.out_dtype],
-                               epi, 0)
-    bg.conv2d_nchw_run(plan, xd, wd, bd, 1e-5, planned)
-    free = torch.full_like(planned, float("nan"))
-    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
-    bg.conv2d_nchw_run_noalloc(spec.N, spec.H, spec.W, spec.CO, spec.CI, spec.K, spec.K,
-                               spec.stride, spec.pad, DT[spec.in_dtype], DT[spec.out_dtype], epi,
-                               xd, wd, bd, 1e-5, free, flag)
+                               bg.EPI_NAMES[spec.epi], 0)
+    bg.conv2d_nchw_run(plan, xd, wd, bd, 1e-5, out)
     torch.cuda.synchronize()
     plan.close()
-    assert flag.item() == 0, "a device wait timed out"
-    return x, w, b, planned.cpu().double().numpy(), free.cpu().double().numpy()
+    return out
 
 
-def _bound(spec, x, w, b):
-    tau = 2 * (TAU["tf32"] if spec.in_dtype == "f32" else TAU["half"])
+def _oracle(spec, x, w, b, scale):
+    """The exact result and the per-element bound at scale * tau."""
+    tau = scale * (TAU["tf32"] if spec.in_dtype == "f32" else TAU["half"])
     if spec.epi == "none":
         ref, sabs = oracle.conv2d_nchw(x, w, stride=spec.stride, pad=spec.pad, nthreads=8)
-        return conv_bound(ref, sabs, tau, spec.out_dtype)
+        return ref, conv_bound(ref, sabs, tau, spec.out_dtype)
     ref, sabs = oracle.conv2d_nchw(x, w, stride=spec.stride, pad=spec.pad, bias=b,
-                                   epi=oracle.EPI_BIAS_EXP, nthreads=8)
+                                   epi=ORACLE_EPI[spec.epi], nthreads=8)
     pre, _ = oracle.conv2d_nchw(x, w, stride=spec.stride, pad=spec.pad, nthreads=8)
     arg = pre + b.double().numpy().reshape(1, -1, 1, 1)
-    return epi_bound(arg, sabs, tau, spec.epi, spec.out_dtype, ref)
+    return ref, epi_bound(arg, sabs, tau, spec.epi, spec.out_dtype, ref)
 
 
-@pytest.mark.parametrize("first,second", [(0, 1), (1, 2), (2, 0)])
-def test_noalloc_matches_planned_run_on_two_calls_in_a_row(first, second):
-    for i, seed in ((first, 10 + first), (second, 20 + second)):
-        spec = CASES[i]
-        x, w, b, planned, free = _outputs(spec, seed)
-        assert not np.isnan(free).any(), f"{spec.name}: unwritten outputs"
-        assert_within(free, planned, _bound(spec, x, w, b), f"noalloc vs planned {spec.name}")
+def _check_call(spec, seed):
+    x, w, b, xd, wd, bd = _inputs(spec, seed)
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    free = _noalloc(spec, xd, wd, bd, flag)
+    torch.cuda.synchronize()
+    assert flag.item() == 0, "a device wait timed out"
+    got = free.cpu().double().numpy()
+    assert not np.isnan(got).any(), f"{spec.name}: unwritten outputs"
+    ref, bound = _oracle(spec, x, w, b, 1.0)
+    assert_within(got, ref, bound, f"noalloc vs oracle {spec.name}")
+    planned = _planned(spec, xd, wd, bd).cpu().double().numpy()
+    _, bound2 = _oracle(spec, x, w, b, 2.0)
+    assert_within(got, planned, bound2, f"noalloc vs planned {spec.name}")
+
+
+@pytest.mark.parametrize("first,second", [(0, 1), (1, 2), (2, 0), (3, 4), (4, 5), (5, 3)])
+def test_noalloc_matches_oracle_and_planned_run_on_two_calls_in_a_row(first, second):
+    _check_call(CASES[first], 10 + first)
+    _check_call(CASES[second], 20 + second)
+
+
+def test_noalloc_without_a_flag_reports_through_the_sticky_word():
+    """With timeout_flag NULL the kernels raise the library's sticky flag, which
+    the call never clears: a timeout recorded before it stays visible after it."""
+    spec = CASES[2]
+    _, _, _, xd, wd, bd = _inputs(spec, 5)
+    bg.bigemm_clear_device_error()
+    bg.bigemm_debug_wait_timeout(20_000)          # a bounded wait that runs out: flag set
+    torch.cuda.synchronize()
+    _noalloc(spec, xd, wd, bd, None)
+    assert bg.bigemm_last_device_error() == 4     # still reported after the no-alloc call
+    bg.bigemm_clear_device_error()
+    out = _noalloc(spec, xd, wd, bd, None)
+    assert bg.bigemm_last_device_error() == 0
+    assert not torch.isnan(out.float()).any()
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
