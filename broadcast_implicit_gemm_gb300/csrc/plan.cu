@@ -6,9 +6,14 @@
 // tilings (the analogue of its split knobs on f/y/x/rc and unroll options) is
 // enumerated; invalid points are rejected on the host before any launch
 // (its "invalid gpu kernel" records); each valid point is timed as three
-// repeats of back-to-back runs, each repeat lasting at least a minimum time
-// (its repeat / min_repeat_ms measure option); and the best record is kept per
-// workload, like its log of best configurations.
+// repeats of runs, each repeat lasting at least a minimum time (its repeat /
+// min_repeat_ms measure option); and the best record is kept per workload,
+// like its log of best configurations.  The candidates run on seeded non-zero
+// inputs, and where the problem's tensors fit in L2 each timed run starts
+// after an L2 flush, as in a step that reads its inputs from HBM.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
 #include <algorithm>
 #include <climits>
 #include <cstdint>
@@ -972,14 +977,48 @@ void append_cache_file(const std::string &key, const std::string &cand, double m
 struct SearchBuffers {
     void *x = nullptr, *w = nullptr, *o = nullptr;
     float *b = nullptr;
+    void *flush = nullptr;          // L2 flush buffer (null: the tensors exceed L2)
+    size_t flush_bytes = 0;
     ~SearchBuffers()
     {
         if (x) cudaFree(x);
         if (w) cudaFree(w);
         if (o) cudaFree(o);
         if (b) cudaFree(b);
+        if (flush) cudaFree(flush);
     }
 };
+
+// Search inputs: element i is a counter-based hash of (i, seed) -- the
+// splitmix64 output function (Steele, Lea and Flood, "Fast splittable
+// pseudorandom number generators", 2014) -- mapped to [-amp, amp] and stored
+// in the operand type.  Non-zero operands keep the tensor cores' power draw
+// (and so their clocks) as in real use; zeros would flatter every candidate.
+__global__ void search_fill(void *p, long long n, int dt, float amp, unsigned long long seed)
+{
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+         i += (long long)gridDim.x * blockDim.x) {
+        unsigned long long z = (unsigned long long)i + (seed + 1) * 0x9E3779B97F4A7C15ull;
+        z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+        z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+        z ^= z >> 31;
+        const float v = ((float)(z >> 40) * (2.0f / 16777216.0f) - 1.0f) * amp;
+        if (dt == BIGEMM_F32)
+            static_cast<float *>(p)[i] = v;
+        else if (dt == BIGEMM_F16)
+            static_cast<__half *>(p)[i] = __float2half_rn(v);
+        else
+            static_cast<__nv_bfloat16 *>(p)[i] = __float2bfloat16_rn(v);
+    }
+}
+
+cudaError_t fill_search_input(void *p, long long n, int dt, float amp, unsigned long long seed,
+                              int sms, cudaStream_t st)
+{
+    const int grid = (int)std::max(1ll, std::min(ceil_div(n, 256), (long long)sms * 8));
+    search_fill<<<grid, 256, 0, st>>>(p, n, dt, amp, seed);
+    return cudaGetLastError();
+}
 
 double min_repeat_ms()
 {
@@ -988,10 +1027,12 @@ double min_repeat_ms()
     return ms > 0 ? ms : 2.0;
 }
 
-// Time one candidate: three repeats, each of `number` back-to-back runs lasting
-// at least min_repeat_ms; cost = median of the repeat means.  status as in the
-// tutorial's measure records: 0 ok, 1 invalid (host check), 4 run error,
-// 6 device wait timed out.
+// Time one candidate: three repeats, each of `number` runs lasting at least
+// min_repeat_ms; cost = median of the repeat means.  Without an L2 flush the
+// runs of a repeat go back to back between two events; with one, every run
+// is timed on its own between events, after a flush that lies outside them.
+// status as in the tutorial's measure records: 0 ok, 1 invalid (host check),
+// 4 run error, 6 device wait timed out.
 int time_candidate(const ConvShape &s, const Cand &c, int sms, SearchBuffers &sb,
                    cudaStream_t st, double *ms_out, std::string *why)
 {
@@ -1006,28 +1047,50 @@ int time_candidate(const ConvShape &s, const Cand &c, int sms, SearchBuffers &sb
     cudaEventCreate(&a);
     cudaEventCreate(&b);
     auto once = [&]() { return run_plan(p, sb.x, sb.w, sb.b, 1e-5f, sb.o, st); };
+    auto flush = [&]() {
+        return sb.flush ? cudaMemsetAsync(sb.flush, 0, sb.flush_bytes, st) : cudaSuccess;
+    };
+    // one run between events (after a flush when there is one); its time in ms, < 0 on failure
+    auto timed_once = [&]() -> float {
+        if (flush() != cudaSuccess) return -1.f;
+        cudaEventRecord(a, st);
+        if (once() != BIGEMM_OK) return -1.f;
+        cudaEventRecord(b, st);
+        if (cudaEventSynchronize(b) != cudaSuccess) return -1.f;
+        float t = 0;
+        cudaEventElapsedTime(&t, a, b);
+        return t;
+    };
     do {
         if (once() != BIGEMM_OK || cudaStreamSynchronize(st) != cudaSuccess) {
             status = 4;
             break;
         }
-        cudaEventRecord(a, st);
-        if (once() != BIGEMM_OK) { status = 4; break; }
-        cudaEventRecord(b, st);
-        if (cudaEventSynchronize(b) != cudaSuccess) { status = 4; break; }
-        float one = 0;
-        cudaEventElapsedTime(&one, a, b);
+        const float one = timed_once();
+        if (one < 0) { status = 4; break; }
         const double target = min_repeat_ms();
-        int number = (int)std::min(10000.0, std::max(1.0, std::ceil(target / std::max(one, 1e-4f))));
+        const int cap = sb.flush ? 64 : 10000;
+        const int number =
+            (int)std::min((double)cap, std::max(1.0, std::ceil(target / std::max(one, 1e-4f))));
         double rep[3];
         for (int r = 0; r < 3 && status == 0; ++r) {
-            cudaEventRecord(a, st);
-            for (int i = 0; i < number; ++i)
-                if (once() != BIGEMM_OK) { status = 4; break; }
-            cudaEventRecord(b, st);
-            if (cudaEventSynchronize(b) != cudaSuccess) { status = 4; break; }
-            float tot = 0;
-            cudaEventElapsedTime(&tot, a, b);
+            double tot = 0;
+            if (sb.flush) {
+                for (int i = 0; i < number; ++i) {
+                    const float t = timed_once();
+                    if (t < 0) { status = 4; break; }
+                    tot += t;
+                }
+            } else {
+                cudaEventRecord(a, st);
+                for (int i = 0; i < number; ++i)
+                    if (once() != BIGEMM_OK) { status = 4; break; }
+                cudaEventRecord(b, st);
+                if (cudaEventSynchronize(b) != cudaSuccess) { status = 4; break; }
+                float t = 0;
+                cudaEventElapsedTime(&t, a, b);
+                tot = t;
+            }
             rep[r] = tot / number;
         }
         if (status) break;
@@ -1051,15 +1114,32 @@ bigemm_status search(const ConvShape &s, int sms, cudaStream_t st, Cand *best, s
 {
     SearchBuffers sb;
     const size_t e = dtype_size(s.in_dt);
-    const size_t xb = (size_t)s.N * s.CI * s.H * s.W * e;
-    const size_t wb = (size_t)s.CO * (s.CI / s.groups) * s.KH * s.KW * e;
+    const long long xn = (long long)s.N * s.CI * s.H * s.W;
+    const long long wn = (long long)s.CO * (s.CI / s.groups) * s.KH * s.KW;
+    const size_t xb = (size_t)xn * e, wb = (size_t)wn * e;
     const size_t ob = (size_t)s.N * s.CO * s.Ho * s.Wo * dtype_size(s.out_dt);
     if (cudaMalloc(&sb.x, xb) != cudaSuccess || cudaMalloc(&sb.w, wb) != cudaSuccess ||
         cudaMalloc(&sb.o, ob) != cudaSuccess || cudaMalloc(&sb.b, s.CO * sizeof(float)) != cudaSuccess)
         return BIGEMM_ERR_CUDA;
-    cudaMemsetAsync(sb.x, 0, xb, st);
-    cudaMemsetAsync(sb.w, 0, wb, st);
-    cudaMemsetAsync(sb.b, 0, s.CO * sizeof(float), st);
+    // inputs like the ones a layer sees: data in [-1, 1], kernel of variance
+    // about 2/fan_in, bias in [-1, 1]
+    const float fan = (float)((s.CI / s.groups) * s.KH * s.KW);
+    if (fill_search_input(sb.x, xn, s.in_dt, 1.0f, 1, sms, st) != cudaSuccess ||
+        fill_search_input(sb.w, wn, s.in_dt, sqrtf(6.0f / fan), 2, sms, st) != cudaSuccess ||
+        fill_search_input(sb.b, s.CO, BIGEMM_F32, 1.0f, 3, sms, st) != cudaSuccess)
+        return BIGEMM_ERR_CUDA;
+    // An L2 flush before every timed run when the tensors would otherwise stay
+    // in L2 between runs: twice the L2 size, written with a memset.
+    int dev = 0, l2 = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) == cudaSuccess && l2 > 0 &&
+        xb + wb + ob < 2 * (size_t)l2) {
+        sb.flush_bytes = 2 * (size_t)l2;
+        if (cudaMalloc(&sb.flush, sb.flush_bytes) != cudaSuccess) {
+            sb.flush = nullptr;
+            return BIGEMM_ERR_CUDA;
+        }
+    }
     if (cudaStreamSynchronize(st) != cudaSuccess) return BIGEMM_ERR_CUDA;
     double best_ms = 1e30;
     int best_i = -1;
