@@ -55,6 +55,7 @@ def test_bcast_small(shape, op, dt):
     out2 = torch.full_like(out, 7.0)
     bg.bcast_nchw_run_flat(N, C, H, W, OPS[op], var.cuda(), 1e-5, out2, bg.DTYPE_CODES[dt])
     torch.cuda.synchronize()
+    check_planes(out2, var, op, dt)       # the flat schedule against the oracle itself
     assert torch.equal(torch.nan_to_num(out, 1.0), torch.nan_to_num(out2, 1.0))
 
 
@@ -68,6 +69,18 @@ def test_bcast_full_size(op):
     check_planes(out, var, op, "f32")
     if op == "rsqrt":   # var ~ U[-2,2]: about half the channels are NaN
         assert 0.3 < torch.isnan(out[0, :, 0, 0]).float().mean().item() < 0.7
+
+
+@pytest.mark.parametrize("op", list(OPS))
+def test_bcast_flat_full_size(op):
+    # the fused-flat-index schedule (one flat loop, op(var[c]) recomputed per
+    # element) at the benchmark's size, against the oracle
+    N, C, H, W = synth.BCAST_SHAPE
+    var = synth.bcast_var(C, seed=3)
+    out = torch.full((N, C, H, W), 7.0, dtype=torch.float32, device="cuda")
+    bg.bcast_nchw_run_flat(N, C, H, W, OPS[op], var.cuda(), synth.BCAST_EPS, out, bg.F32)
+    torch.cuda.synchronize()
+    check_planes(out, var, op, "f32")
 
 
 def test_bcast_unaligned_output_pointer():

@@ -578,6 +578,41 @@ def test_search_picks_a_timed_candidate_and_caches_it():
     again.close()
 
 
+_PLAN_LOG_CHILD = """
+import sys
+sys.path.insert(0, {root!r})
+import broadcast_implicit_gemm_gb300 as bg
+p = bg.conv2d_nchw_plan(2, 13, 15, 72, 48, 3, 3, 1, 1, 1, bg.F16, bg.F32, bg.EPI_BIAS, 1)
+d = p.describe()
+print("PLAN", d["chosen_by"], d["cand"])
+"""
+
+
+def _plan_in_fresh_process(log_path):
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, BIGEMM_PLAN_CACHE=str(log_path))
+    r = subprocess.run([sys.executable, "-c", _PLAN_LOG_CHILD.format(root=root)], env=env,
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = [ln for ln in r.stdout.splitlines() if ln.startswith("PLAN ")][-1]
+    return line.split()[1:]
+
+
+def test_plan_log_round_trip(tmp_path):
+    # The tuning-log flow: a search writes its best record to the JSONL log
+    # (BIGEMM_PLAN_CACHE); a later process with the same log takes the plan
+    # from it without searching.
+    log = tmp_path / "plans.jsonl"
+    chosen_by, cand = _plan_in_fresh_process(log)
+    assert chosen_by == "search"
+    lines = log.read_text().splitlines()
+    assert len(lines) == 1 and f'"cand": "{cand}"' in lines[0] and "|N2|H13|W15|CO72|CI48|" in lines[0]
+    assert _plan_in_fresh_process(log) == ["cache", cand]
+    assert len(log.read_text().splitlines()) == 1      # a cache hit appends nothing
+
+
 def test_forced_invalid_tiling_is_rejected_before_launch():
     with pytest.raises(bg.BigemmError) as e:
         bg.conv2d_nchw_plan_ex(1, 8, 8, 64, 64, 3, 3, 1, 1, 1, bg.F16, bg.F16, bg.EPI_NONE, 0,
@@ -613,12 +648,15 @@ EPI16 = [
 ]
 
 
-@pytest.mark.parametrize("resident", [0, 1])
-@pytest.mark.parametrize("case", EPI16, ids=lambda c: c[0].name)
+# each case with streamed weights, and with resident weights where they can stay
+# (split 1 and a tile's weights within shared memory)
+EPI16_RUNS = [(c, r) for c in EPI16 for r in ((0, 1) if c[2] != -1 else (0,))]
+
+
+@pytest.mark.parametrize("case,resident", EPI16_RUNS,
+                         ids=lambda v: v[0].name if isinstance(v, tuple) else f"res{v}")
 def test_sixteen_epilogue_warps(case, resident):
     spec, mode, res, split = case
-    if res == -1 and resident:
-        pytest.skip("split K, or weights too large to stay resident")
     opts = {"kind": bg.KIND_UMMA, "mode": mode, "tile_n": 128, "split_k": split, "epi_warps": 16,
             "resident_b": 1 if resident else -1}
     info = check(spec, opts)
