@@ -2,9 +2,10 @@
 
 conv:  |gpu - ref| <= tau * S + u_out * |ref|, S = sum |a*w| (from the oracle),
        tau = 2e-3 (TF32 operands), 4e-3 (fp16/bf16 operands, fp32 accumulate),
-       1e-5 (fp32 operands on the FP32 pipes).  u_out is the output type's unit
-       roundoff (2^-24 fp32, 2^-11 fp16, 2^-8 bf16): the rounding of the stored
-       result, which for bf16 alone would fill the 4e-3 budget.
+       1e-5 (fp32 operands on the FP32 pipes).  u_out is 2^-8 for bf16 outputs
+       (the rounding of the stored result, which alone would fill the 4e-3
+       budget) and 0 for fp32 and fp16 outputs, whose rounding (at most
+       2^-24 |ref| and 2^-11 |ref|, with |ref| <= S) the tau * S term holds.
 epilogue f(acc + bias):  the conv bound propagated through f, i.e. the largest
        |f(t) - f(arg)| for |t - arg| <= tau*S + |arg|*2^-23, plus 4 ulp of the output
        type (f's own rounding, <= 2 ulp, and the final store).
@@ -27,8 +28,12 @@ def ulp(x, out_dtype):
     return 2.0 ** (e - 7)
 
 
+# output rounding allowed on top of tau * S: bf16 only
+U_OUT = {"f32": 0.0, "f16": 0.0, "bf16": 2.0 ** -8}
+
+
 def conv_bound(ref, sabs, tau, out_dtype):
-    return tau * sabs + UNIT[out_dtype] * np.abs(ref) + 1e-30
+    return tau * sabs + U_OUT[out_dtype] * np.abs(ref) + 1e-30
 
 
 def epi_bound(arg, sabs, tau, epi, out_dtype, ref, eps=1e-5):
