@@ -1,12 +1,16 @@
 #!/usr/bin/env python3
 """Benchmark: NCHW conv2d TFLOP/s (and the broadcast's GB/s) on one GB300.
 
-Default workload: the fp32 batch-1 layer sweep, five layers
-(CI,CO,H,W,K,stride,pad) = (64,64,56,56,3,1,1), (128,128,28,28,3,1,1),
-(256,256,14,14,3,1,1), (256,512,14,14,3,2,1), (1024,256,14,14,1,1,0).  One
-step runs every layer once through the C ABI; the metric is the step's total
-FLOP over its device time.  Other workloads: --workload resnet_last |
-resnet50_fp16 | fused | depthwise_fp16 | bcast.
+Headline workload (the default line): the five ResNet-50 bottleneck layers at
+N=256, fp16 in / fp32 accumulate / fp16 out, (CI,CO,H,W,K,stride,pad) =
+(64,64,56,56,1,1,0), (64,64,56,56,3,1,1), (64,256,56,56,1,1,0),
+(512,512,7,7,3,1,1), (256,512,28,28,1,2,0).  One step runs every layer once
+through the C ABI; the metric is the step's total FLOP over its device time.
+The same run then measures the other workloads and reports each under
+"workloads" on the same line: the fused 3x3 conv + exp(conv + bias) (N=32),
+the [128,256,32,32] broadcast (with its A/B against the flat schedule and the
+general [B0,P,B1] form), the depthwise layers (N=64), the fp32 batch-1 layer
+sweep and the N=1 512->512 7x7 layer.  --workload W --only measures one.
 
 Timing: W untimed warm-up steps; K timed steps, each bracketed by CUDA events
 on the launch stream, with an L2 flush (a 512 MB write) between steps outside
@@ -32,6 +36,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -115,17 +120,20 @@ class ClockSampler:
         except Exception:
             pass
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        self.f = tempfile.NamedTemporaryFile("w+", prefix="bench_clocks_", suffix=".csv")
 
     def start(self):
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
-            self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
                                           "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+            return
+        # the first sample lands before the timed region starts
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < 3.0 and os.path.getsize(self.f.name) == 0:
+            time.sleep(0.02)
 
     def stop(self):
         if self.proc is None:
@@ -136,10 +144,13 @@ class ClockSampler:
             self.proc.wait(5)
         except Exception:
             self.proc.kill()
+        self.f.flush()
+        self.f.seek(0)
+        rows = self.f.read().splitlines()
         self.f.close()
         sm, smax, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.path):
+        for line in rows:
             parts = [x.strip() for x in line.split(",")]
             if len(parts) < 9:
                 continue
@@ -368,7 +379,7 @@ def kernel_work(name, it):
     return None
 
 
-def kernel_roofline(name, prof, step, peaks, args):
+def kernel_roofline(name, prof, step, peaks, args, workload):
     """Roofline of kernel `name`: its algorithmic work per launch over its mean launch time."""
     n, tms = prof[name]
     works = [(kernel_work(name, it), it) for it in step.items]
@@ -392,7 +403,7 @@ def kernel_roofline(name, prof, step, peaks, args):
     r.update({"kernel": name, "launches": n, "avg_launch_us": per_launch_s * 1e6,
               "flop_per_launch": flop, "bytes_per_launch": byts,
               "roofline_frac": max(t_flop, t_byte) / per_launch_s,
-              "traffic": traffic_for(name, args.workload)})
+              "traffic": traffic_for(name, workload)})
     return r
 
 
@@ -432,8 +443,12 @@ def cpu_baseline(workload, specs, budget_s=12.0):
             break
     dt = (time.perf_counter() - t0) / reps
     names = ", ".join(s.name for s, _ in sample)
+    note = ""
+    if any(s.N > 2 for s in specs):
+        note = (f"; layers of batch {max(s.N for s in specs)} timed at N=1 (the oracle's time "
+                f"grows linearly in N, so its TFLOP/s rate is the full batch's)")
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-            "sample": f"{len(sample)} layers ({names}); {reps} passes of {dt * 1e3:.1f} ms"}
+            "sample": f"{len(sample)} layers ({names}); {reps} passes of {dt * 1e3:.1f} ms{note}"}
 
 
 def reduce_max(value, dist, device):
@@ -496,58 +511,34 @@ def run_reference(args, world, rank):
     return 0
 
 
-def main():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--workload", default="sweep_fp32",
-                    choices=["sweep_fp32", "resnet_last", "resnet50_fp16", "fused",
-                             "depthwise_fp16", "bcast"])
-    ap.add_argument("--layer", default=None, help="run only the named layer of the workload")
-    ap.add_argument("--no-search", action="store_true", help="heuristic plans, no timed search")
-    ap.add_argument("--batch", type=int, default=0,
-                    help="override the workload's batch size (smaller cases for profiling; "
-                         "the line's config records it)")
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    args = ap.parse_args()
-    args.warmup = max(args.warmup, 3)
-    world, rank, local, dist = dist_setup(args)
-    if args.impl == "reference":
-        rc = run_reference(args, world, rank)
-        if dist:
-            dist.destroy_process_group()
-        return rc
+def warm(step_fn, n, torch, stream):
+    for _ in range(n):
+        with torch.cuda.stream(stream):
+            step_fn(stream)
+    torch.cuda.synchronize()
 
+
+def measure(name, args, device, stream, flush, peaks, world, dist, local):
+    """One workload: plans, warm-up, the timed pass, the profiled pass, the
+    end-to-end pass.  Returns the fields of its JSON line."""
     import torch
 
     import broadcast_implicit_gemm_gb300 as bg
-    from broadcast_implicit_gemm_gb300 import synth
-    device = torch.device("cuda", local)
-    torch.cuda.set_device(device)
-    stream = torch.cuda.Stream(device)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
-
-    if args.workload == "bcast":
+    if name == "bcast":
         step = BcastStep(device)
         unit, scale = "GB/s", 1e9
     else:
-        specs = workload_specs(args.workload)
+        specs = workload_specs(name)
         if args.layer:
             specs = [x for x in specs if x.name == args.layer]
             if not specs:
-                raise SystemExit(f"no layer {args.layer} in {args.workload}")
+                raise SystemExit(f"no layer {args.layer} in {name}")
         if args.batch:
             specs = [x.with_batch(args.batch) for x in specs]
         step = ConvStep(specs, device, search=0 if args.no_search else 1)
         unit, scale = "TFLOP/s", 1e12
 
-    for _ in range(args.warmup):
-        with torch.cuda.stream(stream):
-            step.run(stream)
-    torch.cuda.synchronize()
-
+    warm(step.run, args.warmup, torch, stream)
     clocks = ClockSampler(local)
     clocks.start()
     if dist:
@@ -569,33 +560,27 @@ def main():
         dist.barrier()
     clk = clocks.stop()
     if bg.bigemm_last_device_error() != 0:
-        raise SystemExit("a device wait timed out during the timed region")
+        raise SystemExit(f"a device wait timed out during the timed region of {name}")
 
     total_ms = reduce_max(sum(times), dist, device)   # the slowest rank's time
     ms_per_step = total_ms / args.steps
     value = job_rate(step.work(), world, ms_per_step, scale)
 
     # end to end through the public call, host buffers in and out
-    for _ in range(2):
-        with torch.cuda.stream(stream):
-            step.run_e2e(stream)
-    torch.cuda.synchronize()
+    warm(step.run_e2e, 2, torch, stream)
     e2e_steps = max(3, min(args.steps, 20))
     e2e_times, _ = timed_steps(step.run_e2e, e2e_steps, torch, stream, flush)
     e2e_ms = reduce_max(sum(e2e_times), dist, device) / e2e_steps
     e2e_value = job_rate(step.work(), world, e2e_ms, scale)
 
-    peaks = load_peaks()
     line = {
-        "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "data": "synthetic",
+        "value": value, "unit": unit, "ms_per_step": ms_per_step,
         "gpu_launches": sum(v[0] for v in prof.values()), "clocks": clk,
         "profiled_ms_per_step": sum(ptimes) / args.steps,
         "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": step.h2d_bytes(),
                 "d2h_bytes_per_step": step.d2h_bytes(), "ms_per_step": e2e_ms},
     }
-    if args.workload == "bcast":
+    if name == "bcast":
         line["dtype"] = "f32"
         line["config"] = {"workload": "bcast_exp_[128,256,32,32]_fp32", "op": "exp",
                           "l2": "output (134 MB) larger than L2; 512 MB flush between steps"}
@@ -608,9 +593,7 @@ def main():
             res = {}
             for flat in (False, True):
                 fn = (lambda st, o=op, f=flat: step.run_op(st, o, f))
-                for _ in range(3):
-                    with torch.cuda.stream(stream):
-                        fn(stream)
+                warm(fn, 3, torch, stream)
                 tt, _ = timed_steps(fn, max(5, min(args.steps, 20)), torch, stream, flush)
                 res["flat" if flat else "per_channel"] = step.work() / (sum(tt) / len(tt) / 1e3) / 1e9
             ab[opname] = {"per_channel_gbs": res["per_channel"], "flat_gbs": res["flat"],
@@ -619,14 +602,12 @@ def main():
         # the general form [1,P,1] => [B0,P,B1] (bcast_run), exp to fp32, on
         # short, single-element and long rows
         gen = []
-        for B0, P, B1 in synth.BCAST_GENERAL:
-            gvar = synth.bcast_var(P, seed=1).to(device)
+        for B0, P, B1 in synth_bcast_general():
+            gvar = bcast_var_dev(P, device)
             gout = torch.empty((B0, P, B1), dtype=torch.float32, device=device)
             fn = (lambda st, a=(B0, P, B1), v=gvar, o=gout:
                   bg.bcast_run(*a, bg.BC_EXP, v, 1e-5, o, bg.F32, st))
-            for _ in range(3):
-                with torch.cuda.stream(stream):
-                    fn(stream)
+            warm(fn, 3, torch, stream)
             tt, _ = timed_steps(fn, max(5, min(args.steps, 20)), torch, stream, flush)
             gbs = (gout.numel() * 4 + P * 4) / (sum(tt) / len(tt) / 1e3) / 1e9
             gen.append({"shape": [B0, P, B1], "gbs": gbs, "frac": gbs / peaks["hbm"],
@@ -637,12 +618,12 @@ def main():
                             "frac": ach / peaks["hbm"], "kernel": "bcast_nchw", "launches": n,
                             "avg_launch_us": tms / n * 1e3,
                             "peak_source": peaks["source"] + " copy bandwidth",
-                            "traffic": traffic_for("bcast_nchw", args.workload)}
+                            "traffic": traffic_for("bcast_nchw", name)}
     else:
         kinds = sorted({it["info"]["kind"] for it in step.items})
         in_dt = step.items[0]["spec"].in_dtype
         line["dtype"] = "tf32" if in_dt == "f32" and kinds == ["umma"] else in_dt
-        line["config"] = {"workload": args.workload,
+        line["config"] = {"workload": name,
                           "layers": [it["spec"].name for it in step.items],
                           "batch": step.items[0]["spec"].N,
                           "plans": [it["info"]["cand"] for it in step.items],
@@ -671,13 +652,88 @@ def main():
                               "bound": ("tensor" if it["info"]["kind"] == "umma" else "alu")
                               if t_flop >= t_byte else "hbm"})
         line["per_layer"] = per_layer
+        # the whole step against its roofline: the sum of the layers' roofline times
+        line["step_roofline_frac"] = (sum(p["roofline_us"] for p in per_layer) / 1e3
+                                      / ms_per_step)
         if prof:
             dominant = max(prof.items(), key=lambda kv: kv[1][1])[0]
-            line["roofline"] = kernel_roofline(dominant, prof, step, peaks, args)
+            line["roofline"] = kernel_roofline(dominant, prof, step, peaks, args, name)
         line["kernels"] = {k: {"launches": v[0], "ms": v[1]} for k, v in prof.items()}
+    line["_specs"] = None if name == "bcast" else step.specs
+    del step
+    torch.cuda.empty_cache()
+    return line
+
+
+def synth_bcast_general():
+    from broadcast_implicit_gemm_gb300 import synth
+    return synth.BCAST_GENERAL
+
+
+def bcast_var_dev(P, device):
+    from broadcast_implicit_gemm_gb300 import synth
+    return synth.bcast_var(P, seed=1).to(device)
+
+
+HEADLINE = "resnet50_fp16"
+# The other workloads, measured after the headline in the default run and
+# reported under "workloads" on the same line.
+EXTRAS = ["fused", "bcast", "depthwise_fp16", "sweep_fp32", "resnet_last"]
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default=HEADLINE,
+                    choices=["sweep_fp32", "resnet_last", "resnet50_fp16", "fused",
+                             "depthwise_fp16", "bcast"])
+    ap.add_argument("--only", action="store_true",
+                    help="measure the named workload alone (no other workloads on the line)")
+    ap.add_argument("--layer", default=None, help="run only the named layer of the workload")
+    ap.add_argument("--no-search", action="store_true", help="heuristic plans, no timed search")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's batch size (smaller cases for profiling; "
+                         "the line's config records it)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world, rank, local, dist = dist_setup(args)
+    if args.impl == "reference":
+        rc = run_reference(args, world, rank)
+        if dist:
+            dist.destroy_process_group()
+        return rc
+
+    import torch
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    stream = torch.cuda.Stream(device)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    peaks = load_peaks()
+
+    head = measure(args.workload, args, device, stream, flush, peaks, world, dist, local)
+    specs = head.pop("_specs")
+    line = {
+        "metric": METRIC, "value": head.pop("value"), "unit": head.pop("unit"), "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": head.pop("ms_per_step"),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "data": "synthetic",
+    }
+    line.update(head)
+    extras = []
+    if not (args.only or args.layer or args.batch) and args.workload == HEADLINE:
+        extras = EXTRAS
+    if extras:
+        line["workloads"] = {}
+        for name in extras:
+            w = measure(name, args, device, stream, flush, peaks, world, dist, local)
+            w.pop("_specs")
+            line["workloads"][name] = w
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(args.workload,
-                                            None if args.workload == "bcast" else step.specs)
+        line["cpu_baseline"] = cpu_baseline(args.workload, specs)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist:
