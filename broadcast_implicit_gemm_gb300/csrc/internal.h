@@ -35,6 +35,9 @@ enum AMode {
     A_NHWC = 0,     // packed channels-last copy of data, K-major, 4-D box per tap
     A_DIRECT = 1,   // 1x1 / stride 1 / pad 0: data read in place as [CI][H*W], MN-major
     A_HALO = 2,     // stride 1, K x K: one halo box per channel block serves every tap
+    A_STRIDED = 3,  // 1x1 / stride 2 / pad 0, 16-bit: data read in place as rows of 2W
+                    // elements (an even and an odd input row), the pixels the conv
+                    // reads kept by compaction warps into an MN-major operand
 };
 
 // How the pack lays the data out for the A_NHWC / A_HALO kernels.
@@ -150,6 +153,21 @@ cudaError_t launch_umma_add(int amode, int fmt, int bn, bool epi16, const UmmaPa
 cudaError_t launch_umma_res(int amode, int fmt, int bn, bool epi16, const UmmaParams &p,
                             const CUtensorMap &map_a, const CUtensorMap &map_b,
                             const CUtensorMap &map_c, int grid, cudaStream_t stream);
+
+// The strided-mode kernels (strided_conv.cu, strided_plain.cu): the
+// shared-memory layout for a tile of bn output channels, written into p's
+// layout fields (false when it does not fit in smem_limit bytes); its size
+// without a limit; the launch with every output form, and the one narrowed to
+// 16-bit outputs with no epilogue op (tma: written by TMA stores, else from
+// registers).  fmt 0 f16, 1 bf16.
+bool strided_layout(int bn, int smem_limit, UmmaParams &p);
+size_t strided_smem_bytes(int bn);
+cudaError_t launch_strided_conv(int bn, int fmt, const UmmaParams &p, const CUtensorMap &map_a,
+                                const CUtensorMap &map_b, const CUtensorMap &map_c, int grid,
+                                cudaStream_t stream);
+cudaError_t launch_strided_plain(int bn, int fmt, bool tma, const UmmaParams &p,
+                                 const CUtensorMap &map_a, const CUtensorMap &map_b,
+                                 const CUtensorMap &map_c, int grid, cudaStream_t stream);
 
 // -------------------------------------------------------------- other kernels
 cudaError_t launch_pack_nhwc(const void *x, void *xh, int N, int C, int HW, int Ch, int dt,

@@ -45,12 +45,17 @@ struct Cand {
     UmmaTiling t{};
 };
 
+const char *amode_name(int amode)
+{
+    return amode == A_DIRECT ? "direct" : amode == A_HALO ? "halo" : amode == A_STRIDED ? "strided" : "nhwc";
+}
+
 std::string cand_str(const Cand &c)
 {
     char b[160];
     if (c.kind == BIGEMM_KIND_UMMA)
         snprintf(b, sizeof b, "umma:%s:bn%d:box%dx%dx%d:split%d%s%s%s",
-                 c.t.amode == A_DIRECT ? "direct" : c.t.amode == A_HALO ? "halo" : "nhwc", c.t.bn,
+                 amode_name(c.t.amode), c.t.bn,
                  c.t.box_w, c.t.box_h, c.t.bpt, c.t.split,
                  c.t.pack == PACK_SUB ? ":sub" : c.t.pack == PACK_STACK ? ":stack" : "",
                  c.t.bres ? ":bres" : "", c.t.epi16 ? ":e16" : "");
@@ -76,9 +81,10 @@ bool parse_cand(const std::string &s, Cand &c)
     if (got >= 6 && got <= 9) {
         c = Cand{};
         c.kind = BIGEMM_KIND_UMMA;
-        c.t.amode = strcmp(mode, "direct") == 0 ? A_DIRECT
-                    : strcmp(mode, "halo") == 0   ? A_HALO
-                                                  : A_NHWC;
+        c.t.amode = strcmp(mode, "direct") == 0    ? A_DIRECT
+                    : strcmp(mode, "halo") == 0    ? A_HALO
+                    : strcmp(mode, "strided") == 0 ? A_STRIDED
+                                                   : A_NHWC;
         c.t.pack = strcmp(layout, "sub") == 0 ? PACK_SUB : strcmp(layout, "stack") == 0 ? PACK_STACK
                                                                                        : PACK_PLAIN;
         c.t.bres = strcmp(layout, "bres") == 0 || strcmp(layout2, "bres") == 0;
@@ -209,6 +215,14 @@ UmmaGeom umma_geometry(const ConvShape &s0, const UmmaTiling &t, int sm_count)
         p.k_blocks = (t.amode == A_HALO ? 1 : s.KH * s.KW) * p.ci_blocks;
         g.cip = p.ci_blocks * p.bk;
         g.ch = (int)ceil_div(s.CI, 16 / e) * (16 / e);
+    } else if (t.amode == A_STRIDED) {
+        // boxes of box_w x box_h output pixels over the [Ho][Wo] output
+        p.boxes_x = (int)ceil_div(s.Wo, t.box_w);
+        p.boxes_y = (int)ceil_div(s.Ho, t.box_h);
+        bpi = (long long)p.boxes_x * p.boxes_y;
+        p.k_blocks = p.ci_blocks;
+        g.cip = s.CI;
+        g.ch = s.CI;
     } else {
         p.boxes_x = 1, p.boxes_y = 1;
         bpi = ceil_div((long long)s.H * s.W, t.box_w);
@@ -237,6 +251,8 @@ UmmaGeom umma_geometry(const ConvShape &s0, const UmmaTiling &t, int sm_count)
         // shared-memory layout: streamed or resident weights
         g.fits = g.fits && halo_layout(t.bn, t.bres != 0, t.box_h, s.KH, s.KH * s.KW, p.ci_blocks,
                                        limit, p);
+    } else if (t.amode == A_STRIDED) {
+        g.fits = g.fits && strided_layout(t.bn, limit, p);
     } else if (t.bres) {
         // resident weights of one output-channel tile, every K block
         g.fits = g.fits && main_res_layout(t.bn, p.k_blocks, limit, p);
@@ -281,6 +297,18 @@ bool umma_valid(const ConvShape &s0, const UmmaTiling &t, int sm_count, std::str
         if ((s.CI * e) % 16) return bad("CI row not 16-byte multiple");
         if (t.box_w != (int)(128 / e) || t.box_h != 1 || t.bpt * t.box_w != 128)
             return bad("direct box must be one 128-byte row of pixels");
+    } else if (t.amode == A_STRIDED) {
+        if (s.KH != 1 || s.KW != 1 || s.stride != 2 || s.pad != 0)
+            return bad("strided mode needs 1x1 / stride 2 / pad 0");
+        // MN-major operand (tf32 MMAs take K-major operands only)
+        if (s.in_dt == BIGEMM_F32) return bad("strided mode needs 16-bit operands");
+        // rows of 2W elements (an even input row and the odd one below it) are
+        // the TMA rows: 16-byte multiples, and H a whole number of such pairs
+        if (s.H % 2 || (2LL * s.W * e) % 16) return bad("strided mode needs even H and 2W*e a 16-byte multiple");
+        if ((s.CI * e) % 16) return bad("CI row not 16-byte multiple");
+        if (t.box_w != 16 || t.box_h != 4 || t.bpt != 2) return bad("strided boxes are 16 x 4 pixels, two per tile");
+        if (t.bres || t.epi16) return bad("strided mode streams its weights with 8 epilogue warps");
+        if (!umma_geometry(s0, t, 1).fits) return bad("strided buffers exceed shared memory");
     } else if (t.amode == A_HALO) {
         if (t.bres && s.CO > t.bn) return bad("resident weights need one output-channel tile");
         if (!umma_geometry(s0, t, 1).fits) return bad("halo buffers exceed shared memory");
@@ -305,7 +333,8 @@ bool umma_valid(const ConvShape &s0, const UmmaTiling &t, int sm_count, std::str
     if (umma_smem_bytes(t) == 0) return bad("no compiled kernel");
     if (!umma_geometry(s0, t, 1).fits) return bad("more than 2^31 boxes or work units");
     DeviceState *ds = device_state();
-    if (ds && !t.bres && (int)umma_smem_bytes(t) > ds->max_smem_optin) return bad("smem exceeds opt-in limit");
+    if (ds && !t.bres && t.amode != A_STRIDED && (int)umma_smem_bytes(t) > ds->max_smem_optin)
+        return bad("smem exceeds opt-in limit");
     if (t.bres && t.amode != A_HALO && !umma_geometry(s0, t, 1).fits)
         return bad("resident weights exceed shared memory");
     (void)sm_count;
@@ -414,6 +443,8 @@ UmmaTiling default_tiling(const ConvShape &s, int amode, int bn, int sms, int pa
         t.bpt = 128 / t.box_w;
     } else if (amode == A_HALO) {
         t.box_w = 8, t.box_h = 16, t.bpt = 1;
+    } else if (amode == A_STRIDED) {
+        t.box_w = 16, t.box_h = 4, t.bpt = 2;
     } else {
         const Box b = box_options(kernel_shape(s, t)).front();
         t.box_w = b.w, t.box_h = b.h, t.bpt = b.bpt;
@@ -481,6 +512,16 @@ int halo_pack(const ConvShape &s)
     return cs > cp + 0.02 ? PACK_STACK : PACK_PLAIN;
 }
 
+bool strided_ok(const ConvShape &s)
+{
+    UmmaTiling t{};
+    t.amode = A_STRIDED;
+    t.bn = 64;
+    t.box_w = 16, t.box_h = 4, t.bpt = 2;
+    t.split = 1;
+    return umma_valid(s, t, 1, nullptr);
+}
+
 bool direct_ok(const ConvShape &s)
 {
     UmmaTiling t{};
@@ -514,6 +555,8 @@ Cand heuristic(const ConvShape &s, int sms)
         u.kind = BIGEMM_KIND_UMMA;
         if (direct_ok(s))
             u.t = default_tiling(s, A_DIRECT, default_bn(s), sms);
+        else if (strided_ok(s))
+            u.t = default_tiling(s, A_STRIDED, default_bn(s), sms);
         else if (sub_ok(s))
             u.t = default_tiling(s, A_NHWC, default_bn(s), sms, PACK_SUB);
         else if (halo_ok(s)) {
@@ -563,6 +606,7 @@ std::vector<Cand> candidates(const ConvShape &s, int sms)
     const double hc_plain = halo_cover(s, PACK_PLAIN), hc_stack = halo_cover(s, PACK_STACK);
     if (hc_plain >= 0.7) modes.push_back({A_HALO, PACK_PLAIN});
     if (hc_stack >= 0.7 && hc_stack > hc_plain + 0.02) modes.push_back({A_HALO, PACK_STACK});
+    if (strided_ok(s)) modes.push_back({A_STRIDED, PACK_PLAIN});
     if (sub_ok(s)) modes.push_back({A_NHWC, PACK_SUB});
     modes.push_back({A_NHWC, PACK_PLAIN});
     for (const auto &mp : modes) {
@@ -581,6 +625,9 @@ std::vector<Cand> candidates(const ConvShape &s, int sms)
             bpts.push_back(1);
             bx.push_back({8, 32});   // two tiles sharing each weight tile
             bpts.push_back(1);
+        } else if (amode == A_STRIDED) {
+            bx.push_back({16, 4});
+            bpts.push_back(2);
         } else {
             for (size_t i = 0; i < boxes.size() && bx.size() < 2; ++i) {
                 if (i > 0 && boxes[i].eff < boxes[0].eff - 0.05) break;
@@ -807,6 +854,36 @@ bigemm_status encode_direct_maps(bigemm_plan_s *p, const void *data, const void 
     return BIGEMM_OK;
 }
 
+// The strided mode's maps, re-encoded when a pointer changes: the data as
+// rows of 2W elements (an even input row and the odd one below it) x H/2 row
+// pairs x CI x N, read by 32-element x 4-row x 64-channel staging boxes
+// without swizzle; the kernel [CO][CI] as the K-major B operand.
+bigemm_status encode_strided_maps(bigemm_plan_s *p, const void *data, const void *kernel)
+{
+    if (p->maps_ready && p->map_a_src == data && p->map_b_src == kernel) return BIGEMM_OK;
+    const ConvShape &s = p->s;
+    const UmmaTiling &t = p->c.t;
+    const size_t e = dtype_size(s.in_dt);
+    const uint64_t dims[4] = {2ull * s.W, (uint64_t)s.H / 2, (uint64_t)s.CI, (uint64_t)s.N};
+    const uint64_t str[3] = {2ull * s.W * e, (uint64_t)s.H * s.W * e, (uint64_t)s.CI * s.H * s.W * e};
+    const uint32_t box[4] = {2u * (uint32_t)t.box_w, (uint32_t)t.box_h, (uint32_t)p->g.p.bk, 1u};
+    const uint32_t es[4] = {1u, 1u, 1u, 1u};
+    if (!encode_tiled(&p->map_a, tma_dt(s.in_dt), 4, data, dims, str, box, es,
+                      CU_TENSOR_MAP_SWIZZLE_NONE))
+        return BIGEMM_ERR_INVALID_ARG;
+    const uint64_t bd[2] = {(uint64_t)s.CI, (uint64_t)s.CO};
+    const uint64_t bs[1] = {(uint64_t)s.CI * e};
+    const uint32_t bb[2] = {(uint32_t)p->g.p.bk, (uint32_t)t.bn};
+    const uint32_t bes[2] = {1u, 1u};
+    if (!encode_tiled(&p->map_b, tma_dt(s.in_dt), 2, kernel, bd, bs, bb, bes,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
+        return BIGEMM_ERR_INVALID_ARG;
+    p->map_a_src = data;
+    p->map_b_src = kernel;
+    p->maps_ready = true;
+    return BIGEMM_OK;
+}
+
 // The raw-kernel B map of a 1x1 nhwc plan, re-encoded when the kernel pointer
 // changes: [CO][CI] with channel blocks past CI zero-filled by the copy.
 bigemm_status encode_raw_b(bigemm_plan_s *p, const void *kernel)
@@ -829,7 +906,7 @@ int launches_per_run(const bigemm_plan_s *p)
 {
     if (p->c.kind != BIGEMM_KIND_UMMA) return 1;
     int n = 1;
-    if (p->c.t.amode != A_DIRECT) n += 1;
+    if (p->c.t.amode != A_DIRECT && p->c.t.amode != A_STRIDED) n += 1;   // the pack
     if (p->g.p.split > 1 && !p->red_add) n += 1;
     return n;
 }
@@ -863,7 +940,7 @@ bigemm_status run_plan(bigemm_plan_s *p, const void *data, const void *kernel, c
     up.red_add = p->red_add ? 1 : 0;
     up.err = ds->err;
     up.timeout_ns = wait_timeout_ns();
-    if (p->c.t.amode != A_DIRECT) {
+    if (p->c.t.amode != A_DIRECT && p->c.t.amode != A_STRIDED) {
         const int pk = p->c.t.pack;
         const int hop = pk == PACK_SUB ? s.Ho : pk == PACK_STACK ? up.hp : s.H;
         const int wop = pk == PACK_SUB ? s.Wo : s.W;
@@ -877,7 +954,8 @@ bigemm_status run_plan(bigemm_plan_s *p, const void *data, const void *kernel, c
                                  p->red_add ? static_cast<float *>(out) : nullptr, up.out_elems);
         if (e != cudaSuccess) return BIGEMM_ERR_CUDA;
     } else {
-        bigemm_status r = encode_direct_maps(p, data, kernel);
+        bigemm_status r = p->c.t.amode == A_STRIDED ? encode_strided_maps(p, data, kernel)
+                                                    : encode_direct_maps(p, data, kernel);
         if (r != BIGEMM_OK) return r;
         if (p->red_add &&
             cudaMemsetAsync(out, 0, (size_t)up.out_elems * sizeof(float), st) != cudaSuccess)
@@ -1231,12 +1309,14 @@ bigemm_status plan_impl(int N, int H, int W, int CO, int CI, int KH, int KW, int
             }
         } else {
             c.kind = BIGEMM_KIND_UMMA;
-            if (opts->mode < 0 || opts->mode > 5) return BIGEMM_ERR_INVALID_ARG;
+            if (opts->mode < 0 || opts->mode > 6) return BIGEMM_ERR_INVALID_ARG;
             const int amode = (opts->mode == 1 || opts->mode == 4) ? A_NHWC
                               : opts->mode == 2                    ? A_DIRECT
                               : (opts->mode == 3 || opts->mode == 5) ? A_HALO
+                              : opts->mode == 6                    ? A_STRIDED
                               : (opts->box_w && opts->box_h)         ? A_NHWC
                               : direct_ok(s)                         ? A_DIRECT
+                              : strided_ok(s)                        ? A_STRIDED
                               : sub_ok(s)                            ? A_NHWC
                               : halo_ok(s)                           ? A_HALO
                                                                      : A_NHWC;
@@ -1362,8 +1442,7 @@ bigemm_status conv2d_nchw_plan_describe(bigemm_plan plan, char *buf, size_t len)
        << (c.kind == BIGEMM_KIND_UMMA ? "umma" : "simt") << "\"";
     if (c.kind == BIGEMM_KIND_UMMA) {
         const UmmaParams &p = plan->g.p;
-        os << ", \"amode\": \""
-           << (c.t.amode == A_DIRECT ? "direct" : c.t.amode == A_HALO ? "halo" : "nhwc")
+        os << ", \"amode\": \"" << amode_name(c.t.amode)
            << "\", \"pack\": \""
            << (c.t.pack == PACK_SUB ? "sub" : c.t.pack == PACK_STACK ? "stack" : "plain")
            << "\", \"resident_b\": " << (c.t.bres ? "true" : "false")
@@ -1374,7 +1453,8 @@ bigemm_status conv2d_nchw_plan_describe(bigemm_plan plan, char *buf, size_t len)
            << ", \"split_sum\": \"" << (p.split == 1 ? "none" : plan->red_add ? "add" : "reduce") << "\""
            << ", \"pix_tiles\": " << p.pix_tiles << ", \"co_tiles\": " << p.co_tiles
            << ", \"units\": " << p.units << ", \"grid\": " << plan->g.grid
-           << ", \"smem\": " << ((c.t.amode == A_HALO || c.t.bres) ? (size_t)p.halo_smem : umma_smem_bytes(c.t))
+           << ", \"smem\": " << ((c.t.amode == A_HALO || c.t.amode == A_STRIDED || c.t.bres)
+                                   ? (size_t)p.halo_smem : umma_smem_bytes(c.t))
            << ", \"halo_stages\": " << p.halo_sa << ", \"weight_stages\": " << p.halo_sb
            << ", \"store\": \"" << (plan->store_tma ? "tma" : "direct") << "\"";
     }

@@ -41,6 +41,7 @@ int fmt_of(int in_dt) { return in_dt == BIGEMM_F16 ? 0 : in_dt == BIGEMM_BF16 ? 
 size_t umma_smem_bytes(const UmmaTiling &t)
 {
     if (t.amode == A_HALO) return halo_smem_bytes(t.bn);
+    if (t.amode == A_STRIDED) return strided_smem_bytes(t.bn);
     switch (t.bn) {
     case 64: return Cfg<64>::smem;
     case 128: return Cfg<128>::smem;
@@ -51,9 +52,9 @@ size_t umma_smem_bytes(const UmmaTiling &t)
 
 bool umma_tiling_compiled(const UmmaTiling &t, int in_dt)
 {
-    (void)in_dt;
     return (t.bn == 64 || t.bn == 128 || t.bn == 256) &&
-           (t.amode == A_NHWC || t.amode == A_DIRECT || t.amode == A_HALO);
+           (t.amode == A_NHWC || t.amode == A_DIRECT || t.amode == A_HALO ||
+            (t.amode == A_STRIDED && in_dt != BIGEMM_F32));
 }
 
 cudaError_t launch_umma_conv(const UmmaTiling &t, int in_dt, const UmmaParams &p0,
@@ -68,9 +69,10 @@ cudaError_t launch_umma_conv(const UmmaTiling &t, int in_dt, const UmmaParams &p
     p.fd_hp = make_fastdiv((uint32_t)p.hp);
     p.fd_cib = make_fastdiv((uint32_t)p.ci_blocks);
     p.fd_kw = make_fastdiv((uint32_t)p.KW);
-    ProfScope prof(t.amode == A_NHWC ? "umma_conv_nhwc"
-                   : t.amode == A_HALO ? "umma_conv_halo"
-                                       : "umma_conv_direct",
+    ProfScope prof(t.amode == A_NHWC      ? "umma_conv_nhwc"
+                   : t.amode == A_HALO    ? "umma_conv_halo"
+                   : t.amode == A_STRIDED ? "umma_conv_strided"
+                                          : "umma_conv_direct",
                    stream);
     const int fmt = fmt_of(in_dt);
     if (t.amode == A_HALO) return launch_halo_conv(t.bn, fmt, p, map_a, map_b, map_c, grid, stream);
@@ -79,6 +81,13 @@ cudaError_t launch_umma_conv(const UmmaTiling &t, int in_dt, const UmmaParams &p
     // whose epilogue carries only that path
     const bool plain = fmt != 2 && !p.ws && !p.red_add && p.epi == BIGEMM_EPI_NONE &&
                        p.out_dt != BIGEMM_F32;
+    if (t.amode == A_STRIDED) {
+        if (t.bres || e16) return cudaErrorInvalidValue;
+        if (plain)
+            return launch_strided_plain(t.bn, fmt, p.store_tma != 0, p, map_a, map_b, map_c, grid,
+                                        stream);
+        return launch_strided_conv(t.bn, fmt, p, map_a, map_b, map_c, grid, stream);
+    }
     // split-K slices adding into an fp32 output take the kernel narrowed to that
     if (p.red_add && !p.ws && !t.bres && t.amode != A_HALO)
         return launch_umma_add(t.amode, fmt, t.bn, e16, p, map_a, map_b, map_c, grid, stream);

@@ -107,7 +107,12 @@ typedef struct {
                        4 mode 1 over a subsampled copy (1x1, pad 0, stride > 1:
                          only the pixels the conv reads are packed),
                        5 mode 3 with the images stacked, pad zero rows apart,
-                         so that one 16-row tile spans several small images.
+                         so that one 16-row tile spans several small images,
+                       6 NCHW read in place for a 1x1, stride-2, unpadded conv
+                         (16-bit, H even, 2*W*element size a multiple of 16
+                         bytes): TMA brings the even input rows, and warps of
+                         the kernel keep the even pixels, so no packed copy is
+                         made.
                        With kind = SIMT it names the kernel instead: 1 tiled
                        (groups = 1) or naive, 2 depthwise staged band (box_h
                        rows per block), 3 depthwise streaming (box_h = 2, 4

@@ -31,7 +31,7 @@ WORKLOADS = {"resnet50_fp16": synth.RESNET50_FP16, "fused": synth.FUSED_CONV,
 LAYERS = [(w, i, s) for w, specs in WORKLOADS.items() for i, s in enumerate(specs)]
 ORACLE_EPI = {"none": oracle.EPI_NONE, "bias": oracle.EPI_BIAS, "bias_exp": oracle.EPI_BIAS_EXP,
               "bias_rsqrt": oracle.EPI_BIAS_RSQRT, "bias_recip": oracle.EPI_BIAS_RECIP}
-_UMMA = re.compile(r"umma:(nhwc|halo|direct):bn(\d+):box(\d+)x(\d+)x(\d+):split(\d+)((?::\w+)*)$")
+_UMMA = re.compile(r"umma:(nhwc|halo|direct|strided):bn(\d+):box(\d+)x(\d+)x(\d+):split(\d+)((?::\w+)*)$")
 
 
 def cand_options(cand):
@@ -42,7 +42,7 @@ def cand_options(cand):
         flags = set(flags.split(":")[1:])
         mode = {"nhwc": bg.MODE_SUB if "sub" in flags else bg.MODE_NHWC,
                 "halo": bg.MODE_STACK if "stack" in flags else bg.MODE_HALO,
-                "direct": bg.MODE_DIRECT}[amode]
+                "direct": bg.MODE_DIRECT, "strided": bg.MODE_STRIDED}[amode]
         return {"kind": bg.KIND_UMMA, "mode": mode, "tile_n": int(bn), "box_w": int(bw),
                 "box_h": int(bh), "split_k": int(split),
                 "resident_b": 1 if "bres" in flags else -1,

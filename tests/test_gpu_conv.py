@@ -528,6 +528,58 @@ def test_depthwise_whole_planes_rejects_wide_rows():
     assert e.value.status == 2
 
 
+# ------------------------------------------------- strided mode: stride-2 1x1 read in place
+# The data is read as rows of 2W elements (an even input row and the odd one
+# below it); warps of the kernel keep the even pixels.  Cases: the ResNet-50
+# downsampling layer at N = 2, several column boxes per row (Wo > 16), rows
+# TMA can store (Wo = 16), bf16, ragged channels, BN 64 / 128 / 256, split K
+# (adding into fp32, and through the reduction pass), fused epilogues, an
+# image narrower than 16 columns.
+STRIDED = [
+    (S("str_r50_like", 2, 256, 512, 28, 28, 1, 2, 0), {}),
+    (S("str_w32_ragged_h", 1, 64, 128, 22, 32, 1, 2, 0), {"tile_n": 128}),
+    (S("str_wide_rows_56", 1, 64, 128, 56, 56, 1, 2, 0), {}),
+    (S("str_tma_rows_32", 2, 64, 64, 32, 32, 1, 2, 0), {}),
+    (S("str_bf16_ragged", 3, 40, 72, 12, 20, 1, 2, 0, i="bf16", o="bf16"), {}),
+    (S("str_tiny", 2, 16, 16, 2, 4, 1, 2, 0), {}),
+    (S("str_bn64_exp", 2, 128, 96, 14, 28, 1, 2, 0, o="f32", epi="bias_exp"), {"tile_n": 64}),
+    (S("str_bn256_bias_f16", 1, 64, 256, 18, 12, 1, 2, 0, epi="bias"), {"tile_n": 256}),
+    (S("str_split_add_f32", 1, 512, 128, 14, 16, 1, 2, 0, o="f32", epi="bias"), {"split_k": 4}),
+    (S("str_split_reduce_recip", 1, 256, 64, 10, 16, 1, 2, 0, o="f16", epi="bias_recip",
+       dd="absnormal", kd="absnormal"), {"split_k": 2}),
+]
+
+
+@pytest.mark.parametrize("case", STRIDED, ids=lambda c: c[0].name)
+def test_umma_strided_mode(case):
+    spec, extra = case
+    info = check(spec, dict({"kind": bg.KIND_UMMA, "mode": bg.MODE_STRIDED}, **extra))
+    # one launch and no scratch, unless K slices go through the reduction pass
+    assert info["amode"] == "strided"
+    if info["split_sum"] != "reduce":
+        assert info["launches"] == 1 and info["scratch_bytes"] == 0
+
+
+def test_strided_and_subsampled_agree():
+    spec = S("str_vs_sub", 2, 128, 256, 28, 28, 1, 2, 0)
+    a = run(spec, {"kind": bg.KIND_UMMA, "mode": bg.MODE_STRIDED})[-1]
+    b = run(spec, {"kind": bg.KIND_UMMA, "mode": bg.MODE_SUB})[-1]
+    # both fp32-accumulated sums of the same fp16 products, rounded to fp16
+    assert torch.allclose(a.float(), b.float(), rtol=2e-3, atol=2e-3)
+
+
+@pytest.mark.parametrize("shape,dt", [((1, 8, 16, 64, 64), bg.F32),    # tf32: K-major only
+                                      ((1, 9, 16, 64, 64), bg.F16),    # odd H
+                                      ((1, 8, 6, 64, 64), bg.F16),     # 2W*2 = 24 bytes
+                                      ((1, 8, 16, 64, 60), bg.F16)])   # CI*2 = 120 bytes
+def test_strided_mode_rejected(shape, dt):
+    N, H, W, CO, CI = shape
+    with pytest.raises(bg.BigemmError) as e:
+        bg.conv2d_nchw_plan_ex(N, H, W, CO, CI, 1, 1, 2, 0, 1, dt, dt, bg.EPI_NONE, 0,
+                               {"kind": bg.KIND_UMMA, "mode": bg.MODE_STRIDED})
+    assert e.value.status == 2
+
+
 # ------------------------------------------------- full size, sampled outputs
 FULL = synth.RESNET50_FP16 + synth.FUSED_CONV + synth.DEPTHWISE_FP16
 
