@@ -27,7 +27,7 @@ _LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-EPI_NONE, EPI_BIAS, EPI_BIAS_EXP, EPI_BIAS_RSQRT, EPI_BIAS_RECIP = 0, 1, 2, 3, 4
+EPI_NONE, EPI_BIAS, EPI_BIAS_EXP, EPI_BIAS_RSQRT, EPI_BIAS_RECIP, EPI_BIAS_RELU = 0, 1, 2, 3, 4, 5
 BC_COPY, BC_EXP, BC_RSQRT, BC_RECIP = 0, 1, 2, 3
 
 

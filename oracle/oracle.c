@@ -66,9 +66,9 @@ double oracle_conv_flops(int N, int CI, int H, int W, int CO, int KH, int KW,
 
 /* Epilogue codes (the fused per-channel broadcast applied to the conv sum):
  * the complex ops the CINN broadcast page names -- div, exp, rsqrt -- each
- * after the per-channel bias. */
+ * after the per-channel bias, and add + ReLU: max(acc + bias[f], 0). */
 enum { ORC_EPI_NONE = 0, ORC_EPI_BIAS = 1, ORC_EPI_BIAS_EXP = 2, ORC_EPI_BIAS_RSQRT = 3,
-       ORC_EPI_BIAS_RECIP = 4 };
+       ORC_EPI_BIAS_RECIP = 4, ORC_EPI_BIAS_RELU = 5 };
 
 typedef struct {
     int N, CI, H, W, CO, KH, KW, stride, pad, groups, Ho, Wo;
@@ -122,6 +122,7 @@ static double apply_epilogue(int epi, double acc, const double *bias, int f, dou
     case ORC_EPI_BIAS_EXP:   return exp(acc + bias[f]);
     case ORC_EPI_BIAS_RSQRT: return 1.0 / sqrt(acc + bias[f] + eps);
     case ORC_EPI_BIAS_RECIP: return 1.0 / (acc + bias[f]);
+    case ORC_EPI_BIAS_RELU:  return acc + bias[f] > 0.0 ? acc + bias[f] : 0.0;
     default:                 return NAN;
     }
 }
@@ -137,7 +138,7 @@ int oracle_conv2d_nchw(int N, int CI, int H, int W, int CO, int KH, int KW,
 {
     conv_shape s;
     if (make_shape(&s, N, CI, H, W, CO, KH, KW, stride, pad, groups) != 0) return -1;
-    if (epi < ORC_EPI_NONE || epi > ORC_EPI_BIAS_RECIP) return -1;
+    if (epi < ORC_EPI_NONE || epi > ORC_EPI_BIAS_RELU) return -1;
     if (epi != ORC_EPI_NONE && bias == NULL) return -1;
     const long planes = (long)N * CO;
     (void)nthreads;
@@ -169,7 +170,7 @@ int oracle_conv2d_nchw_points(int N, int CI, int H, int W, int CO, int KH, int K
 {
     conv_shape s;
     if (make_shape(&s, N, CI, H, W, CO, KH, KW, stride, pad, groups) != 0) return -1;
-    if (epi < ORC_EPI_NONE || epi > ORC_EPI_BIAS_RECIP) return -1;
+    if (epi < ORC_EPI_NONE || epi > ORC_EPI_BIAS_RELU) return -1;
     if (epi != ORC_EPI_NONE && bias == NULL) return -1;
     const int64_t total = (int64_t)N * CO * s.Ho * s.Wo;
     for (long i = 0; i < npts; ++i) {

@@ -28,6 +28,10 @@ MUTANTS = {
     "absum_signed": ("sabs += fabs(a * w);", "sabs += a * w;"),
     "bias_channel_zero": ("return exp(acc + bias[f]);", "return exp(acc + bias[0]);"),
     "recip_bias_dropped": ("return 1.0 / (acc + bias[f]);", "return 1.0 / acc;"),
+    "rsqrt_eps_dropped": ("return 1.0 / sqrt(acc + bias[f] + eps);", "return 1.0 / sqrt(acc + bias[f]);"),
+    "relu_before_bias": ("return acc + bias[f] > 0.0 ? acc + bias[f] : 0.0;",
+                         "return (acc > 0.0 ? acc : 0.0) + bias[f];"),
+    "relu_dropped": ("return acc + bias[f] > 0.0 ? acc + bias[f] : 0.0;", "return acc + bias[f];"),
     "eps_added_in_double": ("volatile float t = v + eps;", "volatile double t = (double)v + eps;"),
     "image_index_dropped": ("data[(((size_t)n * s->CI + ci)", "data[(((size_t)0 * s->CI + ci)"),
     "flops_missing_factor2": ("return 2.0 * N * CO", "return 1.0 * N * CO"),
@@ -90,6 +94,23 @@ def _battery(lib):
             failed.append("recip")
     except ValueError:
         failed.append("recip-rejected")
+    # rsqrt epilogue with eps on the same sums: 1/sqrt(27 - 26 + 0.25) inside
+    try:
+        out, _ = oracle.conv2d_nchw(np.ones((1, 3, 5, 6)), np.ones((2, 3, 3, 3)), stride=1, pad=1,
+                                    bias=np.array([-26.0, 0.5]), epi=oracle.EPI_BIAS_RSQRT, eps=0.25,
+                                    lib=lib)
+        if out[0, 0, 2, 2] != 1.0 / math.sqrt(1.25):
+            failed.append("rsqrt")
+    except ValueError:
+        failed.append("rsqrt-rejected")
+    # add + ReLU: interior 27 - 20 = 7, a corner 12 - 12.5 clamps to 0
+    try:
+        out, _ = oracle.conv2d_nchw(np.ones((1, 3, 5, 6)), np.ones((2, 3, 3, 3)), stride=1, pad=1,
+                                    bias=np.array([-20.0, -12.5]), epi=oracle.EPI_BIAS_RELU, lib=lib)
+        if out[0, 0, 2, 2] != 7.0 or out[0, 1, 0, 0] != 0.0 or out[0, 1, 0, 2] != 5.5:
+            failed.append("relu")
+    except ValueError:
+        failed.append("relu-rejected")
     return failed
 
 

@@ -78,6 +78,31 @@ def test_epilogue_recip_closed_form(orc):
     assert out[0, 0, 0, 0] == 1.0 / (12 - 30.0) and out[0, 1, 0, 0] == 1.0 / 12.5
 
 
+def test_epilogue_relu_hand_case(orc):
+    """add + ReLU on the hand-worked 1x1 case: max(conv + bias[f], 0) per
+    channel, with channel 0's bias set so that its outputs fall on both sides
+    of zero (and one exactly on it)."""
+    case = [c for c in hand_cases() if c["name"] == "two_channels_two_filters_1x1"][0]
+    hand = case["out"].reshape(1, 2, 2, 2)
+    bias = np.array([-hand[0, 0, 0, 1], 0.5])
+    out, _ = _conv(orc, case["shape"], case["data"], case["kernel"], bias=bias,
+                   epi=oracle.EPI_BIAS_RELU)
+    np.testing.assert_array_equal(out, np.maximum(hand + bias.reshape(1, 2, 1, 1), 0.0))
+    assert out[0, 0, 0, 1] == 0.0
+    assert (out[0, 0] == 0.0).any() and (out[0, 0] > 0.0).any()
+
+
+def test_epilogue_relu_closed_form(orc):
+    """All-ones data and kernel, 3x3 pad 1, CI = 3: an output sums 27 ones inside,
+    18 on an edge, 12 in a corner.  With bias -20 channel 0 keeps only the
+    interior (7), with -12.5 channel 1 keeps interior and edges (14.5, 5.5) and
+    zeroes the corners."""
+    out, _ = oracle.conv2d_nchw(np.ones((1, 3, 5, 6)), np.ones((2, 3, 3, 3)), stride=1, pad=1,
+                                bias=np.array([-20.0, -12.5]), epi=oracle.EPI_BIAS_RELU, lib=orc)
+    assert out[0, 0, 2, 2] == 7.0 and out[0, 0, 0, 2] == 0.0 and out[0, 0, 0, 0] == 0.0
+    assert out[0, 1, 2, 2] == 14.5 and out[0, 1, 0, 2] == 5.5 and out[0, 1, 0, 0] == 0.0
+
+
 def _rand(shape, seed):
     return np.random.default_rng(seed).uniform(-1, 1, shape)
 
