@@ -15,7 +15,7 @@ import os
 import threading
 
 __all__ = [
-    "F32", "F16", "BF16", "EPI_NONE", "EPI_BIAS", "EPI_BIAS_EXP", "EPI_BIAS_RSQRT", "EPI_BIAS_RECIP",
+    "F32", "F16", "BF16", "EPI_NONE", "EPI_BIAS", "EPI_BIAS_EXP", "EPI_BIAS_RSQRT", "EPI_BIAS_RECIP", "EPI_BIAS_RELU",
     "BC_COPY", "BC_EXP", "BC_RSQRT", "BC_RECIP", "KIND_AUTO", "KIND_UMMA", "KIND_SIMT",
     "MODE_NHWC", "MODE_DIRECT", "MODE_HALO", "MODE_SUB", "MODE_STACK", "MODE_STRIDED",
     "BigemmError", "Plan", "PlanOptions", "library_path", "load_library",
@@ -28,12 +28,12 @@ __all__ = [
 ]
 
 F32, F16, BF16 = 0, 1, 2
-EPI_NONE, EPI_BIAS, EPI_BIAS_EXP, EPI_BIAS_RSQRT, EPI_BIAS_RECIP = 0, 1, 2, 3, 4
+EPI_NONE, EPI_BIAS, EPI_BIAS_EXP, EPI_BIAS_RSQRT, EPI_BIAS_RECIP, EPI_BIAS_RELU = 0, 1, 2, 3, 4, 5
 BC_COPY, BC_EXP, BC_RSQRT, BC_RECIP = 0, 1, 2, 3
 KIND_AUTO, KIND_UMMA, KIND_SIMT = 0, 1, 2
 MODE_NHWC, MODE_DIRECT, MODE_HALO, MODE_SUB, MODE_STACK, MODE_STRIDED = 1, 2, 3, 4, 5, 6
 EPI_NAMES = {"none": EPI_NONE, "bias": EPI_BIAS, "bias_exp": EPI_BIAS_EXP,
-             "bias_rsqrt": EPI_BIAS_RSQRT, "bias_recip": EPI_BIAS_RECIP}
+             "bias_rsqrt": EPI_BIAS_RSQRT, "bias_recip": EPI_BIAS_RECIP, "bias_relu": EPI_BIAS_RELU}
 DTYPE_CODES = {"f32": F32, "f16": F16, "bf16": BF16}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))

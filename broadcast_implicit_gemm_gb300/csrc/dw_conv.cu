@@ -41,6 +41,7 @@ __device__ __forceinline__ void dw_store_rows(const SimtArgs &a, const float (&a
             else if (a.epi == BIGEMM_EPI_BIAS_EXP) vv = expf(vv + bv);
             else if (a.epi == BIGEMM_EPI_BIAS_RSQRT) vv = rsqrtf(vv + bv + a.eps);
             else if (a.epi == BIGEMM_EPI_BIAS_RECIP) vv = 1.0f / (vv + bv);
+            else if (a.epi == BIGEMM_EPI_BIAS_RELU) vv = fmaxf(vv + bv, 0.f);
             o8[o] = vv;
         }
         const size_t o = ((size_t)plane * a.Ho + y) * a.Wo + x0;

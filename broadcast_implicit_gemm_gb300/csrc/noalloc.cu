@@ -52,6 +52,7 @@ __device__ __forceinline__ float na_epi(int epi, float acc, float b, float eps)
     case BIGEMM_EPI_BIAS: return acc + b;
     case BIGEMM_EPI_BIAS_EXP: return expf(acc + b);
     case BIGEMM_EPI_BIAS_RSQRT: return rsqrtf(acc + b + eps);
+    case BIGEMM_EPI_BIAS_RELU: return fmaxf(acc + b, 0.f);
     default: return 1.0f / (acc + b);
     }
 }
@@ -118,7 +119,7 @@ extern "C" bigemm_status conv2d_nchw_run_noalloc(int N, int H, int W, int CO, in
     if (N < 1 || H < 1 || W < 1 || CO < 1 || CI < 1 || KH < 1 || KW < 1 || stride < 1 || padding < 0)
         return BIGEMM_ERR_INVALID_ARG;
     if (in_dtype < BIGEMM_F32 || in_dtype > BIGEMM_BF16 || out_dtype < BIGEMM_F32 ||
-        out_dtype > BIGEMM_BF16 || epi < BIGEMM_EPI_NONE || epi > BIGEMM_EPI_BIAS_RECIP)
+        out_dtype > BIGEMM_BF16 || epi < BIGEMM_EPI_NONE || epi > BIGEMM_EPI_BIAS_RELU)
         return BIGEMM_ERR_INVALID_ARG;
     if (!data || !kernel || !out || (epi != BIGEMM_EPI_NONE && !bias)) return BIGEMM_ERR_INVALID_ARG;
     if (((uintptr_t)data | (uintptr_t)kernel | (uintptr_t)out) & 15) return BIGEMM_ERR_INVALID_ARG;

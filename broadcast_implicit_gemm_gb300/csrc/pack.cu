@@ -547,6 +547,7 @@ __device__ __forceinline__ float epi_apply(int epi, float acc, float b, float ep
     case BIGEMM_EPI_BIAS: return acc + b;
     case BIGEMM_EPI_BIAS_EXP: return expf(acc + b);
     case BIGEMM_EPI_BIAS_RSQRT: return rsqrtf(acc + b + eps);
+    case BIGEMM_EPI_BIAS_RELU: return fmaxf(acc + b, 0.f);
     default: return 1.0f / (acc + b);
     }
 }

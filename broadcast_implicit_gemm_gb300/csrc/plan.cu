@@ -381,7 +381,7 @@ bigemm_status validate(const ConvShape &s)
     if (s.CI % s.groups || s.CO % s.groups) return BIGEMM_ERR_INVALID_ARG;
     if (s.in_dt < BIGEMM_F32 || s.in_dt > BIGEMM_BF16) return BIGEMM_ERR_INVALID_ARG;
     if (s.out_dt < BIGEMM_F32 || s.out_dt > BIGEMM_BF16) return BIGEMM_ERR_INVALID_ARG;
-    if (s.epi < BIGEMM_EPI_NONE || s.epi > BIGEMM_EPI_BIAS_RECIP) return BIGEMM_ERR_INVALID_ARG;
+    if (s.epi < BIGEMM_EPI_NONE || s.epi > BIGEMM_EPI_BIAS_RELU) return BIGEMM_ERR_INVALID_ARG;
     if (s.Ho < 1 || s.Wo < 1) return BIGEMM_ERR_INVALID_ARG;
     if ((long long)s.H * s.W > (1ll << 30) || (long long)s.Ho * s.Wo > (1ll << 30))
         return BIGEMM_ERR_UNSUPPORTED;

@@ -36,6 +36,7 @@ __device__ __forceinline__ float epi_apply(int epi, float acc, const float *bias
     case BIGEMM_EPI_BIAS: return acc + bias[f];
     case BIGEMM_EPI_BIAS_EXP: return expf(acc + bias[f]);
     case BIGEMM_EPI_BIAS_RSQRT: return rsqrtf(acc + bias[f] + eps);
+    case BIGEMM_EPI_BIAS_RELU: return fmaxf(acc + bias[f], 0.f);
     default: return 1.0f / (acc + bias[f]);
     }
 }

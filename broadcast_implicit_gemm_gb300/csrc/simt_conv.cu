@@ -283,6 +283,7 @@ __global__ void __launch_bounds__(256) conv_depthwise_kernel(SimtArgs a, int row
                 if (a.epi == BIGEMM_EPI_BIAS) acc[i] += bv;
                 else if (a.epi == BIGEMM_EPI_BIAS_EXP) acc[i] = expf(acc[i] + bv);
                 else if (a.epi == BIGEMM_EPI_BIAS_RSQRT) acc[i] = rsqrtf(acc[i] + bv + a.eps);
+                else if (a.epi == BIGEMM_EPI_BIAS_RELU) acc[i] = fmaxf(acc[i] + bv, 0.f);
                 else acc[i] = 1.0f / (acc[i] + bv);
             }
         }

@@ -277,6 +277,9 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
                 } else if (p.epi == BIGEMM_EPI_BIAS_RSQRT) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = rsqrtf(v[j] + bv[j] + p.eps);
+                } else if (p.epi == BIGEMM_EPI_BIAS_RELU) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = fmaxf(v[j] + bv[j], 0.f);
                 } else {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = 1.0f / (v[j] + bv[j]);

@@ -42,7 +42,7 @@ class ConvSpec:
     out_dtype: str = "f32"
     data_dist: str = "uniform"     # "uniform" [-1,1] | "absnormal" |N(0,1)|
     kernel_dist: str = "he"        # "uniform" [-1,1] | "he" N(0, 2/fan_in) | "dw" N(0, 2/(K*K))
-    epi: str = "none"              # "none" | "bias" | "bias_exp" | "bias_rsqrt"
+    epi: str = "none"              # "none" | "bias" | "bias_exp" | "bias_rsqrt" | "bias_recip" | "bias_relu"
 
     def with_batch(self, N: int) -> "ConvSpec":
         return replace(self, N=N, name=f"{self.name}@N{N}")

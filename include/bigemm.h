@@ -55,13 +55,14 @@ typedef enum { BIGEMM_F32 = 0, BIGEMM_F16 = 1, BIGEMM_BF16 = 2 } bigemm_dtype;
 /* Fused epilogue: out = acc (NONE), acc + bias[f] (BIAS),
  * exp(acc + bias[f]) (BIAS_EXP), 1/sqrt(acc + bias[f] + eps) (BIAS_RSQRT),
  * 1/(acc + bias[f]) (BIAS_RECIP, the div of the CINN broadcast page's complex
- * ops: div, exp, rsqrt). */
+ * ops: div, exp, rsqrt), max(acc + bias[f], 0) (BIAS_RELU, add + ReLU). */
 typedef enum {
     BIGEMM_EPI_NONE = 0,
     BIGEMM_EPI_BIAS = 1,
     BIGEMM_EPI_BIAS_EXP = 2,
     BIGEMM_EPI_BIAS_RSQRT = 3,
-    BIGEMM_EPI_BIAS_RECIP = 4
+    BIGEMM_EPI_BIAS_RECIP = 4,
+    BIGEMM_EPI_BIAS_RELU = 5
 } bigemm_epilogue;
 
 typedef enum {

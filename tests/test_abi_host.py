@@ -119,6 +119,6 @@ def test_enum_values_match_header():
     import broadcast_implicit_gemm_gb300 as bg
     text = open(HEADER).read()
     vals = dict((k, int(v)) for k, v in re.findall(r"\b(BIGEMM_[A-Z0-9_]+)\s*=\s*(\d+)", text))
-    for name in ("EPI_NONE", "EPI_BIAS", "EPI_BIAS_EXP", "EPI_BIAS_RSQRT", "EPI_BIAS_RECIP",
+    for name in ("EPI_NONE", "EPI_BIAS", "EPI_BIAS_EXP", "EPI_BIAS_RSQRT", "EPI_BIAS_RECIP", "EPI_BIAS_RELU",
                  "BC_COPY", "BC_EXP", "BC_RSQRT", "BC_RECIP", "KIND_UMMA", "KIND_SIMT"):
         assert getattr(bg, name) == vals["BIGEMM_" + name], name

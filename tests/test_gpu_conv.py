@@ -73,7 +73,8 @@ def check(spec, options=None, search=0, seed=0):
         bound = conv_bound(ref, sabs, tau, spec.out_dtype)
     else:
         epi = {"bias": oracle.EPI_BIAS, "bias_exp": oracle.EPI_BIAS_EXP,
-               "bias_rsqrt": oracle.EPI_BIAS_RSQRT, "bias_recip": oracle.EPI_BIAS_RECIP}[spec.epi]
+               "bias_rsqrt": oracle.EPI_BIAS_RSQRT, "bias_recip": oracle.EPI_BIAS_RECIP,
+               "bias_relu": oracle.EPI_BIAS_RELU}[spec.epi]
         ref, sabs = oracle.conv2d_nchw(x, w, stride=spec.stride, pad=spec.pad, groups=spec.groups,
                                        bias=b, epi=epi, nthreads=NTH)
         pre, _ = oracle.conv2d_nchw(x, w, stride=spec.stride, pad=spec.pad, groups=spec.groups,
@@ -464,6 +465,36 @@ RECIP = [
 
 @pytest.mark.parametrize("case", RECIP, ids=lambda c: c[0].name)
 def test_div_epilogue(case):
+    spec, opts = case
+    info = check(spec, opts)
+    if opts and opts.get("split_k"):
+        assert info["split_sum"] == "reduce"
+
+
+# ------------------------------------------------- add + ReLU, max(conv + bias, 0)
+# Data and kernels of both signs, so about half of the outputs clamp to zero.
+def _U(name, N, CI, CO, H, W, K, s, p, g=1, i="f16", o="f32", kd="he"):
+    return S(name, N, CI, CO, H, W, K, s, p, g=g, i=i, o=o, epi="bias_relu", kd=kd)
+
+
+RELU = [
+    (_U("relu_halo_f32", 2, 64, 96, 12, 12, 3, 1, 1), {"kind": bg.KIND_UMMA, "mode": bg.MODE_HALO}),
+    (_U("relu_nhwc_f16", 1, 32, 64, 9, 11, 3, 1, 1, o="f16"), {"kind": bg.KIND_UMMA, "mode": bg.MODE_NHWC}),
+    (_U("relu_direct_bf16", 2, 64, 128, 16, 16, 1, 1, 0, i="bf16", o="bf16"),
+     {"kind": bg.KIND_UMMA, "mode": bg.MODE_DIRECT}),
+    (_U("relu_strided_f16", 2, 64, 128, 12, 16, 1, 2, 0, o="f16"),
+     {"kind": bg.KIND_UMMA, "mode": bg.MODE_STRIDED}),
+    (_U("relu_tf32_split_reduce", 1, 256, 64, 9, 12, 3, 1, 1, i="f32"),
+     {"kind": bg.KIND_UMMA, "mode": bg.MODE_NHWC, "split_k": 4}),
+    (_U("relu_simt_tiled", 1, 16, 40, 10, 9, 3, 1, 1, i="f32"), {"kind": bg.KIND_SIMT}),
+    (_U("relu_depthwise_stream", 2, 16, 16, 14, 16, 3, 1, 1, g=16, kd="dw"), None),
+    (_U("relu_depthwise_plane_k5", 2, 24, 24, 14, 14, 5, 1, 2, g=24, kd="dw"), {"kind": bg.KIND_SIMT, "mode": 4}),
+    (_U("relu_depthwise_band", 2, 16, 16, 13, 15, 3, 2, 1, g=16, kd="dw"), {"kind": bg.KIND_SIMT, "mode": 2, "box_h": 4}),
+]
+
+
+@pytest.mark.parametrize("case", RELU, ids=lambda c: c[0].name)
+def test_relu_epilogue(case):
     spec, opts = case
     info = check(spec, opts)
     if opts and opts.get("split_k"):

@@ -45,7 +45,7 @@ def _cases(n=48, seed=2024):
         N = int(rng.integers(1, 4))
         i_dt = str(rng.choice(["f16", "bf16", "f32"]))
         o_dt = str(rng.choice(["f16", "f32"])) if i_dt == "f16" else (i_dt if rng.random() < 0.5 else "f32")
-        epi = str(rng.choice(["none", "none", "bias", "bias_exp", "bias_recip"]))
+        epi = str(rng.choice(["none", "none", "bias", "bias_exp", "bias_recip", "bias_relu"]))
         dd, kd = ("absnormal", "absnormal") if epi == "bias_recip" else ("uniform", "he")
         if epi == "bias_exp":
             o_dt = "f32"          # exp of a large sum would overflow a 16-bit output

@@ -26,7 +26,8 @@ pytestmark = pytest.mark.gpu
 
 DT = {"f32": bg.F32, "f16": bg.F16, "bf16": bg.BF16}
 ORACLE_EPI = {"bias": oracle.EPI_BIAS, "bias_exp": oracle.EPI_BIAS_EXP,
-              "bias_rsqrt": oracle.EPI_BIAS_RSQRT, "bias_recip": oracle.EPI_BIAS_RECIP}
+              "bias_rsqrt": oracle.EPI_BIAS_RSQRT, "bias_recip": oracle.EPI_BIAS_RECIP,
+              "bias_relu": oracle.EPI_BIAS_RELU}
 
 CASES = [
     # fp32 (tf32 MMAs), N=1: few tiles, so the K dimension is split (partial sums in scratch)
@@ -34,8 +35,9 @@ CASES = [
     # fp16 3x3 with the fused exp epilogue, several tiles, no split
     synth.ConvSpec("noalloc_f16_exp", 2, 64, 96, 15, 13, 3, 1, 1, 1, "f16", "f32", "uniform", "he",
                    "bias_exp"),
-    # bf16, stride 2, ragged channels
-    synth.ConvSpec("noalloc_bf16_s2", 3, 40, 72, 17, 17, 3, 2, 1, 1, "bf16", "bf16"),
+    # bf16, stride 2, ragged channels, add + ReLU
+    synth.ConvSpec("noalloc_bf16_s2", 3, 40, 72, 17, 17, 3, 2, 1, 1, "bf16", "bf16", "uniform", "he",
+                   "bias_relu"),
     # N=1, one tile and 36 K blocks: split K, then 1/(acc + bias) and fp16 rounding in the
     # reduction pass (non-negative operands keep the argument away from zero)
     synth.ConvSpec("noalloc_f16_split_recip", 1, 256, 128, 8, 8, 3, 1, 1, 1, "f16", "f16",

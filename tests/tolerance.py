@@ -38,7 +38,7 @@ def conv_bound(ref, sabs, tau, out_dtype):
 
 def epi_bound(arg, sabs, tau, epi, out_dtype, ref, eps=1e-5):
     d = tau * sabs + np.abs(arg) * 2.0 ** -23
-    if epi == "bias":
+    if epi in ("bias", "bias_relu"):   # max(., 0) moves a value no more than its argument
         prop = d
     elif epi == "bias_exp":
         prop = np.exp(arg + d) - np.exp(arg)
