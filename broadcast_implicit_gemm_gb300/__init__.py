@@ -50,7 +50,8 @@ class BigemmError(RuntimeError):
 class PlanOptions(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int), ("tile_n", ctypes.c_int), ("split_k", ctypes.c_int),
                 ("stages", ctypes.c_int), ("box_w", ctypes.c_int), ("box_h", ctypes.c_int),
-                ("mode", ctypes.c_int), ("resident_b", ctypes.c_int), ("epi_warps", ctypes.c_int)]
+                ("mode", ctypes.c_int), ("resident_b", ctypes.c_int), ("epi_warps", ctypes.c_int),
+                ("cta_pair", ctypes.c_int)]
 
 
 class KernelTime(ctypes.Structure):

@@ -61,6 +61,8 @@ struct UmmaTiling {
     int split;        // K slices
     int epi16;        // A_NHWC / A_DIRECT, bn = 128: 16 epilogue warps (four per TMEM
                       // lane quadrant, 576 threads) instead of 8
+    int pair;         // A_HALO with resident weights: clusters of two CTAs share each
+                      // MMA (tcgen05 cta_group::2, M = 256), each holding half of B
 };
 
 struct UmmaParams {
@@ -153,6 +155,17 @@ cudaError_t launch_umma_add(int amode, int fmt, int bn, bool epi16, const UmmaPa
 cudaError_t launch_umma_res(int amode, int fmt, int bn, bool epi16, const UmmaParams &p,
                             const CUtensorMap &map_a, const CUtensorMap &map_b,
                             const CUtensorMap &map_c, int grid, cudaStream_t stream);
+
+// The CTA-pair halo kernels (halo_pair.cu, halo_pair_plain.cu): resident
+// weights, one 16 x 8 tile per CTA, p.units pair units (tiles 2u and 2u + 1),
+// an even grid; the second form is narrowed to 16-bit outputs with no
+// epilogue op (tma: written by TMA stores, else from registers).
+cudaError_t launch_halo_pair(int bn, int fmt, const UmmaParams &p, const CUtensorMap &map_a,
+                             const CUtensorMap &map_b, const CUtensorMap &map_c, int grid,
+                             cudaStream_t stream);
+cudaError_t launch_halo_pair_plain(int bn, int fmt, bool tma, const UmmaParams &p,
+                                   const CUtensorMap &map_a, const CUtensorMap &map_b,
+                                   const CUtensorMap &map_c, int grid, cudaStream_t stream);
 
 // The strided-mode kernels (strided_conv.cu, strided_plain.cu): the
 // shared-memory layout for a tile of bn output channels, written into p's

@@ -54,11 +54,11 @@ std::string cand_str(const Cand &c)
 {
     char b[160];
     if (c.kind == BIGEMM_KIND_UMMA)
-        snprintf(b, sizeof b, "umma:%s:bn%d:box%dx%dx%d:split%d%s%s%s",
+        snprintf(b, sizeof b, "umma:%s:bn%d:box%dx%dx%d:split%d%s%s%s%s",
                  amode_name(c.t.amode), c.t.bn,
                  c.t.box_w, c.t.box_h, c.t.bpt, c.t.split,
                  c.t.pack == PACK_SUB ? ":sub" : c.t.pack == PACK_STACK ? ":stack" : "",
-                 c.t.bres ? ":bres" : "", c.t.epi16 ? ":e16" : "");
+                 c.t.bres ? ":bres" : "", c.t.epi16 ? ":e16" : "", c.t.pair ? ":pair" : "");
     else if (c.simt_variant == SV_DW)
         snprintf(b, sizeof b, "simt:depthwise:rows%d", c.dw_rows);
     else if (c.simt_variant == SV_DWS)
@@ -90,6 +90,8 @@ bool parse_cand(const std::string &s, Cand &c)
         c.t.bres = strcmp(layout, "bres") == 0 || strcmp(layout2, "bres") == 0;
         c.t.epi16 = strcmp(layout, "e16") == 0 || strcmp(layout2, "e16") == 0 ||
                     strcmp(layout3, "e16") == 0;
+        c.t.pair = strcmp(layout, "pair") == 0 || strcmp(layout2, "pair") == 0 ||
+                   strcmp(layout3, "pair") == 0;
         c.t.bn = a, c.t.box_w = b, c.t.box_h = d, c.t.bpt = e, c.t.split = f;
         return true;
     }
@@ -232,7 +234,8 @@ UmmaGeom umma_geometry(const ConvShape &s0, const UmmaTiling &t, int sm_count)
     }
     p.cip = g.cip;
     const long long total = (t.pack == PACK_STACK ? 1 : (long long)s.N) * bpi;
-    const long long ptiles = ceil_div(total, t.bpt);
+    // CTA pairs: a unit is two tiles, one per block of the pair
+    const long long ptiles = ceil_div(ceil_div(total, t.bpt), t.pair ? 2 : 1);
     p.co_tiles = (int)ceil_div(s.CO, t.bn);
     p.kb_per_split = (int)ceil_div(p.k_blocks, t.split);
     p.split = (int)ceil_div(p.k_blocks, p.kb_per_split);
@@ -248,9 +251,10 @@ UmmaGeom umma_geometry(const ConvShape &s0, const UmmaTiling &t, int sm_count)
     DeviceState *ds = device_state();
     const int limit = ds ? ds->max_smem_optin : 232448;
     if (t.amode == A_HALO) {
-        // shared-memory layout: streamed or resident weights
-        g.fits = g.fits && halo_layout(t.bn, t.bres != 0, t.box_h, s.KH, s.KH * s.KW, p.ci_blocks,
-                                       limit, p);
+        // shared-memory layout: streamed or resident weights (a CTA pair's
+        // blocks hold half of the weights each)
+        g.fits = g.fits && halo_layout(t.pair ? t.bn / 2 : t.bn, t.bres != 0, t.box_h, s.KH,
+                                       s.KH * s.KW, p.ci_blocks, limit, p);
     } else if (t.amode == A_STRIDED) {
         g.fits = g.fits && strided_layout(t.bn, limit, p);
     } else if (t.bres) {
@@ -258,6 +262,7 @@ UmmaGeom umma_geometry(const ConvShape &s0, const UmmaTiling &t, int sm_count)
         g.fits = g.fits && main_res_layout(t.bn, p.k_blocks, limit, p);
     }
     g.grid = (int)std::min<long long>(p.units, sm_count);
+    if (t.pair) g.grid = (int)std::min<long long>(2 * p.units, sm_count & ~1);
     if (t.bres && t.amode != A_HALO && p.co_tiles > 0) {
         // each block keeps one output-channel tile: a grid of whole tile groups
         g.grid = std::max(p.co_tiles, g.grid / p.co_tiles * p.co_tiles);
@@ -327,6 +332,13 @@ bool umma_valid(const ConvShape &s0, const UmmaTiling &t, int sm_count, std::str
         if (t.box_w * s.stride > 256 || t.box_h * s.stride > 256) return bad("box > 256");
     }
     if (t.bres && t.amode != A_HALO && t.split != 1) return bad("resident weights need split 1");
+    if (t.pair) {
+        if (t.amode != A_HALO || !t.bres || t.box_h != 16)
+            return bad("CTA pairs run the halo mode with resident weights and 16-row tiles");
+        if (t.bn != 64 && t.bn != 128) return bad("CTA pairs take tile_n 64 or 128");
+        if (t.split != 1) return bad("CTA pairs need split 1");
+        if (sm_count < 2) return bad("CTA pairs need two SMs");
+    }
     if (t.epi16 && (t.amode == A_HALO || t.bn != 128))
         return bad("16 epilogue warps need the nhwc or direct mode and BN = 128");
     if (t.bpt > 16) return bad("more than 16 boxes per tile");
@@ -668,6 +680,11 @@ std::vector<Cand> candidates(const ConvShape &s, int sms)
                     if ((amode == A_HALO && s.CO <= bn) || (amode != A_HALO && split == 1)) {
                         c.t.bres = 1;   // the resident-weights form too
                         if (umma_valid(s, c.t, sms, nullptr)) v.push_back(c);
+                        if (amode == A_HALO && split == 1) {
+                            Cand pc = c;   // and its CTA-pair form
+                            pc.t.pair = 1;
+                            if (umma_valid(s, pc.t, sms, nullptr)) v.push_back(pc);
+                        }
                     }
                     if (amode != A_HALO && bn == 128) {
                         // both forms again with 16 epilogue warps
@@ -770,11 +787,13 @@ bigemm_status setup_plan(bigemm_plan_s *p)
             return BIGEMM_ERR_UNSUPPORTED;
         // packed weights [CO][tap][cip] viewed as (channel, output channel, tap):
         // one box brings TB taps, each a [BN][128 B] K-major tile
+        // (CTA pairs: each block loads half of the tile's output channels)
         const int tb = (t.bres || t.box_h == 32) ? 1 : 32768 / (t.bn * 128);
         const uint64_t kk = (uint64_t)s.KH * s.KW;
         const uint64_t bd[3] = {(uint64_t)p->g.cip, (uint64_t)s.CO, kk};
         const uint64_t bs[2] = {kk * p->g.cip * e, (uint64_t)p->g.cip * e};
-        const uint32_t bb[3] = {(uint32_t)p->g.p.bk, (uint32_t)t.bn, (uint32_t)tb};
+        const uint32_t bb[3] = {(uint32_t)p->g.p.bk, (uint32_t)(t.pair ? t.bn / 2 : t.bn),
+                                (uint32_t)tb};
         const uint32_t bes[3] = {1u, 1u, 1u};
         if (!encode_tiled(&p->map_b, tma_dt(s.in_dt), 3, p->wp, bd, bs, bb, bes,
                           CU_TENSOR_MAP_SWIZZLE_128B))
@@ -1264,13 +1283,13 @@ bigemm_status plan_impl(int N, int H, int W, int CO, int CI, int KH, int KW, int
 
     const bool forced = opts && (opts->kind || opts->tile_n || opts->split_k || opts->box_w ||
                                  opts->box_h || opts->stages || opts->mode || opts->resident_b ||
-                                 opts->epi_warps);
+                                 opts->epi_warps || opts->cta_pair);
     Cand c;
     std::string log, chosen = "heuristic";
     if (forced) {
         if (opts->kind == BIGEMM_KIND_SIMT || (opts->kind == 0 && !opts->tile_n && !opts->split_k &&
                                                !opts->box_w && !opts->box_h && !opts->stages &&
-                                               !opts->mode && !opts->resident_b)) {
+                                               !opts->mode && !opts->resident_b && !opts->cta_pair)) {
             c = heuristic(s, sms);
             if (opts->epi_warps != 0 && opts->epi_warps != 8 && opts->epi_warps != 16)
                 return BIGEMM_ERR_INVALID_ARG;
@@ -1348,6 +1367,8 @@ bigemm_status plan_impl(int N, int H, int W, int CO, int CI, int KH, int KW, int
                 c.t.epi16 = 1;
             else if (opts->epi_warps == 0)
                 prefer_epi16(s, c.t);
+            if (opts->cta_pair < -1 || opts->cta_pair > 1) return BIGEMM_ERR_INVALID_ARG;
+            if (opts->cta_pair == 1) c.t.pair = 1;
         }
         std::string why;
         if (!cand_valid(s, c, sms, &why)) return BIGEMM_ERR_UNSUPPORTED;
@@ -1447,6 +1468,7 @@ bigemm_status conv2d_nchw_plan_describe(bigemm_plan plan, char *buf, size_t len)
            << (c.t.pack == PACK_SUB ? "sub" : c.t.pack == PACK_STACK ? "stack" : "plain")
            << "\", \"resident_b\": " << (c.t.bres ? "true" : "false")
            << ", \"epi_warps\": " << (c.t.epi16 ? 16 : 8)
+           << ", \"cta_pair\": " << (c.t.pair ? "true" : "false")
            << ", \"bn\": " << c.t.bn
            << ", \"box\": [" << c.t.box_w << ", " << c.t.box_h << ", " << c.t.bpt << "]"
            << ", \"split\": " << p.split << ", \"k_blocks\": " << p.k_blocks

@@ -412,6 +412,151 @@ __device__ __forceinline__ void umma4_kmajor(uint32_t d_tmem, uint32_t a_lo, uin
             : "memory");
 }
 
+// ------------------------------------------------------ CTA pairs (cluster of 2)
+// The CTA's rank in its cluster.
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// The shared::cluster address of the same shared-memory offset in CTA `rank`
+// of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+
+// Arrive on an mbarrier given by its shared::cluster address (possibly in the
+// peer CTA), with release semantics at cluster scope.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
+}
+
+// Every thread of every CTA of the cluster: arrive, then wait for all.
+__device__ __forceinline__ void cluster_sync_all()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                     : "memory");
+}
+
+// TMEM allocation for a CTA pair: one warp of each of the two CTAs executes it;
+// the same columns are allocated in both CTAs' tensor memory.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t *dst_smem, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair()
+{
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+// TMA tensor loads into this CTA's shared memory whose completion is counted
+// on an mbarrier of either CTA of the pair (cluster_bar: a shared::cluster
+// address).
+__device__ __forceinline__ void tma_load_3d_pair(void *dst, const CUtensorMap *map,
+                                                 uint32_t cluster_bar, int c0, int c1, int c2)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(cluster_bar), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d_pair(void *dst, const CUtensorMap *map,
+                                                 uint32_t cluster_bar, int c0, int c1, int c2,
+                                                 int c3)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(cluster_bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
+
+// Arrive once on the mbarrier at the same offset in each CTA of `cta_mask`
+// when every tcgen05 operation of the pair issued so far by this thread has
+// completed.
+__device__ __forceinline__ void umma_commit_pair_mc(uint64_t *bar, uint16_t cta_mask)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(smem_u32(bar)),
+        "h"(cta_mask)
+        : "memory");
+}
+
+// Arrive once on this CTA's mbarrier `bar` when every tcgen05 operation of
+// the pair issued so far by this thread has completed.
+__device__ __forceinline__ void umma_commit_pair(uint64_t *bar)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+
+// The four MMAs of one 128-byte K block for a CTA pair (M = 256: each CTA's
+// 128 rows of A and half of B's N rows at the same shared-memory offsets).
+template <bool TF32>
+__device__ __forceinline__ void umma4_kmajor_pair(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
+                                                  uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
+                                                  uint32_t accum_first)
+{
+    if (TF32)
+        asm volatile(
+            "{\n\t.reg .pred p, q;\n\t.reg .b64 ad, bd;\n\t.reg .b32 al, bl;\n\t"
+            "setp.ne.b32 p, %6, 0;\n\t"
+            "setp.eq.b32 q, %6, %6;\n\t"
+            "mov.b64 ad, {%1, %2};\n\tmov.b64 bd, {%3, %4};\n\t"
+            "tcgen05.mma.cta_group::2.kind::tf32 [%0], ad, bd, %5, p;\n\t"
+            "add.u32 al, %1, 2;\n\tadd.u32 bl, %3, 2;\n\t"
+            "mov.b64 ad, {al, %2};\n\tmov.b64 bd, {bl, %4};\n\t"
+            "tcgen05.mma.cta_group::2.kind::tf32 [%0], ad, bd, %5, q;\n\t"
+            "add.u32 al, %1, 4;\n\tadd.u32 bl, %3, 4;\n\t"
+            "mov.b64 ad, {al, %2};\n\tmov.b64 bd, {bl, %4};\n\t"
+            "tcgen05.mma.cta_group::2.kind::tf32 [%0], ad, bd, %5, q;\n\t"
+            "add.u32 al, %1, 6;\n\tadd.u32 bl, %3, 6;\n\t"
+            "mov.b64 ad, {al, %2};\n\tmov.b64 bd, {bl, %4};\n\t"
+            "tcgen05.mma.cta_group::2.kind::tf32 [%0], ad, bd, %5, q;\n\t}" ::"r"(d_tmem),
+            "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accum_first)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p, q;\n\t.reg .b64 ad, bd;\n\t.reg .b32 al, bl;\n\t"
+            "setp.ne.b32 p, %6, 0;\n\t"
+            "setp.eq.b32 q, %6, %6;\n\t"
+            "mov.b64 ad, {%1, %2};\n\tmov.b64 bd, {%3, %4};\n\t"
+            "tcgen05.mma.cta_group::2.kind::f16 [%0], ad, bd, %5, p;\n\t"
+            "add.u32 al, %1, 2;\n\tadd.u32 bl, %3, 2;\n\t"
+            "mov.b64 ad, {al, %2};\n\tmov.b64 bd, {bl, %4};\n\t"
+            "tcgen05.mma.cta_group::2.kind::f16 [%0], ad, bd, %5, q;\n\t"
+            "add.u32 al, %1, 4;\n\tadd.u32 bl, %3, 4;\n\t"
+            "mov.b64 ad, {al, %2};\n\tmov.b64 bd, {bl, %4};\n\t"
+            "tcgen05.mma.cta_group::2.kind::f16 [%0], ad, bd, %5, q;\n\t"
+            "add.u32 al, %1, 6;\n\tadd.u32 bl, %3, 6;\n\t"
+            "mov.b64 ad, {al, %2};\n\tmov.b64 bd, {bl, %4};\n\t"
+            "tcgen05.mma.cta_group::2.kind::f16 [%0], ad, bd, %5, q;\n\t}" ::"r"(d_tmem),
+            "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accum_first)
+            : "memory");
+}
+
 // Instruction descriptor for kind::f16 / kind::tf32 with an fp32 accumulator:
 // operand format (0 f16, 1 bf16, 2 tf32) for A and B, major-ness of A and B
 // (0 K-major, 1 MN-major), N >> 3 at bit 17, M >> 4 at bit 24.

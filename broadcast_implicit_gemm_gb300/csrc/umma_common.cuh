@@ -97,7 +97,12 @@ __device__ __forceinline__ void tmem_wait_ld_regs(uint32_t (&r)[32])
 // (TMA reduce-add boxes or atomic adds), no op but the first slice's bias.
 // (Measured on the 1x1 ResNet-50 layers: the general form's unused paths cost
 // a third of the epilogue's time per tile.)
-template <int BN, bool BOXED, int NEPI = kEpiWarps, int MT = 1, int STG = 4096, int FORM = 0>
+// PAIR: the block is one of a cluster's CTA pair sharing each MMA (M = 256);
+// a pair runs units blockIdx.x / 2, + gridDim.x / 2, ..., this CTA holding
+// pixel tile 2 * pt + rank of each, and the accumulator is handed back to the
+// MMA thread of the pair's even CTA.
+template <int BN, bool BOXED, int NEPI = kEpiWarps, int MT = 1, int STG = 4096, int FORM = 0,
+          bool PAIR = false>
 __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtensorMap *map_c,
                                               uint32_t tmem_base, uint64_t *tfull,
                                               uint64_t *tempty, uint8_t *stage_out,
@@ -144,8 +149,12 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
     int acc = 0;
     uint32_t acc_phase = 0;
     bool alive = true;
-    for (int u = blockIdx.x; alive && u < p.units; u += gridDim.x) {
-        const Unit w = decode(p, u);
+    const int u_first = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const int u_step = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+    const int pair_rank = PAIR ? (int)cluster_ctarank() : 0;
+    for (int u = u_first; alive && u < p.units; u += u_step) {
+        Unit w = decode(p, u);
+        if (PAIR) w.pt = 2 * w.pt + pair_rank;
         // partial sums take no epilogue, except the bias that the first of the
         // slices adding into the output brings.  Lane l fetches channel l of each
         // of the warp's chunks now, before the accumulator is ready; the chunk
@@ -256,7 +265,12 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
             } else if (m == MT - 1) {           // accumulator drained by this warp: hand it back
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&tempty[acc]);
+                if (lane == 0) {
+                    if (PAIR)
+                        mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
+                    else
+                        mbar_arrive(&tempty[acc]);
+                }
             }
             const int cb = co0 + (h + kSplit * i) * 32;
             float v[32];

@@ -70,11 +70,13 @@ cudaError_t launch_umma_conv(const UmmaTiling &t, int in_dt, const UmmaParams &p
     p.fd_cib = make_fastdiv((uint32_t)p.ci_blocks);
     p.fd_kw = make_fastdiv((uint32_t)p.KW);
     ProfScope prof(t.amode == A_NHWC      ? "umma_conv_nhwc"
-                   : t.amode == A_HALO    ? "umma_conv_halo"
+                   : t.amode == A_HALO    ? (t.pair ? "umma_conv_halo_pair" : "umma_conv_halo")
                    : t.amode == A_STRIDED ? "umma_conv_strided"
                                           : "umma_conv_direct",
                    stream);
     const int fmt = fmt_of(in_dt);
+    if (t.amode == A_HALO && t.pair)
+        return launch_halo_pair(t.bn, fmt, p, map_a, map_b, map_c, grid, stream);
     if (t.amode == A_HALO) return launch_halo_conv(t.bn, fmt, p, map_a, map_b, map_c, grid, stream);
     const bool e16 = t.epi16 != 0;
     // a 16-bit output written in place with no epilogue op takes the kernel

@@ -129,6 +129,11 @@ typedef struct {
                        epilogue warps per TMEM lane quadrant (576 threads per
                        block) instead of two (8); 0 chooses; other values:
                        INVALID_ARG                                              */
+    int cta_pair;   /* UMMA modes 3 and 5 with resident weights, tile_n 64 or
+                       128, split_k 1: 1 runs clusters of two blocks that share
+                       each MMA (M = 256 pixels, each block holding half of the
+                       weights), -1 single blocks, 0 chooses; other values:
+                       INVALID_ARG                                              */
 } bigemm_plan_options;
 
 /*

@@ -46,7 +46,8 @@ def cand_options(cand):
         return {"kind": bg.KIND_UMMA, "mode": mode, "tile_n": int(bn), "box_w": int(bw),
                 "box_h": int(bh), "split_k": int(split),
                 "resident_b": 1 if "bres" in flags else -1,
-                "epi_warps": 16 if "e16" in flags else 8}
+                "epi_warps": 16 if "e16" in flags else 8,
+                "cta_pair": 1 if "pair" in flags else -1}
     if cand == "simt:depthwise:plane":
         return {"kind": bg.KIND_SIMT, "mode": 4}
     m = re.match(r"simt:depthwise:(stream|rows)(\d+)$", cand)

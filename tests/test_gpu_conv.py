@@ -611,6 +611,50 @@ def test_strided_mode_rejected(shape, dt):
     assert e.value.status == 2
 
 
+# ------------------------------------------------- CTA pairs: two blocks share each MMA
+# tcgen05 cta_group::2 (M = 256): each block of a cluster pair loads its own
+# 16 x 8 halo tile and half of the resident weights; the even block issues the
+# pair's MMAs.  Cases: the ResNet-50 64 -> 64 3x3 layer at N = 2, an odd tile
+# count (the odd block's last tile is past the output), stacked images, bf16,
+# tf32, a 5x5 kernel, ragged CO, BN = 128, fused exp into fp32.
+PAIR = [
+    S("pair_r50_like", 2, 64, 64, 56, 56, 3, 1, 1),
+    S("pair_odd_tiles", 1, 64, 64, 40, 8, 3, 1, 1),
+    S("pair_bf16_ragged_co", 2, 40, 48, 20, 24, 3, 1, 1, i="bf16", o="bf16"),
+    S("pair_tf32", 1, 32, 64, 18, 16, 3, 1, 1, i="f32", o="f32"),
+    S("pair_k5", 1, 64, 64, 24, 16, 5, 1, 2),
+    S("pair_bn128_exp", 2, 64, 128, 16, 24, 3, 1, 1, o="f32", epi="bias_exp"),
+]
+
+
+@pytest.mark.parametrize("stack", [False, True])
+@pytest.mark.parametrize("spec", PAIR, ids=lambda s: s.name)
+def test_umma_halo_cta_pair(spec, stack):
+    opts = {"kind": bg.KIND_UMMA, "mode": bg.MODE_STACK if stack else bg.MODE_HALO,
+            "resident_b": 1, "cta_pair": 1, "tile_n": 64 if spec.CO <= 64 else 128}
+    info = check(spec, opts)
+    assert info["cta_pair"] and info["grid"] % 2 == 0
+
+
+def test_cta_pair_and_single_block_agree():
+    spec = S("pair_vs_single", 2, 64, 64, 28, 28, 3, 1, 1)
+    base = {"kind": bg.KIND_UMMA, "mode": bg.MODE_HALO, "resident_b": 1, "tile_n": 64}
+    a = run(spec, dict(base, cta_pair=1))[-1]
+    b = run(spec, dict(base, cta_pair=-1))[-1]
+    # the same fp32 sums of the same fp16 products, in the same order
+    assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("opts", [{"mode": bg.MODE_HALO, "resident_b": -1, "cta_pair": 1},    # streamed weights
+                                  {"mode": bg.MODE_NHWC, "cta_pair": 1},                       # not the halo mode
+                                  {"mode": bg.MODE_HALO, "resident_b": 1, "cta_pair": 1, "split_k": 2}])
+def test_cta_pair_rejected(opts):
+    with pytest.raises(bg.BigemmError) as e:
+        bg.conv2d_nchw_plan_ex(1, 16, 16, 64, 64, 3, 3, 1, 1, 1, bg.F16, bg.F16, bg.EPI_NONE, 0,
+                               dict({"kind": bg.KIND_UMMA, "tile_n": 64}, **opts))
+    assert e.value.status == 2
+
+
 # ------------------------------------------------- full size, sampled outputs
 FULL = synth.RESNET50_FP16 + synth.FUSED_CONV + synth.DEPTHWISE_FP16
 
