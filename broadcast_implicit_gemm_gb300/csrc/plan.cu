@@ -339,8 +339,8 @@ bool umma_valid(const ConvShape &s0, const UmmaTiling &t, int sm_count, std::str
         if (t.split != 1) return bad("CTA pairs need split 1");
         if (sm_count < 2) return bad("CTA pairs need two SMs");
     }
-    if (t.epi16 && (t.amode == A_HALO || t.bn != 128))
-        return bad("16 epilogue warps need the nhwc or direct mode and BN = 128");
+    if (t.epi16 && (t.amode == A_HALO || t.amode == A_STRIDED || (t.bn != 128 && t.bn != 64)))
+        return bad("16 epilogue warps need the nhwc or direct mode and BN = 64 or 128");
     if (t.bpt > 16) return bad("more than 16 boxes per tile");
     if (umma_smem_bytes(t) == 0) return bad("no compiled kernel");
     if (!umma_geometry(s0, t, 1).fits) return bad("more than 2^31 boxes or work units");
@@ -686,7 +686,7 @@ std::vector<Cand> candidates(const ConvShape &s, int sms)
                             if (umma_valid(s, pc.t, sms, nullptr)) v.push_back(pc);
                         }
                     }
-                    if (amode != A_HALO && bn == 128) {
+                    if (amode != A_HALO && amode != A_STRIDED && (bn == 128 || bn == 64)) {
                         // both forms again with 16 epilogue warps
                         for (int br : {0, 1}) {
                             if (br && split != 1) continue;

@@ -49,6 +49,11 @@ __device__ __forceinline__ Unit decode(const UmmaParams &p, int u)
 
 constexpr int kMaxBoxes = 16;   // boxes per tile: 128 rows / at least 8 pixels per box (< 32 lanes)
 
+// Epilogue warp groups that take alternate units (epilogue_warp): two for 16
+// warps over 64-channel tiles, else one.  An accumulator is handed back by the
+// NEPI / groups warps that drain it.
+__host__ __device__ constexpr int epi_groups(int bn, int nepi) { return (nepi == 16 && bn == 64) ? 2 : 1; }
+
 // Two floats rounded to nearest-even 16-bit values (fp16 or bf16), a in the
 // low half: one packed conversion instruction for the pair.
 __device__ __forceinline__ uint32_t pack2_16(float a, float b, bool f16)
@@ -78,8 +83,12 @@ __device__ __forceinline__ void tmem_wait_ld_regs(uint32_t (&r)[32])
 
 // Epilogue of one warp (warps 2 .. 2 + NEPI - 1 of the block).  NEPI = 8: two
 // warps per TMEM lane quadrant, each taking every other 32-channel chunk of
-// the accumulator; NEPI = 16: four per quadrant, each taking every fourth;
-// NEPI = 4: one warp per quadrant takes every chunk.  MT = 2:
+// the accumulator; NEPI = 16: four per quadrant, each taking every fourth
+// (BN = 128), or, with BN = 64 (two chunks), two groups of eight warps that
+// take alternate units -- group g the block's units that use accumulator g --
+// so that each warp drains half as many units (the per-unit work, not the
+// chunks, paces 64-channel tiles); NEPI = 4: one warp per quadrant takes every
+// chunk.  MT = 2:
 // a unit is two 128-pixel M tiles stacked vertically (box_h = 32 rows of a
 // halo tile), with accumulators at TMEM columns acc * 2BN and acc * 2BN + BN.
 // BOXED: the tile's pixels are 2-D boxes (box_w x box_h) of one image (or of
@@ -116,12 +125,16 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
     // processed.  With TMA stores the warp stages its 32 pixels x 32 channels
     // in its own STG bytes of shared memory and lane 0 writes them as one box.
     static_assert(NEPI == 4 || NEPI == 8 || NEPI == 16, "one, two or four warps per TMEM lane quadrant");
-    static_assert(BN / 32 >= NEPI / 4, "every warp of a quadrant takes at least one chunk");
-    constexpr int kSplit = NEPI / 4;            // warps sharing a quadrant
+    constexpr int kGroups = epi_groups(BN, NEPI);   // unit-interleaved warp groups
+    static_assert(BN / 32 >= NEPI / 4 / kGroups, "every warp of a quadrant takes at least one chunk");
+    static_assert(kGroups == 1 || (!PAIR && MT == 1), "unit groups: single blocks, one M tile");
+    constexpr int kSplit = NEPI / 4 / kGroups;  // warps of a group sharing a quadrant
     constexpr int kChunks = BN / 32;            // 2, 4 or 8
     constexpr int kMine = kChunks / kSplit;     // chunks per warp
     const int q = warp & 3;                     // TMEM lane quadrant of this warp
-    const int h = (warp - 2) >> 2;              // which share of the chunks (0 when NEPI = 4)
+    const int h4 = (warp - 2) >> 2;             // 0 .. NEPI/4 - 1
+    const int grp = kGroups > 1 ? h4 / kSplit : 0;   // the warp's unit group
+    const int h = h4 - grp * kSplit;            // which share of the chunks (0 when NEPI = 4)
     const int row = q * 32 + lane;              // tile row = pixel
     const int bi = row / box_px, bj = row - bi * box_px;
     const int wbi = (q * 32) / box_px;          // the warp's box
@@ -146,11 +159,13 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
     static_assert(kNB >= 1, "at least one 2 KB buffer per warp");
     int piece = 0;
     const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16);
-    int acc = 0;
+    // with unit groups, group g takes the block's units g, g + 2, ... (in the
+    // block's order), all of which use accumulator g
+    int acc = grp;
     uint32_t acc_phase = 0;
     bool alive = true;
-    const int u_first = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
-    const int u_step = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+    const int u_first = PAIR ? (int)(blockIdx.x >> 1) : (int)(blockIdx.x + grp * gridDim.x);
+    const int u_step = PAIR ? (int)(gridDim.x >> 1) : (int)(kGroups * gridDim.x);
     const int pair_rank = PAIR ? (int)cluster_ctarank() : 0;
     for (int u = u_first; alive && u < p.units; u += u_step) {
         Unit w = decode(p, u);
@@ -422,8 +437,12 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
             }
         }
       }
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1u;
+        if (kGroups > 1) {
+            acc_phase ^= 1u;                    // the group's next use of its accumulator
+        } else {
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+        }
     }
     if (lane == 0) bulk_wait<0>();              // stores complete before the block exits
 }

@@ -17,8 +17,9 @@ constexpr int kResMaxA = 10;   // A stages at most with resident weights
 // weights once, into shared memory laid out by main_res_layout, and the ring
 // carries only the A boxes.
 // NEPI: epilogue warps, 8 (two per TMEM lane quadrant) or 16 (four, for
-// BN = 128): each warp then drains one 32-channel chunk per tile, and the
-// quadrant's stores and address arithmetic run in more warps at once.  The 16
+// BN = 128: each warp then drains one 32-channel chunk per tile; for BN = 64:
+// two groups of eight take alternate units), so the quadrant's stores and
+// address arithmetic run in more warps at once.  The 16
 // warps stage 2 KB each, so the shared-memory layout is the same.  (At
 // BN = 256 the 576-thread block's register budget would spill.)
 template <int NEPI>
@@ -61,7 +62,7 @@ __global__ void __launch_bounds__(main_threads<NEPI>(), 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull[i], 1);
-            mbar_init(&tempty[i], NEPI);
+            mbar_init(&tempty[i], NEPI / epi_groups(BN, NEPI));
         }
         mbar_init(drain, 1);
         mbar_init(b_full, 1);
@@ -241,7 +242,8 @@ __global__ void __launch_bounds__(main_threads<NEPI>(), 1)
         }
     } else {
         // --------------------------------------------------------- epilogue
-        static_assert(NEPI == kEpiWarps || (NEPI == 16 && BN == 128), "16 epilogue warps need BN = 128");
+        static_assert(NEPI == kEpiWarps || (NEPI == 16 && (BN == 128 || BN == 64)),
+                      "16 epilogue warps need BN = 128 or 64");
         epilogue_warp<BN, AMODE != A_DIRECT, NEPI, 1, kEpiWarps * 4096 / NEPI, FORM>(
             p, &map_c, tmem_base, tfull, tempty, stage_out, abort_flag, warp, lane, box_px);
     }
@@ -281,7 +283,7 @@ cudaError_t dispatch_bn(int bn, bool epi16, const UmmaParams &p, const CUtensorM
 {
     switch (bn) {
     case 64:
-        if (epi16) return cudaErrorInvalidValue;
+        if (epi16) return launch_one<64, AMODE, FMT, RB, 16, FORM>(p, ma, mb, mc, grid, s);
         return launch_one<64, AMODE, FMT, RB, kEpiWarps, FORM>(p, ma, mb, mc, grid, s);
     case 128:
         if (epi16) return launch_one<128, AMODE, FMT, RB, 16, FORM>(p, ma, mb, mc, grid, s);

@@ -796,8 +796,32 @@ def test_eight_epilogue_warps_on_request():
     assert info["epi_warps"] == 8
 
 
+# 64-channel tiles with 16 epilogue warps: two groups of eight take alternate
+# units (and accumulators); an odd unit count per block leaves group 1 a unit
+# short.  Direct and per-tap modes, resident and streamed weights, split K
+# adding into fp32, 16-bit register stores, fused epilogues.
+EPI16_64 = [
+    (S("e16g_direct_64_64_56", 2, 64, 64, 56, 56, 1, 1, 0), bg.MODE_DIRECT, 1, 1),
+    (S("e16g_direct_ragged_co40_exp", 1, 64, 40, 20, 28, 1, 1, 0, o="f32", epi="bias_exp"),
+     bg.MODE_DIRECT, -1, 1),
+    (S("e16g_nhwc_k3_relu_bf16", 2, 48, 64, 13, 11, 3, 1, 1, i="bf16", o="bf16", epi="bias_relu"),
+     bg.MODE_NHWC, -1, 1),
+    (S("e16g_nhwc_tf32_split_add", 1, 256, 64, 14, 14, 3, 1, 1, i="f32", o="f32"), bg.MODE_NHWC, -1, 8),
+    (S("e16g_nhwc_regstores_14", 2, 64, 64, 14, 14, 1, 1, 0), bg.MODE_NHWC, 1, 1),
+    (S("e16g_sub_s2", 2, 128, 64, 28, 28, 1, 2, 0), bg.MODE_SUB, 1, 1),
+]
+
+
+@pytest.mark.parametrize("case", EPI16_64, ids=lambda c: c[0].name)
+def test_sixteen_epilogue_warps_64_channel_tiles(case):
+    spec, mode, res, split = case
+    opts = {"kind": bg.KIND_UMMA, "mode": mode, "tile_n": 64, "split_k": split, "epi_warps": 16,
+            "resident_b": res}
+    info = check(spec, opts)
+    assert info["epi_warps"] == 16 and info["bn"] == 64
+
+
 @pytest.mark.parametrize("opts,status", [
-    ({"kind": 1, "mode": bg.MODE_DIRECT, "tile_n": 64, "epi_warps": 16}, 2),
     ({"kind": 1, "mode": bg.MODE_DIRECT, "tile_n": 256, "epi_warps": 16}, 2),
     ({"kind": 1, "mode": bg.MODE_HALO, "tile_n": 128, "epi_warps": 16}, 2),
     ({"kind": 1, "mode": bg.MODE_DIRECT, "tile_n": 128, "epi_warps": 12}, 1),
