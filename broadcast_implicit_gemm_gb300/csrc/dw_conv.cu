@@ -9,7 +9,12 @@
 //    No shared memory and no block barrier, so it streams at HBM rate.
 //  * dw_plane (H, W <= 32): one or two whole planes per warp, staged in shared
 //    memory.
+//  * dw_small (stride 1, outputs at most 16 wide and 32 tall): whole planes
+//    staged per warp, each thread computing a 2-row x 8-column block.
 #include <algorithm>
+#include <map>
+#include <mutex>
+#include <tuple>
 
 #include "simt_common.cuh"
 namespace bigemm {
@@ -401,7 +406,470 @@ __global__ void __launch_bounds__(256) dw_plane_kernel(SimtArgs a, int lp, int t
     }
 }
 
+// Small planes, stride 1 (outputs at most 16 wide and 32 tall): the warp
+// stages one or more whole (image, channel) planes in its shared memory, in
+// the input's own type, inside a zero border that is written once (only the
+// interiors are rewritten for each group of planes), and each thread computes
+// a TY-row x 8-column block of one plane's outputs: the TY + K - 1 input rows
+// of its window are read once each (8 + K - 1 values, two per 32-bit load for
+// 16-bit inputs) and feed all TY output rows, so a block costs
+// (TY + K - 1)(K + 7) values read for 8 TY K^2 FMAs.  The results go to a
+// compact per-warp buffer in the output type, and the warp writes the group's
+// outputs -- one contiguous run of the output, like its input -- with 16-byte
+// stores.  The staging copy looks up each element's place (each pair's, for
+// 16-bit inputs with rows of even length) through a table built once per
+// block, so no element pays for divisions.  (Measured on the 576-channel
+// 14 x 14 5x5 layer, N = 64: the streaming kernel spent about 70 instructions
+// per output for 25 FMAs.)
+constexpr int kDwrTX = 8;
+constexpr int kDwrWarps = 4;   // warps per block
+
+// Column of a staged row where the plane's first column sits: the left border
+// is K/2 wide, widened to an even count for 16-bit inputs so that pairs of
+// columns stay 32-bit aligned.
+__host__ __device__ constexpr int dwr_c0(int K, int es) { return es == 2 ? (K / 2 + 1) & ~1 : K / 2; }
+
+template <int DT>
+struct DwStage {                 // 16-bit inputs: raw halves, converted in pairs on use
+    using T = uint16_t;
+    __device__ static float2 pair(uint32_t w)
+    {
+        if (DT == BIGEMM_F16) return __half22float2(*reinterpret_cast<const __half2 *>(&w));
+        return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w));
+    }
+};
+template <>
+struct DwStage<BIGEMM_F32> {
+    using T = float;
+};
+
+template <int OT>
+__device__ __forceinline__ void dw_put(char *buf, int i, float v)
+{
+    if (OT == BIGEMM_F32) reinterpret_cast<float *>(buf)[i] = v;
+    else if (OT == BIGEMM_F16) reinterpret_cast<__half *>(buf)[i] = __float2half_rn(v);
+    else reinterpret_cast<__nv_bfloat16 *>(buf)[i] = __float2bfloat16_rn(v);
+}
+
+// A thread's outputs into the warp's compact output buffer (plane slot pl,
+// rows oy0.., columns ox0..; those outside the plane are dropped).  With
+// 16-bit outputs and rows of even length, columns go in pairs (one 32-bit
+// store each: every pair starts on an even element).
+template <int OT, int TY>
+__device__ __forceinline__ void dw_put_block(char *ob, const float (&acc)[TY][kDwrTX], int pl,
+                                             int HW, int W, int Ho, int Wo, int oy0, int ox0)
+{
+    if (OT != BIGEMM_F32 && (W & 1) == 0) {
+#pragma unroll
+        for (int oy = 0; oy < TY; ++oy)
+#pragma unroll
+            for (int ox = 0; ox < kDwrTX; ox += 2)
+                if (oy0 + oy < Ho && ox0 + ox < Wo) {
+                    uint32_t pk;
+                    if (OT == BIGEMM_F16) {
+                        const __half2 h = __floats2half2_rn(acc[oy][ox], acc[oy][ox + 1]);
+                        pk = *reinterpret_cast<const uint32_t *>(&h);
+                    } else {
+                        const __nv_bfloat162 h = __floats2bfloat162_rn(acc[oy][ox], acc[oy][ox + 1]);
+                        pk = *reinterpret_cast<const uint32_t *>(&h);
+                    }
+                    reinterpret_cast<uint32_t *>(ob)[(pl * HW + (oy0 + oy) * W + ox0 + ox) >> 1] = pk;
+                }
+        return;
+    }
+#pragma unroll
+    for (int oy = 0; oy < TY; ++oy)
+#pragma unroll
+        for (int ox = 0; ox < kDwrTX; ++ox)
+            if (oy0 + oy < Ho && ox0 + ox < Wo)
+                dw_put<OT>(ob, pl * HW + (oy0 + oy) * W + ox0 + ox, acc[oy][ox]);
+}
+
+// Words of a warp's weight slot: one channel's K x K weights from the 32-bit
+// word holding the first (16-bit weights may start mid-word).
+__host__ __device__ constexpr int dwr_wslot(int K, int es) { return es == 4 ? K * K : (K * K + 1) / 2; }
+
+template <int DT, int K, int TY>
+__global__ void __launch_bounds__(kDwrWarps * 32, TY == 2 ? (K == 7 ? 6 : 8) : (K == 7 ? 4 : 6))
+dw_small_kernel(SimtArgs a, int tpp, int ppw, int bxn, int pitch, int tstride, int wbytes,
+                FastDiv fd_w, FastDiv fd_hw, FastDiv fd_ci, const void *__restrict__ x,
+                const void *__restrict__ w, const float *__restrict__ bias, void *__restrict__ out)
+{
+    constexpr int P = K / 2, TX = kDwrTX, WX = TX + K - 1, KK = K * K;
+    constexpr int VE = DwIn<DT>::VE;
+    constexpr int ES = DT == BIGEMM_F32 ? 4 : 2;
+    constexpr int C0 = dwr_c0(K, ES);
+    constexpr int WS = dwr_wslot(K, ES);
+    using ST = typename DwStage<DT>::T;
+    extern __shared__ __align__(16) char dwr_smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int HW = a.H * a.W;
+    // 16-bit elements of rows of even length move in pairs; 32-bit units (an
+    // fp32 element or such a pair) are copied asynchronously, two groups of
+    // planes in flight per warp (the one computed and the next)
+    const bool pairs = ES == 2 && (a.W & 1) == 0;
+    const bool async_in = ES == 4 || pairs;
+    // weights too, when every channel's block lies inside the tensor's words
+    const bool async_w = async_in && ((a.CI * KK * ES) & 3) == 0;
+    const int tab_n = pairs ? ppw * HW / 2 : ppw * HW;
+    // the staging offset of each element (or pair, in 32-bit words) of a group
+    // of planes, in NCHW order
+    int *tab = reinterpret_cast<int *>(dwr_smem);
+    for (int e = threadIdx.x; e < tab_n; e += blockDim.x) {
+        uint32_t r, ix;
+        const uint32_t q = fd_divmod((uint32_t)(pairs ? 2 * e : e), fd_hw, &r);
+        const uint32_t iy = fd_divmod(r, fd_w, &ix);
+        const int off = (int)(q * tstride + (iy + P) * pitch + ix + C0);
+        tab[e] = pairs ? off >> 1 : off;
+    }
+    // per warp: two staging buffers, two weight buffers, the compact outputs
+    const size_t stg = ((size_t)ppw * tstride * ES + 15) & ~(size_t)15;
+    const size_t wsb = ((size_t)ppw * WS * 4 + 15) & ~(size_t)15;
+    char *wb = dwr_smem + (size_t)((tab_n + 3) & ~3) * 4 + (size_t)warp * wbytes;
+    char *wgt = wb + 2 * stg;
+    char *ob = wgt + 2 * wsb;
+    // the zero borders, once: interiors are rewritten for every group of planes
+    for (int i = lane; i < (int)(2 * stg / 16); i += 32)
+        reinterpret_cast<uint4 *>(wb)[i] = make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+    griddep_enter();
+    const int pl = lane / tpp, t = lane - pl * tpp;      // plane slot, thread of the plane
+    const int by = t / bxn, bx = t - by * bxn;
+    const int oy0 = by * TY, ox0 = bx * TX;
+    const long long planes = (long long)a.N * a.CI;
+    const long long step = (long long)gridDim.x * (blockDim.x >> 5) * ppw;
+    const int ESO = a.out_dt == BIGEMM_F32 ? 4 : 2;
+    const int cstep = (int)(step % a.CI);
+    const uint32_t wwords = (uint32_t)a.CI * KK * ES / 4;
+    // the copies of the group of planes from gpp (first channel gc) into buffer b
+    auto issue = [&](long long gpp, int gc, int b) {
+        if (gpp < planes) {
+            const int gnp = (int)min((long long)ppw, planes - gpp);
+            const int units = gnp * HW * ES / 4;
+            const char *src = static_cast<const char *>(x) + (size_t)gpp * HW * ES;
+            char *dst = wb + b * stg;
+            for (int u = lane; u < units; u += 32) cp_async4(dst + 4 * tab[u], src + 4 * u);
+            if (async_w)
+                for (int i = lane; i < gnp * WS; i += 32) {
+                    const int s = i / WS, wd = i - s * WS;
+                    uint32_t ch;
+                    fd_divmod((uint32_t)(gc + s), fd_ci, &ch);
+                    const uint32_t w0 = ch * KK * ES / 4 + wd;
+                    if (w0 < wwords)
+                        cp_async4(wgt + b * wsb + 4 * i, static_cast<const uint32_t *>(w) + w0);
+                }
+        }
+        cp_async_commit();
+    };
+    long long pp = ((long long)blockIdx.x * (blockDim.x >> 5) + warp) * ppw;
+    int c0 = (int)(pp % a.CI);                         // channel of the group's first plane
+    int buf = 0;
+    if (async_in) issue(pp, c0, 0);
+    for (; pp < planes; pp += step) {
+        const int np = (int)min((long long)ppw, planes - pp);
+        const int nel = np * HW;
+        __syncwarp();                                  // the previous group is read and written out
+        int cn = c0 + cstep;
+        if (cn >= a.CI) cn -= a.CI;
+        if (async_in) {
+            issue(pp + step, cn, buf ^ 1);
+            cp_async_wait<1>();                        // this lane's copies of the group
+        } else {
+            // 16-bit rows of odd length: the np planes (one contiguous run of
+            // the input) element by element
+            ST *tw = reinterpret_cast<ST *>(wb);
+            const char *src = static_cast<const char *>(x) + (size_t)pp * HW * ES;
+            if ((reinterpret_cast<uintptr_t>(src) & 15) == 0 && nel % VE == 0) {
+                const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
+                for (int v = lane; v < nel / VE; v += 32) {
+                    const uint4 u = __ldg(s4 + v);
+                    const int4 o0 = reinterpret_cast<const int4 *>(tab)[2 * v];
+                    const int4 o1 = reinterpret_cast<const int4 *>(tab)[2 * v + 1];
+                    tw[o0.x] = (ST)u.x, tw[o0.y] = (ST)(u.x >> 16);
+                    tw[o0.z] = (ST)u.y, tw[o0.w] = (ST)(u.y >> 16);
+                    tw[o1.x] = (ST)u.z, tw[o1.y] = (ST)(u.z >> 16);
+                    tw[o1.z] = (ST)u.w, tw[o1.w] = (ST)(u.w >> 16);
+                }
+            } else {
+                const ST *xs = reinterpret_cast<const ST *>(src);
+                for (int i = lane; i < nel; i += 32) tw[tab[i]] = xs[i];
+            }
+        }
+        __syncwarp();                                  // every lane's copies are visible
+        const bool active = pl < np && t < tpp;
+        uint32_t c;
+        fd_divmod((uint32_t)(c0 + pl), fd_ci, &c);
+        float acc[TY][TX];
+#pragma unroll
+        for (int oy = 0; oy < TY; ++oy)
+#pragma unroll
+            for (int ox = 0; ox < TX; ++ox) acc[oy][ox] = 0.f;
+        if (active) {
+            float wr[K][K];
+            if (async_w) {
+                const char *ws = wgt + buf * wsb + pl * WS * 4 + ((c * KK * ES) & 3);
+#pragma unroll
+                for (int k = 0; k < KK; ++k) {
+                    if constexpr (ES == 4)
+                        wr[k / K][k % K] = reinterpret_cast<const float *>(ws)[k];
+                    else if (DT == BIGEMM_F16)
+                        wr[k / K][k % K] = __half2float(reinterpret_cast<const __half *>(ws)[k]);
+                    else
+                        wr[k / K][k % K] =
+                            __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(ws)[k]);
+                }
+            } else {
+#pragma unroll
+                for (int ky = 0; ky < K; ++ky)
+#pragma unroll
+                    for (int kx = 0; kx < K; ++kx)
+                        wr[ky][kx] = ld_in(w, (size_t)c * KK + ky * K + kx, DT);
+            }
+            // padded coordinates: output (y, x) reads rows y .. y + K - 1 and
+            // columns x + C0 - P .. x + C0 + P
+            const ST *base = reinterpret_cast<const ST *>(wb + buf * stg) + pl * tstride +
+                             oy0 * pitch + ox0;
+#pragma unroll
+            for (int i = 0; i < TY + K - 1; ++i) {
+                float row[WX];
+                if constexpr (ES == 4) {
+#pragma unroll
+                    for (int j = 0; j < WX; ++j) row[j] = base[i * pitch + C0 - P + j];
+                } else {
+                    // pairs from the even element at or before the window's first
+                    // (pitch, plane stride and ox0 are even)
+                    constexpr int SK = C0 - P;                  // 0 or 1 elements to skip
+                    constexpr int NPR = (WX + SK + 1) / 2;
+                    const uint32_t *r32 = reinterpret_cast<const uint32_t *>(base + i * pitch);
+                    float e[2 * NPR];
+#pragma unroll
+                    for (int j = 0; j < NPR; ++j) {
+                        const float2 f = DwStage<DT>::pair(r32[j]);
+                        e[2 * j] = f.x, e[2 * j + 1] = f.y;
+                    }
+#pragma unroll
+                    for (int j = 0; j < WX; ++j) row[j] = e[j + SK];
+                }
+#pragma unroll
+                for (int oy = 0; oy < TY; ++oy) {
+                    const int ky = i - oy;
+                    if (ky >= 0 && ky < K) {
+#pragma unroll
+                        for (int ox = 0; ox < TX; ++ox)
+#pragma unroll
+                            for (int kx = 0; kx < K; ++kx)
+                                acc[oy][ox] = fmaf(row[ox + kx], wr[ky][kx], acc[oy][ox]);
+                    }
+                }
+            }
+            if (a.epi != BIGEMM_EPI_NONE) {
+                const float bv = bias[c];
+                float *f = &acc[0][0];
+                switch (a.epi) {
+                case BIGEMM_EPI_BIAS:
+#pragma unroll
+                    for (int j = 0; j < TY * TX; ++j) f[j] += bv;
+                    break;
+                case BIGEMM_EPI_BIAS_EXP:
+#pragma unroll
+                    for (int j = 0; j < TY * TX; ++j) f[j] = expf(f[j] + bv);
+                    break;
+                case BIGEMM_EPI_BIAS_RSQRT:
+#pragma unroll
+                    for (int j = 0; j < TY * TX; ++j) f[j] = rsqrtf(f[j] + bv + a.eps);
+                    break;
+                case BIGEMM_EPI_BIAS_RELU:
+#pragma unroll
+                    for (int j = 0; j < TY * TX; ++j) f[j] = fmaxf(f[j] + bv, 0.f);
+                    break;
+                default:
+#pragma unroll
+                    for (int j = 0; j < TY * TX; ++j) f[j] = 1.0f / (f[j] + bv);
+                }
+            }
+            if (a.out_dt == BIGEMM_F32)
+                dw_put_block<BIGEMM_F32, TY>(ob, acc, pl, HW, a.W, a.Ho, a.Wo, oy0, ox0);
+            else if (a.out_dt == BIGEMM_F16)
+                dw_put_block<BIGEMM_F16, TY>(ob, acc, pl, HW, a.W, a.Ho, a.Wo, oy0, ox0);
+            else
+                dw_put_block<BIGEMM_BF16, TY>(ob, acc, pl, HW, a.W, a.Ho, a.Wo, oy0, ox0);
+        }
+        __syncwarp();
+        // the group's outputs are one contiguous run too (Ho = H, Wo = W)
+        char *dst = static_cast<char *>(out) + (size_t)pp * HW * ESO;
+        const int nb = nel * ESO;
+        if ((reinterpret_cast<uintptr_t>(dst) & 15) == 0 && nb % 16 == 0) {
+            for (int v = lane; v < nb / 16; v += 32)
+                reinterpret_cast<uint4 *>(dst)[v] = reinterpret_cast<const uint4 *>(ob)[v];
+        } else if (ESO == 4) {
+            for (int i = lane; i < nel; i += 32)
+                reinterpret_cast<float *>(dst)[i] = reinterpret_cast<const float *>(ob)[i];
+        } else {
+            for (int i = lane; i < nel; i += 32)
+                reinterpret_cast<uint16_t *>(dst)[i] = reinterpret_cast<const uint16_t *>(ob)[i];
+        }
+        c0 = cn;
+        if (async_in) buf ^= 1;
+    }
+    cp_async_wait<0>();
+}
+
+// The small-plane kernel's geometry for a shape and block height TY: threads
+// per plane, planes per warp, column blocks, the staging row pitch and plane
+// stride (elements), each warp's shared bytes (staging, weights, compact
+// outputs) and the dynamic shared memory of a block; false when it does not
+// apply.
+struct DwSmallGeom {
+    int tpp, ppw, bxn, pitch, tstride, wbytes;
+    size_t smem;
+};
+
+constexpr size_t kDwrSmemMax = 96 * 1024;
+
+bool dw_small_geom_search(const ConvShape &s, int TY, DwSmallGeom &g)
+{
+    if (!(s.groups > 1 && s.groups == s.CI && s.CO == s.CI)) return false;
+    if (s.KH != s.KW || s.pad != s.KH / 2 || s.stride != 1) return false;
+    if (!(s.KH == 3 || s.KH == 5 || s.KH == 7)) return false;
+    if (!(TY == 2 || TY == 4)) return false;
+    if (s.Wo > 2 * kDwrTX || s.Ho > 32) return false;
+    const int K = s.KH;
+    const int es = dtype_size(s.in_dt), eso = dtype_size(s.out_dt);
+    const int step = es == 2 ? 2 : 1;        // 16-bit rows are read as pairs: even offsets
+    g.bxn = (s.Wo + kDwrTX - 1) / kDwrTX;
+    const int rb = (s.Ho + TY - 1) / TY;
+    g.tpp = g.bxn * rb;
+    if (g.tpp > 32) return false;
+    // interior at column dwr_c0, right border K/2 wide; 16-bit rows keep one
+    // more column, read (and dropped) by the last pair of a window
+    const int c0 = dwr_c0(K, es), extra = es == 2 ? 1 : 0;
+    const int pmin = (g.bxn * kDwrTX + c0 + K / 2 + extra + step - 1) / step * step;
+    const int rows = rb * TY + K - 1;
+    const int HW = s.H * s.W;
+    // as many planes per warp as fill its lanes, fewer where a block's shared
+    // memory would pass the limit
+    for (g.ppw = 32 / g.tpp; g.ppw >= 1; --g.ppw) {
+        // the row pitch and plane stride (padding of up to 31 elements each)
+        // that put the fewest lanes of a warp on one bank when they read their
+        // windows: the lanes read at the same offset from their first word, so
+        // the first words' banks decide; then the smallest stride
+        int best_conf = 1 << 30;
+        for (int pitch = pmin; pitch < pmin + 32; pitch += step)
+            for (int ts = rows * pitch; ts < rows * pitch + 32; ts += step) {
+                int cnt[32] = {0}, worst = 0;
+                for (int l = 0; l < g.ppw * g.tpp; ++l) {
+                    const int pl = l / g.tpp, t = l - pl * g.tpp;
+                    const int off = pl * ts + (t / g.bxn) * TY * pitch + (t % g.bxn) * kDwrTX;
+                    worst = std::max(worst, ++cnt[(off / step) & 31]);
+                }
+                if (worst < best_conf || (worst == best_conf && ts < g.tstride))
+                    best_conf = worst, g.pitch = pitch, g.tstride = ts;
+            }
+        // the element table (one int per element or pair of a group), then per
+        // warp two staging buffers, two weight buffers and the compact
+        // outputs, each rounded to 16 bytes
+        const bool pairs = es == 2 && (s.W & 1) == 0;
+        const size_t tab = (size_t)(((pairs ? g.ppw * HW / 2 : g.ppw * HW) + 3) & ~3) * 4;
+        const size_t stg = ((size_t)g.ppw * g.tstride * es + 15) & ~(size_t)15;
+        const size_t wsb = ((size_t)g.ppw * dwr_wslot(K, es) * 4 + 15) & ~(size_t)15;
+        const size_t obuf = ((size_t)g.ppw * HW * eso + 15) & ~(size_t)15;
+        g.wbytes = (int)(2 * stg + 2 * wsb + obuf);
+        g.smem = tab + kDwrWarps * (size_t)g.wbytes;
+        if (g.smem <= kDwrSmemMax) return true;
+    }
+    return false;
+}
+
+// The search above runs once per shape and TY: plans and launches look it up.
+bool dw_small_geom(const ConvShape &s, int TY, DwSmallGeom &g)
+{
+    static std::mutex mu;
+    using Key = std::tuple<int, int, int, int, int, int, int, int, int, int>;
+    static std::map<Key, std::pair<bool, DwSmallGeom>> memo;
+    const Key key(s.groups == s.CI && s.CO == s.CI && s.groups > 1 ? 1 : 0, s.Ho, s.Wo, s.KH,
+                  s.KW, s.pad, s.stride, s.in_dt, s.out_dt, TY);
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = memo.find(key);
+    if (it == memo.end()) {
+        DwSmallGeom found{};
+        const bool ok = dw_small_geom_search(s, TY, found);
+        it = memo.emplace(key, std::make_pair(ok, found)).first;
+    }
+    g = it->second.second;
+    return it->second.first;
+}
+
 }  // namespace
+
+// Resident blocks per SM of a small-plane kernel with this much
+// dynamic shared memory (looked up once per kernel and size).
+int dw_small_blocks_per_sm(const void *kern, size_t smem)
+{
+    static std::mutex mu;
+    static std::map<std::pair<const void *, size_t>, int> memo;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = memo.find({kern, smem});
+    if (it != memo.end()) return it->second;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kDwrWarps * 32, smem) != cudaSuccess ||
+        n < 1)
+        n = 1;
+    memo[{kern, smem}] = n;
+    return n;
+}
+
+bool dw_small_ok(const ConvShape &s, int TY)
+{
+    DwSmallGeom g;
+    if (!dw_small_geom(s, TY, g)) return false;
+    DeviceState *ds = device_state();
+    return !ds || g.smem <= (size_t)ds->max_smem_optin;
+}
+
+cudaError_t launch_dw_small(const ConvShape &s, const void *x, const void *w, const float *bias,
+                            float eps, void *out, int TY, cudaStream_t stream)
+{
+    DwSmallGeom g;
+    if (!dw_small_geom(s, TY, g)) return cudaErrorInvalidValue;
+    ProfScope prof("simt_conv_depthwise", stream);
+    const SimtArgs a = make_args(s, eps);
+    const long long planes = (long long)s.N * s.CI;
+    DeviceState *ds = device_state();
+    const int sms = ds ? ds->sm_count : 148;
+    const long long warps_needed = (planes + g.ppw - 1) / g.ppw;
+    const FastDiv fdw = make_fastdiv((uint32_t)s.W), fdhw = make_fastdiv((uint32_t)(s.H * s.W));
+    const FastDiv fdci = make_fastdiv((uint32_t)s.CI);
+    auto go = [&](auto kern) {
+        if (g.smem > 48 * 1024) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)g.smem);
+            if (e != cudaSuccess) return e;
+        }
+        // one wave of resident blocks: each warp builds its table and zero
+        // border once and then takes group after group of planes
+        const int bps = dw_small_blocks_per_sm(reinterpret_cast<const void *>(kern), g.smem);
+        long long blocks =
+            std::min<long long>((warps_needed + kDwrWarps - 1) / kDwrWarps, (long long)sms * bps);
+        if (blocks < 1) blocks = 1;
+        return launch_pdl(kern, dim3((unsigned)blocks), dim3(kDwrWarps * 32), g.smem, stream, a,
+                          g.tpp, g.ppw,
+                          g.bxn, g.pitch, g.tstride, g.wbytes, fdw, fdhw, fdci, x, w, bias, out);
+    };
+#define BIGEMM_DWR(DTV, TYV)                                          \
+    if (s.KH == 3) return go(dw_small_kernel<DTV, 3, TYV>);           \
+    if (s.KH == 5) return go(dw_small_kernel<DTV, 5, TYV>);           \
+    if (s.KH == 7) return go(dw_small_kernel<DTV, 7, TYV>);           \
+    return cudaErrorInvalidValue;
+    if (TY == 2) {
+        if (s.in_dt == BIGEMM_F32) { BIGEMM_DWR(BIGEMM_F32, 2) }
+        if (s.in_dt == BIGEMM_F16) { BIGEMM_DWR(BIGEMM_F16, 2) }
+        BIGEMM_DWR(BIGEMM_BF16, 2)
+    }
+    if (s.in_dt == BIGEMM_F32) { BIGEMM_DWR(BIGEMM_F32, 4) }
+    if (s.in_dt == BIGEMM_F16) { BIGEMM_DWR(BIGEMM_F16, 4) }
+    BIGEMM_DWR(BIGEMM_BF16, 4)
+#undef BIGEMM_DWR
+}
 
 bool dw_stream_ok(const ConvShape &s)
 {

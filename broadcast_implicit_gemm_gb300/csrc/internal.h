@@ -213,6 +213,12 @@ cudaError_t launch_dw_stream(const ConvShape &s, const void *x, const void *w, c
 bool dw_plane_ok(const ConvShape &s);
 cudaError_t launch_dw_plane(const ConvShape &s, const void *x, const void *w, const float *bias,
                             float eps, void *out, cudaStream_t stream);
+// Small-plane depthwise kernel (stride 1, square 3/5/7 with pad K/2, outputs at
+// most 16 wide and 32 tall): whole planes per warp in shared memory, ty x 8
+// outputs per thread (ty = 2 or 4).
+bool dw_small_ok(const ConvShape &s, int ty);
+cudaError_t launch_dw_small(const ConvShape &s, const void *x, const void *w, const float *bias,
+                            float eps, void *out, int ty, cudaStream_t stream);
 // [1, P, 1] => [B0, P, B1]: the per-channel kernel for long rows, bcast_rows
 // for short ones (bcast.cu).
 bool bcast_long_rows(long long B1, int out_dt);

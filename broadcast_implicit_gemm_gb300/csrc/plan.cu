@@ -36,7 +36,7 @@ size_t dw_smem_bytes(const ConvShape &s, int rows);
 
 namespace {
 
-enum SimtVariant { SV_NAIVE = 0, SV_TILED = 1, SV_DW = 2, SV_DWS = 3, SV_DWP = 4 };
+enum SimtVariant { SV_NAIVE = 0, SV_TILED = 1, SV_DW = 2, SV_DWS = 3, SV_DWP = 4, SV_DWR = 5 };
 
 struct Cand {
     int kind = BIGEMM_KIND_SIMT;
@@ -65,7 +65,8 @@ std::string cand_str(const Cand &c)
         snprintf(b, sizeof b, "simt:depthwise:stream%d", c.dw_rows);
     else if (c.simt_variant == SV_DWP)
         snprintf(b, sizeof b, "simt:depthwise:plane");
-
+    else if (c.simt_variant == SV_DWR)
+        snprintf(b, sizeof b, "simt:depthwise:small%d", c.dw_rows);
     else
         snprintf(b, sizeof b, "simt:%s", c.simt_variant == SV_TILED ? "tiled" : "naive");
     return b;
@@ -106,6 +107,11 @@ bool parse_cand(const std::string &s, Cand &c)
         return true;
     }
     if (s == "simt:depthwise:plane") return c = Cand{}, c.simt_variant = SV_DWP, true;
+    if (sscanf(s.c_str(), "simt:depthwise:small%d", &g) == 1 && (g == 2 || g == 4)) {
+        c = Cand{};
+        c.simt_variant = SV_DWR, c.dw_rows = g;
+        return true;
+    }
     if (s == "simt:tiled") return c = Cand{}, c.simt_variant = SV_TILED, true;
     if (s == "simt:naive") return c = Cand{}, c.simt_variant = SV_NAIVE, true;
     return false;
@@ -410,6 +416,11 @@ bool simt_valid(const ConvShape &s, const Cand &c, std::string *why)
     if (c.simt_variant == SV_DWP && !dw_plane_ok(s))
         return why && (*why = "plane depthwise needs a streaming-kernel shape with H, W <= 32", true),
                false;
+    if (c.simt_variant == SV_DWR && !dw_small_ok(s, c.dw_rows))
+        return why && (*why = "small-plane depthwise needs a square 3/5/7 kernel, pad K/2, stride 1 "
+                              "and outputs at most 16 wide, 32 tall",
+                       true),
+               false;
     if (c.simt_variant == SV_DWS && !dw_stream_ok(s))
         return why && (*why = "streaming depthwise needs a square 3/5/7 kernel, pad K/2, stride 1-2",
                        true),
@@ -549,6 +560,13 @@ bool direct_ok(const ConvShape &s)
 Cand heuristic(const ConvShape &s, int sms)
 {
     Cand c;
+    // small planes: whole planes per warp (4-row blocks above 8 rows)
+    for (int ty : {s.Ho > 8 ? 4 : 2, 2})
+        if (dw_small_ok(s, ty)) {
+            c.simt_variant = SV_DWR;
+            c.dw_rows = ty;
+            return c;
+        }
     if (dw_stream_ok(s)) {
         c.simt_variant = SV_DWS;
         c.dw_rows = 2;
@@ -587,6 +605,13 @@ std::vector<Cand> candidates(const ConvShape &s, int sms)
 {
     std::vector<Cand> v;
     if (is_depthwise(s)) {
+        for (int ty : {4, 2})
+            if (dw_small_ok(s, ty)) {
+                Cand c;
+                c.simt_variant = SV_DWR;
+                c.dw_rows = ty;
+                v.push_back(c);
+            }
         if (dw_plane_ok(s)) {
             Cand c;
             c.simt_variant = SV_DWP;
@@ -941,7 +966,9 @@ bigemm_status run_plan(bigemm_plan_s *p, const void *data, const void *kernel, c
     if (!ds) return BIGEMM_ERR_CUDA;
     cudaError_t e = cudaSuccess;
     if (p->c.kind != BIGEMM_KIND_UMMA) {
-        if (p->c.simt_variant == SV_DWP)
+        if (p->c.simt_variant == SV_DWR)
+            e = launch_dw_small(s, data, kernel, bias, eps, out, p->c.dw_rows, st);
+        else if (p->c.simt_variant == SV_DWP)
             e = launch_dw_plane(s, data, kernel, bias, eps, out, st);
         else if (p->c.simt_variant == SV_DWS)
             e = launch_dw_stream(s, data, kernel, bias, eps, out, p->c.dw_rows, st);
@@ -1298,8 +1325,9 @@ bigemm_status plan_impl(int N, int H, int W, int CO, int CI, int KH, int KW, int
             if (opts->kind == BIGEMM_KIND_SIMT && opts->mode != 0) {
                 // an explicit SIMT kernel: 1 tiled (groups = 1) or naive, 2 depthwise staged
                 // band (box_h rows per block), 3 depthwise streaming (box_h rows per thread),
-                // 4 depthwise whole planes (H, W <= 32)
-                if (opts->mode < 1 || opts->mode > 4) return BIGEMM_ERR_INVALID_ARG;
+                // 4 depthwise whole planes (H, W <= 32), 5 depthwise small planes (stride 1,
+                // outputs at most 16 x 32; box_h = 2 or 4 output rows per thread)
+                if (opts->mode < 1 || opts->mode > 5) return BIGEMM_ERR_INVALID_ARG;
                 c = Cand{};
                 if (opts->mode == 1) {
                     c.simt_variant = groups == 1 ? SV_TILED : SV_NAIVE;
@@ -1308,6 +1336,10 @@ bigemm_status plan_impl(int N, int H, int W, int CO, int CI, int KH, int KW, int
                     c.dw_rows = opts->box_h > 0 ? opts->box_h : 8;
                 } else if (opts->mode == 4) {
                     c.simt_variant = SV_DWP;
+                } else if (opts->mode == 5) {
+                    c.simt_variant = SV_DWR;
+                    c.dw_rows = opts->box_h > 0 ? opts->box_h : 4;
+                    if (c.dw_rows != 2 && c.dw_rows != 4) return BIGEMM_ERR_INVALID_ARG;
                 } else {
                     c.simt_variant = SV_DWS;
                     c.dw_rows = opts->box_h > 0 ? opts->box_h : 2;

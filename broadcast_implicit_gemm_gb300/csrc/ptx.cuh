@@ -186,6 +186,20 @@ __device__ __forceinline__ void tma_reduce_add_4d(const CUtensorMap *map, const 
         : "memory");
 }
 
+// 4-byte asynchronous global -> shared copy through L1; a thread's copies
+// complete in commit-group order (cp_async_wait<N>: all but the newest N groups)
+__device__ __forceinline__ void cp_async4(void *dst_smem, const void *src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst_smem)), "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 // Wait until at most N committed bulk groups are still reading shared memory.

@@ -118,7 +118,11 @@ typedef struct {
                        (groups = 1) or naive, 2 depthwise staged band (box_h
                        rows per block), 3 depthwise streaming (box_h = 2, 4
                        or 8 rows per thread), 4 depthwise whole planes
-                       (H, W <= 32, one or two planes per warp).
+                       (H, W <= 32, one or two planes per warp), 5 depthwise
+                       small planes (stride 1, square 3/5/7 kernel, pad K/2,
+                       outputs at most 16 wide and 32 tall; each thread
+                       computes a box_h x 8 block of outputs, box_h = 2 or 4,
+                       0 meaning 4).
                        Other values: INVALID_ARG.                               */
     int resident_b; /* UMMA: 1 keeps the weights resident in shared memory --
                        halo modes: one output-channel tile must cover CO and

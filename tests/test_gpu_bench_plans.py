@@ -50,6 +50,9 @@ def cand_options(cand):
                 "cta_pair": 1 if "pair" in flags else -1}
     if cand == "simt:depthwise:plane":
         return {"kind": bg.KIND_SIMT, "mode": 4}
+    m = re.match(r"simt:depthwise:small(\d)$", cand)
+    if m:
+        return {"kind": bg.KIND_SIMT, "mode": 5, "box_h": int(m.group(1))}
     m = re.match(r"simt:depthwise:(stream|rows)(\d+)$", cand)
     if m:
         return {"kind": bg.KIND_SIMT, "mode": 3 if m.group(1) == "stream" else 2,

@@ -521,7 +521,11 @@ DW = [
 @pytest.mark.parametrize("spec", DW, ids=lambda s: s.name)
 def test_depthwise_heuristic(spec):
     info = check(spec)
-    assert info["cand"].startswith("simt:depthwise:stream")
+    # stride 1 with outputs at most 16 wide and 32 tall: the small-plane kernel
+    if spec.stride == 1 and spec.W <= 16 and spec.H <= 32:
+        assert info["cand"] == f"simt:depthwise:small{4 if spec.H > 8 else 2}"
+    else:
+        assert info["cand"].startswith("simt:depthwise:stream")
 
 
 @pytest.mark.parametrize("rows", [2, 4, 8])
@@ -550,6 +554,52 @@ DW_PLANE = [x for x in DW if x.H <= 32 and x.W <= 32] + [
 def test_depthwise_whole_planes(spec):
     info = check(spec, {"kind": bg.KIND_SIMT, "mode": 4})
     assert info["cand"] == "simt:depthwise:plane"
+
+
+# Small planes (stride 1, outputs at most 16 wide and 32 tall), 2 x 8 or 4 x 8
+# outputs per thread: several planes per warp (up to sixteen for 7 x 7), one
+# plane per warp at 16 x 32, ragged column and row blocks, plane counts that
+# leave the last warp short, element counts that rule out the 16-byte staging
+# and output copies, each dtype and epilogue, an fp32 output from 16-bit
+# inputs, K = 3, 5, 7 (a 7x7 over a 1-row image reads only border rows).
+DW_SMALL = [
+    S("dwr_k5_576_like", 2, 24, 24, 14, 14, 5, 1, 2, g=24, kd="dw"),
+    S("dwr_k3_7x7_odd_planes", 1, 7, 7, 7, 7, 3, 1, 1, g=7, kd="dw"),
+    S("dwr_k3_bf16_ragged", 3, 40, 40, 11, 13, 3, 1, 1, g=40, i="bf16", o="bf16", kd="dw"),
+    S("dwr_k7_f32_16x32", 2, 6, 6, 32, 16, 7, 1, 3, g=6, i="f32", o="f32", kd="dw"),
+    S("dwr_k5_f16_bias_exp", 2, 16, 16, 9, 12, 5, 1, 2, g=16, o="f32", epi="bias_exp", kd="dw"),
+    S("dwr_k3_rsqrt", 1, 16, 16, 16, 16, 3, 1, 1, g=16, o="f32", epi="bias_rsqrt", dd="absnormal",
+      kd="dw"),
+    S("dwr_k3_recip", 2, 12, 12, 5, 6, 3, 1, 1, g=12, epi="bias_recip", dd="absnormal",
+      kd="absnormal"),
+    S("dwr_k7_relu_bf16", 1, 10, 10, 12, 15, 7, 1, 3, g=10, i="bf16", o="bf16", epi="bias_relu",
+      kd="dw"),
+    S("dwr_k7_one_row", 2, 8, 8, 1, 9, 7, 1, 3, g=8, kd="dw"),
+    S("dwr_k5_f32_bias_3x3", 3, 9, 9, 3, 3, 5, 1, 2, g=9, i="f32", o="f32", epi="bias", kd="dw"),
+]
+
+
+@pytest.mark.parametrize("ty", [2, 4])
+@pytest.mark.parametrize("spec", DW_SMALL, ids=lambda s: s.name)
+def test_depthwise_small_planes(spec, ty):
+    info = check(spec, {"kind": bg.KIND_SIMT, "mode": 5, "box_h": ty})
+    assert info["cand"] == f"simt:depthwise:small{ty}"
+
+
+@pytest.mark.parametrize("shape", [(14, 17, 3, 1), (33, 8, 3, 1), (14, 14, 3, 2), (14, 14, 4, 1)])
+def test_depthwise_small_planes_rejects_other_shapes(shape):
+    H, W, K, stride = shape
+    with pytest.raises(bg.BigemmError) as e:
+        bg.conv2d_nchw_plan_ex(1, H, W, 8, 8, K, K, stride, K // 2, 8, bg.F16, bg.F16,
+                               bg.EPI_NONE, 0, {"kind": bg.KIND_SIMT, "mode": 5})
+    assert e.value.status == 2
+
+
+def test_depthwise_small_planes_rejects_other_block_heights():
+    with pytest.raises(bg.BigemmError) as e:
+        bg.conv2d_nchw_plan_ex(1, 14, 14, 8, 8, 3, 3, 1, 1, 8, bg.F16, bg.F16, bg.EPI_NONE, 0,
+                               {"kind": bg.KIND_SIMT, "mode": 5, "box_h": 3})
+    assert e.value.status == 1
 
 
 def test_depthwise_whole_planes_rejects_wide_rows():
