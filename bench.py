@@ -13,8 +13,8 @@ general [B0,P,B1] form), the depthwise layers (N=64), the fp32 batch-1 layer
 sweep and the N=1 512->512 7x7 layer.  --workload W --only measures one.
 
 Timing: W untimed warm-up steps; K timed steps, each bracketed by CUDA events
-on the launch stream, with an L2 flush (a 512 MB write) between steps outside
-the events.  A second pass of K steps, also timed, adds the library's own
+on the launch stream, with an L2 flush (a 512 MB write, then a 512 MB read that
+drains the write's dirty lines) between steps outside the events.  A second pass of K steps, also timed, adds the library's own
 per-kernel event records and an event after every layer; the roofline and the
 per-layer figures come from it (those events serialise the launches, so it is
 reported separately as profiled_ms_per_step).  `e2e` repeats the
@@ -318,13 +318,30 @@ def bg_long_rows(B1, esize=4):
     return B1 * esize >= 1024
 
 
+class L2Flush:
+    """Evicts the previous step's data from L2 between timed steps: a write of
+    a buffer four times L2's size, then a read of a second one, so that the
+    write's dirty lines are written back during the read -- before the next
+    step's events, not inside its first layer -- and L2 is left holding clean
+    lines of neither the workload's inputs nor its outputs."""
+
+    def __init__(self, torch, device):
+        self.wr = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+        self.rd = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+        self.torch = torch
+
+    def __call__(self):
+        self.wr.fill_(1)
+        self.torch.sum(self.rd)
+
+
 def timed_steps(step_fn, steps, torch, stream, flush):
     """Per-step CUDA event pairs (ms), with an L2 flush before each step."""
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(steps)]
     with torch.cuda.stream(stream):
         for a, b in evs:
-            flush.fill_(1)
+            flush()
             a.record(stream)
             step_fn(stream)
             b.record(stream)
@@ -583,7 +600,7 @@ def measure(name, args, device, stream, flush, peaks, world, dist, local):
     if name == "bcast":
         line["dtype"] = "f32"
         line["config"] = {"workload": "bcast_exp_[128,256,32,32]_fp32", "op": "exp",
-                          "l2": "output (134 MB) larger than L2; 512 MB flush between steps"}
+                          "l2": "output (134 MB) larger than L2; flushed between steps (512 MB write, 512 MB read)"}
         n, tms = prof.get("bcast_nchw", (args.steps, total_ms))
         ach = step.work() / (tms / n / 1e3) / 1e9
         # A/B: the per-channel mapping against the flat fused-index schedule, per op
@@ -627,7 +644,7 @@ def measure(name, args, device, stream, flush, peaks, world, dist, local):
                           "layers": [it["spec"].name for it in step.items],
                           "batch": step.items[0]["spec"].N,
                           "plans": [it["info"]["cand"] for it in step.items],
-                          "l2": "flushed between steps (512 MB write)"}
+                          "l2": "flushed between steps (512 MB write, 512 MB read)"}
         # per-layer device time from the marks recorded after each layer
         layer_ms = [0.0] * len(step.items)
         starts = [a for a, _ in evs]
@@ -712,7 +729,7 @@ def main():
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     stream = torch.cuda.Stream(device)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    flush = L2Flush(torch, device)
     peaks = load_peaks()
 
     head = measure(args.workload, args, device, stream, flush, peaks, world, dist, local)
