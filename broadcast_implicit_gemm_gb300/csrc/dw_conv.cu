@@ -437,6 +437,16 @@ struct DwStage {                 // 16-bit inputs: raw halves, converted in pair
         if (DT == BIGEMM_F16) return __half22float2(*reinterpret_cast<const __half2 *>(&w));
         return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w));
     }
+    // one element of a pair: the low (hi = 0) or the high half
+    __device__ static float half(uint32_t w, int hi)
+    {
+        if (DT == BIGEMM_F16) {
+            const __half2 h = *reinterpret_cast<const __half2 *>(&w);
+            return hi ? __high2float(h) : __low2float(h);
+        }
+        const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162 *>(&w);
+        return hi ? __high2float(h) : __low2float(h);
+    }
 };
 template <>
 struct DwStage<BIGEMM_F32> {
@@ -799,6 +809,250 @@ bool dw_small_geom(const ConvShape &s, int TY, DwSmallGeom &g)
     return it->second.first;
 }
 
+// Bands of large planes (rows of 16-byte multiples, at most 512 bytes): a warp
+// takes a run of (plane, band) items -- a band is rbw x 4 output rows of one
+// plane, all its columns -- and stages each band's input rows in its shared
+// memory with 16-byte cp.async copies, inside a zero border (left and right
+// columns written once, rows outside the plane zeroed per band), the next
+// band arriving while the current one is computed.  Each thread computes a
+// 4-row x 8-column block (rbw row blocks x bxn column blocks per warp) as the
+// small-plane kernel does, with stride S, and writes each output row's 8
+// values with one 16-byte store (two for fp32).  A warp's items are
+// consecutive, so its weights are loaded once per plane.
+constexpr int kDwbTY = 4;
+
+template <int DT, int K, int S>
+__global__ void __launch_bounds__(kDwrWarps * 32, 4)
+dw_band_kernel(SimtArgs a, int bxn, int rbw, int nbands, int ir, int pitch, int wbytes, int ipw,
+               FastDiv fd_nb, FastDiv fd_ci, const void *__restrict__ x, const void *__restrict__ w,
+               const float *__restrict__ bias, void *__restrict__ out)
+{
+    constexpr int P = K / 2, TX = kDwrTX, TY = kDwbTY, KK = K * K;
+    constexpr int ES = DT == BIGEMM_F32 ? 4 : 2;
+    constexpr int C0 = 16 / ES;                        // left border: 16 bytes
+    constexpr int WXS = (TX - 1) * S + K;              // window columns of a thread
+    constexpr int NR = (TY - 1) * S + K;               // window rows of a thread
+    using ST = typename DwStage<DT>::T;
+    extern __shared__ __align__(16) char dwb_smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    char *wb = dwb_smem + (size_t)warp * wbytes;
+    const int stg = (ir * pitch * ES + 15) & ~15;
+    for (int i = lane; i < 2 * stg / 16; i += 32)
+        reinterpret_cast<uint4 *>(wb)[i] = make_uint4(0u, 0u, 0u, 0u);
+    __syncwarp();
+    griddep_enter();
+    const int cw = a.W * ES / 16;                      // 16-byte chunks of an input row
+    const int rpi = 32 / cw;                           // rows copied per pass of the warp
+    const int rr = lane / cw, ck = lane - rr * cw;
+    const int by = lane / bxn, bx = lane - by * bxn;   // the thread's row block, column block
+    const bool active = by < rbw;
+    const int ox0 = bx * TX;
+    const int items = a.N * a.CI * nbands;
+    const int it0 = ((int)blockIdx.x * kDwrWarps + warp) * ipw;
+    const int it1 = min(items, it0 + ipw);
+    const size_t plane_in = (size_t)a.H * a.W, plane_out = (size_t)a.Ho * a.Wo;
+    // the input rows of item `item` into buffer b
+    auto issue = [&](int item, int b) {
+        if (item < it1) {
+            uint32_t band;
+            const uint32_t plane = fd_divmod((uint32_t)item, fd_nb, &band);
+            const int iy0 = (int)band * rbw * TY * S - P;
+            const char *src = static_cast<const char *>(x) + plane * plane_in * ES;
+            char *dst = wb + b * stg + C0 * ES + ck * 16;
+            if (rr < rpi)
+                for (int r = rr; r < ir; r += rpi) {
+                    const int iy = iy0 + r;
+                    char *d = dst + (size_t)r * pitch * ES;
+                    if (iy >= 0 && iy < a.H)
+                        cp_async16(d, src + (size_t)iy * a.W * ES + ck * 16);
+                    else
+                        *reinterpret_cast<uint4 *>(d) = make_uint4(0u, 0u, 0u, 0u);
+                }
+        }
+        cp_async_commit();
+    };
+    float wr[K][K];
+    int wplane = -1;
+    int buf = 0;
+    if (it0 < it1) issue(it0, 0);
+    for (int item = it0; item < it1; ++item) {
+        __syncwarp();                                  // the previous band is read
+        issue(item + 1, buf ^ 1);
+        cp_async_wait<1>();                            // this lane's copies of the band
+        __syncwarp();                                  // every lane's copies and zeros are visible
+        uint32_t band;
+        const uint32_t plane = fd_divmod((uint32_t)item, fd_nb, &band);
+        uint32_t c;
+        fd_divmod(plane, fd_ci, &c);
+        if ((int)plane != wplane) {
+            wplane = (int)plane;
+#pragma unroll
+            for (int k = 0; k < KK; ++k) wr[k / K][k % K] = ld_in(w, (size_t)c * KK + k, DT);
+        }
+        const int y0 = (int)band * rbw * TY + by * TY;   // the thread's first output row
+        if (active && y0 < a.Ho && ox0 < a.Wo) {
+            float acc[TY][TX];
+#pragma unroll
+            for (int oy = 0; oy < TY; ++oy)
+#pragma unroll
+                for (int ox = 0; ox < TX; ++ox) acc[oy][ox] = 0.f;
+            // band-local row (by * TY + oy) * S + ky, column ox * S + kx + C0 - P
+            const ST *base = reinterpret_cast<const ST *>(wb + buf * stg) +
+                             (size_t)by * TY * S * pitch + ox0 * S;
+            // the window's row i as 16-byte chunks from the thread's first
+            // column (16-byte aligned: pitch and ox0 * S are multiples of a chunk)
+            constexpr int EPC = 16 / ES;                       // elements per chunk
+            constexpr int LO = C0 - P;                         // first window element in the run
+            constexpr int NCH = (LO + WXS + EPC - 1) / EPC;
+#pragma unroll
+            for (int i = 0; i < NR; ++i) {
+                float row[WXS];
+                const uint4 *rc = reinterpret_cast<const uint4 *>(base + i * pitch);
+                uint32_t wd[4 * NCH];
+#pragma unroll
+                for (int k = 0; k < NCH; ++k) {
+                    const uint4 u = rc[k];
+                    wd[4 * k] = u.x, wd[4 * k + 1] = u.y, wd[4 * k + 2] = u.z, wd[4 * k + 3] = u.w;
+                }
+#pragma unroll
+                for (int j = 0; j < WXS; ++j) {
+                    const int el = LO + j;
+                    if constexpr (ES == 4)
+                        row[j] = __uint_as_float(wd[el]);
+                    else
+                        row[j] = DwStage<DT>::half(wd[el >> 1], el & 1);
+                }
+#pragma unroll
+                for (int oy = 0; oy < TY; ++oy) {
+                    const int ky = i - oy * S;
+                    if (ky >= 0 && ky < K) {
+#pragma unroll
+                        for (int ox = 0; ox < TX; ++ox)
+#pragma unroll
+                            for (int kx = 0; kx < K; ++kx)
+                                acc[oy][ox] = fmaf(row[ox * S + kx], wr[ky][kx], acc[oy][ox]);
+                    }
+                }
+            }
+            if (a.epi != BIGEMM_EPI_NONE) {
+                const float bv = bias[c];
+                float *f = &acc[0][0];
+                switch (a.epi) {
+                case BIGEMM_EPI_BIAS:
+#pragma unroll
+                    for (int j = 0; j < TY * TX; ++j) f[j] += bv;
+                    break;
+                case BIGEMM_EPI_BIAS_EXP:
+#pragma unroll
+                    for (int j = 0; j < TY * TX; ++j) f[j] = expf(f[j] + bv);
+                    break;
+                case BIGEMM_EPI_BIAS_RSQRT:
+#pragma unroll
+                    for (int j = 0; j < TY * TX; ++j) f[j] = rsqrtf(f[j] + bv + a.eps);
+                    break;
+                case BIGEMM_EPI_BIAS_RELU:
+#pragma unroll
+                    for (int j = 0; j < TY * TX; ++j) f[j] = fmaxf(f[j] + bv, 0.f);
+                    break;
+                default:
+#pragma unroll
+                    for (int j = 0; j < TY * TX; ++j) f[j] = 1.0f / (f[j] + bv);
+                }
+            }
+            const int ESO = a.out_dt == BIGEMM_F32 ? 4 : 2;
+            char *orow = static_cast<char *>(out) + (plane * plane_out + (size_t)y0 * a.Wo + ox0) * ESO;
+            // 16-byte stores: whole 8-column blocks of rows that keep 16-byte alignment
+            const bool vec = ox0 + TX <= a.Wo && (a.Wo * ESO) % 16 == 0 &&
+                             (reinterpret_cast<uintptr_t>(out) & 15) == 0;
+#pragma unroll
+            for (int oy = 0; oy < TY; ++oy) {
+                if (y0 + oy >= a.Ho) break;
+                char *o = orow + (size_t)oy * a.Wo * ESO;
+                if (vec) {
+                    if (a.out_dt == BIGEMM_F32) {
+                        reinterpret_cast<float4 *>(o)[0] =
+                            make_float4(acc[oy][0], acc[oy][1], acc[oy][2], acc[oy][3]);
+                        reinterpret_cast<float4 *>(o)[1] =
+                            make_float4(acc[oy][4], acc[oy][5], acc[oy][6], acc[oy][7]);
+                    } else {
+                        uint32_t pk[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            if (a.out_dt == BIGEMM_F16) {
+                                const __half2 h = __floats2half2_rn(acc[oy][2 * k], acc[oy][2 * k + 1]);
+                                pk[k] = *reinterpret_cast<const uint32_t *>(&h);
+                            } else {
+                                const __nv_bfloat162 h =
+                                    __floats2bfloat162_rn(acc[oy][2 * k], acc[oy][2 * k + 1]);
+                                pk[k] = *reinterpret_cast<const uint32_t *>(&h);
+                            }
+                        }
+                        *reinterpret_cast<uint4 *>(o) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    }
+                } else {
+#pragma unroll
+                    for (int ox = 0; ox < TX; ++ox)
+                        if (ox0 + ox < a.Wo)
+                            st_out(out, plane * plane_out + (size_t)(y0 + oy) * a.Wo + ox0 + ox,
+                                   acc[oy][ox], a.out_dt);
+                }
+            }
+        }
+        buf ^= 1;
+    }
+    cp_async_wait<0>();
+}
+
+// The band kernel's geometry: column blocks, row blocks per warp, bands per
+// plane, input rows per band, the staging row pitch (elements), each warp's
+// shared bytes (two staging buffers) and a block's; false when it does not
+// apply.
+struct DwBandGeom {
+    int bxn, rbw, nbands, ir, pitch, wbytes;
+    size_t smem;
+};
+
+bool dw_band_geom(const ConvShape &s, DwBandGeom &g)
+{
+    if (!(s.groups > 1 && s.groups == s.CI && s.CO == s.CI)) return false;
+    if (s.KH != s.KW || s.pad != s.KH / 2 || !(s.stride == 1 || s.stride == 2)) return false;
+    if (!(s.KH == 3 || s.KH == 5 || s.KH == 7)) return false;
+    const int es = dtype_size(s.in_dt), K = s.KH, S = s.stride, P = K / 2;
+    if ((s.W * es) % 16 != 0 || s.W * es > 512) return false;   // whole 16-byte chunks, <= 32 per row
+    g.bxn = (s.Wo + kDwrTX - 1) / kDwrTX;
+    if (g.bxn > 32) return false;
+    g.rbw = std::min(32 / g.bxn, (s.Ho + kDwbTY - 1) / kDwbTY);
+    const int rows = g.rbw * kDwbTY;
+    g.nbands = (s.Ho + rows - 1) / rows;
+    if ((long long)s.N * s.CI * g.nbands >= (1ll << 31)) return false;
+    g.ir = (rows - 1) * S + K;
+    const int c0 = 16 / es, step = 16 / es;        // rows start on 16-byte boundaries
+    // the last column block's window ends at (bxn * 8 - 1) * S + P (+1 for the
+    // pair read) past the left border
+    const int need = c0 + std::max(s.W, (g.bxn * kDwrTX - 1) * S + P + 2);
+    const int pmin = (need + step - 1) / step * step;
+    // threads read their rows as 16-byte chunks, served a quarter-warp (eight
+    // threads) at a time: the pitch that puts the fewest threads of a quarter
+    // on one 16-byte bank group
+    int best = 1 << 30;
+    for (int pitch = pmin; pitch < pmin + 16 * step; pitch += step) {
+        int worst = 0;
+        for (int q0 = 0; q0 < g.rbw * g.bxn; q0 += 8) {
+            int cnt[8] = {0};
+            for (int l = q0; l < std::min(q0 + 8, g.rbw * g.bxn); ++l) {
+                const int b_y = l / g.bxn, b_x = l - b_y * g.bxn;
+                const int off = b_y * kDwbTY * S * pitch + b_x * kDwrTX * S;   // elements
+                worst = std::max(worst, ++cnt[(off / step) & 7]);
+            }
+        }
+        if (worst < best) best = worst, g.pitch = pitch;
+    }
+    const size_t stg = ((size_t)g.ir * g.pitch * es + 15) & ~(size_t)15;
+    g.wbytes = (int)(2 * stg);
+    g.smem = kDwrWarps * (size_t)g.wbytes;
+    return g.smem <= kDwrSmemMax;
+}
+
 }  // namespace
 
 // Resident blocks per SM of a small-plane kernel with this much
@@ -869,6 +1123,57 @@ cudaError_t launch_dw_small(const ConvShape &s, const void *x, const void *w, co
     if (s.in_dt == BIGEMM_F16) { BIGEMM_DWR(BIGEMM_F16, 4) }
     BIGEMM_DWR(BIGEMM_BF16, 4)
 #undef BIGEMM_DWR
+}
+
+bool dw_band_ok(const ConvShape &s)
+{
+    DwBandGeom g;
+    if (!dw_band_geom(s, g)) return false;
+    DeviceState *ds = device_state();
+    return !ds || g.smem <= (size_t)ds->max_smem_optin;
+}
+
+cudaError_t launch_dw_band(const ConvShape &s, const void *x, const void *w, const float *bias,
+                           float eps, void *out, cudaStream_t stream)
+{
+    DwBandGeom g;
+    if (!dw_band_geom(s, g)) return cudaErrorInvalidValue;
+    ProfScope prof("simt_conv_depthwise", stream);
+    const SimtArgs a = make_args(s, eps);
+    DeviceState *ds = device_state();
+    const int sms = ds ? ds->sm_count : 148;
+    const long long items = (long long)s.N * s.CI * g.nbands;
+    const FastDiv fdnb = make_fastdiv((uint32_t)g.nbands), fdci = make_fastdiv((uint32_t)s.CI);
+    auto go = [&](auto kern) {
+        if (g.smem > 48 * 1024) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)g.smem);
+            if (e != cudaSuccess) return e;
+        }
+        // one wave of resident blocks; each warp takes a run of consecutive items
+        const int bps = dw_small_blocks_per_sm(reinterpret_cast<const void *>(kern), g.smem);
+        const long long warps = std::max<long long>(
+            1, std::min<long long>((long long)sms * bps * kDwrWarps, items));
+        const int ipw = (int)((items + warps - 1) / warps);
+        const long long blocks = ((items + ipw - 1) / ipw + kDwrWarps - 1) / kDwrWarps;
+        return launch_pdl(kern, dim3((unsigned)blocks), dim3(kDwrWarps * 32), g.smem, stream, a,
+                          g.bxn, g.rbw, g.nbands, g.ir, g.pitch, g.wbytes, ipw, fdnb, fdci, x, w,
+                          bias, out);
+    };
+#define BIGEMM_DWB(DTV, SV)                                         \
+    if (s.KH == 3) return go(dw_band_kernel<DTV, 3, SV>);           \
+    if (s.KH == 5) return go(dw_band_kernel<DTV, 5, SV>);           \
+    if (s.KH == 7) return go(dw_band_kernel<DTV, 7, SV>);           \
+    return cudaErrorInvalidValue;
+    if (s.stride == 1) {
+        if (s.in_dt == BIGEMM_F32) { BIGEMM_DWB(BIGEMM_F32, 1) }
+        if (s.in_dt == BIGEMM_F16) { BIGEMM_DWB(BIGEMM_F16, 1) }
+        BIGEMM_DWB(BIGEMM_BF16, 1)
+    }
+    if (s.in_dt == BIGEMM_F32) { BIGEMM_DWB(BIGEMM_F32, 2) }
+    if (s.in_dt == BIGEMM_F16) { BIGEMM_DWB(BIGEMM_F16, 2) }
+    BIGEMM_DWB(BIGEMM_BF16, 2)
+#undef BIGEMM_DWB
 }
 
 bool dw_stream_ok(const ConvShape &s)

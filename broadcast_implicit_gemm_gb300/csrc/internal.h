@@ -217,6 +217,12 @@ cudaError_t launch_dw_plane(const ConvShape &s, const void *x, const void *w, co
 // most 16 wide and 32 tall): whole planes per warp in shared memory, ty x 8
 // outputs per thread (ty = 2 or 4).
 bool dw_small_ok(const ConvShape &s, int ty);
+// Band depthwise kernel (square 3/5/7 with pad K/2, stride 1 or 2, input rows
+// of whole 16-byte chunks up to 512 bytes): bands of rows per warp in shared
+// memory, 4 x 8 outputs per thread.
+bool dw_band_ok(const ConvShape &s);
+cudaError_t launch_dw_band(const ConvShape &s, const void *x, const void *w, const float *bias,
+                           float eps, void *out, cudaStream_t stream);
 cudaError_t launch_dw_small(const ConvShape &s, const void *x, const void *w, const float *bias,
                             float eps, void *out, int ty, cudaStream_t stream);
 // [1, P, 1] => [B0, P, B1]: the per-channel kernel for long rows, bcast_rows

@@ -36,7 +36,7 @@ size_t dw_smem_bytes(const ConvShape &s, int rows);
 
 namespace {
 
-enum SimtVariant { SV_NAIVE = 0, SV_TILED = 1, SV_DW = 2, SV_DWS = 3, SV_DWP = 4, SV_DWR = 5 };
+enum SimtVariant { SV_NAIVE = 0, SV_TILED = 1, SV_DW = 2, SV_DWS = 3, SV_DWP = 4, SV_DWR = 5, SV_DWB = 6 };
 
 struct Cand {
     int kind = BIGEMM_KIND_SIMT;
@@ -67,6 +67,8 @@ std::string cand_str(const Cand &c)
         snprintf(b, sizeof b, "simt:depthwise:plane");
     else if (c.simt_variant == SV_DWR)
         snprintf(b, sizeof b, "simt:depthwise:small%d", c.dw_rows);
+    else if (c.simt_variant == SV_DWB)
+        snprintf(b, sizeof b, "simt:depthwise:band");
     else
         snprintf(b, sizeof b, "simt:%s", c.simt_variant == SV_TILED ? "tiled" : "naive");
     return b;
@@ -107,6 +109,7 @@ bool parse_cand(const std::string &s, Cand &c)
         return true;
     }
     if (s == "simt:depthwise:plane") return c = Cand{}, c.simt_variant = SV_DWP, true;
+    if (s == "simt:depthwise:band") return c = Cand{}, c.simt_variant = SV_DWB, true;
     if (sscanf(s.c_str(), "simt:depthwise:small%d", &g) == 1 && (g == 2 || g == 4)) {
         c = Cand{};
         c.simt_variant = SV_DWR, c.dw_rows = g;
@@ -421,6 +424,11 @@ bool simt_valid(const ConvShape &s, const Cand &c, std::string *why)
                               "and outputs at most 16 wide, 32 tall",
                        true),
                false;
+    if (c.simt_variant == SV_DWB && !dw_band_ok(s))
+        return why && (*why = "band depthwise needs a square 3/5/7 kernel, pad K/2, stride 1-2 and "
+                              "input rows of 16-byte chunks, at most 512 bytes",
+                       true),
+               false;
     if (c.simt_variant == SV_DWS && !dw_stream_ok(s))
         return why && (*why = "streaming depthwise needs a square 3/5/7 kernel, pad K/2, stride 1-2",
                        true),
@@ -612,6 +620,11 @@ std::vector<Cand> candidates(const ConvShape &s, int sms)
                 c.dw_rows = ty;
                 v.push_back(c);
             }
+        if (dw_band_ok(s)) {
+            Cand c;
+            c.simt_variant = SV_DWB;
+            v.push_back(c);
+        }
         if (dw_plane_ok(s)) {
             Cand c;
             c.simt_variant = SV_DWP;
@@ -968,6 +981,8 @@ bigemm_status run_plan(bigemm_plan_s *p, const void *data, const void *kernel, c
     if (p->c.kind != BIGEMM_KIND_UMMA) {
         if (p->c.simt_variant == SV_DWR)
             e = launch_dw_small(s, data, kernel, bias, eps, out, p->c.dw_rows, st);
+        else if (p->c.simt_variant == SV_DWB)
+            e = launch_dw_band(s, data, kernel, bias, eps, out, st);
         else if (p->c.simt_variant == SV_DWP)
             e = launch_dw_plane(s, data, kernel, bias, eps, out, st);
         else if (p->c.simt_variant == SV_DWS)
@@ -1326,8 +1341,9 @@ bigemm_status plan_impl(int N, int H, int W, int CO, int CI, int KH, int KW, int
                 // an explicit SIMT kernel: 1 tiled (groups = 1) or naive, 2 depthwise staged
                 // band (box_h rows per block), 3 depthwise streaming (box_h rows per thread),
                 // 4 depthwise whole planes (H, W <= 32), 5 depthwise small planes (stride 1,
-                // outputs at most 16 x 32; box_h = 2 or 4 output rows per thread)
-                if (opts->mode < 1 || opts->mode > 5) return BIGEMM_ERR_INVALID_ARG;
+                // outputs at most 16 x 32; box_h = 2 or 4 output rows per thread), 6
+                // depthwise bands of rows (input rows of 16-byte chunks, at most 512 bytes)
+                if (opts->mode < 1 || opts->mode > 6) return BIGEMM_ERR_INVALID_ARG;
                 c = Cand{};
                 if (opts->mode == 1) {
                     c.simt_variant = groups == 1 ? SV_TILED : SV_NAIVE;
@@ -1336,6 +1352,8 @@ bigemm_status plan_impl(int N, int H, int W, int CO, int CI, int KH, int KW, int
                     c.dw_rows = opts->box_h > 0 ? opts->box_h : 8;
                 } else if (opts->mode == 4) {
                     c.simt_variant = SV_DWP;
+                } else if (opts->mode == 6) {
+                    c.simt_variant = SV_DWB;
                 } else if (opts->mode == 5) {
                     c.simt_variant = SV_DWR;
                     c.dw_rows = opts->box_h > 0 ? opts->box_h : 4;

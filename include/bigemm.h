@@ -122,7 +122,10 @@ typedef struct {
                        small planes (stride 1, square 3/5/7 kernel, pad K/2,
                        outputs at most 16 wide and 32 tall; each thread
                        computes a box_h x 8 block of outputs, box_h = 2 or 4,
-                       0 meaning 4).
+                       0 meaning 4), 6 depthwise bands of rows (square 3/5/7
+                       kernel, pad K/2, stride 1 or 2, input rows whose bytes
+                       are a multiple of 16 and at most 512; 4 x 8 outputs
+                       per thread).
                        Other values: INVALID_ARG.                               */
     int resident_b; /* UMMA: 1 keeps the weights resident in shared memory --
                        halo modes: one output-channel tile must cover CO and

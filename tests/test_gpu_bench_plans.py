@@ -50,6 +50,8 @@ def cand_options(cand):
                 "cta_pair": 1 if "pair" in flags else -1}
     if cand == "simt:depthwise:plane":
         return {"kind": bg.KIND_SIMT, "mode": 4}
+    if cand == "simt:depthwise:band":
+        return {"kind": bg.KIND_SIMT, "mode": 6}
     m = re.match(r"simt:depthwise:small(\d)$", cand)
     if m:
         return {"kind": bg.KIND_SIMT, "mode": 5, "box_h": int(m.group(1))}

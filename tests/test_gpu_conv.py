@@ -595,6 +595,47 @@ def test_depthwise_small_planes_rejects_other_shapes(shape):
     assert e.value.status == 2
 
 
+# Bands of rows (input rows of 16-byte chunks up to 512 bytes), 4 x 8 outputs
+# per thread, stride 1 and 2: the workload's 112- and 56-wide layers at N = 2,
+# several bands per plane with a ragged last band, rows whose width is not a
+# multiple of 8 outputs (scalar stores), one row block per warp (32 column
+# blocks), fp32 and bf16, fp32 output from 16-bit input, each epilogue, K = 5
+# and 7, a stride-2 layer with an odd input height.
+DW_BAND = [
+    S("dwb_32_112_k3", 2, 32, 32, 112, 112, 3, 1, 1, g=32, kd="dw"),
+    S("dwb_96_112_k3s2", 2, 96, 96, 112, 112, 3, 2, 1, g=96, kd="dw"),
+    S("dwb_144_56_k3", 2, 16, 16, 56, 56, 3, 1, 1, g=16, kd="dw"),
+    S("dwb_ragged_rows_k5", 3, 8, 8, 37, 24, 5, 1, 2, g=8, kd="dw", epi="bias"),
+    S("dwb_wide_256_k3_bf16", 1, 4, 4, 9, 256, 3, 1, 1, g=4, i="bf16", o="bf16", kd="dw"),
+    S("dwb_f32_k7_s2", 2, 6, 6, 29, 64, 7, 2, 3, g=6, i="f32", o="f32", kd="dw"),
+    S("dwb_f32_k3_exp", 2, 8, 8, 20, 20, 3, 1, 1, g=8, i="f32", o="f32", epi="bias_exp", kd="dw"),
+    S("dwb_rsqrt_f32out", 1, 16, 16, 16, 40, 3, 1, 1, g=16, o="f32", epi="bias_rsqrt",
+      dd="absnormal", kd="dw"),
+    S("dwb_recip_s2_odd_h", 2, 8, 8, 31, 48, 3, 2, 1, g=8, epi="bias_recip", dd="absnormal",
+      kd="absnormal"),
+    S("dwb_relu_k7", 1, 12, 12, 21, 72, 7, 1, 3, g=12, i="bf16", o="bf16", epi="bias_relu",
+      kd="dw"),
+    S("dwb_k5_s2_w24", 2, 10, 10, 24, 24, 5, 2, 2, g=10, kd="dw"),
+]
+
+
+@pytest.mark.parametrize("spec", DW_BAND, ids=lambda s: s.name)
+def test_depthwise_bands(spec):
+    info = check(spec, {"kind": bg.KIND_SIMT, "mode": 6})
+    assert info["cand"] == "simt:depthwise:band"
+
+
+@pytest.mark.parametrize("shape", [(16, 20, 3, 1, "f16"), (8, 264, 3, 1, "f16"), (8, 16, 3, 3, "f16"),
+                                   (8, 130, 3, 1, "f32")])
+def test_depthwise_bands_reject_other_shapes(shape):
+    H, W, K, stride, dt = shape
+    d = {"f16": bg.F16, "f32": bg.F32}[dt]
+    with pytest.raises(bg.BigemmError) as e:
+        bg.conv2d_nchw_plan_ex(1, H, W, 8, 8, K, K, stride, K // 2, 8, d, d, bg.EPI_NONE, 0,
+                               {"kind": bg.KIND_SIMT, "mode": 6})
+    assert e.value.status == 2
+
+
 def test_depthwise_small_planes_rejects_other_block_heights():
     with pytest.raises(bg.BigemmError) as e:
         bg.conv2d_nchw_plan_ex(1, 14, 14, 8, 8, 3, 3, 1, 1, 8, bg.F16, bg.F16, bg.EPI_NONE, 0,
