@@ -18,6 +18,7 @@ __all__ = [
     "F32", "F16", "BF16", "EPI_NONE", "EPI_BIAS", "EPI_BIAS_EXP", "EPI_BIAS_RSQRT", "EPI_BIAS_RECIP", "EPI_BIAS_RELU",
     "BC_COPY", "BC_EXP", "BC_RSQRT", "BC_RECIP", "KIND_AUTO", "KIND_UMMA", "KIND_SIMT",
     "MODE_NHWC", "MODE_DIRECT", "MODE_HALO", "MODE_SUB", "MODE_STACK", "MODE_STRIDED",
+    "MODE_IM2COL",
     "BigemmError", "Plan", "PlanOptions", "library_path", "load_library",
     "conv2d_nchw_plan", "conv2d_nchw_plan_ex", "conv2d_nchw_run", "conv2d_nchw_plan_destroy",
     "conv2d_nchw_plan_describe", "conv2d_nchw_run_noalloc", "bcast_nchw_run",
@@ -31,7 +32,7 @@ F32, F16, BF16 = 0, 1, 2
 EPI_NONE, EPI_BIAS, EPI_BIAS_EXP, EPI_BIAS_RSQRT, EPI_BIAS_RECIP, EPI_BIAS_RELU = 0, 1, 2, 3, 4, 5
 BC_COPY, BC_EXP, BC_RSQRT, BC_RECIP = 0, 1, 2, 3
 KIND_AUTO, KIND_UMMA, KIND_SIMT = 0, 1, 2
-MODE_NHWC, MODE_DIRECT, MODE_HALO, MODE_SUB, MODE_STACK, MODE_STRIDED = 1, 2, 3, 4, 5, 6
+MODE_NHWC, MODE_DIRECT, MODE_HALO, MODE_SUB, MODE_STACK, MODE_STRIDED, MODE_IM2COL = 1, 2, 3, 4, 5, 6, 7
 EPI_NAMES = {"none": EPI_NONE, "bias": EPI_BIAS, "bias_exp": EPI_BIAS_EXP,
              "bias_rsqrt": EPI_BIAS_RSQRT, "bias_recip": EPI_BIAS_RECIP, "bias_relu": EPI_BIAS_RELU}
 DTYPE_CODES = {"f32": F32, "f16": F16, "bf16": BF16}

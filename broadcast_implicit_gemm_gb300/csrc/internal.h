@@ -47,6 +47,9 @@ enum PackLayout {
                       // the kernel then runs a stride-1 1x1 conv over it
     PACK_STACK = 2,   // stride 1: [N][H+pad][W][Ch], images stacked with pad zero rows
                       // between them, so a halo tile may span several images
+    PACK_IM2COL = 3,  // [N][H][W][Ch] read by TMA im2col loads (A_NHWC): a tile is 128
+                      // consecutive output pixels of the flattened N x Ho x Wo, across
+                      // rows and images, and each tap's load walks their windows
 };
 
 struct UmmaTiling {
@@ -92,13 +95,15 @@ struct UmmaParams {
     int hp;                         // A_HALO over stacked images: rows per image (H + pad)
                                     // in the packed data and in tile row space; 0 otherwise
     int res_b_bytes;                // resident weights: their bytes (0: streamed)
+    int im2col;                     // A_NHWC over PACK_IM2COL: tile pt is the flattened output
+                                    // pixels 128 pt .. 128 pt + 127 (no boxes)
     // Dynamic shared-memory layout of the halo kernels (halo_layout) and of the
     // resident-weight nhwc / direct kernels (main_res_layout): A stages, streamed
     // weight stages, byte offsets of the weights, the output staging and the
     // barriers, and the total
     int halo_sa, halo_sb, halo_b_off, halo_stage_off, halo_bar_off, halo_smem;
     // divisors of the index arithmetic; launch_umma_conv fills them from the fields above
-    FastDiv fd_co, fd_pix, fd_bpi, fd_bx, fd_hp, fd_cib, fd_kw;
+    FastDiv fd_co, fd_pix, fd_bpi, fd_bx, fd_hp, fd_cib, fd_kw, fd_howo, fd_wo;
 };
 
 // Returns a CUDA error code of the launch.
@@ -282,5 +287,14 @@ struct ProfScope {
 bool encode_tiled(CUtensorMap *map, CUtensorMapDataType dt, int rank, const void *base,
                   const uint64_t *dims, const uint64_t *strides_bytes, const uint32_t *box,
                   const uint32_t *estrides, CUtensorMapSwizzle swz);
+// An im2col descriptor over a 4-D channels-last tensor {C, W, H, N}: each load
+// brings `pixels` consecutive pixels (W fastest, then H, then N) of `channels`
+// channels, walking base positions from lower[d] to dims[d] - 1 + upper[d]
+// (d = W, H) in steps of estrides[d + 1]; the load's offsets shift every
+// pixel's read position, and reads outside the tensor are zeros.
+bool encode_im2col(CUtensorMap *map, CUtensorMapDataType dt, const void *base,
+                   const uint64_t *dims, const uint64_t *strides_bytes, const int *lower,
+                   const int *upper, uint32_t channels, uint32_t pixels, const uint32_t *estrides,
+                   CUtensorMapSwizzle swz);
 
 }  // namespace bigemm

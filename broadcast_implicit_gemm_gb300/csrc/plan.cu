@@ -57,7 +57,10 @@ std::string cand_str(const Cand &c)
         snprintf(b, sizeof b, "umma:%s:bn%d:box%dx%dx%d:split%d%s%s%s%s",
                  amode_name(c.t.amode), c.t.bn,
                  c.t.box_w, c.t.box_h, c.t.bpt, c.t.split,
-                 c.t.pack == PACK_SUB ? ":sub" : c.t.pack == PACK_STACK ? ":stack" : "",
+                 c.t.pack == PACK_SUB     ? ":sub"
+                 : c.t.pack == PACK_STACK ? ":stack"
+                 : c.t.pack == PACK_IM2COL ? ":im2col"
+                                           : "",
                  c.t.bres ? ":bres" : "", c.t.epi16 ? ":e16" : "", c.t.pair ? ":pair" : "");
     else if (c.simt_variant == SV_DW)
         snprintf(b, sizeof b, "simt:depthwise:rows%d", c.dw_rows);
@@ -88,8 +91,10 @@ bool parse_cand(const std::string &s, Cand &c)
                     : strcmp(mode, "halo") == 0    ? A_HALO
                     : strcmp(mode, "strided") == 0 ? A_STRIDED
                                                    : A_NHWC;
-        c.t.pack = strcmp(layout, "sub") == 0 ? PACK_SUB : strcmp(layout, "stack") == 0 ? PACK_STACK
-                                                                                       : PACK_PLAIN;
+        c.t.pack = strcmp(layout, "sub") == 0      ? PACK_SUB
+                   : strcmp(layout, "stack") == 0  ? PACK_STACK
+                   : strcmp(layout, "im2col") == 0 ? PACK_IM2COL
+                                                   : PACK_PLAIN;
         c.t.bres = strcmp(layout, "bres") == 0 || strcmp(layout2, "bres") == 0;
         c.t.epi16 = strcmp(layout, "e16") == 0 || strcmp(layout2, "e16") == 0 ||
                     strcmp(layout3, "e16") == 0;
@@ -213,7 +218,15 @@ UmmaGeom umma_geometry(const ConvShape &s0, const UmmaTiling &t, int sm_count)
     p.ci_blocks = (int)ceil_div(s.CI, p.bk);
     p.box_w = t.box_w, p.box_h = t.box_h, p.bpt = t.bpt;
     long long bpi;
-    if (t.amode == A_NHWC || t.amode == A_HALO) {
+    if (t.pack == PACK_IM2COL) {
+        // 128-pixel tiles of the flattened N x Ho x Wo output, one im2col load per tap
+        p.boxes_x = 1, p.boxes_y = 1;
+        bpi = ceil_div((long long)s.N * s.Ho * s.Wo, 128);
+        p.k_blocks = s.KH * s.KW * p.ci_blocks;
+        g.cip = p.ci_blocks * p.bk;
+        g.ch = (int)ceil_div(s.CI, 16 / e) * (16 / e);
+        p.im2col = 1;
+    } else if (t.amode == A_NHWC || t.amode == A_HALO) {
         p.boxes_x = (int)ceil_div(s.Wo, t.box_w);
         p.boxes_y = (int)ceil_div(s.Ho, t.box_h);
         if (t.pack == PACK_STACK) {
@@ -242,7 +255,7 @@ UmmaGeom umma_geometry(const ConvShape &s0, const UmmaTiling &t, int sm_count)
         g.ch = s.CI;
     }
     p.cip = g.cip;
-    const long long total = (t.pack == PACK_STACK ? 1 : (long long)s.N) * bpi;
+    const long long total = (t.pack == PACK_STACK || t.pack == PACK_IM2COL ? 1 : (long long)s.N) * bpi;
     // CTA pairs: a unit is two tiles, one per block of the pair
     const long long ptiles = ceil_div(ceil_div(total, t.bpt), t.pair ? 2 : 1);
     p.co_tiles = (int)ceil_div(s.CO, t.bn);
@@ -293,6 +306,13 @@ bool umma_valid(const ConvShape &s0, const UmmaTiling &t, int sm_count, std::str
         if (t.amode != A_HALO) return bad("stacked images feed the halo mode");
         if (s0.Ho > s0.H + s0.pad) return bad("stacking needs pad <= KH - 1");
         if ((long long)s0.N * stack_pitch(s0, t) + 16 >= (1ll << 31)) return bad("stacked rows exceed 2^31");
+    } else if (t.pack == PACK_IM2COL) {
+        if (t.amode != A_NHWC) return bad("im2col loads feed the nhwc mode");
+        if (s0.KH * s0.KW < 2) return bad("im2col tiles are for kernels larger than 1x1");
+        if (s0.stride > 2) return bad("im2col tiles take stride 1 or 2");
+        if (s0.KH > 8 || s0.KW > 8 || s0.pad > 7) return bad("im2col offsets and corners are small");
+        if (t.box_w != 128 || t.box_h != 1 || t.bpt != 1) return bad("an im2col tile is 128 pixels");
+        if ((long long)s0.N * s0.Ho * s0.Wo >= (1ll << 31)) return bad("more than 2^31 output pixels");
     } else if (t.pack != PACK_PLAIN) {
         return bad("unknown pack layout");
     }
@@ -476,6 +496,8 @@ UmmaTiling default_tiling(const ConvShape &s, int amode, int bn, int sms, int pa
         t.box_w = 8, t.box_h = 16, t.bpt = 1;
     } else if (amode == A_STRIDED) {
         t.box_w = 16, t.box_h = 4, t.bpt = 2;
+    } else if (pack == PACK_IM2COL) {
+        t.box_w = 128, t.box_h = 1, t.bpt = 1;
     } else {
         const Box b = box_options(kernel_shape(s, t)).front();
         t.box_w = b.w, t.box_h = b.h, t.bpt = b.bpt;
@@ -659,6 +681,7 @@ std::vector<Cand> candidates(const ConvShape &s, int sms)
     if (strided_ok(s)) modes.push_back({A_STRIDED, PACK_PLAIN});
     if (sub_ok(s)) modes.push_back({A_NHWC, PACK_SUB});
     modes.push_back({A_NHWC, PACK_PLAIN});
+    if (s.KH * s.KW > 1 && s.stride <= 2) modes.push_back({A_NHWC, PACK_IM2COL});
     for (const auto &mp : modes) {
         const int amode = mp.first, pack = mp.second;
         UmmaTiling probe{};
@@ -678,6 +701,9 @@ std::vector<Cand> candidates(const ConvShape &s, int sms)
         } else if (amode == A_STRIDED) {
             bx.push_back({16, 4});
             bpts.push_back(2);
+        } else if (pack == PACK_IM2COL) {
+            bx.push_back({128, 1});
+            bpts.push_back(1);
         } else {
             for (size_t i = 0; i < boxes.size() && bx.size() < 2; ++i) {
                 if (i > 0 && boxes[i].eff < boxes[0].eff - 0.05) break;
@@ -748,6 +774,8 @@ std::vector<Cand> candidates(const ConvShape &s, int sms)
 bool store_tma_ok(const ConvShape &s, const UmmaTiling &t, int split)
 {
     const long long ec = split > 1 ? 4 : (long long)dtype_size(s.out_dt);
+    // im2col tiles run across rows and images: stores from registers
+    if (t.pack == PACK_IM2COL) return false;
     if ((t.box_w * ec) % 16) return false;
     // each epilogue warp stores its 32 pixels as one box: 32 of a row, or whole rows
     const bool wide = t.box_w % 32 == 0;
@@ -852,9 +880,18 @@ bigemm_status setup_plan(bigemm_plan_s *p)
         const uint32_t box[4] = {(uint32_t)p->g.p.bk, (uint32_t)(t.box_w * k.stride),
                                  (uint32_t)(t.box_h * k.stride), 1u};
         const uint32_t es[4] = {1u, (uint32_t)k.stride, (uint32_t)k.stride, 1u};
-        if (!encode_tiled(&p->map_a, tma_dt(s.in_dt), 4, p->xh, dims, str, box, es,
-                          CU_TENSOR_MAP_SWIZZLE_128B))
+        if (t.pack == PACK_IM2COL) {
+            // window base positions x * stride - pad for the Wo (Ho) outputs: from
+            // -pad to W - 1 + (pad - (KW - 1)), in steps of the stride
+            const int lower[2] = {-k.pad, -k.pad};
+            const int upper[2] = {k.pad - (k.KW - 1), k.pad - (k.KH - 1)};
+            if (!encode_im2col(&p->map_a, tma_dt(s.in_dt), p->xh, dims, str, lower, upper,
+                               (uint32_t)p->g.p.bk, 128u, es, CU_TENSOR_MAP_SWIZZLE_128B))
+                return BIGEMM_ERR_UNSUPPORTED;
+        } else if (!encode_tiled(&p->map_a, tma_dt(s.in_dt), 4, p->xh, dims, str, box, es,
+                                 CU_TENSOR_MAP_SWIZZLE_128B)) {
             return BIGEMM_ERR_UNSUPPORTED;
+        }
         if (!p->raw_b) {
             const uint64_t kt = (uint64_t)k.KH * k.KW * p->g.cip;
             const uint64_t bd[2] = {kt, (uint64_t)k.CO};
@@ -1378,8 +1415,8 @@ bigemm_status plan_impl(int N, int H, int W, int CO, int CI, int KH, int KW, int
             }
         } else {
             c.kind = BIGEMM_KIND_UMMA;
-            if (opts->mode < 0 || opts->mode > 6) return BIGEMM_ERR_INVALID_ARG;
-            const int amode = (opts->mode == 1 || opts->mode == 4) ? A_NHWC
+            if (opts->mode < 0 || opts->mode > 7) return BIGEMM_ERR_INVALID_ARG;
+            const int amode = (opts->mode == 1 || opts->mode == 4 || opts->mode == 7) ? A_NHWC
                               : opts->mode == 2                    ? A_DIRECT
                               : (opts->mode == 3 || opts->mode == 5) ? A_HALO
                               : opts->mode == 6                    ? A_STRIDED
@@ -1391,12 +1428,13 @@ bigemm_status plan_impl(int N, int H, int W, int CO, int CI, int KH, int KW, int
                                                                      : A_NHWC;
             const int pack = opts->mode == 4   ? PACK_SUB
                              : opts->mode == 5 ? PACK_STACK
+                             : opts->mode == 7 ? PACK_IM2COL
                              : opts->mode != 0 ? PACK_PLAIN
                              : amode == A_NHWC && sub_ok(s) && !(opts->box_w && opts->box_h) ? PACK_SUB
                              : amode == A_HALO ? halo_pack(s)
                                                : PACK_PLAIN;
             c.t = default_tiling(s, amode, opts->tile_n ? opts->tile_n : default_bn(s), sms, pack);
-            if (opts->box_w && opts->box_h) {
+            if (opts->box_w && opts->box_h && pack != PACK_IM2COL) {
                 c.t.box_w = opts->box_w, c.t.box_h = opts->box_h;
                 c.t.bpt = std::max(1, 128 / (opts->box_w * opts->box_h));
                 c.t.split = heuristic_split(s, c.t, sms);
@@ -1515,7 +1553,10 @@ bigemm_status conv2d_nchw_plan_describe(bigemm_plan plan, char *buf, size_t len)
         const UmmaParams &p = plan->g.p;
         os << ", \"amode\": \"" << amode_name(c.t.amode)
            << "\", \"pack\": \""
-           << (c.t.pack == PACK_SUB ? "sub" : c.t.pack == PACK_STACK ? "stack" : "plain")
+           << (c.t.pack == PACK_SUB      ? "sub"
+               : c.t.pack == PACK_STACK  ? "stack"
+               : c.t.pack == PACK_IM2COL ? "im2col"
+                                         : "plain")
            << "\", \"resident_b\": " << (c.t.bres ? "true" : "false")
            << ", \"epi_warps\": " << (c.t.epi16 ? 16 : 8)
            << ", \"cta_pair\": " << (c.t.pair ? "true" : "false")

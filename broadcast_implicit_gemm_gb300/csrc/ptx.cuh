@@ -238,6 +238,20 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, u
         : "memory");
 }
 
+// im2col load of a 4-D channels-last tensor: the pixels from base position
+// (c1, c2, c3) = (w, h, n), channels from c0, each read at its position
+// shifted by (ow, oh) (a filter tap)
+__device__ __forceinline__ void tma_load_im2col_4d(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                                   int c0, int c1, int c2, int c3, uint16_t ow,
+                                                   uint16_t oh)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.im2col.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2], {%7, %8};" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "h"(ow), "h"(oh)
+        : "memory");
+}
+
 // ------------------------------------------------------------------- tcgen05
 // TMEM allocation: executed by one whole warp; the allocated base address is
 // written to shared memory.  ncols is a power of two in [32, 512].

@@ -78,6 +78,27 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
+typedef CUresult (*EncodeIm2colFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const int *, const int *,
+                                   cuuint32_t, cuuint32_t, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+EncodeIm2colFn encode_im2col_fn()
+{
+    static EncodeIm2colFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeIm2col", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeIm2colFn>(p);
+    });
+    return fn;
+}
+
 }  // namespace
 
 DeviceState *device_state()
@@ -139,6 +160,27 @@ bool encode_tiled(CUtensorMap *map, CUtensorMapDataType dt, int rank, const void
         if (i + 1 < rank) st[i] = strides_bytes[i];
     }
     CUresult r = fn(map, dt, (cuuint32_t)rank, const_cast<void *>(base), d, st, b, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool encode_im2col(CUtensorMap *map, CUtensorMapDataType dt, const void *base,
+                   const uint64_t *dims, const uint64_t *strides_bytes, const int *lower,
+                   const int *upper, uint32_t channels, uint32_t pixels, const uint32_t *estrides,
+                   CUtensorMapSwizzle swz)
+{
+    EncodeIm2colFn fn = encode_im2col_fn();
+    if (!fn) return false;
+    cuuint64_t d[4], st[3];
+    cuuint32_t es[4];
+    for (int i = 0; i < 4; ++i) {
+        d[i] = dims[i];
+        es[i] = estrides[i];
+        if (i < 3) st[i] = strides_bytes[i];
+    }
+    int lo[2] = {lower[0], lower[1]}, up[2] = {upper[0], upper[1]};
+    CUresult r = fn(map, dt, 4u, const_cast<void *>(base), d, st, lo, up, channels, pixels, es,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;

@@ -195,7 +195,13 @@ __device__ __forceinline__ void epilogue_warp(const UmmaParams &p, const CUtenso
             int n = (int)fd_divmod((uint32_t)b, p.fd_bpi, &urem);
             const int rem = (int)urem;
             long long pix;
-            if (BOXED) {
+            if (BOXED && p.im2col) {
+                // the tile is 128 consecutive pixels of the flattened N x Ho x Wo
+                const long long g = (long long)w.pt * 128 + row;
+                n = (int)fd_divmod((uint32_t)g, p.fd_howo, &urem);
+                pix = urem;
+                valid = g < (long long)p.N * howo;
+            } else if (BOXED) {
                 const int byi = (int)fd_divmod((uint32_t)rem, p.fd_bx, &urem), bxi = (int)urem;
                 int y = byi * p.box_h + m * 16 + bj_y;
                 const int x = bxi * p.box_w + bj_x;

@@ -69,6 +69,8 @@ cudaError_t launch_umma_conv(const UmmaTiling &t, int in_dt, const UmmaParams &p
     p.fd_hp = make_fastdiv((uint32_t)p.hp);
     p.fd_cib = make_fastdiv((uint32_t)p.ci_blocks);
     p.fd_kw = make_fastdiv((uint32_t)p.KW);
+    p.fd_howo = make_fastdiv((uint32_t)((long long)p.Ho * p.Wo));
+    p.fd_wo = make_fastdiv((uint32_t)p.Wo);
     ProfScope prof(t.amode == A_NHWC      ? "umma_conv_nhwc"
                    : t.amode == A_HALO    ? (t.pair ? "umma_conv_halo_pair" : "umma_conv_halo")
                    : t.amode == A_STRIDED ? "umma_conv_strided"

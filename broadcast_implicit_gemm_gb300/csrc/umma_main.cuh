@@ -112,7 +112,14 @@ __global__ void __launch_bounds__(main_threads<NEPI>(), 1)
                 const int nbox = min(p.bpt, p.total_boxes - box0);
                 const uint32_t tx = (uint32_t)nbox * box_bytes + (RB ? 0u : (uint32_t)C::b_bytes);
                 int mbx = 0, mby = 0, mbn = 0;
-                if (lane < nbox) {
+                if (AMODE == A_NHWC && p.im2col) {
+                    // the tile's first output pixel, as its window's base position
+                    uint32_t r, x;
+                    mbn = (int)fd_divmod((uint32_t)box0 * 128u, p.fd_howo, &r);
+                    const int y = (int)fd_divmod(r, p.fd_wo, &x);
+                    mbx = (int)x * p.stride - p.pad;
+                    mby = y * p.stride - p.pad;
+                } else if (lane < nbox) {
                     const int bb = box0 + lane;
                     uint32_t urem;
                     const int n = (int)fd_divmod((uint32_t)bb, p.fd_bpi, &urem);
@@ -143,7 +150,10 @@ __global__ void __launch_bounds__(main_threads<NEPI>(), 1)
                     uint8_t *a_dst = sa + stage * kABytes;
                     uint8_t *b_dst = sb + stage * C::b_bytes;
                     if (lane < nbox) {
-                        if (AMODE == A_NHWC)
+                        if (AMODE == A_NHWC && p.im2col)
+                            tma_load_im2col_4d(a_dst, &map_a, &full[stage], cb * p.bk, mbx, mby, mbn,
+                                               (uint16_t)rx, (uint16_t)ry);
+                        else if (AMODE == A_NHWC)
                             tma_load_4d(a_dst + lane * box_bytes, &map_a, &full[stage], cb * p.bk,
                                         mbx + rx, mby + ry, mbn);
                         else

@@ -114,6 +114,12 @@ typedef struct {
                          bytes): TMA brings the even input rows, and warps of
                          the kernel keep the even pixels, so no packed copy is
                          made.
+                       7 mode 1 with im2col tiles (K x K > 1, stride 1 or 2):
+                         a tile is 128 consecutive output pixels of the
+                         flattened N x Ho x Wo, across rows and images, and
+                         each tap's operand is one TMA im2col load over the
+                         channels-last copy (box_w and box_h are ignored;
+                         outputs are written from registers).
                        With kind = SIMT it names the kernel instead: 1 tiled
                        (groups = 1) or naive, 2 depthwise staged band (box_h
                        rows per block), 3 depthwise streaming (box_h = 2, 4

@@ -40,7 +40,8 @@ def cand_options(cand):
     if m:
         amode, bn, bw, bh, _bpt, split, flags = m.groups()
         flags = set(flags.split(":")[1:])
-        mode = {"nhwc": bg.MODE_SUB if "sub" in flags else bg.MODE_NHWC,
+        mode = {"nhwc": bg.MODE_SUB if "sub" in flags else bg.MODE_IM2COL if "im2col" in flags
+                else bg.MODE_NHWC,
                 "halo": bg.MODE_STACK if "stack" in flags else bg.MODE_HALO,
                 "direct": bg.MODE_DIRECT, "strided": bg.MODE_STRIDED}[amode]
         return {"kind": bg.KIND_UMMA, "mode": mode, "tile_n": int(bn), "box_w": int(bw),

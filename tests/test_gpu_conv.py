@@ -471,6 +471,70 @@ def test_div_epilogue(case):
         assert info["split_sum"] == "reduce"
 
 
+# ------------------------------------------------- im2col tiles: 128 flattened output pixels
+# A tile runs across output rows and images (7 x 7 planes: one tile holds parts
+# of three images), and each tap's operand is one TMA im2col load whose
+# out-of-image reads are zeros.  Cases: tiles spanning images with a partial
+# last tile, stride 2 (odd and even input sizes), 5 x 5 and 7 x 7 kernels,
+# unpadded and non-square kernels, ragged channels (zero-padded K blocks,
+# partial output-channel tiles), bf16, tf32, BN 64 / 128 / 256, resident
+# weights, 16 epilogue warps, split K adding into fp32 and through the
+# reduction pass, fused epilogues.
+IM2COL = [
+    (S("i2c_r50_7x7_like", 5, 128, 256, 7, 7, 3, 1, 1), {"tile_n": 256}),
+    (S("i2c_14x14_bn64", 2, 64, 64, 14, 14, 3, 1, 1), {"tile_n": 64}),
+    (S("i2c_s2_odd", 3, 64, 128, 15, 15, 3, 2, 1, o="f32", epi="bias"), {"tile_n": 128}),
+    (S("i2c_s2_even_bf16", 2, 64, 64, 16, 12, 3, 2, 1, i="bf16", o="bf16"), {"tile_n": 64}),
+    (S("i2c_k5_ragged_ci", 2, 40, 96, 9, 9, 5, 1, 2, o="f32", epi="bias_exp"), {"tile_n": 128}),
+    (S("i2c_k7_s2", 1, 32, 64, 16, 16, 7, 2, 3), {"tile_n": 64}),
+    (S("i2c_valid_p0", 2, 64, 64, 10, 10, 3, 1, 0, epi="bias_relu"), {"tile_n": 64}),
+    (S("i2c_tf32_split_add", 1, 256, 64, 7, 7, 3, 1, 1, i="f32", o="f32"),
+     {"tile_n": 64, "split_k": 8}),
+    (S("i2c_split_reduce_f16", 1, 256, 128, 7, 7, 3, 1, 1, epi="bias_rsqrt", dd="absnormal"),
+     {"tile_n": 128, "split_k": 4}),
+    (S("i2c_resident_e16", 4, 64, 128, 8, 8, 3, 1, 1), {"tile_n": 128, "resident_b": 1, "epi_warps": 16}),
+    (S("i2c_recip_bf16", 3, 64, 64, 6, 9, 3, 1, 1, i="bf16", o="f32", epi="bias_recip", dd="absnormal",
+       kd="absnormal"), {"tile_n": 64}),
+]
+
+
+@pytest.mark.parametrize("case", IM2COL, ids=lambda c: c[0].name)
+def test_im2col_tiles(case):
+    spec, opts = case
+    info = check(spec, dict({"kind": bg.KIND_UMMA, "mode": bg.MODE_IM2COL}, **opts))
+    assert info["cand"].startswith("umma:nhwc:") and ":im2col" in info["cand"]
+    assert info["pack"] == "im2col"
+
+
+def test_im2col_non_square_kernel():
+    # 3 x 5 kernel, pad 1: the corners differ per spatial dimension
+    spec = S("i2c_3x5", 2, 32, 64, 9, 11, 3, 1, 1)
+    x, _, _ = synth.conv_inputs(spec, 3)
+    # the spec helper draws square kernels: the 3 x 5 kernel is drawn here
+    g = torch.Generator().manual_seed(7)
+    w35 = (torch.randn(64, 32, 3, 5, generator=g) * 0.1).to(torch.float16)
+    xd, wd = x.cuda(), w35.cuda()
+    Ho, Wo = 9, 11 + 2 - 5 + 1
+    out = torch.empty(2, 64, Ho, Wo, dtype=torch.float16, device="cuda")
+    plan = bg.conv2d_nchw_plan_ex(2, 9, 11, 64, 32, 3, 5, 1, 1, 1, bg.F16, bg.F16, bg.EPI_NONE, 0,
+                                  {"kind": bg.KIND_UMMA, "mode": bg.MODE_IM2COL, "tile_n": 64})
+    bg.conv2d_nchw_run(plan, xd, wd, None, 1e-5, out)
+    torch.cuda.synchronize()
+    assert plan.describe()["pack"] == "im2col"
+    plan.close()
+    ref, sabs = oracle.conv2d_nchw(x, w35, stride=1, pad=1, nthreads=NTH)
+    assert_within(out.cpu().double().numpy(), ref, conv_bound(ref, sabs, TAU["half"], "f16"), "im2col 3x5")
+
+
+def test_im2col_rejects_1x1_and_stride_3():
+    x = torch.empty(16, dtype=torch.float16, device="cuda")
+    for K, st in ((1, 1), (3, 3)):
+        with pytest.raises(bg.BigemmError) as e:
+            bg.conv2d_nchw_plan_ex(1, 12, 12, 64, 64, K, K, st, K // 2, 1, bg.F16, bg.F16, bg.EPI_NONE, 0,
+                                   {"kind": bg.KIND_UMMA, "mode": bg.MODE_IM2COL})
+        assert e.value.status == 2
+
+
 # ------------------------------------------------- add + ReLU, max(conv + bias, 0)
 # Data and kernels of both signs, so about half of the outputs clamp to zero.
 def _U(name, N, CI, CO, H, W, K, s, p, g=1, i="f16", o="f32", kd="he"):
