@@ -20,7 +20,9 @@ per-layer figures come from it (those events serialise the launches, so it is
 reported separately as profiled_ms_per_step).  `e2e` repeats the
 step with host buffers: pinned host->device copies of every layer's inputs and
 device->host copies of its output inside the timed region, on two copy streams
-that overlap the layers' convs (the layers are independent problems).  `cpu_baseline` times
+that overlap the convs.  Layers and images are independent problems, so each
+layer moves in four batch slices (each with its own plan), the layers with the
+most output first: the first outputs leave while later inputs still arrive.  `cpu_baseline` times
 the CPU oracle on this host on a bounded sample of the same workload.  With
 --impl reference the CPU oracle is the measured arm.
 
@@ -44,6 +46,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "conv2d TFLOP/s per shape and % of roofline at 1 GB300; broadcast HBM GB/s"
 L2_FLUSH_BYTES = 512 << 20
+E2E_CHUNKS = 4        # batch slices per layer in the end-to-end step
 
 
 # ---------------------------------------------------------------- workloads
@@ -215,13 +218,44 @@ class ConvStep:
                               device=device)
             first = segs[0][0]
             last = max(sg[0] + sg[1] for sg in segs if sg is not None)
-            self.items.append({
+            item = {
                 "spec": s, "plan": plan, "info": plan.describe(),
                 "x": view(self.stage_d, segs[0]), "w": view(self.stage_d, segs[1]),
                 "b": view(self.stage_d, segs[2]) if segs[2] is not None else None,
                 "in_d": self.stage_d[first:last], "in_h": self.stage_h[first:last],
                 "out": out, "out_h": torch.empty(out.shape, dtype=out.dtype).pin_memory(),
-            })
+            }
+            # The end-to-end step moves a layer in E2E_CHUNKS batch slices, each
+            # with its own plan, so that the first outputs leave while later
+            # inputs are still arriving (images are independent problems).
+            k = E2E_CHUNKS if s.N % E2E_CHUNKS == 0 and s.N >= E2E_CHUNKS else 1
+            nc = s.N // k
+            # every slice must start on a 16-byte boundary, as the library requires
+            if (segs[0][1] // s.N * nc) % 16 or (out[0].numel() * out.element_size() * nc) % 16:
+                k, nc = 1, s.N
+            if k > 1:
+                cplan = bg.conv2d_nchw_plan(nc, s.H, s.W, s.CO, s.CI, s.K, s.K, s.stride, s.pad,
+                                            s.groups, bg.DTYPE_CODES[s.in_dtype],
+                                            bg.DTYPE_CODES[s.out_dtype], bg.EPI_NAMES[s.epi],
+                                            search)
+            else:
+                cplan = plan
+            xo, xnb = segs[0][0], segs[0][1]
+            wb_first = segs[1][0]
+            item["e2e"] = {
+                "plan": cplan,
+                # the kernel and bias, then the data slices, each one copy
+                "wb_d": self.stage_d[wb_first:last], "wb_h": self.stage_h[wb_first:last],
+                "x_d": [self.stage_d[xo + j * xnb // k: xo + (j + 1) * xnb // k] for j in range(k)],
+                "x_h": [self.stage_h[xo + j * xnb // k: xo + (j + 1) * xnb // k] for j in range(k)],
+                "x": [item["x"][j * nc:(j + 1) * nc] for j in range(k)],
+                "out": [out[j * nc:(j + 1) * nc] for j in range(k)],
+                "out_h": [item["out_h"][j * nc:(j + 1) * nc] for j in range(k)],
+            }
+            self.items.append(item)
+        # layers with the most output bytes first: the device-to-host copies,
+        # the longer direction, start early and stay busy
+        self.e2e_order = sorted(self.items, key=lambda it: -it["out"].numel() * it["out"].element_size())
         self.stage_d.copy_(self.stage_h)
         torch.cuda.synchronize()
 
@@ -234,11 +268,11 @@ class ConvStep:
                 self.marks.append((i, ev))
 
     def run_e2e(self, stream):
-        """The step from pinned host buffers: every layer's inputs go in on a
-        copy-in stream, its conv runs on `stream` once they have landed, and its
-        output comes back on a copy-out stream, so the copies of one layer
-        overlap the other layers' convs and the two directions overlap each other.
-        The step ends on `stream` when the last output is on the host."""
+        """The step from pinned host buffers: every layer's kernel and bias, then
+        its batch slices, go in on a copy-in stream; each slice's conv runs on
+        `stream` once it has landed, and its output comes back on a copy-out
+        stream, so copies overlap the convs and the two directions overlap each
+        other.  The step ends on `stream` when the last output is on the host."""
         torch = self.torch
         if getattr(self, "copy_streams", None) is None:
             self.copy_streams = (torch.cuda.Stream(), torch.cuda.Stream())
@@ -246,23 +280,33 @@ class ConvStep:
         h2d.wait_stream(stream)          # the previous step is done with the input buffers
         landed = []
         with torch.cuda.stream(h2d):
-            for it in self.items:
-                it["in_d"].copy_(it["in_h"], non_blocking=True)   # data, kernel, bias in one copy
-                ev = torch.cuda.Event()
-                ev.record(h2d)
-                landed.append(ev)
-        for it, ev in zip(self.items, landed):
-            stream.wait_event(ev)
-            self.bg.conv2d_nchw_run(it["plan"], it["x"], it["w"], it["b"], 1e-5, it["out"], stream)
-            done = torch.cuda.Event()
-            done.record(stream)
-            d2h.wait_event(done)
-            with torch.cuda.stream(d2h):
-                it["out_h"].copy_(it["out"], non_blocking=True)
+            for it in self.e2e_order:
+                e = it["e2e"]
+                e["wb_d"].copy_(e["wb_h"], non_blocking=True)
+                evs = []
+                for xd, xh in zip(e["x_d"], e["x_h"]):
+                    xd.copy_(xh, non_blocking=True)
+                    ev = torch.cuda.Event()
+                    ev.record(h2d)
+                    evs.append(ev)
+                landed.append(evs)
+        for it, evs in zip(self.e2e_order, landed):
+            e = it["e2e"]
+            for j, ev in enumerate(evs):
+                stream.wait_event(ev)
+                self.bg.conv2d_nchw_run(e["plan"], e["x"][j], it["w"], it["b"], 1e-5, e["out"][j],
+                                        stream)
+                done = torch.cuda.Event()
+                done.record(stream)
+                d2h.wait_event(done)
+                with torch.cuda.stream(d2h):
+                    e["out_h"][j].copy_(e["out"][j], non_blocking=True)
         stream.wait_stream(d2h)
 
     def h2d_bytes(self):
-        return sum(it["in_h"].numel() for it in self.items)   # the copied bytes, alignment gaps included
+        # the bytes the end-to-end step copies: each layer's kernel and bias, and its data
+        return sum(it["e2e"]["wb_h"].numel() + sum(x.numel() for x in it["e2e"]["x_h"])
+                   for it in self.items)
 
     def d2h_bytes(self):
         return sum(it["out"].numel() * it["out"].element_size() for it in self.items)
