@@ -13,7 +13,8 @@ from tests.test_gpu_conv import DT, S, check
 pytestmark = pytest.mark.gpu
 
 MODES = {"auto": None, "nhwc": bg.MODE_NHWC, "halo": bg.MODE_HALO, "direct": bg.MODE_DIRECT,
-         "sub": bg.MODE_SUB, "stack": bg.MODE_STACK}
+         "sub": bg.MODE_SUB, "stack": bg.MODE_STACK, "strided": bg.MODE_STRIDED,
+         "im2col": bg.MODE_IM2COL}
 
 
 def _draw_opts(rng):
@@ -82,3 +83,57 @@ def test_random_shape(case):
         opts = {"kind": bg.KIND_UMMA}
     info = check(spec, opts)
     assert info["kind"] == "umma"
+
+
+# ------------------------------------------------------------- depthwise
+# Seeded random depthwise shapes through every SIMT depthwise kernel: the
+# staged band (2), streaming (3), whole-plane (4), small-plane (5) and band of
+# rows (6) kernels, or the library's own choice.  Widths are drawn so that both
+# the 16-byte-row and the odd-width paths come up.
+DW_MODES = [None, (2, 4), (3, 2), (3, 4), (4, 0), (5, 2), (5, 4), (6, 0)]
+
+
+def _dw_opts(rng):
+    m = DW_MODES[int(rng.integers(0, len(DW_MODES)))]
+    if m is None:
+        return {"kind": bg.KIND_SIMT}
+    opts = {"kind": bg.KIND_SIMT, "mode": m[0]}
+    if m[1]:
+        opts["box_h"] = m[1]
+    return opts
+
+
+def _dw_cases(n=40, seed=77):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        K = int(rng.choice([3, 3, 5, 7]))
+        stride = int(rng.choice([1, 1, 2]))
+        H = int(rng.integers(1, 41))
+        W = int(rng.choice([int(rng.integers(1, 41)), 8 * int(rng.integers(1, 9))]))
+        C = int(rng.choice([2, 3, 8, 16, 24, 40]))
+        N = int(rng.integers(1, 4))
+        i_dt = str(rng.choice(["f16", "bf16", "f32"]))
+        o_dt = i_dt if rng.random() < 0.6 else "f32"
+        epi = str(rng.choice(["none", "bias", "bias_exp", "bias_relu", "bias_recip"]))
+        dd, kd = ("absnormal", "absnormal") if epi == "bias_recip" else ("uniform", "dw")
+        if epi == "bias_exp":
+            o_dt = "f32"
+        spec = S(f"rdw{i}_k{K}s{stride}_{H}x{W}_c{C}_n{N}_{i_dt}{o_dt}_{epi}", N, C, C, H, W, K,
+                 stride, K // 2, g=C, i=i_dt, o=o_dt, epi=epi, dd=dd, kd=kd)
+        out.append((spec, _dw_opts(rng), seed * 1000 + i))
+    return out
+
+
+@pytest.mark.parametrize("case", _dw_cases(), ids=lambda c: c[0].name)
+def test_random_depthwise(case):
+    spec, opts, seed = case
+    rng = np.random.default_rng(seed)
+    for _ in range(8):
+        if _accepted(spec, opts):
+            break
+        opts = _dw_opts(rng)
+    else:
+        opts = {"kind": bg.KIND_SIMT}
+    info = check(spec, opts)
+    assert info["kind"] == "simt"
