@@ -156,8 +156,15 @@ __device__ __forceinline__ void pack_weight_part(const T *__restrict__ w, T *__r
                     uint4 u;
                     T e[VEC];
                 } o;
+                if (c + VEC <= nc) {
+                    // all VEC source channels present: a strided gather, no tests
+                    const T *col = buf + c * KHKW + t;
 #pragma unroll
-                for (int j = 0; j < VEC; ++j) o.e[j] = c + j < nc ? buf[(c + j) * KHKW + t] : T(0);
+                    for (int j = 0; j < VEC; ++j) o.e[j] = col[j * KHKW];
+                } else {
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j) o.e[j] = c + j < nc ? buf[(c + j) * KHKW + t] : T(0);
+                }
                 *reinterpret_cast<uint4 *>(dst + (size_t)t * cip + c) = o.u;
             }
         } else {
@@ -333,10 +340,18 @@ __global__ void __launch_bounds__(256) pack_plane_kernel(const T *__restrict__ x
             uint4 u;
             T e[VEC];
         } o;
+        if (p < HWi && (k + 1) * VEC <= nc) {
+            // a pixel of the plane with all VEC channels present: one strided
+            // gather down the channel planes, no per-element tests
+            const T *col = sp + k * VEC * HWi + p;
 #pragma unroll
-        for (int j = 0; j < VEC; ++j) {
-            const int ch = k * VEC + j;
-            o.e[j] = (p < HWi && ch < nc) ? sp[ch * HWi + p] : T(0);
+            for (int j = 0; j < VEC; ++j) o.e[j] = col[j * HWi];
+        } else {
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) {
+                const int ch = k * VEC + j;
+                o.e[j] = (p < HWi && ch < nc) ? sp[ch * HWi + p] : T(0);
+            }
         }
         *reinterpret_cast<uint4 *>(xd + (size_t)p * Ch + c) = o.u;
     }
