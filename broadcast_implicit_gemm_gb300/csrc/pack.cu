@@ -104,19 +104,45 @@ __global__ void __launch_bounds__(256) pack_nhwc_vec_kernel(const T *__restrict_
 // (16 KB, so that a run of input channels x taps of one output channel fits).
 constexpr int kPackSmemBytes = 16384;
 
+// How pack_weight_part divides the kernel re-layout among blocks, for a
+// shared buffer of cap elements: items of cc input channels of one output
+// channel (cc * KHKW contiguous source elements), or, when one such run covers
+// every input channel, items of fpi whole output channels (fpi * CI * KHKW
+// contiguous source elements), so that small kernels take few blocks.  cc < 1:
+// a kernel too large for the buffer, re-laid out element by element.
+struct WeightSplit {
+    int cc, runs, fpi;
+    long long items;
+};
+
+__host__ __device__ inline WeightSplit weight_split(int CO, int CI, int KHKW, int cip, int cap)
+{
+    WeightSplit ws{};
+    int cc = cap / KHKW;
+    if (cc >= 32) cc &= ~31;
+    ws.cc = cc;
+    if (cc < 1) {
+        ws.runs = 0, ws.fpi = 0;
+        ws.items = ((long long)CO * KHKW * cip + 255) / 256;
+        return ws;
+    }
+    ws.runs = (cip + cc - 1) / cc;
+    ws.fpi = ws.runs == 1 ? max(1, cap / (CI * KHKW)) : 1;
+    ws.items = ws.runs == 1 ? ((long long)CO + ws.fpi - 1) / ws.fpi : (long long)CO * ws.runs;
+    return ws;
+}
+
 // The kernel re-layout [CO][CI][KHKW] -> [CO][KHKW][cip] by blocks
-// first, first + nblocks, ...: each work item is one output channel f and a
-// run of cc input channels, whose cc * KHKW source elements are contiguous.
-// They are read coalesced into the shared buffer `buf` (cap elements) and
-// written back as KHKW runs of cc channels, zero past CI.
+// first, first + nblocks, ...: each work item (weight_split) is read coalesced
+// into the shared buffer `buf` (cap elements) and written back as KHKW runs of
+// channels per output channel, zero past CI.
 template <typename T>
 __device__ __forceinline__ void pack_weight_part(const T *__restrict__ w, T *__restrict__ wp,
                                                  int CO, int CI, int KHKW, int cip, int first,
                                                  int nblocks, T *buf, int cap)
 {
-    int cc = cap / KHKW;
-    if (cc >= 32) cc &= ~31;
-    if (cc < 1) {   // a kernel too large for the buffer: element by element
+    const WeightSplit sp = weight_split(CO, CI, KHKW, cip, cap);
+    if (sp.cc < 1) {   // a kernel too large for the buffer: element by element
         const long long total = (long long)CO * KHKW * cip;
         const long long nthreads = (long long)nblocks * blockDim.x;
         for (long long i = (long long)first * blockDim.x + threadIdx.x; i < total; i += nthreads) {
@@ -128,15 +154,17 @@ __device__ __forceinline__ void pack_weight_part(const T *__restrict__ w, T *__r
         }
         return;
     }
-    const int runs = (cip + cc - 1) / cc;
-    const long long items = (long long)CO * runs;
-    for (long long it = first; it < items; it += nblocks) {
-        const int f = (int)(it / runs);
-        const int c0 = (int)(it - (long long)f * runs) * cc;
+    const int cc = sp.cc, runs = sp.runs;
+    constexpr int VEC = 16 / sizeof(T);
+    for (long long it = first; it < sp.items; it += nblocks) {
+        // output channels [f0, f0 + nf), input channels [c0, c0 + nc) of each
+        const int f0 = runs == 1 ? (int)it * sp.fpi : (int)(it / runs);
+        const int nf = runs == 1 ? min(sp.fpi, CO - f0) : 1;
+        const int c0 = runs == 1 ? 0 : (int)(it - (long long)f0 * runs) * cc;
         const int nc = min(cc, CI - c0);   // source channels in this run (may be <= 0)
-        const T *src = w + ((size_t)f * CI + c0) * KHKW;
-        const int nsrc = nc > 0 ? nc * KHKW : 0;
-        constexpr int VEC = 16 / sizeof(T);
+        const T *src = w + ((size_t)f0 * CI + c0) * KHKW;
+        const int per_f = nc > 0 ? nc * KHKW : 0;   // source elements per output channel
+        const int nsrc = per_f * nf;                // contiguous: nf > 1 only with whole channels
         if ((reinterpret_cast<uintptr_t>(src) & 15) == 0 && nsrc % VEC == 0) {
             const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
             for (int i = threadIdx.x; i < nsrc / VEC; i += blockDim.x)
@@ -146,31 +174,36 @@ __device__ __forceinline__ void pack_weight_part(const T *__restrict__ w, T *__r
         }
         __syncthreads();
         const int wc = min(cc, cip - c0);  // destination channels in this run
-        T *dst = wp + (size_t)f * KHKW * cip + c0;
         if (wc % VEC == 0 && (cip * sizeof(T)) % 16 == 0 && ((c0 * sizeof(T)) & 15) == 0) {
             // runs of VEC channels of one tap per 16-byte store
             const int wv = wc / VEC;
-            for (int i = threadIdx.x; i < KHKW * wv; i += blockDim.x) {
-                const int t = i / wv, c = (i - t * wv) * VEC;
+            const int per = KHKW * wv;     // stores per output channel
+            for (int i = threadIdx.x; i < nf * per; i += blockDim.x) {
+                const int ff = i / per, r = i - ff * per;
+                const int t = r / wv, c = (r - t * wv) * VEC;
+                const T *fb = buf + (size_t)ff * per_f;
                 union {
                     uint4 u;
                     T e[VEC];
                 } o;
                 if (c + VEC <= nc) {
                     // all VEC source channels present: a strided gather, no tests
-                    const T *col = buf + c * KHKW + t;
+                    const T *col = fb + c * KHKW + t;
 #pragma unroll
                     for (int j = 0; j < VEC; ++j) o.e[j] = col[j * KHKW];
                 } else {
 #pragma unroll
-                    for (int j = 0; j < VEC; ++j) o.e[j] = c + j < nc ? buf[(c + j) * KHKW + t] : T(0);
+                    for (int j = 0; j < VEC; ++j) o.e[j] = c + j < nc ? fb[(c + j) * KHKW + t] : T(0);
                 }
-                *reinterpret_cast<uint4 *>(dst + (size_t)t * cip + c) = o.u;
+                *reinterpret_cast<uint4 *>(wp + ((size_t)(f0 + ff) * KHKW + t) * cip + c0 + c) = o.u;
             }
         } else {
-            for (int i = threadIdx.x; i < KHKW * wc; i += blockDim.x) {
-                const int t = i / wc, c = i - t * wc;
-                dst[(size_t)t * cip + c] = c < nc ? buf[c * KHKW + t] : T(0);
+            const int per = KHKW * wc;
+            for (int i = threadIdx.x; i < nf * per; i += blockDim.x) {
+                const int ff = i / per, r = i - ff * per;
+                const int t = r / wc, c = r - t * wc;
+                wp[((size_t)(f0 + ff) * KHKW + t) * cip + c0 + c] =
+                    c < nc ? buf[(size_t)ff * per_f + c * KHKW + t] : T(0);
             }
         }
         __syncthreads();
@@ -282,10 +315,13 @@ __global__ void __launch_bounds__(256) pack_operands_kernel(const T *__restrict_
 }
 
 // Small planes (HWi <= kPlaneMax): a data tile is the whole plane of one image
-// for 128 bytes of channels, which is one contiguous run of the input.  The
-// run is copied to shared memory (16-byte loads where it is aligned), then
-// each thread writes 16-byte channel runs of output pixels gathered from the
-// plane rows.  Tile index flattened as (channel tile, image).
+// for ipb x 128 bytes of channels (ipb channel tiles, ipb * HWi <= kPlaneMax),
+// which is one contiguous run of the input.  The run is copied to shared
+// memory (16-byte loads where it is aligned), then each thread writes 16-byte
+// channel runs of output pixels gathered from the plane rows.  Tile index
+// flattened as (channel group, image).  (Several tiles per block: each block
+// keeps more bytes in flight and the grid fits one wave; one 128-byte tile per
+// block left the 512-channel 7 x 7 layer's pack at half the copy bandwidth.)
 constexpr int kPlaneMax = 256;
 // the whole-plane kernels' shared buffer (128 bytes of channels x kPlaneMax
 // pixels), which their weight blocks use whole: twice the channel run of the
@@ -295,7 +331,8 @@ constexpr int kPlaneBufBytes = 128 * kPlaneMax;
 template <typename T>
 __global__ void __launch_bounds__(256) pack_plane_kernel(const T *__restrict__ x,
                                                          T *__restrict__ xh, int C, int HWi,
-                                                         int HWo, int Ch, int ctiles, int wblocks,
+                                                         int HWo, int Ch, int cgroups, int ipb,
+                                                         int wblocks,
                                                          const T *__restrict__ w,
                                                          T *__restrict__ wp, int CO, int CI,
                                                          int KHKW, int cip, float *z,
@@ -318,9 +355,10 @@ __global__ void __launch_bounds__(256) pack_plane_kernel(const T *__restrict__ x
         return;
     }
     const int t = (int)blockIdx.x - wblocks;
-    const int ct = t % ctiles, n = t / ctiles;
-    const int c0 = ct * TC;
-    const int nc = min(TC, C - c0);       // channels of the input in this tile (<= 0: padding)
+    const int g = t % cgroups, n = t / cgroups;
+    const int c0 = g * ipb * TC;
+    const int nc = min(ipb * TC, C - c0);  // channels of the input in this group (<= 0: padding)
+    const int kcb = ipb * KC;              // 16-byte channel runs per pixel of the group
     const T *src = x + ((size_t)n * C + c0) * HWi;
     const int cnt = nc > 0 ? nc * HWi : 0;
     if ((reinterpret_cast<uintptr_t>(src) & 15) == 0 && cnt % VEC == 0) {
@@ -332,8 +370,11 @@ __global__ void __launch_bounds__(256) pack_plane_kernel(const T *__restrict__ x
     }
     __syncthreads();
     T *xd = xh + (size_t)n * HWo * Ch;
-    for (int q = threadIdx.x; q < HWo * KC; q += blockDim.x) {
-        const int p = q / KC, k = q - p * KC;
+    for (int q = threadIdx.x; q < HWo * kcb; q += blockDim.x) {
+        // q = (tile, pixel, run): the eight lanes of a pixel gather eight
+        // channel rows from distinct bank groups, as with one tile per block
+        const int r = q / KC, kt = r / HWo;
+        const int p = r - kt * HWo, k = kt * KC + (q - r * KC);
         const int c = c0 + k * VEC;
         if (c >= Ch) continue;
         union {
@@ -651,15 +692,28 @@ cudaError_t launch_pack_operands(const void *x, void *xh, int N, int C, int H, i
     const long long tc = 128 / (long long)dtype_size(dt);   // plane / rows tiles: 128 B of channels
     const long long ptiles = (kind == 0 || kind == 3) ? 1 : kind == 1 ? (hwo + 127) / 128 : (hwo + tile - 1) / tile;
     const long long ctiles = kind == 2 ? (Ch + tile - 1) / tile : (Ch + tc - 1) / tc;
-    const long long data_blocks = ptiles * ctiles * N;
+    // whole planes: ipb channel tiles per block, as many as the buffer holds
+    // while every SM still gets two data blocks, then as few as give the same
+    // number of groups (balanced groups)
+    long long ipb = 1;
+    if (kind == 0) {
+        DeviceState *ds = device_state();
+        const long long want = 2ll * (ds ? ds->sm_count : 148);
+        const long long maxb = std::max<long long>(1, std::min<long long>(kPlaneMax / hwi, ctiles));
+        for (long long b = maxb; b > 1; --b)
+            if ((long long)N * ((ctiles + b - 1) / b) >= want) {
+                ipb = b;
+                break;
+            }
+        const long long groups = (ctiles + ipb - 1) / ipb;
+        while (ipb > 1 && (ctiles + ipb - 2) / (ipb - 1) == groups) --ipb;
+    }
+    const long long cgroups = (ctiles + ipb - 1) / ipb;
+    const long long data_blocks = ptiles * (kind == 0 ? cgroups : ctiles) * N;
     // weight blocks: one per (output channel, channel run) item of pack_weight_part;
     // none when w is null (the conv reads the caller's kernel as it is)
-    const long long cap = ((kind == 0 || kind == 3) ? kPlaneBufBytes : kPackSmemBytes) /
-                          (long long)dtype_size(dt);
-    long long cc = cap / KHKW;
-    if (cc >= 32) cc &= ~31ll;
-    const long long witems = cc >= 1 ? (long long)CO * ((cip + cc - 1) / cc)
-                                     : ((long long)CO * KHKW * cip + 255) / 256;
+    const int cap = ((kind == 0 || kind == 3) ? kPlaneBufBytes : kPackSmemBytes) / (int)dtype_size(dt);
+    const long long witems = weight_split(CO, CI, KHKW, cip, cap).items;
     const long long wblocks = w ? std::max<long long>(1, std::min<long long>(witems, 2048)) : 0;
     if (zero && (reinterpret_cast<uintptr_t>(zero) & 15)) return cudaErrorInvalidValue;
     const long long zblocks =
@@ -671,12 +725,12 @@ cudaError_t launch_pack_operands(const void *x, void *xh, int N, int C, int H, i
         if (dtype_size(dt) == 4)
             return launch_pdl(pack_plane_kernel<uint32_t>, dim3(grid), dim3(256), 0, stream,
                               static_cast<const uint32_t *>(x), static_cast<uint32_t *>(xh), C,
-                              (int)hwi, (int)hwo, Ch, (int)ctiles, (int)wblocks,
+                              (int)hwi, (int)hwo, Ch, (int)cgroups, (int)ipb, (int)wblocks,
                               static_cast<const uint32_t *>(w), static_cast<uint32_t *>(wp), CO, CI,
                               KHKW, cip, zero, zero_elems, (int)zblocks);
         return launch_pdl(pack_plane_kernel<uint16_t>, dim3(grid), dim3(256), 0, stream,
                           static_cast<const uint16_t *>(x), static_cast<uint16_t *>(xh), C,
-                          (int)hwi, (int)hwo, Ch, (int)ctiles, (int)wblocks,
+                          (int)hwi, (int)hwo, Ch, (int)cgroups, (int)ipb, (int)wblocks,
                           static_cast<const uint16_t *>(w), static_cast<uint16_t *>(wp), CO, CI,
                           KHKW, cip, zero, zero_elems, (int)zblocks);
     }

@@ -372,6 +372,28 @@ def test_stacking_rejects_padding_wider_than_the_kernel():
     assert e.value.status == 2
 
 
+# ------------------------------------------------- pack launches with grouped work
+# The whole-plane pack moves several 128-byte channel tiles of an image per
+# block when the grid still gives every SM two blocks, and the kernel re-layout
+# takes several whole output channels per block when their source elements fit
+# its buffer.  These shapes reach both, with ragged last groups (a partial
+# channel tile, an output-channel group of fewer channels).
+PACK_GROUPS = [
+    (_H("pack_groups_7x7_ci200_co76", 160, 200, 76, 7, 7, 3, 1), bg.MODE_STACK),
+    (_H("pack_groups_4x4_ci1024_co32", 80, 1024, 32, 4, 4, 3, 1), bg.MODE_STACK),
+    (_H("pack_groups_tf32_7x7_ci100_co40", 160, 100, 40, 7, 7, 3, 1, i="f32", o="f32"), bg.MODE_STACK),
+    (_H("pack_groups_bf16_6x6_ci136_co20_exp", 160, 136, 20, 6, 6, 3, 1, i="bf16", o="f32", epi="bias_exp"),
+     bg.MODE_NHWC),
+    (_H("pack_groups_rows_20x20_ci96_co50", 2, 96, 50, 20, 20, 3, 1), bg.MODE_HALO),
+]
+
+
+@pytest.mark.parametrize("case", PACK_GROUPS, ids=lambda c: c[0].name)
+def test_pack_groups(case):
+    spec, mode = case
+    check(spec, {"kind": bg.KIND_UMMA, "mode": mode})
+
+
 def test_heuristic_stacks_small_images():
     spec = synth.RESNET50_FP16[3].with_batch(2)
     info = check(spec)
