@@ -104,45 +104,19 @@ __global__ void __launch_bounds__(256) pack_nhwc_vec_kernel(const T *__restrict_
 // (16 KB, so that a run of input channels x taps of one output channel fits).
 constexpr int kPackSmemBytes = 16384;
 
-// How pack_weight_part divides the kernel re-layout among blocks, for a
-// shared buffer of cap elements: items of cc input channels of one output
-// channel (cc * KHKW contiguous source elements), or, when one such run covers
-// every input channel, items of fpi whole output channels (fpi * CI * KHKW
-// contiguous source elements), so that small kernels take few blocks.  cc < 1:
-// a kernel too large for the buffer, re-laid out element by element.
-struct WeightSplit {
-    int cc, runs, fpi;
-    long long items;
-};
-
-__host__ __device__ inline WeightSplit weight_split(int CO, int CI, int KHKW, int cip, int cap)
-{
-    WeightSplit ws{};
-    int cc = cap / KHKW;
-    if (cc >= 32) cc &= ~31;
-    ws.cc = cc;
-    if (cc < 1) {
-        ws.runs = 0, ws.fpi = 0;
-        ws.items = ((long long)CO * KHKW * cip + 255) / 256;
-        return ws;
-    }
-    ws.runs = (cip + cc - 1) / cc;
-    ws.fpi = ws.runs == 1 ? max(1, cap / (CI * KHKW)) : 1;
-    ws.items = ws.runs == 1 ? ((long long)CO + ws.fpi - 1) / ws.fpi : (long long)CO * ws.runs;
-    return ws;
-}
-
 // The kernel re-layout [CO][CI][KHKW] -> [CO][KHKW][cip] by blocks
-// first, first + nblocks, ...: each work item (weight_split) is read coalesced
-// into the shared buffer `buf` (cap elements) and written back as KHKW runs of
-// channels per output channel, zero past CI.
+// first, first + nblocks, ...: each work item is one output channel f and a
+// run of cc input channels, whose cc * KHKW source elements are contiguous.
+// They are read coalesced into the shared buffer `buf` (cap elements) and
+// written back as KHKW runs of cc channels, zero past CI.
 template <typename T>
 __device__ __forceinline__ void pack_weight_part(const T *__restrict__ w, T *__restrict__ wp,
                                                  int CO, int CI, int KHKW, int cip, int first,
                                                  int nblocks, T *buf, int cap)
 {
-    const WeightSplit sp = weight_split(CO, CI, KHKW, cip, cap);
-    if (sp.cc < 1) {   // a kernel too large for the buffer: element by element
+    int cc = cap / KHKW;
+    if (cc >= 32) cc &= ~31;
+    if (cc < 1) {   // a kernel too large for the buffer: element by element
         const long long total = (long long)CO * KHKW * cip;
         const long long nthreads = (long long)nblocks * blockDim.x;
         for (long long i = (long long)first * blockDim.x + threadIdx.x; i < total; i += nthreads) {
@@ -154,17 +128,15 @@ __device__ __forceinline__ void pack_weight_part(const T *__restrict__ w, T *__r
         }
         return;
     }
-    const int cc = sp.cc, runs = sp.runs;
-    constexpr int VEC = 16 / sizeof(T);
-    for (long long it = first; it < sp.items; it += nblocks) {
-        // output channels [f0, f0 + nf), input channels [c0, c0 + nc) of each
-        const int f0 = runs == 1 ? (int)it * sp.fpi : (int)(it / runs);
-        const int nf = runs == 1 ? min(sp.fpi, CO - f0) : 1;
-        const int c0 = runs == 1 ? 0 : (int)(it - (long long)f0 * runs) * cc;
+    const int runs = (cip + cc - 1) / cc;
+    const long long items = (long long)CO * runs;
+    for (long long it = first; it < items; it += nblocks) {
+        const int f = (int)(it / runs);
+        const int c0 = (int)(it - (long long)f * runs) * cc;
         const int nc = min(cc, CI - c0);   // source channels in this run (may be <= 0)
-        const T *src = w + ((size_t)f0 * CI + c0) * KHKW;
-        const int per_f = nc > 0 ? nc * KHKW : 0;   // source elements per output channel
-        const int nsrc = per_f * nf;                // contiguous: nf > 1 only with whole channels
+        const T *src = w + ((size_t)f * CI + c0) * KHKW;
+        const int nsrc = nc > 0 ? nc * KHKW : 0;
+        constexpr int VEC = 16 / sizeof(T);
         if ((reinterpret_cast<uintptr_t>(src) & 15) == 0 && nsrc % VEC == 0) {
             const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
             for (int i = threadIdx.x; i < nsrc / VEC; i += blockDim.x)
@@ -174,36 +146,31 @@ __device__ __forceinline__ void pack_weight_part(const T *__restrict__ w, T *__r
         }
         __syncthreads();
         const int wc = min(cc, cip - c0);  // destination channels in this run
+        T *dst = wp + (size_t)f * KHKW * cip + c0;
         if (wc % VEC == 0 && (cip * sizeof(T)) % 16 == 0 && ((c0 * sizeof(T)) & 15) == 0) {
             // runs of VEC channels of one tap per 16-byte store
             const int wv = wc / VEC;
-            const int per = KHKW * wv;     // stores per output channel
-            for (int i = threadIdx.x; i < nf * per; i += blockDim.x) {
-                const int ff = i / per, r = i - ff * per;
-                const int t = r / wv, c = (r - t * wv) * VEC;
-                const T *fb = buf + (size_t)ff * per_f;
+            for (int i = threadIdx.x; i < KHKW * wv; i += blockDim.x) {
+                const int t = i / wv, c = (i - t * wv) * VEC;
                 union {
                     uint4 u;
                     T e[VEC];
                 } o;
                 if (c + VEC <= nc) {
                     // all VEC source channels present: a strided gather, no tests
-                    const T *col = fb + c * KHKW + t;
+                    const T *col = buf + c * KHKW + t;
 #pragma unroll
                     for (int j = 0; j < VEC; ++j) o.e[j] = col[j * KHKW];
                 } else {
 #pragma unroll
-                    for (int j = 0; j < VEC; ++j) o.e[j] = c + j < nc ? fb[(c + j) * KHKW + t] : T(0);
+                    for (int j = 0; j < VEC; ++j) o.e[j] = c + j < nc ? buf[(c + j) * KHKW + t] : T(0);
                 }
-                *reinterpret_cast<uint4 *>(wp + ((size_t)(f0 + ff) * KHKW + t) * cip + c0 + c) = o.u;
+                *reinterpret_cast<uint4 *>(dst + (size_t)t * cip + c) = o.u;
             }
         } else {
-            const int per = KHKW * wc;
-            for (int i = threadIdx.x; i < nf * per; i += blockDim.x) {
-                const int ff = i / per, r = i - ff * per;
-                const int t = r / wc, c = r - t * wc;
-                wp[((size_t)(f0 + ff) * KHKW + t) * cip + c0 + c] =
-                    c < nc ? buf[(size_t)ff * per_f + c * KHKW + t] : T(0);
+            for (int i = threadIdx.x; i < KHKW * wc; i += blockDim.x) {
+                const int t = i / wc, c = i - t * wc;
+                dst[(size_t)t * cip + c] = c < nc ? buf[c * KHKW + t] : T(0);
             }
         }
         __syncthreads();
@@ -712,8 +679,12 @@ cudaError_t launch_pack_operands(const void *x, void *xh, int N, int C, int H, i
     const long long data_blocks = ptiles * (kind == 0 ? cgroups : ctiles) * N;
     // weight blocks: one per (output channel, channel run) item of pack_weight_part;
     // none when w is null (the conv reads the caller's kernel as it is)
-    const int cap = ((kind == 0 || kind == 3) ? kPlaneBufBytes : kPackSmemBytes) / (int)dtype_size(dt);
-    const long long witems = weight_split(CO, CI, KHKW, cip, cap).items;
+    const long long cap = ((kind == 0 || kind == 3) ? kPlaneBufBytes : kPackSmemBytes) /
+                          (long long)dtype_size(dt);
+    long long cc = cap / KHKW;
+    if (cc >= 32) cc &= ~31ll;
+    const long long witems = cc >= 1 ? (long long)CO * ((cip + cc - 1) / cc)
+                                     : ((long long)CO * KHKW * cip + 255) / 256;
     const long long wblocks = w ? std::max<long long>(1, std::min<long long>(witems, 2048)) : 0;
     if (zero && (reinterpret_cast<uintptr_t>(zero) & 15)) return cudaErrorInvalidValue;
     const long long zblocks =

@@ -374,10 +374,9 @@ def test_stacking_rejects_padding_wider_than_the_kernel():
 
 # ------------------------------------------------- pack launches with grouped work
 # The whole-plane pack moves several 128-byte channel tiles of an image per
-# block when the grid still gives every SM two blocks, and the kernel re-layout
-# takes several whole output channels per block when their source elements fit
-# its buffer.  These shapes reach both, with ragged last groups (a partial
-# channel tile, an output-channel group of fewer channels).
+# block when the grid still gives every SM two blocks.  These shapes reach it
+# with ragged last groups (a partial channel tile, a group of fewer tiles),
+# beside the large-plane form for comparison.
 PACK_GROUPS = [
     (_H("pack_groups_7x7_ci200_co76", 160, 200, 76, 7, 7, 3, 1), bg.MODE_STACK),
     (_H("pack_groups_4x4_ci1024_co32", 80, 1024, 32, 4, 4, 3, 1), bg.MODE_STACK),
