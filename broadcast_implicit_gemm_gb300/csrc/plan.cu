@@ -182,11 +182,13 @@ std::vector<Box> box_options(const ConvShape &s)
             const double eff = (double)s.Ho * s.Wo / cover;
             v.push_back({w, h, bpt, eff});
         }
-    // also boxes that match the image width exactly (w*h multiple of 8, < 128 rows)
+    // also boxes that match the image width exactly (w*h multiple of 8, < 128 rows),
+    // unless the power-of-two sizes above already hold the same box
     for (int h = 1; h <= 128; ++h) {
         const int w = s.Wo;
         if (w > 128 || w * h > 128 || (w * h) % 8) continue;
         if (w * s.stride > 256 || h * s.stride > 256) continue;
+        if (std::any_of(v.begin(), v.end(), [&](const Box &b) { return b.w == w && b.h == h; })) continue;
         const int bpt = 128 / (w * h);
         const double cover = (double)ceil_div(s.Ho, h) * h * w;
         const double eff = (double)s.Ho * s.Wo / cover * (double)(bpt * w * h) / 128.0;
@@ -1320,6 +1322,7 @@ bigemm_status search(const ConvShape &s, int sms, cudaStream_t st, Cand *best, s
     double best_ms = 1e30;
     int best_i = -1;
     std::ostringstream os;
+    os.precision(9);   // enough digits that the log orders the records as the choice did
     os << "[";
     for (size_t i = 0; i < cands.size(); ++i) {
         double ms = 0;

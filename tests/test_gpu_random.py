@@ -137,3 +137,40 @@ def test_random_depthwise(case):
         opts = {"kind": bg.KIND_SIMT}
     info = check(spec, opts)
     assert info["kind"] == "simt"
+
+
+# ------------------------------------------------------------- searched plans
+# Seeded random shapes planned by the timed search over every candidate the
+# library generates (all operand modes, tiles, splits, resident weights,
+# epilogue-warp counts, pairs), as the benchmark plans its layers: whichever
+# candidate wins must compute the conv, and it must be the fastest valid one
+# of the search's own records.
+def _search_cases(n=12, seed=4242):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        K = int(rng.choice([1, 3, 3, 5]))
+        stride = int(rng.choice([1, 1, 2]))
+        pad = int(rng.integers(0, K // 2 + 1))
+        H, W = int(rng.integers(K + 2, 40)), int(rng.integers(K + 2, 40))
+        CI = int(rng.choice([16, 32, 64, 96, 128]))
+        CO = int(rng.choice([32, 64, 96, 128, 256]))
+        N = int(rng.integers(1, 5))
+        i_dt = str(rng.choice(["f16", "bf16", "f32"]))
+        o_dt = "f32" if i_dt == "f32" or rng.random() < 0.3 else i_dt
+        epi = str(rng.choice(["none", "bias", "bias_relu"]))
+        spec = S(f"srch{i}_k{K}s{stride}p{pad}_{H}x{W}_ci{CI}_co{CO}_n{N}_{i_dt}{o_dt}_{epi}",
+                 N, CI, CO, H, W, K, stride, pad, i=i_dt, o=o_dt, epi=epi)
+        out.append((spec, seed * 1000 + i))
+    return out
+
+
+@pytest.mark.parametrize("case", _search_cases(), ids=lambda c: c[0].name)
+def test_random_shape_searched_plan(case):
+    spec, seed = case
+    info = check(spec, search=1, seed=seed)
+    assert info["chosen_by"] in ("search", "cache")
+    if info["chosen_by"] == "search":
+        ok = [r for r in info["search"] if r["status"] == 0]
+        chosen = [r["ms"] for r in ok if r["cand"] == info["cand"]]
+        assert chosen and min(chosen) == min(r["ms"] for r in ok)   # the fastest record
