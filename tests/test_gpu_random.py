@@ -174,3 +174,34 @@ def test_random_shape_searched_plan(case):
         ok = [r for r in info["search"] if r["status"] == 0]
         chosen = [r["ms"] for r in ok if r["cand"] == info["cand"]]
         assert chosen and min(chosen) == min(r["ms"] for r in ok)   # the fastest record
+
+
+def _dw_search_cases(n=8, seed=99):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        K = int(rng.choice([3, 5, 7]))
+        stride = int(rng.choice([1, 2]))
+        H = int(rng.integers(5, 60))
+        W = int(rng.choice([int(rng.integers(5, 60)), 8 * int(rng.integers(1, 9))]))
+        C = int(rng.choice([8, 24, 32, 96]))
+        N = int(rng.integers(1, 5))
+        i_dt = str(rng.choice(["f16", "bf16", "f32"]))
+        o_dt = i_dt if rng.random() < 0.6 else "f32"
+        epi = str(rng.choice(["none", "bias", "bias_relu"]))
+        spec = S(f"sdw{i}_k{K}s{stride}_{H}x{W}_c{C}_n{N}_{i_dt}{o_dt}_{epi}", N, C, C, H, W, K,
+                 stride, K // 2, g=C, i=i_dt, o=o_dt, epi=epi, kd="dw")
+        out.append((spec, seed * 1000 + i))
+    return out
+
+
+@pytest.mark.parametrize("case", _dw_search_cases(), ids=lambda c: c[0].name)
+def test_random_depthwise_searched_plan(case):
+    # the timed search over the depthwise kernels that take the shape
+    spec, seed = case
+    info = check(spec, search=1, seed=seed)
+    assert info["kind"] == "simt" and info["chosen_by"] in ("search", "cache")
+    if info["chosen_by"] == "search":
+        ok = [r for r in info["search"] if r["status"] == 0]
+        chosen = [r["ms"] for r in ok if r["cand"] == info["cand"]]
+        assert chosen and min(chosen) == min(r["ms"] for r in ok)
