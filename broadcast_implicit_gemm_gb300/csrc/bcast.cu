@@ -13,7 +13,7 @@
 // The general form of the same page (Introduction): any [1, P, 1] => [B0, P, B1]
 // after axis fusion, the last axis broadcast.  The page says the tactic binds
 // the axes three ways by dim size but gives no detail; the bindings here are
-// this build's: long rows (B1 of 64 vectors or more) take the per-channel
+// two, chosen by row length: long rows (B1 of 64 vectors or more) take the per-channel
 // kernel above with N = B0, C = P, H*W = B1; short rows take bcast_rows, where
 // each thread owns a fixed 16-byte piece of a b0 slice's P*B1 run, computes
 // op(var[p]) for its elements once and stores the piece into every b0 slice of
